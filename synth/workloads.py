@@ -1,0 +1,90 @@
+"""The five synthetic workloads: shapes, value distributions and seeds.
+
+Each recipe states what one configuration feeds the path; the arrays come from
+the counter-based generators in this package, seeded with 20261202 + index.
+``rows``/``cols`` overrides keep the distribution but change the shape, which is
+how the parity tests build small cases that still span several tiles and a
+ragged tail.  No method arithmetic lives here.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+from . import indices, normal_bf16, normal_f32, targets, uniform_f32
+
+SEED_BASE = 20261202
+IGNORE_INDEX = -100
+
+
+@dataclass
+class Workload:
+    name: str
+    op: str
+    rows: int
+    cols: int
+    arrays: dict = field(default_factory=dict)
+    params: dict = field(default_factory=dict)
+
+
+# (op, rows, cols) of each configuration at full size.
+FULL_SHAPES = {
+    0: ("relu_add_sum", 64, 128),
+    1: ("softmax", 32768, 1024),
+    2: ("layernorm", 4096, 32768),
+    3: ("relu_add_sum", 8, 33554432),
+    4: ("xent", 8192, 50257),
+}
+
+NAMES = {
+    0: "relu_add_sum persistent fp32 [64,128] (Example 1.1)",
+    1: "softmax persistent fp32 [32768,1024]",
+    2: "layernorm looped Welford bf16 [4096,32768]",
+    3: "relu_add_sum split fp32 [8,33554432]",
+    4: "log-softmax+cross-entropy bf16 [8192,50257], int64 targets, 5% ignore_index=-100",
+}
+
+
+def seed_of(cfg: int) -> int:
+    return SEED_BASE + cfg
+
+
+def make(cfg: int, rows: int | None = None, cols: int | None = None, nan_variant: bool = False,
+         seed: int | None = None) -> Workload:
+    """Host arrays for configuration ``cfg`` (optionally at another shape)."""
+    op, R, C = FULL_SHAPES[cfg]
+    R = R if rows is None else rows
+    C = C if cols is None else cols
+    s = seed_of(cfg) if seed is None else seed
+    w = Workload(name=NAMES[cfg], op=op, rows=R, cols=C)
+    if op == "relu_add_sum":
+        w.arrays["a"] = uniform_f32((R, C), s, 0, -1.0, 1.0)
+        w.arrays["b"] = uniform_f32((R, C), s, 1, -1.0, 1.0)
+        w.params["scale"] = 2.0
+        if nan_variant:
+            # 4 NaNs at seeded (array, row, col) positions; positions may share rows.
+            flat = indices(4, 2 * R * C, s, 2)
+            pos = []
+            for f in flat.tolist():
+                arr, rem = divmod(f, R * C)
+                r, c = divmod(rem, C)
+                name = "a" if arr == 0 else "b"
+                w.arrays[name][r, c] = np.float32("nan")
+                pos.append((name, r, c))
+            w.params["nan_positions"] = pos
+    elif op == "softmax":
+        w.arrays["x"] = normal_f32((R, C), s, 0, 0.0, 4.0)
+    elif op == "layernorm":
+        w.arrays["x"] = normal_bf16((R, C), s, 0, 0.5, 2.0)
+        w.arrays["gamma"] = normal_f32((C,), s, 1, 1.0, 0.1)
+        w.arrays["beta"] = normal_f32((C,), s, 2, 0.0, 0.1)
+        w.params["eps"] = 1e-5
+    elif op == "xent":
+        w.arrays["logits"] = normal_bf16((R, C), s, 0, 0.0, 3.0)
+        n_ignore = int(round(0.05 * R))
+        w.arrays["target"] = targets(R, C, n_ignore, IGNORE_INDEX, s, 1)
+        w.params["ignore_index"] = IGNORE_INDEX
+    else:
+        raise ValueError(op)
+    return w
