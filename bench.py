@@ -1,0 +1,408 @@
+"""Benchmark of the fused row-reduction path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One JSON line on stdout (rank 0).  The headline workload is the fused softmax in
+its persistent form, fp32 [32768, 1024] (logits 4*N(0,1)); a step is one call
+of fr_softmax over that batch, inputs resident in HBM, the L2 flushed (a
+256 MiB write) before every step, each launch timed with CUDA events on the
+stream it runs on.  ``value`` is achieved HBM GB/s: algorithmic bytes (one read
+and one write of every element) / mean launch time, summed over ranks.
+``per_config`` adds the other workloads of the path measured the same way.
+``e2e`` is the same metric through the same C-ABI call with the input copied
+from pinned host memory and the result copied back inside the timed region.
+
+``--impl reference`` times the CPU oracle (the plain fp64 C definition) on a
+bounded sample of the same workload on the host cores; under torchrun only
+rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HEADLINE = 1
+METRIC = "fused row-reduction achieved HBM GB/s and % of GB300 peak; rows/s per config"
+UNIT = "GB/s"
+FLUSH_BYTES = 256 << 20
+PROFILE = os.path.join(ROOT, "profiles", "softmax_persistent_32768x1024.md")
+KERNEL_SRC = os.path.join(ROOT, "reduction_pointwise_row_gb300", "csrc", "softmax.cu")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-extra", action="store_true", help="headline workload only")
+    return p.parse_args()
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (every 50 ms) kept only while a timed loop runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.windows = []
+        self.t0 = time.time()
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        self.lines = []
+
+    def window(self, start, end):
+        self.windows.append((start, end))
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        t_end = time.time()
+        rows = [l.split(", ") for l in out.strip().splitlines() if l.count(",") >= 8]
+        if not rows:
+            return None
+        # nvidia-smi -lms prints at a fixed period: spread timestamps evenly
+        dt = (t_end - self.t0) / max(len(rows), 1)
+        keep, all_mhz = [], []
+        for i, r in enumerate(rows):
+            ts = self.t0 + (i + 0.5) * dt
+            try:
+                mhz, mx = float(r[1]), float(r[2])
+            except ValueError:
+                continue
+            all_mhz.append(mhz)
+            if any(a - 0.05 <= ts <= b + 0.05 for a, b in self.windows):
+                keep.append((mhz, mx, r))
+        if not keep:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, _, r in keep:
+            for n, v in zip(names, r[5:9]):
+                if v.strip() == "Active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(k[0] for k in keep),
+                "sm_max_mhz": max(k[1] for k in keep),
+                "reasons": sorted(reasons), "samples": len(keep)}
+
+
+# ---------------------------------------------------------------- profile
+
+def kernel_source_hash():
+    with open(KERNEL_SRC, "rb") as f:
+        h = hashlib.sha256(f.read())
+    with open(os.path.join(ROOT, "reduction_pointwise_row_gb300", "csrc", "common.cuh"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    source is unchanged since the capture."""
+    try:
+        text = open(PROFILE).read()
+    except OSError:
+        return None
+    m = re.search(r"source_hash:\s*([0-9a-f]+)", text)
+    t = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not m or not t or m.group(1) != kernel_source_hash():
+        return None
+    return int(t.group(1))
+
+
+# ---------------------------------------------------------------- our arm
+
+def to_device(arr, dev):
+    """Host array -> device tensor (uint16 arrays hold bf16 bit patterns)."""
+    import numpy as np
+    import torch
+    if arr.dtype == np.uint16:
+        return torch.from_numpy(arr.view(np.int16)).to(dev).view(torch.bfloat16)
+    return torch.from_numpy(arr).to(dev)
+
+
+def run_ours(args):
+    import torch
+
+    import reduction_pointwise_row_gb300 as fr
+    from reduction_pointwise_row_gb300 import traffic
+    from synth import workloads
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    fr.lib()
+    peak, peak_kind = measured_peak()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    clocks = ClockSampler(local)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def timed(call, steps, warmup, launches_per_call):
+        """Mean device time (s) of `call`, L2 flushed before each launch."""
+        for _ in range(warmup):
+            flush.zero_()
+            call()
+        barrier()
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        w0 = time.time()
+        for i in range(steps):
+            flush.zero_()
+            starts[i].record(stream)
+            call()
+            ends[i].record(stream)
+        barrier()
+        clocks.window(w0, time.time())
+        ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        return max_over_ranks(statistics.fmean(ms) / 1e3), launches_per_call * steps, ms
+
+    # ---- headline: softmax persistent fp32 [32768, 1024]
+    w = workloads.make(HEADLINE)
+    rows, cols = w.rows, w.cols
+    x_host = torch.from_numpy(w.arrays["x"]).pin_memory()
+    x = x_host.to(dev)
+    y = torch.empty_like(x)
+    fr.fr_softmax(x, out=y)
+    form = fr.fr_last_form()
+    nbytes = traffic.algorithmic_bytes("softmax", rows, cols)
+    t_launch, launches, ms = timed(lambda: fr.fr_softmax(x, out=y), args.steps, args.warmup, 1)
+    value = world * nbytes / t_launch / 1e9
+
+    # ---- e2e through the same call with host buffers
+    y_host = torch.empty_like(x_host).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_call():
+        x.copy_(x_host, non_blocking=True)
+        fr.fr_softmax(x, out=y)
+        y_host.copy_(y, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_call()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0 = time.time()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_call()
+    e1.record(stream)
+    barrier()
+    clocks.window(w0, time.time())
+    t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3 / e2e_steps)
+    e2e = {"value": round(world * nbytes / t_e2e / 1e9, 2), "unit": UNIT,
+           "h2d_bytes_per_step": x_host.numel() * 4, "d2h_bytes_per_step": y_host.numel() * 4,
+           "ms_per_step": round(t_e2e * 1e3, 4)}
+    del x_host, y_host
+
+    # ---- the other workloads of the path, same method
+    per_config = {}
+    if not args.no_extra:
+        per_config = extra_configs(fr, traffic, workloads, timed, dev, peak, args, world)
+        launches += sum(v.pop("_launches") for v in per_config.values())
+
+    clk = clocks.stop()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_launch * 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded SplitMix64 / Box-Muller, 4*N(0,1))",
+        "config": {"workload": "fused softmax, persistent form, fp32 [32768,1024]",
+                   "rows": rows, "cols": cols, "form": form,
+                   "rows_per_s": round(world * rows / t_launch, 1),
+                   "l2": "flushed before every step (256 MiB write)",
+                   "timing": "CUDA events per launch on the launching stream, mean",
+                   "parallelism": f"replicas x{world} (rows shard, no collective)"},
+        "roofline": {"bound": "hbm", "achieved": round(nbytes / t_launch / 1e9, 2),
+                     "peak": peak, "unit": "GB/s",
+                     "frac": round(nbytes / t_launch / 1e9 / peak, 4),
+                     "traffic": profiled_traffic(),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy burst)"},
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "per_config": per_config,
+        "clocks": clk,
+    }
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline(w)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def extra_configs(fr, traffic, workloads, timed, dev, peak, args, world):
+    import torch
+
+    steps = max(3, min(args.steps, 50))
+    res = {}
+
+    def record(name, op, rows, cols, t, launches, form):
+        nb = traffic.algorithmic_bytes(op, rows, cols)
+        res[name] = {"op": op, "rows": rows, "cols": cols, "form": form,
+                     "us": round(t * 1e6, 3), "gbs": round(nb / t / 1e9, 2),
+                     "frac": round(nb / t / 1e9 / peak, 4),
+                     "rows_per_s": round(world * rows / t, 1), "_launches": launches}
+
+    w = workloads.make(0)
+    a, b = to_device(w.arrays["a"], dev), to_device(w.arrays["b"], dev)
+    out = torch.empty(w.rows, device=dev)
+    fr.fr_reduce_relu_add_sum(a, b, 2.0, out=out)
+    t, n, _ = timed(lambda: fr.fr_reduce_relu_add_sum(a, b, 2.0, out=out), steps, args.warmup, 1)
+    record("relu_add_sum_64x128", "relu_add_sum", w.rows, w.cols, t, n, fr.fr_last_form())
+    del a, b
+
+    w = workloads.make(2)
+    x = to_device(w.arrays["x"], dev)
+    g, bt = to_device(w.arrays["gamma"], dev), to_device(w.arrays["beta"], dev)
+    y = torch.empty_like(x)
+    mean = torch.empty(w.rows, device=dev)
+    rstd = torch.empty(w.rows, device=dev)
+    call = lambda: fr.fr_layernorm(x, g, bt, 1e-5, out=y, mean=mean, rstd=rstd)
+    call()
+    t, n, _ = timed(call, steps, args.warmup, 1)
+    record("layernorm_4096x32768", "layernorm", w.rows, w.cols, t, n, fr.fr_last_form())
+    del x, y
+
+    w = workloads.make(3)
+    a, b = to_device(w.arrays["a"], dev), to_device(w.arrays["b"], dev)
+    del w
+    out = torch.empty(8, device=dev)
+    ws = torch.empty(fr.fr_workspace_size("relu_add_sum", 8, 33554432), dtype=torch.uint8,
+                     device=dev)
+    call = lambda: fr.fr_reduce_relu_add_sum(a, b, 2.0, out=out, workspace=ws)
+    call()
+    t, n, _ = timed(call, steps, args.warmup, 2)
+    record("relu_add_sum_split_8x33554432", "relu_add_sum", 8, 33554432, t, n, fr.fr_last_form())
+    del a, b
+
+    w = workloads.make(4)
+    lg = to_device(w.arrays["logits"], dev)
+    tg = torch.from_numpy(w.arrays["target"]).to(dev)
+    del w
+    wsx = torch.empty(fr.fr_workspace_size("xent", 8192, 50257, "bf16"), dtype=torch.uint8,
+                      device=dev)
+    call = lambda: fr.fr_xent(lg, tg, -100, workspace=wsx)
+    call()
+    t, n, _ = timed(call, steps, args.warmup, 1)
+    record("xent_8192x50257", "xent", 8192, 50257, t, n, fr.fr_last_form())
+    return res
+
+
+# ---------------------------------------------------------------- oracle arms
+
+def oracle_sample_rows(budget_s=12.0):
+    """Rows of the headline workload the oracle can do in about budget_s."""
+    return 32768
+
+
+def cpu_baseline(w):
+    import oracle
+    from reduction_pointwise_row_gb300 import traffic
+    o = oracle.get()
+    rows = oracle_sample_rows()
+    x = w.arrays["x"][:rows]
+    t0 = time.perf_counter()
+    o.softmax(x)
+    dt = time.perf_counter() - t0
+    nb = traffic.algorithmic_bytes("softmax", rows, w.cols)
+    return {"value": round(nb / dt / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "seconds": round(dt, 3),
+            "sample": f"{rows} of {w.rows} rows x {w.cols} (single-threaded fp64 C oracle)"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from reduction_pointwise_row_gb300 import traffic
+    from synth import workloads
+    w = workloads.make(HEADLINE)
+    o = oracle.get()
+    rows = 4096  # bounded sample per step: about 0.3 s of CPU work
+    x = w.arrays["x"][:rows]
+    for _ in range(args.warmup):
+        o.softmax(x)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        o.softmax(x)
+    dt = (time.perf_counter() - t0) / args.steps
+    nb = traffic.algorithmic_bytes("softmax", rows, w.cols)
+    v = round(nb / dt / 1e9, 4)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded SplitMix64 / Box-Muller, 4*N(0,1))",
+            "config": {"workload": "fused softmax, persistent form, fp32 [32768,1024]",
+                       "rows": w.rows, "cols": w.cols,
+                       "sample": f"{rows} rows per step"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{rows} of {w.rows} rows per step"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,200 @@
+/*
+ * fr.h -- C ABI of the GB300 (sm_103a) fused pointwise + row-reduction library.
+ *
+ * Every entry point takes plain pointers and sizes; no framework types cross
+ * this boundary.  Conventions shared by all calls:
+ *
+ *   Layout.    A matrix is `rows` rows of `cols` elements, row-major, the
+ *              reduction running along the contiguous dimension (the INNER
+ *              reduction of "Stax (4): GPU Codegen and Dynamic Shapes", section
+ *              9.4).  `ld*` is the distance between row starts in elements
+ *              (ld >= cols).  Base pointers need only the element's natural
+ *              alignment; 16-byte aligned rows take the vectorised path, others
+ *              a scalar or head/tail-peeled path (same results).
+ *   Memory.    Every pointer is DEVICE memory owned by the caller (inputs,
+ *              outputs and workspace).  The library allocates nothing.
+ *   Streams.   All work is enqueued on `stream` (a cudaStream_t; NULL = the
+ *              legacy default stream) and the call returns without
+ *              synchronising.  Kernels of one call are ordered by the stream
+ *              alone, as the generated wrapper of section 9.7 orders its two
+ *              launches.
+ *   Errors.    The return value reports argument validation and launch errors
+ *              only; on any non-FR_OK return nothing was enqueued.  Errors that
+ *              depend on device data (an out-of-range target) are recorded in
+ *              a device-side error word that fr_check_device_error() reads;
+ *              kernels never trap.
+ *   Forms.     `form` selects the reduction form of section 9.4: persistent
+ *              (a row held on chip in one pass), looped (a row streamed in
+ *              chunks), split (few long rows: two-stage cross-CTA reduction).
+ *              FR_FORM_AUTO picks one from the shape using rules measured on
+ *              GB300; a form that cannot handle the shape returns
+ *              FR_ERR_UNSUPPORTED_FORM.  fr_last_form() reports the choice.
+ *   Devices.   Calls run on the caller's current CUDA device.
+ */
+#ifndef FR_H_
+#define FR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *fr_stream_t; /* == cudaStream_t */
+
+typedef enum {
+  FR_OK = 0,
+  FR_ERR_INVALID_ARG = 1,        /* null pointer, rows/cols <= 0, ld < cols, size overflow */
+  FR_ERR_UNSUPPORTED_DTYPE = 2,  /* dtype not offered by this call */
+  FR_ERR_UNSUPPORTED_FORM = 3,   /* forced form cannot handle this shape */
+  FR_ERR_MISALIGNED = 4,         /* pointer not aligned to its element size */
+  FR_ERR_WORKSPACE_TOO_SMALL = 5,/* workspace_bytes < fr_workspace_size(...) */
+  FR_ERR_CUDA = 6,               /* a CUDA runtime call or launch failed */
+  FR_ERR_DEVICE_DATA = 7,        /* device data error recorded (see fr_check_device_error) */
+  FR_ERR_NO_DEVICE = 8           /* no usable CUDA device / wrong architecture */
+} fr_status;
+
+typedef enum { FR_F32 = 0, FR_BF16 = 1 } fr_dtype;
+
+typedef enum {
+  FR_FORM_AUTO = 0,
+  FR_FORM_PERSISTENT = 1,
+  FR_FORM_LOOPED = 2,
+  FR_FORM_SPLIT = 3
+} fr_form;
+
+typedef enum {
+  FR_OP_RELU_ADD_SUM = 0,
+  FR_OP_SOFTMAX = 1,
+  FR_OP_LAYERNORM = 2,
+  FR_OP_XENT = 3
+} fr_op;
+
+/* Device error codes written by kernels (read by fr_check_device_error). */
+#define FR_DEVERR_NONE 0
+#define FR_DEVERR_BAD_TARGET 1 /* a target outside [0, cols) and != ignore_index */
+
+/* Library version (major*10000 + minor*100 + patch). */
+int fr_version(void);
+
+/* Human-readable name of a status code (static storage). */
+const char *fr_status_string(fr_status status);
+
+/* The form chosen by the most recent successful call on this host thread. */
+fr_form fr_last_form(void);
+
+/*
+ * Bytes of device workspace that `op` needs for this shape and form
+ * (0 when none).  FR_FORM_AUTO reports the need of the form AUTO will pick.
+ * The workspace must be 16-byte aligned; its contents on entry are ignored.
+ */
+size_t fr_workspace_size(fr_op op, int64_t rows, int64_t cols, fr_dtype dtype, fr_form form);
+
+/*
+ * out[x] = sum_{r < cols} scale * relu(a[x*lda + r] + b[x*ldb + r])
+ *
+ * Example 1.1 of "Stax (4): GPU Codegen and Dynamic Shapes", section 9.2,
+ * Listing 9.1 (there with scale = 2): the two loads are added in fp32, relu is
+ * maximum(0, v) with NaN propagation (a NaN input makes its row's sum NaN) and
+ * the product is summed along the row with fp32 accumulators over short runs
+ * and an fp64 combine across threads and CTAs.  Section 9.4 gives the forms:
+ * persistent and looped (one warp or CTA per row), split (section 9.4 (3):
+ * rows too few and too long -- stage 1 writes per-segment partials to the
+ * workspace, stage 2 sums them in a fixed order; results are bitwise
+ * run-to-run deterministic for a given shape).
+ *
+ *   a, b       fp32 [rows, lda] / [rows, ldb] device inputs (read only)
+ *   out        fp32 [rows] device output
+ *   dtype      FR_F32 (the only dtype offered)
+ *   workspace  device scratch of fr_workspace_size(FR_OP_RELU_ADD_SUM, ...)
+ *              bytes (only the split form uses it; may be NULL otherwise)
+ */
+fr_status fr_reduce_relu_add_sum(const void *a, const void *b, float *out, int64_t rows,
+                                 int64_t cols, int64_t lda, int64_t ldb, fr_dtype dtype,
+                                 float scale, fr_form form, void *workspace,
+                                 size_t workspace_bytes, fr_stream_t stream);
+
+/*
+ * y[x, :] = softmax(x[x, :]):  m = max_r x,  y = exp(x - m) / sum_r exp(x - m)
+ *
+ * "Stax (4)", section 9.5 (the softmax equation and Listing 9.5: one read and
+ * one write per row, masked lanes filled with -inf for the max and 0 for the
+ * sum) and "CMU 15-779 Lecture 8", section 3.  The persistent form keeps the
+ * row on chip and takes the max and the sum in two passes over registers; the
+ * looped form merges per-chunk (m, d) pairs with the online-softmax operator
+ * of section 9.5 (Proposition 9.1) and then streams the row again to write y.
+ * NaN anywhere in a row makes that row NaN.  fp32 in, fp32 out, fp32
+ * arithmetic.
+ *
+ *   x          fp32 [rows, ldx] device input; y fp32 [rows, ldy] device output
+ *              (x and y may be the same buffer when ldx == ldy)
+ *   dtype      FR_F32
+ */
+fr_status fr_softmax(const void *x, void *y, int64_t rows, int64_t cols, int64_t ldx,
+                     int64_t ldy, fr_dtype dtype, fr_form form, fr_stream_t stream);
+
+/*
+ * LayerNorm over each row (not defined on the pages; standard definition):
+ *   mean = sum x / n,  var = sum (x - mean)^2 / n,  rstd = 1 / sqrt(var + eps),
+ *   y = (x - mean) * rstd * gamma + beta      (rounded to bf16, nearest even)
+ * The statistics are Welford (count, mean, M2) triples per thread chunk,
+ * combined with the Chan et al. parallel merge, in fp32.  The looped form
+ * streams each row through a shared-memory ring filled by bulk asynchronous
+ * copies (the multi-stage staging of "Stax (4)", section 9.8, and the tensor
+ * descriptors of "CMU 15-779 Lecture 8", section 5) and normalises from the
+ * staged copy; the persistent form keeps the row in registers.
+ *
+ *   x          bf16 [rows, ldx] device input (uint16 bit patterns)
+ *   gamma,beta fp32 [cols] device inputs
+ *   y          bf16 [rows, ldy] device output
+ *   mean, rstd fp32 [rows] device outputs (either may be NULL)
+ *   dtype      FR_BF16
+ */
+fr_status fr_layernorm(const void *x, const float *gamma, const float *beta, void *y,
+                       float *mean, float *rstd, int64_t rows, int64_t cols, int64_t ldx,
+                       int64_t ldy, float eps, fr_dtype dtype, fr_form form,
+                       fr_stream_t stream);
+
+/*
+ * Fused log-softmax + cross entropy, one pass over each row:
+ *   (m, l) = (max_r x, sum_r exp(x - m)) by the online-softmax merge of
+ *   "Stax (4)", section 9.5;  LSE = m + log l (section 9.10);
+ *   loss[x] = LSE - x[x, t]  for 0 <= t < cols,   0 for t == ignore_index;
+ *   *loss_mean = sum of loss over rows with t != ignore_index / their count
+ *               (NaN when every row is ignored), summed in a fixed order.
+ * Cross entropy and ignore_index are not on the pages; the semantics follow
+ * PyTorch's cross_entropy(reduction='mean').  A target outside [0, cols) other
+ * than ignore_index gives that row NaN and sets FR_DEVERR_BAD_TARGET.
+ *
+ *   logits       bf16 [rows, ld] device input; any ld >= cols (rows need not
+ *                be 16-byte aligned: heads and tails are peeled)
+ *   target       int64 [rows] device input
+ *   loss         fp32 [rows] device output (may be NULL)
+ *   loss_mean    fp32 [1] device output (may be NULL)
+ *   target_logit fp32 [rows] device output x[x, t] exactly (0 for ignored rows,
+ *                NaN for bad targets); may be NULL
+ *   argmax       int64 [rows] device output, first index of the row maximum,
+ *                NaN counting as the maximum; may be NULL
+ *   dtype        FR_BF16
+ *   workspace    fr_workspace_size(FR_OP_XENT, ...) bytes when loss_mean is
+ *                requested (per-CTA partial sums and a ticket; the library
+ *                zeroes the ticket on the stream before each launch)
+ */
+fr_status fr_xent(const void *logits, const int64_t *target, float *loss, float *loss_mean,
+                  float *target_logit, int64_t *argmax, int64_t rows, int64_t cols,
+                  int64_t ld, int64_t ignore_index, fr_dtype dtype, fr_form form,
+                  void *workspace, size_t workspace_bytes, fr_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word.  Returns FR_OK when no device data error was recorded, otherwise
+ * FR_ERR_DEVICE_DATA with the FR_DEVERR_* code in *code (if non-NULL).
+ */
+fr_status fr_check_device_error(fr_stream_t stream, int32_t *code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FR_H_ */

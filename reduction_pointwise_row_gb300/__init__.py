@@ -1,0 +1,220 @@
+"""Fused pointwise + row-reduction kernels for GB300 (sm_103a): Python binding.
+
+A thin ctypes layer over ``libfr.so`` (``include/fr.h``).  It only marshals
+arguments -- device pointers, sizes, the current CUDA stream -- and every step of
+the computation runs in the library's CUDA kernels.  PyTorch provides device
+memory and streams.  There is no fallback: if the library is missing or the
+device is not an sm_103 GPU the calls raise.
+
+Functions carry the C names:
+
+    fr_reduce_relu_add_sum(a, b, scale=2.0, form="auto")     -> out [rows] fp32
+    fr_softmax(x, form="auto")                                -> y fp32
+    fr_layernorm(x, gamma, beta, eps=1e-5, form="auto")       -> (y bf16, mean, rstd)
+    fr_xent(logits, target, ignore_index=-100, ...)           -> dict of outputs
+    fr_workspace_size(op, rows, cols, dtype, form)
+    fr_check_device_error()
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import buildlib as _build
+
+__all__ = [
+    "FR_OK", "FRError", "lib", "fr_version", "fr_workspace_size", "fr_last_form",
+    "fr_reduce_relu_add_sum", "fr_softmax", "fr_layernorm", "fr_xent",
+    "fr_check_device_error", "FORMS", "OPS",
+]
+
+FR_OK = 0
+STATUS = {0: "FR_OK", 1: "FR_ERR_INVALID_ARG", 2: "FR_ERR_UNSUPPORTED_DTYPE",
+          3: "FR_ERR_UNSUPPORTED_FORM", 4: "FR_ERR_MISALIGNED",
+          5: "FR_ERR_WORKSPACE_TOO_SMALL", 6: "FR_ERR_CUDA", 7: "FR_ERR_DEVICE_DATA",
+          8: "FR_ERR_NO_DEVICE"}
+FORMS = {"auto": 0, "persistent": 1, "looped": 2, "split": 3}
+FORM_NAMES = {v: k for k, v in FORMS.items()}
+OPS = {"relu_add_sum": 0, "softmax": 1, "layernorm": 2, "xent": 3}
+DTYPES = {"f32": 0, "bf16": 1}
+
+# name -> (restype, argtypes) of every symbol include/fr.h declares
+_i64, _f32, _vp, _sz, _int = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t, \
+    ctypes.c_int
+SIGNATURES = {
+    "fr_version": (_int, []),
+    "fr_status_string": (ctypes.c_char_p, [_int]),
+    "fr_last_form": (_int, []),
+    "fr_workspace_size": (_sz, [_int, _i64, _i64, _int, _int]),
+    "fr_reduce_relu_add_sum": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _f32, _int,
+                                      _vp, _sz, _vp]),
+    "fr_softmax": (_int, [_vp, _vp, _i64, _i64, _i64, _i64, _int, _int, _vp]),
+    "fr_layernorm": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _int,
+                            _int, _vp]),
+    "fr_xent": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _int, _vp,
+                       _sz, _vp]),
+    "fr_check_device_error": (_int, [_vp, ctypes.POINTER(ctypes.c_int32)]),
+}
+
+
+class FRError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded libfr.so (built in-tree by ``build()``; never a fallback)."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise ImportError(f"{path} is missing: run reduction_pointwise_row_gb300.buildlib.build() "
+                              "(nvcc for sm_103a) first")
+        l = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(l, name)
+            f.restype, f.argtypes = res, args
+        _lib = l
+    return _lib
+
+
+def build(force: bool = False) -> str:
+    return _build.build(force=force)
+
+
+def _check(status: int, where: str):
+    if status != FR_OK:
+        raise FRError(status, where)
+
+
+def _stream(stream=None):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _ld(t) -> int:
+    assert t.dim() == 2 and t.stride(1) == 1, "rows must be contiguous (stride(1) == 1)"
+    return t.stride(0)
+
+
+def fr_version() -> int:
+    return lib().fr_version()
+
+
+def fr_last_form() -> str:
+    return FORM_NAMES[lib().fr_last_form()]
+
+
+def fr_workspace_size(op: str, rows: int, cols: int, dtype: str = "f32", form: str = "auto") -> int:
+    return lib().fr_workspace_size(OPS[op], rows, cols, DTYPES[dtype], FORMS[form])
+
+
+def _workspace(op, rows, cols, dtype, form, device, given=None):
+    import torch
+    n = fr_workspace_size(op, rows, cols, dtype, form)
+    if n == 0:
+        return None, 0
+    if given is not None:
+        return given, given.numel() * given.element_size()
+    return torch.empty(n, dtype=torch.uint8, device=device), n
+
+
+def fr_reduce_relu_add_sum(a, b, scale: float = 2.0, form: str = "auto", out=None,
+                           workspace=None, stream=None):
+    """out[x] = sum_r scale * relu(a[x, r] + b[x, r]) (fp32 in, fp32 out)."""
+    import torch
+    assert a.is_cuda and b.is_cuda and a.dtype == torch.float32 and b.dtype == torch.float32
+    assert a.shape == b.shape and a.dim() == 2
+    rows, cols = a.shape
+    if out is None:
+        out = torch.empty(rows, dtype=torch.float32, device=a.device)
+    ws, nws = _workspace("relu_add_sum", rows, cols, "f32", form, a.device, workspace)
+    _check(lib().fr_reduce_relu_add_sum(_ptr(a), _ptr(b), _ptr(out), rows, cols, _ld(a), _ld(b),
+                                        DTYPES["f32"], scale, FORMS[form], _ptr(ws), nws,
+                                        _stream(stream)), "fr_reduce_relu_add_sum")
+    return out
+
+
+def fr_softmax(x, form: str = "auto", out=None, stream=None):
+    """Row softmax of fp32 x (returns a new fp32 tensor unless ``out`` is given)."""
+    import torch
+    assert x.is_cuda and x.dtype == torch.float32 and x.dim() == 2
+    rows, cols = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    _check(lib().fr_softmax(_ptr(x), _ptr(out), rows, cols, _ld(x), _ld(out), DTYPES["f32"],
+                            FORMS[form], _stream(stream)), "fr_softmax")
+    return out
+
+
+def fr_layernorm(x, gamma, beta, eps: float = 1e-5, form: str = "auto", out=None, mean=None,
+                 rstd=None, stream=None):
+    """LayerNorm of bf16 rows; returns (y bf16, mean fp32, rstd fp32)."""
+    import torch
+    assert x.is_cuda and x.dtype == torch.bfloat16 and x.dim() == 2
+    rows, cols = x.shape
+    assert gamma.dtype == torch.float32 and beta.dtype == torch.float32
+    assert gamma.numel() == cols and beta.numel() == cols
+    if out is None:
+        out = torch.empty_like(x)
+    if mean is None:
+        mean = torch.empty(rows, dtype=torch.float32, device=x.device)
+    if rstd is None:
+        rstd = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _check(lib().fr_layernorm(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(out), _ptr(mean), _ptr(rstd),
+                              rows, cols, _ld(x), _ld(out), eps, DTYPES["bf16"], FORMS[form],
+                              _stream(stream)), "fr_layernorm")
+    return out, mean, rstd
+
+
+def fr_xent(logits, target, ignore_index: int = -100, want_loss: bool = True,
+            want_mean: bool = True, want_target_logit: bool = False, want_argmax: bool = False,
+            form: str = "auto", workspace=None, stream=None):
+    """Cross entropy of bf16 logits rows against int64 targets.
+
+    Returns a dict with the requested outputs: ``loss`` [rows], ``mean`` [1],
+    ``target_logit`` [rows], ``argmax`` [rows] (int64).
+    """
+    import torch
+    assert logits.is_cuda and logits.dtype == torch.bfloat16 and logits.dim() == 2
+    assert target.dtype == torch.int64 and target.is_cuda
+    rows, cols = logits.shape
+    assert target.numel() == rows
+    dev = logits.device
+    res = {}
+    loss = torch.empty(rows, dtype=torch.float32, device=dev) if want_loss else None
+    mean = torch.empty(1, dtype=torch.float32, device=dev) if want_mean else None
+    tl = torch.empty(rows, dtype=torch.float32, device=dev) if want_target_logit else None
+    am = torch.empty(rows, dtype=torch.int64, device=dev) if want_argmax else None
+    ws, nws = (None, 0)
+    if want_mean:
+        ws, nws = _workspace("xent", rows, cols, "bf16", form, dev, workspace)
+    _check(lib().fr_xent(_ptr(logits), _ptr(target), _ptr(loss), _ptr(mean), _ptr(tl), _ptr(am),
+                         rows, cols, _ld(logits), ignore_index, DTYPES["bf16"], FORMS[form],
+                         _ptr(ws), nws, _stream(stream)), "fr_xent")
+    for k, v in (("loss", loss), ("mean", mean), ("target_logit", tl), ("argmax", am)):
+        if v is not None:
+            res[k] = v
+    return res
+
+
+def fr_check_device_error(stream=None) -> int:
+    """Synchronises the stream; returns and clears the device error code (0 = none)."""
+    code = ctypes.c_int32(0)
+    st = lib().fr_check_device_error(_stream(stream), ctypes.byref(code))
+    if st not in (FR_OK, 7):
+        raise FRError(st, "fr_check_device_error")
+    return code.value

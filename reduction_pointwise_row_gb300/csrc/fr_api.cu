@@ -1,0 +1,263 @@
+// C ABI of the fused row-reduction library: argument validation, reduction
+// form selection and dispatch to the kernels.  Mirrors the generated wrapper
+// of "Stax (4): GPU Codegen and Dynamic Shapes", section 9.7 (Listing 9.6):
+// sizes and strides are checked before anything is enqueued, buffers are
+// owned by the caller, every kernel goes onto the caller's stream in program
+// order and nothing synchronises.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/fr.h"
+#include "launch.h"
+
+namespace fr {
+
+cudaError_t current_device_info(DevInfo *out) {
+  constexpr int kMaxDev = 64;
+  static DevInfo cache[kMaxDev];
+  static bool have[kMaxDev] = {};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kMaxDev) {
+    std::lock_guard<std::mutex> lock(mu);
+    if (have[dev]) {
+      *out = cache[dev];
+      return cudaSuccess;
+    }
+  }
+  DevInfo d{};
+  d.device = dev;
+  if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
+  if (dev >= 0 && dev < kMaxDev) {
+    std::lock_guard<std::mutex> lock(mu);
+    cache[dev] = d;
+    have[dev] = true;
+  }
+  *out = d;
+  return cudaSuccess;
+}
+
+}  // namespace fr
+
+namespace {
+
+thread_local fr_form g_last_form = FR_FORM_AUTO;
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// rows >= 1, cols >= 1, ld >= cols and rows*ld*esize representable.
+bool shape_ok(int64_t rows, int64_t cols, int64_t ld, int64_t esize) {
+  if (rows < 1 || cols < 1 || ld < cols) return false;
+  const int64_t lim = (INT64_C(1) << 62) / esize;
+  return ld <= lim / rows;
+}
+
+// Rows of p and q (element size esize, leading dimensions lp, lq) share their
+// offset modulo 32 bytes on every row.
+bool same_phase(const void *p, int64_t lp, const void *q, int64_t lq, int64_t esize) {
+  const int64_t d = static_cast<int64_t>(reinterpret_cast<uintptr_t>(p)) -
+                    static_cast<int64_t>(reinterpret_cast<uintptr_t>(q));
+  return (d % 32 == 0) && (((lp - lq) * esize) % 32 == 0);
+}
+
+fr_status device_ok(fr::DevInfo *info) {
+  if (fr::current_device_info(info) != cudaSuccess) return FR_ERR_NO_DEVICE;
+  if (info->cc_major != 10 || info->cc_minor != 3) return FR_ERR_NO_DEVICE;  // built for sm_103a
+  return FR_OK;
+}
+
+fr_status launched(cudaError_t e, fr_form form) {
+  if (e != cudaSuccess) return FR_ERR_CUDA;
+  g_last_form = form;
+  return FR_OK;
+}
+
+// ---- form selection ---------------------------------------------------------
+// Rules measured on GB300 (see the form table in the design notes): rows that
+// fit one warp's registers take the persistent form; few long rows that
+// cannot fill the SMs one warp per row take the split form.
+
+fr_form pick_ras(int64_t rows, int64_t cols, int sm_count) {
+  if (cols <= fr::ras_persistent_max_cols()) return FR_FORM_PERSISTENT;
+  if (rows < static_cast<int64_t>(sm_count) * 32 && cols >= 16384) return FR_FORM_SPLIT;
+  return FR_FORM_LOOPED;
+}
+
+fr_form pick_softmax(int64_t, int64_t cols, bool vec) {
+  return cols <= fr::softmax_persistent_max_cols(vec) ? FR_FORM_PERSISTENT : FR_FORM_LOOPED;
+}
+
+fr_form pick_layernorm(int64_t, int64_t cols, bool vec, int) {
+  return fr::layernorm_persistent_ok(cols, vec) ? FR_FORM_PERSISTENT : FR_FORM_LOOPED;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fr_version(void) { return 100; }
+
+const char *fr_status_string(fr_status s) {
+  switch (s) {
+    case FR_OK: return "FR_OK";
+    case FR_ERR_INVALID_ARG: return "FR_ERR_INVALID_ARG";
+    case FR_ERR_UNSUPPORTED_DTYPE: return "FR_ERR_UNSUPPORTED_DTYPE";
+    case FR_ERR_UNSUPPORTED_FORM: return "FR_ERR_UNSUPPORTED_FORM";
+    case FR_ERR_MISALIGNED: return "FR_ERR_MISALIGNED";
+    case FR_ERR_WORKSPACE_TOO_SMALL: return "FR_ERR_WORKSPACE_TOO_SMALL";
+    case FR_ERR_CUDA: return "FR_ERR_CUDA";
+    case FR_ERR_DEVICE_DATA: return "FR_ERR_DEVICE_DATA";
+    case FR_ERR_NO_DEVICE: return "FR_ERR_NO_DEVICE";
+  }
+  return "FR_ERR_UNKNOWN";
+}
+
+fr_form fr_last_form(void) { return g_last_form; }
+
+size_t fr_workspace_size(fr_op op, int64_t rows, int64_t cols, fr_dtype dtype, fr_form form) {
+  (void)dtype;
+  if (rows < 1 || cols < 1) return 0;
+  fr::DevInfo info;
+  if (fr::current_device_info(&info) != cudaSuccess) return 0;
+  switch (op) {
+    case FR_OP_RELU_ADD_SUM: {
+      const fr_form f = form == FR_FORM_AUTO ? pick_ras(rows, cols, info.sm_count) : form;
+      return f == FR_FORM_SPLIT ? fr::ras_split_workspace(rows, cols, info.sm_count) : 0;
+    }
+    case FR_OP_XENT: return fr::xent_workspace(rows, info.sm_count);
+    default: return 0;
+  }
+}
+
+fr_status fr_reduce_relu_add_sum(const void *a, const void *b, float *out, int64_t rows,
+                                 int64_t cols, int64_t lda, int64_t ldb, fr_dtype dtype,
+                                 float scale, fr_form form, void *workspace,
+                                 size_t workspace_bytes, fr_stream_t stream) {
+  if (dtype != FR_F32) return FR_ERR_UNSUPPORTED_DTYPE;
+  if (!a || !b || !out) return FR_ERR_INVALID_ARG;
+  if (!shape_ok(rows, cols, lda, 4) || !shape_ok(rows, cols, ldb, 4)) return FR_ERR_INVALID_ARG;
+  if (!aligned(a, 4) || !aligned(b, 4) || !aligned(out, 4)) return FR_ERR_MISALIGNED;
+  fr::DevInfo info;
+  if (fr_status st = device_ok(&info)) return st;
+  const fr_form f = form == FR_FORM_AUTO ? pick_ras(rows, cols, info.sm_count) : form;
+  const bool vec = same_phase(a, lda, b, ldb, 4);
+  const float *fa = static_cast<const float *>(a);
+  const float *fb = static_cast<const float *>(b);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (f) {
+    case FR_FORM_PERSISTENT:
+      if (cols > fr::ras_persistent_max_cols()) return FR_ERR_UNSUPPORTED_FORM;
+      return launched(fr::launch_ras_persistent(fa, fb, out, rows, cols, lda, ldb, scale, vec, s), f);
+    case FR_FORM_LOOPED:
+      return launched(fr::launch_ras_looped(fa, fb, out, rows, cols, lda, ldb, scale, vec, s), f);
+    case FR_FORM_SPLIT: {
+      if (rows > 65535) return FR_ERR_UNSUPPORTED_FORM;
+      const size_t need = fr::ras_split_workspace(rows, cols, info.sm_count);
+      if (!workspace || workspace_bytes < need) return FR_ERR_WORKSPACE_TOO_SMALL;
+      if (!aligned(workspace, 16)) return FR_ERR_MISALIGNED;
+      const int segs = fr::ras_split_segments(rows, cols, info.sm_count);
+      return launched(fr::launch_ras_split(fa, fb, out, rows, cols, lda, ldb, scale, vec,
+                                           static_cast<double *>(workspace), segs, s), f);
+    }
+    default: return FR_ERR_UNSUPPORTED_FORM;
+  }
+}
+
+fr_status fr_softmax(const void *x, void *y, int64_t rows, int64_t cols, int64_t ldx,
+                     int64_t ldy, fr_dtype dtype, fr_form form, fr_stream_t stream) {
+  if (dtype != FR_F32) return FR_ERR_UNSUPPORTED_DTYPE;
+  if (!x || !y) return FR_ERR_INVALID_ARG;
+  if (!shape_ok(rows, cols, ldx, 4) || !shape_ok(rows, cols, ldy, 4)) return FR_ERR_INVALID_ARG;
+  if (!aligned(x, 4) || !aligned(y, 4)) return FR_ERR_MISALIGNED;
+  if (x == y && ldx != ldy) return FR_ERR_INVALID_ARG;
+  fr::DevInfo info;
+  if (fr_status st = device_ok(&info)) return st;
+  const bool vec = same_phase(x, ldx, y, ldy, 4);
+  const fr_form f = form == FR_FORM_AUTO ? pick_softmax(rows, cols, vec) : form;
+  const float *fx = static_cast<const float *>(x);
+  float *fy = static_cast<float *>(y);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (f) {
+    case FR_FORM_PERSISTENT:
+      if (cols > fr::softmax_persistent_max_cols(vec)) return FR_ERR_UNSUPPORTED_FORM;
+      return launched(fr::launch_softmax_persistent(fx, fy, rows, cols, ldx, ldy, vec, s), f);
+    case FR_FORM_LOOPED:
+      return launched(fr::launch_softmax_looped(fx, fy, rows, cols, ldx, ldy, vec, info.sm_count, s), f);
+    default: return FR_ERR_UNSUPPORTED_FORM;
+  }
+}
+
+fr_status fr_layernorm(const void *x, const float *gamma, const float *beta, void *y,
+                       float *mean, float *rstd, int64_t rows, int64_t cols, int64_t ldx,
+                       int64_t ldy, float eps, fr_dtype dtype, fr_form form,
+                       fr_stream_t stream) {
+  if (dtype != FR_BF16) return FR_ERR_UNSUPPORTED_DTYPE;
+  if (!x || !gamma || !beta || !y) return FR_ERR_INVALID_ARG;
+  if (!shape_ok(rows, cols, ldx, 2) || !shape_ok(rows, cols, ldy, 2)) return FR_ERR_INVALID_ARG;
+  if (!(eps >= 0.0f)) return FR_ERR_INVALID_ARG;
+  if (!aligned(x, 2) || !aligned(y, 2) || !aligned(gamma, 4) || !aligned(beta, 4) ||
+      (mean && !aligned(mean, 4)) || (rstd && !aligned(rstd, 4)))
+    return FR_ERR_MISALIGNED;
+  fr::DevInfo info;
+  if (fr_status st = device_ok(&info)) return st;
+  const bool vec = aligned(x, 32) && aligned(y, 32) && aligned(gamma, 32) && aligned(beta, 32) &&
+                   ldx % 16 == 0 && ldy % 16 == 0 && cols % 16 == 0;
+  const fr_form f = form == FR_FORM_AUTO ? pick_layernorm(rows, cols, vec, info.max_smem_optin) : form;
+  const uint16_t *bx = static_cast<const uint16_t *>(x);
+  uint16_t *by = static_cast<uint16_t *>(y);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (f) {
+    case FR_FORM_PERSISTENT:
+      if (!fr::layernorm_persistent_ok(cols, vec)) return FR_ERR_UNSUPPORTED_FORM;
+      return launched(fr::launch_layernorm_persistent(bx, gamma, beta, by, mean, rstd, rows, cols,
+                                                      ldx, ldy, eps, s), f);
+    case FR_FORM_LOOPED:
+      return launched(fr::launch_layernorm_looped(bx, gamma, beta, by, mean, rstd, rows, cols, ldx,
+                                                  ldy, eps, vec, info.sm_count,
+                                                  info.max_smem_optin, s), f);
+    default: return FR_ERR_UNSUPPORTED_FORM;
+  }
+}
+
+fr_status fr_xent(const void *logits, const int64_t *target, float *loss, float *loss_mean,
+                  float *target_logit, int64_t *argmax, int64_t rows, int64_t cols, int64_t ld,
+                  int64_t ignore_index, fr_dtype dtype, fr_form form, void *workspace,
+                  size_t workspace_bytes, fr_stream_t stream) {
+  if (dtype != FR_BF16) return FR_ERR_UNSUPPORTED_DTYPE;
+  if (!logits || !target) return FR_ERR_INVALID_ARG;
+  if (!shape_ok(rows, cols, ld, 2)) return FR_ERR_INVALID_ARG;
+  if (!aligned(logits, 2) || !aligned(target, 8) || (loss && !aligned(loss, 4)) ||
+      (loss_mean && !aligned(loss_mean, 4)) || (target_logit && !aligned(target_logit, 4)) ||
+      (argmax && !aligned(argmax, 8)))
+    return FR_ERR_MISALIGNED;
+  if (form != FR_FORM_AUTO && form != FR_FORM_LOOPED) return FR_ERR_UNSUPPORTED_FORM;
+  fr::DevInfo info;
+  if (fr_status st = device_ok(&info)) return st;
+  if (loss_mean) {
+    if (!workspace || workspace_bytes < fr::xent_workspace(rows, info.sm_count))
+      return FR_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned(workspace, 16)) return FR_ERR_MISALIGNED;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return launched(fr::launch_xent(static_cast<const uint16_t *>(logits), target, loss, loss_mean,
+                                  target_logit, argmax, rows, cols, ld, ignore_index, workspace,
+                                  info.sm_count, s),
+                  FR_FORM_LOOPED);
+}
+
+fr_status fr_check_device_error(fr_stream_t stream, int32_t *code) {
+  int v = 0;
+  if (fr::device_error_read_and_clear(reinterpret_cast<cudaStream_t>(stream), &v) != cudaSuccess)
+    return FR_ERR_CUDA;
+  if (code) *code = v;
+  return v == 0 ? FR_OK : FR_ERR_DEVICE_DATA;
+}
+
+}  // extern "C"

@@ -1,0 +1,72 @@
+// Host-side launchers of the row-reduction kernels.  Only fr_api.cu calls
+// these; each returns the launch's cudaError_t and never synchronises.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fr {
+
+// Properties of the current device the launch shapes depend on.
+struct DevInfo {
+  int device;
+  int sm_count;
+  int cc_major, cc_minor;
+  int max_smem_optin;  // bytes of shared memory one CTA may opt in to
+};
+cudaError_t current_device_info(DevInfo *out);
+
+// ---- Example 1.1: out[x] = sum_r scale * relu(a + b) ------------------------
+
+// Largest row (elements) the persistent form holds in one pass.
+int64_t ras_persistent_max_cols();
+// Segments per row of the split form for this shape (fixed per device model).
+int ras_split_segments(int64_t rows, int64_t cols, int sm_count);
+size_t ras_split_workspace(int64_t rows, int64_t cols, int sm_count);
+
+cudaError_t launch_ras_persistent(const float *a, const float *b, float *out, int64_t rows,
+                                  int64_t cols, int64_t lda, int64_t ldb, float scale,
+                                  bool vec, cudaStream_t s);
+cudaError_t launch_ras_looped(const float *a, const float *b, float *out, int64_t rows,
+                              int64_t cols, int64_t lda, int64_t ldb, float scale, bool vec,
+                              cudaStream_t s);
+cudaError_t launch_ras_split(const float *a, const float *b, float *out, int64_t rows,
+                             int64_t cols, int64_t lda, int64_t ldb, float scale, bool vec,
+                             double *partials, int segments, cudaStream_t s);
+
+// ---- softmax ---------------------------------------------------------------
+
+int64_t softmax_persistent_max_cols(bool vec);
+cudaError_t launch_softmax_persistent(const float *x, float *y, int64_t rows, int64_t cols,
+                                      int64_t ldx, int64_t ldy, bool vec, cudaStream_t s);
+cudaError_t launch_softmax_looped(const float *x, float *y, int64_t rows, int64_t cols,
+                                  int64_t ldx, int64_t ldy, bool vec, int sm_count,
+                                  cudaStream_t s);
+
+// ---- LayerNorm -------------------------------------------------------------
+
+// True when the persistent (register-resident) form can hold this row.
+bool layernorm_persistent_ok(int64_t cols, bool vec);
+bool layernorm_looped_ring_ok(int64_t cols, bool vec, int max_smem_optin);
+cudaError_t launch_layernorm_persistent(const uint16_t *x, const float *gamma,
+                                        const float *beta, uint16_t *y, float *mean,
+                                        float *rstd, int64_t rows, int64_t cols, int64_t ldx,
+                                        int64_t ldy, float eps, cudaStream_t s);
+cudaError_t launch_layernorm_looped(const uint16_t *x, const float *gamma, const float *beta,
+                                    uint16_t *y, float *mean, float *rstd, int64_t rows,
+                                    int64_t cols, int64_t ldx, int64_t ldy, float eps,
+                                    bool vec, int sm_count, int max_smem_optin,
+                                    cudaStream_t s);
+
+// ---- cross entropy ---------------------------------------------------------
+
+size_t xent_workspace(int64_t rows, int sm_count);
+cudaError_t launch_xent(const uint16_t *logits, const int64_t *target, float *loss,
+                        float *loss_mean, float *target_logit, int64_t *argmax, int64_t rows,
+                        int64_t cols, int64_t ld, int64_t ignore_index, void *workspace,
+                        int sm_count, cudaStream_t s);
+// Reads and clears the device error word of the current device (synchronises s).
+cudaError_t device_error_read_and_clear(cudaStream_t s, int *code);
+
+}  // namespace fr

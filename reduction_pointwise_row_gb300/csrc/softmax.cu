@@ -1,0 +1,294 @@
+// Row softmax, "Stax (4): GPU Codegen and Dynamic Shapes", section 9.5
+// (Listing 9.5) and "CMU 15-779 Lecture 8", section 3:
+//     m = max_r x,   y = exp(x - m) / sum_r exp(x - m).
+//
+// persistent  one warp per row, the row held in registers (up to 1024 fp32 per
+//             warp), the max and the sum taken in two passes over registers:
+//             one read and one write of each element (the 2N lower bound).
+// looped      one CTA per row (grid-stride over rows) for rows longer than a
+//             warp can hold.  Pass 1 keeps a per-thread online pair (m, d) and
+//             folds each chunk in with the merge of section 9.5 (a chunk's max
+//             first, then one exponential per element and one rescale per
+//             chunk); the CTA combines the pairs with the same merge
+//             (Proposition 9.1 makes the order irrelevant).  Pass 2 streams the
+//             row again (an L2 hit when the row was just read) and writes y.
+//
+// exp(x - m) is computed as 2^(x*log2(e) - m*log2(e)) with one FMA and one
+// SFU instruction; masked lanes are -inf for the max and contribute 0 to the
+// sum.  A NaN makes the row's max NaN (max.NaN), hence the whole row NaN.
+#include "common.cuh"
+#include "launch.h"
+
+namespace fr {
+namespace {
+
+constexpr int kWarpRowThreads = 256;
+constexpr int kLoopThreads = 512;
+constexpr int kLoopU = 2;
+
+__device__ __forceinline__ float fbits(uint32_t w) { return __uint_as_float(w); }
+
+// Persistent form, 32-byte vectors: NV vectors per lane (cols <= 256*NV).
+// x and y rows share their offset modulo 32 bytes (checked by the host).
+template <int NV>
+__global__ void __launch_bounds__(kWarpRowThreads)
+softmax_warp_vec(const float *__restrict__ x, float *__restrict__ y, int64_t rows, int64_t cols,
+                 int64_t ldx, int64_t ldy) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row =
+      static_cast<int64_t>(blockIdx.x) * (kWarpRowThreads / 32) + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const float *px = x + row * ldx;
+  float *py = y + row * ldy;
+  const RowSplit sp = row_split(px, cols, 4);
+  // head and tail scalars (at most 7 + 7): one per lane
+  int64_t si = -1;
+  if (lane < sp.head) si = lane;
+  else if (lane < sp.head + sp.tail) si = sp.head + sp.nvec * 8 + (lane - sp.head);
+  const float *vx = px + sp.head;
+  V8 v[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int64_t vi = lane + 32 * k;
+    if (vi < sp.nvec) v[k] = ld_stream_v8(vx + vi * 8);
+  }
+  float sv = -INFINITY;
+  if (si >= 0) sv = ld_stream_f32(px + si);
+
+  float m = sv;
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+    if (lane + 32 * k < sp.nvec) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m = max_nan(m, fbits(v[k].w[j]));
+    }
+  m = warp_max_nan(m);
+  const float mb = m * kLog2e;
+
+  float se = si >= 0 ? ex2(fmaf(sv, kLog2e, -mb)) : 0.0f;
+  float d = se;
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+    if (lane + 32 * k < sp.nvec) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float e = ex2(fmaf(fbits(v[k].w[j]), kLog2e, -mb));
+        v[k].w[j] = __float_as_uint(e);
+        d += e;
+      }
+    }
+  d = warp_sum(d);
+  const float inv = __frcp_rn(d);
+
+  float *vy = py + sp.head;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int64_t vi = lane + 32 * k;
+    if (vi < sp.nvec) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[k].w[j] = __float_as_uint(fbits(v[k].w[j]) * inv);
+      st_stream_v8(vy + vi * 8, v[k]);
+    }
+  }
+  if (si >= 0) st_stream_f32(py + si, se * inv);
+}
+
+// Persistent form, scalar lane-strided elements (rows without a shared 32-byte
+// alignment): NS elements per lane, cols <= 32*NS.
+template <int NS>
+__global__ void __launch_bounds__(kWarpRowThreads)
+softmax_warp_scalar(const float *__restrict__ x, float *__restrict__ y, int64_t rows,
+                    int64_t cols, int64_t ldx, int64_t ldy) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row =
+      static_cast<int64_t>(blockIdx.x) * (kWarpRowThreads / 32) + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const float *px = x + row * ldx;
+  float *py = y + row * ldy;
+  float v[NS];
+#pragma unroll
+  for (int k = 0; k < NS; ++k) {
+    const int64_t i = lane + 32 * k;
+    v[k] = i < cols ? ld_stream_f32(px + i) : -INFINITY;
+  }
+  float m = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < NS; ++k)
+    if (lane + 32 * k < cols) m = max_nan(m, v[k]);
+  m = warp_max_nan(m);
+  const float mb = m * kLog2e;
+  float d = 0.0f;
+#pragma unroll
+  for (int k = 0; k < NS; ++k)
+    if (lane + 32 * k < cols) {
+      v[k] = ex2(fmaf(v[k], kLog2e, -mb));
+      d += v[k];
+    }
+  d = warp_sum(d);
+  const float inv = __frcp_rn(d);
+#pragma unroll
+  for (int k = 0; k < NS; ++k) {
+    const int64_t i = lane + 32 * k;
+    if (i < cols) st_stream_f32(py + i, v[k] * inv);
+  }
+}
+
+// Fold `n` values (already max-reduced to cm) into the online pair st.
+__device__ __forceinline__ MD fold_chunk(MD st, float cm) {
+  const float M = max_nan(st.m, cm);
+  if (M == -INFINITY) return st;  // nothing but masked values so far
+  st.d = st.d * ex2((st.m - M) * kLog2e);
+  st.m = M;
+  return st;
+}
+
+// CTA-wide merge of the per-thread pairs; every thread gets the row's (m, d).
+__device__ __forceinline__ MD block_md(MD st, MD *smem) {
+  constexpr int NW = kLoopThreads / 32;
+  st = warp_md(st);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) smem[warp] = st;
+  __syncthreads();
+  MD r = lane < NW ? smem[lane] : MD{-INFINITY, 0.0f};
+  r = warp_md(r);
+  __syncthreads();  // smem free for the next row
+  return r;
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(kLoopThreads)
+softmax_block_looped(const float *__restrict__ x, float *__restrict__ y, int64_t rows,
+                     int64_t cols, int64_t ldx, int64_t ldy) {
+  __shared__ MD red[kLoopThreads / 32];
+  const int tid = threadIdx.x;
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    const float *px = x + row * ldx;
+    float *py = y + row * ldy;
+    const RowSplit sp = VEC ? row_split(px, cols, 4) : RowSplit{0, 0, static_cast<int>(0)};
+    MD st{-INFINITY, 0.0f};
+    if constexpr (VEC) {
+      const float *vx = px + sp.head;
+      for (int64_t base = 0; base < sp.nvec; base += kLoopThreads * kLoopU) {
+        V8 v[kLoopU];
+        float cm = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < kLoopU; ++u) {
+          const int64_t vi = base + tid + kLoopThreads * u;
+          if (vi < sp.nvec) {
+            v[u] = ld_keep_v8(vx + vi * 8);  // pass 2 re-reads it from L2
+#pragma unroll
+            for (int j = 0; j < 8; ++j) cm = max_nan(cm, fbits(v[u].w[j]));
+          }
+        }
+        st = fold_chunk(st, cm);
+        if (st.m == -INFINITY) continue;  // every value so far is -inf: adds 0
+        const float mb = st.m * kLog2e;
+#pragma unroll
+        for (int u = 0; u < kLoopU; ++u)
+          if (base + tid + kLoopThreads * u < sp.nvec) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) st.d += ex2(fmaf(fbits(v[u].w[j]), kLog2e, -mb));
+          }
+      }
+      int64_t si = -1;
+      if (tid < sp.head) si = tid;
+      else if (tid < sp.head + sp.tail) si = sp.head + sp.nvec * 8 + (tid - sp.head);
+      if (si >= 0) st = md_merge(st, MD{ld_stream_f32(px + si), 1.0f});
+    } else {
+      for (int64_t base = 0; base < cols; base += kLoopThreads * 8) {
+        float v[8];
+        float cm = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int64_t i = base + tid + kLoopThreads * u;
+          v[u] = i < cols ? px[i] : -INFINITY;
+          cm = max_nan(cm, v[u]);
+        }
+        st = fold_chunk(st, cm);
+        if (st.m == -INFINITY) continue;
+        const float mb = st.m * kLog2e;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (base + tid + kLoopThreads * u < cols) st.d += ex2(fmaf(v[u], kLog2e, -mb));
+      }
+    }
+    const MD r = block_md(st, red);
+    const float mb = r.m * kLog2e;
+    const float inv = __frcp_rn(r.d);
+    if constexpr (VEC) {
+      const float *vx = px + sp.head;
+      float *vy = py + sp.head;
+      for (int64_t base = 0; base < sp.nvec; base += kLoopThreads * kLoopU) {
+        V8 v[kLoopU];
+#pragma unroll
+        for (int u = 0; u < kLoopU; ++u) {
+          const int64_t vi = base + tid + kLoopThreads * u;
+          if (vi < sp.nvec) v[u] = ld_stream_v8(vx + vi * 8);
+        }
+#pragma unroll
+        for (int u = 0; u < kLoopU; ++u) {
+          const int64_t vi = base + tid + kLoopThreads * u;
+          if (vi < sp.nvec) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              v[u].w[j] = __float_as_uint(ex2(fmaf(fbits(v[u].w[j]), kLog2e, -mb)) * inv);
+            st_stream_v8(vy + vi * 8, v[u]);
+          }
+        }
+      }
+      int64_t si = -1;
+      if (tid < sp.head) si = tid;
+      else if (tid < sp.head + sp.tail) si = sp.head + sp.nvec * 8 + (tid - sp.head);
+      if (si >= 0) st_stream_f32(py + si, ex2(fmaf(ld_stream_f32(px + si), kLog2e, -mb)) * inv);
+    } else {
+      for (int64_t i = tid; i < cols; i += kLoopThreads)
+        st_stream_f32(py + i, ex2(fmaf(ld_stream_f32(px + i), kLog2e, -mb)) * inv);
+    }
+  }
+}
+
+unsigned warp_row_grid(int64_t rows) {
+  return static_cast<unsigned>((rows + kWarpRowThreads / 32 - 1) / (kWarpRowThreads / 32));
+}
+
+}  // namespace
+
+int64_t softmax_persistent_max_cols(bool vec) { return vec ? 1024 : 1024; }
+
+cudaError_t launch_softmax_persistent(const float *x, float *y, int64_t rows, int64_t cols,
+                                      int64_t ldx, int64_t ldy, bool vec, cudaStream_t s) {
+  const unsigned grid = warp_row_grid(rows);
+  if (vec) {
+    const int64_t nv = (cols + 255) / 256;
+    switch (nv) {
+      case 1: softmax_warp_vec<1><<<grid, kWarpRowThreads, 0, s>>>(x, y, rows, cols, ldx, ldy); break;
+      case 2: softmax_warp_vec<2><<<grid, kWarpRowThreads, 0, s>>>(x, y, rows, cols, ldx, ldy); break;
+      case 3: softmax_warp_vec<3><<<grid, kWarpRowThreads, 0, s>>>(x, y, rows, cols, ldx, ldy); break;
+      case 4: softmax_warp_vec<4><<<grid, kWarpRowThreads, 0, s>>>(x, y, rows, cols, ldx, ldy); break;
+      default: return cudaErrorInvalidValue;
+    }
+  } else {
+    if (cols <= 128) softmax_warp_scalar<4><<<grid, kWarpRowThreads, 0, s>>>(x, y, rows, cols, ldx, ldy);
+    else if (cols <= 256) softmax_warp_scalar<8><<<grid, kWarpRowThreads, 0, s>>>(x, y, rows, cols, ldx, ldy);
+    else if (cols <= 512) softmax_warp_scalar<16><<<grid, kWarpRowThreads, 0, s>>>(x, y, rows, cols, ldx, ldy);
+    else if (cols <= 1024) softmax_warp_scalar<32><<<grid, kWarpRowThreads, 0, s>>>(x, y, rows, cols, ldx, ldy);
+    else return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_softmax_looped(const float *x, float *y, int64_t rows, int64_t cols,
+                                  int64_t ldx, int64_t ldy, bool vec, int sm_count,
+                                  cudaStream_t s) {
+  int64_t grid = static_cast<int64_t>(sm_count) * 2;
+  if (grid > rows) grid = rows;
+  if (vec)
+    softmax_block_looped<true><<<static_cast<unsigned>(grid), kLoopThreads, 0, s>>>(
+        x, y, rows, cols, ldx, ldy);
+  else
+    softmax_block_looped<false><<<static_cast<unsigned>(grid), kLoopThreads, 0, s>>>(
+        x, y, rows, cols, ldx, ldy);
+  return cudaGetLastError();
+}
+
+}  // namespace fr

@@ -1,0 +1,309 @@
+"""GPU parity: every op, every form, against the CPU oracle, element by element.
+
+Shapes span several tiles with ragged tails (row lengths that are not powers of
+two, rows that are not 32-byte aligned, padded row strides); outputs live in
+canary-filled buffers so a write outside the logical block fails the test.
+Tolerances are those of tests/compare.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import reduction_pointwise_row_gb300 as fr
+import synth
+from compare import assert_bits_equal, assert_close
+from gpu_util import bf16_to_f32_host, bf16_tensor, empty_like_placed, place
+from synth import workloads
+
+pytestmark = pytest.mark.gpu
+
+COLS = [1, 2, 3, 7, 13, 31, 33, 127, 128, 129, 781, 1000, 1023, 1024, 1025, 4097]
+# (offset of input a/x, offset of b/y, extra row padding)
+LAYOUTS = [(0, 0, 0), (1, 1, 5), (0, 3, 0)]
+
+
+@pytest.fixture(scope="module")
+def o():
+    return oracle.get()
+
+
+def forms_for(op, cols):
+    if op == "relu_add_sum":
+        return (["persistent"] if cols <= 1024 else []) + ["looped", "split"]
+    if op == "softmax":
+        return (["persistent"] if cols <= 1024 else []) + ["looped"]
+    raise ValueError(op)
+
+
+# ---------------------------------------------------------------- Example 1.1
+
+def run_ras(a, b, form, la=(0, 0, 0), scale=2.0):
+    rows, cols = a.shape
+    oa, ob, pad = la
+    pa = place(a, oa, cols + pad)
+    pb = place(b, ob, cols + pad)
+    po = empty_like_placed(1, rows, torch.float32)
+    fr.fr_reduce_relu_add_sum(pa.t, pb.t, scale, form=form, out=po.t[0])
+    torch.cuda.synchronize()
+    assert po.canaries_intact(), "write outside out[]"
+    return po.t[0].cpu().numpy()
+
+
+@pytest.mark.parametrize("cols", COLS)
+@pytest.mark.parametrize("rows", [1, 7, 65])
+@pytest.mark.parametrize("layout", LAYOUTS, ids=["aligned", "offset_same_phase", "offset_scalar"])
+def test_relu_add_sum_forms(o, rows, cols, layout):
+    w = workloads.make(0, rows=rows, cols=cols, seed=1000 + rows * 7 + cols)
+    ref = o.relu_add_sum(w.arrays["a"], w.arrays["b"], 2.0)
+    for form in forms_for("relu_add_sum", cols):
+        got = run_ras(w.arrays["a"], w.arrays["b"], form, layout)
+        assert_close(got, ref, "f32", f"{form} {rows}x{cols} {layout}")
+
+
+def test_relu_add_sum_example_1_1_and_nan_variant(o):
+    for nan in (False, True):
+        w = workloads.make(0, nan_variant=nan)
+        ref = o.relu_add_sum(w.arrays["a"], w.arrays["b"], 2.0)
+        for form in ("auto", "persistent", "looped", "split"):
+            got = run_ras(w.arrays["a"], w.arrays["b"], form)
+            assert_close(got, ref, "f32", f"Example 1.1 {form} nan={nan}")
+        if nan:
+            rows_with_nan = {r for _, r, _ in w.params["nan_positions"]}
+            assert set(np.flatnonzero(np.isnan(got)).tolist()) == rows_with_nan
+
+
+@pytest.mark.parametrize("cols", [128, 1000, 4097, 65535])
+def test_relu_add_sum_dyadic_is_bit_exact(o, cols):
+    """k/64 inputs: every partial sum is exact, so all forms equal the oracle bitwise."""
+    rng = np.random.default_rng(cols)
+    a = (rng.integers(-64, 65, (9, cols)) / 64).astype(np.float32)
+    b = (rng.integers(-64, 65, (9, cols)) / 64).astype(np.float32)
+    ref = o.relu_add_sum(a, b, 2.0).astype(np.float32)
+    for form in forms_for("relu_add_sum", cols):
+        assert_bits_equal(run_ras(a, b, form), ref, f"{form} {cols}")
+
+
+def test_relu_add_sum_split_long_rows_deterministic(o):
+    rows, cols = 3, (1 << 20) + 3
+    w = workloads.make(3, rows=rows, cols=cols)
+    ref = o.relu_add_sum(w.arrays["a"], w.arrays["b"], 2.0)
+    pa, pb = place(w.arrays["a"], 1), place(w.arrays["b"], 1)
+    first = None
+    for _ in range(50):
+        got = fr.fr_reduce_relu_add_sum(pa.t, pb.t, 2.0, form="split").cpu().numpy()
+        if first is None:
+            first = got
+            assert_close(got, ref, "f32", "split long rows")
+        assert_bits_equal(got, first, "split run-to-run")
+
+
+def test_relu_add_sum_scale_and_infinities(o):
+    a = np.array([[np.inf, 1.0, -2.0], [-np.inf, 0.5, 0.25], [np.inf, 0.0, 0.0]], np.float32)
+    b = np.array([[1.0, 1.0, 1.0], [1.0, 0.5, 0.25], [-np.inf, 0.0, 0.0]], np.float32)
+    for scale in (2.0, -3.0, 0.5):
+        ref = o.relu_add_sum(a, b, scale)
+        for form in forms_for("relu_add_sum", 3):
+            assert_close(run_ras(a, b, form, scale=scale), ref, "f32", f"{form} scale {scale}")
+
+
+# ---------------------------------------------------------------- softmax
+
+def run_softmax(x, form, layout=(0, 0, 0)):
+    rows, cols = x.shape
+    ox, oy, pad = layout
+    px = place(x, ox, cols + pad)
+    py = empty_like_placed(rows, cols, torch.float32, oy, cols + pad)
+    fr.fr_softmax(px.t, form=form, out=py.t)
+    torch.cuda.synchronize()
+    assert py.canaries_intact(), "softmax wrote outside y"
+    return py.t.cpu().numpy()
+
+
+@pytest.mark.parametrize("cols", COLS + [65537])
+@pytest.mark.parametrize("rows", [1, 7, 33])
+@pytest.mark.parametrize("layout", LAYOUTS, ids=["aligned", "offset_same_phase", "offset_scalar"])
+def test_softmax_forms(o, rows, cols, layout):
+    w = workloads.make(1, rows=rows, cols=cols, seed=2000 + rows * 7 + cols)
+    ref = o.softmax(w.arrays["x"])
+    for form in forms_for("softmax", cols):
+        assert_close(run_softmax(w.arrays["x"], form, layout), ref, "f32",
+                     f"{form} {rows}x{cols} {layout}")
+
+
+@pytest.mark.parametrize("cols", [5, 1000, 4097])
+def test_softmax_special_values(o, cols):
+    x = workloads.make(1, rows=6, cols=cols, seed=7).arrays["x"].copy()
+    x[1, cols // 2] = np.nan                 # NaN row
+    x[2, : cols // 2] = -np.inf              # partly -inf
+    x[3, :] = -np.inf                        # all -inf: 0/0
+    x[4, cols - 1] = np.inf                  # +inf: inf - inf
+    ref = o.softmax(x)
+    for form in forms_for("softmax", cols):
+        got = run_softmax(x, form)
+        assert_close(got, ref, "f32", f"{form} special {cols}")
+        assert np.isnan(got[[1, 3, 4]]).all() and np.isfinite(got[[0, 2, 5]]).all()
+
+
+def test_softmax_in_place_and_rows_sum_to_one(o):
+    w = workloads.make(1, rows=65, cols=1000)
+    ref = o.softmax(w.arrays["x"])
+    for form in ("persistent", "looped"):
+        t = torch.from_numpy(w.arrays["x"]).cuda()
+        fr.fr_softmax(t, form=form, out=t)
+        got = t.cpu().numpy()
+        assert_close(got, ref, "f32", f"in place {form}")
+        assert np.abs(got.astype(np.float64).sum(1) - 1).max() < 1e-5
+
+
+# ---------------------------------------------------------------- LayerNorm
+
+def run_layernorm(x_bits, gamma, beta, eps, form, offset=0):
+    rows, cols = x_bits.shape
+    px = place(x_bits, offset)
+    py = empty_like_placed(rows, cols, torch.bfloat16, offset)
+    g, b = torch.from_numpy(gamma).cuda(), torch.from_numpy(beta).cuda()
+    mean = torch.full((rows,), float("nan"), device="cuda")
+    rstd = torch.full((rows,), float("nan"), device="cuda")
+    fr.fr_layernorm(px.t, g, b, eps, form=form, out=py.t, mean=mean, rstd=rstd)
+    torch.cuda.synchronize()
+    assert py.canaries_intact(), "layernorm wrote outside y"
+    return bf16_to_f32_host(py.t), mean.cpu().numpy(), rstd.cpu().numpy()
+
+
+@pytest.mark.parametrize("cols", [1, 3, 16, 32, 48, 781, 1000, 1024, 4096, 4112, 32768, 65537])
+@pytest.mark.parametrize("rows", [1, 7, 33])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_layernorm_forms(o, rows, cols, offset):
+    w = workloads.make(2, rows=rows, cols=cols, seed=3000 + rows * 7 + cols)
+    eps = float(np.float32(w.params["eps"]))
+    ry, rm, rr = o.layernorm(w.arrays["x"], w.arrays["gamma"], w.arrays["beta"], eps)
+    vec_ok = offset == 0 and cols % 16 == 0 and cols <= 32768
+    forms = (["persistent"] if vec_ok else []) + ["looped"]
+    for form in forms:
+        y, m, r = run_layernorm(w.arrays["x"], w.arrays["gamma"], w.arrays["beta"], eps, form,
+                                offset)
+        assert_close(y, ry, "bf16", f"{form} y {rows}x{cols}")
+        assert_close(m, rm, "mean", f"{form} mean")
+        assert_close(r, rr, "f32", f"{form} rstd")
+    if not vec_ok:
+        with pytest.raises(fr.FRError) as e:
+            run_layernorm(w.arrays["x"], w.arrays["gamma"], w.arrays["beta"], eps, "persistent",
+                          offset)
+        assert e.value.status == 3
+
+
+def test_layernorm_constant_rows(o):
+    cols = 4096
+    x = np.full((4, cols), 0x4060, np.uint16)  # 3.5 in bf16
+    gamma = np.ones(cols, np.float32)
+    beta = np.linspace(-1, 1, cols).astype(np.float32)
+    eps = float(np.float32(1e-5))
+    ry, rm, rr = o.layernorm(x, gamma, beta, eps)
+    for form in ("persistent", "looped"):
+        y, m, r = run_layernorm(x, gamma, beta, eps, form)
+        assert_close(y, ry, "bf16", form)
+        assert (m == 3.5).all()
+        assert_close(r, rr, "f32", form)
+
+
+# ---------------------------------------------------------------- cross entropy
+
+def run_xent(bits, target, ignore=-100, offset=0, pad=0):
+    rows, cols = bits.shape
+    px = place(bits, offset, cols + pad)
+    t = torch.from_numpy(target).cuda()
+    r = fr.fr_xent(px.t, t, ignore, want_target_logit=True, want_argmax=True)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in r.items()}
+
+
+def check_xent(got, ref, what):
+    assert_close(got["loss"], ref["loss"], "loss", f"{what} loss")
+    assert_close(got["mean"][0], ref["mean"], "loss", f"{what} mean")
+    assert_bits_equal(got["target_logit"], ref["target_logit"].astype(np.float32),
+                      f"{what} target logit")
+    assert_bits_equal(got["argmax"], ref["argmax"], f"{what} argmax")
+
+
+@pytest.mark.parametrize("cols", [1, 2, 3, 7, 13, 31, 33, 127, 128, 129, 1000, 4097, 50257])
+@pytest.mark.parametrize("rows", [1, 7, 65])
+@pytest.mark.parametrize("layout", [(0, 0), (1, 0), (3, 5)], ids=["base0", "base1", "base3_pad5"])
+def test_xent(o, rows, cols, layout):
+    w = workloads.make(4, rows=rows, cols=cols, seed=4000 + rows * 7 + cols)
+    ref = o.xent(w.arrays["logits"], w.arrays["target"], -100)
+    got = run_xent(w.arrays["logits"], w.arrays["target"], -100, *layout)
+    check_xent(got, ref, f"{rows}x{cols} {layout}")
+    assert fr.fr_check_device_error() == 0
+
+
+def test_xent_ties_nan_and_ignore(o):
+    rng = np.random.default_rng(5)
+    rows, cols = 40, 3001
+    vals = rng.integers(-3, 4, (rows, cols)).astype(np.float32)  # many ties
+    bits = (vals.view(np.uint32) >> 16).astype(np.uint16)
+    bits[5, 17] = 0x7FC0            # NaN
+    bits[6, [3, 2999]] = 0x7FC0     # two NaNs: first wins
+    bits[7, :] = 0xFF80             # all -inf
+    t = rng.integers(0, cols, rows)
+    t[[1, 2, 3]] = -100
+    ref = o.xent(bits, t, -100)
+    got = run_xent(bits, t, -100, offset=1)
+    check_xent(got, ref, "ties/nan")
+    assert got["argmax"][5] == 17 and got["argmax"][6] == 3
+    # every row ignored: mean is 0/0
+    allign = np.full(rows, -100, np.int64)
+    got = run_xent(bits, allign)
+    assert np.isnan(got["mean"][0]) and (got["loss"] == 0).all()
+    assert fr.fr_check_device_error() == 0
+
+
+def test_xent_bad_target_sets_device_error(o):
+    w = workloads.make(4, rows=9, cols=777)
+    t = w.arrays["target"].copy()
+    t[4] = 777          # == cols: out of range
+    t[6] = -5           # negative, not ignore_index
+    ref = o.xent(w.arrays["logits"], t, -100)
+    got = run_xent(w.arrays["logits"], t)
+    check_xent(got, ref, "bad target")
+    assert np.isnan(got["loss"][[4, 6]]).all()
+    assert fr.fr_check_device_error() == 1
+    assert fr.fr_check_device_error() == 0   # read clears it
+
+
+# ---------------------------------------------------------------- boundary
+
+def test_error_statuses_on_device():
+    x = torch.zeros(4, 2000, device="cuda")
+    with pytest.raises(fr.FRError) as e:
+        fr.fr_softmax(x, form="persistent")
+    assert e.value.status == 3
+    with pytest.raises(fr.FRError) as e:
+        fr.fr_softmax(x, form="split")
+    assert e.value.status == 3
+    a = torch.zeros(2, 1 << 20, device="cuda")
+    ws = torch.empty(8, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fr.FRError) as e:
+        fr.fr_reduce_relu_add_sum(a, a, 2.0, form="split", workspace=ws)
+    assert e.value.status == 5
+    lg = torch.zeros(3, 10, dtype=torch.bfloat16, device="cuda")
+    tg = torch.zeros(3, dtype=torch.int64, device="cuda")
+    with pytest.raises(fr.FRError) as e:
+        fr.fr_xent(lg, tg, form="persistent")
+    assert e.value.status == 3
+    assert fr.fr_last_form() in ("persistent", "looped", "split")
+
+
+def test_auto_form_choices():
+    a = torch.zeros(64, 128, device="cuda")
+    fr.fr_reduce_relu_add_sum(a, a)
+    assert fr.fr_last_form() == "persistent"
+    a = torch.zeros(8, 1 << 20, device="cuda")
+    fr.fr_reduce_relu_add_sum(a, a)
+    assert fr.fr_last_form() == "split"
+    x = torch.zeros(16, 1024, device="cuda")
+    fr.fr_softmax(x)
+    assert fr.fr_last_form() == "persistent"
+    x = torch.zeros(16, 4097, device="cuda")
+    fr.fr_softmax(x)
+    assert fr.fr_last_form() == "looped"
