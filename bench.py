@@ -4,9 +4,10 @@
 
 One JSON line on stdout (rank 0).  The headline workload is the fused softmax in
 its persistent form, fp32 [32768, 1024] (logits 4*N(0,1)); a step is one call
-of fr_softmax over that batch, inputs resident in HBM, the L2 flushed (a
-256 MiB write) before every step, each launch timed with CUDA events on the
-stream it runs on.  ``value`` is achieved HBM GB/s: algorithmic bytes (one read
+of fr_softmax over that batch, inputs resident in HBM, launched back to back
+over rotating copies of the inputs and outputs (1 GiB in all, eight times the
+L2, so no launch finds its operands cached), each launch timed with CUDA
+events on the stream it runs on.  ``value`` is achieved HBM GB/s: algorithmic bytes (one read
 and one write of every element) / mean launch time, summed over ranks.
 ``per_config`` adds the other workloads of the path measured the same way.
 ``e2e`` is the same metric through the same C-ABI call with the input copied
@@ -34,7 +35,6 @@ sys.path.insert(0, ROOT)
 HEADLINE = 1
 METRIC = "fused row-reduction achieved HBM GB/s and % of GB300 peak; rows/s per config"
 UNIT = "GB/s"
-FLUSH_BYTES = 256 << 20
 PROFILE = os.path.join(ROOT, "profiles", "softmax_persistent_32768x1024.md")
 KERNEL_SRC = os.path.join(ROOT, "reduction_pointwise_row_gb300", "csrc", "softmax.cu")
 
@@ -46,6 +46,8 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-extra", action="store_true", help="headline workload only")
+    p.add_argument("--only", choices=["relu_add_sum", "softmax", "layernorm", "split", "xent"],
+                   help="time one workload alone (for profiler captures) and exit")
     return p.parse_args()
 
 
@@ -173,8 +175,7 @@ def run_ours(args):
     fr.lib()
     peak, peak_kind = measured_peak()
     stream = torch.cuda.current_stream()
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(local) if not args.only else None
 
     def barrier():
         if world > 1:
@@ -190,36 +191,45 @@ def run_ours(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         return float(t.item())
 
-    def timed(call, steps, warmup, launches_per_call):
-        """Mean device time (s) of `call`, L2 flushed before each launch."""
-        for _ in range(warmup):
-            flush.zero_()
-            call()
+    def timed(calls, steps, warmup, launches_per_call):
+        """Mean device time (s) per launch: launches back to back, cycling over
+        the rotating input sets, each bracketed by CUDA events on the stream."""
+        for i in range(warmup):
+            calls[i % len(calls)]()
         barrier()
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         w0 = time.time()
         for i in range(steps):
-            flush.zero_()
             starts[i].record(stream)
-            call()
+            calls[i % len(calls)]()
             ends[i].record(stream)
         barrier()
-        clocks.window(w0, time.time())
+        if clocks:
+            clocks.window(w0, time.time())
         ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
         return max_over_ranks(statistics.fmean(ms) / 1e3), launches_per_call * steps, ms
+
+    if args.only:
+        res = extra_configs(fr, traffic, workloads, timed, dev, peak, args, world, [args.only])
+        if rank == 0:
+            print(json.dumps({"only": args.only, **next(iter(res.values()))}), flush=True)
+        return
 
     # ---- headline: softmax persistent fp32 [32768, 1024]
     w = workloads.make(HEADLINE)
     rows, cols = w.rows, w.cols
-    x_host = torch.from_numpy(w.arrays["x"]).pin_memory()
-    x = x_host.to(dev)
-    y = torch.empty_like(x)
-    fr.fr_softmax(x, out=y)
+    calls, _, _, _, _ = setup_workload("softmax", fr, workloads, dev)
+    calls[0]()
     form = fr.fr_last_form()
     nbytes = traffic.algorithmic_bytes("softmax", rows, cols)
-    t_launch, launches, ms = timed(lambda: fr.fr_softmax(x, out=y), args.steps, args.warmup, 1)
+    t_launch, launches, ms = timed(calls, args.steps, args.warmup, 1)
     value = world * nbytes / t_launch / 1e9
+    nsets = len(calls)
+    del calls
+    x_host = torch.from_numpy(w.arrays["x"]).pin_memory()
+    x = torch.empty(rows, cols, device=dev)
+    y = torch.empty_like(x)
 
     # ---- e2e through the same call with host buffers
     y_host = torch.empty_like(x_host).pin_memory()
@@ -262,7 +272,7 @@ def run_ours(args):
         "config": {"workload": "fused softmax, persistent form, fp32 [32768,1024]",
                    "rows": rows, "cols": cols, "form": form,
                    "rows_per_s": round(world * rows / t_launch, 1),
-                   "l2": "flushed before every step (256 MiB write)",
+                   "l2": f"inputs larger than L2: {nsets} rotating x/y sets (1 GiB), launches back to back",
                    "timing": "CUDA events per launch on the launching stream, mean",
                    "parallelism": f"replicas x{world} (rows shard, no collective)"},
         "roofline": {"bound": "hbm", "achieved": round(nbytes / t_launch / 1e9, 2),
@@ -283,61 +293,87 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def extra_configs(fr, traffic, workloads, timed, dev, peak, args, world):
-    import torch
+ROTATE_BYTES = 1 << 30  # footprint of the rotating input/output sets (8x the L2)
 
+
+def setup_workload(name, fr, workloads, dev):
+    """Device inputs and calls of one workload: (calls, op, rows, cols,
+    launches per call).  ``calls`` cycles over enough copies of the inputs
+    and outputs that their footprint is >= 1 GiB, so no launch finds its
+    operands in the 126 MB L2.  Inputs are generated on the host once."""
+    import torch
+    from reduction_pointwise_row_gb300 import traffic
+
+    def nsets(op, rows, cols):
+        return max(1, -(-ROTATE_BYTES // traffic.algorithmic_bytes(op, rows, cols)))
+
+    calls = []
+    if name == "relu_add_sum":
+        w = workloads.make(0)
+        a, b = to_device(w.arrays["a"], dev), to_device(w.arrays["b"], dev)
+        out = torch.empty(w.rows, device=dev)
+        calls.append(lambda: fr.fr_reduce_relu_add_sum(a, b, 2.0, out=out))
+        return calls, "relu_add_sum", w.rows, w.cols, 1
+    if name == "softmax":
+        w = workloads.make(1)
+        for _ in range(nsets("softmax", w.rows, w.cols)):
+            x = to_device(w.arrays["x"], dev)
+            y = torch.empty_like(x)
+            calls.append(lambda x=x, y=y: fr.fr_softmax(x, out=y))
+        return calls, "softmax", w.rows, w.cols, 1
+    if name == "layernorm":
+        w = workloads.make(2)
+        g, bt = to_device(w.arrays["gamma"], dev), to_device(w.arrays["beta"], dev)
+        for _ in range(nsets("layernorm", w.rows, w.cols)):
+            x = to_device(w.arrays["x"], dev)
+            y = torch.empty_like(x)
+            mean = torch.empty(w.rows, device=dev)
+            rstd = torch.empty(w.rows, device=dev)
+            calls.append(lambda x=x, y=y, mean=mean, rstd=rstd:
+                         fr.fr_layernorm(x, g, bt, 1e-5, out=y, mean=mean, rstd=rstd))
+        return calls, "layernorm", w.rows, w.cols, 1
+    if name == "split":
+        w = workloads.make(3)
+        rows, cols = w.rows, w.cols
+        for _ in range(nsets("relu_add_sum", rows, cols)):
+            a, b = to_device(w.arrays["a"], dev), to_device(w.arrays["b"], dev)
+            out = torch.empty(rows, device=dev)
+            ws = torch.empty(fr.fr_workspace_size("relu_add_sum", rows, cols), dtype=torch.uint8,
+                             device=dev)
+            calls.append(lambda a=a, b=b, out=out, ws=ws:
+                         fr.fr_reduce_relu_add_sum(a, b, 2.0, out=out, workspace=ws))
+        return calls, "relu_add_sum", rows, cols, 2
+    if name == "xent":
+        w = workloads.make(4)
+        rows, cols = w.rows, w.cols
+        tg = torch.from_numpy(w.arrays["target"]).to(dev)
+        for _ in range(nsets("xent", rows, cols)):
+            lg = to_device(w.arrays["logits"], dev)
+            wsx = torch.empty(fr.fr_workspace_size("xent", rows, cols, "bf16"),
+                              dtype=torch.uint8, device=dev)
+            calls.append(lambda lg=lg, wsx=wsx: fr.fr_xent(lg, tg, -100, workspace=wsx))
+        return calls, "xent", rows, cols, 1
+    raise ValueError(name)
+
+
+EXTRA = {"relu_add_sum": "relu_add_sum_64x128", "layernorm": "layernorm_4096x32768",
+         "split": "relu_add_sum_split_8x33554432", "xent": "xent_8192x50257"}
+
+
+def extra_configs(fr, traffic, workloads, timed, dev, peak, args, world, names=None):
     steps = max(3, min(args.steps, 50))
     res = {}
-
-    def record(name, op, rows, cols, t, launches, form):
+    for name in (names or EXTRA):
+        calls, op, rows, cols, lpc = setup_workload(name, fr, workloads, dev)
+        calls[0]()
+        t, n, _ = timed(calls, steps, args.warmup, lpc)
         nb = traffic.algorithmic_bytes(op, rows, cols)
-        res[name] = {"op": op, "rows": rows, "cols": cols, "form": form,
-                     "us": round(t * 1e6, 3), "gbs": round(nb / t / 1e9, 2),
-                     "frac": round(nb / t / 1e9 / peak, 4),
-                     "rows_per_s": round(world * rows / t, 1), "_launches": launches}
-
-    w = workloads.make(0)
-    a, b = to_device(w.arrays["a"], dev), to_device(w.arrays["b"], dev)
-    out = torch.empty(w.rows, device=dev)
-    fr.fr_reduce_relu_add_sum(a, b, 2.0, out=out)
-    t, n, _ = timed(lambda: fr.fr_reduce_relu_add_sum(a, b, 2.0, out=out), steps, args.warmup, 1)
-    record("relu_add_sum_64x128", "relu_add_sum", w.rows, w.cols, t, n, fr.fr_last_form())
-    del a, b
-
-    w = workloads.make(2)
-    x = to_device(w.arrays["x"], dev)
-    g, bt = to_device(w.arrays["gamma"], dev), to_device(w.arrays["beta"], dev)
-    y = torch.empty_like(x)
-    mean = torch.empty(w.rows, device=dev)
-    rstd = torch.empty(w.rows, device=dev)
-    call = lambda: fr.fr_layernorm(x, g, bt, 1e-5, out=y, mean=mean, rstd=rstd)
-    call()
-    t, n, _ = timed(call, steps, args.warmup, 1)
-    record("layernorm_4096x32768", "layernorm", w.rows, w.cols, t, n, fr.fr_last_form())
-    del x, y
-
-    w = workloads.make(3)
-    a, b = to_device(w.arrays["a"], dev), to_device(w.arrays["b"], dev)
-    del w
-    out = torch.empty(8, device=dev)
-    ws = torch.empty(fr.fr_workspace_size("relu_add_sum", 8, 33554432), dtype=torch.uint8,
-                     device=dev)
-    call = lambda: fr.fr_reduce_relu_add_sum(a, b, 2.0, out=out, workspace=ws)
-    call()
-    t, n, _ = timed(call, steps, args.warmup, 2)
-    record("relu_add_sum_split_8x33554432", "relu_add_sum", 8, 33554432, t, n, fr.fr_last_form())
-    del a, b
-
-    w = workloads.make(4)
-    lg = to_device(w.arrays["logits"], dev)
-    tg = torch.from_numpy(w.arrays["target"]).to(dev)
-    del w
-    wsx = torch.empty(fr.fr_workspace_size("xent", 8192, 50257, "bf16"), dtype=torch.uint8,
-                      device=dev)
-    call = lambda: fr.fr_xent(lg, tg, -100, workspace=wsx)
-    call()
-    t, n, _ = timed(call, steps, args.warmup, 1)
-    record("xent_8192x50257", "xent", 8192, 50257, t, n, fr.fr_last_form())
+        res[EXTRA.get(name, name)] = {
+            "op": op, "rows": rows, "cols": cols, "form": fr.fr_last_form(),
+            "us": round(t * 1e6, 3), "gbs": round(nb / t / 1e9, 2),
+            "frac": round(nb / t / 1e9 / peak, 4), "rows_per_s": round(world * rows / t, 1),
+            "_launches": n, "rotating_sets": len(calls)}
+        del calls
     return res
 
 
