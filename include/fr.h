@@ -187,6 +187,45 @@ fr_status fr_xent(const void *logits, const int64_t *target, float *loss, float 
                   void *workspace, size_t workspace_bytes, fr_stream_t stream);
 
 /*
+ * Size of the library's built-in scratch array used by
+ * fr_reduce_relu_add_sum_split_static (64 KiB = 8192 fp64 partial sums).
+ */
+#define FR_STATIC_SCRATCH_BYTES 65536
+
+/*
+ * The split form of fr_reduce_relu_add_sum without a caller workspace: same
+ * arguments minus form/workspace, same result bit for bit (the same kernels
+ * with the same segment count).  The pages have no counterpart of this call;
+ * it exists for callers that cannot allocate device memory where they launch
+ * -- code inside a host framework that owns every device allocation and
+ * forbids raw cudaMalloc in its operator callbacks, latency-critical paths
+ * where cudaMalloc/cudaFree may synchronise the device, and interfaces with no
+ * way to pass a workspace pointer.
+ *
+ * The stage-1 partial sums go to a fixed FR_STATIC_SCRATCH_BYTES array in the
+ * library's device memory (a static __device__ variable: every GPU that loads
+ * the library keeps it until the process exits).  No cudaMalloc, cudaFree or
+ * other allocating call is made.
+ *
+ *   Limit.     rows * segments partials must fit the array (8192 of them; on a
+ *              152-SM GB300 every shape with rows <= 8192 fits).  Larger shapes
+ *              return FR_ERR_WORKSPACE_TOO_SMALL and nothing is enqueued;
+ *              rows > 65535 return FR_ERR_UNSUPPORTED_FORM as for the split form.
+ *   First use. The first call on each device looks up the array's device
+ *              address (cudaGetSymbolAddress, with that device current) and
+ *              caches it; make that first call before any stream capture.
+ *   Sharing.   All calls on a device share the one array and it keeps the last
+ *              call's partials.  Stage 1 overwrites every partial it uses, so
+ *              nothing needs clearing, but calls that overlap on the GPU (on
+ *              different streams, or from several host threads without
+ *              ordering) race on the array: order them on one stream.
+ */
+fr_status fr_reduce_relu_add_sum_split_static(const void *a, const void *b, float *out,
+                                              int64_t rows, int64_t cols, int64_t lda,
+                                              int64_t ldb, fr_dtype dtype, float scale,
+                                              fr_stream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error
  * word.  Returns FR_OK when no device data error was recorded, otherwise
  * FR_ERR_DEVICE_DATA with the FR_DEVERR_* code in *code (if non-NULL).

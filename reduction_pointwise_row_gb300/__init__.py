@@ -54,6 +54,8 @@ SIGNATURES = {
     "fr_xent": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _int, _vp,
                        _sz, _vp]),
     "fr_check_device_error": (_int, [_vp, ctypes.POINTER(ctypes.c_int32)]),
+    "fr_reduce_relu_add_sum_split_static": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _int,
+                                                   _f32, _vp]),
 }
 
 
@@ -209,6 +211,24 @@ def fr_xent(logits, target, ignore_index: int = -100, want_loss: bool = True,
         if v is not None:
             res[k] = v
     return res
+
+
+def fr_reduce_relu_add_sum_split_static(a, b, scale: float = 2.0, out=None, stream=None):
+    """Split-form relu_add_sum with no workspace: the partial sums live in the
+    library's fixed 64 KiB device array, so nothing is allocated for the call
+    (for callers that cannot allocate device memory where they launch).  Calls
+    on one device share that array: keep them ordered on one stream."""
+    import torch
+    assert a.is_cuda and b.is_cuda and a.dtype == torch.float32 and b.dtype == torch.float32
+    assert a.shape == b.shape and a.dim() == 2
+    rows, cols = a.shape
+    if out is None:
+        out = torch.empty(rows, dtype=torch.float32, device=a.device)
+    _check(lib().fr_reduce_relu_add_sum_split_static(_ptr(a), _ptr(b), _ptr(out), rows, cols,
+                                                     _ld(a), _ld(b), DTYPES["f32"], scale,
+                                                     _stream(stream)),
+           "fr_reduce_relu_add_sum_split_static")
+    return out
 
 
 def fr_check_device_error(stream=None) -> int:
