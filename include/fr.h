@@ -74,6 +74,8 @@ typedef enum {
 /* Device error codes written by kernels (read by fr_check_device_error). */
 #define FR_DEVERR_NONE 0
 #define FR_DEVERR_BAD_TARGET 1 /* a target outside [0, cols) and != ignore_index */
+#define FR_DEVERR_TIMEOUT 2    /* an asynchronous copy did not complete within its
+                                  time budget; the kernel gave up and returned */
 
 /* Library version (major*10000 + minor*100 + patch). */
 int fr_version(void);

@@ -48,7 +48,22 @@ cudaError_t launch_softmax_looped(const float *x, float *y, int64_t rows, int64_
 
 // True when the persistent (register-resident) form can hold this row.
 bool layernorm_persistent_ok(int64_t cols, bool vec);
-bool layernorm_looped_ring_ok(int64_t cols, bool vec, int max_smem_optin);
+// The looped form with bulk-copy staging: 32-byte aligned rows and
+// gamma/beta, cols % 16 == 0, the row fits one CTA's shared memory.
+// The cluster form: rows split over a thread-block cluster, gamma/beta held
+// in registers; 16-byte aligned rows and gamma/beta, cols % 8 == 0 and at most
+// 32768 columns (8 CTAs x 512 threads x 8 columns).
+bool layernorm_cluster_ok(int64_t cols, bool aligned16);
+cudaError_t launch_layernorm_cluster(const uint16_t *x, const float *gamma, const float *beta,
+                                     uint16_t *y, float *mean, float *rstd, int64_t rows,
+                                     int64_t cols, int64_t ldx, int64_t ldy, float eps,
+                                     cudaStream_t s);
+bool layernorm_ring_ok(int64_t cols, bool vec, int max_smem_optin);
+size_t layernorm_ring_smem(int64_t cols, int nbuf);
+cudaError_t launch_layernorm_ring(const uint16_t *x, const float *gamma, const float *beta,
+                                  uint16_t *y, float *mean, float *rstd, int64_t rows,
+                                  int64_t cols, int64_t ldx, int64_t ldy, float eps, int sm_count,
+                                  int max_smem_optin, cudaStream_t s);
 cudaError_t launch_layernorm_persistent(const uint16_t *x, const float *gamma,
                                         const float *beta, uint16_t *y, float *mean,
                                         float *rstd, int64_t rows, int64_t cols, int64_t ldx,
@@ -66,6 +81,9 @@ cudaError_t launch_xent(const uint16_t *logits, const int64_t *target, float *lo
                         float *loss_mean, float *target_logit, int64_t *argmax, int64_t rows,
                         int64_t cols, int64_t ld, int64_t ignore_index, void *workspace,
                         int sm_count, cudaStream_t s);
+// Device address of the current device's error word (kernels record
+// FR_DEVERR_* codes there with atomicCAS; the first code wins).
+cudaError_t device_error_word(int **out);
 // Reads and clears the device error word of the current device (synchronises s).
 cudaError_t device_error_read_and_clear(cudaStream_t s, int *code);
 

@@ -158,34 +158,46 @@ def test_softmax_in_place_and_rows_sum_to_one(o):
 
 # ---------------------------------------------------------------- LayerNorm
 
-def run_layernorm(x_bits, gamma, beta, eps, form, offset=0):
+def run_layernorm(x_bits, gamma, beta, eps, form, offset=0, kernel=None):
+    """kernel pins the looped form's kernel (cluster, ring or scalar)."""
+    import os
+    if kernel:
+        os.environ["FR_LAYERNORM_KERNEL"] = kernel
+    else:
+        os.environ.pop("FR_LAYERNORM_KERNEL", None)
     rows, cols = x_bits.shape
     px = place(x_bits, offset)
     py = empty_like_placed(rows, cols, torch.bfloat16, offset)
     g, b = torch.from_numpy(gamma).cuda(), torch.from_numpy(beta).cuda()
     mean = torch.full((rows,), float("nan"), device="cuda")
     rstd = torch.full((rows,), float("nan"), device="cuda")
-    fr.fr_layernorm(px.t, g, b, eps, form=form, out=py.t, mean=mean, rstd=rstd)
+    try:
+        fr.fr_layernorm(px.t, g, b, eps, form=form, out=py.t, mean=mean, rstd=rstd)
+    finally:
+        os.environ.pop("FR_LAYERNORM_KERNEL", None)
     torch.cuda.synchronize()
     assert py.canaries_intact(), "layernorm wrote outside y"
     return bf16_to_f32_host(py.t), mean.cpu().numpy(), rstd.cpu().numpy()
 
 
-@pytest.mark.parametrize("cols", [1, 3, 16, 32, 48, 781, 1000, 1024, 4096, 4112, 32768, 65537])
-@pytest.mark.parametrize("rows", [1, 7, 33])
+@pytest.mark.parametrize("cols", [1, 3, 8, 16, 32, 48, 776, 781, 1000, 1024, 4096, 4112, 8200,
+                                  16384, 32768, 40000, 65537, 106496])
+@pytest.mark.parametrize("rows", [1, 7, 33, 301])
 @pytest.mark.parametrize("offset", [0, 1])
 def test_layernorm_forms(o, rows, cols, offset):
     w = workloads.make(2, rows=rows, cols=cols, seed=3000 + rows * 7 + cols)
     eps = float(np.float32(w.params["eps"]))
     ry, rm, rr = o.layernorm(w.arrays["x"], w.arrays["gamma"], w.arrays["beta"], eps)
     vec_ok = offset == 0 and cols % 16 == 0 and cols <= 32768
-    forms = (["persistent"] if vec_ok else []) + ["looped"]
-    for form in forms:
+    runs = ([("persistent", None)] if vec_ok else []) + \
+        [("looped", k) for k in ("cluster", "ring", "scalar")]
+    for form, kernel in runs:
         y, m, r = run_layernorm(w.arrays["x"], w.arrays["gamma"], w.arrays["beta"], eps, form,
-                                offset)
-        assert_close(y, ry, "bf16", f"{form} y {rows}x{cols}")
-        assert_close(m, rm, "mean", f"{form} mean")
-        assert_close(r, rr, "f32", f"{form} rstd")
+                                offset, kernel)
+        what = f"{form}/{kernel} {rows}x{cols} offset {offset}"
+        assert_close(y, ry, "bf16", f"{what} y")
+        assert_close(m, rm, "mean", f"{what} mean")
+        assert_close(r, rr, "f32", f"{what} rstd")
     if not vec_ok:
         with pytest.raises(fr.FRError) as e:
             run_layernorm(w.arrays["x"], w.arrays["gamma"], w.arrays["beta"], eps, "persistent",
@@ -200,11 +212,12 @@ def test_layernorm_constant_rows(o):
     beta = np.linspace(-1, 1, cols).astype(np.float32)
     eps = float(np.float32(1e-5))
     ry, rm, rr = o.layernorm(x, gamma, beta, eps)
-    for form in ("persistent", "looped"):
-        y, m, r = run_layernorm(x, gamma, beta, eps, form)
-        assert_close(y, ry, "bf16", form)
+    for form, kernel in (("persistent", None), ("looped", "cluster"), ("looped", "ring"),
+                         ("looped", "scalar")):
+        y, m, r = run_layernorm(x, gamma, beta, eps, form, kernel=kernel)
+        assert_close(y, ry, "bf16", f"{form}/{kernel}")
         assert (m == 3.5).all()
-        assert_close(r, rr, "f32", form)
+        assert_close(r, rr, "f32", f"{form}/{kernel}")
 
 
 # ---------------------------------------------------------------- cross entropy
