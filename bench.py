@@ -48,6 +48,8 @@ def parse():
     p.add_argument("--no-extra", action="store_true", help="headline workload only")
     p.add_argument("--only", choices=["relu_add_sum", "softmax", "layernorm", "split", "xent"],
                    help="time one workload alone (for profiler captures) and exit")
+    p.add_argument("--form", default="auto", choices=["auto", "persistent", "looped", "split"],
+                   help="with --only: force a reduction form")
     return p.parse_args()
 
 
@@ -211,7 +213,8 @@ def run_ours(args):
         return max_over_ranks(statistics.fmean(ms) / 1e3), launches_per_call * steps, ms
 
     if args.only:
-        res = extra_configs(fr, traffic, workloads, timed, dev, peak, args, world, [args.only])
+        res = extra_configs(fr, traffic, workloads, timed, dev, peak, args, world, [args.only],
+                            args.form)
         if rank == 0:
             print(json.dumps({"only": args.only, **next(iter(res.values()))}), flush=True)
         return
@@ -296,7 +299,7 @@ def run_ours(args):
 ROTATE_BYTES = 1 << 30  # footprint of the rotating input/output sets (8x the L2)
 
 
-def setup_workload(name, fr, workloads, dev):
+def setup_workload(name, fr, workloads, dev, form="auto"):
     """Device inputs and calls of one workload: (calls, op, rows, cols,
     launches per call).  ``calls`` cycles over enough copies of the inputs
     and outputs that their footprint is >= 1 GiB, so no launch finds its
@@ -312,14 +315,14 @@ def setup_workload(name, fr, workloads, dev):
         w = workloads.make(0)
         a, b = to_device(w.arrays["a"], dev), to_device(w.arrays["b"], dev)
         out = torch.empty(w.rows, device=dev)
-        calls.append(lambda: fr.fr_reduce_relu_add_sum(a, b, 2.0, out=out))
+        calls.append(lambda: fr.fr_reduce_relu_add_sum(a, b, 2.0, out=out, form=form))
         return calls, "relu_add_sum", w.rows, w.cols, 1
     if name == "softmax":
         w = workloads.make(1)
         for _ in range(nsets("softmax", w.rows, w.cols)):
             x = to_device(w.arrays["x"], dev)
             y = torch.empty_like(x)
-            calls.append(lambda x=x, y=y: fr.fr_softmax(x, out=y))
+            calls.append(lambda x=x, y=y: fr.fr_softmax(x, out=y, form=form))
         return calls, "softmax", w.rows, w.cols, 1
     if name == "layernorm":
         w = workloads.make(2)
@@ -330,7 +333,8 @@ def setup_workload(name, fr, workloads, dev):
             mean = torch.empty(w.rows, device=dev)
             rstd = torch.empty(w.rows, device=dev)
             calls.append(lambda x=x, y=y, mean=mean, rstd=rstd:
-                         fr.fr_layernorm(x, g, bt, 1e-5, out=y, mean=mean, rstd=rstd))
+                         fr.fr_layernorm(x, g, bt, 1e-5, out=y, mean=mean, rstd=rstd,
+                                         form=form))
         return calls, "layernorm", w.rows, w.cols, 1
     if name == "split":
         w = workloads.make(3)
@@ -338,10 +342,11 @@ def setup_workload(name, fr, workloads, dev):
         for _ in range(nsets("relu_add_sum", rows, cols)):
             a, b = to_device(w.arrays["a"], dev), to_device(w.arrays["b"], dev)
             out = torch.empty(rows, device=dev)
-            ws = torch.empty(fr.fr_workspace_size("relu_add_sum", rows, cols), dtype=torch.uint8,
-                             device=dev)
+            f = "split" if form == "auto" else form
+            ws = torch.empty(max(16, fr.fr_workspace_size("relu_add_sum", rows, cols, "f32", f)),
+                             dtype=torch.uint8, device=dev)
             calls.append(lambda a=a, b=b, out=out, ws=ws:
-                         fr.fr_reduce_relu_add_sum(a, b, 2.0, out=out, workspace=ws))
+                         fr.fr_reduce_relu_add_sum(a, b, 2.0, out=out, workspace=ws, form=form))
         return calls, "relu_add_sum", rows, cols, 2
     if name == "xent":
         w = workloads.make(4)
@@ -360,11 +365,12 @@ EXTRA = {"relu_add_sum": "relu_add_sum_64x128", "layernorm": "layernorm_4096x327
          "split": "relu_add_sum_split_8x33554432", "xent": "xent_8192x50257"}
 
 
-def extra_configs(fr, traffic, workloads, timed, dev, peak, args, world, names=None):
+def extra_configs(fr, traffic, workloads, timed, dev, peak, args, world, names=None,
+                  form="auto"):
     steps = max(3, min(args.steps, 50))
     res = {}
     for name in (names or EXTRA):
-        calls, op, rows, cols, lpc = setup_workload(name, fr, workloads, dev)
+        calls, op, rows, cols, lpc = setup_workload(name, fr, workloads, dev, form)
         calls[0]()
         t, n, _ = timed(calls, steps, args.warmup, lpc)
         nb = traffic.algorithmic_bytes(op, rows, cols)

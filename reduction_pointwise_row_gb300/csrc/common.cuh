@@ -258,6 +258,21 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
       : "memory");
 }
 
+// Per-thread asynchronous 16-byte global -> shared copy (no registers; the
+// L1 is bypassed).  Copies are grouped with commit and waited for with
+// wait_group<N>: at most N of the thread's most recent groups still pending.
+__device__ __forceinline__ void cp_async_16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // 32 bytes from shared memory (two 16-byte loads).
 __device__ __forceinline__ V8 lds_v8(const void *p) {
   V8 v;

@@ -96,9 +96,11 @@ fr_form pick_softmax(int64_t, int64_t cols, bool vec) {
   return cols <= fr::softmax_persistent_max_cols(vec) ? FR_FORM_PERSISTENT : FR_FORM_LOOPED;
 }
 
-fr_form pick_layernorm(int64_t, int64_t cols, bool vec, int) {
-  // Measured on GB300, bf16 [4096, 32768]: persistent 193 us, looped staged
-  // ring 256 us, looped scalar 265 us, looped cluster 345 us.
+fr_form pick_layernorm(int64_t, int64_t cols, bool vec, int max_smem_optin) {
+  // Measured on GB300, bf16 [4096, 32768]: looped cp.async ring (two rows per
+  // gamma/beta pass) 156 us, persistent 193 us, looped cluster (gamma/beta in
+  // shared memory) 214 us, looped scalar 265 us.
+  if (fr::layernorm_ring_ok(cols, vec, max_smem_optin)) return FR_FORM_LOOPED;
   return fr::layernorm_persistent_ok(cols, vec) ? FR_FORM_PERSISTENT : FR_FORM_LOOPED;
 }
 
@@ -213,8 +215,8 @@ fr_status fr_layernorm(const void *x, const float *gamma, const float *beta, voi
   if (fr_status st = device_ok(&info)) return st;
   const bool vec = aligned(x, 32) && aligned(y, 32) && aligned(gamma, 32) && aligned(beta, 32) &&
                    ldx % 16 == 0 && ldy % 16 == 0 && cols % 16 == 0;
-  const bool aligned16 = aligned(x, 16) && aligned(y, 16) && aligned(gamma, 16) &&
-                         aligned(beta, 16) && ldx % 8 == 0 && ldy % 8 == 0;
+  const bool aligned16 = aligned(x, 32) && aligned(y, 32) && aligned(gamma, 16) &&
+                         aligned(beta, 16) && ldx % 16 == 0 && ldy % 16 == 0;
   const fr_form f = form == FR_FORM_AUTO ? pick_layernorm(rows, cols, vec, info.max_smem_optin) : form;
   const uint16_t *bx = static_cast<const uint16_t *>(x);
   uint16_t *by = static_cast<uint16_t *>(y);

@@ -51,9 +51,10 @@ bool layernorm_persistent_ok(int64_t cols, bool vec);
 // The looped form with bulk-copy staging: 32-byte aligned rows and
 // gamma/beta, cols % 16 == 0, the row fits one CTA's shared memory.
 // The cluster form: rows split over a thread-block cluster, gamma/beta held
-// in registers; 16-byte aligned rows and gamma/beta, cols % 8 == 0 and at most
-// 32768 columns (8 CTAs x 512 threads x 8 columns).
-bool layernorm_cluster_ok(int64_t cols, bool aligned16);
+// in registers; 32-byte aligned rows, 16-byte aligned gamma/beta,
+// cols % (16 * cluster) == 0 and at most 32768 columns (8 CTAs x 256 threads
+// x 16 columns).
+bool layernorm_cluster_ok(int64_t cols, bool aligned);
 cudaError_t launch_layernorm_cluster(const uint16_t *x, const float *gamma, const float *beta,
                                      uint16_t *y, float *mean, float *rstd, int64_t rows,
                                      int64_t cols, int64_t ldx, int64_t ldy, float eps,

@@ -16,6 +16,8 @@
 // looped      one CTA per row, grid-stride over rows: pass 1 streams the row
 //             in chunks merging Welford triples, pass 2 streams it again
 //             (from L2) to write y.  Any alignment (scalar lane-strided).
+#include <cstdlib>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -175,354 +177,304 @@ layernorm_looped_scalar(const uint16_t *__restrict__ x, const float *__restrict_
   }
 }
 
-// ---- looped form with bulk-copy staging ------------------------------------
-// A persistent CTA per SM owns rows blockIdx.x + k * gridDim.x and keeps NB
-// row buffers in shared memory.  Row k is copied into buffer k % NB as
-// kRingChunk-byte bulk copies, each completing on its own mbarrier; pass 1
-// merges Welford triples of each chunk as it lands, pass 2 normalises from
-// shared memory and streams y out, then buffer k % NB is refilled with row
-// k + NB.  So NB - 1 rows are always in flight while one row is computed.
-constexpr int kRingThreads = 1024;
-constexpr int kRingChunk = 16384;     // bytes per bulk copy
-constexpr int kRingMaxChunks = 13;    // rows of up to 208 KiB (106496 bf16)
-constexpr int kRingMaxBuffers = 4;
-constexpr int kRingHeader = 512;      // mbarriers (NB x chunks), then the buffers
-constexpr long long kWaitBudget = 1LL << 31;  // SM clocks (about one second)
+// ---- looped form with asynchronous-copy staging -----------------------------
+// A persistent CTA per SM owns rows blockIdx.x + k * gridDim.x, stages them in
+// a ring of kRingBufs shared-memory row buffers (row k in buffer k % kRingBufs)
+// and works on R rows at a time.  Every thread copies its own 32-byte pieces
+// of a row with cp.async (16 bytes per copy, one commit group per row) and
+// later reads back exactly those pieces, so staging needs no barrier of its
+// own.  Pass 1 lifts the R rows' pieces into registers (Welford triples per 16
+// elements) and immediately refills their buffers with the next rows, so
+// kRingBufs rows are always in flight; after one CTA merge of the R triples,
+// pass 2 normalises all R rows from registers with one load of each
+// gamma/beta value -- the fp32 gamma/beta re-reads, four times the bytes of
+// x, are what limit a one-row-at-a-time LayerNorm.
+constexpr int kRingThreads = 512;
+constexpr int kRingBufs = 3;
+constexpr int kRingPieces = 4;    // 32-byte pieces per thread per row: rows of
+                                  // at most 512 * 4 * 16 = 32768 bf16
 
+// CTA-wide merge of R triples at once (one pair of barriers for all R).
+template <int R>
+__device__ __forceinline__ void block_welford_n(Welford (&w)[R], Welford (*smem)[32]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = (blockDim.x + 31) >> 5;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    w[r] = warp_welford(w[r]);
+    if (lane == 0) smem[r][warp] = w[r];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    Welford t = lane < nw ? smem[r][lane] : Welford{0.0f, 0.0f, 0.0f};
+    w[r] = warp_welford(t);
+  }
+  __syncthreads();
+}
+
+template <int R>
 __global__ void __launch_bounds__(kRingThreads, 1)
 layernorm_ring(const uint16_t *__restrict__ x, const float *__restrict__ gamma,
                const float *__restrict__ beta, uint16_t *__restrict__ y,
                float *__restrict__ mean_out, float *__restrict__ rstd_out, int64_t rows,
-               int64_t cols, int64_t ldx, int64_t ldy, float eps, int nbuf,
-               int *__restrict__ err) {
+               int64_t cols, int64_t ldx, int64_t ldy, float eps) {
   extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem);  // [nbuf][nch]
-  __shared__ Welford red[32];
-  __shared__ int timed_out;
+  __shared__ Welford red[R][32];
   const int tid = threadIdx.x;
-  const int64_t row_bytes = cols * 2;
-  const size_t buf_bytes = static_cast<size_t>((row_bytes + 127) / 128 * 128);
-  const int nch = static_cast<int>((row_bytes + kRingChunk - 1) / kRingChunk);
-  const int npieces = static_cast<int>(cols >> 4);  // 32-byte pieces (cols % 16 == 0)
-  constexpr int kPiecesPerChunk = kRingChunk / 32;
-  const uint64_t policy = l2_evict_first_policy();
-  auto buffer = [&](int b) { return smem + kRingHeader + static_cast<size_t>(b) * buf_bytes; };
+  const int npieces = static_cast<int>(cols >> 4);  // cols % 16 == 0
+  const size_t buf_bytes = static_cast<size_t>(npieces) * 32;
+  const int64_t G = gridDim.x;
+  // rows of this CTA: blockIdx.x + k * G for k < nk
+  const int64_t nk = blockIdx.x < rows ? (rows - blockIdx.x + G - 1) / G : 0;
 
-  auto issue = [&](int64_t row, int b) {  // thread 0 only
-    const unsigned char *src = reinterpret_cast<const unsigned char *>(x + row * ldx);
-    unsigned char *dst = buffer(b);
-    for (int c = 0; c < nch; ++c) {
-      const int64_t off = static_cast<int64_t>(c) * kRingChunk;
-      const uint32_t bytes =
-          static_cast<uint32_t>(row_bytes - off < kRingChunk ? row_bytes - off : kRingChunk);
-      mbar_arrive_expect_tx(&full[b * nch + c], bytes);
-      bulk_copy_g2s(dst + off, src + off, bytes, &full[b * nch + c], policy);
+  auto stage = [&](int64_t k) {  // this thread's pieces of row k into buffer k % kRingBufs
+    if (k < nk) {
+      const unsigned char *src = reinterpret_cast<const unsigned char *>(x + (blockIdx.x + k * G) * ldx);
+      unsigned char *dst = smem + static_cast<size_t>(k % kRingBufs) * buf_bytes;
+#pragma unroll
+      for (int j = 0; j < kRingPieces; ++j) {
+        const int p = tid + j * kRingThreads;
+        if (p < npieces) {
+          cp_async_16(dst + static_cast<size_t>(p) * 32, src + static_cast<size_t>(p) * 32);
+          cp_async_16(dst + static_cast<size_t>(p) * 32 + 16, src + static_cast<size_t>(p) * 32 + 16);
+        }
+      }
     }
+    cp_async_commit();  // one group per row index, empty past the last row
   };
 
-  if (tid == 0) {
-    timed_out = 0;
-    for (int i = 0; i < nbuf * nch; ++i) mbar_init(&full[i], 1);
-    mbar_init_fence();
-  }
-  __syncthreads();
-  if (tid == 0)
-    for (int b = 0; b < nbuf; ++b) {
-      const int64_t r = blockIdx.x + static_cast<int64_t>(b) * gridDim.x;
-      if (r < rows) issue(r, b);
-    }
-  int64_t k = 0;
-  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, ++k) {
-    const int b = static_cast<int>(k % nbuf);
-    const uint32_t parity = static_cast<uint32_t>((k / nbuf) & 1);
-    const unsigned char *buf = buffer(b);
-    // pass 1: Welford over 16-element pieces, chunk by chunk as copies land
-    Welford w{0.0f, 0.0f, 0.0f};
-    for (int c = 0; c < nch; ++c) {
-      if (!timed_out && !mbar_wait_bounded(&full[b * nch + c], parity, kWaitBudget)) {
-        timed_out = 1;  // benign race: every writer stores 1
-        atomicCAS(err, 0, FR_DEVERR_TIMEOUT);
+  for (int b = 0; b < kRingBufs; ++b) stage(b);
+  int64_t next = kRingBufs;  // next row index to stage
+  for (int64_t k0 = 0; k0 < nk; k0 += R) {
+    V8 v[R][kRingPieces];
+    Welford w[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      // Groups committed so far: rows 0 .. next - 1 = k0 + r + kRingBufs - 1.
+      // Row k0 + r has landed once at most the kRingBufs - 1 newer ones pend.
+      cp_async_wait<kRingBufs - 1>();
+      w[r] = Welford{0.0f, 0.0f, 0.0f};
+      const unsigned char *buf = smem + static_cast<size_t>((k0 + r) % kRingBufs) * buf_bytes;
+#pragma unroll
+      for (int j = 0; j < kRingPieces; ++j) {
+        const int p = tid + j * kRingThreads;
+        if (k0 + r < nk && p < npieces) {
+          v[r][j] = lds_v8(buf + static_cast<size_t>(p) * 32);
+          w[r] = chan_merge(w[r], welford16(v[r][j]));
+        }
       }
-      const int p_end = (c + 1) * kPiecesPerChunk < npieces ? (c + 1) * kPiecesPerChunk : npieces;
-      for (int p = c * kPiecesPerChunk + tid; p < p_end; p += kRingThreads)
-        w = chan_merge(w, welford16(lds_v8(buf + static_cast<size_t>(p) * 32)));
+      stage(next++);  // buffer of row k0 + r is in registers: refill it
     }
-    const Welford r = block_welford(w, red);
-    const float mean = r.mean;
-    const float rstd = rsqrtf(fmaf(r.m2, __frcp_rn(r.n), eps));
-    if (tid == 0) {
-      if (mean_out) mean_out[row] = mean;
-      if (rstd_out) rstd_out[row] = rstd;
+    block_welford_n<R>(w, red);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int64_t row = blockIdx.x + (k0 + r) * G;
+      if (k0 + r < nk && tid == 0) {
+        if (mean_out) mean_out[row] = w[r].mean;
+        if (rstd_out) rstd_out[row] = rsqrtf(fmaf(w[r].m2, __frcp_rn(w[r].n), eps));
+      }
     }
-    // pass 2: y = (x - mean) * rstd * gamma + beta from the staged row
-    uint16_t *py = y + row * ldy;
-    for (int p = tid; p < npieces; p += kRingThreads) {
-      V8 v = lds_v8(buf + static_cast<size_t>(p) * 32);
+    float mean[R], rstd[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      mean[r] = w[r].mean;
+      rstd[r] = rsqrtf(fmaf(w[r].m2, __frcp_rn(w[r].n), eps));
+    }
+#pragma unroll
+    for (int j = 0; j < kRingPieces; ++j) {
+      const int p = tid + j * kRingThreads;
+      if (p >= npieces) continue;
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         const float4 g = ld_keep_f4(gamma + p * 16 + 4 * h);
         const float4 bb = ld_keep_f4(beta + p * 16 + 4 * h);
-        const uint32_t w0 = v.w[2 * h], w1 = v.w[2 * h + 1];
-        v.w[2 * h] = pack_bf16x2(fmaf((bf16_lo(w0) - mean) * rstd, g.x, bb.x),
-                                 fmaf((bf16_hi(w0) - mean) * rstd, g.y, bb.y));
-        v.w[2 * h + 1] = pack_bf16x2(fmaf((bf16_lo(w1) - mean) * rstd, g.z, bb.z),
-                                     fmaf((bf16_hi(w1) - mean) * rstd, g.w, bb.w));
-      }
-      st_stream_v8(py + static_cast<int64_t>(p) * 16, v);
-    }
-    __syncthreads();  // the whole CTA is done reading buffer b
-    if (timed_out) {
-      // Give every copy still in flight a last bounded wait, then stop.
-      if (tid == 0)
-        for (int j = 0; j < nbuf; ++j) {
-          const int64_t kj = k + j;
-          const int64_t rj = blockIdx.x + kj * gridDim.x;
-          if (rj >= rows) break;
-          const int bj = static_cast<int>(kj % nbuf);
-          const uint32_t pj = static_cast<uint32_t>((kj / nbuf) & 1);
-          for (int c = 0; c < nch; ++c) mbar_wait_bounded(&full[bj * nch + c], pj, kWaitBudget);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const uint32_t w0 = v[r][j].w[2 * h], w1 = v[r][j].w[2 * h + 1];
+          v[r][j].w[2 * h] = pack_bf16x2(fmaf((bf16_lo(w0) - mean[r]) * rstd[r], g.x, bb.x),
+                                         fmaf((bf16_hi(w0) - mean[r]) * rstd[r], g.y, bb.y));
+          v[r][j].w[2 * h + 1] = pack_bf16x2(fmaf((bf16_lo(w1) - mean[r]) * rstd[r], g.z, bb.z),
+                                             fmaf((bf16_hi(w1) - mean[r]) * rstd[r], g.w, bb.w));
         }
-      return;
-    }
-    const int64_t next = row + static_cast<int64_t>(nbuf) * gridDim.x;
-    if (tid == 0 && next < rows) {
-      fence_proxy_async_smem();
-      issue(next, b);
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        if (k0 + r < nk)
+          st_stream_v8(y + (blockIdx.x + (k0 + r) * G) * ldy + static_cast<int64_t>(p) * 16,
+                       v[r][j]);
     }
   }
+  cp_async_wait<0>();  // no copy may still target this CTA's shared memory
 }
 
-// ---- cluster form: row slices across CTAs, gamma/beta in registers ---------
-// A cluster of C CTAs splits every row into C column slices of S = cols / C;
-// thread t of CTA rank q owns columns q*S + 8t .. q*S + 8t + 7 for the whole
-// kernel, so its 8 gamma and 8 beta values are loaded once into registers and
-// the only per-row traffic is x in and y out.  Each CTA streams its slices of
-// kClRows rows at a time through a kClStages-deep ring of bulk copies.  Per
-// row group: Welford triples of 8 elements per thread -> warp -> CTA; warp 0
-// then pushes the CTA's triple of each row into every CTA of the cluster
-// (st.async into the peer's shared memory, counted on the peer's mbarrier).
-// Each CTA waits on its own barrier, merges the C triples in rank order (the
-// same bits in every CTA) and normalises the x it still holds in registers.
-// The merge of group g - 1 follows the publication of group g, so the
-// exchange latency overlaps the next group's work.
-constexpr int kClThreads = 512;
-constexpr int kClRows = 2;     // rows per group
-constexpr int kClStages = 4;   // groups in the bulk-copy ring
-constexpr int kClSlots = 4;    // partial slots: a peer can write group g + 4 only
-                               // after this CTA published g + 2, i.e. after it
-                               // finished reading group g
-constexpr int kClMaxCluster = 8;
+constexpr long long kWaitBudget = 1LL << 31;  // SM clocks (about one second) per wait
 
-__device__ __forceinline__ Welford welford8(uint4 v) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  float s = 0.0f;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) s += bf16_lo(w[j]) + bf16_hi(w[j]);
-  const float mean = s * 0.125f;
-  float q = 0.0f;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float a = bf16_lo(w[j]) - mean, b = bf16_hi(w[j]) - mean;
-    q = fmaf(a, a, q);
-    q = fmaf(b, b, q);
-  }
-  return Welford{8.0f, mean, q};
-}
+// ---- cluster form: gamma/beta resident in shared memory -----------------------
+// A cluster of C CTAs (C = 1 or 2) splits every row into C column slices of
+// S = cols / C <= 16384.  Each CTA keeps the gamma/beta of its slice in shared
+// memory for the whole kernel (S * 8 <= 128 KiB) and streams x through a ring
+// of kClBufs slice buffers filled with per-thread cp.async copies, kClBufs rows
+// (a wave) at a time: pass 1 lifts the wave's x into registers (thread t owns
+// the 16 columns 16t .. 16t + 15 of the slice) and refills the ring at once;
+// one CTA merge reduces the wave's Welford triples; warp 0 pushes them into
+// every CTA of the cluster (st.async, counted on the receiver's mbarrier); each
+// CTA merges the C triples of a row in rank order (the same bits everywhere)
+// and normalises the wave from registers, reading each gamma/beta value from
+// shared memory once per wave.  HBM sees x once and y once; gamma/beta are
+// read from HBM once per CTA.
+constexpr int kClThreads = 1024;
+constexpr int kClBufs = 3;        // rows per wave = slice buffers in the ring
+constexpr int kClSlots = 4;       // published triples: wave w + 4 is written
+                                  // only after this CTA published wave w + 1
+constexpr int kClMaxCluster = 2;
+constexpr int64_t kClMaxSlice = 16 * kClThreads;  // 16384 columns
 
-__global__ void __launch_bounds__(kClThreads, 2)
+__global__ void __launch_bounds__(kClThreads, 1)
 layernorm_cluster(const uint16_t *__restrict__ x, const float *__restrict__ gamma,
                   const float *__restrict__ beta, uint16_t *__restrict__ y,
                   float *__restrict__ mean_out, float *__restrict__ rstd_out, int64_t rows,
                   int64_t cols, int64_t ldx, int64_t ldy, float eps, int *__restrict__ err) {
   extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem);  // [kClStages] bulk-copy barriers
-  uint64_t *pbar = full + kClStages;                    // [kClSlots] partial barriers
-  unsigned char *stages = smem + 128;
-  // slot[s][j][k]: rank k's triple of row j of the group using slot s
-  __shared__ __align__(16) float4 slot[kClSlots][kClRows][kClMaxCluster];
-  __shared__ Welford red[2][kClRows][kClThreads / 32];
+  __shared__ __align__(16) float4 slot[kClSlots][kClBufs][kClMaxCluster];  // [wave%4][row][rank]
+  __shared__ __align__(8) uint64_t pbar[kClSlots];
+  __shared__ Welford red[kClBufs][32];
   __shared__ int timed_out;
 
   const uint32_t C = cluster_nctarank(), q = cluster_ctarank();
   const int64_t cid = cluster_id_x(), ncl = ncluster_x();
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t S = cols / C;  // columns of this CTA's slice
-  const uint32_t slice_bytes = static_cast<uint32_t>(S * 2);
-  const bool own = 8 * static_cast<int64_t>(tid) < S;
-  const int64_t col0 = static_cast<int64_t>(q) * S + 8 * tid;
-  const int64_t nrows_c = cid < rows ? (rows - cid + ncl - 1) / ncl : 0;
-  const int64_t ngroups = (nrows_c + kClRows - 1) / kClRows;
-  const uint32_t part_bytes = 16u * kClRows * C;  // triples arriving per group
-  const uint64_t policy = l2_evict_first_policy();
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t S = cols / C;
+  const int npieces = static_cast<int>(S >> 4);        // 16 columns per piece, <= 1024
+  const bool own = tid < npieces;
+  const int64_t c0 = static_cast<int64_t>(q) * S;       // first column of the slice
+  const int64_t col0 = c0 + 16 * static_cast<int64_t>(tid);
+  float *sg = reinterpret_cast<float *>(smem);          // gamma[S], beta[S]
+  float *sb = sg + S;
+  unsigned char *ring = smem + static_cast<size_t>(S) * 8;
+  const size_t buf_bytes = static_cast<size_t>(S) * 2;
+  const int64_t nr = cid < rows ? (rows - cid + ncl - 1) / ncl : 0;  // rows of this cluster
+  const int64_t nwaves = (nr + kClBufs - 1) / kClBufs;
+  const uint32_t part_bytes = 16u * kClBufs * C;
 
-  float g8[8], b8[8];
-  if (own) {
-    const float4 g0 = ld_keep_f4(gamma + col0), g1 = ld_keep_f4(gamma + col0 + 4);
-    const float4 b0 = ld_keep_f4(beta + col0), b1 = ld_keep_f4(beta + col0 + 4);
-    g8[0] = g0.x; g8[1] = g0.y; g8[2] = g0.z; g8[3] = g0.w;
-    g8[4] = g1.x; g8[5] = g1.y; g8[6] = g1.z; g8[7] = g1.w;
-    b8[0] = b0.x; b8[1] = b0.y; b8[2] = b0.z; b8[3] = b0.w;
-    b8[4] = b1.x; b8[5] = b1.y; b8[6] = b1.z; b8[7] = b1.w;
+  // gamma/beta of the slice into shared memory (once)
+  for (int64_t i = tid; i < S / 4; i += kClThreads) {
+    reinterpret_cast<float4 *>(sg)[i] = ld_keep_f4(gamma + c0 + 4 * i);
+    reinterpret_cast<float4 *>(sb)[i] = ld_keep_f4(beta + c0 + 4 * i);
   }
-  auto row_of = [&](int64_t gi, int j) { return cid + (gi * kClRows + j) * ncl; };
-  auto issue = [&](int64_t gi) {  // thread 0: group gi into stage gi % kClStages
-    const int st = static_cast<int>(gi % kClStages);
-    int nvalid = 0;
-    for (int j = 0; j < kClRows; ++j) nvalid += row_of(gi, j) < rows;
-    mbar_arrive_expect_tx(&full[st], nvalid * slice_bytes);
-    for (int j = 0; j < kClRows; ++j) {
-      const int64_t r = row_of(gi, j);
-      if (r < rows)
-        bulk_copy_g2s(stages + (static_cast<size_t>(st) * kClRows + j) * slice_bytes,
-                      x + r * ldx + static_cast<int64_t>(q) * S, slice_bytes, &full[st], policy);
+  auto stage = [&](int64_t k) {  // row k of this cluster into buffer k % kClBufs
+    if (k < nr && own) {
+      const unsigned char *src =
+          reinterpret_cast<const unsigned char *>(x + (cid + k * ncl) * ldx + col0);
+      unsigned char *dst = ring + static_cast<size_t>(k % kClBufs) * buf_bytes + 32 * tid;
+      cp_async_16(dst, src);
+      cp_async_16(dst + 16, src + 16);
     }
+    cp_async_commit();
   };
-
   if (tid == 0) {
     timed_out = 0;
-    for (int i = 0; i < kClStages; ++i) mbar_init(&full[i], 1);
     for (int i = 0; i < kClSlots; ++i) mbar_init(&pbar[i], 1);
     mbar_init_fence();
-    // arm the partial barriers of the first groups (peers may send at once
-    // after the cluster barrier below)
-    for (int64_t gi = 0; gi < kClSlots && gi < ngroups; ++gi)
-      mbar_arrive_expect_tx(&pbar[gi], part_bytes);
-    for (int64_t gi = 0; gi < kClStages && gi < ngroups; ++gi) issue(gi);
+    for (int64_t w = 0; w < kClSlots && w < nwaves; ++w) mbar_arrive_expect_tx(&pbar[w], part_bytes);
   }
-  // every CTA's barriers are initialised and armed before anyone sends
+  for (int b = 0; b < kClBufs; ++b) stage(b);
+  // gamma/beta and the barriers are ready in every CTA before anyone sends
+  __syncthreads();
   cluster_arrive();
   cluster_wait();
 
-  uint4 xprev[kClRows], xcur[kClRows];
-  for (int64_t gi = 0; gi <= ngroups; ++gi) {
-    if (gi < ngroups) {
-      const int st = static_cast<int>(gi % kClStages);
-      const uint32_t parity = static_cast<uint32_t>((gi / kClStages) & 1);
-      if (!timed_out && !mbar_wait_bounded(&full[st], parity, kWaitBudget)) {
-        timed_out = 1;
-        atomicCAS(err, 0, FR_DEVERR_TIMEOUT);
-      }
-      Welford w[kClRows];
+  int64_t next = kClBufs;
+  for (int64_t wv = 0; wv < nwaves; ++wv) {
+    const int64_t k0 = wv * kClBufs;
+    V8 v[kClBufs];
+    Welford w[kClBufs];
 #pragma unroll
-      for (int j = 0; j < kClRows; ++j) {
-        w[j] = Welford{0.0f, 0.0f, 0.0f};
-        xcur[j] = make_uint4(0, 0, 0, 0);
-        if (own && row_of(gi, j) < rows) {
-          xcur[j] = lds_u4(stages + (static_cast<size_t>(st) * kClRows + j) * slice_bytes +
-                           16 * static_cast<size_t>(tid));
-          w[j] = welford8(xcur[j]);
-        }
-        w[j] = warp_welford(w[j]);
-        if (lane == 0) red[gi & 1][j][warp] = w[j];
+    for (int r = 0; r < kClBufs; ++r) {
+      cp_async_wait<kClBufs - 1>();  // row k0 + r landed (the newer rows may pend)
+      w[r] = Welford{0.0f, 0.0f, 0.0f};
+      if (own && k0 + r < nr) {
+        v[r] = lds_v8(ring + static_cast<size_t>((k0 + r) % kClBufs) * buf_bytes + 32 * tid);
+        w[r] = welford16(v[r]);
       }
-      __syncthreads();  // every thread has read stage st; red[gi & 1] complete
-      if (tid == 0 && gi + kClStages < ngroups) {
-        fence_proxy_async_smem();
-        issue(gi + kClStages);
-      }
-      if (warp == 0) {
-        // CTA triple of every row, then lane (j * C + k) sends row j's triple
-        // to rank k.
-        float4 mine = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      stage(next++);  // the row is in registers: refill its buffer
+    }
+    block_welford_n<kClBufs>(w, red);  // w[r] = this CTA's triple of row k0 + r
+    const int sl = static_cast<int>(wv % kClSlots);
+    if (tid < kClBufs * static_cast<int>(C)) {  // lanes of warp 0: (row, destination rank)
+      const int r = tid / static_cast<int>(C), k = tid % static_cast<int>(C);
+      Welford m = w[0];
+      if (r == 1) m = w[1];
+      if (r == 2) m = w[2];
+      st_async_f4(&slot[sl][r][q], &pbar[sl], static_cast<uint32_t>(k),
+                  make_float4(m.n, m.mean, m.m2, 0.0f));
+    }
+    if (!timed_out &&
+        !mbar_wait_bounded(&pbar[sl], static_cast<uint32_t>((wv / kClSlots) & 1), 1LL << 31)) {
+      timed_out = 1;
+      atomicCAS(err, 0, FR_DEVERR_TIMEOUT);
+    }
+    float mean[kClBufs], rstd[kClBufs];
 #pragma unroll
-        for (int j = 0; j < kClRows; ++j) {
-          Welford r = lane < kClThreads / 32 ? red[gi & 1][j][lane] : Welford{0.0f, 0.0f, 0.0f};
-          r = warp_welford(r);
-          if (lane / static_cast<int>(C) == j) mine = make_float4(r.n, r.mean, r.m2, 0.0f);
-        }
-        if (lane < kClRows * static_cast<int>(C)) {
-          const int j = lane / static_cast<int>(C), k = lane % static_cast<int>(C);
-          const int sl = static_cast<int>(gi % kClSlots);
-          st_async_f4(&slot[sl][j][q], &pbar[sl], static_cast<uint32_t>(k), mine);
-        }
+    for (int r = 0; r < kClBufs; ++r) {
+      Welford t{0.0f, 0.0f, 0.0f};
+      for (uint32_t k = 0; k < C; ++k) {  // rank order: identical in every CTA
+        const float4 u = slot[sl][r][k];
+        t = chan_merge(t, Welford{u.x, u.y, u.z});
+      }
+      mean[r] = t.mean;
+      rstd[r] = rsqrtf(fmaf(t.m2, __frcp_rn(t.n), eps));
+      const int64_t row = cid + (k0 + r) * ncl;
+      if (q == 0 && tid == 0 && k0 + r < nr) {
+        if (mean_out) mean_out[row] = mean[r];
+        if (rstd_out) rstd_out[row] = rstd[r];
       }
     }
-    if (gi > 0) {
-      // finalise group gi - 1: wait for every rank's triples, merge in rank order
-      const int64_t gp = gi - 1;
-      const int sl = static_cast<int>(gp % kClSlots);
-      const uint32_t pp = static_cast<uint32_t>((gp / kClSlots) & 1);
-      if (!timed_out && !mbar_wait_bounded(&pbar[sl], pp, kWaitBudget)) {
-        timed_out = 1;
-        atomicCAS(err, 0, FR_DEVERR_TIMEOUT);
-      }
-      const int j_l = lane / static_cast<int>(C), k_l = lane % static_cast<int>(C);
-      Welford pw{0.0f, 0.0f, 0.0f};
-      if (j_l < kClRows) {
-        const float4 v = slot[sl][j_l][k_l];
-        pw = Welford{v.x, v.y, v.z};
-      }
-      // fixed butterfly inside each group of C lanes (lower rank first), so
-      // every lane of the group and every CTA gets the same bits
-      for (uint32_t o = 1; o < C; o <<= 1) {
-        Welford v{__shfl_xor_sync(0xffffffffu, pw.n, o), __shfl_xor_sync(0xffffffffu, pw.mean, o),
-                  __shfl_xor_sync(0xffffffffu, pw.m2, o)};
-        pw = (k_l & o) ? chan_merge(v, pw) : chan_merge(pw, v);
-      }
-      // Re-arm slot sl for group gp + kClSlots.  Peers can send that group only
-      // after this CTA publishes group gp + 2, which every thread reaches only
-      // after finishing this finalisation, so the slot's data and the phase
-      // every thread here waits on are both safe.
-      if (tid == 0 && gp + kClSlots < ngroups) mbar_arrive_expect_tx(&pbar[sl], part_bytes);
+    // Re-arm the slot for wave wv + 4: peers write it only after this CTA
+    // publishes wave wv + 1, which every thread reaches after this point.
+    if (tid == 0 && wv + kClSlots < nwaves) mbar_arrive_expect_tx(&pbar[sl], part_bytes);
+    if (own) {
 #pragma unroll
-      for (int j = 0; j < kClRows; ++j) {
-        const int src = j * static_cast<int>(C);
-        const float n = __shfl_sync(0xffffffffu, pw.n, src);
-        const float mean = __shfl_sync(0xffffffffu, pw.mean, src);
-        const float m2 = __shfl_sync(0xffffffffu, pw.m2, src);
-        const int64_t r = row_of(gp, j);
-        if (r >= rows) continue;
-        const float rstd = rsqrtf(fmaf(m2, __frcp_rn(n), eps));
-        if (q == 0 && tid == 0) {
-          if (mean_out) mean_out[r] = mean;
-          if (rstd_out) rstd_out[r] = rstd;
-        }
-        if (own) {
-          const uint32_t wv[4] = {xprev[j].x, xprev[j].y, xprev[j].z, xprev[j].w};
-          uint32_t o[4];
+      for (int h = 0; h < 4; ++h) {  // 4 columns of gamma/beta at a time, shared by the wave
+        const float4 g = *reinterpret_cast<const float4 *>(sg + 16 * tid + 4 * h);
+        const float4 bb = *reinterpret_cast<const float4 *>(sb + 16 * tid + 4 * h);
 #pragma unroll
-          for (int h = 0; h < 4; ++h)
-            o[h] = pack_bf16x2(fmaf((bf16_lo(wv[h]) - mean) * rstd, g8[2 * h], b8[2 * h]),
-                               fmaf((bf16_hi(wv[h]) - mean) * rstd, g8[2 * h + 1], b8[2 * h + 1]));
-          uint16_t *dst = y + r * ldy + col0;
-          asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(dst), "r"(o[0]), "r"(o[1]),
-                       "r"(o[2]), "r"(o[3])
-                       : "memory");
+        for (int r = 0; r < kClBufs; ++r) {
+          const uint32_t w0 = v[r].w[2 * h], w1 = v[r].w[2 * h + 1];
+          v[r].w[2 * h] = pack_bf16x2(fmaf((bf16_lo(w0) - mean[r]) * rstd[r], g.x, bb.x),
+                                      fmaf((bf16_hi(w0) - mean[r]) * rstd[r], g.y, bb.y));
+          v[r].w[2 * h + 1] = pack_bf16x2(fmaf((bf16_lo(w1) - mean[r]) * rstd[r], g.z, bb.z),
+                                          fmaf((bf16_hi(w1) - mean[r]) * rstd[r], g.w, bb.w));
         }
       }
+#pragma unroll
+      for (int r = 0; r < kClBufs; ++r)
+        if (k0 + r < nr) st_stream_v8(y + (cid + (k0 + r) * ncl) * ldy + col0, v[r]);
     }
-#pragma unroll
-    for (int j = 0; j < kClRows; ++j) xprev[j] = xcur[j];
   }
-  // No CTA may leave while a peer can still write into or read its shared memory.
+  cp_async_wait<0>();
+  // No CTA may leave while a peer can still write into its shared memory.
   cluster_arrive();
   cluster_wait();
-  if (timed_out && tid == 0)  // last bounded wait on each stage's latest copy
-    for (int64_t gl = ngroups - 1; gl >= 0 && gl >= ngroups - kClStages; --gl)
-      mbar_wait_bounded(&full[gl % kClStages], static_cast<uint32_t>((gl / kClStages) & 1),
-                        kWaitBudget);
-}
-
-// Buffers per CTA for a row of `cols` bf16 within `max_smem` bytes.
-int ring_buffers(int64_t cols, int max_smem) {
-  const size_t buf = static_cast<size_t>((cols * 2 + 127) / 128 * 128);
-  const size_t avail = static_cast<size_t>(max_smem) - kRingHeader - 1024;  // static smem
-  int nb = static_cast<int>(avail / buf);
-  if (nb > kRingMaxBuffers) nb = kRingMaxBuffers;
-  return nb;
 }
 
 }  // namespace
 
-// Smallest cluster size whose slices fit one thread per 8 columns.
+// Cluster size: 1 when gamma/beta of the whole row fit one CTA, else 2.
 int cluster_size_for(int64_t cols) {
   for (int c = 1; c <= kClMaxCluster; c <<= 1)
-    if (cols % (8 * c) == 0 && cols / c <= 8 * kClThreads) return c;
+    if (cols % (16 * c) == 0 && cols / c <= kClMaxSlice) return c;
   return 0;
 }
 
-bool layernorm_cluster_ok(int64_t cols, bool aligned16) {
-  return aligned16 && cluster_size_for(cols) > 0;
+size_t cluster_smem(int64_t cols, int c) {
+  const int64_t S = cols / c;
+  return static_cast<size_t>(S) * 8 + static_cast<size_t>(kClBufs) * S * 2;
+}
+
+bool layernorm_cluster_ok(int64_t cols, bool aligned) {
+  const int c = cluster_size_for(cols);
+  return aligned && c > 0;
 }
 
 cudaError_t launch_layernorm_cluster(const uint16_t *x, const float *gamma, const float *beta,
@@ -534,7 +486,7 @@ cudaError_t launch_layernorm_cluster(const uint16_t *x, const float *gamma, cons
   if (e != cudaSuccess) return e;
   const int C = cluster_size_for(cols);
   if (C == 0) return cudaErrorInvalidValue;
-  const size_t smem = 128 + static_cast<size_t>(kClStages) * kClRows * (cols / C) * 2;
+  const size_t smem = cluster_smem(cols, C);
   e = cudaFuncSetAttribute(layernorm_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -554,8 +506,7 @@ cudaError_t launch_layernorm_cluster(const uint16_t *x, const float *gamma, cons
   e = cudaOccupancyMaxActiveClusters(&clusters, layernorm_cluster, &cfg);
   if (e != cudaSuccess) return e;
   if (clusters < 1) return cudaErrorInvalidConfiguration;
-  // Persistent: every cluster that can be resident, no more than one per row.
-  int64_t ncl = clusters;
+  int64_t ncl = clusters;  // persistent: every cluster that can be resident
   if (ncl > rows) ncl = rows;
   cfg.gridDim = dim3(static_cast<unsigned>(ncl * C));
   return cudaLaunchKernelEx(&cfg, layernorm_cluster, x, gamma, beta, y, mean, rstd, rows, cols,
@@ -563,37 +514,40 @@ cudaError_t launch_layernorm_cluster(const uint16_t *x, const float *gamma, cons
 }
 
 size_t layernorm_ring_smem(int64_t cols, int nbuf) {
-  return static_cast<size_t>(kRingHeader) +
-         static_cast<size_t>(nbuf) * static_cast<size_t>((cols * 2 + 127) / 128 * 128);
+  return static_cast<size_t>(nbuf) * static_cast<size_t>(cols) * 2;
 }
 
 bool layernorm_ring_ok(int64_t cols, bool vec, int max_smem_optin) {
-  return vec && cols % 16 == 0 && (cols * 2 + kRingChunk - 1) / kRingChunk <= kRingMaxChunks &&
-         ring_buffers(cols, max_smem_optin) >= 1;
+  return vec && cols % 16 == 0 && cols / 16 <= static_cast<int64_t>(kRingThreads) * kRingPieces &&
+         layernorm_ring_smem(cols, kRingBufs) + 1024 <= static_cast<size_t>(max_smem_optin);
 }
 
 cudaError_t launch_layernorm_ring(const uint16_t *x, const float *gamma, const float *beta,
                                   uint16_t *y, float *mean, float *rstd, int64_t rows,
                                   int64_t cols, int64_t ldx, int64_t ldy, float eps, int sm_count,
-                                  int max_smem_optin, cudaStream_t s) {
-  int *err = nullptr;
-  cudaError_t e = device_error_word(&err);
-  if (e != cudaSuccess) return e;
-  const int nbuf = ring_buffers(cols, max_smem_optin);
-  if (nbuf < 1) return cudaErrorInvalidValue;
-  const size_t smem = layernorm_ring_smem(cols, nbuf);
-  e = cudaFuncSetAttribute(layernorm_ring, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem));
+                                  int, cudaStream_t s) {
+  const size_t smem = layernorm_ring_smem(cols, kRingBufs);
+  // R rows per gamma/beta pass; FR_LAYERNORM_ROWS=1|2 pins it (default 2;
+  // three rows need more than the 128 registers a thread can have).
+  int R = 2;
+  if (const char *e = getenv("FR_LAYERNORM_ROWS")) {
+    const int v = atoi(e);
+    if (v >= 1 && v <= 2) R = v;
+  }
+  const void *kern = R == 1 ? reinterpret_cast<const void *>(&layernorm_ring<1>)
+                            : reinterpret_cast<const void *>(&layernorm_ring<2>);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, layernorm_ring, kRingThreads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRingThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   int64_t grid = static_cast<int64_t>(sm_count) * per_sm;
   if (grid > rows) grid = rows;
-  layernorm_ring<<<static_cast<unsigned>(grid), kRingThreads, smem, s>>>(
-      x, gamma, beta, y, mean, rstd, rows, cols, ldx, ldy, eps, nbuf, err);
-  return cudaGetLastError();
+  void *args[] = {&x, &gamma, &beta, &y, &mean, &rstd, &rows, &cols, &ldx, &ldy, &eps};
+  return cudaLaunchKernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kRingThreads), args, smem,
+                          s);
 }
 
 bool layernorm_persistent_ok(int64_t cols, bool vec) {
