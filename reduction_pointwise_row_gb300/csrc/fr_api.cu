@@ -270,7 +270,7 @@ fr_status fr_xent(const void *logits, const int64_t *target, float *loss, float 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return launched(fr::launch_xent(static_cast<const uint16_t *>(logits), target, loss, loss_mean,
                                   target_logit, argmax, rows, cols, ld, ignore_index, workspace,
-                                  info.sm_count, s),
+                                  info.sm_count, info.max_smem_optin, s),
                   FR_FORM_LOOPED);
 }
 

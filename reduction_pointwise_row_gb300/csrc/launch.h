@@ -81,7 +81,7 @@ size_t xent_workspace(int64_t rows, int sm_count);
 cudaError_t launch_xent(const uint16_t *logits, const int64_t *target, float *loss,
                         float *loss_mean, float *target_logit, int64_t *argmax, int64_t rows,
                         int64_t cols, int64_t ld, int64_t ignore_index, void *workspace,
-                        int sm_count, cudaStream_t s);
+                        int sm_count, int max_smem_optin, cudaStream_t s);
 // Device address of the current device's error word (kernels record
 // FR_DEVERR_* codes there with atomicCAS; the first code wins).
 cudaError_t device_error_word(int **out);

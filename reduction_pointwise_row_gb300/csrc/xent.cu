@@ -21,6 +21,7 @@
 // CTA order.
 #include <algorithm>
 #include <cstdlib>
+#include <cstring>
 
 #include "common.cuh"
 #include "launch.h"
@@ -33,6 +34,7 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kCtasPerSm = 2;
+constexpr int kMaxCtasPerSm = 16;  // largest persistent grid: 16 CTAs per SM (workspace bound)
 
 struct ArgBest {
   float v;
@@ -77,14 +79,16 @@ __device__ __forceinline__ Workspace carve(void *ws, int grid) {
 
 // U: 32-byte vectors (16 bf16 each) per thread per chunk.  DB: load the next
 // chunk into a second register buffer while the current one is reduced.
-template <bool ARGMAX, int U, bool DB>
-__global__ void __launch_bounds__(kThreads, (ARGMAX || (DB && U > 1)) ? 1 : 2)
+// T: threads per CTA (one row per CTA at a time).
+template <bool ARGMAX, int U, bool DB, int T = kThreads>
+__global__ void __launch_bounds__(T, (ARGMAX || (DB && U > 1)) ? 1 : 1024 / T)
 xent_rows(const uint16_t *__restrict__ logits, const int64_t *__restrict__ target,
           float *__restrict__ loss, float *__restrict__ target_logit, int64_t *__restrict__ argmax,
           float *__restrict__ loss_mean, void *__restrict__ ws, int64_t rows, int64_t cols,
           int64_t ld, int64_t ignore_index) {
   // Per-warp partials, double-buffered by row parity so one barrier per row
   // suffices (the next row writes the other half).
+  constexpr int kThreads = T;
   __shared__ MD red_md[2][kThreads / 32];
   __shared__ ArgBest red_arg[2][kThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -215,8 +219,7 @@ xent_rows(const uint16_t *__restrict__ logits, const int64_t *__restrict__ targe
     }
     __syncthreads();
     if (warp == 0) {
-      MD r = red_md[parity][lane < kThreads / 32 ? lane : 0];
-      if (lane >= kThreads / 32) r = MD{-INFINITY, 0.0f};
+      MD r = lane < kThreads / 32 ? red_md[parity][lane] : MD{-INFINITY, 0.0f};
       r = warp_md(r);
       ArgBest b{-INFINITY, INT64_MAX};
       if constexpr (ARGMAX) {
@@ -276,27 +279,488 @@ xent_rows(const uint16_t *__restrict__ logits, const int64_t *__restrict__ targe
   }
 }
 
+// ---- staged variant: whole rows through shared memory by bulk copies --------
+// One persistent CTA per SM with two row buffers: row k + 1's bulk copies are
+// in flight while row k is reduced from shared memory, and row k + 2's are
+// issued as soon as every thread has read row k.  A row's 16-byte aligned
+// interior is copied in kStParts parts (each with its own mbarrier, so work
+// starts when the first part lands); its head and tail (fewer than 8 elements
+// each) are plain loads.  Copies of 25 KB and more stream at HBM speed on
+// GB300, where a CTA's bulk copies complete one after another.
+constexpr int kStThreads = 1024;
+constexpr int kStParts = 4;
+constexpr long long kStWaitBudget = 1LL << 31;  // SM clocks (about one second)
+
+struct RowGeom {
+  const uint16_t *row;  // row start
+  uint64_t a0;          // first 16-byte boundary at or after the row start
+  uint32_t ibytes;      // interior bytes (multiple of 16)
+  int head;             // elements before a0
+  int tail;             // elements after the interior
+};
+
+__device__ __forceinline__ RowGeom row_geom(const uint16_t *logits, int64_t row, int64_t ld,
+                                            int64_t cols) {
+  RowGeom g;
+  g.row = logits + row * ld;
+  const uint64_t s0 = reinterpret_cast<uint64_t>(g.row);
+  const uint64_t s1 = s0 + 2 * static_cast<uint64_t>(cols);
+  const uint64_t a0 = (s0 + 15) & ~uint64_t(15), a1 = s1 & ~uint64_t(15);
+  if (a1 <= a0) {  // a row too short to hold an aligned 16 bytes: all head
+    g.a0 = s0;
+    g.ibytes = 0;
+    g.head = static_cast<int>(cols);
+    g.tail = 0;
+    return g;
+  }
+  g.a0 = a0;
+  g.ibytes = static_cast<uint32_t>(a1 - a0);
+  g.head = static_cast<int>((a0 - s0) / 2);
+  g.tail = static_cast<int>((s1 - a1) / 2);
+  return g;
+}
+
+__device__ __forceinline__ uint32_t part_begin(uint32_t ibytes, int p) {
+  // parts of equal size rounded up to 32 bytes; the last takes the remainder
+  const uint32_t per = ((ibytes / kStParts) + 31u) & ~31u;
+  const uint32_t b = per * static_cast<uint32_t>(p);
+  return b < ibytes ? b : ibytes;
+}
+
+template <bool ARGMAX>
+__global__ void __launch_bounds__(kStThreads, 1)
+xent_staged(const uint16_t *__restrict__ logits, const int64_t *__restrict__ target,
+            float *__restrict__ loss, float *__restrict__ target_logit,
+            int64_t *__restrict__ argmax, float *__restrict__ loss_mean, void *__restrict__ ws,
+            int64_t rows, int64_t cols, int64_t ld, int64_t ignore_index, uint32_t buf_bytes) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem);  // [2][kStParts]
+  unsigned char *bufs = smem + 128;
+  __shared__ MD red_md[2][kStThreads / 32];
+  __shared__ ArgBest red_arg[2][kStThreads / 32];
+  __shared__ int timed_out;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t G = gridDim.x;
+  const int64_t nk = blockIdx.x < rows ? (rows - blockIdx.x + G - 1) / G : 0;
+  const uint64_t policy = l2_evict_first_policy();
+
+  auto issue = [&](int64_t k) {  // thread 0: row k of this CTA into buffer k & 1
+    if (k >= nk) return;
+    const RowGeom g = row_geom(logits, blockIdx.x + k * G, ld, cols);
+    const int b = static_cast<int>(k & 1);
+    for (int p = 0; p < kStParts; ++p) {
+      const uint32_t lo = part_begin(g.ibytes, p), hi = part_begin(g.ibytes, p + 1);
+      const uint32_t n = (p == kStParts - 1 ? g.ibytes : hi) - lo;
+      mbar_arrive_expect_tx(&full[b * kStParts + p], n);
+      if (n > 0)
+        bulk_copy_g2s(bufs + static_cast<size_t>(b) * buf_bytes + lo,
+                      reinterpret_cast<const unsigned char *>(g.a0) + lo, n,
+                      &full[b * kStParts + p], policy);
+    }
+  };
+
+  if (tid == 0) {
+    timed_out = 0;
+    for (int i = 0; i < 2 * kStParts; ++i) mbar_init(&full[i], 1);
+    mbar_init_fence();
+    issue(0);
+    issue(1);
+  }
+  __syncthreads();
+
+  double cta_sum = 0.0;
+  long long cta_cnt = 0;
+  int64_t t_next = (tid == 0 && nk > 0) ? target[blockIdx.x] : 0;
+  for (int64_t k = 0; k < nk; ++k) {
+    const int64_t row = blockIdx.x + k * G;
+    const int b = static_cast<int>(k & 1);
+    const uint32_t parity = static_cast<uint32_t>((k >> 1) & 1);
+    const RowGeom g = row_geom(logits, row, ld, cols);
+    int64_t t = 0;
+    uint16_t xt_bits = 0;
+    if (tid == 0) {
+      t = t_next;
+      if (t >= 0 && t < cols) xt_bits = g.row[t];
+      if (k + 1 < nk) t_next = target[row + G];
+    }
+    MD st{-INFINITY, 0.0f};
+    ArgBest best{-INFINITY, INT64_MAX};
+    const unsigned char *buf = bufs + static_cast<size_t>(b) * buf_bytes;
+    for (int p = 0; p < kStParts; ++p) {
+      if (!timed_out && !mbar_wait_bounded(&full[b * kStParts + p], parity, kStWaitBudget)) {
+        timed_out = 1;
+        atomicCAS(&g_fr_device_error, 0, FR_DEVERR_TIMEOUT);
+      }
+      const uint32_t lo = part_begin(g.ibytes, p);
+      const uint32_t hi = p == kStParts - 1 ? g.ibytes : part_begin(g.ibytes, p + 1);
+      // 32-byte pieces (16 bf16) of this part, thread-strided; a 16-byte
+      // remainder at the end of the interior is padded with -inf
+      for (uint32_t off = lo + 32u * tid; off < hi; off += 32u * kStThreads) {
+        const bool two = off + 16u < hi;
+        const uint4 a = lds_u4(buf + off);
+        const uint4 c = two ? lds_u4(buf + off + 16u) : make_uint4(0xFF80FF80u, 0xFF80FF80u,
+                                                                  0xFF80FF80u, 0xFF80FF80u);
+        const uint32_t wv[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+        uint32_t m2 = max_nan_bf16x2(max_nan_bf16x2(a.x, a.y), max_nan_bf16x2(a.z, a.w));
+        m2 = max_nan_bf16x2(m2, max_nan_bf16x2(max_nan_bf16x2(c.x, c.y), max_nan_bf16x2(c.z, c.w)));
+        const float cm = max_nan(bf16_lo(m2), bf16_hi(m2));
+        if constexpr (ARGMAX) {
+          if (best.i == INT64_MAX || cm > best.v || (cm != cm && best.v == best.v)) {
+            bool found = false;
+            const int nval = two ? 16 : 8;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float e = (j & 1) ? bf16_hi(wv[j >> 1]) : bf16_lo(wv[j >> 1]);
+              const bool hit = (cm != cm) ? (e != e) : (e == cm);
+              if (!found && hit && j < nval) {
+                found = true;
+                best = ArgBest{cm, g.head + static_cast<int64_t>(off / 2) + j};
+              }
+            }
+          }
+        }
+        st = fold_chunk(st, cm);
+        if (st.m != -INFINITY) {
+          const float nmb = -st.m * kLog2e;
+          const uint64_t l2e2 = pack_f32x2(kLog2e, kLog2e), nmb2 = pack_f32x2(nmb, nmb);
+          uint64_t acc2 = 0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint64_t t2 = fma_f32x2(pack_f32x2(bf16_lo(wv[j]), bf16_hi(wv[j])), l2e2, nmb2);
+            acc2 = add_f32x2(acc2, pack_f32x2(ex2(f32x2_lo(t2)), ex2(f32x2_hi(t2))));
+          }
+          st.d += f32x2_lo(acc2) + f32x2_hi(acc2);
+        }
+      }
+    }
+    // head and tail scalars from global memory
+    int64_t si = -1;
+    if (tid < g.head) si = tid;
+    else if (tid < g.head + g.tail) si = g.head + g.ibytes / 2 + (tid - g.head);
+    if (si >= 0) {
+      const float e = bf16_to_f32(ld_stream_u16(g.row + si));
+      st = md_merge(st, MD{e, 1.0f});
+      if constexpr (ARGMAX) best = arg_better(best, ArgBest{e, si});
+    }
+    // CTA combine; the barrier also frees buffer b for row k + 2
+    st = warp_md(st);
+    if constexpr (ARGMAX) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        ArgBest other{__shfl_xor_sync(0xffffffffu, best.v, o),
+                      static_cast<int64_t>(__shfl_xor_sync(0xffffffffu,
+                                                           static_cast<long long>(best.i), o))};
+        best = arg_better(best, other);
+      }
+    }
+    if (lane == 0) {
+      red_md[b][warp] = st;
+      if constexpr (ARGMAX) red_arg[b][warp] = best;
+    }
+    __syncthreads();
+    if (tid == 0 && !timed_out) {
+      fence_proxy_async_smem();
+      issue(k + 2);
+    }
+    if (warp == 0) {
+      MD r = red_md[b][lane];
+      r = warp_md(r);
+      ArgBest bb{-INFINITY, INT64_MAX};
+      if constexpr (ARGMAX) {
+        bb = red_arg[b][lane];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          ArgBest other{__shfl_xor_sync(0xffffffffu, bb.v, o),
+                        static_cast<int64_t>(__shfl_xor_sync(0xffffffffu,
+                                                             static_cast<long long>(bb.i), o))};
+          bb = arg_better(bb, other);
+        }
+      }
+      if (lane == 0) {  // thread 0 holds t and x[t]
+        const float lse = r.m + logf(r.d);
+        float l, xt;
+        if (t == ignore_index) {
+          l = 0.0f;
+          xt = 0.0f;
+        } else if (t < 0 || t >= cols) {
+          l = __int_as_float(0x7fc00000);
+          xt = l;
+          atomicCAS(&g_fr_device_error, 0, FR_DEVERR_BAD_TARGET);
+        } else {
+          xt = bf16_to_f32(xt_bits);
+          l = lse - xt;
+        }
+        if (loss) loss[row] = l;
+        if (target_logit) target_logit[row] = xt;
+        if constexpr (ARGMAX) argmax[row] = bb.i;
+        if (t != ignore_index) {
+          cta_sum += static_cast<double>(l);
+          ++cta_cnt;
+        }
+      }
+    }
+    // red_*[b] is next written two rows later, after the barrier of row k + 1.
+  }
+  if (timed_out && tid == 0)  // last bounded wait on copies that may be in flight
+    for (int i = 0; i < 2 * kStParts; ++i) mbar_wait_bounded(&full[i], 0, kStWaitBudget);
+
+  if (loss_mean != nullptr && tid == 0) {
+    Workspace w = carve(ws, gridDim.x);
+    w.sums[blockIdx.x] = cta_sum;
+    w.counts[blockIdx.x] = cta_cnt;
+    __threadfence();
+    const unsigned int ticket = atomicAdd(w.ticket, 1u);
+    if (ticket == gridDim.x - 1) {
+      __threadfence();
+      double s = 0.0;
+      long long c = 0;
+      for (unsigned int i = 0; i < gridDim.x; ++i) {
+        s += *reinterpret_cast<volatile double *>(&w.sums[i]);
+        c += *reinterpret_cast<volatile long long *>(&w.counts[i]);
+      }
+      *loss_mean = static_cast<float>(s / static_cast<double>(c));
+      *w.ticket = 0u;
+    }
+  }
+}
+
+uint32_t staged_buf_bytes(int64_t cols) {
+  return static_cast<uint32_t>((2 * cols + 16 + 127) / 128 * 128);
+}
+
+// ---- asynchronous-copy ring variant ---------------------------------------------
+// Each thread streams its share of the CTA's rows as items of U 16-byte vectors
+// (item c of row k covers vectors c*T*U + u*T + tid of the row's 16-byte
+// aligned interior).  Items go through a per-thread ring of NS shared-memory
+// stages filled with cp.async (no registers held, one commit group per item),
+// continuing across row boundaries, so NS - 1 items per thread are always in
+// flight -- also while the CTA combines a finished row.
+template <bool ARGMAX, int T, int U, int NS>
+__global__ void __launch_bounds__(T, 1)
+xent_async(const uint16_t *__restrict__ logits, const int64_t *__restrict__ target,
+           float *__restrict__ loss, float *__restrict__ target_logit,
+           int64_t *__restrict__ argmax, float *__restrict__ loss_mean, void *__restrict__ ws,
+           int64_t rows, int64_t cols, int64_t ld, int64_t ignore_index) {
+  extern __shared__ __align__(128) unsigned char smem[];  // [NS][U][T] x 16 bytes
+  __shared__ MD red_md[2][T / 32];
+  __shared__ ArgBest red_arg[2][T / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t G = gridDim.x;
+  const int64_t nk = blockIdx.x < rows ? (rows - blockIdx.x + G - 1) / G : 0;
+  auto slot = [&](int s, int u) {
+    return smem + (static_cast<size_t>(s * U + u) * T + tid) * 16;
+  };
+  // Producer cursor: the next item to copy is item pc of row pk (pn items).
+  // Rows without items (too short for an aligned interior) are skipped, as
+  // the consumer skips them: the i-th item produced is the i-th consumed.
+  int64_t pk = 0;
+  int pc = 0, pn = 0, ps = 0;
+  RowGeom pg{};
+  auto load_row = [&]() {
+    for (; pk < nk; ++pk) {
+      pg = row_geom(logits, blockIdx.x + pk * G, ld, cols);
+      pn = static_cast<int>((pg.ibytes / 16 + T * U - 1) / (T * U));
+      if (pn > 0) return;
+    }
+  };
+  load_row();
+  auto produce = [&]() {
+    if (pk < nk) {
+      const int nv = static_cast<int>(pg.ibytes / 16);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = pc * T * U + u * T + tid;
+        if (v < nv)
+          cp_async_16(slot(ps, u),
+                      reinterpret_cast<const unsigned char *>(pg.a0) + 16 * static_cast<size_t>(v));
+      }
+      if (++pc >= pn) {  // next row with items
+        pc = 0;
+        ++pk;
+        load_row();
+      }
+    }
+    cp_async_commit();  // one group per item, empty past the last item
+    ps = ps + 1 == NS ? 0 : ps + 1;
+  };
+#pragma unroll
+  for (int i = 0; i < NS - 1; ++i) produce();
+
+  double cta_sum = 0.0;
+  long long cta_cnt = 0;
+  int64_t t_next = (tid == 0 && nk > 0) ? target[blockIdx.x] : 0;
+  int cs = 0;  // consumer stage
+  int parity = 0;
+  for (int64_t k = 0; k < nk; ++k, parity ^= 1) {
+    const int64_t row = blockIdx.x + k * G;
+    const RowGeom g = row_geom(logits, row, ld, cols);
+    int64_t t = 0;
+    uint16_t xt_bits = 0;
+    if (tid == 0) {
+      t = t_next;
+      if (t >= 0 && t < cols) xt_bits = g.row[t];
+      if (k + 1 < nk) t_next = target[row + G];
+    }
+    const int nv = static_cast<int>(g.ibytes / 16);
+    const int nitems = (nv + T * U - 1) / (T * U);
+    MD st{-INFINITY, 0.0f};
+    ArgBest best{-INFINITY, INT64_MAX};
+    for (int c = 0; c < nitems; ++c) {
+      produce();                 // keep NS - 1 items in flight
+      cp_async_wait<NS - 1>();   // this thread's copies of item (k, c) landed
+      uint32_t wv[U][4];
+      uint32_t m2 = 0xFF80FF80u;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = c * T * U + u * T + tid;
+        if (v < nv) {
+          const uint4 q = lds_u4(slot(cs, u));
+          wv[u][0] = q.x; wv[u][1] = q.y; wv[u][2] = q.z; wv[u][3] = q.w;
+          m2 = max_nan_bf16x2(m2, max_nan_bf16x2(max_nan_bf16x2(q.x, q.y), max_nan_bf16x2(q.z, q.w)));
+        } else {
+          wv[u][0] = wv[u][1] = wv[u][2] = wv[u][3] = 0xFF80FF80u;  // -inf: adds nothing
+        }
+      }
+      cs = cs + 1 == NS ? 0 : cs + 1;
+      const float cm = max_nan(bf16_lo(m2), bf16_hi(m2));
+      if constexpr (ARGMAX) {
+        if (best.i == INT64_MAX || cm > best.v || (cm != cm && best.v == best.v)) {
+          bool found = false;
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int v = c * T * U + u * T + tid;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float e = (j & 1) ? bf16_hi(wv[u][j >> 1]) : bf16_lo(wv[u][j >> 1]);
+              const bool hit = (cm != cm) ? (e != e) : (e == cm);
+              if (!found && hit && v < nv) {
+                found = true;
+                best = ArgBest{cm, g.head + 8 * static_cast<int64_t>(v) + j};
+              }
+            }
+          }
+        }
+      }
+      st = fold_chunk(st, cm);
+      if (st.m != -INFINITY) {
+        const float nmb = -st.m * kLog2e;
+        const uint64_t l2e2 = pack_f32x2(kLog2e, kLog2e), nmb2 = pack_f32x2(nmb, nmb);
+        uint64_t acc2 = 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint64_t t2 =
+                fma_f32x2(pack_f32x2(bf16_lo(wv[u][j]), bf16_hi(wv[u][j])), l2e2, nmb2);
+            acc2 = add_f32x2(acc2, pack_f32x2(ex2(f32x2_lo(t2)), ex2(f32x2_hi(t2))));
+          }
+        st.d += f32x2_lo(acc2) + f32x2_hi(acc2);
+      }
+    }
+    int64_t si = -1;
+    if (tid < g.head) si = tid;
+    else if (tid < g.head + g.tail) si = g.head + g.ibytes / 2 + (tid - g.head);
+    if (si >= 0) {
+      const float e = bf16_to_f32(ld_stream_u16(g.row + si));
+      st = md_merge(st, MD{e, 1.0f});
+      if constexpr (ARGMAX) best = arg_better(best, ArgBest{e, si});
+    }
+    st = warp_md(st);
+    if constexpr (ARGMAX) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        ArgBest other{__shfl_xor_sync(0xffffffffu, best.v, o),
+                      static_cast<int64_t>(__shfl_xor_sync(0xffffffffu,
+                                                           static_cast<long long>(best.i), o))};
+        best = arg_better(best, other);
+      }
+    }
+    if (lane == 0) {
+      red_md[parity][warp] = st;
+      if constexpr (ARGMAX) red_arg[parity][warp] = best;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      MD r = lane < T / 32 ? red_md[parity][lane] : MD{-INFINITY, 0.0f};
+      r = warp_md(r);
+      ArgBest bb{-INFINITY, INT64_MAX};
+      if constexpr (ARGMAX) {
+        if (lane < T / 32) bb = red_arg[parity][lane];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          ArgBest other{__shfl_xor_sync(0xffffffffu, bb.v, o),
+                        static_cast<int64_t>(__shfl_xor_sync(0xffffffffu,
+                                                             static_cast<long long>(bb.i), o))};
+          bb = arg_better(bb, other);
+        }
+      }
+      if (lane == 0) {
+        const float lse = r.m + logf(r.d);
+        float l, xt;
+        if (t == ignore_index) {
+          l = 0.0f;
+          xt = 0.0f;
+        } else if (t < 0 || t >= cols) {
+          l = __int_as_float(0x7fc00000);
+          xt = l;
+          atomicCAS(&g_fr_device_error, 0, FR_DEVERR_BAD_TARGET);
+        } else {
+          xt = bf16_to_f32(xt_bits);
+          l = lse - xt;
+        }
+        if (loss) loss[row] = l;
+        if (target_logit) target_logit[row] = xt;
+        if constexpr (ARGMAX) argmax[row] = bb.i;
+        if (t != ignore_index) {
+          cta_sum += static_cast<double>(l);
+          ++cta_cnt;
+        }
+      }
+    }
+  }
+  cp_async_wait<0>();
+  if (loss_mean != nullptr && tid == 0) {
+    Workspace w = carve(ws, gridDim.x);
+    w.sums[blockIdx.x] = cta_sum;
+    w.counts[blockIdx.x] = cta_cnt;
+    __threadfence();
+    const unsigned int ticket = atomicAdd(w.ticket, 1u);
+    if (ticket == gridDim.x - 1) {
+      __threadfence();
+      double sum = 0.0;
+      long long cnt = 0;
+      for (unsigned int i = 0; i < gridDim.x; ++i) {
+        sum += *reinterpret_cast<volatile double *>(&w.sums[i]);
+        cnt += *reinterpret_cast<volatile long long *>(&w.counts[i]);
+      }
+      *loss_mean = static_cast<float>(sum / static_cast<double>(cnt));
+      *w.ticket = 0u;
+    }
+  }
+}
+
 // Launch-configuration candidates (Stax (4), section 9.6, Algorithm 9.1):
 // a small set of compiled variants, the fastest chosen by measurement on
 // GB300; FR_XENT_VARIANT=<index> forces one (for re-measuring the choice).
 struct XentVariant {
   const void *kern;      // the non-argmax kernel
   const void *kern_arg;  // the argmax kernel
-  int ctas_per_sm;
+  int threads;
 };
 
-template <int U, bool DB>
+template <int U, bool DB, int T>
 XentVariant make_variant() {
-  return XentVariant{reinterpret_cast<const void *>(&xent_rows<false, U, DB>),
-                     reinterpret_cast<const void *>(&xent_rows<true, U, DB>), 0};
+  return XentVariant{reinterpret_cast<const void *>(&xent_rows<false, U, DB, T>),
+                     reinterpret_cast<const void *>(&xent_rows<true, U, DB, T>), T};
 }
 
-constexpr int kNumVariants = 4;
+constexpr int kNumVariants = 6;
 constexpr int kDefaultVariant = 0;
 
 XentVariant *variants() {
-  static XentVariant v[kNumVariants] = {make_variant<2, false>(), make_variant<1, true>(),
-                                        make_variant<4, false>(), make_variant<2, true>()};
+  static XentVariant v[kNumVariants] = {
+      make_variant<2, false, 512>(), make_variant<1, true, 512>(), make_variant<4, false, 512>(),
+      make_variant<2, true, 512>(),  make_variant<2, false, 256>(), make_variant<2, false, 128>()};
   return v;
 }
 
@@ -317,7 +781,7 @@ int chosen_variant() {
 int xent_ctas_per_sm(bool argmax) {
   XentVariant &v = variants()[chosen_variant()];
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, argmax ? v.kern_arg : v.kern, kThreads,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, argmax ? v.kern_arg : v.kern, v.threads,
                                                     0) != cudaSuccess) {
     cudaGetLastError();
     return kCtasPerSm;
@@ -327,7 +791,7 @@ int xent_ctas_per_sm(bool argmax) {
 
 // Persistent grid of one kernel: every CTA it can keep resident on every SM.
 int xent_grid(int64_t rows, int sm_count, bool argmax) {
-  int64_t g = static_cast<int64_t>(sm_count) * xent_ctas_per_sm(argmax);
+  int64_t g = static_cast<int64_t>(sm_count) * std::min(xent_ctas_per_sm(argmax), 16);
   if (g > rows) g = rows;
   if (g < 1) g = 1;
   return static_cast<int>(g);
@@ -336,15 +800,121 @@ int xent_grid(int64_t rows, int sm_count, bool argmax) {
 }  // namespace
 
 size_t xent_workspace(int64_t rows, int sm_count) {
-  // One fp64 sum and one count per CTA of the larger of the two grids.
-  const int g = std::max(xent_grid(rows, sm_count, false), xent_grid(rows, sm_count, true));
+  // A ticket, then one fp64 sum and one count per CTA of the largest grid.
+  int64_t g = static_cast<int64_t>(sm_count) * kMaxCtasPerSm;
+  if (g > rows) g = rows;
+  if (g < 1) g = 1;
   return 16 + 16 * static_cast<size_t>(g);
+}
+
+// The staged kernel, pinned with FR_XENT_VARIANT=staged, when its two row
+// buffers fit one CTA's shared memory.  Measured on GB300 (8192 x 50257) it
+// is slower than register streaming (230 us against 170 us), so it is not the
+// default.
+bool xent_use_staged(int64_t cols, int max_smem_optin) {
+  const char *e = getenv("FR_XENT_VARIANT");
+  if (e == nullptr || strcmp(e, "staged") != 0) return false;
+  return 128 + 2 * static_cast<size_t>(staged_buf_bytes(cols)) + 4096 <=
+         static_cast<size_t>(max_smem_optin);
+}
+
+cudaError_t launch_xent_staged(const uint16_t *logits, const int64_t *target, float *loss,
+                               float *loss_mean, float *target_logit, int64_t *argmax,
+                               int64_t rows, int64_t cols, int64_t ld, int64_t ignore_index,
+                               void *workspace, int sm_count, cudaStream_t s) {
+  const uint32_t bb = staged_buf_bytes(cols);
+  const size_t smem = 128 + 2 * static_cast<size_t>(bb);
+  const void *kern = argmax != nullptr ? reinterpret_cast<const void *>(&xent_staged<true>)
+                                       : reinterpret_cast<const void *>(&xent_staged<false>);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  int64_t grid = sm_count;  // one CTA per SM (the two buffers fill its shared memory)
+  if (grid > rows) grid = rows;
+  if (loss_mean != nullptr) {
+    e = cudaMemsetAsync(workspace, 0, 16, s);
+    if (e != cudaSuccess) return e;
+  }
+  uint32_t bbv = bb;
+  void *args[] = {&logits, &target, &loss, &target_logit, &argmax, &loss_mean, &workspace,
+                  &rows, &cols, &ld, &ignore_index, &bbv};
+  return cudaLaunchKernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kStThreads), args, smem, s);
+}
+
+struct AsyncVariant {
+  const void *kern, *kern_arg;
+  int threads;
+  size_t smem;
+  int max_per_sm;  // CTAs per SM to launch at most (measured best)
+};
+
+template <int T, int U, int NS>
+AsyncVariant make_async(int max_per_sm) {
+  return AsyncVariant{reinterpret_cast<const void *>(&xent_async<false, T, U, NS>),
+                      reinterpret_cast<const void *>(&xent_async<true, T, U, NS>), T,
+                      static_cast<size_t>(NS) * U * T * 16, max_per_sm};
+}
+
+constexpr int kNumAsync = 7;
+
+// The default launch configuration: measured on GB300 (8192 x 50257 bf16),
+// async2 (256 threads, 4 x 16 bytes per item, 4 stages, 2 CTAs per SM) takes
+// 156 us; async3 159, async5 165, async6 164, async0/1 204, async4 194; the
+// register-streaming variants 169 (0, 4), 183 (1), 192 (2), 195 (5), 224 (3);
+// whole-row bulk-copy staging 230.
+constexpr int kDefaultAsync = 2;
+
+// FR_XENT_VARIANT=async0..async6 selects an asynchronous-copy variant, a bare
+// index a register-streaming one, "staged" the bulk-copy one; unset = default.
+int async_variant() {
+  const char *e = getenv("FR_XENT_VARIANT");
+  if (e == nullptr || e[0] == 0) return kDefaultAsync;
+  if (strncmp(e, "async", 5) != 0) return -1;
+  const int k = atoi(e + 5);
+  return k >= 0 && k < kNumAsync ? k : -1;
+}
+
+cudaError_t launch_xent_async(int which, const uint16_t *logits, const int64_t *target,
+                              float *loss, float *loss_mean, float *target_logit, int64_t *argmax,
+                              int64_t rows, int64_t cols, int64_t ld, int64_t ignore_index,
+                              void *workspace, int sm_count, cudaStream_t s) {
+  static AsyncVariant v[kNumAsync] = {
+      make_async<512, 4, 4>(16), make_async<512, 2, 4>(16), make_async<256, 4, 4>(2),
+      make_async<256, 4, 6>(16), make_async<128, 4, 4>(16), make_async<256, 2, 8>(16),
+      make_async<256, 8, 3>(2)};
+  const AsyncVariant &a = v[which];
+  const void *kern = argmax != nullptr ? a.kern_arg : a.kern;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(a.smem));
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, a.threads, a.smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  if (per_sm > a.max_per_sm) per_sm = a.max_per_sm;
+  if (per_sm > kMaxCtasPerSm) per_sm = kMaxCtasPerSm;
+  int64_t grid = static_cast<int64_t>(sm_count) * per_sm;
+  if (grid > rows) grid = rows;
+  if (loss_mean != nullptr) {
+    e = cudaMemsetAsync(workspace, 0, 16, s);
+    if (e != cudaSuccess) return e;
+  }
+  void *args[] = {&logits, &target, &loss, &target_logit, &argmax, &loss_mean, &workspace,
+                  &rows, &cols, &ld, &ignore_index};
+  return cudaLaunchKernel(kern, dim3(static_cast<unsigned>(grid)), dim3(a.threads), args, a.smem,
+                          s);
 }
 
 cudaError_t launch_xent(const uint16_t *logits, const int64_t *target, float *loss,
                         float *loss_mean, float *target_logit, int64_t *argmax, int64_t rows,
                         int64_t cols, int64_t ld, int64_t ignore_index, void *workspace,
-                        int sm_count, cudaStream_t s) {
+                        int sm_count, int max_smem_optin, cudaStream_t s) {
+  if (const int av = async_variant(); av >= 0)
+    return launch_xent_async(av, logits, target, loss, loss_mean, target_logit, argmax, rows,
+                             cols, ld, ignore_index, workspace, sm_count, s);
+  if (xent_use_staged(cols, max_smem_optin))
+    return launch_xent_staged(logits, target, loss, loss_mean, target_logit, argmax, rows, cols,
+                              ld, ignore_index, workspace, sm_count, s);
   const int grid = xent_grid(rows, sm_count, argmax != nullptr);
   if (loss_mean != nullptr) {
     cudaError_t e = cudaMemsetAsync(workspace, 0, 16, s);
@@ -353,7 +923,7 @@ cudaError_t launch_xent(const uint16_t *logits, const int64_t *target, float *lo
   const XentVariant &v = variants()[chosen_variant()];
   void *args[] = {&logits, &target, &loss, &target_logit, &argmax, &loss_mean, &workspace,
                   &rows, &cols, &ld, &ignore_index};
-  return cudaLaunchKernel(argmax != nullptr ? v.kern_arg : v.kern, dim3(grid), dim3(kThreads),
+  return cudaLaunchKernel(argmax != nullptr ? v.kern_arg : v.kern, dim3(grid), dim3(v.threads),
                           args, 0, s);
 }
 

@@ -222,11 +222,21 @@ def test_layernorm_constant_rows(o):
 
 # ---------------------------------------------------------------- cross entropy
 
-def run_xent(bits, target, ignore=-100, offset=0, pad=0):
+# register streaming (default), whole rows staged by bulk copies, cp.async ring
+XENT_KERNELS = ["0", "staged", "async0", "async1", "async2", "async3", "async4", "async5", "async6"]
+
+
+def run_xent(bits, target, ignore=-100, offset=0, pad=0, kernel="staged", argmax=True):
+    """kernel pins the implementation: "staged" or a register variant index."""
+    import os
     rows, cols = bits.shape
     px = place(bits, offset, cols + pad)
     t = torch.from_numpy(target).cuda()
-    r = fr.fr_xent(px.t, t, ignore, want_target_logit=True, want_argmax=True)
+    os.environ["FR_XENT_VARIANT"] = kernel
+    try:
+        r = fr.fr_xent(px.t, t, ignore, want_target_logit=True, want_argmax=argmax)
+    finally:
+        os.environ.pop("FR_XENT_VARIANT", None)
     torch.cuda.synchronize()
     return {k: v.cpu().numpy() for k, v in r.items()}
 
@@ -236,7 +246,8 @@ def check_xent(got, ref, what):
     assert_close(got["mean"][0], ref["mean"], "loss", f"{what} mean")
     assert_bits_equal(got["target_logit"], ref["target_logit"].astype(np.float32),
                       f"{what} target logit")
-    assert_bits_equal(got["argmax"], ref["argmax"], f"{what} argmax")
+    if "argmax" in got:
+        assert_bits_equal(got["argmax"], ref["argmax"], f"{what} argmax")
 
 
 @pytest.mark.parametrize("cols", [1, 2, 3, 7, 13, 31, 33, 127, 128, 129, 1000, 4097, 50257])
@@ -245,8 +256,11 @@ def check_xent(got, ref, what):
 def test_xent(o, rows, cols, layout):
     w = workloads.make(4, rows=rows, cols=cols, seed=4000 + rows * 7 + cols)
     ref = o.xent(w.arrays["logits"], w.arrays["target"], -100)
-    got = run_xent(w.arrays["logits"], w.arrays["target"], -100, *layout)
-    check_xent(got, ref, f"{rows}x{cols} {layout}")
+    for kernel in XENT_KERNELS:
+        for argmax in (True, False):
+            got = run_xent(w.arrays["logits"], w.arrays["target"], -100, *layout, kernel=kernel,
+                           argmax=argmax)
+            check_xent(got, ref, f"{kernel} argmax={argmax} {rows}x{cols} {layout}")
     assert fr.fr_check_device_error() == 0
 
 
@@ -261,13 +275,15 @@ def test_xent_ties_nan_and_ignore(o):
     t = rng.integers(0, cols, rows)
     t[[1, 2, 3]] = -100
     ref = o.xent(bits, t, -100)
-    got = run_xent(bits, t, -100, offset=1)
-    check_xent(got, ref, "ties/nan")
-    assert got["argmax"][5] == 17 and got["argmax"][6] == 3
-    # every row ignored: mean is 0/0
-    allign = np.full(rows, -100, np.int64)
-    got = run_xent(bits, allign)
-    assert np.isnan(got["mean"][0]) and (got["loss"] == 0).all()
+    for kernel in XENT_KERNELS:
+        for offset in (0, 1):
+            got = run_xent(bits, t, -100, offset=offset, kernel=kernel)
+            check_xent(got, ref, f"ties/nan {kernel} offset {offset}")
+            assert got["argmax"][5] == 17 and got["argmax"][6] == 3
+        # every row ignored: mean is 0/0
+        allign = np.full(rows, -100, np.int64)
+        got = run_xent(bits, allign, kernel=kernel)
+        assert np.isnan(got["mean"][0]) and (got["loss"] == 0).all()
     assert fr.fr_check_device_error() == 0
 
 
@@ -277,11 +293,12 @@ def test_xent_bad_target_sets_device_error(o):
     t[4] = 777          # == cols: out of range
     t[6] = -5           # negative, not ignore_index
     ref = o.xent(w.arrays["logits"], t, -100)
-    got = run_xent(w.arrays["logits"], t)
-    check_xent(got, ref, "bad target")
-    assert np.isnan(got["loss"][[4, 6]]).all()
-    assert fr.fr_check_device_error() == 1
-    assert fr.fr_check_device_error() == 0   # read clears it
+    for kernel in XENT_KERNELS:
+        got = run_xent(w.arrays["logits"], t, kernel=kernel)
+        check_xent(got, ref, f"bad target {kernel}")
+        assert np.isnan(got["loss"][[4, 6]]).all()
+        assert fr.fr_check_device_error() == 1
+        assert fr.fr_check_device_error() == 0   # read clears it
 
 
 # ---------------------------------------------------------------- boundary
