@@ -191,9 +191,18 @@ fr_status fr_softmax(const void *x, void *y, int64_t rows, int64_t cols, int64_t
   float *fy = static_cast<float *>(y);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   switch (f) {
-    case FR_FORM_PERSISTENT:
+    case FR_FORM_PERSISTENT: {
       if (cols > fr::softmax_persistent_max_cols(vec)) return FR_ERR_UNSUPPORTED_FORM;
+      // FR_SOFTMAX_KERNEL=async|plain pins the persistent kernel.  Default:
+      // plain (measured on GB300, fp32 [32768, 1024]: 45.2 us; the per-warp
+      // cp.async ring runs half the warps per SM and takes 49.0 us).
+      const char *pin = getenv("FR_SOFTMAX_KERNEL");
+      const bool use_async = pin != nullptr && strcmp(pin, "async") == 0;
+      const bool aligned16 = aligned(x, 16) && aligned(y, 16) && ldx % 4 == 0 && ldy % 4 == 0;
+      if (use_async && fr::softmax_async_ok(cols, aligned16))
+        return launched(fr::launch_softmax_async(fx, fy, rows, cols, ldx, ldy, info.sm_count, s), f);
       return launched(fr::launch_softmax_persistent(fx, fy, rows, cols, ldx, ldy, vec, s), f);
+    }
     case FR_FORM_LOOPED:
       return launched(fr::launch_softmax_looped(fx, fy, rows, cols, ldx, ldy, vec, info.sm_count, s), f);
     default: return FR_ERR_UNSUPPORTED_FORM;

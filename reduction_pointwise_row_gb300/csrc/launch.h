@@ -40,6 +40,11 @@ cudaError_t launch_ras_split(const float *a, const float *b, float *out, int64_t
 int64_t softmax_persistent_max_cols(bool vec);
 cudaError_t launch_softmax_persistent(const float *x, float *y, int64_t rows, int64_t cols,
                                       int64_t ldx, int64_t ldy, bool vec, cudaStream_t s);
+// Persistent warp-per-row form with a per-warp cp.async ring (16-byte aligned
+// x and y rows, cols <= 1024).
+bool softmax_async_ok(int64_t cols, bool aligned16);
+cudaError_t launch_softmax_async(const float *x, float *y, int64_t rows, int64_t cols,
+                                 int64_t ldx, int64_t ldy, int sm_count, cudaStream_t s);
 cudaError_t launch_softmax_looped(const float *x, float *y, int64_t rows, int64_t cols,
                                   int64_t ldx, int64_t ldy, bool vec, int sm_count,
                                   cudaStream_t s);

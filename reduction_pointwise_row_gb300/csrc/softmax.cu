@@ -247,6 +247,95 @@ softmax_block_looped(const float *__restrict__ x, float *__restrict__ y, int64_t
   }
 }
 
+// Persistent form with asynchronous-copy staging: warp w of the grid owns rows
+// w, w + W, w + 2W, ... (W = warps in the grid) and keeps its next NS - 1 rows
+// in flight in a per-warp shared-memory ring filled with cp.async (16 bytes per
+// lane per copy, one commit group per row), so loads never stop while a row is
+// reduced from registers and stored.  Rows of at most 128 * VPL fp32 with
+// 16-byte aligned starts (x and y); the last cols % 4 elements are scalars.
+constexpr int kAsyncThreads = 256;
+constexpr int kAsyncStages = 3;
+
+template <int VPL>
+__global__ void __launch_bounds__(kAsyncThreads)
+softmax_warp_async(const float *__restrict__ x, float *__restrict__ y, int64_t rows, int64_t cols,
+                   int64_t ldx, int64_t ldy) {
+  extern __shared__ __align__(128) unsigned char smem[];  // [warps][stages][VPL*32] x 16 B
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int kWarps = kAsyncThreads / 32;
+  const int64_t W = static_cast<int64_t>(gridDim.x) * kWarps;
+  const int64_t wg = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+  const int64_t nk = wg < rows ? (rows - wg + W - 1) / W : 0;
+  const int nvec = static_cast<int>(cols >> 2);  // whole 16-byte vectors
+  const int tail = static_cast<int>(cols & 3);
+  unsigned char *wbuf = smem + static_cast<size_t>(warp) * kAsyncStages * VPL * 32 * 16;
+  auto slot = [&](int st, int j) { return wbuf + (static_cast<size_t>(st) * VPL * 32 + j * 32 + lane) * 16; };
+  auto stage = [&](int64_t k) {
+    if (k < nk) {
+      const float *src = x + (wg + k * W) * ldx;
+      const int st = static_cast<int>(k % kAsyncStages);
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) {
+        const int v = j * 32 + lane;
+        if (v < nvec) cp_async_16(slot(st, j), src + 4 * v);
+      }
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int i = 0; i < kAsyncStages - 1; ++i) stage(i);
+  for (int64_t k = 0; k < nk; ++k) {
+    stage(k + kAsyncStages - 1);
+    cp_async_wait<kAsyncStages - 1>();
+    const int64_t row = wg + k * W;
+    const int st = static_cast<int>(k % kAsyncStages);
+    float v[VPL][4];
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      if (j * 32 + lane < nvec) {
+        const uint4 q = lds_u4(slot(st, j));
+        v[j][0] = __uint_as_float(q.x); v[j][1] = __uint_as_float(q.y);
+        v[j][2] = __uint_as_float(q.z); v[j][3] = __uint_as_float(q.w);
+      } else {
+        v[j][0] = v[j][1] = v[j][2] = v[j][3] = -INFINITY;
+      }
+    }
+    float sv = -INFINITY;  // tail scalar (at most 3, one per lane)
+    if (lane < tail) sv = ld_stream_f32(x + row * ldx + 4 * nvec + lane);
+    float m = sv;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) m = max_nan(m, v[j][e]);
+    m = warp_max_nan(m);
+    const float mb = m * kLog2e;
+    float d = 0.0f;
+    float se = lane < tail ? ex2(fmaf(sv, kLog2e, -mb)) : 0.0f;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j)
+      if (j * 32 + lane < nvec) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          v[j][e] = ex2(fmaf(v[j][e], kLog2e, -mb));
+          d += v[j][e];
+        }
+      }
+    d = warp_sum(d + se);
+    const float inv = __frcp_rn(d);
+    float *py = y + row * ldy;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      const int vv = j * 32 + lane;
+      if (vv < nvec)
+        asm volatile("st.global.cs.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(py + 4 * vv),
+                     "f"(v[j][0] * inv), "f"(v[j][1] * inv), "f"(v[j][2] * inv), "f"(v[j][3] * inv)
+                     : "memory");
+    }
+    if (lane < tail) st_stream_f32(py + 4 * nvec + lane, se * inv);
+  }
+  cp_async_wait<0>();
+}
+
 unsigned warp_row_grid(int64_t rows) {
   return static_cast<unsigned>((rows + kWarpRowThreads / 32 - 1) / (kWarpRowThreads / 32));
 }
@@ -275,6 +364,41 @@ cudaError_t launch_softmax_persistent(const float *x, float *y, int64_t rows, in
     else return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
+}
+
+bool softmax_async_ok(int64_t cols, bool aligned16) { return aligned16 && cols <= 1024; }
+
+cudaError_t launch_softmax_async(const float *x, float *y, int64_t rows, int64_t cols,
+                                 int64_t ldx, int64_t ldy, int sm_count, cudaStream_t s) {
+  const int vpl = static_cast<int>((cols / 4 + 31) / 32);
+  const void *kern;
+  switch (vpl) {
+    case 0:
+    case 1: kern = reinterpret_cast<const void *>(&softmax_warp_async<1>); break;
+    case 2: kern = reinterpret_cast<const void *>(&softmax_warp_async<2>); break;
+    case 3:
+    case 4: kern = reinterpret_cast<const void *>(&softmax_warp_async<4>); break;
+    case 5:
+    case 6:
+    case 7:
+    case 8: kern = reinterpret_cast<const void *>(&softmax_warp_async<8>); break;
+    default: return cudaErrorInvalidValue;
+  }
+  const int vp = vpl <= 1 ? 1 : vpl <= 2 ? 2 : vpl <= 4 ? 4 : 8;
+  const size_t smem = static_cast<size_t>(kAsyncThreads / 32) * kAsyncStages * vp * 32 * 16;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kAsyncThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  int64_t grid = static_cast<int64_t>(sm_count) * per_sm;
+  const int64_t need = (rows + kAsyncThreads / 32 - 1) / (kAsyncThreads / 32);
+  if (grid > need) grid = need;
+  void *args[] = {&x, &y, &rows, &cols, &ldx, &ldy};
+  return cudaLaunchKernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kAsyncThreads), args, smem,
+                          s);
 }
 
 cudaError_t launch_softmax_looped(const float *x, float *y, int64_t rows, int64_t cols,

@@ -109,12 +109,19 @@ def test_relu_add_sum_scale_and_infinities(o):
 
 # ---------------------------------------------------------------- softmax
 
-def run_softmax(x, form, layout=(0, 0, 0)):
+def run_softmax(x, form, layout=(0, 0, 0), kernel=None):
+    """kernel pins the persistent kernel: "async" (cp.async ring) or "plain"."""
+    import os
     rows, cols = x.shape
     ox, oy, pad = layout
     px = place(x, ox, cols + pad)
     py = empty_like_placed(rows, cols, torch.float32, oy, cols + pad)
-    fr.fr_softmax(px.t, form=form, out=py.t)
+    if kernel:
+        os.environ["FR_SOFTMAX_KERNEL"] = kernel
+    try:
+        fr.fr_softmax(px.t, form=form, out=py.t)
+    finally:
+        os.environ.pop("FR_SOFTMAX_KERNEL", None)
     torch.cuda.synchronize()
     assert py.canaries_intact(), "softmax wrote outside y"
     return py.t.cpu().numpy()
@@ -127,8 +134,23 @@ def test_softmax_forms(o, rows, cols, layout):
     w = workloads.make(1, rows=rows, cols=cols, seed=2000 + rows * 7 + cols)
     ref = o.softmax(w.arrays["x"])
     for form in forms_for("softmax", cols):
-        assert_close(run_softmax(w.arrays["x"], form, layout), ref, "f32",
-                     f"{form} {rows}x{cols} {layout}")
+        for kernel in (("async", "plain") if form == "persistent" else (None,)):
+            assert_close(run_softmax(w.arrays["x"], form, layout, kernel), ref, "f32",
+                         f"{form}/{kernel} {rows}x{cols} {layout}")
+
+
+@pytest.mark.parametrize("cols", [c for c in COLS if c <= 1024])
+@pytest.mark.parametrize("rows", [1, 9, 300, 2500])
+def test_softmax_persistent_aligned_rows_with_tails(o, rows, cols):
+    """16-byte aligned rows whose length is not a multiple of 4 (row stride
+    padded to a multiple of 4): the cp.async persistent kernel's tail path,
+    and more rows than the persistent grid has warps."""
+    w = workloads.make(1, rows=rows, cols=cols, seed=2500 + rows + cols)
+    ref = o.softmax(w.arrays["x"])
+    pad = (-cols) % 4 + 4
+    for kernel in ("async", "plain"):
+        assert_close(run_softmax(w.arrays["x"], "persistent", (0, 0, pad), kernel), ref, "f32",
+                     f"{kernel} {rows}x{cols}")
 
 
 @pytest.mark.parametrize("cols", [5, 1000, 4097])
