@@ -98,8 +98,8 @@ fr_form pick_softmax(int64_t, int64_t cols, bool vec) {
 
 fr_form pick_layernorm(int64_t, int64_t cols, bool vec, int max_smem_optin) {
   // Measured on GB300, bf16 [4096, 32768]: looped cp.async ring (two rows per
-  // gamma/beta pass) 156 us, persistent 193 us, looped cluster (gamma/beta in
-  // shared memory) 214 us, looped scalar 265 us.
+  // gamma/beta pass) 137 us, persistent 168 us, looped cluster (gamma/beta in
+  // shared memory) 182 us, looped scalar 265 us.
   if (fr::layernorm_ring_ok(cols, vec, max_smem_optin)) return FR_FORM_LOOPED;
   return fr::layernorm_persistent_ok(cols, vec) ? FR_FORM_PERSISTENT : FR_FORM_LOOPED;
 }
