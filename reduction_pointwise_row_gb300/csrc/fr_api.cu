@@ -97,9 +97,10 @@ fr_form pick_softmax(int64_t, int64_t cols, bool vec) {
 }
 
 fr_form pick_layernorm(int64_t, int64_t cols, bool vec, int max_smem_optin) {
-  // Measured on GB300, bf16 [4096, 32768]: looped cp.async ring (two rows per
-  // gamma/beta pass) 137 us, persistent 168 us, looped cluster (gamma/beta in
-  // shared memory) 182 us, looped scalar 265 us.
+  // Measured on GB300, bf16 [4096, 32768]: looped cluster (gamma/beta in
+  // registers, rows split over a 2-CTA cluster) 132 us, looped cp.async ring
+  // (two rows per gamma/beta pass) 137 us, persistent 168 us, looped scalar
+  // 265 us.  The looped form tries cluster, then ring, then scalar.
   if (fr::layernorm_ring_ok(cols, vec, max_smem_optin)) return FR_FORM_LOOPED;
   return fr::layernorm_persistent_ok(cols, vec) ? FR_FORM_PERSISTENT : FR_FORM_LOOPED;
 }
@@ -238,16 +239,16 @@ fr_status fr_layernorm(const void *x, const float *gamma, const float *beta, voi
     case FR_FORM_LOOPED: {
       // FR_LAYERNORM_KERNEL=cluster|ring|scalar pins one looped kernel (for
       // re-measuring the choice and for tests); unset = the first that fits.
-      // Preference (measured): staged ring, then scalar, then cluster.
+      // Preference (measured): cluster, then staged ring, then scalar.
       const char *pin = getenv("FR_LAYERNORM_KERNEL");
       const bool any = pin == nullptr || pin[0] == 0;
+      if ((any || strcmp(pin, "cluster") == 0) && fr::layernorm_cluster_ok(cols, aligned16))
+        return launched(fr::launch_layernorm_cluster(bx, gamma, beta, by, mean, rstd, rows, cols,
+                                                     ldx, ldy, eps, s), f);
       if ((any || strcmp(pin, "ring") == 0) && fr::layernorm_ring_ok(cols, vec, info.max_smem_optin))
         return launched(fr::launch_layernorm_ring(bx, gamma, beta, by, mean, rstd, rows, cols,
                                                   ldx, ldy, eps, info.sm_count,
                                                   info.max_smem_optin, s), f);
-      if (!any && strcmp(pin, "cluster") == 0 && fr::layernorm_cluster_ok(cols, aligned16))
-        return launched(fr::launch_layernorm_cluster(bx, gamma, beta, by, mean, rstd, rows, cols,
-                                                     ldx, ldy, eps, s), f);
       return launched(fr::launch_layernorm_looped(bx, gamma, beta, by, mean, rstd, rows, cols, ldx,
                                                   ldy, eps, vec, info.sm_count,
                                                   info.max_smem_optin, s), f);

@@ -17,6 +17,7 @@
 //             in chunks merging Welford triples, pass 2 streams it again
 //             (from L2) to write y.  Any alignment (scalar lane-strided).
 #include <cstdlib>
+#include <cstring>
 
 #include "common.cuh"
 #include "launch.h"
@@ -219,22 +220,37 @@ __device__ __forceinline__ void block_welford_n(Welford (&w)[R], Welford (*smem)
   __syncthreads();
 }
 
-template <int R>
+// BULK: stage each row with one bulk asynchronous copy completing on an
+// mbarrier (the copy writes shared memory without the load/store path that
+// per-thread copies occupy) instead of per-thread cp.async.
+template <int R, bool BULK>
 __global__ void __launch_bounds__(kRingThreads, 1)
 layernorm_ring(const uint16_t *__restrict__ x, const float *__restrict__ gamma,
                const float *__restrict__ beta, uint16_t *__restrict__ y,
                float *__restrict__ mean_out, float *__restrict__ rstd_out, int64_t rows,
-               int64_t cols, int64_t ldx, int64_t ldy, float eps) {
+               int64_t cols, int64_t ldx, int64_t ldy, float eps, int *__restrict__ err) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ Welford red[R][32];
+  __shared__ __align__(8) uint64_t full[kRingBufs];
+  __shared__ int timed_out;
   const int tid = threadIdx.x;
   const int npieces = static_cast<int>(cols >> 4);  // cols % 16 == 0
   const size_t buf_bytes = static_cast<size_t>(npieces) * 32;
   const int64_t G = gridDim.x;
   // rows of this CTA: blockIdx.x + k * G for k < nk
   const int64_t nk = blockIdx.x < rows ? (rows - blockIdx.x + G - 1) / G : 0;
+  const uint64_t policy = l2_evict_first_policy();
 
+  auto stage_bulk = [&](int64_t k) {  // thread 0: row k into buffer k % kRingBufs
+    if (k < nk) {
+      const int b = static_cast<int>(k % kRingBufs);
+      mbar_arrive_expect_tx(&full[b], static_cast<uint32_t>(buf_bytes));
+      bulk_copy_g2s(smem + static_cast<size_t>(b) * buf_bytes, x + (blockIdx.x + k * G) * ldx,
+                    static_cast<uint32_t>(buf_bytes), &full[b], policy);
+    }
+  };
   auto stage = [&](int64_t k) {  // this thread's pieces of row k into buffer k % kRingBufs
+    if constexpr (BULK) return;
     if (k < nk) {
       const unsigned char *src = reinterpret_cast<const unsigned char *>(x + (blockIdx.x + k * G) * ldx);
       unsigned char *dst = smem + static_cast<size_t>(k % kRingBufs) * buf_bytes;
@@ -250,16 +266,36 @@ layernorm_ring(const uint16_t *__restrict__ x, const float *__restrict__ gamma,
     cp_async_commit();  // one group per row index, empty past the last row
   };
 
-  for (int b = 0; b < kRingBufs; ++b) stage(b);
+  if constexpr (BULK) {
+    if (tid == 0) {
+      timed_out = 0;
+      for (int b = 0; b < kRingBufs; ++b) mbar_init(&full[b], 1);
+      mbar_init_fence();
+      for (int b = 0; b < kRingBufs; ++b) stage_bulk(b);
+    }
+    __syncthreads();
+  } else {
+    for (int b = 0; b < kRingBufs; ++b) stage(b);
+  }
   int64_t next = kRingBufs;  // next row index to stage
   for (int64_t k0 = 0; k0 < nk; k0 += R) {
     V8 v[R][kRingPieces];
     Welford w[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      // Groups committed so far: rows 0 .. next - 1 = k0 + r + kRingBufs - 1.
-      // Row k0 + r has landed once at most the kRingBufs - 1 newer ones pend.
-      cp_async_wait<kRingBufs - 1>();
+      if constexpr (BULK) {
+        const int64_t kk = k0 + r;
+        if (kk < nk && !timed_out &&
+            !mbar_wait_bounded(&full[kk % kRingBufs], static_cast<uint32_t>((kk / kRingBufs) & 1),
+                               1LL << 31)) {
+          timed_out = 1;
+          atomicCAS(err, 0, FR_DEVERR_TIMEOUT);
+        }
+      } else {
+        // Groups committed so far: rows 0 .. next - 1 = k0 + r + kRingBufs - 1.
+        // Row k0 + r has landed once at most the kRingBufs - 1 newer ones pend.
+        cp_async_wait<kRingBufs - 1>();
+      }
       w[r] = Welford{0.0f, 0.0f, 0.0f};
       const unsigned char *buf = smem + static_cast<size_t>((k0 + r) % kRingBufs) * buf_bytes;
 #pragma unroll
@@ -273,6 +309,15 @@ layernorm_ring(const uint16_t *__restrict__ x, const float *__restrict__ gamma,
       stage(next++);  // buffer of row k0 + r is in registers: refill it
     }
     block_welford_n<R>(w, red);
+    if constexpr (BULK) {
+      // every thread has read the R buffers (the reduction's barriers lie
+      // between): refill them with the next rows
+      if (tid == 0 && !timed_out) {
+        fence_proxy_async_smem();
+#pragma unroll
+        for (int r = 0; r < R; ++r) stage_bulk(next - R + r);
+      }
+    }
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const int64_t row = blockIdx.x + (k0 + r) * G;
@@ -312,151 +357,155 @@ layernorm_ring(const uint16_t *__restrict__ x, const float *__restrict__ gamma,
     }
   }
   cp_async_wait<0>();  // no copy may still target this CTA's shared memory
+  if constexpr (BULK) {
+    __syncthreads();
+    if (tid == 0 && timed_out)  // last bounded wait on copies that may be in flight
+      for (int b = 0; b < kRingBufs; ++b) mbar_wait_bounded(&full[b], 0, 1LL << 31);
+  }
 }
 
 constexpr long long kWaitBudget = 1LL << 31;  // SM clocks (about one second) per wait
 
-// ---- cluster form: gamma/beta resident in shared memory -----------------------
+// ---- cluster form: gamma/beta resident in registers -----------------------------
 // A cluster of C CTAs (C = 1 or 2) splits every row into C column slices of
-// S = cols / C <= 16384.  Each CTA keeps the gamma/beta of its slice in shared
-// memory for the whole kernel (S * 8 <= 128 KiB) and streams x through a ring
-// of kClBufs slice buffers filled with per-thread cp.async copies, kClBufs rows
-// (a wave) at a time: pass 1 lifts the wave's x into registers (thread t owns
-// the 16 columns 16t .. 16t + 15 of the slice) and refills the ring at once;
-// one CTA merge reduces the wave's Welford triples; warp 0 pushes them into
-// every CTA of the cluster (st.async, counted on the receiver's mbarrier); each
-// CTA merges the C triples of a row in rank order (the same bits everywhere)
-// and normalises the wave from registers, reading each gamma/beta value from
-// shared memory once per wave.  HBM sees x once and y once; gamma/beta are
-// read from HBM once per CTA.
-constexpr int kClThreads = 1024;
-constexpr int kClBufs = 3;        // rows per wave = slice buffers in the ring
-constexpr int kClSlots = 4;       // published triples: wave w + 4 is written
-                                  // only after this CTA published wave w + 1
+// S = cols / C <= 16384; thread t of CTA rank q owns the 32 columns
+// q*S + 32t .. + 31 for the whole kernel, so its 32 gamma and 32 beta values
+// live in registers and per row only x comes in and y goes out -- no per-row
+// re-read of the fp32 gamma/beta (4x the bytes of x).  Each thread streams its
+// 64-byte pieces of the cluster's rows through a kClStages-deep cp.async ring
+// (no barrier: every thread reads back exactly what it copied).  Per row:
+// Welford triple of 32 elements -> warp -> CTA (warp 0) -> pushed into every
+// CTA of the cluster (st.async, counted on the receiver's mbarrier).  Row k is
+// published before row k - 1 is finalised (merge of the C triples in rank
+// order, identical in every CTA, then normalisation of the x held in
+// registers), so the exchange latency overlaps the next row's work.
+constexpr int kClThreads = 512;
+constexpr int kClCols = 32;      // columns per thread
+constexpr int kClStages = 4;     // rows in the cp.async ring
+constexpr int kClSlots = 4;      // triple slots: a peer writes row k + 4 only after
+                                 // this CTA published row k + 2, i.e. after it
+                                 // finalised row k
 constexpr int kClMaxCluster = 2;
-constexpr int64_t kClMaxSlice = 16 * kClThreads;  // 16384 columns
+constexpr int64_t kClMaxSlice = static_cast<int64_t>(kClCols) * kClThreads;  // 16384
 
 __global__ void __launch_bounds__(kClThreads, 1)
 layernorm_cluster(const uint16_t *__restrict__ x, const float *__restrict__ gamma,
                   const float *__restrict__ beta, uint16_t *__restrict__ y,
                   float *__restrict__ mean_out, float *__restrict__ rstd_out, int64_t rows,
                   int64_t cols, int64_t ldx, int64_t ldy, float eps, int *__restrict__ err) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ __align__(16) float4 slot[kClSlots][kClBufs][kClMaxCluster];  // [wave%4][row][rank]
+  extern __shared__ __align__(128) unsigned char smem[];  // [kClStages][T] x 64 bytes
+  __shared__ __align__(16) float4 slot[kClSlots][kClMaxCluster];  // [row % 4][rank]
   __shared__ __align__(8) uint64_t pbar[kClSlots];
-  __shared__ Welford red[kClBufs][32];
+  __shared__ Welford red[2][32];  // per-warp triples, double-buffered by row
   __shared__ int timed_out;
 
   const uint32_t C = cluster_nctarank(), q = cluster_ctarank();
   const int64_t cid = cluster_id_x(), ncl = ncluster_x();
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t S = cols / C;
-  const int npieces = static_cast<int>(S >> 4);        // 16 columns per piece, <= 1024
-  const bool own = tid < npieces;
-  const int64_t c0 = static_cast<int64_t>(q) * S;       // first column of the slice
-  const int64_t col0 = c0 + 16 * static_cast<int64_t>(tid);
-  float *sg = reinterpret_cast<float *>(smem);          // gamma[S], beta[S]
-  float *sb = sg + S;
-  unsigned char *ring = smem + static_cast<size_t>(S) * 8;
-  const size_t buf_bytes = static_cast<size_t>(S) * 2;
+  const bool own = static_cast<int64_t>(kClCols) * tid < S;
+  const int64_t col0 = static_cast<int64_t>(q) * S + static_cast<int64_t>(kClCols) * tid;
   const int64_t nr = cid < rows ? (rows - cid + ncl - 1) / ncl : 0;  // rows of this cluster
-  const int64_t nwaves = (nr + kClBufs - 1) / kClBufs;
-  const uint32_t part_bytes = 16u * kClBufs * C;
+  const uint32_t part_bytes = 16u * C;
 
-  // gamma/beta of the slice into shared memory (once)
-  for (int64_t i = tid; i < S / 4; i += kClThreads) {
-    reinterpret_cast<float4 *>(sg)[i] = ld_keep_f4(gamma + c0 + 4 * i);
-    reinterpret_cast<float4 *>(sb)[i] = ld_keep_f4(beta + c0 + 4 * i);
+  float g[kClCols], b[kClCols];
+  if (own) {
+#pragma unroll
+    for (int h = 0; h < kClCols / 4; ++h) {
+      const float4 gv = ld_keep_f4(gamma + col0 + 4 * h), bv = ld_keep_f4(beta + col0 + 4 * h);
+      g[4 * h] = gv.x; g[4 * h + 1] = gv.y; g[4 * h + 2] = gv.z; g[4 * h + 3] = gv.w;
+      b[4 * h] = bv.x; b[4 * h + 1] = bv.y; b[4 * h + 2] = bv.z; b[4 * h + 3] = bv.w;
+    }
   }
-  auto stage = [&](int64_t k) {  // row k of this cluster into buffer k % kClBufs
+  auto row_of = [&](int64_t k) { return cid + k * ncl; };
+  auto piece = [&](int64_t k) {
+    return smem + (static_cast<size_t>(k % kClStages) * kClThreads + tid) * 64;
+  };
+  auto stage = [&](int64_t k) {  // this thread's 64 bytes of row k
     if (k < nr && own) {
-      const unsigned char *src =
-          reinterpret_cast<const unsigned char *>(x + (cid + k * ncl) * ldx + col0);
-      unsigned char *dst = ring + static_cast<size_t>(k % kClBufs) * buf_bytes + 32 * tid;
-      cp_async_16(dst, src);
-      cp_async_16(dst + 16, src + 16);
+      const uint16_t *src = x + row_of(k) * ldx + col0;
+      unsigned char *dst = piece(k);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) cp_async_16(dst + 16 * c, src + 8 * c);
     }
     cp_async_commit();
   };
+
   if (tid == 0) {
     timed_out = 0;
     for (int i = 0; i < kClSlots; ++i) mbar_init(&pbar[i], 1);
     mbar_init_fence();
-    for (int64_t w = 0; w < kClSlots && w < nwaves; ++w) mbar_arrive_expect_tx(&pbar[w], part_bytes);
+    for (int64_t k = 0; k < kClSlots && k < nr; ++k) mbar_arrive_expect_tx(&pbar[k], part_bytes);
   }
-  for (int b = 0; b < kClBufs; ++b) stage(b);
-  // gamma/beta and the barriers are ready in every CTA before anyone sends
+  for (int i = 0; i < kClStages - 1; ++i) stage(i);
   __syncthreads();
-  cluster_arrive();
+  cluster_arrive();  // every CTA's barriers are armed before anyone sends
   cluster_wait();
 
-  int64_t next = kClBufs;
-  for (int64_t wv = 0; wv < nwaves; ++wv) {
-    const int64_t k0 = wv * kClBufs;
-    V8 v[kClBufs];
-    Welford w[kClBufs];
-#pragma unroll
-    for (int r = 0; r < kClBufs; ++r) {
-      cp_async_wait<kClBufs - 1>();  // row k0 + r landed (the newer rows may pend)
-      w[r] = Welford{0.0f, 0.0f, 0.0f};
-      if (own && k0 + r < nr) {
-        v[r] = lds_v8(ring + static_cast<size_t>((k0 + r) % kClBufs) * buf_bytes + 32 * tid);
-        w[r] = welford16(v[r]);
+  V8 xa[2], xb[2];  // rows k (current) and k - 1 (being finalised): 32 bf16 each
+  for (int64_t k = 0; k <= nr; ++k) {
+    if (k < nr) {
+      stage(k + kClStages - 1);
+      cp_async_wait<kClStages - 1>();  // row k landed
+      Welford w{0.0f, 0.0f, 0.0f};
+      if (own) {
+        xa[0] = lds_v8(piece(k));
+        xa[1] = lds_v8(piece(k) + 32);
+        w = chan_merge(welford16(xa[0]), welford16(xa[1]));
       }
-      stage(next++);  // the row is in registers: refill its buffer
-    }
-    block_welford_n<kClBufs>(w, red);  // w[r] = this CTA's triple of row k0 + r
-    const int sl = static_cast<int>(wv % kClSlots);
-    if (tid < kClBufs * static_cast<int>(C)) {  // lanes of warp 0: (row, destination rank)
-      const int r = tid / static_cast<int>(C), k = tid % static_cast<int>(C);
-      Welford m = w[0];
-      if (r == 1) m = w[1];
-      if (r == 2) m = w[2];
-      st_async_f4(&slot[sl][r][q], &pbar[sl], static_cast<uint32_t>(k),
-                  make_float4(m.n, m.mean, m.m2, 0.0f));
-    }
-    if (!timed_out &&
-        !mbar_wait_bounded(&pbar[sl], static_cast<uint32_t>((wv / kClSlots) & 1), 1LL << 31)) {
-      timed_out = 1;
-      atomicCAS(err, 0, FR_DEVERR_TIMEOUT);
-    }
-    float mean[kClBufs], rstd[kClBufs];
-#pragma unroll
-    for (int r = 0; r < kClBufs; ++r) {
-      Welford t{0.0f, 0.0f, 0.0f};
-      for (uint32_t k = 0; k < C; ++k) {  // rank order: identical in every CTA
-        const float4 u = slot[sl][r][k];
-        t = chan_merge(t, Welford{u.x, u.y, u.z});
-      }
-      mean[r] = t.mean;
-      rstd[r] = rsqrtf(fmaf(t.m2, __frcp_rn(t.n), eps));
-      const int64_t row = cid + (k0 + r) * ncl;
-      if (q == 0 && tid == 0 && k0 + r < nr) {
-        if (mean_out) mean_out[row] = mean[r];
-        if (rstd_out) rstd_out[row] = rstd[r];
-      }
-    }
-    // Re-arm the slot for wave wv + 4: peers write it only after this CTA
-    // publishes wave wv + 1, which every thread reaches after this point.
-    if (tid == 0 && wv + kClSlots < nwaves) mbar_arrive_expect_tx(&pbar[sl], part_bytes);
-    if (own) {
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {  // 4 columns of gamma/beta at a time, shared by the wave
-        const float4 g = *reinterpret_cast<const float4 *>(sg + 16 * tid + 4 * h);
-        const float4 bb = *reinterpret_cast<const float4 *>(sb + 16 * tid + 4 * h);
-#pragma unroll
-        for (int r = 0; r < kClBufs; ++r) {
-          const uint32_t w0 = v[r].w[2 * h], w1 = v[r].w[2 * h + 1];
-          v[r].w[2 * h] = pack_bf16x2(fmaf((bf16_lo(w0) - mean[r]) * rstd[r], g.x, bb.x),
-                                      fmaf((bf16_hi(w0) - mean[r]) * rstd[r], g.y, bb.y));
-          v[r].w[2 * h + 1] = pack_bf16x2(fmaf((bf16_lo(w1) - mean[r]) * rstd[r], g.z, bb.z),
-                                          fmaf((bf16_hi(w1) - mean[r]) * rstd[r], g.w, bb.w));
+      w = warp_welford(w);
+      if (lane == 0) red[k & 1][warp] = w;
+      __syncthreads();
+      if (warp == 0) {  // only warp 0 needs the CTA's triple
+        Welford m = lane < kClThreads / 32 ? red[k & 1][lane] : Welford{0.0f, 0.0f, 0.0f};
+        m = warp_welford(m);
+        if (lane < static_cast<int>(C)) {
+          const int sl = static_cast<int>(k % kClSlots);
+          st_async_f4(&slot[sl][q], &pbar[sl], static_cast<uint32_t>(lane),
+                      make_float4(m.n, m.mean, m.m2, 0.0f));
         }
       }
-#pragma unroll
-      for (int r = 0; r < kClBufs; ++r)
-        if (k0 + r < nr) st_stream_v8(y + (cid + (k0 + r) * ncl) * ldy + col0, v[r]);
     }
+    if (k > 0) {  // finalise row k - 1 with the x held in xb
+      const int64_t kp = k - 1;
+      const int sl = static_cast<int>(kp % kClSlots);
+      if (!timed_out &&
+          !mbar_wait_bounded(&pbar[sl], static_cast<uint32_t>((kp / kClSlots) & 1), 1LL << 31)) {
+        timed_out = 1;
+        atomicCAS(err, 0, FR_DEVERR_TIMEOUT);
+      }
+      const float4 u0 = slot[sl][0];
+      Welford t{u0.x, u0.y, u0.z};
+      if (C == 2) {  // rank order: identical in every CTA
+        const float4 u1 = slot[sl][1];
+        t = chan_merge(t, Welford{u1.x, u1.y, u1.z});
+      }
+      // Re-arm slot sl for row kp + 4 (peers send it only after this CTA
+      // publishes row kp + 2, which comes after this point).
+      if (tid == 0 && kp + kClSlots < nr) mbar_arrive_expect_tx(&pbar[sl], part_bytes);
+      const int64_t row = row_of(kp);
+      const float mean = t.mean;
+      const float rstd = rsqrtf(fmaf(t.m2, __frcp_rn(t.n), eps));
+      if (q == 0 && tid == 0) {
+        if (mean_out) mean_out[row] = mean;
+        if (rstd_out) rstd_out[row] = rstd;
+      }
+      if (own) {
+#pragma unroll
+        for (int hv = 0; hv < 2; ++hv) {
+          V8 o;
+#pragma unroll
+          for (int h = 0; h < 8; ++h) {
+            const int c = 16 * hv + 2 * h;
+            o.w[h] = pack_bf16x2(fmaf((bf16_lo(xb[hv].w[h]) - mean) * rstd, g[c], b[c]),
+                                 fmaf((bf16_hi(xb[hv].w[h]) - mean) * rstd, g[c + 1], b[c + 1]));
+          }
+          st_stream_v8(y + row * ldy + col0 + 16 * hv, o);
+        }
+      }
+    }
+    xb[0] = xa[0];
+    xb[1] = xa[1];
   }
   cp_async_wait<0>();
   // No CTA may leave while a peer can still write into its shared memory.
@@ -466,16 +515,16 @@ layernorm_cluster(const uint16_t *__restrict__ x, const float *__restrict__ gamm
 
 }  // namespace
 
-// Cluster size: 1 when gamma/beta of the whole row fit one CTA, else 2.
+// Cluster size: the smallest C in {1, 2} with slices of at most 16384
+// columns (32 columns per thread).
 int cluster_size_for(int64_t cols) {
   for (int c = 1; c <= kClMaxCluster; c <<= 1)
-    if (cols % (16 * c) == 0 && cols / c <= kClMaxSlice) return c;
+    if (cols % (kClCols * c) == 0 && cols / c <= kClMaxSlice) return c;
   return 0;
 }
 
-size_t cluster_smem(int64_t cols, int c) {
-  const int64_t S = cols / c;
-  return static_cast<size_t>(S) * 8 + static_cast<size_t>(kClBufs) * S * 2;
+size_t cluster_smem(int64_t, int) {
+  return static_cast<size_t>(kClStages) * kClThreads * 64;  // the cp.async ring
 }
 
 bool layernorm_cluster_ok(int64_t cols, bool aligned) {
@@ -540,8 +589,17 @@ cudaError_t launch_layernorm_ring(const uint16_t *x, const float *gamma, const f
     const int v = atoi(e);
     if (v >= 1 && v <= 2) R = v;
   }
-  const void *kern = R == 1 ? reinterpret_cast<const void *>(&layernorm_ring<1>)
-                            : reinterpret_cast<const void *>(&layernorm_ring<2>);
+  // FR_LAYERNORM_STAGE=bulk stages rows with one bulk copy each (default:
+  // per-thread cp.async).
+  const char *st = getenv("FR_LAYERNORM_STAGE");
+  const bool bulk = st != nullptr && strcmp(st, "bulk") == 0;
+  const void *kern =
+      R == 1 ? (bulk ? reinterpret_cast<const void *>(&layernorm_ring<1, true>)
+                     : reinterpret_cast<const void *>(&layernorm_ring<1, false>))
+             : (bulk ? reinterpret_cast<const void *>(&layernorm_ring<2, true>)
+                     : reinterpret_cast<const void *>(&layernorm_ring<2, false>));
+  int *err = nullptr;
+  if (cudaError_t ee = device_error_word(&err); ee != cudaSuccess) return ee;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -551,7 +609,7 @@ cudaError_t launch_layernorm_ring(const uint16_t *x, const float *gamma, const f
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   int64_t grid = static_cast<int64_t>(sm_count) * per_sm;
   if (grid > rows) grid = rows;
-  void *args[] = {&x, &gamma, &beta, &y, &mean, &rstd, &rows, &cols, &ldx, &ldy, &eps};
+  void *args[] = {&x, &gamma, &beta, &y, &mean, &rstd, &rows, &cols, &ldx, &ldy, &eps, &err};
   return cudaLaunchKernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kRingThreads), args, smem,
                           s);
 }

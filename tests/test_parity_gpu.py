@@ -181,8 +181,13 @@ def test_softmax_in_place_and_rows_sum_to_one(o):
 # ---------------------------------------------------------------- LayerNorm
 
 def run_layernorm(x_bits, gamma, beta, eps, form, offset=0, kernel=None):
-    """kernel pins the looped form's kernel (cluster, ring or scalar)."""
+    """kernel pins the looped form's kernel: cluster, ring, ring-bulk (rows
+    staged by bulk copies) or scalar."""
     import os
+    os.environ.pop("FR_LAYERNORM_STAGE", None)
+    if kernel == "ring-bulk":
+        kernel = "ring"
+        os.environ["FR_LAYERNORM_STAGE"] = "bulk"
     if kernel:
         os.environ["FR_LAYERNORM_KERNEL"] = kernel
     else:
@@ -197,6 +202,7 @@ def run_layernorm(x_bits, gamma, beta, eps, form, offset=0, kernel=None):
         fr.fr_layernorm(px.t, g, b, eps, form=form, out=py.t, mean=mean, rstd=rstd)
     finally:
         os.environ.pop("FR_LAYERNORM_KERNEL", None)
+        os.environ.pop("FR_LAYERNORM_STAGE", None)
     torch.cuda.synchronize()
     assert py.canaries_intact(), "layernorm wrote outside y"
     return bf16_to_f32_host(py.t), mean.cpu().numpy(), rstd.cpu().numpy()
@@ -212,7 +218,7 @@ def test_layernorm_forms(o, rows, cols, offset):
     ry, rm, rr = o.layernorm(w.arrays["x"], w.arrays["gamma"], w.arrays["beta"], eps)
     vec_ok = offset == 0 and cols % 16 == 0 and cols <= 32768
     runs = ([("persistent", None)] if vec_ok else []) + \
-        [("looped", k) for k in ("cluster", "ring", "scalar")]
+        [("looped", k) for k in ("cluster", "ring", "ring-bulk", "scalar")]
     for form, kernel in runs:
         y, m, r = run_layernorm(w.arrays["x"], w.arrays["gamma"], w.arrays["beta"], eps, form,
                                 offset, kernel)
@@ -235,7 +241,7 @@ def test_layernorm_constant_rows(o):
     eps = float(np.float32(1e-5))
     ry, rm, rr = o.layernorm(x, gamma, beta, eps)
     for form, kernel in (("persistent", None), ("looped", "cluster"), ("looped", "ring"),
-                         ("looped", "scalar")):
+                         ("looped", "ring-bulk"), ("looped", "scalar")):
         y, m, r = run_layernorm(x, gamma, beta, eps, form, kernel=kernel)
         assert_close(y, ry, "bf16", f"{form}/{kernel}")
         assert (m == 3.5).all()
