@@ -54,13 +54,15 @@ class Oracle:
         lib.oracle_planted.restype = ctypes.c_int
         lib.oracle_relu_add_sum.argtypes = [vp, vp, i64, i64, i64, i64, f32, vp]
         lib.oracle_row_sumsq.argtypes = [vp, i64, i64, i64, vp]
+        lib.oracle_row_l2norm.argtypes = [vp, i64, i64, i64, vp]
         lib.oracle_softmax.argtypes = [vp, i64, i64, i64, vp]
         lib.oracle_md_merge.argtypes = [f64, f64, f64, f64, vp, vp]
         lib.oracle_md_fold.argtypes = [vp, i64, vp, vp]
         lib.oracle_online_attn_row.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp, vp, vp, vp]
         lib.oracle_layernorm.argtypes = [vp, i64, i64, i64, vp, vp, f64, vp, vp, vp]
         lib.oracle_xent.argtypes = [vp, i64, i64, i64, vp, i64, vp, vp, vp, vp, vp, vp, vp]
-        for name in ("oracle_relu_add_sum", "oracle_row_sumsq", "oracle_softmax",
+        for name in ("oracle_relu_add_sum", "oracle_row_sumsq", "oracle_row_l2norm",
+                     "oracle_softmax",
                      "oracle_md_merge", "oracle_md_fold", "oracle_online_attn_row",
                      "oracle_layernorm", "oracle_xent"):
             getattr(lib, name).restype = None
@@ -84,6 +86,14 @@ class Oracle:
         out = np.empty(x.shape[0], dtype=np.float64)
         self.lib.oracle_row_sumsq(x.ctypes.data, x.shape[0], x.shape[1], x.strides[0] // 4,
                                   out.ctypes.data)
+        return out
+
+    def row_l2norm(self, x: np.ndarray) -> np.ndarray:
+        """sqrt(sum_r x[x, r]^2) per row (fp32 squares, fp64 sum and root)."""
+        assert x.dtype == np.float32 and x.strides[1] == 4
+        out = np.empty(x.shape[0], dtype=np.float64)
+        self.lib.oracle_row_l2norm(x.ctypes.data, x.shape[0], x.shape[1], x.strides[0] // 4,
+                                   out.ctypes.data)
         return out
 
     # ---- softmax -----------------------------------------------------------

@@ -96,6 +96,19 @@ void oracle_row_sumsq(const float *x, int64_t rows, int64_t cols, int64_t ld, do
   }
 }
 
+/* Row L2 norm, [L8] section 12, exercise 1: the square root of the row's sum of
+ * squares (the same fp32 squares as above), taken in fp64. */
+void oracle_row_l2norm(const float *x, int64_t rows, int64_t cols, int64_t ld, double *out) {
+  oracle_row_sumsq(x, rows, cols, ld, out);
+  for (int64_t i = 0; i < rows; ++i) {
+#if ORACLE_PLANT == 10
+    out[i] = out[i] / (double)cols; /* planted: mean square instead of the root */
+#else
+    out[i] = sqrt(out[i]);
+#endif
+  }
+}
+
 /* ------------------------------------------------------------------------
  * Softmax along the row, [Stax4] section 9.5 (the softmax definition and
  * Listing 9.5) and [L8] section 3:

@@ -140,6 +140,25 @@ def pin_sumsq_dyadic(o):
     assert math.sqrt(o.row_sumsq(np.array([[3.0, 4.0]], np.float32))[0]) == 5.0
 
 
+def pin_l2norm_pythagorean_rows(o):
+    """Row L2 norm (Lecture 8, exercise 1) on integer rows whose norm is an
+    integer: [3, 4] -> 5, [5, 12] -> 13, [1, 2, 2] -> 3, [2, 3, 6] -> 7,
+    [1, 4, 8] -> 9; a one-hot row gives |value|; a power-of-two scale c gives
+    |c| times the norm exactly."""
+    rows = [([3, 4], 5), ([5, 12], 13), ([1, 2, 2], 3), ([2, 3, 6], 7), ([1, 4, 8], 9),
+            ([0, 0, 0, -7.5, 0], 7.5)]
+    x = np.zeros((len(rows), 5), np.float32)
+    for i, (vals, _) in enumerate(rows):
+        x[i, :len(vals)] = vals
+    got = o.row_l2norm(x)
+    assert got.tolist() == [float(n) for _, n in rows]
+    rng = _rng(6)
+    y = rng.standard_normal((3, 777)).astype(np.float32)
+    base = o.row_l2norm(y)
+    assert (o.row_l2norm(y * np.float32(-0.25)) == 0.25 * base).all()
+    assert (o.row_l2norm(y * np.float32(8.0)) == 8.0 * base).all()
+
+
 # ---------------------------------------------------------------------------
 # softmax and the (m, d) monoid
 # ---------------------------------------------------------------------------

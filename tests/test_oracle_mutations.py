@@ -18,6 +18,7 @@ PLANTS = {
     7: "argmax: last index wins ties",
     8: "log-sum-exp without the max term",
     9: "ignored rows counted in the mean",
+    10: "row L2 norm as the mean square instead of the root",
 }
 
 
