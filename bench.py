@@ -46,7 +46,9 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-extra", action="store_true", help="headline workload only")
-    p.add_argument("--only", choices=["relu_add_sum", "softmax", "layernorm", "split", "xent"],
+    p.add_argument("--only", choices=["relu_add_sum", "softmax", "layernorm", "split", "xent",
+                                      "sumsq", "l2norm", "softmax_4097", "softmax_65537",
+                                      "looped", "softmax_bf16"],
                    help="time one workload alone (for profiler captures) and exit")
     p.add_argument("--form", default="auto", choices=["auto", "persistent", "looped", "split"],
                    help="with --only: force a reduction form")
@@ -334,6 +336,30 @@ def setup_workload(name, fr, workloads, dev, form="auto"):
             y = torch.empty_like(x)
             calls.append(lambda x=x, y=y: fr.fr_softmax(x, out=y, form=form))
         return calls, "softmax", w.rows, w.cols, 1
+    if name in ("softmax_4097", "softmax_65537"):
+        # the looped online-softmax form on the two sweep lengths, 256 MiB each
+        cols = int(name.split("_")[1])
+        w = workloads.make(1, rows=(1 << 25) // cols, cols=cols)
+        for _ in range(nsets("softmax", w.rows, w.cols)):
+            x = to_device(w.arrays["x"], dev)
+            y = torch.empty_like(x)
+            calls.append(lambda x=x, y=y: fr.fr_softmax(x, out=y, form=form))
+        return calls, "softmax", w.rows, w.cols, 1
+    if name == "softmax_bf16":
+        # the bf16 softmax on [65536, 1024] (the fp32 workload's 256 MiB)
+        w = workloads.make_softmax_bf16(65536, 1024)
+        for _ in range(nsets("softmax_bf16", w.rows, w.cols)):
+            x = to_device(w.arrays["x"], dev)
+            y = torch.empty_like(x)
+            calls.append(lambda x=x, y=y: fr.fr_softmax(x, out=y, form=form))
+        return calls, "softmax_bf16", w.rows, w.cols, 1
+    if name == "looped":
+        # Example 1.1's looped form on 16384 rows of 8192 (1 GiB of a and b)
+        w = workloads.make(0, rows=16384, cols=8192)
+        a, b = to_device(w.arrays["a"], dev), to_device(w.arrays["b"], dev)
+        out = torch.empty(w.rows, device=dev)
+        calls.append(lambda: fr.fr_reduce_relu_add_sum(a, b, 2.0, out=out, form=form))
+        return calls, "relu_add_sum", w.rows, w.cols, 1
     if name == "layernorm":
         w = workloads.make(2)
         g, bt = to_device(w.arrays["gamma"], dev), to_device(w.arrays["beta"], dev)
@@ -358,6 +384,21 @@ def setup_workload(name, fr, workloads, dev, form="auto"):
             calls.append(lambda a=a, b=b, out=out, ws=ws:
                          fr.fr_reduce_relu_add_sum(a, b, 2.0, out=out, workspace=ws, form=form))
         return calls, "relu_add_sum", rows, cols, 2
+    if name in ("sumsq", "l2norm"):
+        # Example 6.2's [64, 16384] sum of squares (split form), and the row L2
+        # norm over 1 GiB of [16384, 16384] rows (looped form)
+        w = workloads.make_sumsq() if name == "sumsq" else workloads.make_sumsq(16384, 16384)
+        rows, cols = w.rows, w.cols
+        epi = "sum" if name == "sumsq" else "sqrt"
+        for _ in range(nsets("sumsq", rows, cols)):
+            x = to_device(w.arrays["x"], dev)
+            out = torch.empty(rows, device=dev)
+            ws = torch.empty(max(16, fr.fr_workspace_size("sumsq", rows, cols, "f32", form)),
+                             dtype=torch.uint8, device=dev)
+            calls.append(lambda x=x, out=out, ws=ws:
+                         fr.fr_reduce_sumsq(x, epi, out=out, workspace=ws, form=form))
+        split = fr.fr_workspace_size("sumsq", rows, cols, "f32", form) > 0
+        return calls, "sumsq", rows, cols, 2 if split else 1
     if name == "xent":
         w = workloads.make(4)
         rows, cols = w.rows, w.cols
@@ -372,7 +413,10 @@ def setup_workload(name, fr, workloads, dev, form="auto"):
 
 
 EXTRA = {"relu_add_sum": "relu_add_sum_64x128", "layernorm": "layernorm_4096x32768",
-         "split": "relu_add_sum_split_8x33554432", "xent": "xent_8192x50257"}
+         "split": "relu_add_sum_split_8x33554432", "xent": "xent_8192x50257",
+         "sumsq": "sumsq_split_64x16384", "l2norm": "l2norm_looped_16384x16384",
+         "softmax_4097": "softmax_looped_8190x4097", "softmax_65537": "softmax_looped_511x65537",
+         "looped": "relu_add_sum_looped_16384x8192", "softmax_bf16": "softmax_bf16_65536x1024"}
 
 
 def extra_configs(fr, traffic, workloads, timed, dev, peak, args, world, names=None,
@@ -389,6 +433,9 @@ def extra_configs(fr, traffic, workloads, timed, dev, peak, args, world, names=N
             "us": round(t * 1e6, 3), "gbs": round(nb / t / 1e9, 2),
             "frac": round(nb / t / 1e9 / peak, 4), "rows_per_s": round(world * rows / t, 1),
             "_launches": n, "rotating_sets": len(calls)}
+        if name in ("relu_add_sum", "sumsq"):
+            res[EXTRA[name]].update(graph_replay(calls[0], steps, args.warmup))
+            res[EXTRA[name]]["_launches"] += GRAPH_CALLS * steps * lpc
         del calls
         if op == "layernorm" and not args.only:
             # context: a device copy of the same bytes (x in, y out)
@@ -400,6 +447,37 @@ def extra_configs(fr, traffic, workloads, timed, dev, peak, args, world, names=N
             res[EXTRA.get(name, name)]["same_bytes_device_copy_gbs"] = round(nb / tc / 1e9, 2)
             del srcs, dsts, cps
     return res
+
+
+GRAPH_CALLS = 64  # calls recorded in one CUDA graph for the launch-bound case
+
+
+def graph_replay(call, steps, warmup):
+    """The launch-bound small case replayed from a CUDA graph holding
+    GRAPH_CALLS back-to-back calls: one submission per replay, so the time per
+    call is the device's, not the host's launch path."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(GRAPH_CALLS):
+            call()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (steps * GRAPH_CALLS)
+    return {"graph_us_per_call": round(us, 3), "graph_calls_per_replay": GRAPH_CALLS}
 
 
 # ---------------------------------------------------------------- oracle arms

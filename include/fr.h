@@ -68,8 +68,15 @@ typedef enum {
   FR_OP_RELU_ADD_SUM = 0,
   FR_OP_SOFTMAX = 1,
   FR_OP_LAYERNORM = 2,
-  FR_OP_XENT = 3
+  FR_OP_XENT = 3,
+  FR_OP_SUMSQ = 4
 } fr_op;
+
+/* Epilogue applied to a row sum after the reduction. */
+typedef enum {
+  FR_EPI_SUM = 0, /* the sum itself */
+  FR_EPI_SQRT = 1 /* its square root (taken in fp64, rounded once to fp32) */
+} fr_epilogue;
 
 /* Device error codes written by kernels (read by fr_check_device_error). */
 #define FR_DEVERR_NONE 0
@@ -118,6 +125,31 @@ fr_status fr_reduce_relu_add_sum(const void *a, const void *b, float *out, int64
                                  size_t workspace_bytes, fr_stream_t stream);
 
 /*
+ * out[x] = sum_{r < cols} x[x*ldx + r]^2            (epilogue FR_EPI_SUM)
+ * out[x] = sqrt(sum_{r < cols} x[x*ldx + r]^2)      (epilogue FR_EPI_SQRT)
+ *
+ * The sum of squares is Example 6.2 of "Stax (4): GPU Codegen and Dynamic
+ * Shapes" (Listing 9.4: each element squared in fp32, summed along the row;
+ * there [64, 16384] split into two segments per row); the square-root epilogue
+ * is the row-wise L2 norm of Exercise 1 in "CMU 15-779 Lecture 8: ML Compilers
+ * Part 1, Tile-based DSLs", section 12 (masked lanes contribute 0).  The same
+ * kernels and forms as fr_reduce_relu_add_sum with a one-input prologue: fp32
+ * accumulators over short runs, fp64 combine, the split form's partials in
+ * the workspace summed in a fixed order (bitwise run-to-run deterministic);
+ * the square root is taken in fp64 on the fp64 sum.
+ *
+ *   x          fp32 [rows, ldx] device input (read only)
+ *   out        fp32 [rows] device output
+ *   dtype      FR_F32 (the only dtype offered)
+ *   epilogue   FR_EPI_SUM or FR_EPI_SQRT; anything else is FR_ERR_INVALID_ARG
+ *   workspace  device scratch of fr_workspace_size(FR_OP_SUMSQ, ...) bytes
+ *              (only the split form uses it; may be NULL otherwise)
+ */
+fr_status fr_reduce_sumsq(const void *x, float *out, int64_t rows, int64_t cols, int64_t ldx,
+                          fr_dtype dtype, fr_epilogue epilogue, fr_form form, void *workspace,
+                          size_t workspace_bytes, fr_stream_t stream);
+
+/*
  * y[x, :] = softmax(x[x, :]):  m = max_r x,  y = exp(x - m) / sum_r exp(x - m)
  *
  * "Stax (4)", section 9.5 (the softmax equation and Listing 9.5: one read and
@@ -126,12 +158,15 @@ fr_status fr_reduce_relu_add_sum(const void *a, const void *b, float *out, int64
  * row on chip and takes the max and the sum in two passes over registers; the
  * looped form merges per-chunk (m, d) pairs with the online-softmax operator
  * of section 9.5 (Proposition 9.1) and then streams the row again to write y.
- * NaN anywhere in a row makes that row NaN.  fp32 in, fp32 out, fp32
- * arithmetic.
+ * NaN anywhere in a row makes that row NaN.  Arithmetic is fp32 for both
+ * dtypes: FR_F32 reads and writes fp32; FR_BF16 reads bf16, widens it exactly
+ * to fp32 (the listing's load-then-cast) and rounds y to bf16 (nearest even).
  *
- *   x          fp32 [rows, ldx] device input; y fp32 [rows, ldy] device output
- *              (x and y may be the same buffer when ldx == ldy)
- *   dtype      FR_F32
+ *   x          [rows, ldx] device input; y [rows, ldy] device output, both of
+ *              `dtype` (bf16 as uint16 bit patterns); x and y may be the same
+ *              buffer when ldx == ldy
+ *   dtype      FR_F32 (persistent up to 1024 columns) or FR_BF16 (persistent
+ *              up to 2048 columns); longer rows take the looped form
  */
 fr_status fr_softmax(const void *x, void *y, int64_t rows, int64_t cols, int64_t ldx,
                      int64_t ldy, fr_dtype dtype, fr_form form, fr_stream_t stream);

@@ -24,8 +24,9 @@ from . import buildlib as _build
 
 __all__ = [
     "FR_OK", "FRError", "lib", "fr_version", "fr_workspace_size", "fr_last_form",
-    "fr_reduce_relu_add_sum", "fr_softmax", "fr_layernorm", "fr_xent",
-    "fr_check_device_error", "FORMS", "OPS",
+    "fr_reduce_relu_add_sum", "fr_reduce_sumsq", "fr_softmax", "fr_layernorm", "fr_xent",
+    "fr_reduce_relu_add_sum_split_static", "fr_check_device_error", "FORMS", "OPS",
+    "EPILOGUES",
 ]
 
 FR_OK = 0
@@ -35,7 +36,8 @@ STATUS = {0: "FR_OK", 1: "FR_ERR_INVALID_ARG", 2: "FR_ERR_UNSUPPORTED_DTYPE",
           8: "FR_ERR_NO_DEVICE"}
 FORMS = {"auto": 0, "persistent": 1, "looped": 2, "split": 3}
 FORM_NAMES = {v: k for k, v in FORMS.items()}
-OPS = {"relu_add_sum": 0, "softmax": 1, "layernorm": 2, "xent": 3}
+OPS = {"relu_add_sum": 0, "softmax": 1, "layernorm": 2, "xent": 3, "sumsq": 4}
+EPILOGUES = {"sum": 0, "sqrt": 1}
 DTYPES = {"f32": 0, "bf16": 1}
 
 # name -> (restype, argtypes) of every symbol include/fr.h declares
@@ -48,6 +50,7 @@ SIGNATURES = {
     "fr_workspace_size": (_sz, [_int, _i64, _i64, _int, _int]),
     "fr_reduce_relu_add_sum": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _f32, _int,
                                       _vp, _sz, _vp]),
+    "fr_reduce_sumsq": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp, _sz, _vp]),
     "fr_softmax": (_int, [_vp, _vp, _i64, _i64, _i64, _i64, _int, _int, _vp]),
     "fr_layernorm": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _int,
                             _int, _vp]),
@@ -150,14 +153,33 @@ def fr_reduce_relu_add_sum(a, b, scale: float = 2.0, form: str = "auto", out=Non
     return out
 
 
-def fr_softmax(x, form: str = "auto", out=None, stream=None):
-    """Row softmax of fp32 x (returns a new fp32 tensor unless ``out`` is given)."""
+def fr_reduce_sumsq(x, epilogue: str = "sum", form: str = "auto", out=None, workspace=None,
+                    stream=None):
+    """out[x] = sum_r x[x, r]^2 (epilogue "sum") or its square root, the row L2
+    norm (epilogue "sqrt"); fp32 in, fp32 out."""
     import torch
     assert x.is_cuda and x.dtype == torch.float32 and x.dim() == 2
     rows, cols = x.shape
     if out is None:
+        out = torch.empty(rows, dtype=torch.float32, device=x.device)
+    ws, nws = _workspace("sumsq", rows, cols, "f32", form, x.device, workspace)
+    _check(lib().fr_reduce_sumsq(_ptr(x), _ptr(out), rows, cols, _ld(x), DTYPES["f32"],
+                                 EPILOGUES[epilogue], FORMS[form], _ptr(ws), nws,
+                                 _stream(stream)), "fr_reduce_sumsq")
+    return out
+
+
+def fr_softmax(x, form: str = "auto", out=None, stream=None):
+    """Row softmax of fp32 or bf16 x, y of the same dtype (returns a new tensor
+    unless ``out`` is given)."""
+    import torch
+    assert x.is_cuda and x.dtype in (torch.float32, torch.bfloat16) and x.dim() == 2
+    rows, cols = x.shape
+    if out is None:
         out = torch.empty_like(x)
-    _check(lib().fr_softmax(_ptr(x), _ptr(out), rows, cols, _ld(x), _ld(out), DTYPES["f32"],
+    assert out.dtype == x.dtype and out.shape == x.shape
+    dt = DTYPES["f32"] if x.dtype == torch.float32 else DTYPES["bf16"]
+    _check(lib().fr_softmax(_ptr(x), _ptr(out), rows, cols, _ld(x), _ld(out), dt,
                             FORMS[form], _stream(stream)), "fr_softmax")
     return out
 

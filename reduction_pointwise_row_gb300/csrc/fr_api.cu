@@ -138,6 +138,10 @@ size_t fr_workspace_size(fr_op op, int64_t rows, int64_t cols, fr_dtype dtype, f
       const fr_form f = form == FR_FORM_AUTO ? pick_ras(rows, cols, info.sm_count) : form;
       return f == FR_FORM_SPLIT ? fr::ras_split_workspace(rows, cols, info.sm_count) : 0;
     }
+    case FR_OP_SUMSQ: {
+      const fr_form f = form == FR_FORM_AUTO ? pick_ras(rows, cols, info.sm_count) : form;
+      return f == FR_FORM_SPLIT ? fr::ras_split_workspace(rows, cols, info.sm_count) : 0;
+    }
     case FR_OP_XENT: return fr::xent_workspace(rows, info.sm_count);
     default: return 0;
   }
@@ -177,20 +181,72 @@ fr_status fr_reduce_relu_add_sum(const void *a, const void *b, float *out, int64
   }
 }
 
+fr_status fr_reduce_sumsq(const void *x, float *out, int64_t rows, int64_t cols, int64_t ldx,
+                          fr_dtype dtype, fr_epilogue epilogue, fr_form form, void *workspace,
+                          size_t workspace_bytes, fr_stream_t stream) {
+  if (dtype != FR_F32) return FR_ERR_UNSUPPORTED_DTYPE;
+  if (!x || !out) return FR_ERR_INVALID_ARG;
+  if (epilogue != FR_EPI_SUM && epilogue != FR_EPI_SQRT) return FR_ERR_INVALID_ARG;
+  if (!shape_ok(rows, cols, ldx, 4)) return FR_ERR_INVALID_ARG;
+  if (!aligned(x, 4) || !aligned(out, 4)) return FR_ERR_MISALIGNED;
+  fr::DevInfo info;
+  if (fr_status st = device_ok(&info)) return st;
+  // Same rule as Example 1.1: the kernels are the same with one input.
+  const fr_form f = form == FR_FORM_AUTO ? pick_ras(rows, cols, info.sm_count) : form;
+  const bool root = epilogue == FR_EPI_SQRT;
+  const float *fx = static_cast<const float *>(x);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (f) {
+    case FR_FORM_PERSISTENT:
+      if (cols > fr::ras_persistent_max_cols()) return FR_ERR_UNSUPPORTED_FORM;
+      return launched(fr::launch_sumsq_persistent(fx, out, rows, cols, ldx, root, s), f);
+    case FR_FORM_LOOPED:
+      return launched(fr::launch_sumsq_looped(fx, out, rows, cols, ldx, root, s), f);
+    case FR_FORM_SPLIT: {
+      if (rows > 65535) return FR_ERR_UNSUPPORTED_FORM;
+      const size_t need = fr::ras_split_workspace(rows, cols, info.sm_count);
+      if (!workspace || workspace_bytes < need) return FR_ERR_WORKSPACE_TOO_SMALL;
+      if (!aligned(workspace, 16)) return FR_ERR_MISALIGNED;
+      const int segs = fr::ras_split_segments(rows, cols, info.sm_count);
+      return launched(fr::launch_sumsq_split(fx, out, rows, cols, ldx, root,
+                                             static_cast<double *>(workspace), segs, s), f);
+    }
+    default: return FR_ERR_UNSUPPORTED_FORM;
+  }
+}
+
 fr_status fr_softmax(const void *x, void *y, int64_t rows, int64_t cols, int64_t ldx,
                      int64_t ldy, fr_dtype dtype, fr_form form, fr_stream_t stream) {
-  if (dtype != FR_F32) return FR_ERR_UNSUPPORTED_DTYPE;
+  if (dtype != FR_F32 && dtype != FR_BF16) return FR_ERR_UNSUPPORTED_DTYPE;
+  const int64_t esize = dtype == FR_F32 ? 4 : 2;
   if (!x || !y) return FR_ERR_INVALID_ARG;
-  if (!shape_ok(rows, cols, ldx, 4) || !shape_ok(rows, cols, ldy, 4)) return FR_ERR_INVALID_ARG;
-  if (!aligned(x, 4) || !aligned(y, 4)) return FR_ERR_MISALIGNED;
+  if (!shape_ok(rows, cols, ldx, esize) || !shape_ok(rows, cols, ldy, esize))
+    return FR_ERR_INVALID_ARG;
+  if (!aligned(x, esize) || !aligned(y, esize)) return FR_ERR_MISALIGNED;
   if (x == y && ldx != ldy) return FR_ERR_INVALID_ARG;
   fr::DevInfo info;
   if (fr_status st = device_ok(&info)) return st;
-  const bool vec = same_phase(x, ldx, y, ldy, 4);
+  const bool vec = same_phase(x, ldx, y, ldy, esize);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == FR_BF16) {
+    const int64_t max_p = fr::softmax_bf16_persistent_max_cols();
+    const fr_form f = form == FR_FORM_AUTO ? (cols <= max_p ? FR_FORM_PERSISTENT : FR_FORM_LOOPED)
+                                           : form;
+    const uint16_t *bx = static_cast<const uint16_t *>(x);
+    uint16_t *by = static_cast<uint16_t *>(y);
+    switch (f) {
+      case FR_FORM_PERSISTENT:
+        if (cols > max_p) return FR_ERR_UNSUPPORTED_FORM;
+        return launched(fr::launch_softmax_bf16_persistent(bx, by, rows, cols, ldx, ldy, vec, s), f);
+      case FR_FORM_LOOPED:
+        return launched(fr::launch_softmax_bf16_looped(bx, by, rows, cols, ldx, ldy, vec,
+                                                       info.sm_count, s), f);
+      default: return FR_ERR_UNSUPPORTED_FORM;
+    }
+  }
   const fr_form f = form == FR_FORM_AUTO ? pick_softmax(rows, cols, vec) : form;
   const float *fx = static_cast<const float *>(x);
   float *fy = static_cast<float *>(y);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   switch (f) {
     case FR_FORM_PERSISTENT: {
       if (cols > fr::softmax_persistent_max_cols(vec)) return FR_ERR_UNSUPPORTED_FORM;

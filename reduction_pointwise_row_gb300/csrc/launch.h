@@ -35,6 +35,16 @@ cudaError_t launch_ras_split(const float *a, const float *b, float *out, int64_t
                              int64_t cols, int64_t lda, int64_t ldb, float scale, bool vec,
                              double *partials, int segments, cudaStream_t s);
 
+// ---- Example 6.2 and its L2-norm epilogue: out[x] = (sqrt) sum_r x^2 ------
+// Same forms, segment rule and workspace as above.
+cudaError_t launch_sumsq_persistent(const float *x, float *out, int64_t rows, int64_t cols,
+                                    int64_t ldx, bool sqrt_out, cudaStream_t s);
+cudaError_t launch_sumsq_looped(const float *x, float *out, int64_t rows, int64_t cols,
+                                int64_t ldx, bool sqrt_out, cudaStream_t s);
+cudaError_t launch_sumsq_split(const float *x, float *out, int64_t rows, int64_t cols,
+                               int64_t ldx, bool sqrt_out, double *partials, int segments,
+                               cudaStream_t s);
+
 // ---- softmax ---------------------------------------------------------------
 
 int64_t softmax_persistent_max_cols(bool vec);
@@ -48,6 +58,15 @@ cudaError_t launch_softmax_async(const float *x, float *y, int64_t rows, int64_t
 cudaError_t launch_softmax_looped(const float *x, float *y, int64_t rows, int64_t cols,
                                   int64_t ldx, int64_t ldy, bool vec, int sm_count,
                                   cudaStream_t s);
+
+// bf16 rows (x and y bf16, fp32 arithmetic): persistent up to 2048 columns.
+int64_t softmax_bf16_persistent_max_cols();
+cudaError_t launch_softmax_bf16_persistent(const uint16_t *x, uint16_t *y, int64_t rows,
+                                           int64_t cols, int64_t ldx, int64_t ldy, bool vec,
+                                           cudaStream_t s);
+cudaError_t launch_softmax_bf16_looped(const uint16_t *x, uint16_t *y, int64_t rows,
+                                       int64_t cols, int64_t ldx, int64_t ldy, bool vec,
+                                       int sm_count, cudaStream_t s);
 
 // ---- LayerNorm -------------------------------------------------------------
 

@@ -1,6 +1,6 @@
-// Example 1.1 of "Stax (4): GPU Codegen and Dynamic Shapes" (section 9.2,
-// Listing 9.1):  out[x] = sum_r scale * relu(a[x, r] + b[x, r])  in its three
-// reduction forms (section 9.4):
+// Row sums with a fused pointwise prologue and an optional epilogue, in the
+// three reduction forms of "Stax (4): GPU Codegen and Dynamic Shapes",
+// section 9.4:
 //
 //   persistent  one warp per row, the whole row loaded in one pass (all of a
 //               lane's loads in flight before any arithmetic), cols <= 1024;
@@ -12,11 +12,19 @@
 //               splits the reduction when there are too few outputs to fill the
 //               GPU; here the segment count fills every SM of the device.
 //
-// Arithmetic: a + b in fp32 (Listing 9.1 tmp2), relu keeping NaN (tmp4,
-// PropagateNan.ALL), times scale in fp32 (tmp6).  Runs of at most 8*U terms
-// are summed in fp32 and then added into an fp64 accumulator; the warp/CTA
-// combine and the cross-CTA combine are fp64 in a fixed tree order, so a given
-// shape on a given device model always gives the same bits.
+// Prologues:
+//   ReluAdd  Example 1.1 (section 9.2, Listing 9.1): scale * relu(a + b), a + b
+//            in fp32 (tmp2), relu keeping NaN (tmp4, PropagateNan.ALL), times
+//            scale in fp32 (tmp6);
+//   Square   Example 6.2 (Listing 9.4): x * x in fp32 (tmp1 = tmp0 * tmp0).
+// Epilogue: the plain sum, or its square root (the row L2 norm of Exercise 1
+// of "CMU 15-779 Lecture 8: ML Compilers Part 1, Tile-based DSLs", section 12),
+// taken in fp64 on the fp64 sum and rounded once to fp32.
+//
+// Runs of at most 8*U terms are summed in fp32 and then added into an fp64
+// accumulator; the warp/CTA combine and the cross-CTA combine are fp64 in a
+// fixed tree order, so a given shape on a given device model always gives the
+// same bits.
 #include "common.cuh"
 #include "launch.h"
 
@@ -28,56 +36,92 @@ constexpr int kPersistNV = 4;     // 32-byte vectors per lane in the persistent 
 constexpr int kSplitThreads = 256;
 constexpr int kSplitU = 2;        // vector pairs in flight per thread per iteration
 
-__device__ __forceinline__ float term(float a, float b, float scale) {
-  return relu_nan(a + b) * scale;
+struct ReluAdd {
+  static constexpr bool kTwoInputs = true;
+  float scale;
+  __device__ __forceinline__ float operator()(float a, float b) const {
+    return relu_nan(a + b) * scale;
+  }
+};
+
+struct Square {
+  static constexpr bool kTwoInputs = false;
+  __device__ __forceinline__ float operator()(float x, float) const { return x * x; }
+};
+
+template <class Op>
+__device__ __forceinline__ float term_at(const Op &op, const float *pa, const float *pb,
+                                         int64_t i) {
+  if constexpr (Op::kTwoInputs) return op(ld_stream_f32(pa + i), ld_stream_f32(pb + i));
+  else return op(ld_stream_f32(pa + i), 0.0f);
 }
 
-__device__ __forceinline__ float terms_v8(const V8 &va, const V8 &vb, float scale) {
-  float t = 0.0f;
+// N 32-byte vectors of each input in flight per thread (one-input prologues
+// hold no second array).
+template <class Op, int N>
+struct VecBuf {
+  V8 a[N];
+  V8 b[Op::kTwoInputs ? N : 1];
+
+  __device__ __forceinline__ void load(int k, const float *pa, const float *pb, int64_t off) {
+    a[k] = ld_stream_v8(pa + off);
+    if constexpr (Op::kTwoInputs) b[k] = ld_stream_v8(pb + off);
+  }
+
+  __device__ __forceinline__ float terms(int k, const Op &op) const {
+    float t = 0.0f;
+    if constexpr (Op::kTwoInputs) {
 #pragma unroll
-  for (int j = 0; j < 8; ++j) t += term(__uint_as_float(va.w[j]), __uint_as_float(vb.w[j]), scale);
-  return t;
+      for (int j = 0; j < 8; ++j) t += op(__uint_as_float(a[k].w[j]), __uint_as_float(b[k].w[j]));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) t += op(__uint_as_float(a[k].w[j]), 0.0f);
+    }
+    return t;
+  }
+};
+
+template <bool SQRT>
+__device__ __forceinline__ float finish(double acc) {
+  if constexpr (SQRT) return static_cast<float>(sqrt(acc));
+  else return static_cast<float>(acc);
 }
 
-// Warp-per-row form.  VEC: a and b rows share their offset modulo 32 bytes, so
-// one head/body/tail split serves both; otherwise every element is a scalar
-// (still coalesced: lane-strided).
-template <bool VEC, bool LOOP>
+// Warp-per-row form.  VEC: the input rows share their offset modulo 32 bytes,
+// so one head/body/tail split serves both; otherwise every element is a
+// scalar (still coalesced: lane-strided).  b is unused by one-input prologues.
+template <class Op, bool VEC, bool LOOP, bool SQRT>
 __global__ void __launch_bounds__(kRowThreads)
-ras_warp_row(const float *__restrict__ a, const float *__restrict__ b, float *__restrict__ out,
-             int64_t rows, int64_t cols, int64_t lda, int64_t ldb, float scale) {
+rowsum_warp(const float *__restrict__ a, const float *__restrict__ b, float *__restrict__ out,
+            int64_t rows, int64_t cols, int64_t lda, int64_t ldb, Op op) {
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (kRowThreads / 32) + (threadIdx.x >> 5);
   if (row >= rows) return;
   const float *pa = a + row * lda;
-  const float *pb = b + row * ldb;
+  const float *pb = Op::kTwoInputs ? b + row * ldb : nullptr;
   double acc = 0.0;
   if constexpr (VEC) {
     const RowSplit sp = row_split(pa, cols, 4);
     float s = 0.0f;  // head and tail: at most 7 + 7 scalars, one per lane
     if (lane < sp.head) {
-      s = term(ld_stream_f32(pa + lane), ld_stream_f32(pb + lane), scale);
+      s = term_at(op, pa, pb, lane);
     } else if (lane < sp.head + sp.tail) {
-      const int64_t i = sp.head + sp.nvec * 8 + (lane - sp.head);
-      s = term(ld_stream_f32(pa + i), ld_stream_f32(pb + i), scale);
+      s = term_at(op, pa, pb, sp.head + sp.nvec * 8 + (lane - sp.head));
     }
     acc = s;
     const float *va = pa + sp.head;
-    const float *vb = pb + sp.head;
+    const float *vb = Op::kTwoInputs ? pb + sp.head : nullptr;
     for (int64_t base = 0; base < sp.nvec; base += 32 * kPersistNV) {
-      V8 xa[kPersistNV], xb[kPersistNV];
+      VecBuf<Op, kPersistNV> buf;
 #pragma unroll
       for (int k = 0; k < kPersistNV; ++k) {
         const int64_t vi = base + lane + 32 * k;
-        if (vi < sp.nvec) {
-          xa[k] = ld_stream_v8(va + vi * 8);
-          xb[k] = ld_stream_v8(vb + vi * 8);
-        }
+        if (vi < sp.nvec) buf.load(k, va, vb, vi * 8);
       }
       float t = 0.0f;
 #pragma unroll
       for (int k = 0; k < kPersistNV; ++k)
-        if (base + lane + 32 * k < sp.nvec) t += terms_v8(xa[k], xb[k], scale);
+        if (base + lane + 32 * k < sp.nvec) t += buf.terms(k, op);
       acc += static_cast<double>(t);
       if constexpr (!LOOP) break;
     }
@@ -87,7 +131,7 @@ ras_warp_row(const float *__restrict__ a, const float *__restrict__ b, float *__
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const int64_t i = base + lane + 32 * k;
-        if (i < cols) t += term(ld_stream_f32(pa + i), ld_stream_f32(pb + i), scale);
+        if (i < cols) t += term_at(op, pa, pb, i);
       }
       acc += static_cast<double>(t);
       if constexpr (!LOOP) {
@@ -96,20 +140,20 @@ ras_warp_row(const float *__restrict__ a, const float *__restrict__ b, float *__
     }
   }
   acc = warp_sum_f64(acc);
-  if (lane == 0) out[row] = static_cast<float>(acc);
+  if (lane == 0) out[row] = finish<SQRT>(acc);
 }
 
 // Split form, stage 1: CTA (seg, row) sums its segment of the row's body
 // vectors (segment 0 also takes the head scalars, the last segment the tail).
-template <bool VEC>
+template <class Op, bool VEC>
 __global__ void __launch_bounds__(kSplitThreads)
-ras_split_stage1(const float *__restrict__ a, const float *__restrict__ b, int64_t cols,
-                 int64_t lda, int64_t ldb, float scale, double *__restrict__ partials, int S) {
+rowsum_split_stage1(const float *__restrict__ a, const float *__restrict__ b, int64_t cols,
+                    int64_t lda, int64_t ldb, Op op, double *__restrict__ partials, int S) {
   const int seg = blockIdx.x;
   const int64_t row = blockIdx.y;
   const int tid = threadIdx.x;
   const float *pa = a + row * lda;
-  const float *pb = b + row * ldb;
+  const float *pb = Op::kTwoInputs ? b + row * ldb : nullptr;
   const RowSplit sp = VEC ? row_split(pa, cols, 4) : RowSplit{0, cols, 0};
   const int64_t per = (sp.nvec + S - 1) / S;
   const int64_t lo = seg * per;
@@ -117,36 +161,30 @@ ras_split_stage1(const float *__restrict__ a, const float *__restrict__ b, int64
   double acc = 0.0;
   if constexpr (VEC) {
     const float *va = pa + sp.head;
-    const float *vb = pb + sp.head;
+    const float *vb = Op::kTwoInputs ? pb + sp.head : nullptr;
     for (int64_t base = lo; base < hi; base += kSplitThreads * kSplitU) {
-      V8 xa[kSplitU], xb[kSplitU];
+      VecBuf<Op, kSplitU> buf;
 #pragma unroll
       for (int u = 0; u < kSplitU; ++u) {
         const int64_t vi = base + tid + kSplitThreads * u;
-        if (vi < hi) {
-          xa[u] = ld_stream_v8(va + vi * 8);
-          xb[u] = ld_stream_v8(vb + vi * 8);
-        }
+        if (vi < hi) buf.load(u, va, vb, vi * 8);
       }
       float t = 0.0f;
 #pragma unroll
       for (int u = 0; u < kSplitU; ++u)
-        if (base + tid + kSplitThreads * u < hi) t += terms_v8(xa[u], xb[u], scale);
+        if (base + tid + kSplitThreads * u < hi) t += buf.terms(u, op);
       acc += static_cast<double>(t);
     }
-    if (seg == 0 && tid < sp.head)
-      acc += static_cast<double>(term(ld_stream_f32(pa + tid), ld_stream_f32(pb + tid), scale));
-    if (seg == S - 1 && tid < sp.tail) {
-      const int64_t i = sp.head + sp.nvec * 8 + tid;
-      acc += static_cast<double>(term(ld_stream_f32(pa + i), ld_stream_f32(pb + i), scale));
-    }
+    if (seg == 0 && tid < sp.head) acc += static_cast<double>(term_at(op, pa, pb, tid));
+    if (seg == S - 1 && tid < sp.tail)
+      acc += static_cast<double>(term_at(op, pa, pb, sp.head + sp.nvec * 8 + tid));
   } else {
     for (int64_t base = lo; base < hi; base += kSplitThreads * 8) {
       float t = 0.0f;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int64_t i = base + tid + kSplitThreads * u;
-        if (i < hi) t += term(ld_stream_f32(pa + i), ld_stream_f32(pb + i), scale);
+        if (i < hi) t += term_at(op, pa, pb, i);
       }
       acc += static_cast<double>(t);
     }
@@ -164,20 +202,51 @@ ras_split_stage1(const float *__restrict__ a, const float *__restrict__ b, int64
 }
 
 // Split form, stage 2: one warp per row adds its S partials in a fixed order.
+template <bool SQRT>
 __global__ void __launch_bounds__(kRowThreads)
-ras_split_stage2(const double *__restrict__ partials, float *__restrict__ out, int64_t rows,
-                 int S) {
+rowsum_split_stage2(const double *__restrict__ partials, float *__restrict__ out, int64_t rows,
+                    int S) {
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (kRowThreads / 32) + (threadIdx.x >> 5);
   if (row >= rows) return;
   double t = 0.0;
   for (int k = lane; k < S; k += 32) t += partials[row * S + k];
   t = warp_sum_f64(t);
-  if (lane == 0) out[row] = static_cast<float>(t);
+  if (lane == 0) out[row] = finish<SQRT>(t);
 }
 
 unsigned warp_row_grid(int64_t rows) {
   return static_cast<unsigned>((rows + kRowThreads / 32 - 1) / (kRowThreads / 32));
+}
+
+template <class Op, bool LOOP, bool SQRT>
+cudaError_t launch_warp(const float *a, const float *b, float *out, int64_t rows, int64_t cols,
+                        int64_t lda, int64_t ldb, Op op, bool vec, cudaStream_t s) {
+  if (vec)
+    rowsum_warp<Op, true, LOOP, SQRT><<<warp_row_grid(rows), kRowThreads, 0, s>>>(
+        a, b, out, rows, cols, lda, ldb, op);
+  else
+    rowsum_warp<Op, false, LOOP, SQRT><<<warp_row_grid(rows), kRowThreads, 0, s>>>(
+        a, b, out, rows, cols, lda, ldb, op);
+  return cudaGetLastError();
+}
+
+template <class Op, bool SQRT>
+cudaError_t launch_split(const float *a, const float *b, float *out, int64_t rows, int64_t cols,
+                         int64_t lda, int64_t ldb, Op op, bool vec, double *partials,
+                         int segments, cudaStream_t s) {
+  dim3 grid(static_cast<unsigned>(segments), static_cast<unsigned>(rows));
+  if (vec)
+    rowsum_split_stage1<Op, true><<<grid, kSplitThreads, 0, s>>>(a, b, cols, lda, ldb, op,
+                                                                partials, segments);
+  else
+    rowsum_split_stage1<Op, false><<<grid, kSplitThreads, 0, s>>>(a, b, cols, lda, ldb, op,
+                                                                 partials, segments);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  rowsum_split_stage2<SQRT><<<warp_row_grid(rows), kRowThreads, 0, s>>>(partials, out, rows,
+                                                                        segments);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -203,41 +272,49 @@ size_t ras_split_workspace(int64_t rows, int64_t cols, int sm_count) {
 cudaError_t launch_ras_persistent(const float *a, const float *b, float *out, int64_t rows,
                                   int64_t cols, int64_t lda, int64_t ldb, float scale,
                                   bool vec, cudaStream_t s) {
-  if (vec)
-    ras_warp_row<true, false><<<warp_row_grid(rows), kRowThreads, 0, s>>>(a, b, out, rows, cols,
-                                                                         lda, ldb, scale);
-  else
-    ras_warp_row<false, false><<<warp_row_grid(rows), kRowThreads, 0, s>>>(a, b, out, rows,
-                                                                          cols, lda, ldb, scale);
-  return cudaGetLastError();
+  return launch_warp<ReluAdd, false, false>(a, b, out, rows, cols, lda, ldb, ReluAdd{scale},
+                                            vec, s);
 }
 
 cudaError_t launch_ras_looped(const float *a, const float *b, float *out, int64_t rows,
                               int64_t cols, int64_t lda, int64_t ldb, float scale, bool vec,
                               cudaStream_t s) {
-  if (vec)
-    ras_warp_row<true, true><<<warp_row_grid(rows), kRowThreads, 0, s>>>(a, b, out, rows, cols,
-                                                                        lda, ldb, scale);
-  else
-    ras_warp_row<false, true><<<warp_row_grid(rows), kRowThreads, 0, s>>>(a, b, out, rows, cols,
-                                                                         lda, ldb, scale);
-  return cudaGetLastError();
+  return launch_warp<ReluAdd, true, false>(a, b, out, rows, cols, lda, ldb, ReluAdd{scale},
+                                           vec, s);
 }
 
 cudaError_t launch_ras_split(const float *a, const float *b, float *out, int64_t rows,
                              int64_t cols, int64_t lda, int64_t ldb, float scale, bool vec,
                              double *partials, int segments, cudaStream_t s) {
-  dim3 grid(static_cast<unsigned>(segments), static_cast<unsigned>(rows));
-  if (vec)
-    ras_split_stage1<true><<<grid, kSplitThreads, 0, s>>>(a, b, cols, lda, ldb, scale, partials,
-                                                         segments);
-  else
-    ras_split_stage1<false><<<grid, kSplitThreads, 0, s>>>(a, b, cols, lda, ldb, scale, partials,
-                                                          segments);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  ras_split_stage2<<<warp_row_grid(rows), kRowThreads, 0, s>>>(partials, out, rows, segments);
-  return cudaGetLastError();
+  return launch_split<ReluAdd, false>(a, b, out, rows, cols, lda, ldb, ReluAdd{scale}, vec,
+                                      partials, segments, s);
+}
+
+// One-input rows need no common phase with a second input: every row takes
+// the vector path with its own head/body/tail split.
+cudaError_t launch_sumsq_persistent(const float *x, float *out, int64_t rows, int64_t cols,
+                                    int64_t ldx, bool sqrt_out, cudaStream_t s) {
+  return sqrt_out ? launch_warp<Square, false, true>(x, nullptr, out, rows, cols, ldx, 0,
+                                                     Square{}, true, s)
+                  : launch_warp<Square, false, false>(x, nullptr, out, rows, cols, ldx, 0,
+                                                      Square{}, true, s);
+}
+
+cudaError_t launch_sumsq_looped(const float *x, float *out, int64_t rows, int64_t cols,
+                                int64_t ldx, bool sqrt_out, cudaStream_t s) {
+  return sqrt_out ? launch_warp<Square, true, true>(x, nullptr, out, rows, cols, ldx, 0,
+                                                    Square{}, true, s)
+                  : launch_warp<Square, true, false>(x, nullptr, out, rows, cols, ldx, 0,
+                                                     Square{}, true, s);
+}
+
+cudaError_t launch_sumsq_split(const float *x, float *out, int64_t rows, int64_t cols,
+                               int64_t ldx, bool sqrt_out, double *partials, int segments,
+                               cudaStream_t s) {
+  return sqrt_out ? launch_split<Square, true>(x, nullptr, out, rows, cols, ldx, 0, Square{},
+                                               true, partials, segments, s)
+                  : launch_split<Square, false>(x, nullptr, out, rows, cols, ldx, 0, Square{},
+                                                true, partials, segments, s);
 }
 
 }  // namespace fr

@@ -1,0 +1,305 @@
+// Row softmax on bf16 rows ("Stax (4): GPU Codegen and Dynamic Shapes",
+// section 9.5 and Listing 9.5, whose loads cast to fp32 before the max):
+// x is read as bf16 and widened exactly to fp32, the max, the exponentials,
+// the sum and the division are fp32, and y is rounded to bf16 (nearest even).
+//
+// persistent  one warp per row, the row's exponentials held in registers (up
+//             to 2048 elements per warp, 32-byte vectors of 16 bf16 per lane),
+//             the max and the sum in two passes over registers: one read and
+//             one write of each element.
+// looped      one CTA per row (grid-stride over rows) for longer rows: per-
+//             thread online pairs (m, d) folded chunk by chunk with the merge
+//             of section 9.5, combined across the CTA in any order
+//             (Proposition 9.1), then a second streaming pass writes y.
+//
+// The max runs on packed bf16 pairs (max.NaN.bf16x2 is exact on bf16 values);
+// NaN anywhere in the row makes the row NaN; masked lanes are -inf for the max
+// and 0 for the sum.
+#include "common.cuh"
+#include "launch.h"
+
+namespace fr {
+namespace {
+
+constexpr int kWarpRowThreads = 256;
+constexpr int kLoopThreads = 512;
+constexpr int kLoopU = 2;
+constexpr int kPer = 16;                    // bf16 per 32-byte vector
+constexpr uint32_t kNegInfBf16x2 = 0xFF80FF80u;
+
+__device__ __forceinline__ float vec_max(const V8 &v) {
+  uint32_t m = kNegInfBf16x2;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) m = max_nan_bf16x2(m, v.w[j]);
+  return max_nan(bf16_lo(m), bf16_hi(m));
+}
+
+// Persistent form, 32-byte vectors: NV vectors of 16 elements per lane
+// (cols <= 512 * NV).  x and y rows share their offset modulo 32 bytes.  The
+// 16 * NV exponentials stay in registers (89 at NV = 4, no spill).
+template <int NV>
+__global__ void __launch_bounds__(kWarpRowThreads, 1)
+softmax_bf16_warp_vec(const uint16_t *__restrict__ x, uint16_t *__restrict__ y, int64_t rows,
+                      int64_t cols, int64_t ldx, int64_t ldy) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row =
+      static_cast<int64_t>(blockIdx.x) * (kWarpRowThreads / 32) + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const uint16_t *px = x + row * ldx;
+  uint16_t *py = y + row * ldy;
+  const RowSplit sp = row_split(px, cols, 2);
+  // head and tail scalars (at most 15 + 15): one per lane
+  int64_t si = -1;
+  if (lane < sp.head) si = lane;
+  else if (lane < sp.head + sp.tail) si = sp.head + sp.nvec * kPer + (lane - sp.head);
+  const uint16_t *vx = px + sp.head;
+  V8 v[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int64_t vi = lane + 32 * k;
+    if (vi < sp.nvec) v[k] = ld_stream_v8(vx + vi * kPer);
+  }
+  const float sv = si >= 0 ? bf16_to_f32(ld_stream_u16(px + si)) : -INFINITY;
+
+  float m = sv;
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+    if (lane + 32 * k < sp.nvec) m = max_nan(m, vec_max(v[k]));
+  m = warp_max_nan(m);
+  const float mb = m * kLog2e;
+
+  const float se = si >= 0 ? ex2(fmaf(sv, kLog2e, -mb)) : 0.0f;
+  float e[NV][kPer];
+  float d = se;
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+    if (lane + 32 * k < sp.nvec) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        e[k][2 * j] = ex2(fmaf(bf16_lo(v[k].w[j]), kLog2e, -mb));
+        e[k][2 * j + 1] = ex2(fmaf(bf16_hi(v[k].w[j]), kLog2e, -mb));
+        d += e[k][2 * j] + e[k][2 * j + 1];
+      }
+    }
+  d = warp_sum(d);
+  const float inv = __frcp_rn(d);
+
+  uint16_t *vy = py + sp.head;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int64_t vi = lane + 32 * k;
+    if (vi < sp.nvec) {
+      V8 o;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) o.w[j] = pack_bf16x2(e[k][2 * j] * inv, e[k][2 * j + 1] * inv);
+      st_stream_v8(vy + vi * kPer, o);
+    }
+  }
+  if (si >= 0) st_stream_u16(py + si, to_bf16(se * inv));
+}
+
+// Persistent form, lane-strided scalars (x and y rows out of phase): NS
+// elements per lane, cols <= 32 * NS.
+template <int NS>
+__global__ void __launch_bounds__(kWarpRowThreads)
+softmax_bf16_warp_scalar(const uint16_t *__restrict__ x, uint16_t *__restrict__ y, int64_t rows,
+                         int64_t cols, int64_t ldx, int64_t ldy) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row =
+      static_cast<int64_t>(blockIdx.x) * (kWarpRowThreads / 32) + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const uint16_t *px = x + row * ldx;
+  uint16_t *py = y + row * ldy;
+  float v[NS];
+#pragma unroll
+  for (int k = 0; k < NS; ++k) {
+    const int64_t i = lane + 32 * k;
+    v[k] = i < cols ? bf16_to_f32(ld_stream_u16(px + i)) : -INFINITY;
+  }
+  float m = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < NS; ++k)
+    if (lane + 32 * k < cols) m = max_nan(m, v[k]);
+  m = warp_max_nan(m);
+  const float mb = m * kLog2e;
+  float d = 0.0f;
+#pragma unroll
+  for (int k = 0; k < NS; ++k)
+    if (lane + 32 * k < cols) {
+      v[k] = ex2(fmaf(v[k], kLog2e, -mb));
+      d += v[k];
+    }
+  d = warp_sum(d);
+  const float inv = __frcp_rn(d);
+#pragma unroll
+  for (int k = 0; k < NS; ++k) {
+    const int64_t i = lane + 32 * k;
+    if (i < cols) st_stream_u16(py + i, to_bf16(v[k] * inv));
+  }
+}
+
+// Fold a chunk whose max is cm into the online pair: rescale d to the new max.
+__device__ __forceinline__ MD fold_chunk(MD st, float cm) {
+  const float M = max_nan(st.m, cm);
+  if (M == -INFINITY) return st;  // nothing but masked values so far
+  st.d = st.d * ex2((st.m - M) * kLog2e);
+  st.m = M;
+  return st;
+}
+
+// CTA-wide merge of the per-thread pairs; every thread gets the row's (m, d).
+__device__ __forceinline__ MD block_md(MD st, MD *smem) {
+  constexpr int NW = kLoopThreads / 32;
+  st = warp_md(st);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) smem[warp] = st;
+  __syncthreads();
+  MD r = lane < NW ? smem[lane] : MD{-INFINITY, 0.0f};
+  r = warp_md(r);
+  __syncthreads();  // smem free for the next row
+  return r;
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(kLoopThreads)
+softmax_bf16_block_looped(const uint16_t *__restrict__ x, uint16_t *__restrict__ y, int64_t rows,
+                          int64_t cols, int64_t ldx, int64_t ldy) {
+  __shared__ MD red[kLoopThreads / 32];
+  const int tid = threadIdx.x;
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    const uint16_t *px = x + row * ldx;
+    uint16_t *py = y + row * ldy;
+    const RowSplit sp = VEC ? row_split(px, cols, 2) : RowSplit{0, 0, 0};
+    MD st{-INFINITY, 0.0f};
+    if constexpr (VEC) {
+      const uint16_t *vx = px + sp.head;
+      for (int64_t base = 0; base < sp.nvec; base += kLoopThreads * kLoopU) {
+        V8 v[kLoopU];
+        float cm = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < kLoopU; ++u) {
+          const int64_t vi = base + tid + kLoopThreads * u;
+          if (vi < sp.nvec) {
+            v[u] = ld_keep_v8(vx + vi * kPer);  // pass 2 re-reads it from L2
+            cm = max_nan(cm, vec_max(v[u]));
+          }
+        }
+        st = fold_chunk(st, cm);
+        if (st.m == -INFINITY) continue;  // every value so far is -inf: adds 0
+        const float mb = st.m * kLog2e;
+#pragma unroll
+        for (int u = 0; u < kLoopU; ++u)
+          if (base + tid + kLoopThreads * u < sp.nvec) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              st.d += ex2(fmaf(bf16_lo(v[u].w[j]), kLog2e, -mb)) +
+                      ex2(fmaf(bf16_hi(v[u].w[j]), kLog2e, -mb));
+          }
+      }
+      int64_t si = -1;
+      if (tid < sp.head) si = tid;
+      else if (tid < sp.head + sp.tail) si = sp.head + sp.nvec * kPer + (tid - sp.head);
+      if (si >= 0) st = md_merge(st, MD{bf16_to_f32(ld_stream_u16(px + si)), 1.0f});
+    } else {
+      for (int64_t base = 0; base < cols; base += kLoopThreads * 8) {
+        float v[8];
+        float cm = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int64_t i = base + tid + kLoopThreads * u;
+          v[u] = i < cols ? bf16_to_f32(ld_stream_u16(px + i)) : -INFINITY;
+          cm = max_nan(cm, v[u]);
+        }
+        st = fold_chunk(st, cm);
+        if (st.m == -INFINITY) continue;
+        const float mb = st.m * kLog2e;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (base + tid + kLoopThreads * u < cols) st.d += ex2(fmaf(v[u], kLog2e, -mb));
+      }
+    }
+    const MD r = block_md(st, red);
+    const float mb = r.m * kLog2e;
+    const float inv = __frcp_rn(r.d);
+    if constexpr (VEC) {
+      const uint16_t *vx = px + sp.head;
+      uint16_t *vy = py + sp.head;
+      for (int64_t base = 0; base < sp.nvec; base += kLoopThreads * kLoopU) {
+        V8 v[kLoopU];
+#pragma unroll
+        for (int u = 0; u < kLoopU; ++u) {
+          const int64_t vi = base + tid + kLoopThreads * u;
+          if (vi < sp.nvec) v[u] = ld_stream_v8(vx + vi * kPer);
+        }
+#pragma unroll
+        for (int u = 0; u < kLoopU; ++u) {
+          const int64_t vi = base + tid + kLoopThreads * u;
+          if (vi < sp.nvec) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              v[u].w[j] = pack_bf16x2(ex2(fmaf(bf16_lo(v[u].w[j]), kLog2e, -mb)) * inv,
+                                      ex2(fmaf(bf16_hi(v[u].w[j]), kLog2e, -mb)) * inv);
+            st_stream_v8(vy + vi * kPer, v[u]);
+          }
+        }
+      }
+      int64_t si = -1;
+      if (tid < sp.head) si = tid;
+      else if (tid < sp.head + sp.tail) si = sp.head + sp.nvec * kPer + (tid - sp.head);
+      if (si >= 0)
+        st_stream_u16(py + si,
+                      to_bf16(ex2(fmaf(bf16_to_f32(ld_stream_u16(px + si)), kLog2e, -mb)) * inv));
+    } else {
+      for (int64_t i = tid; i < cols; i += kLoopThreads)
+        st_stream_u16(py + i,
+                      to_bf16(ex2(fmaf(bf16_to_f32(ld_stream_u16(px + i)), kLog2e, -mb)) * inv));
+    }
+  }
+}
+
+unsigned warp_row_grid(int64_t rows) {
+  return static_cast<unsigned>((rows + kWarpRowThreads / 32 - 1) / (kWarpRowThreads / 32));
+}
+
+}  // namespace
+
+int64_t softmax_bf16_persistent_max_cols() { return 2048; }
+
+cudaError_t launch_softmax_bf16_persistent(const uint16_t *x, uint16_t *y, int64_t rows,
+                                           int64_t cols, int64_t ldx, int64_t ldy, bool vec,
+                                           cudaStream_t s) {
+  const unsigned grid = warp_row_grid(rows);
+  if (vec) {
+    const int64_t nv = (cols + 32 * kPer - 1) / (32 * kPer);
+    switch (nv) {
+      case 1: softmax_bf16_warp_vec<1><<<grid, kWarpRowThreads, 0, s>>>(x, y, rows, cols, ldx, ldy); break;
+      case 2: softmax_bf16_warp_vec<2><<<grid, kWarpRowThreads, 0, s>>>(x, y, rows, cols, ldx, ldy); break;
+      case 3: softmax_bf16_warp_vec<3><<<grid, kWarpRowThreads, 0, s>>>(x, y, rows, cols, ldx, ldy); break;
+      case 4: softmax_bf16_warp_vec<4><<<grid, kWarpRowThreads, 0, s>>>(x, y, rows, cols, ldx, ldy); break;
+      default: return cudaErrorInvalidValue;
+    }
+  } else {
+    if (cols <= 128) softmax_bf16_warp_scalar<4><<<grid, kWarpRowThreads, 0, s>>>(x, y, rows, cols, ldx, ldy);
+    else if (cols <= 512) softmax_bf16_warp_scalar<16><<<grid, kWarpRowThreads, 0, s>>>(x, y, rows, cols, ldx, ldy);
+    else if (cols <= 1024) softmax_bf16_warp_scalar<32><<<grid, kWarpRowThreads, 0, s>>>(x, y, rows, cols, ldx, ldy);
+    else if (cols <= 2048) softmax_bf16_warp_scalar<64><<<grid, kWarpRowThreads, 0, s>>>(x, y, rows, cols, ldx, ldy);
+    else return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_softmax_bf16_looped(const uint16_t *x, uint16_t *y, int64_t rows,
+                                       int64_t cols, int64_t ldx, int64_t ldy, bool vec,
+                                       int sm_count, cudaStream_t s) {
+  int64_t grid = static_cast<int64_t>(sm_count) * 2;
+  if (grid > rows) grid = rows;
+  if (vec)
+    softmax_bf16_block_looped<true><<<static_cast<unsigned>(grid), kLoopThreads, 0, s>>>(
+        x, y, rows, cols, ldx, ldy);
+  else
+    softmax_bf16_block_looped<false><<<static_cast<unsigned>(grid), kLoopThreads, 0, s>>>(
+        x, y, rows, cols, ldx, ldy);
+  return cudaGetLastError();
+}
+
+}  // namespace fr

@@ -28,8 +28,12 @@ def fused_softmax_elements(rows: int, cols: int) -> tuple[int, int]:
 def algorithmic_bytes(op: str, rows: int, cols: int, **kw) -> int:
     if op == "relu_add_sum":          # a, b fp32 in; out fp32 [rows]
         return 2 * rows * cols * 4 + rows * 4
+    if op == "sumsq":                 # x fp32 in; out fp32 [rows]
+        return rows * cols * 4 + rows * 4
     if op == "softmax":               # x fp32 in; y fp32 out
         return 2 * rows * cols * 4
+    if op == "softmax_bf16":          # x bf16 in; y bf16 out
+        return 2 * rows * cols * 2
     if op == "layernorm":             # x bf16 in, y bf16 out, gamma/beta fp32, mean/rstd fp32
         return 2 * rows * cols * 2 + 2 * cols * 4 + 2 * rows * 4
     if op == "xent":                  # logits bf16, targets int64, loss fp32 [rows], mean fp32

@@ -88,3 +88,30 @@ def make(cfg: int, rows: int | None = None, cols: int | None = None, nan_variant
     else:
         raise ValueError(op)
     return w
+
+
+# Example 6.2 of the Stax codegen chapter: x fp32 [64, 16384] reduced to its
+# row sums of squares (the listing's wrapper asserts that shape); the pages
+# give no value distribution, so x ~ N(0, 1) (torch.randn's).  Seeded with
+# 20261202 + 5.
+SUMSQ_SHAPE = (64, 16384)
+
+
+def make_sumsq(rows: int | None = None, cols: int | None = None,
+               seed: int | None = None) -> Workload:
+    R = SUMSQ_SHAPE[0] if rows is None else rows
+    C = SUMSQ_SHAPE[1] if cols is None else cols
+    s = SEED_BASE + 5 if seed is None else seed
+    w = Workload(name="row sum of squares / L2 norm fp32 (Example 6.2)", op="sumsq", rows=R,
+                 cols=C)
+    w.arrays["x"] = normal_f32((R, C), s, 0, 0.0, 1.0)
+    return w
+
+
+def make_softmax_bf16(rows: int, cols: int, seed: int | None = None) -> Workload:
+    """The softmax workload's distribution, 4 * N(0, 1), rounded to bf16 (bit
+    patterns), for the bf16 variant of the softmax row."""
+    s = SEED_BASE + 6 if seed is None else seed
+    w = Workload(name=f"softmax bf16 [{rows},{cols}]", op="softmax", rows=rows, cols=cols)
+    w.arrays["x"] = normal_bf16((rows, cols), s, 0, 0.0, 4.0)
+    return w

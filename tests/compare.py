@@ -46,3 +46,32 @@ def assert_bits_equal(got, ref, what: str = ""):
         g, o = g.view(np.uint8), o.view(np.uint8)
     neq = g != o
     assert not neq.any(), f"{what}: {int(neq.sum())} mismatches, first {np.argwhere(neq)[:5].tolist()}"
+
+
+def bf16_nearest_bits(ref) -> np.ndarray:
+    """bf16 bit patterns nearest (ties to even) to fp64 values, by way of fp32
+    (the double rounding can move a value by at most one bf16 step)."""
+    f = np.asarray(ref, dtype=np.float64).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    r[np.isnan(f)] = 0x7FC0
+    return r
+
+
+def assert_bf16_within_steps(got_bits, ref, steps: int = 1, what: str = ""):
+    """Non-negative bf16 results (uint16 bit patterns) within `steps` bf16
+    steps of the nearest bf16 to the oracle's fp64 value; NaN where the oracle
+    has NaN."""
+    g = np.asarray(got_bits, dtype=np.uint16)
+    o = np.asarray(ref, dtype=np.float64)
+    assert g.shape == o.shape, f"{what}: shape {g.shape} vs {o.shape}"
+    gn = (g & 0x7FFF) > 0x7F80
+    on = np.isnan(o)
+    bad = gn != on
+    assert not bad.any(), f"{what}: NaN mismatch at {np.argwhere(bad)[:5].tolist()}"
+    assert (o[~on] >= 0).all() and not (g[~gn] & 0x8000).any(), f"{what}: negative values"
+    d = np.abs(g[~gn].astype(np.int64) - bf16_nearest_bits(o[~on]).astype(np.int64))
+    if d.size and d.max() > steps:
+        k = tuple(np.argwhere(~gn)[np.argmax(d)])
+        raise AssertionError(f"{what}: worst at {list(k)}: gpu bits {int(g[k]):#06x} "
+                             f"oracle {o[k]!r} ({int(d.max())} bf16 steps > {steps})")

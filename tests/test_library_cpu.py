@@ -18,7 +18,8 @@ def declared_symbols():
 
 def test_header_declares_the_entry_points():
     names = declared_symbols()
-    for must in ("fr_reduce_relu_add_sum", "fr_softmax", "fr_layernorm", "fr_xent",
+    for must in ("fr_reduce_relu_add_sum", "fr_reduce_sumsq", "fr_softmax", "fr_layernorm",
+                 "fr_xent",
                  "fr_workspace_size", "fr_check_device_error", "fr_status_string"):
         assert must in names
 
@@ -105,9 +106,16 @@ def test_argument_validation_needs_no_device():
     big = 1 << 40
     assert lib.fr_reduce_relu_add_sum(good, good, good, big, big, big, big, 0, 2.0, 0, None, 0,
                                       None) == 1
+    # sum of squares / row L2 norm
+    assert lib.fr_reduce_sumsq(None, good, 4, 8, 8, 0, 0, 0, None, 0, None) == 1
+    assert lib.fr_reduce_sumsq(good, good, 4, 8, 7, 0, 0, 0, None, 0, None) == 1
+    assert lib.fr_reduce_sumsq(good, good, 4, 8, 8, 1, 0, 0, None, 0, None) == 2
+    assert lib.fr_reduce_sumsq(good, good, 4, 8, 8, 0, 2, 0, None, 0, None) == 1  # epilogue
+    assert lib.fr_reduce_sumsq(odd, good, 4, 8, 8, 0, 1, 0, None, 0, None) == 4
     # softmax
     assert lib.fr_softmax(good, good, 4, 0, 8, 8, 0, 0, None) == 1
-    assert lib.fr_softmax(good, good, 4, 8, 8, 8, 1, 0, None) == 2
+    assert lib.fr_softmax(good, good, 4, 8, 8, 8, 2, 0, None) == 2      # no such dtype
+    assert lib.fr_softmax(odd, good, 4, 8, 8, 8, 1, 0, None) == 4       # bf16, odd address
     assert lib.fr_softmax(good, good, 4, 8, 8, 16, 0, 0, None) == 1   # in place, ldx != ldy
     assert lib.fr_softmax(good, odd, 4, 8, 8, 8, 0, 0, None) == 4
     # layernorm

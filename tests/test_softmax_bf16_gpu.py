@@ -1,0 +1,87 @@
+"""GPU parity of the bf16 softmax (bf16 rows in and out, fp32 arithmetic;
+"Stax (4): GPU Codegen and Dynamic Shapes", section 9.5, Listing 9.5) against
+the oracle's fp64 softmax of the same (exactly widened) values: every output
+within one bf16 step of the nearest bf16 to the oracle's value."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import reduction_pointwise_row_gb300 as fr
+from compare import assert_bf16_within_steps
+from gpu_util import empty_like_placed, place
+from synth import workloads
+
+pytestmark = pytest.mark.gpu
+
+COLS = [1, 2, 15, 16, 17, 31, 129, 511, 512, 513, 1000, 1024, 1536, 2047, 2048, 2049, 4097,
+        65537]
+# (offset of x, offset of y, extra row padding), in elements
+LAYOUTS = [(0, 0, 0), (3, 3, 7), (0, 5, 0)]
+
+
+@pytest.fixture(scope="module")
+def o():
+    return oracle.get()
+
+
+def widen(bits):
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+def forms(cols):
+    return (["persistent"] if cols <= 2048 else []) + ["looped", "auto"]
+
+
+def run(bits, form, layout=(0, 0, 0)):
+    rows, cols = bits.shape
+    ox, oy, pad = layout
+    px = place(bits, ox, cols + pad)
+    py = empty_like_placed(rows, cols, torch.bfloat16, oy, cols + pad)
+    fr.fr_softmax(px.t, form=form, out=py.t)
+    torch.cuda.synchronize()
+    assert py.canaries_intact(), "softmax wrote outside y"
+    return py.t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("cols", COLS)
+@pytest.mark.parametrize("rows", [1, 9, 40])
+@pytest.mark.parametrize("layout", LAYOUTS, ids=["aligned", "offset_same_phase", "offset_scalar"])
+def test_softmax_bf16_forms(o, rows, cols, layout):
+    bits = workloads.make_softmax_bf16(rows, cols, seed=6000 + rows * 11 + cols).arrays["x"]
+    ref = o.softmax(widen(bits))
+    for form in forms(cols):
+        assert_bf16_within_steps(run(bits, form, layout), ref, 1, f"{form} {rows}x{cols} {layout}")
+
+
+@pytest.mark.parametrize("cols", [7, 1000, 2048, 4097])
+def test_softmax_bf16_special_values(o, cols):
+    bits = workloads.make_softmax_bf16(6, cols, seed=61).arrays["x"].copy()
+    bits[1, cols // 2] = 0x7FC0               # NaN row
+    bits[2, : cols // 2] = 0xFF80             # partly -inf
+    bits[3, :] = 0xFF80                       # all -inf: 0/0
+    bits[4, cols - 1] = 0x7F80                # +inf: inf - inf
+    ref = o.softmax(widen(bits))
+    for form in forms(cols):
+        got = run(bits, form)
+        assert_bf16_within_steps(got, ref, 1, f"{form} special {cols}")
+
+
+def test_softmax_bf16_in_place_and_full_headline_shape(o):
+    """In place (x and y the same buffer), and the softmax workload's shape
+    [32768, 1024] in bf16 checked on sampled rows."""
+    bits = workloads.make_softmax_bf16(65, 1000).arrays["x"]
+    ref = o.softmax(widen(bits))
+    for form in ("persistent", "looped"):
+        t = torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
+        fr.fr_softmax(t, form=form, out=t)
+        got = t.view(torch.int16).cpu().numpy().view(np.uint16)
+        assert_bf16_within_steps(got, ref, 1, f"in place {form}")
+    full = workloads.make_softmax_bf16(32768, 1024).arrays["x"]
+    x = torch.from_numpy(full.view(np.int16)).cuda().view(torch.bfloat16)
+    y = fr.fr_softmax(x)
+    assert fr.fr_last_form() == "persistent"
+    got = y.view(torch.int16).cpu().numpy().view(np.uint16)
+    rows = np.random.default_rng(3).choice(32768, 64, replace=False)
+    rows.sort()
+    assert_bf16_within_steps(got[rows], o.softmax(widen(full[rows])), 1, "sampled rows")
