@@ -47,7 +47,8 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-extra", action="store_true", help="headline workload only")
     p.add_argument("--only", choices=["relu_add_sum", "softmax", "layernorm", "split", "xent",
-                                      "sumsq", "l2norm", "softmax_4097", "softmax_65537",
+                                      "sumsq", "l2norm", "softmax_4097", "softmax_4097_looped",
+                                      "softmax_65537", "softmax_65537_looped",
                                       "looped", "softmax_bf16"],
                    help="time one workload alone (for profiler captures) and exit")
     p.add_argument("--form", default="auto", choices=["auto", "persistent", "looped", "split"],
@@ -336,14 +337,17 @@ def setup_workload(name, fr, workloads, dev, form="auto"):
             y = torch.empty_like(x)
             calls.append(lambda x=x, y=y: fr.fr_softmax(x, out=y, form=form))
         return calls, "softmax", w.rows, w.cols, 1
-    if name in ("softmax_4097", "softmax_65537"):
-        # the looped online-softmax form on the two sweep lengths, 256 MiB each
+    if name in ("softmax_4097", "softmax_65537", "softmax_4097_looped", "softmax_65537_looped"):
+        # the two long-row sweep lengths, 256 MiB each: the form AUTO picks
+        # (one CTA per row at 4097, a cluster per row at 65537) and the looped
+        # online form
         cols = int(name.split("_")[1])
+        f = "looped" if name.endswith("_looped") else form
         w = workloads.make(1, rows=(1 << 25) // cols, cols=cols)
         for _ in range(nsets("softmax", w.rows, w.cols)):
             x = to_device(w.arrays["x"], dev)
             y = torch.empty_like(x)
-            calls.append(lambda x=x, y=y: fr.fr_softmax(x, out=y, form=form))
+            calls.append(lambda x=x, y=y: fr.fr_softmax(x, out=y, form=f))
         return calls, "softmax", w.rows, w.cols, 1
     if name == "softmax_bf16":
         # the bf16 softmax on [65536, 1024] (the fp32 workload's 256 MiB)
@@ -415,7 +419,8 @@ def setup_workload(name, fr, workloads, dev, form="auto"):
 EXTRA = {"relu_add_sum": "relu_add_sum_64x128", "layernorm": "layernorm_4096x32768",
          "split": "relu_add_sum_split_8x33554432", "xent": "xent_8192x50257",
          "sumsq": "sumsq_split_64x16384", "l2norm": "l2norm_looped_16384x16384",
-         "softmax_4097": "softmax_looped_8190x4097", "softmax_65537": "softmax_looped_511x65537",
+         "softmax_4097": "softmax_8190x4097", "softmax_4097_looped": "softmax_looped_8190x4097",
+         "softmax_65537": "softmax_511x65537", "softmax_65537_looped": "softmax_looped_511x65537",
          "looped": "relu_add_sum_looped_16384x8192", "softmax_bf16": "softmax_bf16_65536x1024"}
 
 

@@ -365,6 +365,14 @@ __device__ __forceinline__ void st_async_f4(const void *local_dst, const uint64_
       : "memory");
 }
 
+// Writes 8 bytes into the shared memory of CTA `rank` of this cluster (at the
+// address `local` has in this CTA); made visible by the next cluster barrier.
+__device__ __forceinline__ void st_cluster_f2(void *local, uint32_t rank, float a, float b) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(remote), "f"(a), "f"(b) : "memory");
+}
+
 __device__ __forceinline__ uint4 lds_u4(const void *p) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"

@@ -92,8 +92,16 @@ fr_form pick_ras(int64_t rows, int64_t cols, int sm_count) {
   return FR_FORM_LOOPED;
 }
 
-fr_form pick_softmax(int64_t, int64_t cols, bool vec) {
-  return cols <= fr::softmax_persistent_max_cols(vec) ? FR_FORM_PERSISTENT : FR_FORM_LOOPED;
+fr_form pick_softmax(int64_t rows, int64_t cols, bool vec, int sm_count) {
+  // A row within a warp: persistent.  Longer in-phase rows: persistent with a
+  // CTA per row while there are enough rows to fill the SMs, else split over a
+  // cluster of CTAs; rows out of phase or too long for a cluster: looped.
+  if (cols <= 1024) return FR_FORM_PERSISTENT;
+  if (vec && cols <= fr::softmax_persistent_max_cols(vec) &&
+      rows >= 4 * static_cast<int64_t>(sm_count))
+    return FR_FORM_PERSISTENT;
+  if (vec && cols <= fr::softmax_split_max_cols()) return FR_FORM_SPLIT;
+  return FR_FORM_LOOPED;
 }
 
 fr_form pick_layernorm(int64_t, int64_t cols, bool vec, int max_smem_optin) {
@@ -244,7 +252,7 @@ fr_status fr_softmax(const void *x, void *y, int64_t rows, int64_t cols, int64_t
       default: return FR_ERR_UNSUPPORTED_FORM;
     }
   }
-  const fr_form f = form == FR_FORM_AUTO ? pick_softmax(rows, cols, vec) : form;
+  const fr_form f = form == FR_FORM_AUTO ? pick_softmax(rows, cols, vec, info.sm_count) : form;
   const float *fx = static_cast<const float *>(x);
   float *fy = static_cast<float *>(y);
   switch (f) {
@@ -262,6 +270,10 @@ fr_status fr_softmax(const void *x, void *y, int64_t rows, int64_t cols, int64_t
     }
     case FR_FORM_LOOPED:
       return launched(fr::launch_softmax_looped(fx, fy, rows, cols, ldx, ldy, vec, info.sm_count, s), f);
+    case FR_FORM_SPLIT:
+      if (!vec || cols <= 1024 || cols > fr::softmax_split_max_cols() || rows > 0x7fffffff / 8)
+        return FR_ERR_UNSUPPORTED_FORM;
+      return launched(fr::launch_softmax_split(fx, fy, rows, cols, ldx, ldy, s), f);
     default: return FR_ERR_UNSUPPORTED_FORM;
   }
 }

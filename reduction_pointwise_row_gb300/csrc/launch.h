@@ -58,6 +58,12 @@ cudaError_t launch_softmax_async(const float *x, float *y, int64_t rows, int64_t
 cudaError_t launch_softmax_looped(const float *x, float *y, int64_t rows, int64_t cols,
                                   int64_t ldx, int64_t ldy, bool vec, int sm_count,
                                   cudaStream_t s);
+// Split form: a thread-block cluster of up to 8 CTAs per row exchanging the
+// (m, d) pairs through distributed shared memory (x and y in phase, rows of
+// 1025 .. 262144 elements).
+int64_t softmax_split_max_cols();
+cudaError_t launch_softmax_split(const float *x, float *y, int64_t rows, int64_t cols,
+                                 int64_t ldx, int64_t ldy, cudaStream_t s);
 
 // bf16 rows (x and y bf16, fp32 arithmetic): persistent up to 2048 columns.
 int64_t softmax_bf16_persistent_max_cols();

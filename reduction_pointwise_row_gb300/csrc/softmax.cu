@@ -133,6 +133,171 @@ softmax_warp_scalar(const float *__restrict__ x, float *__restrict__ y, int64_t 
   }
 }
 
+// Persistent form for rows longer than a warp holds: one CTA of T threads per
+// row, NV 32-byte vectors per thread in registers (body <= 8 * T * NV
+// elements; the head and tail scalars, at most 7 + 7, one per thread).  The max
+// and the sum are CTA reductions (one barrier each); each element is read once
+// and written once.  x and y rows share their offset modulo 32 bytes.
+template <int T, int NV>
+__global__ void __launch_bounds__(T)
+softmax_cta_vec(const float *__restrict__ x, float *__restrict__ y, int64_t cols, int64_t ldx,
+                int64_t ldy) {
+  constexpr int W = T / 32;
+  __shared__ float red[2][W];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t row = blockIdx.x;
+  const float *px = x + row * ldx;
+  float *py = y + row * ldy;
+  const RowSplit sp = row_split(px, cols, 4);
+  int64_t si = -1;
+  if (tid < sp.head) si = tid;
+  else if (tid < sp.head + sp.tail) si = sp.head + sp.nvec * 8 + (tid - sp.head);
+  const float *vx = px + sp.head;
+  V8 v[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int64_t vi = tid + static_cast<int64_t>(T) * k;
+    if (vi < sp.nvec) v[k] = ld_stream_v8(vx + vi * 8);
+  }
+  const float sv = si >= 0 ? ld_stream_f32(px + si) : -INFINITY;
+
+  float m = sv;
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+    if (tid + T * k < sp.nvec) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m = max_nan(m, fbits(v[k].w[j]));
+    }
+  m = warp_max_nan(m);
+  if (lane == 0) red[0][warp] = m;
+  __syncthreads();
+  m = warp_max_nan(lane < W ? red[0][lane] : -INFINITY);
+  const float mb = m * kLog2e;
+
+  const float se = si >= 0 ? ex2(fmaf(sv, kLog2e, -mb)) : 0.0f;
+  float d = se;
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+    if (tid + T * k < sp.nvec) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float e = ex2(fmaf(fbits(v[k].w[j]), kLog2e, -mb));
+        v[k].w[j] = __float_as_uint(e);
+        d += e;
+      }
+    }
+  d = warp_sum(d);
+  if (lane == 0) red[1][warp] = d;
+  __syncthreads();
+  d = warp_sum(lane < W ? red[1][lane] : 0.0f);
+  const float inv = __frcp_rn(d);
+
+  float *vy = py + sp.head;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int64_t vi = tid + static_cast<int64_t>(T) * k;
+    if (vi < sp.nvec) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[k].w[j] = __float_as_uint(fbits(v[k].w[j]) * inv);
+      st_stream_v8(vy + vi * 8, v[k]);
+    }
+  }
+  if (si >= 0) st_stream_f32(py + si, se * inv);
+}
+
+// Split form for long rows: a thread-block cluster of C CTAs holds one row,
+// CTA rank q its slice of the row's body vectors in registers (rank 0 also the
+// head scalars, rank C - 1 the tail).  Each CTA reduces its slice to the pair
+// (m_q, d_q) (two passes over registers), writes the pair into every CTA of
+// the cluster (distributed shared memory) and, after one cluster barrier,
+// merges the C pairs in rank order with the merge of section 9.5 -- the same
+// (M, D) in every CTA (Proposition 9.1 makes it the row's) -- then writes its
+// exponentials scaled by 2^((m_q - M) log2 e) / D.  One read and one write per
+// element; the exchange is 8 bytes per CTA pair.  No CTA touches a peer's
+// shared memory after the barrier, so CTAs may leave right after it.
+constexpr int kSmClusterMax = 8;
+
+template <int T, int NV>
+__global__ void __launch_bounds__(T)
+softmax_cluster(const float *__restrict__ x, float *__restrict__ y, int64_t cols, int64_t ldx,
+                int64_t ldy) {
+  constexpr int W = T / 32;
+  __shared__ float red[2][W];
+  __shared__ __align__(8) float2 pairs[kSmClusterMax];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t C = cluster_nctarank(), q = cluster_ctarank();
+  const int64_t row = cluster_id_x();
+  const float *px = x + row * ldx;
+  float *py = y + row * ldy;
+  const RowSplit sp = row_split(px, cols, 4);
+  const int64_t per = (sp.nvec + C - 1) / C;
+  const int64_t lo = per * q;
+  const int64_t hi = lo + per < sp.nvec ? lo + per : sp.nvec;
+  int64_t si = -1;  // head scalars: rank 0, threads 0..6; tail: rank C - 1, threads 32..38
+  if (q == 0 && tid < sp.head) si = tid;
+  else if (q == C - 1 && tid >= 32 && tid - 32 < sp.tail) si = sp.head + sp.nvec * 8 + (tid - 32);
+  const float *vx = px + sp.head;
+  V8 v[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int64_t vi = lo + tid + static_cast<int64_t>(T) * k;
+    if (vi < hi) v[k] = ld_stream_v8(vx + vi * 8);
+  }
+  const float sv = si >= 0 ? ld_stream_f32(px + si) : -INFINITY;
+
+  float m = sv;
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+    if (lo + tid + T * k < hi) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m = max_nan(m, fbits(v[k].w[j]));
+    }
+  m = warp_max_nan(m);
+  if (lane == 0) red[0][warp] = m;
+  __syncthreads();
+  m = warp_max_nan(lane < W ? red[0][lane] : -INFINITY);
+  // a slice of nothing but -inf contributes d = 0 (and scales to 0 below)
+  const float mb = m == -INFINITY ? 0.0f : m * kLog2e;
+
+  const float se = si >= 0 ? ex2(fmaf(sv, kLog2e, -mb)) : 0.0f;
+  float d = se;
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+    if (lo + tid + T * k < hi) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float e = ex2(fmaf(fbits(v[k].w[j]), kLog2e, -mb));
+        v[k].w[j] = __float_as_uint(e);
+        d += e;
+      }
+    }
+  d = warp_sum(d);
+  if (lane == 0) red[1][warp] = d;
+  __syncthreads();
+  d = warp_sum(lane < W ? red[1][lane] : 0.0f);
+  if (tid < static_cast<int>(C)) st_cluster_f2(&pairs[q], static_cast<uint32_t>(tid), m, d);
+  cluster_arrive();
+  cluster_wait();
+  float M = -INFINITY;
+  for (uint32_t r = 0; r < C; ++r) M = max_nan(M, pairs[r].x);
+  float D = 0.0f;
+  if (M != -INFINITY)
+    for (uint32_t r = 0; r < C; ++r) D += pairs[r].y * ex2((pairs[r].x - M) * kLog2e);
+  const float scale = (M == -INFINITY ? 1.0f : ex2((m - M) * kLog2e)) * __frcp_rn(D);
+
+  float *vy = py + sp.head;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int64_t vi = lo + tid + static_cast<int64_t>(T) * k;
+    if (vi < hi) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[k].w[j] = __float_as_uint(fbits(v[k].w[j]) * scale);
+      st_stream_v8(vy + vi * 8, v[k]);
+    }
+  }
+  if (si >= 0) st_stream_f32(py + si, se * scale);
+}
+
 // Fold `n` values (already max-reduced to cm) into the online pair st.
 __device__ __forceinline__ MD fold_chunk(MD st, float cm) {
   const float M = max_nan(st.m, cm);
@@ -342,11 +507,33 @@ unsigned warp_row_grid(int64_t rows) {
 
 }  // namespace
 
-int64_t softmax_persistent_max_cols(bool vec) { return vec ? 1024 : 1024; }
+// Rows up to 1024 take one warp; longer rows with a shared 32-byte phase take
+// one CTA of up to 1024 threads x 4 vectors (32768 elements, 128 KiB of
+// registers).
+int64_t softmax_persistent_max_cols(bool vec) { return vec ? 32768 : 1024; }
+
+namespace {
+template <int T, int NV>
+cudaError_t launch_cta(const float *x, float *y, int64_t rows, int64_t cols, int64_t ldx,
+                       int64_t ldy, cudaStream_t s) {
+  softmax_cta_vec<T, NV><<<static_cast<unsigned>(rows), T, 0, s>>>(x, y, cols, ldx, ldy);
+  return cudaGetLastError();
+}
+}  // namespace
 
 cudaError_t launch_softmax_persistent(const float *x, float *y, int64_t rows, int64_t cols,
                                       int64_t ldx, int64_t ldy, bool vec, cudaStream_t s) {
   const unsigned grid = warp_row_grid(rows);
+  if (vec && cols > 1024) {
+    if (rows > 0x7fffffff) return cudaErrorInvalidValue;
+    const int64_t nvec = cols / 8;  // at least the body's vectors
+    if (nvec <= 128 * 2) return launch_cta<128, 2>(x, y, rows, cols, ldx, ldy, s);
+    if (nvec <= 128 * 4) return launch_cta<128, 4>(x, y, rows, cols, ldx, ldy, s);
+    if (nvec <= 256 * 4) return launch_cta<256, 4>(x, y, rows, cols, ldx, ldy, s);
+    if (nvec <= 512 * 4) return launch_cta<512, 4>(x, y, rows, cols, ldx, ldy, s);
+    if (nvec <= 1024 * 4) return launch_cta<1024, 4>(x, y, rows, cols, ldx, ldy, s);
+    return cudaErrorInvalidValue;
+  }
   if (vec) {
     const int64_t nv = (cols + 255) / 256;
     switch (nv) {
@@ -399,6 +586,54 @@ cudaError_t launch_softmax_async(const float *x, float *y, int64_t rows, int64_t
   void *args[] = {&x, &y, &rows, &cols, &ldx, &ldy};
   return cudaLaunchKernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kAsyncThreads), args, smem,
                           s);
+}
+
+// The split (cluster) form: C CTAs of T threads x 4 vectors per row, the
+// smallest T in {256, 512, 1024} whose C-fold (C <= 8) holds the row's body;
+// 0 when no cluster holds it.
+namespace {
+bool cluster_shape(int64_t cols, int *T, int *C) {
+  const int64_t nvec = cols / 8;  // at least the body's vectors
+  for (int t = 256; t <= 1024; t <<= 1)
+    for (int c = 2; c <= kSmClusterMax; c <<= 1)
+      if (nvec <= static_cast<int64_t>(c) * t * 4) {
+        *T = t;
+        *C = c;
+        return true;
+      }
+  return false;
+}
+
+template <int T, int NV>
+cudaError_t launch_cluster_kernel(const float *x, float *y, int64_t rows, int64_t cols,
+                                  int64_t ldx, int64_t ldy, int C, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(C);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(rows * C));
+  cfg.blockDim = dim3(T);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, softmax_cluster<T, NV>, x, y, cols, ldx, ldy);
+}
+}  // namespace
+
+int64_t softmax_split_max_cols() { return static_cast<int64_t>(kSmClusterMax) * 1024 * 4 * 8; }
+
+cudaError_t launch_softmax_split(const float *x, float *y, int64_t rows, int64_t cols,
+                                 int64_t ldx, int64_t ldy, cudaStream_t s) {
+  int T = 0, C = 0;
+  if (!cluster_shape(cols, &T, &C) || rows * C > 0x7fffffff) return cudaErrorInvalidValue;
+  switch (T) {
+    case 256: return launch_cluster_kernel<256, 4>(x, y, rows, cols, ldx, ldy, C, s);
+    case 512: return launch_cluster_kernel<512, 4>(x, y, rows, cols, ldx, ldy, C, s);
+    default: return launch_cluster_kernel<1024, 4>(x, y, rows, cols, ldx, ldy, C, s);
+  }
 }
 
 cudaError_t launch_softmax_looped(const float *x, float *y, int64_t rows, int64_t cols,

@@ -28,11 +28,13 @@ def o():
     return oracle.get()
 
 
-def forms_for(op, cols):
+def forms_for(op, cols, in_phase=True):
     if op == "relu_add_sum":
         return (["persistent"] if cols <= 1024 else []) + ["looped", "split"]
-    if op == "softmax":
-        return (["persistent"] if cols <= 1024 else []) + ["looped"]
+    if op == "softmax":  # in phase, rows past 1024 stay persistent (a CTA per row) or
+        # split over a cluster of CTAs
+        return ((["persistent"] if cols <= 1024 or (cols <= 32768 and in_phase) else []) +
+                (["split"] if in_phase and 1024 < cols <= 262144 else []) + ["looped"])
     raise ValueError(op)
 
 
@@ -127,13 +129,14 @@ def run_softmax(x, form, layout=(0, 0, 0), kernel=None):
     return py.t.cpu().numpy()
 
 
-@pytest.mark.parametrize("cols", COLS + [65537])
+@pytest.mark.parametrize("cols", COLS + [2048, 2055, 2056, 8193, 16385, 32768, 32769, 65537])
 @pytest.mark.parametrize("rows", [1, 7, 33])
 @pytest.mark.parametrize("layout", LAYOUTS, ids=["aligned", "offset_same_phase", "offset_scalar"])
 def test_softmax_forms(o, rows, cols, layout):
     w = workloads.make(1, rows=rows, cols=cols, seed=2000 + rows * 7 + cols)
     ref = o.softmax(w.arrays["x"])
-    for form in forms_for("softmax", cols):
+    in_phase = layout[0] == layout[1]
+    for form in forms_for("softmax", cols, in_phase):
         for kernel in (("async", "plain") if form == "persistent" else (None,)):
             assert_close(run_softmax(w.arrays["x"], form, layout, kernel), ref, "f32",
                          f"{form}/{kernel} {rows}x{cols} {layout}")
@@ -167,14 +170,26 @@ def test_softmax_special_values(o, cols):
         assert np.isnan(got[[1, 3, 4]]).all() and np.isfinite(got[[0, 2, 5]]).all()
 
 
-def test_softmax_in_place_and_rows_sum_to_one(o):
-    w = workloads.make(1, rows=65, cols=1000)
+@pytest.mark.parametrize("cols", [1025, 8193, 32769, 65537, 131071, 262144])
+def test_softmax_split_long_rows(o, cols):
+    """The cluster split form on few long rows, row by row against the oracle,
+    and the form AUTO picks for them (split while a cluster holds the row)."""
+    w = workloads.make(1, rows=3, cols=cols, seed=2900 + cols)
     ref = o.softmax(w.arrays["x"])
-    for form in ("persistent", "looped"):
+    assert_close(run_softmax(w.arrays["x"], "split"), ref, "f32", f"split 3x{cols}")
+    assert_close(run_softmax(w.arrays["x"], "auto"), ref, "f32", f"auto 3x{cols}")
+    assert fr.fr_last_form() == "split"
+
+
+def test_softmax_in_place_and_rows_sum_to_one(o):
+    for form, cols in (("persistent", 1000), ("looped", 1000), ("persistent", 5000),
+                       ("split", 5000)):
+        w = workloads.make(1, rows=65, cols=cols)
+        ref = o.softmax(w.arrays["x"])
         t = torch.from_numpy(w.arrays["x"]).cuda()
         fr.fr_softmax(t, form=form, out=t)
         got = t.cpu().numpy()
-        assert_close(got, ref, "f32", f"in place {form}")
+        assert_close(got, ref, "f32", f"in place {form} {cols}")
         assert np.abs(got.astype(np.float64).sum(1) - 1).max() < 1e-5
 
 
@@ -363,5 +378,8 @@ def test_auto_form_choices():
     fr.fr_softmax(x)
     assert fr.fr_last_form() == "persistent"
     x = torch.zeros(16, 4097, device="cuda")
+    fr.fr_softmax(x)
+    assert fr.fr_last_form() == "persistent"  # one CTA per row
+    x = torch.zeros(4, 32769, device="cuda")
     fr.fr_softmax(x)
     assert fr.fr_last_form() == "looped"
