@@ -49,7 +49,7 @@ def parse():
     p.add_argument("--only", choices=["relu_add_sum", "softmax", "layernorm", "split", "xent",
                                       "sumsq", "l2norm", "softmax_4097", "softmax_4097_looped",
                                       "softmax_65537", "softmax_65537_looped",
-                                      "looped", "softmax_bf16"],
+                                      "looped", "softmax_bf16", "xent_box"],
                    help="time one workload alone (for profiler captures) and exit")
     p.add_argument("--form", default="auto", choices=["auto", "persistent", "looped", "split"],
                    help="with --only: force a reduction form")
@@ -215,6 +215,10 @@ def run_ours(args):
         ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
         return max_over_ranks(statistics.fmean(ms) / 1e3), launches_per_call * steps, ms
 
+    if args.only == "xent_box":
+        if rank == 0:
+            print(json.dumps(xent_box(fr, workloads, dev, timed, args, peak)), flush=True)
+        return
     if args.only:
         res = extra_configs(fr, traffic, workloads, timed, dev, peak, args, world, [args.only],
                             args.form)
@@ -441,6 +445,10 @@ def extra_configs(fr, traffic, workloads, timed, dev, peak, args, world, names=N
         if name in ("relu_add_sum", "sumsq"):
             res[EXTRA[name]].update(graph_replay(calls[0], steps, args.warmup))
             res[EXTRA[name]]["_launches"] += GRAPH_CALLS * steps * lpc
+        if name == "xent":
+            tuned = tune_xent(fr, workloads, dev, calls, timed, steps, args, nb, peak)
+            res[EXTRA[name]]["_launches"] += tuned.pop("_launches")
+            res[EXTRA[name]].update(tuned)
         del calls
         if op == "layernorm" and not args.only:
             # context: a device copy of the same bytes (x in, y out)
@@ -452,6 +460,52 @@ def extra_configs(fr, traffic, workloads, timed, dev, peak, args, world, names=N
             res[EXTRA.get(name, name)]["same_bytes_device_copy_gbs"] = round(nb / tc / 1e9, 2)
             del srcs, dsts, cps
     return res
+
+
+def xent_box(fr, workloads, dev, timed, args, peak):
+    """Every runnable point of the cross-entropy kernel's configuration box
+    (threads x vectors x stages x CTAs per SM), timed like the bench's other
+    lines: the measurements behind the default configuration."""
+    from reduction_pointwise_row_gb300 import traffic
+    calls, op, rows, cols, _ = setup_workload("xent", fr, workloads, dev)
+    nb = traffic.algorithmic_bytes(op, rows, cols)
+    steps = max(3, min(args.steps, 30))
+    out = []
+    for t in (128, 256, 512, 1024):
+        for u in (1, 2, 4, 8):
+            for s in (2, 4, 8):
+                for g in (1, 2, 4, 8, 16):
+                    try:
+                        fr.fr_xent_set_config(rows, cols, (t, u, s, g))
+                    except fr.FRError:
+                        continue
+                    sec, _, _ = timed(calls, steps, args.warmup, 1)
+                    out.append({"config": [t, u, s, g], "us": round(sec * 1e6, 2),
+                                "frac": round(nb / sec / 1e9 / peak, 4)})
+    fr.fr_xent_set_config(rows, cols, None)
+    out.sort(key=lambda r: r["us"])
+    return {"only": "xent_box", "rows": rows, "cols": cols, "runnable": len(out),
+            "default_config": list(fr.fr_xent_get_config(rows, cols)), "points": out}
+
+
+def tune_xent(fr, workloads, dev, calls, timed, steps, args, nb, peak):
+    """Launch-configuration search for the cross-entropy kernel on this
+    workload (candidate set, then coordinate descent, eps = 0.02), followed by
+    the same back-to-back timing with the chosen configuration."""
+    import torch
+    w = workloads.make(4)
+    lg = to_device(w.arrays["logits"], dev)
+    tg = torch.from_numpy(w.arrays["target"]).to(dev)
+    fr.fr_xent_set_config(w.rows, w.cols, None)
+    default = fr.fr_xent_get_config(w.rows, w.cols)
+    r = fr.fr_xent_tune(lg, tg, -100, eps=0.02, reps=5)
+    del lg
+    t, n, _ = timed(calls, steps, args.warmup, 1)
+    fr.fr_xent_set_config(w.rows, w.cols, None)
+    return {"default_config": list(default), "tuned_config": list(r["config"]),
+            "tune_evaluations": r["evaluations"], "tuned_us": round(t * 1e6, 3),
+            "tuned_gbs": round(nb / t / 1e9, 2), "tuned_frac": round(nb / t / 1e9 / peak, 4),
+            "_launches": n}
 
 
 GRAPH_CALLS = 64  # calls recorded in one CUDA graph for the launch-bound case

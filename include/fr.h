@@ -223,6 +223,94 @@ fr_status fr_xent(const void *logits, const int64_t *target, float *loss, float 
                   int64_t ld, int64_t ignore_index, fr_dtype dtype, fr_form form,
                   void *workspace, size_t workspace_bytes, fr_stream_t stream);
 
+/* ---- launch configurations ----------------------------------------------
+ *
+ * "Stax (4)", section 9.6: a kernel's launch configuration is a point of a
+ * box of parameters (Definition 9.2), chosen by measuring a small candidate
+ * set (Algorithm 9.1) and refined by coordinate descent (Algorithm 9.2).
+ */
+
+/* Largest number of parameters fr_coordinate_descent takes. */
+#define FR_CD_MAX_PARAMS 8
+
+/* Measured cost of a configuration given as log2 of each parameter; return
+ * +inf (or NaN) for a configuration that cannot run. */
+typedef double (*fr_cost_fn)(const int32_t *log2_params, void *ctx);
+
+/*
+ * Algorithm 9.2 over the box lo[i] <= c[i] <= hi[i] of log2 parameters: the
+ * neighbours of c are c with one coordinate +1 or -1 (that parameter times or
+ * divided by 2); a neighbour is accepted when its cost is below (1 - eps)
+ * times the current one; the search ends after a full pass without an
+ * acceptance.  Each configuration is costed at most once (the result is
+ * remembered), so by Proposition 9.2 the number of acceptances is at most
+ * min(|box|, ceil(log(t(c0) / t_min) / -log(1 - eps))) and no neighbour of
+ * the result is cheaper by the factor (1 - eps).  Host code only; runs on the
+ * calling thread.
+ *
+ *   p            number of parameters, 1 .. FR_CD_MAX_PARAMS
+ *   lo, hi       the box, per parameter (lo[i] <= hi[i])
+ *   c            in: the start (inside the box, finite cost); out: the result
+ *   eps          acceptance threshold, 0 < eps < 1
+ *   acceptances  moves accepted (may be NULL)
+ *   evaluations  distinct configurations costed (may be NULL)
+ * FR_ERR_INVALID_ARG for a bad argument or a start of infinite cost (c is
+ * then left unchanged).
+ */
+fr_status fr_coordinate_descent(int32_t p, const int32_t *lo, const int32_t *hi, int32_t *c,
+                                double eps, fr_cost_fn cost, void *ctx, int32_t *acceptances,
+                                int32_t *evaluations);
+
+/* A launch configuration of the cross-entropy kernel (fr_xent without
+ * argmax): each field a power of two. */
+typedef struct {
+  int32_t threads;     /* threads per CTA, 128 .. 1024 */
+  int32_t vectors;     /* 16-byte copies per thread per ring item, 1 .. 8 */
+  int32_t stages;      /* items in each thread's copy ring, 2 .. 8 */
+  int32_t ctas_per_sm; /* CTAs per SM of the persistent grid, 1 .. 16 */
+} fr_xent_config;
+
+/*
+ * The configuration fr_xent uses (without argmax) for this shape on the
+ * current device: the one recorded by fr_xent_tune or fr_xent_set_config,
+ * else the default.  FR_ERR_INVALID_ARG for a bad shape or a NULL out.
+ */
+fr_status fr_xent_get_config(int64_t rows, int64_t cols, int64_t ld, fr_xent_config *out);
+
+/*
+ * Records `cfg` for this shape on the current device (NULL forgets the
+ * record).  FR_ERR_INVALID_ARG when cfg is outside the box,
+ * FR_ERR_UNSUPPORTED_FORM when it cannot run on this device (shared memory,
+ * residency of ctas_per_sm CTAs, register spills).  Records live until the
+ * process exits.
+ */
+fr_status fr_xent_set_config(int64_t rows, int64_t cols, int64_t ld, const fr_xent_config *cfg);
+
+/*
+ * Chooses and records the configuration for this shape by measurement on the
+ * caller's data (Algorithm 9.1 then Algorithm 9.2).  If a configuration is
+ * already recorded for the shape it is returned unmeasured (Algorithm 9.1,
+ * line 1).  Otherwise a candidate set of six configurations is timed (those
+ * that cannot run cost +inf), and coordinate descent with threshold `eps`
+ * walks the box threads x vectors x stages x ctas_per_sm from the fastest.
+ * Each configuration is timed over `reps` launches after one warm-up launch
+ * (CUDA events on `stream`, the median).  The launches write `loss` (which
+ * may be NULL); the call synchronises `stream` and must not be captured into
+ * a CUDA graph.  Inputs larger than the L2 cache give cold-cache times.
+ *
+ *   logits, target, rows, cols, ld, ignore_index, dtype   as for fr_xent
+ *   eps          0 < eps < 1; above twice the relative timing noise
+ *   reps         1 .. 1000
+ *   out          the chosen configuration (may be NULL)
+ *   evaluations  configurations timed (may be NULL)
+ *   best_ms      median time of the chosen configuration (may be NULL; 0
+ *                when the record was returned unmeasured)
+ */
+fr_status fr_xent_tune(const void *logits, const int64_t *target, float *loss, int64_t rows,
+                       int64_t cols, int64_t ld, int64_t ignore_index, fr_dtype dtype,
+                       double eps, int32_t reps, fr_stream_t stream, fr_xent_config *out,
+                       int32_t *evaluations, float *best_ms);
+
 /*
  * Size of the library's built-in scratch array used by
  * fr_reduce_relu_add_sum_split_static (64 KiB = 8192 fp64 partial sums).

@@ -26,7 +26,8 @@ __all__ = [
     "FR_OK", "FRError", "lib", "fr_version", "fr_workspace_size", "fr_last_form",
     "fr_reduce_relu_add_sum", "fr_reduce_sumsq", "fr_softmax", "fr_layernorm", "fr_xent",
     "fr_reduce_relu_add_sum_split_static", "fr_check_device_error", "FORMS", "OPS",
-    "EPILOGUES",
+    "EPILOGUES", "fr_coordinate_descent", "fr_xent_get_config", "fr_xent_set_config",
+    "fr_xent_tune",
 ]
 
 FR_OK = 0
@@ -57,6 +58,12 @@ SIGNATURES = {
     "fr_xent": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _int, _vp,
                        _sz, _vp]),
     "fr_check_device_error": (_int, [_vp, ctypes.POINTER(ctypes.c_int32)]),
+    "fr_coordinate_descent": (_int, [ctypes.c_int32, _vp, _vp, _vp, ctypes.c_double, _vp, _vp,
+                                     _vp, _vp]),
+    "fr_xent_get_config": (_int, [_i64, _i64, _i64, _vp]),
+    "fr_xent_set_config": (_int, [_i64, _i64, _i64, _vp]),
+    "fr_xent_tune": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, ctypes.c_double,
+                            ctypes.c_int32, _vp, _vp, _vp, _vp]),
     "fr_reduce_relu_add_sum_split_static": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _int,
                                                    _f32, _vp]),
 }
@@ -251,6 +258,64 @@ def fr_reduce_relu_add_sum_split_static(a, b, scale: float = 2.0, out=None, stre
                                                      _stream(stream)),
            "fr_reduce_relu_add_sum_split_static")
     return out
+
+
+# ---- launch configurations ----------------------------------------------------
+
+COST_FN = ctypes.CFUNCTYPE(ctypes.c_double, ctypes.POINTER(ctypes.c_int32), ctypes.c_void_p)
+
+
+class XentConfig(ctypes.Structure):
+    _fields_ = [("threads", ctypes.c_int32), ("vectors", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32)]
+
+    def as_tuple(self):
+        return (self.threads, self.vectors, self.stages, self.ctas_per_sm)
+
+
+def fr_coordinate_descent(lo, hi, start, eps: float, cost):
+    """Coordinate descent (Algorithm 9.2) over log2 parameters in the box
+    [lo, hi] from ``start``; ``cost(tuple)`` returns a time (inf: cannot run).
+    Returns (result, acceptances, evaluations)."""
+    p = len(start)
+    arr = ctypes.c_int32 * p
+    c_lo, c_hi, c = arr(*lo), arr(*hi), arr(*start)
+    fn = COST_FN(lambda q, _ctx: float(cost(tuple(q[i] for i in range(p)))))
+    acc, ev = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(lib().fr_coordinate_descent(p, ctypes.byref(c_lo), ctypes.byref(c_hi),
+                                       ctypes.byref(c), eps, ctypes.cast(fn, ctypes.c_void_p),
+                                       None, ctypes.byref(acc), ctypes.byref(ev)),
+           "fr_coordinate_descent")
+    return tuple(c), acc.value, ev.value
+
+
+def fr_xent_get_config(rows: int, cols: int, ld: int | None = None) -> tuple:
+    out = XentConfig()
+    _check(lib().fr_xent_get_config(rows, cols, cols if ld is None else ld, ctypes.byref(out)),
+           "fr_xent_get_config")
+    return out.as_tuple()
+
+
+def fr_xent_set_config(rows: int, cols: int, cfg, ld: int | None = None):
+    """Records (threads, vectors, stages, ctas_per_sm) for this shape; None forgets."""
+    ptr = None if cfg is None else ctypes.byref(XentConfig(*cfg))
+    _check(lib().fr_xent_set_config(rows, cols, cols if ld is None else ld, ptr),
+           "fr_xent_set_config")
+
+
+def fr_xent_tune(logits, target, ignore_index: int = -100, eps: float = 0.02, reps: int = 5,
+                 loss=None, stream=None) -> dict:
+    """Algorithm 9.1 + 9.2 on the caller's data; records and returns the chosen
+    configuration with the number of configurations timed and its median ms."""
+    import torch
+    assert logits.is_cuda and logits.dtype == torch.bfloat16 and logits.dim() == 2
+    rows, cols = logits.shape
+    out, ev, ms = XentConfig(), ctypes.c_int32(0), ctypes.c_float(0)
+    _check(lib().fr_xent_tune(_ptr(logits), _ptr(target), _ptr(loss), rows, cols, _ld(logits),
+                              ignore_index, DTYPES["bf16"], eps, reps, _stream(stream),
+                              ctypes.byref(out), ctypes.byref(ev), ctypes.byref(ms)),
+           "fr_xent_tune")
+    return {"config": out.as_tuple(), "evaluations": ev.value, "ms": ms.value}
 
 
 def fr_check_device_error(stream=None) -> int:

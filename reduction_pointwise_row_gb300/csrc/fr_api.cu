@@ -6,10 +6,14 @@
 // order and nothing synchronises.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <limits>
 #include <mutex>
+#include <vector>
 
 #include "../../include/fr.h"
 #include "launch.h"
@@ -350,6 +354,164 @@ fr_status fr_xent(const void *logits, const int64_t *target, float *loss, float 
                                   target_logit, argmax, rows, cols, ld, ignore_index, workspace,
                                   info.sm_count, info.max_smem_optin, s),
                   FR_FORM_LOOPED);
+}
+
+namespace {
+
+fr::XentConfig from_c(const fr_xent_config &c) {
+  return fr::XentConfig{c.threads, c.vectors, c.stages, c.ctas_per_sm};
+}
+fr_xent_config to_c(const fr::XentConfig &c) {
+  return fr_xent_config{c.threads, c.vectors, c.stages, c.ctas_per_sm};
+}
+
+// Median time (ms) of `reps` launches of configuration cfg after one warm-up
+// launch; +inf when the configuration cannot run.
+double time_xent_config(const fr::XentConfig &cfg, const uint16_t *logits, const int64_t *target,
+                        float *loss, int64_t rows, int64_t cols, int64_t ld,
+                        int64_t ignore_index, int reps, const fr::DevInfo &info,
+                        cudaStream_t s) {
+  const double inf = std::numeric_limits<double>::infinity();
+  if (fr::xent_config_check(cfg, info.max_smem_optin) != cudaSuccess) {
+    cudaGetLastError();
+    return inf;
+  }
+  auto launch = [&]() {
+    return fr::launch_xent_config(cfg, logits, target, loss, nullptr, nullptr, rows, cols, ld,
+                                  ignore_index, nullptr, info.sm_count, info.max_smem_optin, s);
+  };
+  if (launch() != cudaSuccess) {
+    cudaGetLastError();
+    return inf;
+  }
+  std::vector<cudaEvent_t> ev(2 * static_cast<size_t>(reps));
+  for (auto &e : ev)
+    if (cudaEventCreate(&e) != cudaSuccess) return inf;
+  bool ok = true;
+  for (int r = 0; r < reps && ok; ++r) {
+    ok = cudaEventRecord(ev[2 * r], s) == cudaSuccess && launch() == cudaSuccess &&
+         cudaEventRecord(ev[2 * r + 1], s) == cudaSuccess;
+  }
+  std::vector<double> ms;
+  if (ok && cudaStreamSynchronize(s) == cudaSuccess) {
+    for (int r = 0; r < reps; ++r) {
+      float t = 0.0f;
+      if (cudaEventElapsedTime(&t, ev[2 * r], ev[2 * r + 1]) != cudaSuccess) {
+        ok = false;
+        break;
+      }
+      ms.push_back(t);
+    }
+  } else {
+    ok = false;
+  }
+  for (auto &e : ev) cudaEventDestroy(e);
+  if (!ok) {
+    cudaGetLastError();
+    return inf;
+  }
+  std::sort(ms.begin(), ms.end());
+  return ms[ms.size() / 2];
+}
+
+int ilog2(int v) {
+  int k = 0;
+  while ((1 << (k + 1)) <= v) ++k;
+  return k;
+}
+
+}  // namespace
+
+fr_status fr_xent_get_config(int64_t rows, int64_t cols, int64_t ld, fr_xent_config *out) {
+  if (!out || !shape_ok(rows, cols, ld, 2)) return FR_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return FR_ERR_NO_DEVICE;
+  }
+  fr::XentConfig c = fr::xent_default_config();
+  fr::xent_recorded_config(dev, rows, cols, ld, &c);
+  *out = to_c(c);
+  return FR_OK;
+}
+
+fr_status fr_xent_set_config(int64_t rows, int64_t cols, int64_t ld, const fr_xent_config *cfg) {
+  if (!shape_ok(rows, cols, ld, 2)) return FR_ERR_INVALID_ARG;
+  fr::DevInfo info;
+  if (fr_status st = device_ok(&info)) return st;
+  if (cfg == nullptr) {
+    fr::xent_record_config(info.device, rows, cols, ld, nullptr);
+    return FR_OK;
+  }
+  const fr::XentConfig c = from_c(*cfg);
+  const cudaError_t e = fr::xent_config_check(c, info.max_smem_optin);
+  if (e == cudaErrorInvalidValue) return FR_ERR_INVALID_ARG;
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FR_ERR_UNSUPPORTED_FORM;
+  }
+  fr::xent_record_config(info.device, rows, cols, ld, &c);
+  return FR_OK;
+}
+
+fr_status fr_xent_tune(const void *logits, const int64_t *target, float *loss, int64_t rows,
+                       int64_t cols, int64_t ld, int64_t ignore_index, fr_dtype dtype,
+                       double eps, int32_t reps, fr_stream_t stream, fr_xent_config *out,
+                       int32_t *evaluations, float *best_ms) {
+  if (dtype != FR_BF16) return FR_ERR_UNSUPPORTED_DTYPE;
+  if (!logits || !target) return FR_ERR_INVALID_ARG;
+  if (!shape_ok(rows, cols, ld, 2)) return FR_ERR_INVALID_ARG;
+  if (!(eps > 0.0 && eps < 1.0) || reps < 1 || reps > 1000) return FR_ERR_INVALID_ARG;
+  if (!aligned(logits, 2) || !aligned(target, 8) || (loss && !aligned(loss, 4)))
+    return FR_ERR_MISALIGNED;
+  if (cols >= (INT64_C(1) << 31)) return FR_ERR_UNSUPPORTED_FORM;
+  fr::DevInfo info;
+  if (fr_status st = device_ok(&info)) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const uint16_t *lg = static_cast<const uint16_t *>(logits);
+  if (evaluations) *evaluations = 0;
+  if (best_ms) *best_ms = 0.0f;
+
+  fr::XentConfig best{};
+  if (fr::xent_recorded_config(info.device, rows, cols, ld, &best)) {  // Algorithm 9.1, line 1
+    if (out) *out = to_c(best);
+    return FR_OK;
+  }
+  int evals = 0;
+  auto cost = [&](const fr::XentConfig &c) {
+    ++evals;
+    return time_xent_config(c, lg, target, loss, rows, cols, ld, ignore_index, reps, info, s);
+  };
+  // Algorithm 9.1: the fastest of a small candidate set (the hand-picked
+  // shapes the kernel was developed with, and the default).
+  const fr::XentConfig cands[] = {fr::xent_default_config(), {256, 4, 4, 2}, {512, 4, 4, 1},
+                                  {128, 4, 4, 4},            {256, 2, 8, 2}, {256, 8, 2, 2}};
+  double t_best = std::numeric_limits<double>::infinity();
+  for (const fr::XentConfig &c : cands) {
+    const double t = cost(c);
+    if (t < t_best) {
+      t_best = t;
+      best = c;
+    }
+  }
+  if (!std::isfinite(t_best)) return FR_ERR_CUDA;  // nothing could run
+  // Algorithm 9.2 from there over the box of log2 parameters.
+  const int lo[4] = {7, 0, 1, 0}, hi[4] = {10, 3, 3, 4};
+  int c[4] = {ilog2(best.threads), ilog2(best.vectors), ilog2(best.stages),
+              ilog2(best.ctas_per_sm)};
+  const fr::CdResult r = fr::coordinate_descent(4, lo, hi, c, eps, [&](const int *q) {
+    const fr::XentConfig x{1 << q[0], 1 << q[1], 1 << q[2], 1 << q[3]};
+    if (x.threads == best.threads && x.vectors == best.vectors && x.stages == best.stages &&
+        x.ctas_per_sm == best.ctas_per_sm)
+      return t_best;  // already timed
+    return cost(x);
+  });
+  best = fr::XentConfig{1 << c[0], 1 << c[1], 1 << c[2], 1 << c[3]};
+  fr::xent_record_config(info.device, rows, cols, ld, &best);
+  if (out) *out = to_c(best);
+  if (evaluations) *evaluations = evals;
+  if (best_ms) *best_ms = static_cast<float>(r.t);
+  return cudaGetLastError() == cudaSuccess ? FR_OK : FR_ERR_CUDA;
 }
 
 fr_status fr_check_device_error(fr_stream_t stream, int32_t *code) {

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <functional>
 #include <cuda_runtime.h>
 
 namespace fr {
@@ -105,7 +106,45 @@ cudaError_t launch_layernorm_looped(const uint16_t *x, const float *gamma, const
                                     bool vec, int sm_count, int max_smem_optin,
                                     cudaStream_t s);
 
+// ---- launch-configuration search (Algorithm 9.2) -----------------------------
+
+struct CdResult {
+  int acceptances;  // moves accepted
+  int evaluations;  // distinct configurations measured
+  double t;         // cost of the returned configuration
+};
+// Coordinate descent over log2 parameters c[i] in [lo[i], hi[i]]; c is updated
+// in place.  A start of infinite cost returns at once (t = inf).
+CdResult coordinate_descent(int p, const int *lo, const int *hi, int *c, double eps,
+                            const std::function<double(const int *)> &cost);
+
 // ---- cross entropy ---------------------------------------------------------
+
+// One point of the cross-entropy kernel's configuration space.
+struct XentConfig {
+  int threads;      // per CTA: 128 .. 1024
+  int vectors;      // 16-byte copies per thread per item: 1 .. 8
+  int stages;       // items in the per-thread ring: 2 .. 8
+  int ctas_per_sm;  // CTAs per SM in the persistent grid: 1 .. 16
+};
+// The configuration used when none was recorded for a shape.
+XentConfig xent_default_config();
+// cudaSuccess when cfg is in the space and can run on this device (shared
+// memory, residency of ctas_per_sm CTAs, no register spills);
+// cudaErrorInvalidValue outside the space, cudaErrorInvalidConfiguration when
+// it cannot run.
+cudaError_t xent_config_check(const XentConfig &cfg, int max_smem_optin);
+// The configuration recorded for (device, rows, cols, ld), if any; recording
+// nullptr forgets it.
+bool xent_recorded_config(int device, int64_t rows, int64_t cols, int64_t ld, XentConfig *out);
+void xent_record_config(int device, int64_t rows, int64_t cols, int64_t ld,
+                        const XentConfig *cfg);
+// The non-argmax kernel with configuration cfg.
+cudaError_t launch_xent_config(const XentConfig &cfg, const uint16_t *logits,
+                               const int64_t *target, float *loss, float *loss_mean,
+                               float *target_logit, int64_t rows, int64_t cols, int64_t ld,
+                               int64_t ignore_index, void *workspace, int sm_count,
+                               int max_smem_optin, cudaStream_t s);
 
 size_t xent_workspace(int64_t rows, int sm_count);
 cudaError_t launch_xent(const uint16_t *logits, const int64_t *target, float *loss,

@@ -347,13 +347,23 @@ def test_xent_bad_target_sets_device_error(o):
 # ---------------------------------------------------------------- boundary
 
 def test_error_statuses_on_device():
-    x = torch.zeros(4, 2000, device="cuda")
+    x = torch.zeros(4, 40000, device="cuda")  # longer than a CTA holds
     with pytest.raises(fr.FRError) as e:
         fr.fr_softmax(x, form="persistent")
     assert e.value.status == 3
-    with pytest.raises(fr.FRError) as e:
-        fr.fr_softmax(x, form="split")
+    with pytest.raises(fr.FRError) as e:  # short enough for one warp: no split
+        fr.fr_softmax(torch.zeros(4, 1000, device="cuda"), form="split")
     assert e.value.status == 3
+    with pytest.raises(fr.FRError) as e:  # longer than a cluster holds
+        fr.fr_softmax(torch.zeros(2, 262145, device="cuda"), form="split")
+    assert e.value.status == 3
+    buf = torch.zeros(4 * 2001 + 3, device="cuda")  # x and y rows out of 32-byte phase
+    xs = buf[:4 * 2001].view(4, 2001)[:, :2000]
+    ys = torch.empty(4 * 2000 + 3, device="cuda")[3:].view(4, 2000)
+    for form in ("persistent", "split"):
+        with pytest.raises(fr.FRError) as e:
+            fr.fr_softmax(xs, form=form, out=ys)
+        assert e.value.status == 3
     a = torch.zeros(2, 1 << 20, device="cuda")
     ws = torch.empty(8, dtype=torch.uint8, device="cuda")
     with pytest.raises(fr.FRError) as e:
@@ -377,9 +387,15 @@ def test_auto_form_choices():
     x = torch.zeros(16, 1024, device="cuda")
     fr.fr_softmax(x)
     assert fr.fr_last_form() == "persistent"
+    x = torch.zeros(1024, 4097, device="cuda")
+    fr.fr_softmax(x)
+    assert fr.fr_last_form() == "persistent"  # one CTA per row, enough rows
     x = torch.zeros(16, 4097, device="cuda")
     fr.fr_softmax(x)
-    assert fr.fr_last_form() == "persistent"  # one CTA per row
+    assert fr.fr_last_form() == "split"  # too few rows: a cluster per row
     x = torch.zeros(4, 32769, device="cuda")
     fr.fr_softmax(x)
-    assert fr.fr_last_form() == "looped"
+    assert fr.fr_last_form() == "split"
+    x = torch.zeros(2, 300000, device="cuda")
+    fr.fr_softmax(x)
+    assert fr.fr_last_form() == "looped"  # longer than a cluster holds
