@@ -338,6 +338,11 @@ __device__ __forceinline__ void cluster_arrive() {
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Arrive without releasing this thread's writes (for signalling that this
+// CTA's mbarriers are initialised, after fence.mbarrier_init).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
 // 16 bytes from the shared memory of CTA `rank` of this cluster, at the
 // offset that `local` has in this CTA's shared memory.
 __device__ __forceinline__ float4 ld_dsmem_f4(const void *local, uint32_t rank) {

@@ -208,24 +208,37 @@ softmax_cta_vec(const float *__restrict__ x, float *__restrict__ y, int64_t cols
 // Split form for long rows: a thread-block cluster of C CTAs holds one row,
 // CTA rank q its slice of the row's body vectors in registers (rank 0 also the
 // head scalars, rank C - 1 the tail).  Each CTA reduces its slice to the pair
-// (m_q, d_q) (two passes over registers), writes the pair into every CTA of
-// the cluster (distributed shared memory) and, after one cluster barrier,
-// merges the C pairs in rank order with the merge of section 9.5 -- the same
-// (M, D) in every CTA (Proposition 9.1 makes it the row's) -- then writes its
-// exponentials scaled by 2^((m_q - M) log2 e) / D.  One read and one write per
-// element; the exchange is 8 bytes per CTA pair.  No CTA touches a peer's
-// shared memory after the barrier, so CTAs may leave right after it.
+// (m_q, d_q) (two passes over registers) and pushes the pair into every CTA of
+// the cluster with st.async, which counts the bytes on the receiver's
+// mbarrier; once its own mbarrier has seen all C pairs, a CTA merges them in
+// rank order with the merge of section 9.5 -- the same (M, D) in every CTA
+// (Proposition 9.1 makes it the row's) -- and writes its exponentials scaled
+// by 2^((m_q - M) log2 e) / D.  One read and one write per element; the
+// exchange is 16 bytes per CTA pair and needs no release fence.  The only
+// cluster barrier tells the peers that this CTA's mbarrier is initialised;
+// it is arrived at before the loads and waited for after them.  A CTA leaves
+// only after receiving every pair sent to it.  The wait is bounded; on expiry
+// the kernel records FR_DEVERR_TIMEOUT and goes on.
 constexpr int kSmClusterMax = 8;
+constexpr long long kSmWaitBudget = 1LL << 31;  // SM clocks (about one second)
 
 template <int T, int NV>
 __global__ void __launch_bounds__(T)
 softmax_cluster(const float *__restrict__ x, float *__restrict__ y, int64_t cols, int64_t ldx,
-                int64_t ldy) {
+                int64_t ldy, int *__restrict__ err) {
   constexpr int W = T / 32;
   __shared__ float red[2][W];
-  __shared__ __align__(8) float2 pairs[kSmClusterMax];
+  __shared__ __align__(16) float4 pairs[kSmClusterMax];
+  __shared__ __align__(8) uint64_t xbar;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t C = cluster_nctarank(), q = cluster_ctarank();
+  if (tid == 0) {
+    mbar_init(&xbar, 1);
+    mbar_init_fence();
+    mbar_arrive_expect_tx(&xbar, 16u * C);
+  }
+  __syncthreads();
+  cluster_arrive_relaxed();  // this CTA's mbarrier is ready for the peers' pairs
   const int64_t row = cluster_id_x();
   const float *px = x + row * ldx;
   float *py = y + row * ldy;
@@ -275,9 +288,10 @@ softmax_cluster(const float *__restrict__ x, float *__restrict__ y, int64_t cols
   if (lane == 0) red[1][warp] = d;
   __syncthreads();
   d = warp_sum(lane < W ? red[1][lane] : 0.0f);
-  if (tid < static_cast<int>(C)) st_cluster_f2(&pairs[q], static_cast<uint32_t>(tid), m, d);
-  cluster_arrive();
-  cluster_wait();
+  cluster_wait();  // every peer's mbarrier is initialised
+  if (tid < static_cast<int>(C))
+    st_async_f4(&pairs[q], &xbar, static_cast<uint32_t>(tid), make_float4(m, d, 0.0f, 0.0f));
+  if (!mbar_wait_bounded(&xbar, 0, kSmWaitBudget) && tid == 0) atomicCAS(err, 0, FR_DEVERR_TIMEOUT);
   float M = -INFINITY;
   for (uint32_t r = 0; r < C; ++r) M = max_nan(M, pairs[r].x);
   float D = 0.0f;
@@ -619,7 +633,10 @@ cudaError_t launch_cluster_kernel(const float *x, float *y, int64_t rows, int64_
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, softmax_cluster<T, NV>, x, y, cols, ldx, ldy);
+  int *err = nullptr;
+  cudaError_t e = device_error_word(&err);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, softmax_cluster<T, NV>, x, y, cols, ldx, ldy, err);
 }
 }  // namespace
 
