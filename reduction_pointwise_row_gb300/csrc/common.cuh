@@ -74,6 +74,12 @@ __device__ __forceinline__ void st_stream_v8(void *p, const V8 &v) {
                : "memory");
 }
 
+__device__ __forceinline__ void st_stream_u4(void *p, uint4 v) {
+  asm volatile("st.global.cs.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
 __device__ __forceinline__ void st_stream_f32(float *p, float v) {
   asm volatile("st.global.cs.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }

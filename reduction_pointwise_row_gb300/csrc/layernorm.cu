@@ -513,6 +513,254 @@ layernorm_cluster(const uint16_t *__restrict__ x, const float *__restrict__ gamm
   cluster_wait();
 }
 
+// ---- the cluster form when every thread holds 32 columns ----------------------
+// When cols = C * 512 * 32 (every thread of every CTA owns exactly 32
+// columns) all the triples merged at one tree level have equal counts, and
+// the Chan merge needs no reciprocal: with n_a = n_b = n the weight is 1/2 and
+// the correction delta^2 * n_a * n_b / (n_a + n_b) is delta^2 * n / 2.  The
+// per-element work uses paired fp32 instructions (two columns per
+// instruction).  Each CTA's 32 KB slice of a row arrives in shared memory by
+// one bulk asynchronous copy (the tensor-memory-accelerator path, which does
+// not occupy the load/store pipe that per-thread copies and the shared-memory
+// reads share), completing on the slot's mbarrier; the row being finalised is
+// read again from its slot instead of being held in registers.  Otherwise the
+// same design as layernorm_cluster.
+// Ring geometry of layernorm_cluster_full<R>: rows in flight ahead of the
+// step being reduced, and row slots (the previous step's R rows, this step's
+// R and those ahead).
+__host__ __device__ constexpr int full_ahead(int R) { return R == 1 ? 3 : R; }
+__host__ __device__ constexpr int full_slots(int R) { return 2 * R + full_ahead(R); }
+
+__device__ __forceinline__ void merge_equal(float &mean, float &m2, float mean_b, float m2_b,
+                                            float half_n) {
+  const float delta = mean_b - mean;
+  mean = fmaf(delta, 0.5f, mean);
+  m2 = fmaf(delta * delta, half_n, m2 + m2_b);
+}
+
+// (mean, M2) of the 16 bf16 values of one 32-byte vector, two passes over
+// registers in paired fp32 (the values are unpacked again for the second
+// pass rather than held: registers are the cluster kernel's limit).
+__device__ __forceinline__ uint64_t unpack_pair(uint32_t w) {
+  return pack_f32x2(bf16_lo(w), bf16_hi(w));
+}
+__device__ __forceinline__ void stats16(const V8 &v, float &mean, float &m2) {
+  const uint64_t s =
+      add_f32x2(add_f32x2(add_f32x2(unpack_pair(v.w[0]), unpack_pair(v.w[1])),
+                          add_f32x2(unpack_pair(v.w[2]), unpack_pair(v.w[3]))),
+                add_f32x2(add_f32x2(unpack_pair(v.w[4]), unpack_pair(v.w[5])),
+                          add_f32x2(unpack_pair(v.w[6]), unpack_pair(v.w[7]))));
+  mean = (f32x2_lo(s) + f32x2_hi(s)) * (1.0f / 16.0f);
+  const uint64_t nm = pack_f32x2(-mean, -mean);
+  uint64_t q0 = 0, q1 = 0;
+#pragma unroll
+  for (int h = 0; h < 8; h += 2) {
+    const uint64_t d0 = add_f32x2(unpack_pair(v.w[h]), nm);
+    const uint64_t d1 = add_f32x2(unpack_pair(v.w[h + 1]), nm);
+    q0 = fma_f32x2(d0, d0, q0);
+    q1 = fma_f32x2(d1, d1, q1);
+  }
+  const uint64_t q = add_f32x2(q0, q1);
+  m2 = f32x2_lo(q) + f32x2_hi(q);
+}
+
+template <int R>
+__global__ void __launch_bounds__(kClThreads, 1)
+layernorm_cluster_full(const uint16_t *__restrict__ x, const float *__restrict__ gamma,
+                       const float *__restrict__ beta, uint16_t *__restrict__ y,
+                       float *__restrict__ mean_out, float *__restrict__ rstd_out, int64_t rows,
+                       int64_t cols, int64_t ldx, int64_t ldy, float eps, int *__restrict__ err) {
+  constexpr int kSlotsR = full_slots(R), kAhead = full_ahead(R);
+  extern __shared__ __align__(128) unsigned char smem[];  // [kSlotsR] row slices
+  __shared__ __align__(8) uint64_t landed[kSlotsR];       // bulk-copy completion per slot
+  __shared__ __align__(16) float4 slot[kClSlots][kClMaxCluster];  // [step % 4][rank]
+  __shared__ __align__(8) uint64_t pbar[kClSlots];
+  __shared__ float2 red[2][R][kClThreads / 32];  // per-warp (mean, M2), double-buffered by step
+  __shared__ int timed_out;
+
+  const uint32_t C = cluster_nctarank(), q = cluster_ctarank();
+  const int64_t cid = cluster_id_x(), ncl = ncluster_x();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t S = cols / C;  // = 512 * 32
+  const uint32_t slice = static_cast<uint32_t>(S) * 2;  // bytes of a row slice
+  // Thread t owns the 16-byte chunks j = t + 512 c (c = 0..3) of its CTA's
+  // slice, columns 8j .. 8j + 7: a warp's shared-memory reads and global
+  // stores of one chunk are 512 contiguous bytes (no bank conflicts).
+  const int64_t cbase = static_cast<int64_t>(q) * S + 8 * static_cast<int64_t>(tid);
+  constexpr int64_t kChunkStride = 8 * kClThreads;  // columns between a thread's chunks
+  const int64_t nr = cid < rows ? (rows - cid + ncl - 1) / ncl : 0;  // rows of this cluster
+  const int64_t ns = (nr + R - 1) / R;                                // steps of R rows
+  const uint32_t part_bytes = 16u * C;
+  const float inv_n = __frcp_rn(static_cast<float>(cols));
+
+  auto row_of = [&](int64_t k) { return cid + k * ncl; };
+  auto slot_of = [&](int64_t k) { return smem + static_cast<size_t>(k % kSlotsR) * slice; };
+  uint64_t g2[kClCols / 2], b2[kClCols / 2];  // gamma/beta pairs of this thread's columns
+#pragma unroll
+  for (int h = 0; h < kClCols / 4; ++h) {  // chunk h / 2, columns 4 (h % 2) .. + 3
+    const int64_t col = cbase + kChunkStride * (h >> 1) + 4 * (h & 1);
+    const float4 gv = ld_keep_f4(gamma + col), bv = ld_keep_f4(beta + col);
+    g2[2 * h] = pack_f32x2(gv.x, gv.y);
+    g2[2 * h + 1] = pack_f32x2(gv.z, gv.w);
+    b2[2 * h] = pack_f32x2(bv.x, bv.y);
+    b2[2 * h + 1] = pack_f32x2(bv.z, bv.w);
+  }
+  // this thread's 32 values of a staged row: chunks 0, 1 in one V8, 2, 3 in another
+  auto read_row = [&](int64_t k, V8 &c0, V8 &c1) {
+    const unsigned char *p = slot_of(k) + static_cast<size_t>(tid) * 16;
+    const uint4 a = lds_u4(p), b = lds_u4(p + 16 * kClThreads), c = lds_u4(p + 32 * kClThreads),
+                d = lds_u4(p + 48 * kClThreads);
+    c0.w[0] = a.x; c0.w[1] = a.y; c0.w[2] = a.z; c0.w[3] = a.w;
+    c0.w[4] = b.x; c0.w[5] = b.y; c0.w[6] = b.z; c0.w[7] = b.w;
+    c1.w[0] = c.x; c1.w[1] = c.y; c1.w[2] = c.z; c1.w[3] = c.w;
+    c1.w[4] = d.x; c1.w[5] = d.y; c1.w[6] = d.z; c1.w[7] = d.w;
+  };
+  const uint64_t policy = l2_evict_first_policy();
+  auto issue = [&](int64_t k) {  // thread 0: this CTA's slice of row k, one bulk copy
+    if (k < nr) {
+      uint64_t *b = &landed[k % kSlotsR];
+      mbar_arrive_expect_tx(b, slice);
+      bulk_copy_g2s(slot_of(k), x + row_of(k) * ldx + static_cast<int64_t>(q) * S, slice, b,
+                    policy);
+    }
+  };
+  auto wait_row = [&](int64_t k) {
+    if (!timed_out &&
+        !mbar_wait_bounded(&landed[k % kSlotsR], static_cast<uint32_t>((k / kSlotsR) & 1),
+                           1LL << 31)) {
+      timed_out = 1;
+      atomicCAS(err, 0, FR_DEVERR_TIMEOUT);
+    }
+  };
+
+  if (tid == 0) {
+    timed_out = 0;
+    for (int i = 0; i < kSlotsR; ++i) mbar_init(&landed[i], 1);
+    for (int i = 0; i < kClSlots; ++i) mbar_init(&pbar[i], 1);
+    mbar_init_fence();
+    for (int64_t st = 0; st < kClSlots && st < ns; ++st) mbar_arrive_expect_tx(&pbar[st], part_bytes);
+    for (int i = 0; i < kAhead; ++i) issue(i);
+  }
+  __syncthreads();
+  cluster_arrive();  // every CTA's barriers are armed before anyone sends
+  cluster_wait();
+
+  // Step s: reduce rows sR .. sR + R - 1 (this thread's 32 values of each) and
+  // publish the CTA's R (mean, M2) pairs in one 16-byte message; then finalise
+  // the rows of step s - 1, reading their values again from their slots.
+  // Slots hold the previous step's rows, this step's and kAhead rows ahead;
+  // after this step's barrier every thread has finished with the rows of step
+  // s - 2, whose slots thread 0 then refills with the next rows.
+  for (int64_t s = 0; s <= ns; ++s) {
+    if (s < ns) {
+      float mean[R], m2[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int64_t k = s * R + r;
+        float mb = 0.0f, m2b = 0.0f;
+        mean[r] = m2[r] = 0.0f;
+        if (k < nr) {
+          wait_row(k);
+          V8 c0, c1;
+          read_row(k, c0, c1);
+          stats16(c0, mean[r], m2[r]);
+          stats16(c1, mb, m2b);
+        }
+        merge_equal(mean[r], m2[r], mb, m2b, 8.0f);  // 16 + 16
+      }
+      float half_n = 16.0f;  // half of each side's count
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1, half_n *= 2.0f)
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+          merge_equal(mean[r], m2[r], __shfl_xor_sync(0xffffffffu, mean[r], o),
+                      __shfl_xor_sync(0xffffffffu, m2[r], o), half_n);
+      if (lane == 0)
+#pragma unroll
+        for (int r = 0; r < R; ++r) red[s & 1][r][warp] = make_float2(mean[r], m2[r]);
+      __syncthreads();
+      if (tid == 0) {  // refill the slots of step s - 2 with the rows kAhead ahead
+        fence_proxy_async_smem();
+#pragma unroll
+        for (int r = 0; r < R; ++r) issue(s * R + r + kAhead);
+      }
+      if (warp == 0) {  // the CTA's 16 warp pairs (1024 values each) on lanes 0..15
+        float wm[R], w2[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float2 t = red[s & 1][r][lane & (kClThreads / 32 - 1)];
+          wm[r] = t.x;
+          w2[r] = t.y;
+        }
+        float hn = 512.0f;
+#pragma unroll
+        for (int o = kClThreads / 64; o > 0; o >>= 1, hn *= 2.0f)
+#pragma unroll
+          for (int r = 0; r < R; ++r)
+            merge_equal(wm[r], w2[r], __shfl_xor_sync(0xffffffffu, wm[r], o),
+                        __shfl_xor_sync(0xffffffffu, w2[r], o), hn);
+        if (lane < static_cast<int>(C)) {
+          const int sl = static_cast<int>(s % kClSlots);
+          st_async_f4(&slot[sl][q], &pbar[sl], static_cast<uint32_t>(lane),
+                      make_float4(wm[0], w2[0], R > 1 ? wm[R - 1] : 0.0f,
+                                  R > 1 ? w2[R - 1] : 0.0f));
+        }
+      }
+    }
+    if (s > 0) {  // finalise the rows of step s - 1
+      const int64_t sp = s - 1;
+      const int sl = static_cast<int>(sp % kClSlots);
+      if (!timed_out &&
+          !mbar_wait_bounded(&pbar[sl], static_cast<uint32_t>((sp / kClSlots) & 1), 1LL << 31)) {
+        timed_out = 1;
+        atomicCAS(err, 0, FR_DEVERR_TIMEOUT);
+      }
+      const float4 u0 = slot[sl][0];
+      const float4 u1 = C == 2 ? slot[sl][1] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      // Re-arm slot sl for step sp + 4 (peers send it only after this CTA
+      // publishes step sp + 2, which comes after this point).
+      if (tid == 0 && sp + kClSlots < ns) mbar_arrive_expect_tx(&pbar[sl], part_bytes);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int64_t k = sp * R + r;
+        if (k >= nr) break;
+        float mean = r == 0 ? u0.x : u0.z, m2 = r == 0 ? u0.y : u0.w;
+        if (C == 2)  // rank order: identical in every CTA
+          merge_equal(mean, m2, r == 0 ? u1.x : u1.z, r == 0 ? u1.y : u1.w,
+                      0.5f * static_cast<float>(S));
+        const int64_t row = row_of(k);
+        const float rstd = rsqrtf(fmaf(m2, inv_n, eps));
+        if (q == 0 && tid == 0) {
+          if (mean_out) mean_out[row] = mean;
+          if (rstd_out) rstd_out[row] = rstd;
+        }
+        const uint64_t nm = pack_f32x2(-mean, -mean), r2 = pack_f32x2(rstd, rstd);
+        const unsigned char *p = slot_of(k) + static_cast<size_t>(tid) * 16;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {  // chunk c: 8 columns, pairs 4c .. 4c + 3
+          const uint4 v = lds_u4(p + 16 * kClThreads * c);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const uint64_t d = add_f32x2(unpack_pair(w[h]), nm);
+            const uint64_t yv = fma_f32x2(mul_f32x2(d, r2), g2[4 * c + h], b2[4 * c + h]);
+            o[h] = pack_bf16x2(f32x2_lo(yv), f32x2_hi(yv));
+          }
+          st_stream_u4(y + row * ldy + cbase + kChunkStride * c,
+                       make_uint4(o[0], o[1], o[2], o[3]));
+        }
+      }
+    }
+  }
+  if (timed_out && tid == 0)  // last bounded wait on copies that may be in flight
+    for (int64_t k = nr > kSlotsR ? nr - kSlotsR : 0; k < nr; ++k)
+      mbar_wait_bounded(&landed[k % kSlotsR], static_cast<uint32_t>((k / kSlotsR) & 1), 1LL << 31);
+  // No CTA may leave while a peer can still write into its shared memory.
+  cluster_arrive();
+  cluster_wait();
+}
+
 }  // namespace
 
 // Cluster size: the smallest C in {1, 2} with slices of at most 16384
@@ -541,8 +789,19 @@ cudaError_t launch_layernorm_cluster(const uint16_t *x, const float *gamma, cons
   if (e != cudaSuccess) return e;
   const int C = cluster_size_for(cols);
   if (C == 0) return cudaErrorInvalidValue;
-  const size_t smem = cluster_smem(cols, C);
-  e = cudaFuncSetAttribute(layernorm_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  // Every thread holding 32 columns: the equal-count kernel with R rows per
+  // step (FR_LAYERNORM_CLUSTER=classic|r1|r2 pins one; default r1).  Measured
+  // on GB300, bf16 [4096, 32768]: r1 92.7 us, r2 96.4 us, classic 132.3 us.
+  const char *pin = getenv("FR_LAYERNORM_CLUSTER");
+  const bool full = cols == static_cast<int64_t>(C) * kClThreads * kClCols &&
+                    !(pin != nullptr && strcmp(pin, "classic") == 0);
+  const int R = pin != nullptr && strcmp(pin, "r2") == 0 ? 2 : 1;
+  auto kern = !full ? layernorm_cluster : R == 1 ? layernorm_cluster_full<1>
+                                                 : layernorm_cluster_full<2>;
+  const size_t smem = !full ? cluster_smem(cols, C)
+                            : static_cast<size_t>(R == 1 ? full_slots(1) : full_slots(2)) *
+                                  static_cast<size_t>(cols / C) * 2;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -558,14 +817,14 @@ cudaError_t launch_layernorm_cluster(const uint16_t *x, const float *gamma, cons
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(C));
   int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, layernorm_cluster, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
   if (e != cudaSuccess) return e;
   if (clusters < 1) return cudaErrorInvalidConfiguration;
   int64_t ncl = clusters;  // persistent: every cluster that can be resident
   if (ncl > rows) ncl = rows;
   cfg.gridDim = dim3(static_cast<unsigned>(ncl * C));
-  return cudaLaunchKernelEx(&cfg, layernorm_cluster, x, gamma, beta, y, mean, rstd, rows, cols,
-                            ldx, ldy, eps, err);
+  return cudaLaunchKernelEx(&cfg, kern, x, gamma, beta, y, mean, rstd, rows, cols, ldx, ldy, eps,
+                            err);
 }
 
 size_t layernorm_ring_smem(int64_t cols, int nbuf) {
