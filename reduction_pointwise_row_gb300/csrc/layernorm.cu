@@ -525,11 +525,10 @@ layernorm_cluster(const uint16_t *__restrict__ x, const float *__restrict__ gamm
 // reads share), completing on the slot's mbarrier; the row being finalised is
 // read again from its slot instead of being held in registers.  Otherwise the
 // same design as layernorm_cluster.
-// Ring geometry of layernorm_cluster_full<R>: rows in flight ahead of the
-// step being reduced, and row slots (the previous step's R rows, this step's
-// R and those ahead).
-__host__ __device__ constexpr int full_ahead(int R) { return R == 1 ? 3 : R; }
-__host__ __device__ constexpr int full_slots(int R) { return 2 * R + full_ahead(R); }
+// Ring geometry of layernorm_cluster_full<R, A>: A rows in flight ahead of
+// the step being reduced, and 2R + A row slots (the previous step's R rows,
+// this step's R and those ahead).
+__host__ __device__ constexpr int full_slots(int R, int A) { return 2 * R + A; }
 
 __device__ __forceinline__ void merge_equal(float &mean, float &m2, float mean_b, float m2_b,
                                             float half_n) {
@@ -564,13 +563,14 @@ __device__ __forceinline__ void stats16(const V8 &v, float &mean, float &m2) {
   m2 = f32x2_lo(q) + f32x2_hi(q);
 }
 
-template <int R>
+template <int R, int A>  // A >= R: the rows a step reduces were issued a step earlier
 __global__ void __launch_bounds__(kClThreads, 1)
 layernorm_cluster_full(const uint16_t *__restrict__ x, const float *__restrict__ gamma,
                        const float *__restrict__ beta, uint16_t *__restrict__ y,
                        float *__restrict__ mean_out, float *__restrict__ rstd_out, int64_t rows,
                        int64_t cols, int64_t ldx, int64_t ldy, float eps, int *__restrict__ err) {
-  constexpr int kSlotsR = full_slots(R), kAhead = full_ahead(R);
+  static_assert(A >= R, "a step's rows must be issued during the step before");
+  constexpr int kSlotsR = full_slots(R, A), kAhead = A;
   extern __shared__ __align__(128) unsigned char smem[];  // [kSlotsR] row slices
   __shared__ __align__(8) uint64_t landed[kSlotsR];       // bulk-copy completion per slot
   __shared__ __align__(16) float4 slot[kClSlots][kClMaxCluster];  // [step % 4][rank]
@@ -790,17 +790,30 @@ cudaError_t launch_layernorm_cluster(const uint16_t *x, const float *gamma, cons
   const int C = cluster_size_for(cols);
   if (C == 0) return cudaErrorInvalidValue;
   // Every thread holding 32 columns: the equal-count kernel with R rows per
-  // step (FR_LAYERNORM_CLUSTER=classic|r1|r2 pins one; default r1).  Measured
-  // on GB300, bf16 [4096, 32768]: r1 92.7 us, r2 96.4 us, classic 132.3 us.
+  // step and A rows ahead (FR_LAYERNORM_CLUSTER=classic|r1a1|...|r2a2 pins
+  // one; default r1a2).  Measured on GB300, bf16 [4096, 32768]: r1a2 91.4 us,
+  // r1a3 93.2, r2a2 95.8, r1a5 97.3, r1a4 98.2, r1a1 113.9, classic 132.3.
   const char *pin = getenv("FR_LAYERNORM_CLUSTER");
-  const bool full = cols == static_cast<int64_t>(C) * kClThreads * kClCols &&
-                    !(pin != nullptr && strcmp(pin, "classic") == 0);
-  const int R = pin != nullptr && strcmp(pin, "r2") == 0 ? 2 : 1;
-  auto kern = !full ? layernorm_cluster : R == 1 ? layernorm_cluster_full<1>
-                                                 : layernorm_cluster_full<2>;
+  auto pinned = [&](const char *v) { return pin != nullptr && strcmp(pin, v) == 0; };
+  const bool full = cols == static_cast<int64_t>(C) * kClThreads * kClCols && !pinned("classic");
+  struct Shape {
+    const char *name;
+    void (*kern)(const uint16_t *, const float *, const float *, uint16_t *, float *, float *,
+                 int64_t, int64_t, int64_t, int64_t, float, int *);
+    int slots;
+  };
+  static const Shape shapes[] = {{"r1a2", layernorm_cluster_full<1, 2>, full_slots(1, 2)},
+                                 {"r1a1", layernorm_cluster_full<1, 1>, full_slots(1, 1)},
+                                 {"r1a3", layernorm_cluster_full<1, 3>, full_slots(1, 3)},
+                                 {"r1a4", layernorm_cluster_full<1, 4>, full_slots(1, 4)},
+                                 {"r1a5", layernorm_cluster_full<1, 5>, full_slots(1, 5)},
+                                 {"r2a2", layernorm_cluster_full<2, 2>, full_slots(2, 2)}};
+  const Shape *sh = &shapes[0];
+  for (const Shape &c : shapes)
+    if (pinned(c.name)) sh = &c;
+  auto kern = full ? sh->kern : layernorm_cluster;
   const size_t smem = !full ? cluster_smem(cols, C)
-                            : static_cast<size_t>(R == 1 ? full_slots(1) : full_slots(2)) *
-                                  static_cast<size_t>(cols / C) * 2;
+                            : static_cast<size_t>(sh->slots) * static_cast<size_t>(cols / C) * 2;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem));
   if (e != cudaSuccess) return e;

@@ -248,6 +248,35 @@ def test_layernorm_forms(o, rows, cols, offset):
         assert e.value.status == 3
 
 
+@pytest.mark.parametrize("variant", ["r1a2", "r1a1", "r1a3", "r1a4", "r1a5", "r2a2", "classic"])
+@pytest.mark.parametrize("cols", [16384, 32768])
+def test_layernorm_cluster_variants(o, variant, cols):
+    """The cluster kernels where every thread holds 32 columns (one CTA per
+    16384 columns), every ring depth and rows per step, on row counts that
+    leave clusters with different numbers of rows (and with none), plus a
+    constant row and a row of one repeated large value."""
+    import os
+    for rows in (1, 5, 77, 301):
+        w = workloads.make(2, rows=rows, cols=cols, seed=3500 + rows + cols)
+        x = w.arrays["x"].copy()
+        if rows >= 5:
+            x[1, :] = 0x4060   # 3.5: var 0, y = beta
+            x[3, :] = 0x4780   # 65536: large mean, var 0
+        eps = float(np.float32(w.params["eps"]))
+        ry, rm, rr = o.layernorm(x, w.arrays["gamma"], w.arrays["beta"], eps)
+        os.environ["FR_LAYERNORM_CLUSTER"] = variant
+        try:
+            y, m, r = run_layernorm(x, w.arrays["gamma"], w.arrays["beta"], eps, "looped",
+                                    kernel="cluster")
+        finally:
+            os.environ.pop("FR_LAYERNORM_CLUSTER", None)
+        what = f"{variant} {rows}x{cols}"
+        assert_close(y, ry, "bf16", f"{what} y")
+        assert_close(m, rm, "mean", f"{what} mean")
+        assert_close(r, rr, "f32", f"{what} rstd")
+    assert fr.fr_check_device_error() == 0
+
+
 def test_layernorm_constant_rows(o):
     cols = 4096
     x = np.full((4, cols), 0x4060, np.uint16)  # 3.5 in bf16
