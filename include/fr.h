@@ -172,6 +172,30 @@ fr_status fr_softmax(const void *x, void *y, int64_t rows, int64_t cols, int64_t
                      int64_t ldy, fr_dtype dtype, fr_form form, fr_stream_t stream);
 
 /*
+ * fr_softmax over rows held in HOST memory: the rows go to the device in
+ * chunks of `chunk_rows`, through three device staging slots each way (the
+ * caller's workspace), and come back the same way, with a chunk's copy in,
+ * the previous chunk's kernel and the copy out of the one before running at
+ * the same time on the library's own streams (created once per device).  The
+ * results are those of fr_softmax on the same rows.  The call returns without
+ * synchronising; `stream` resumes after the last copy out, and work queued on
+ * `stream` before the call runs first.  The pages have no counterpart: this
+ * is the end-to-end path from host memory.
+ *
+ *   x_host, y_host  [rows, cols] contiguous, of `dtype`, in page-locked host
+ *                   memory (cudaHostAlloc or cudaHostRegister); anything else
+ *                   is FR_ERR_INVALID_ARG.  They may be the same buffer.
+ *   chunk_rows      rows per chunk, >= 1
+ *   workspace       device memory of fr_softmax_host_workspace(...) bytes,
+ *                   256-byte aligned; one call at a time may use it
+ *   dtype           FR_F32 or FR_BF16
+ */
+size_t fr_softmax_host_workspace(int64_t cols, fr_dtype dtype, int64_t chunk_rows);
+fr_status fr_softmax_host(const void *x_host, void *y_host, int64_t rows, int64_t cols,
+                          fr_dtype dtype, int64_t chunk_rows, void *workspace,
+                          size_t workspace_bytes, fr_stream_t stream);
+
+/*
  * LayerNorm over each row (not defined on the pages; standard definition):
  *   mean = sum x / n,  var = sum (x - mean)^2 / n,  rstd = 1 / sqrt(var + eps),
  *   y = (x - mean) * rstd * gamma + beta      (rounded to bf16, nearest even)

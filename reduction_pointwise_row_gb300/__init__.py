@@ -24,7 +24,8 @@ from . import buildlib as _build
 
 __all__ = [
     "FR_OK", "FRError", "lib", "fr_version", "fr_workspace_size", "fr_last_form",
-    "fr_reduce_relu_add_sum", "fr_reduce_sumsq", "fr_softmax", "fr_layernorm", "fr_xent",
+    "fr_reduce_relu_add_sum", "fr_reduce_sumsq", "fr_softmax", "fr_softmax_host", "fr_layernorm",
+    "fr_xent",
     "fr_reduce_relu_add_sum_split_static", "fr_check_device_error", "FORMS", "OPS",
     "EPILOGUES", "fr_coordinate_descent", "fr_xent_get_config", "fr_xent_set_config",
     "fr_xent_tune",
@@ -53,6 +54,8 @@ SIGNATURES = {
                                       _vp, _sz, _vp]),
     "fr_reduce_sumsq": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp, _sz, _vp]),
     "fr_softmax": (_int, [_vp, _vp, _i64, _i64, _i64, _i64, _int, _int, _vp]),
+    "fr_softmax_host_workspace": (_sz, [_i64, _int, _i64]),
+    "fr_softmax_host": (_int, [_vp, _vp, _i64, _i64, _int, _i64, _vp, _sz, _vp]),
     "fr_layernorm": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _f32, _int,
                             _int, _vp]),
     "fr_xent": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _int, _vp,
@@ -188,6 +191,32 @@ def fr_softmax(x, form: str = "auto", out=None, stream=None):
     dt = DTYPES["f32"] if x.dtype == torch.float32 else DTYPES["bf16"]
     _check(lib().fr_softmax(_ptr(x), _ptr(out), rows, cols, _ld(x), _ld(out), dt,
                             FORMS[form], _stream(stream)), "fr_softmax")
+    return out
+
+
+def fr_softmax_host(x_host, out=None, chunk_rows: int | None = None, workspace=None,
+                    stream=None, device=None):
+    """Row softmax of a page-locked host tensor (fp32 or bf16) through the
+    library's chunked copy-in / kernel / copy-out pipeline; ``out`` (page-locked,
+    same shape and dtype) receives y.  Returns ``out``.  Ordered on ``stream``
+    (default: the current stream of ``device``) without synchronising."""
+    import torch
+    assert not x_host.is_cuda and x_host.dtype in (torch.float32, torch.bfloat16)
+    assert x_host.dim() == 2 and x_host.is_contiguous()
+    rows, cols = x_host.shape
+    if out is None:
+        out = torch.empty_like(x_host).pin_memory()
+    assert out.shape == x_host.shape and out.dtype == x_host.dtype and out.is_contiguous()
+    dt = DTYPES["f32"] if x_host.dtype == torch.float32 else DTYPES["bf16"]
+    if chunk_rows is None:  # about 16 MiB of input per chunk
+        chunk_rows = max(1, min(rows, (16 << 20) // (cols * x_host.element_size())))
+    n = lib().fr_softmax_host_workspace(cols, dt, min(chunk_rows, rows))
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    if workspace is None:
+        workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+    _check(lib().fr_softmax_host(_ptr(x_host), _ptr(out), rows, cols, dt, chunk_rows,
+                                 _ptr(workspace), workspace.numel(), _stream(stream)),
+           "fr_softmax_host")
     return out
 
 

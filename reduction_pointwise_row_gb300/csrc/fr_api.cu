@@ -282,6 +282,51 @@ fr_status fr_softmax(const void *x, void *y, int64_t rows, int64_t cols, int64_t
   }
 }
 
+size_t fr_softmax_host_workspace(int64_t cols, fr_dtype dtype, int64_t chunk_rows) {
+  if (cols < 1 || chunk_rows < 1 || (dtype != FR_F32 && dtype != FR_BF16)) return 0;
+  const int64_t es = dtype == FR_F32 ? 4 : 2;
+  return fr::host_pipeline_workspace(cols, es, es, chunk_rows);
+}
+
+namespace {
+bool page_locked(const void *p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost;
+}
+}  // namespace
+
+fr_status fr_softmax_host(const void *x_host, void *y_host, int64_t rows, int64_t cols,
+                          fr_dtype dtype, int64_t chunk_rows, void *workspace,
+                          size_t workspace_bytes, fr_stream_t stream) {
+  if (dtype != FR_F32 && dtype != FR_BF16) return FR_ERR_UNSUPPORTED_DTYPE;
+  const int64_t es = dtype == FR_F32 ? 4 : 2;
+  if (!x_host || !y_host || chunk_rows < 1) return FR_ERR_INVALID_ARG;
+  if (!shape_ok(rows, cols, cols, es)) return FR_ERR_INVALID_ARG;
+  if (!aligned(x_host, es) || !aligned(y_host, es)) return FR_ERR_MISALIGNED;
+  fr::DevInfo info;
+  if (fr_status st = device_ok(&info)) return st;
+  if (!page_locked(x_host) || !page_locked(y_host)) return FR_ERR_INVALID_ARG;
+  if (chunk_rows > rows) chunk_rows = rows;
+  if (!workspace || workspace_bytes < fr::host_pipeline_workspace(cols, es, es, chunk_rows))
+    return FR_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned(workspace, 256)) return FR_ERR_MISALIGNED;
+  fr_status kst = FR_OK;
+  const fr::RowKernel kernel = [&](const void *x, void *y, int64_t nr, cudaStream_t s) {
+    kst = fr_softmax(x, y, nr, cols, cols, cols, dtype, FR_FORM_AUTO,
+                     reinterpret_cast<fr_stream_t>(s));
+    return kst == FR_OK ? cudaSuccess : cudaErrorInvalidValue;
+  };
+  const cudaError_t e =
+      fr::host_pipeline_run(x_host, y_host, rows, cols, es, es, chunk_rows, workspace,
+                            reinterpret_cast<cudaStream_t>(stream), kernel);
+  if (kst != FR_OK) return kst;
+  return e == cudaSuccess ? FR_OK : FR_ERR_CUDA;
+}
+
 fr_status fr_layernorm(const void *x, const float *gamma, const float *beta, void *y,
                        float *mean, float *rstd, int64_t rows, int64_t cols, int64_t ldx,
                        int64_t ldy, float eps, fr_dtype dtype, fr_form form,

@@ -106,6 +106,21 @@ cudaError_t launch_layernorm_looped(const uint16_t *x, const float *gamma, const
                                     bool vec, int sm_count, int max_smem_optin,
                                     cudaStream_t s);
 
+// ---- rows held in host memory ------------------------------------------------
+
+// Computes chunk rows x [rows, cols] (contiguous, device) -> y on stream s.
+using RowKernel = std::function<cudaError_t(const void *x, void *y, int64_t rows,
+                                            cudaStream_t s)>;
+// Device staging bytes for chunks of chunk_rows rows (three slots each way).
+size_t host_pipeline_workspace(int64_t cols, int64_t esize_in, int64_t esize_out,
+                               int64_t chunk_rows);
+// Copies x_host in, runs `kernel` chunk by chunk and copies y out, copies and
+// kernels overlapping on the device's internal streams; ordered after the
+// caller's earlier work on `caller`, which resumes after the last copy out.
+cudaError_t host_pipeline_run(const void *x_host, void *y_host, int64_t rows, int64_t cols,
+                              int64_t esize_in, int64_t esize_out, int64_t chunk_rows,
+                              void *workspace, cudaStream_t caller, const RowKernel &kernel);
+
 // ---- launch-configuration search (Algorithm 9.2) -----------------------------
 
 struct CdResult {

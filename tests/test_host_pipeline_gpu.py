@@ -1,0 +1,63 @@
+"""fr_softmax_host: rows in page-locked host memory go through the library's
+chunked copy-in / kernel / copy-out pipeline; results must be fr_softmax's,
+compared with the oracle element by element (fp32) or in bf16 steps (bf16)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import reduction_pointwise_row_gb300 as fr
+from compare import assert_bf16_within_steps, assert_close
+from synth import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def o():
+    return oracle.get()
+
+
+@pytest.mark.parametrize("rows,cols,chunk", [(1000, 1000, 64), (7, 4097, 2), (300, 20000, 300),
+                                             (513, 100, 1000), (64, 65537, 5)])
+def test_host_pipeline_fp32(o, rows, cols, chunk):
+    w = workloads.make(1, rows=rows, cols=cols, seed=8000 + rows + cols)
+    x = torch.from_numpy(w.arrays["x"]).pin_memory()
+    y = fr.fr_softmax_host(x, chunk_rows=chunk)
+    torch.cuda.current_stream().synchronize()
+    assert_close(y.numpy(), o.softmax(w.arrays["x"]), "f32", f"host {rows}x{cols}/{chunk}")
+
+
+def test_host_pipeline_bf16_and_in_place(o):
+    bits = workloads.make_softmax_bf16(300, 2048, seed=81).arrays["x"]
+    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    ref = o.softmax((bits.astype(np.uint32) << 16).view(np.float32))
+    y = fr.fr_softmax_host(x, chunk_rows=50)
+    torch.cuda.current_stream().synchronize()
+    assert_bf16_within_steps(y.view(torch.int16).numpy().view(np.uint16), ref, 1, "host bf16")
+    fr.fr_softmax_host(x, out=x, chunk_rows=7)  # in place
+    torch.cuda.current_stream().synchronize()
+    assert_bf16_within_steps(x.view(torch.int16).numpy().view(np.uint16), ref, 1, "in place")
+
+
+def test_host_pipeline_orders_after_earlier_work_and_full_shape(o):
+    """Work queued on the stream before the call (a copy into the pinned input)
+    comes first; the softmax workload's shape, sampled rows against the oracle."""
+    w = workloads.make(1)
+    src = torch.from_numpy(w.arrays["x"]).cuda()
+    x = torch.empty(src.shape, dtype=torch.float32).pin_memory()
+    x.copy_(src, non_blocking=True)  # on the current stream, not yet done
+    y = fr.fr_softmax_host(x, chunk_rows=2048)
+    torch.cuda.current_stream().synchronize()
+    rows = np.random.default_rng(5).choice(w.rows, 48, replace=False)
+    rows.sort()
+    assert_close(y.numpy()[rows], o.softmax(w.arrays["x"][rows]), "f32", "sampled rows")
+
+
+def test_host_pipeline_refuses_pageable_memory():
+    x = torch.zeros(4, 16)  # not page-locked
+    with pytest.raises(fr.FRError, match="INVALID_ARG"):
+        fr.fr_softmax_host(x, out=torch.zeros(4, 16).pin_memory())
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fr.FRError, match="WORKSPACE_TOO_SMALL"):
+        fr.fr_softmax_host(torch.zeros(64, 1024).pin_memory(), chunk_rows=32, workspace=ws)
