@@ -108,12 +108,14 @@ fr_form pick_softmax(int64_t rows, int64_t cols, bool vec, int sm_count) {
   return FR_FORM_LOOPED;
 }
 
-fr_form pick_layernorm(int64_t, int64_t cols, bool vec, int max_smem_optin) {
+fr_form pick_layernorm(int64_t, int64_t cols, bool vec, bool aligned16, int max_smem_optin) {
   // Measured on GB300, bf16 [4096, 32768]: looped cluster (gamma/beta in
-  // registers, rows split over a 2-CTA cluster) 132 us, looped cp.async ring
-  // (two rows per gamma/beta pass) 137 us, persistent 168 us, looped scalar
-  // 265 us.  The looped form tries cluster, then ring, then scalar.
-  if (fr::layernorm_ring_ok(cols, vec, max_smem_optin)) return FR_FORM_LOOPED;
+  // registers, rows split over a 2-CTA cluster, every thread 32 columns)
+  // 91.4 us, its general form 132 us, looped cp.async ring (two rows per
+  // gamma/beta pass) 137 us, persistent 168 us, looped scalar 265 us.  The
+  // looped form tries cluster, then ring, then scalar.
+  if (fr::layernorm_cluster_ok(cols, aligned16) || fr::layernorm_ring_ok(cols, vec, max_smem_optin))
+    return FR_FORM_LOOPED;
   return fr::layernorm_persistent_ok(cols, vec) ? FR_FORM_PERSISTENT : FR_FORM_LOOPED;
 }
 
@@ -344,7 +346,8 @@ fr_status fr_layernorm(const void *x, const float *gamma, const float *beta, voi
                    ldx % 16 == 0 && ldy % 16 == 0 && cols % 16 == 0;
   const bool aligned16 = aligned(x, 32) && aligned(y, 32) && aligned(gamma, 16) &&
                          aligned(beta, 16) && ldx % 16 == 0 && ldy % 16 == 0;
-  const fr_form f = form == FR_FORM_AUTO ? pick_layernorm(rows, cols, vec, info.max_smem_optin) : form;
+  const fr_form f =
+      form == FR_FORM_AUTO ? pick_layernorm(rows, cols, vec, aligned16, info.max_smem_optin) : form;
   const uint16_t *bx = static_cast<const uint16_t *>(x);
   uint16_t *by = static_cast<uint16_t *>(y);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

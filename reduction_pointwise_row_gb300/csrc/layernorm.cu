@@ -529,6 +529,7 @@ layernorm_cluster(const uint16_t *__restrict__ x, const float *__restrict__ gamm
 // the step being reduced, and 2R + A row slots (the previous step's R rows,
 // this step's R and those ahead).
 __host__ __device__ constexpr int full_slots(int R, int A) { return 2 * R + A; }
+constexpr int kFullMaxCluster = 8;
 
 __device__ __forceinline__ void merge_equal(float &mean, float &m2, float mean_b, float m2_b,
                                             float half_n) {
@@ -563,8 +564,10 @@ __device__ __forceinline__ void stats16(const V8 &v, float &mean, float &m2) {
   m2 = f32x2_lo(q) + f32x2_hi(q);
 }
 
-template <int R, int A>  // A >= R: the rows a step reduces were issued a step earlier
-__global__ void __launch_bounds__(kClThreads, 1)
+// T threads per CTA (a power of two, 64 .. 512), a cluster of C CTAs
+// (1, 2, 4 or 8) per row: cols = C * T * 32.  R rows per step, A rows ahead.
+template <int T, int R, int A>  // A >= R: the rows a step reduces were issued a step earlier
+__global__ void __launch_bounds__(T, 1)
 layernorm_cluster_full(const uint16_t *__restrict__ x, const float *__restrict__ gamma,
                        const float *__restrict__ beta, uint16_t *__restrict__ y,
                        float *__restrict__ mean_out, float *__restrict__ rstd_out, int64_t rows,
@@ -573,21 +576,22 @@ layernorm_cluster_full(const uint16_t *__restrict__ x, const float *__restrict__
   constexpr int kSlotsR = full_slots(R, A), kAhead = A;
   extern __shared__ __align__(128) unsigned char smem[];  // [kSlotsR] row slices
   __shared__ __align__(8) uint64_t landed[kSlotsR];       // bulk-copy completion per slot
-  __shared__ __align__(16) float4 slot[kClSlots][kClMaxCluster];  // [step % 4][rank]
+  __shared__ __align__(16) float4 slot[kClSlots][kFullMaxCluster];  // [step % 4][rank]
   __shared__ __align__(8) uint64_t pbar[kClSlots];
-  __shared__ float2 red[2][R][kClThreads / 32];  // per-warp (mean, M2), double-buffered by step
+  constexpr int W = T / 32;
+  __shared__ float2 red[2][R][W];  // per-warp (mean, M2), double-buffered by step
   __shared__ int timed_out;
 
   const uint32_t C = cluster_nctarank(), q = cluster_ctarank();
   const int64_t cid = cluster_id_x(), ncl = ncluster_x();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t S = cols / C;  // = 512 * 32
+  const int64_t S = cols / C;  // = T * 32
   const uint32_t slice = static_cast<uint32_t>(S) * 2;  // bytes of a row slice
-  // Thread t owns the 16-byte chunks j = t + 512 c (c = 0..3) of its CTA's
+  // Thread t owns the 16-byte chunks j = t + T c (c = 0..3) of its CTA's
   // slice, columns 8j .. 8j + 7: a warp's shared-memory reads and global
   // stores of one chunk are 512 contiguous bytes (no bank conflicts).
   const int64_t cbase = static_cast<int64_t>(q) * S + 8 * static_cast<int64_t>(tid);
-  constexpr int64_t kChunkStride = 8 * kClThreads;  // columns between a thread's chunks
+  constexpr int64_t kChunkStride = 8 * T;  // columns between a thread's chunks
   const int64_t nr = cid < rows ? (rows - cid + ncl - 1) / ncl : 0;  // rows of this cluster
   const int64_t ns = (nr + R - 1) / R;                                // steps of R rows
   const uint32_t part_bytes = 16u * C;
@@ -608,8 +612,8 @@ layernorm_cluster_full(const uint16_t *__restrict__ x, const float *__restrict__
   // this thread's 32 values of a staged row: chunks 0, 1 in one V8, 2, 3 in another
   auto read_row = [&](int64_t k, V8 &c0, V8 &c1) {
     const unsigned char *p = slot_of(k) + static_cast<size_t>(tid) * 16;
-    const uint4 a = lds_u4(p), b = lds_u4(p + 16 * kClThreads), c = lds_u4(p + 32 * kClThreads),
-                d = lds_u4(p + 48 * kClThreads);
+    const uint4 a = lds_u4(p), b = lds_u4(p + 16 * T), c = lds_u4(p + 32 * T),
+                d = lds_u4(p + 48 * T);
     c0.w[0] = a.x; c0.w[1] = a.y; c0.w[2] = a.z; c0.w[3] = a.w;
     c0.w[4] = b.x; c0.w[5] = b.y; c0.w[6] = b.z; c0.w[7] = b.w;
     c1.w[0] = c.x; c1.w[1] = c.y; c1.w[2] = c.z; c1.w[3] = c.w;
@@ -684,17 +688,17 @@ layernorm_cluster_full(const uint16_t *__restrict__ x, const float *__restrict__
 #pragma unroll
         for (int r = 0; r < R; ++r) issue(s * R + r + kAhead);
       }
-      if (warp == 0) {  // the CTA's 16 warp pairs (1024 values each) on lanes 0..15
+      if (warp == 0) {  // the CTA's W warp pairs (1024 values each) on lanes 0..W-1
         float wm[R], w2[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-          const float2 t = red[s & 1][r][lane & (kClThreads / 32 - 1)];
+          const float2 t = red[s & 1][r][lane & (W - 1)];
           wm[r] = t.x;
           w2[r] = t.y;
         }
         float hn = 512.0f;
 #pragma unroll
-        for (int o = kClThreads / 64; o > 0; o >>= 1, hn *= 2.0f)
+        for (int o = W / 2; o > 0; o >>= 1, hn *= 2.0f)
 #pragma unroll
           for (int r = 0; r < R; ++r)
             merge_equal(wm[r], w2[r], __shfl_xor_sync(0xffffffffu, wm[r], o),
@@ -715,19 +719,32 @@ layernorm_cluster_full(const uint16_t *__restrict__ x, const float *__restrict__
         timed_out = 1;
         atomicCAS(err, 0, FR_DEVERR_TIMEOUT);
       }
-      const float4 u0 = slot[sl][0];
-      const float4 u1 = C == 2 ? slot[sl][1] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      // Re-arm slot sl for step sp + 4 (peers send it only after this CTA
-      // publishes step sp + 2, which comes after this point).
+      // Re-arm slot sl for step sp + 4 after reading it (peers send it only
+      // after this CTA publishes step sp + 2, which comes after this point).
+      float4 u[kFullMaxCluster];
+#pragma unroll
+      for (int rk = 0; rk < kFullMaxCluster; ++rk)
+        u[rk] = rk < static_cast<int>(C) ? slot[sl][rk] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       if (tid == 0 && sp + kClSlots < ns) mbar_arrive_expect_tx(&pbar[sl], part_bytes);
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         const int64_t k = sp * R + r;
         if (k >= nr) break;
-        float mean = r == 0 ? u0.x : u0.z, m2 = r == 0 ? u0.y : u0.w;
-        if (C == 2)  // rank order: identical in every CTA
-          merge_equal(mean, m2, r == 0 ? u1.x : u1.z, r == 0 ? u1.y : u1.w,
-                      0.5f * static_cast<float>(S));
+        // the C ranks' pairs merged by a fixed tree over rank order (equal
+        // counts at every level): the same bits in every CTA of the cluster
+        float cm[kFullMaxCluster], c2[kFullMaxCluster];
+#pragma unroll
+        for (int rk = 0; rk < kFullMaxCluster; ++rk) {
+          cm[rk] = r == 0 ? u[rk].x : u[rk].z;
+          c2[rk] = r == 0 ? u[rk].y : u[rk].w;
+        }
+        float hs = 0.5f * static_cast<float>(S);
+#pragma unroll
+        for (int w = 1; w < kFullMaxCluster; w <<= 1, hs *= 2.0f)
+#pragma unroll
+          for (int rk = 0; rk + w < kFullMaxCluster; rk += 2 * w)
+            if (rk + w < static_cast<int>(C)) merge_equal(cm[rk], c2[rk], cm[rk + w], c2[rk + w], hs);
+        const float mean = cm[0], m2 = c2[0];
         const int64_t row = row_of(k);
         const float rstd = rsqrtf(fmaf(m2, inv_n, eps));
         if (q == 0 && tid == 0) {
@@ -738,7 +755,7 @@ layernorm_cluster_full(const uint16_t *__restrict__ x, const float *__restrict__
         const unsigned char *p = slot_of(k) + static_cast<size_t>(tid) * 16;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {  // chunk c: 8 columns, pairs 4c .. 4c + 3
-          const uint4 v = lds_u4(p + 16 * kClThreads * c);
+          const uint4 v = lds_u4(p + 16 * T * c);
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
           uint32_t o[4];
 #pragma unroll
@@ -775,9 +792,49 @@ size_t cluster_smem(int64_t, int) {
   return static_cast<size_t>(kClStages) * kClThreads * 64;  // the cp.async ring
 }
 
+
+namespace {
+
+using LnKern = void (*)(const uint16_t *, const float *, const float *, uint16_t *, float *,
+                        float *, int64_t, int64_t, int64_t, int64_t, float, int *);
+
+// One rows-per-step / rows-ahead choice of the equal-count kernel, for each
+// CTA size.
+struct FullShape {
+  const char *name;
+  int slots;
+  LnKern kern[4];  // T = 64, 128, 256, 512
+};
+
+#define FR_LNF(R, A)                                                                       \
+  {layernorm_cluster_full<64, R, A>, layernorm_cluster_full<128, R, A>,                      \
+   layernorm_cluster_full<256, R, A>, layernorm_cluster_full<512, R, A>}
+const FullShape kFullShapes[] = {{"r1a2", full_slots(1, 2), FR_LNF(1, 2)},
+                                 {"r1a1", full_slots(1, 1), FR_LNF(1, 1)},
+                                 {"r1a3", full_slots(1, 3), FR_LNF(1, 3)},
+                                 {"r1a4", full_slots(1, 4), FR_LNF(1, 4)},
+                                 {"r1a5", full_slots(1, 5), FR_LNF(1, 5)},
+                                 {"r2a2", full_slots(2, 2), FR_LNF(2, 2)}};
+#undef FR_LNF
+
+// The equal-count kernel's shape for a row length: cols = C * T * 32 with T a
+// power of two in 64 .. 512 (the largest that fits) and C in 1, 2, 4, 8.
+bool full_shape(int64_t cols, int *T, int *C) {
+  for (int c = 1; c <= kFullMaxCluster; c <<= 1)
+    for (int t = 512; t >= 64; t >>= 1)
+      if (cols == static_cast<int64_t>(c) * t * kClCols) {
+        *T = t;
+        *C = c;
+        return true;
+      }
+  return false;
+}
+
+}  // namespace
+
 bool layernorm_cluster_ok(int64_t cols, bool aligned) {
-  const int c = cluster_size_for(cols);
-  return aligned && c > 0;
+  int t = 0, c = 0;
+  return aligned && (cluster_size_for(cols) > 0 || full_shape(cols, &t, &c));
 }
 
 cudaError_t launch_layernorm_cluster(const uint16_t *x, const float *gamma, const float *beta,
@@ -787,43 +844,38 @@ cudaError_t launch_layernorm_cluster(const uint16_t *x, const float *gamma, cons
   int *err = nullptr;
   cudaError_t e = device_error_word(&err);
   if (e != cudaSuccess) return e;
-  const int C = cluster_size_for(cols);
-  if (C == 0) return cudaErrorInvalidValue;
-  // Every thread holding 32 columns: the equal-count kernel with R rows per
-  // step and A rows ahead (FR_LAYERNORM_CLUSTER=classic|r1a1|...|r2a2 pins
-  // one; default r1a2).  Measured on GB300, bf16 [4096, 32768]: r1a2 91.4 us,
-  // r1a3 93.2, r2a2 95.8, r1a5 97.3, r1a4 98.2, r1a1 113.9, classic 132.3.
+  // Rows of C * T * 32 columns: the equal-count kernel (every thread 32
+  // columns), R rows per step and A rows ahead (FR_LAYERNORM_CLUSTER=classic|
+  // r1a1|...|r2a2 pins one; default r1a2).  Measured on GB300, bf16
+  // [4096, 32768]: r1a2 91.4 us, r1a3 93.2, r2a2 95.8, r1a5 97.3, r1a4 98.2,
+  // r1a1 113.9, classic 132.3.  Other rows: the general cluster kernel.
   const char *pin = getenv("FR_LAYERNORM_CLUSTER");
   auto pinned = [&](const char *v) { return pin != nullptr && strcmp(pin, v) == 0; };
-  const bool full = cols == static_cast<int64_t>(C) * kClThreads * kClCols && !pinned("classic");
-  struct Shape {
-    const char *name;
-    void (*kern)(const uint16_t *, const float *, const float *, uint16_t *, float *, float *,
-                 int64_t, int64_t, int64_t, int64_t, float, int *);
-    int slots;
-  };
-  static const Shape shapes[] = {{"r1a2", layernorm_cluster_full<1, 2>, full_slots(1, 2)},
-                                 {"r1a1", layernorm_cluster_full<1, 1>, full_slots(1, 1)},
-                                 {"r1a3", layernorm_cluster_full<1, 3>, full_slots(1, 3)},
-                                 {"r1a4", layernorm_cluster_full<1, 4>, full_slots(1, 4)},
-                                 {"r1a5", layernorm_cluster_full<1, 5>, full_slots(1, 5)},
-                                 {"r2a2", layernorm_cluster_full<2, 2>, full_slots(2, 2)}};
-  const Shape *sh = &shapes[0];
-  for (const Shape &c : shapes)
+  int T = kClThreads, C = 0;
+  const bool full = !pinned("classic") && full_shape(cols, &T, &C);
+  if (!full) {
+    T = kClThreads;
+    C = cluster_size_for(cols);
+  }
+  if (C == 0) return cudaErrorInvalidValue;
+  const FullShape *sh = &kFullShapes[0];
+  for (const FullShape &c : kFullShapes)
     if (pinned(c.name)) sh = &c;
-  auto kern = full ? sh->kern : layernorm_cluster;
+  const int ti = T == 64 ? 0 : T == 128 ? 1 : T == 256 ? 2 : 3;
+  LnKern kern = full ? sh->kern[ti] : layernorm_cluster;
   const size_t smem = !full ? cluster_smem(cols, C)
                             : static_cast<size_t>(sh->slots) * static_cast<size_t>(cols / C) * 2;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem));
   if (e != cudaSuccess) return e;
+  if (C > 8) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(C);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kClThreads);
+  cfg.blockDim = dim3(static_cast<unsigned>(T));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = attr;

@@ -277,6 +277,32 @@ def test_layernorm_cluster_variants(o, variant, cols):
     assert fr.fr_check_device_error() == 0
 
 
+@pytest.mark.parametrize("variant", ["r1a2", "r2a2", "r1a3"])
+@pytest.mark.parametrize("cols", [2048, 4096, 8192, 65536, 131072])
+def test_layernorm_equal_count_shapes(o, variant, cols):
+    """The equal-count cluster kernel at every CTA size (64 .. 512 threads) and
+    cluster size (1 .. 8 CTAs per row): cols = C x T x 32."""
+    import os
+    for rows in ((1, 5, 77, 301) if cols <= 8192 else (1, 5, 40)):
+        w = workloads.make(2, rows=rows, cols=cols, seed=3700 + rows + cols)
+        x = w.arrays["x"].copy()
+        if rows >= 5:
+            x[2, :] = 0x3F80  # 1.0: var 0
+        eps = float(np.float32(w.params["eps"]))
+        ry, rm, rr = o.layernorm(x, w.arrays["gamma"], w.arrays["beta"], eps)
+        os.environ["FR_LAYERNORM_CLUSTER"] = variant
+        try:
+            y, m, r = run_layernorm(x, w.arrays["gamma"], w.arrays["beta"], eps, "looped",
+                                    kernel="cluster")
+        finally:
+            os.environ.pop("FR_LAYERNORM_CLUSTER", None)
+        what = f"{variant} {rows}x{cols}"
+        assert_close(y, ry, "bf16", f"{what} y")
+        assert_close(m, rm, "mean", f"{what} mean")
+        assert_close(r, rr, "f32", f"{what} rstd")
+    assert fr.fr_check_device_error() == 0
+
+
 def test_layernorm_constant_rows(o):
     cols = 4096
     x = np.full((4, cols), 0x4060, np.uint16)  # 3.5 in bf16
