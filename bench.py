@@ -188,13 +188,11 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize()
 
-    def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        import torch.distributed as dist
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    global SHARD
+    SHARD = (rank, world)
+
+    def max_ranks(x: float) -> float:
+        return max_over_ranks(x, world, dev)
 
     def timed(calls, steps, warmup, launches_per_call):
         """Mean device time (s) per launch: launches back to back, cycling over
@@ -213,7 +211,7 @@ def run_ours(args):
         if clocks:
             clocks.window(w0, time.time())
         ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-        return max_over_ranks(statistics.fmean(ms) / 1e3), launches_per_call * steps, ms
+        return max_ranks(statistics.fmean(ms) / 1e3), launches_per_call * steps, ms
 
     if args.only == "xent_box":
         if rank == 0:
@@ -227,7 +225,7 @@ def run_ours(args):
         return
 
     # ---- headline: softmax persistent fp32 [32768, 1024]
-    w = workloads.make(HEADLINE)
+    w = make_shard(workloads, HEADLINE)
     rows, cols = w.rows, w.cols
     calls, _, _, _, _ = setup_workload("softmax", fr, workloads, dev)
     calls[0]()
@@ -272,7 +270,7 @@ def run_ours(args):
     e1.record(stream)
     barrier()
     clocks.window(w0, time.time())
-    t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3 / e2e_steps)
+    t_e2e = max_ranks(e0.elapsed_time(e1) / 1e3 / e2e_steps)
     e2e = {"value": round(world * nbytes / t_e2e / 1e9, 2), "unit": UNIT,
            "h2d_bytes_per_step": x_host.numel() * 4, "d2h_bytes_per_step": y_host.numel() * 4,
            "ms_per_step": round(t_e2e * 1e3, 4), "api": "fr_softmax_host",
@@ -319,6 +317,35 @@ def run_ours(args):
 
 ROTATE_BYTES = 1 << 30  # footprint of the rotating input/output sets (8x the L2)
 
+# This rank's shard of every workload: with N ranks the global batch has N
+# times the rows and rank r holds rows r*R .. r*R + R - 1 (the generators are
+# counter-based, so a shard is exactly those rows of the global array).  Rows
+# are independent, so no rank exchanges anything (weak scaling).
+SHARD = (0, 1)
+
+
+def shard_rows(rows: int, rank: int, world: int) -> tuple[int, int]:
+    """(first row, global rows) of rank's shard when every rank holds `rows`."""
+    return rank * rows, world * rows
+
+
+def make_shard(workloads, cfg: int, rows: int | None = None, cols: int | None = None, **kw):
+    rank, world = SHARD
+    R = workloads.FULL_SHAPES[cfg][1] if rows is None else rows
+    row0, g = shard_rows(R, rank, world)
+    return workloads.make(cfg, rows=R, cols=cols, row0=row0, global_rows=g, **kw)
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of the ranks' values (every rank gets it)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
 
 def setup_workload(name, fr, workloads, dev, form="auto"):
     """Device inputs and calls of one workload: (calls, op, rows, cols,
@@ -333,13 +360,13 @@ def setup_workload(name, fr, workloads, dev, form="auto"):
 
     calls = []
     if name == "relu_add_sum":
-        w = workloads.make(0)
+        w = make_shard(workloads, 0)
         a, b = to_device(w.arrays["a"], dev), to_device(w.arrays["b"], dev)
         out = torch.empty(w.rows, device=dev)
         calls.append(lambda: fr.fr_reduce_relu_add_sum(a, b, 2.0, out=out, form=form))
         return calls, "relu_add_sum", w.rows, w.cols, 1
     if name == "softmax":
-        w = workloads.make(1)
+        w = make_shard(workloads, 1)
         for _ in range(nsets("softmax", w.rows, w.cols)):
             x = to_device(w.arrays["x"], dev)
             y = torch.empty_like(x)
@@ -351,7 +378,7 @@ def setup_workload(name, fr, workloads, dev, form="auto"):
         # online form
         cols = int(name.split("_")[1])
         f = "looped" if name.endswith("_looped") else form
-        w = workloads.make(1, rows=(1 << 25) // cols, cols=cols)
+        w = make_shard(workloads, 1, rows=(1 << 25) // cols, cols=cols)
         for _ in range(nsets("softmax", w.rows, w.cols)):
             x = to_device(w.arrays["x"], dev)
             y = torch.empty_like(x)
@@ -359,7 +386,7 @@ def setup_workload(name, fr, workloads, dev, form="auto"):
         return calls, "softmax", w.rows, w.cols, 1
     if name == "softmax_bf16":
         # the bf16 softmax on [65536, 1024] (the fp32 workload's 256 MiB)
-        w = workloads.make_softmax_bf16(65536, 1024)
+        w = workloads.make_softmax_bf16(65536, 1024, seed=20261202 + 6 + 1000 * SHARD[0])
         for _ in range(nsets("softmax_bf16", w.rows, w.cols)):
             x = to_device(w.arrays["x"], dev)
             y = torch.empty_like(x)
@@ -367,13 +394,13 @@ def setup_workload(name, fr, workloads, dev, form="auto"):
         return calls, "softmax_bf16", w.rows, w.cols, 1
     if name == "looped":
         # Example 1.1's looped form on 16384 rows of 8192 (1 GiB of a and b)
-        w = workloads.make(0, rows=16384, cols=8192)
+        w = make_shard(workloads, 0, rows=16384, cols=8192)
         a, b = to_device(w.arrays["a"], dev), to_device(w.arrays["b"], dev)
         out = torch.empty(w.rows, device=dev)
         calls.append(lambda: fr.fr_reduce_relu_add_sum(a, b, 2.0, out=out, form=form))
         return calls, "relu_add_sum", w.rows, w.cols, 1
     if name == "layernorm":
-        w = workloads.make(2)
+        w = make_shard(workloads, 2)
         g, bt = to_device(w.arrays["gamma"], dev), to_device(w.arrays["beta"], dev)
         for _ in range(nsets("layernorm", w.rows, w.cols)):
             x = to_device(w.arrays["x"], dev)
@@ -385,7 +412,7 @@ def setup_workload(name, fr, workloads, dev, form="auto"):
                                          form=form))
         return calls, "layernorm", w.rows, w.cols, 1
     if name == "split":
-        w = workloads.make(3)
+        w = make_shard(workloads, 3)
         rows, cols = w.rows, w.cols
         for _ in range(nsets("relu_add_sum", rows, cols)):
             a, b = to_device(w.arrays["a"], dev), to_device(w.arrays["b"], dev)
@@ -399,7 +426,9 @@ def setup_workload(name, fr, workloads, dev, form="auto"):
     if name in ("sumsq", "l2norm"):
         # Example 6.2's [64, 16384] sum of squares (split form), and the row L2
         # norm over 1 GiB of [16384, 16384] rows (looped form)
-        w = workloads.make_sumsq() if name == "sumsq" else workloads.make_sumsq(16384, 16384)
+        sd = 20261202 + 5 + 1000 * SHARD[0]  # rank r: its own batch of rows
+        w = (workloads.make_sumsq(seed=sd) if name == "sumsq"
+             else workloads.make_sumsq(16384, 16384, seed=sd))
         rows, cols = w.rows, w.cols
         epi = "sum" if name == "sumsq" else "sqrt"
         for _ in range(nsets("sumsq", rows, cols)):
@@ -412,7 +441,7 @@ def setup_workload(name, fr, workloads, dev, form="auto"):
         split = fr.fr_workspace_size("sumsq", rows, cols, "f32", form) > 0
         return calls, "sumsq", rows, cols, 2 if split else 1
     if name == "xent":
-        w = workloads.make(4)
+        w = make_shard(workloads, 4)
         rows, cols = w.rows, w.cols
         tg = torch.from_numpy(w.arrays["target"]).to(dev)
         for _ in range(nsets("xent", rows, cols)):
@@ -497,7 +526,7 @@ def tune_xent(fr, workloads, dev, calls, timed, steps, args, nb, peak):
     workload (candidate set, then coordinate descent, eps = 0.02), followed by
     the same back-to-back timing with the chosen configuration."""
     import torch
-    w = workloads.make(4)
+    w = make_shard(workloads, 4)
     lg = to_device(w.arrays["logits"], dev)
     tg = torch.from_numpy(w.arrays["target"]).to(dev)
     fr.fr_xent_set_config(w.rows, w.cols, None)
@@ -585,7 +614,7 @@ def run_reference(args):
     import oracle
     from reduction_pointwise_row_gb300 import traffic
     from synth import workloads
-    w = workloads.make(HEADLINE)
+    w = make_shard(workloads, HEADLINE)
     o = oracle.get()
     rows = 4096  # bounded sample per step: about 0.3 s of CPU work
     x = w.arrays["x"][:rows]

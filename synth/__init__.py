@@ -39,12 +39,16 @@ def _load():
         lib.synth_uniform_f32.argtypes = [vp, i64, u64, u64, dbl, dbl]
         lib.synth_normal_f32.argtypes = [vp, i64, u64, u64, dbl, dbl]
         lib.synth_normal_bf16.argtypes = [vp, i64, u64, u64, dbl, dbl]
+        lib.synth_uniform_f32_at.argtypes = [vp, i64, u64, u64, u64, dbl, dbl]
+        lib.synth_normal_f32_at.argtypes = [vp, i64, u64, u64, u64, dbl, dbl]
+        lib.synth_normal_bf16_at.argtypes = [vp, i64, u64, u64, u64, dbl, dbl]
         lib.synth_targets.argtypes = [vp, i64, u64, u64, i64, i64, i64]
         lib.synth_targets.restype = ctypes.c_int
         lib.synth_indices.argtypes = [vp, i64, u64, u64, i64]
         lib.synth_u64.argtypes = [u64, u64, u64]
         lib.synth_u64.restype = u64
         for f in (lib.synth_uniform_f32, lib.synth_normal_f32, lib.synth_normal_bf16,
+                  lib.synth_uniform_f32_at, lib.synth_normal_f32_at, lib.synth_normal_bf16_at,
                   lib.synth_indices):
             f.restype = None
         _lib = lib
@@ -63,24 +67,28 @@ def u64(seed: int, stream: int, i: int) -> int:
     return int(_load().synth_u64(seed, stream, i))
 
 
-def uniform_f32(shape, seed: int, stream: int, lo: float = -1.0, hi: float = 1.0, out=None):
-    """fp32 array, each element uniform in [lo, hi) (24 random bits)."""
+def uniform_f32(shape, seed: int, stream: int, lo: float = -1.0, hi: float = 1.0, out=None,
+                first: int = 0):
+    """fp32 array, each element uniform in [lo, hi) (24 random bits); elements
+    first .. of the stream (a slice of a larger array when first > 0)."""
     a = _empty(shape, np.float32, out)
-    _load().synth_uniform_f32(a.ctypes.data, a.size, seed, stream, lo, hi)
+    _load().synth_uniform_f32_at(a.ctypes.data, a.size, seed, stream, first, lo, hi)
     return a
 
 
-def normal_f32(shape, seed: int, stream: int, mean: float = 0.0, std: float = 1.0, out=None):
+def normal_f32(shape, seed: int, stream: int, mean: float = 0.0, std: float = 1.0, out=None,
+               first: int = 0):
     """fp32 array of mean + std * N(0, 1) (Box-Muller in fp64, cast RNE)."""
     a = _empty(shape, np.float32, out)
-    _load().synth_normal_f32(a.ctypes.data, a.size, seed, stream, mean, std)
+    _load().synth_normal_f32_at(a.ctypes.data, a.size, seed, stream, first, mean, std)
     return a
 
 
-def normal_bf16(shape, seed: int, stream: int, mean: float = 0.0, std: float = 1.0, out=None):
+def normal_bf16(shape, seed: int, stream: int, mean: float = 0.0, std: float = 1.0, out=None,
+                first: int = 0):
     """uint16 array holding the bf16 bit patterns of mean + std * N(0, 1)."""
     a = _empty(shape, np.uint16, out)
-    _load().synth_normal_bf16(a.ctypes.data, a.size, seed, stream, mean, std)
+    _load().synth_normal_bf16_at(a.ctypes.data, a.size, seed, stream, first, mean, std)
     return a
 
 

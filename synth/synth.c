@@ -81,7 +81,7 @@ typedef struct {
   int kind;
   void *out;
   int64_t begin, end;
-  uint64_t s0;
+  uint64_t s0, first; /* output i holds stream element first + i */
   double p0, p1;
 } fill_job;
 
@@ -90,21 +90,21 @@ static void *fill_worker(void *arg) {
   if (j->kind == K_UNIFORM_F32) {
     float *o = (float *)j->out;
     for (int64_t i = j->begin; i < j->end; ++i)
-      o[i] = (float)(j->p0 + (j->p1 - j->p0) * u24(sm64_at(j->s0, (uint64_t)i)));
+      o[i] = (float)(j->p0 + (j->p1 - j->p0) * u24(sm64_at(j->s0, j->first + (uint64_t)i)));
   } else if (j->kind == K_NORMAL_F32) {
     float *o = (float *)j->out;
     for (int64_t i = j->begin; i < j->end; ++i)
-      o[i] = (float)(j->p0 + j->p1 * normal_at(j->s0, (uint64_t)i));
+      o[i] = (float)(j->p0 + j->p1 * normal_at(j->s0, j->first + (uint64_t)i));
   } else {
     uint16_t *o = (uint16_t *)j->out;
     for (int64_t i = j->begin; i < j->end; ++i)
-      o[i] = f32_to_bf16_rne((float)(j->p0 + j->p1 * normal_at(j->s0, (uint64_t)i)));
+      o[i] = f32_to_bf16_rne((float)(j->p0 + j->p1 * normal_at(j->s0, j->first + (uint64_t)i)));
   }
   return NULL;
 }
 
-static void fill(int kind, void *out, int64_t n, uint64_t seed, uint64_t stream, double p0,
-                 double p1) {
+static void fill(int kind, void *out, int64_t n, uint64_t seed, uint64_t stream, uint64_t first,
+                 double p0, double p1) {
   enum { MAX_T = 64 };
   long nc = sysconf(_SC_NPROCESSORS_ONLN);
   int t = (int)(nc < 1 ? 1 : (nc > MAX_T ? MAX_T : nc));
@@ -117,7 +117,7 @@ static void fill(int kind, void *out, int64_t n, uint64_t seed, uint64_t stream,
     int64_t b = (int64_t)k * per, e = b + per;
     if (b > n) b = n;
     if (e > n) e = n;
-    jobs[k] = (fill_job){kind, out, b, e, s0, p0, p1};
+    jobs[k] = (fill_job){kind, out, b, e, s0, first, p0, p1};
   }
   int started[MAX_T] = {0};
   for (int k = 1; k < t; ++k) {
@@ -129,22 +129,35 @@ static void fill(int kind, void *out, int64_t n, uint64_t seed, uint64_t stream,
     if (started[k]) pthread_join(th[k], NULL);
 }
 
-/* n fp32 values uniform in [lo, hi). */
+/* n fp32 values uniform in [lo, hi): elements first .. first + n - 1 of the
+ * stream (first = 0: the start; a later first gives a slice of a larger array). */
+void synth_uniform_f32_at(float *out, int64_t n, uint64_t seed, uint64_t stream, uint64_t first,
+                          double lo, double hi) {
+  fill(K_UNIFORM_F32, out, n, seed, stream, first, lo, hi);
+}
 void synth_uniform_f32(float *out, int64_t n, uint64_t seed, uint64_t stream, double lo,
                        double hi) {
-  fill(K_UNIFORM_F32, out, n, seed, stream, lo, hi);
+  synth_uniform_f32_at(out, n, seed, stream, 0, lo, hi);
 }
 
-/* n fp32 values mean + std * N(0,1). */
+/* n fp32 values mean + std * N(0,1) (elements first .. of the stream). */
+void synth_normal_f32_at(float *out, int64_t n, uint64_t seed, uint64_t stream, uint64_t first,
+                         double mean, double std) {
+  fill(K_NORMAL_F32, out, n, seed, stream, first, mean, std);
+}
 void synth_normal_f32(float *out, int64_t n, uint64_t seed, uint64_t stream, double mean,
                       double std) {
-  fill(K_NORMAL_F32, out, n, seed, stream, mean, std);
+  synth_normal_f32_at(out, n, seed, stream, 0, mean, std);
 }
 
 /* n bf16 bit patterns of mean + std * N(0,1) (fp64 -> fp32 -> bf16, each RNE). */
+void synth_normal_bf16_at(uint16_t *out, int64_t n, uint64_t seed, uint64_t stream,
+                          uint64_t first, double mean, double std) {
+  fill(K_NORMAL_BF16, out, n, seed, stream, first, mean, std);
+}
 void synth_normal_bf16(uint16_t *out, int64_t n, uint64_t seed, uint64_t stream, double mean,
                        double std) {
-  fill(K_NORMAL_BF16, out, n, seed, stream, mean, std);
+  synth_normal_bf16_at(out, n, seed, stream, 0, mean, std);
 }
 
 /* n class indices uniform in [0, V) (Lemire's multiply-shift), then exactly

@@ -51,18 +51,28 @@ def seed_of(cfg: int) -> int:
 
 
 def make(cfg: int, rows: int | None = None, cols: int | None = None, nan_variant: bool = False,
-         seed: int | None = None) -> Workload:
-    """Host arrays for configuration ``cfg`` (optionally at another shape)."""
+         seed: int | None = None, row0: int = 0, global_rows: int | None = None) -> Workload:
+    """Host arrays for configuration ``cfg`` (optionally at another shape).
+
+    ``row0``/``global_rows``: rows row0 .. row0 + rows - 1 of the same workload
+    with ``global_rows`` rows (a data-parallel shard); the values are exactly
+    those rows of the whole array (the generators are counter-based).
+    """
     op, R, C = FULL_SHAPES[cfg]
     R = R if rows is None else rows
     C = C if cols is None else cols
+    G = row0 + R if global_rows is None else global_rows
+    assert 0 <= row0 and row0 + R <= G
+    f = row0 * C  # first stream element of the shard
     s = seed_of(cfg) if seed is None else seed
     w = Workload(name=NAMES[cfg], op=op, rows=R, cols=C)
+    w.params["row0"], w.params["global_rows"] = row0, G
     if op == "relu_add_sum":
-        w.arrays["a"] = uniform_f32((R, C), s, 0, -1.0, 1.0)
-        w.arrays["b"] = uniform_f32((R, C), s, 1, -1.0, 1.0)
+        w.arrays["a"] = uniform_f32((R, C), s, 0, -1.0, 1.0, first=f)
+        w.arrays["b"] = uniform_f32((R, C), s, 1, -1.0, 1.0, first=f)
         w.params["scale"] = 2.0
         if nan_variant:
+            assert row0 == 0 and G == R, "the NaN variant is not sharded"
             # 4 NaNs at seeded (array, row, col) positions; positions may share rows.
             flat = indices(4, 2 * R * C, s, 2)
             pos = []
@@ -74,16 +84,16 @@ def make(cfg: int, rows: int | None = None, cols: int | None = None, nan_variant
                 pos.append((name, r, c))
             w.params["nan_positions"] = pos
     elif op == "softmax":
-        w.arrays["x"] = normal_f32((R, C), s, 0, 0.0, 4.0)
+        w.arrays["x"] = normal_f32((R, C), s, 0, 0.0, 4.0, first=f)
     elif op == "layernorm":
-        w.arrays["x"] = normal_bf16((R, C), s, 0, 0.5, 2.0)
+        w.arrays["x"] = normal_bf16((R, C), s, 0, 0.5, 2.0, first=f)
         w.arrays["gamma"] = normal_f32((C,), s, 1, 1.0, 0.1)
         w.arrays["beta"] = normal_f32((C,), s, 2, 0.0, 0.1)
         w.params["eps"] = 1e-5
     elif op == "xent":
-        w.arrays["logits"] = normal_bf16((R, C), s, 0, 0.0, 3.0)
-        n_ignore = int(round(0.05 * R))
-        w.arrays["target"] = targets(R, C, n_ignore, IGNORE_INDEX, s, 1)
+        w.arrays["logits"] = normal_bf16((R, C), s, 0, 0.0, 3.0, first=f)
+        n_ignore = int(round(0.05 * G))  # 5 % of the whole batch
+        w.arrays["target"] = targets(G, C, n_ignore, IGNORE_INDEX, s, 1)[row0:row0 + R].copy()
         w.params["ignore_index"] = IGNORE_INDEX
     else:
         raise ValueError(op)
