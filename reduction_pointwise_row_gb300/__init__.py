@@ -110,10 +110,17 @@ def _check(status: int, where: str):
         raise FRError(status, where)
 
 
-def _stream(stream=None):
+def _stream(stream=None, device_index=None):
+    """The raw cudaStream_t to launch on: `stream`, else the current stream of
+    the current (or given) device."""
     import torch
-    s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+    if stream is not None:
+        return ctypes.c_void_p(stream.cuda_stream)
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:  # one call instead of building a Stream object
+        idx = torch.cuda.current_device() if device_index is None else device_index
+        return ctypes.c_void_p(raw(idx))
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
 def _ptr(t):
@@ -137,9 +144,15 @@ def fr_workspace_size(op: str, rows: int, cols: int, dtype: str = "f32", form: s
     return lib().fr_workspace_size(OPS[op], rows, cols, DTYPES[dtype], FORMS[form])
 
 
+_WS_SIZES = {}  # (op, rows, cols, dtype, form, device index) -> bytes
+
+
 def _workspace(op, rows, cols, dtype, form, device, given=None):
     import torch
-    n = fr_workspace_size(op, rows, cols, dtype, form)
+    key = (op, rows, cols, dtype, form, device.index)
+    n = _WS_SIZES.get(key)
+    if n is None:  # depends only on the shape and the device model
+        n = _WS_SIZES[key] = fr_workspace_size(op, rows, cols, dtype, form)
     if n == 0:
         return None, 0
     if given is not None:

@@ -1019,11 +1019,46 @@ void xent_record_config(int device, int64_t rows, int64_t cols, int64_t ld,
   if (cfg) g_recorded.push_back(Recorded{device, rows, cols, ld, *cfg});
 }
 
+// The argmax kernel at the default point of the box (up to its CTAs per SM
+// when the larger argmax kernel keeps fewer resident).
+cudaError_t launch_xent_argmax_default(const uint16_t *logits, const int64_t *target, float *loss,
+                                       float *loss_mean, float *target_logit, int64_t *argmax,
+                                       int64_t rows, int64_t cols, int64_t ld,
+                                       int64_t ignore_index, void *workspace, int sm_count,
+                                       cudaStream_t s) {
+  constexpr int T = 128, U = 8, NS = 2;
+  const XentConfig d = xent_default_config();
+  static_assert(T == 128 && U == 8 && NS == 2, "keep in step with xent_default_config()");
+  if (d.threads != T || d.vectors != U || d.stages != NS) return cudaErrorInvalidValue;
+  const void *kern = reinterpret_cast<const void *>(&xent_async<true, T, U, NS>);
+  const size_t smem = static_cast<size_t>(NS) * U * T * 16;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, T, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  if (per_sm > d.ctas_per_sm) per_sm = d.ctas_per_sm;
+  int64_t grid = static_cast<int64_t>(sm_count) * per_sm;
+  if (grid > rows) grid = rows;
+  if (loss_mean != nullptr) {
+    e = cudaMemsetAsync(workspace, 0, 16, s);
+    if (e != cudaSuccess) return e;
+  }
+  void *args[] = {&logits, &target, &loss, &target_logit, &argmax, &loss_mean, &workspace,
+                  &rows, &cols, &ld, &ignore_index};
+  return cudaLaunchKernel(kern, dim3(static_cast<unsigned>(grid)), dim3(T), args, smem, s);
+}
+
 cudaError_t launch_xent(const uint16_t *logits, const int64_t *target, float *loss,
                         float *loss_mean, float *target_logit, int64_t *argmax, int64_t rows,
                         int64_t cols, int64_t ld, int64_t ignore_index, void *workspace,
                         int sm_count, int max_smem_optin, cudaStream_t s) {
   const char *pin = getenv("FR_XENT_VARIANT");
+  if ((pin == nullptr || pin[0] == 0) && argmax != nullptr)
+    return launch_xent_argmax_default(logits, target, loss, loss_mean, target_logit, argmax, rows,
+                                      cols, ld, ignore_index, workspace, sm_count, s);
   if ((pin == nullptr || pin[0] == 0) && argmax == nullptr) {
     // the configuration recorded for this shape (fr_xent_tune / _set_config),
     // else the default point of the box
