@@ -189,6 +189,8 @@ fr_status fr_softmax(const void *x, void *y, int64_t rows, int64_t cols, int64_t
  *   workspace       device memory of fr_softmax_host_workspace(...) bytes,
  *                   256-byte aligned; one call at a time may use it
  *   dtype           FR_F32 or FR_BF16
+ * Arguments are checked before anything is enqueued; a CUDA error while the
+ * chunks are being enqueued (FR_ERR_CUDA) may leave part of the work queued.
  */
 size_t fr_softmax_host_workspace(int64_t cols, fr_dtype dtype, int64_t chunk_rows);
 fr_status fr_softmax_host(const void *x_host, void *y_host, int64_t rows, int64_t cols,
