@@ -6,9 +6,12 @@ One JSON line on stdout (rank 0).  The headline workload is the fused softmax in
 its persistent form, fp32 [32768, 1024] (logits 4*N(0,1)); a step is one call
 of fr_softmax over that batch, inputs resident in HBM, launched back to back
 over rotating copies of the inputs and outputs (1 GiB in all, eight times the
-L2, so no launch finds its operands cached), each launch timed with CUDA
-events on the stream it runs on.  ``value`` is achieved HBM GB/s: algorithmic bytes (one read
-and one write of every element) / mean launch time, summed over ranks.
+L2, so no launch finds its operands cached), the K steps timed together
+between two CUDA events on the stream they run on.  Consecutive kernels are
+programmatic dependents of one another (a kernel's CTAs are placed while the
+one before it finishes, and read nothing before it has).  ``value`` is
+achieved HBM GB/s: algorithmic bytes (one read and one write of every element)
+/ time per step, summed over ranks.
 ``per_config`` adds the other workloads of the path measured the same way.
 ``e2e`` is the same metric through the C-ABI's host-buffer call with the input copied
 from pinned host memory and the result copied back inside the timed region.
@@ -195,23 +198,22 @@ def run_ours(args):
         return max_over_ranks(x, world, dev)
 
     def timed(calls, steps, warmup, launches_per_call):
-        """Mean device time (s) per launch: launches back to back, cycling over
-        the rotating input sets, each bracketed by CUDA events on the stream."""
+        """Device time (s) per step: `steps` calls back to back, cycling over the
+        rotating input sets, between two CUDA events on the launching stream
+        (a barrier and a synchronize on both sides); the slowest rank's."""
         for i in range(warmup):
             calls[i % len(calls)]()
         barrier()
-        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         w0 = time.time()
+        e0.record(stream)
         for i in range(steps):
-            starts[i].record(stream)
             calls[i % len(calls)]()
-            ends[i].record(stream)
+        e1.record(stream)
         barrier()
         if clocks:
             clocks.window(w0, time.time())
-        ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-        return max_ranks(statistics.fmean(ms) / 1e3), launches_per_call * steps, ms
+        return max_ranks(e0.elapsed_time(e1) / 1e3 / steps), launches_per_call * steps, None
 
     if args.only == "xent_box":
         if rank == 0:
@@ -294,7 +296,7 @@ def run_ours(args):
                    "rows": rows, "cols": cols, "form": form,
                    "rows_per_s": round(world * rows / t_launch, 1),
                    "l2": f"inputs larger than L2: {nsets} rotating x/y sets (1 GiB), launches back to back",
-                   "timing": "CUDA events per launch on the launching stream, mean",
+                   "timing": "CUDA events around the K back-to-back steps on the launching stream",
                    "parallelism": f"replicas x{world} (rows shard, no collective)"},
         "roofline": {"bound": "hbm", "achieved": round(nbytes / t_launch / 1e9, 2),
                      "peak": peak, "unit": "GB/s",

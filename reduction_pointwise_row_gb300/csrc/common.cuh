@@ -11,6 +11,8 @@
 #pragma once
 
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 #include <cuda_runtime.h>
 
 #include "../../include/fr.h"
@@ -414,6 +416,77 @@ __device__ __forceinline__ RowSplit row_split(const void *p, int64_t cols, int e
   s.nvec = nvec;
   s.tail = static_cast<int>(cols - head - nvec * per);
   return s;
+}
+
+// ---- programmatic dependent launch ------------------------------------------
+// A kernel launched with launch_k may be placed on the SMs while the kernel
+// before it on the stream is finishing (its CTAs take the slots that kernel's
+// exiting CTAs free).  It starts with pdl_enter(): let the next grid be
+// placed the same way, then wait until the previous grid has completed and
+// its memory writes are visible -- so nothing is read early, whatever the
+// previous kernel wrote.  Both instructions do nothing in an ordinary launch.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// FR_PDL=0 turns the overlap off (every kernel then waits for the one before
+// it to finish before any of its CTAs is placed).
+inline bool pdl_enabled() {
+  static const bool on = [] {
+    const char *e = getenv("FR_PDL");
+    return !(e != nullptr && strcmp(e, "0") == 0);
+  }();
+  return on;
+}
+
+// Launches kern<<<grid, block, smem, s>>>(args...) as a programmatic
+// dependent of the previous kernel on s (unless FR_PDL=0).  cluster > 0: a
+// cluster launch of `cluster` CTAs along x (kernels that use cluster
+// barriers, mapa or shared::cluster stores are always launched as clusters,
+// also of one CTA); cluster = 0: an ordinary grid.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                     unsigned cluster, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (pdl_enabled()) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster > 0) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// The same for a kernel held as an untyped pointer with packed arguments.
+inline cudaError_t launch_pdl(const void *kern, dim3 grid, dim3 block, void **args, size_t smem,
+                              cudaStream_t s) {
+  if (!pdl_enabled()) return cudaLaunchKernel(kern, grid, block, args, smem, s);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, kern, args);
 }
 
 }  // namespace fr

@@ -573,6 +573,7 @@ layernorm_cluster_full(const uint16_t *__restrict__ x, const float *__restrict__
                        float *__restrict__ mean_out, float *__restrict__ rstd_out, int64_t rows,
                        int64_t cols, int64_t ldx, int64_t ldy, float eps, int *__restrict__ err) {
   static_assert(A >= R, "a step's rows must be issued during the step before");
+  pdl_enter();
   constexpr int kSlotsR = full_slots(R, A), kAhead = A;
   extern __shared__ __align__(128) unsigned char smem[];  // [kSlotsR] row slices
   __shared__ __align__(8) uint64_t landed[kSlotsR];       // bulk-copy completion per slot
@@ -887,9 +888,14 @@ cudaError_t launch_layernorm_cluster(const uint16_t *x, const float *gamma, cons
   if (clusters < 1) return cudaErrorInvalidConfiguration;
   int64_t ncl = clusters;  // persistent: every cluster that can be resident
   if (ncl > rows) ncl = rows;
-  cfg.gridDim = dim3(static_cast<unsigned>(ncl * C));
-  return cudaLaunchKernelEx(&cfg, kern, x, gamma, beta, y, mean, rstd, rows, cols, ldx, ldy, eps,
-                            err);
+  if (!full) {  // the general kernel: a cluster launch without the programmatic overlap
+    cfg.gridDim = dim3(static_cast<unsigned>(ncl * C));
+    return cudaLaunchKernelEx(&cfg, kern, x, gamma, beta, y, mean, rstd, rows, cols, ldx, ldy,
+                              eps, err);
+  }
+  return launch_k(kern, dim3(static_cast<unsigned>(ncl * C)), dim3(static_cast<unsigned>(T)),
+                  smem, s, static_cast<unsigned>(C), x, gamma, beta, y, mean, rstd, rows, cols, ldx,
+                  ldy, eps, err);
 }
 
 size_t layernorm_ring_smem(int64_t cols, int nbuf) {

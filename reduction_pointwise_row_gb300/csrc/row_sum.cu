@@ -94,6 +94,7 @@ template <class Op, bool VEC, bool LOOP, bool SQRT>
 __global__ void __launch_bounds__(kRowThreads)
 rowsum_warp(const float *__restrict__ a, const float *__restrict__ b, float *__restrict__ out,
             int64_t rows, int64_t cols, int64_t lda, int64_t ldb, Op op) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (kRowThreads / 32) + (threadIdx.x >> 5);
   if (row >= rows) return;
@@ -149,6 +150,7 @@ template <class Op, bool VEC>
 __global__ void __launch_bounds__(kSplitThreads)
 rowsum_split_stage1(const float *__restrict__ a, const float *__restrict__ b, int64_t cols,
                     int64_t lda, int64_t ldb, Op op, double *__restrict__ partials, int S) {
+  pdl_enter();
   const int seg = blockIdx.x;
   const int64_t row = blockIdx.y;
   const int tid = threadIdx.x;
@@ -206,6 +208,7 @@ template <bool SQRT>
 __global__ void __launch_bounds__(kRowThreads)
 rowsum_split_stage2(const double *__restrict__ partials, float *__restrict__ out, int64_t rows,
                     int S) {
+  pdl_enter();  // the partials are stage 1's: read only after it has completed
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (kRowThreads / 32) + (threadIdx.x >> 5);
   if (row >= rows) return;
@@ -222,31 +225,27 @@ unsigned warp_row_grid(int64_t rows) {
 template <class Op, bool LOOP, bool SQRT>
 cudaError_t launch_warp(const float *a, const float *b, float *out, int64_t rows, int64_t cols,
                         int64_t lda, int64_t ldb, Op op, bool vec, cudaStream_t s) {
+  const dim3 grid(warp_row_grid(rows)), block(kRowThreads);
   if (vec)
-    rowsum_warp<Op, true, LOOP, SQRT><<<warp_row_grid(rows), kRowThreads, 0, s>>>(
-        a, b, out, rows, cols, lda, ldb, op);
-  else
-    rowsum_warp<Op, false, LOOP, SQRT><<<warp_row_grid(rows), kRowThreads, 0, s>>>(
-        a, b, out, rows, cols, lda, ldb, op);
-  return cudaGetLastError();
+    return launch_k(rowsum_warp<Op, true, LOOP, SQRT>, grid, block, 0, s, 0, a, b, out, rows, cols,
+                    lda, ldb, op);
+  return launch_k(rowsum_warp<Op, false, LOOP, SQRT>, grid, block, 0, s, 0, a, b, out, rows, cols,
+                  lda, ldb, op);
 }
 
 template <class Op, bool SQRT>
 cudaError_t launch_split(const float *a, const float *b, float *out, int64_t rows, int64_t cols,
                          int64_t lda, int64_t ldb, Op op, bool vec, double *partials,
                          int segments, cudaStream_t s) {
-  dim3 grid(static_cast<unsigned>(segments), static_cast<unsigned>(rows));
-  if (vec)
-    rowsum_split_stage1<Op, true><<<grid, kSplitThreads, 0, s>>>(a, b, cols, lda, ldb, op,
-                                                                partials, segments);
-  else
-    rowsum_split_stage1<Op, false><<<grid, kSplitThreads, 0, s>>>(a, b, cols, lda, ldb, op,
-                                                                 partials, segments);
-  cudaError_t e = cudaGetLastError();
+  const dim3 grid(static_cast<unsigned>(segments), static_cast<unsigned>(rows));
+  cudaError_t e =
+      vec ? launch_k(rowsum_split_stage1<Op, true>, grid, dim3(kSplitThreads), 0, s, 0, a, b, cols,
+                     lda, ldb, op, partials, segments)
+          : launch_k(rowsum_split_stage1<Op, false>, grid, dim3(kSplitThreads), 0, s, 0, a, b,
+                     cols, lda, ldb, op, partials, segments);
   if (e != cudaSuccess) return e;
-  rowsum_split_stage2<SQRT><<<warp_row_grid(rows), kRowThreads, 0, s>>>(partials, out, rows,
-                                                                        segments);
-  return cudaGetLastError();
+  return launch_k(rowsum_split_stage2<SQRT>, dim3(warp_row_grid(rows)), dim3(kRowThreads), 0, s, 0,
+                  partials, out, rows, segments);
 }
 
 }  // namespace

@@ -41,6 +41,7 @@ template <int NV>
 __global__ void __launch_bounds__(kWarpRowThreads, 1)
 softmax_bf16_warp_vec(const uint16_t *__restrict__ x, uint16_t *__restrict__ y, int64_t rows,
                       int64_t cols, int64_t ldx, int64_t ldy) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int64_t row =
       static_cast<int64_t>(blockIdx.x) * (kWarpRowThreads / 32) + (threadIdx.x >> 5);
@@ -272,10 +273,10 @@ cudaError_t launch_softmax_bf16_persistent(const uint16_t *x, uint16_t *y, int64
   if (vec) {
     const int64_t nv = (cols + 32 * kPer - 1) / (32 * kPer);
     switch (nv) {
-      case 1: softmax_bf16_warp_vec<1><<<grid, kWarpRowThreads, 0, s>>>(x, y, rows, cols, ldx, ldy); break;
-      case 2: softmax_bf16_warp_vec<2><<<grid, kWarpRowThreads, 0, s>>>(x, y, rows, cols, ldx, ldy); break;
-      case 3: softmax_bf16_warp_vec<3><<<grid, kWarpRowThreads, 0, s>>>(x, y, rows, cols, ldx, ldy); break;
-      case 4: softmax_bf16_warp_vec<4><<<grid, kWarpRowThreads, 0, s>>>(x, y, rows, cols, ldx, ldy); break;
+      case 1: return launch_k(softmax_bf16_warp_vec<1>, dim3(grid), dim3(kWarpRowThreads), 0, s, 0, x, y, rows, cols, ldx, ldy);
+      case 2: return launch_k(softmax_bf16_warp_vec<2>, dim3(grid), dim3(kWarpRowThreads), 0, s, 0, x, y, rows, cols, ldx, ldy);
+      case 3: return launch_k(softmax_bf16_warp_vec<3>, dim3(grid), dim3(kWarpRowThreads), 0, s, 0, x, y, rows, cols, ldx, ldy);
+      case 4: return launch_k(softmax_bf16_warp_vec<4>, dim3(grid), dim3(kWarpRowThreads), 0, s, 0, x, y, rows, cols, ldx, ldy);
       default: return cudaErrorInvalidValue;
     }
   } else {

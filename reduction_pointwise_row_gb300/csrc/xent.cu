@@ -562,6 +562,7 @@ xent_async(const uint16_t *__restrict__ logits, const int64_t *__restrict__ targ
            float *__restrict__ loss, float *__restrict__ target_logit,
            int64_t *__restrict__ argmax, float *__restrict__ loss_mean, void *__restrict__ ws,
            int64_t rows, int64_t cols, int64_t ld, int64_t ignore_index) {
+  pdl_enter();
   extern __shared__ __align__(128) unsigned char smem[];  // [NS][U][T] x 16 bytes
   __shared__ MD red_md[2][T / 32];
   __shared__ ArgBest red_arg[2][T / 32];
@@ -993,7 +994,7 @@ cudaError_t launch_xent_config(const XentConfig &cfg, const uint16_t *logits,
   int64_t *no_argmax = nullptr;
   void *args[] = {&logits, &target, &loss, &target_logit, &no_argmax, &loss_mean, &workspace,
                   &rows, &cols, &ld, &ignore_index};
-  return cudaLaunchKernel(a->kern, dim3(static_cast<unsigned>(grid)), dim3(a->T), args, smem, s);
+  return launch_pdl(a->kern, dim3(static_cast<unsigned>(grid)), dim3(a->T), args, smem, s);
 }
 
 bool xent_recorded_config(int device, int64_t rows, int64_t cols, int64_t ld, XentConfig *out) {
@@ -1048,7 +1049,7 @@ cudaError_t launch_xent_argmax_default(const uint16_t *logits, const int64_t *ta
   }
   void *args[] = {&logits, &target, &loss, &target_logit, &argmax, &loss_mean, &workspace,
                   &rows, &cols, &ld, &ignore_index};
-  return cudaLaunchKernel(kern, dim3(static_cast<unsigned>(grid)), dim3(T), args, smem, s);
+  return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(T), args, smem, s);
 }
 
 cudaError_t launch_xent(const uint16_t *logits, const int64_t *target, float *loss,
