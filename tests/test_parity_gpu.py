@@ -248,9 +248,10 @@ def test_layernorm_forms(o, rows, cols, offset):
         assert e.value.status == 3
 
 
+@pytest.mark.parametrize("cta", ["256", "512", "128"])
 @pytest.mark.parametrize("variant", ["r1a2", "r1a1", "r1a3", "r1a4", "r1a5", "r2a2", "classic"])
 @pytest.mark.parametrize("cols", [16384, 32768])
-def test_layernorm_cluster_variants(o, variant, cols):
+def test_layernorm_cluster_variants(o, variant, cols, cta):
     """The cluster kernels where every thread holds 32 columns (one CTA per
     16384 columns), every ring depth and rows per step, on row counts that
     leave clusters with different numbers of rows (and with none), plus a
@@ -265,12 +266,14 @@ def test_layernorm_cluster_variants(o, variant, cols):
         eps = float(np.float32(w.params["eps"]))
         ry, rm, rr = o.layernorm(x, w.arrays["gamma"], w.arrays["beta"], eps)
         os.environ["FR_LAYERNORM_CLUSTER"] = variant
+        os.environ["FR_LAYERNORM_CTA"] = cta  # largest CTA of the equal-count kernel
         try:
             y, m, r = run_layernorm(x, w.arrays["gamma"], w.arrays["beta"], eps, "looped",
                                     kernel="cluster")
         finally:
             os.environ.pop("FR_LAYERNORM_CLUSTER", None)
-        what = f"{variant} {rows}x{cols}"
+            os.environ.pop("FR_LAYERNORM_CTA", None)
+        what = f"{variant}/{cta} {rows}x{cols}"
         assert_close(y, ry, "bf16", f"{what} y")
         assert_close(m, rm, "mean", f"{what} mean")
         assert_close(r, rr, "f32", f"{what} rstd")
