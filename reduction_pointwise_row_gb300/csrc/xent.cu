@@ -976,6 +976,36 @@ cudaError_t xent_config_check(const XentConfig &cfg, int max_smem_optin) {
   return per_sm >= cfg.ctas_per_sm ? cudaSuccess : cudaErrorInvalidConfiguration;
 }
 
+// Dynamic shared memory for a launch that must keep at most `per_sm` CTAs on
+// an SM: the kernel's own need, raised so that per_sm + 1 CTAs (each with the
+// runtime's reserved shared memory) no longer fit.  The grid is per_sm CTAs
+// per SM; without the cap the CTAs of a launch that overlaps the previous one
+// (a programmatic dependent, or any concurrent kernel) fill the spare slot of
+// the SMs that free up first and pile up there.  FR_XENT_PAD=0 launches with
+// the kernel's own need only.
+cudaError_t capped_smem(size_t need, int per_sm, size_t *out) {
+  *out = need;
+  if (const char *e = getenv("FR_XENT_PAD"); e != nullptr && e[0] == '0') return cudaSuccess;
+  int dev = 0, per_sm_smem = 0, reserved = 0, max_smem_optin = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                  dev)) != cudaSuccess)
+    return e;
+  if ((e = cudaDeviceGetAttribute(&per_sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                                  dev)) != cudaSuccess)
+    return e;
+  if ((e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) !=
+      cudaSuccess)
+    return e;
+  // (per_sm + 1) * (pad + reserved) > per_sm_smem
+  const int64_t pad = per_sm_smem / (per_sm + 1) - reserved + 1;
+  if (pad > static_cast<int64_t>(need) && pad <= max_smem_optin &&
+      static_cast<int64_t>(per_sm) * (pad + reserved) <= per_sm_smem)
+    *out = static_cast<size_t>(pad);
+  return cudaSuccess;
+}
+
 cudaError_t launch_xent_config(const XentConfig &cfg, const uint16_t *logits,
                                const int64_t *target, float *loss, float *loss_mean,
                                float *target_logit, int64_t rows, int64_t cols, int64_t ld,
@@ -984,7 +1014,12 @@ cudaError_t launch_xent_config(const XentConfig &cfg, const uint16_t *logits,
   cudaError_t e = xent_config_check(cfg, max_smem_optin);
   if (e != cudaSuccess) return e;
   const AsyncEntry *a = async_entry(cfg);
-  const size_t smem = static_cast<size_t>(a->NS) * a->U * a->T * 16;
+  size_t smem = 0;
+  e = capped_smem(static_cast<size_t>(a->NS) * a->U * a->T * 16, cfg.ctas_per_sm, &smem);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(a->kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(smem))) != cudaSuccess)
+    return e;
   int64_t grid = static_cast<int64_t>(sm_count) * cfg.ctas_per_sm;
   if (grid > rows) grid = rows;
   if (loss_mean != nullptr) {
@@ -1041,6 +1076,11 @@ cudaError_t launch_xent_argmax_default(const uint16_t *logits, const int64_t *ta
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   if (per_sm > d.ctas_per_sm) per_sm = d.ctas_per_sm;
+  size_t smem_cap = 0;
+  if ((e = capped_smem(smem, per_sm, &smem_cap)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(smem_cap))) != cudaSuccess)
+    return e;
   int64_t grid = static_cast<int64_t>(sm_count) * per_sm;
   if (grid > rows) grid = rows;
   if (loss_mean != nullptr) {
@@ -1049,7 +1089,7 @@ cudaError_t launch_xent_argmax_default(const uint16_t *logits, const int64_t *ta
   }
   void *args[] = {&logits, &target, &loss, &target_logit, &argmax, &loss_mean, &workspace,
                   &rows, &cols, &ld, &ignore_index};
-  return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(T), args, smem, s);
+  return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(T), args, smem_cap, s);
 }
 
 cudaError_t launch_xent(const uint16_t *logits, const int64_t *target, float *loss,
