@@ -172,22 +172,28 @@ fr_status fr_softmax(const void *x, void *y, int64_t rows, int64_t cols, int64_t
                      int64_t ldy, fr_dtype dtype, fr_form form, fr_stream_t stream);
 
 /*
- * fr_softmax over rows held in HOST memory: the rows go to the device in
- * chunks of `chunk_rows`, through three device staging slots each way (the
- * caller's workspace), and come back the same way, with a chunk's copy in,
- * the previous chunk's kernel and the copy out of the one before running at
- * the same time on the library's own streams (created once per device).  The
- * results are those of fr_softmax on the same rows.  The call returns without
- * synchronising; `stream` resumes after the last copy out, and work queued on
- * `stream` before the call runs first.  The pages have no counterpart: this
- * is the end-to-end path from host memory.
+ * fr_softmax over rows held in HOST memory, in one of two ways.
+ *   direct (chunk_rows = 0): the softmax kernel itself reads x_host and writes
+ *     y_host where they are, over the host link (NVLink-C2C on GB300, which
+ *     keeps the GPU coherent with host memory); no staging, no workspace.
+ *   staged (chunk_rows >= 1): the rows go to the device in chunks of
+ *     `chunk_rows`, through three device staging slots each way (the caller's
+ *     workspace), and come back the same way, with a chunk's copy in, the
+ *     previous chunk's kernel and the copy out of the one before running at
+ *     the same time on the library's own streams (created once per device).
+ * The results are those of fr_softmax on the same rows.  The call returns
+ * without synchronising; `stream` resumes after the last write of y_host,
+ * and work queued on `stream` before the call runs first.  The pages have no
+ * counterpart: this is the end-to-end path from host memory.  Measured on
+ * GB300 with fp32 [32768, 1024]: direct 900 us, staged (4096-row chunks) 950.
  *
  *   x_host, y_host  [rows, cols] contiguous, of `dtype`, in page-locked host
  *                   memory (cudaHostAlloc or cudaHostRegister); anything else
  *                   is FR_ERR_INVALID_ARG.  They may be the same buffer.
- *   chunk_rows      rows per chunk, >= 1
- *   workspace       device memory of fr_softmax_host_workspace(...) bytes,
- *                   256-byte aligned; one call at a time may use it
+ *   chunk_rows      0 (direct) or rows per chunk (staged)
+ *   workspace       staged: device memory of fr_softmax_host_workspace(...)
+ *                   bytes, 256-byte aligned, one call at a time may use it;
+ *                   direct: ignored (may be NULL)
  *   dtype           FR_F32 or FR_BF16
  * Arguments are checked before anything is enqueued; a CUDA error while the
  * chunks are being enqueued (FR_ERR_CUDA) may leave part of the work queued.

@@ -209,10 +209,13 @@ def fr_softmax(x, form: str = "auto", out=None, stream=None):
 
 def fr_softmax_host(x_host, out=None, chunk_rows: int | None = None, workspace=None,
                     stream=None, device=None):
-    """Row softmax of a page-locked host tensor (fp32 or bf16) through the
-    library's chunked copy-in / kernel / copy-out pipeline; ``out`` (page-locked,
-    same shape and dtype) receives y.  Returns ``out``.  Ordered on ``stream``
-    (default: the current stream of ``device``) without synchronising."""
+    """Row softmax of a page-locked host tensor (fp32 or bf16); ``out``
+    (page-locked, same shape and dtype) receives y.  ``chunk_rows`` None or 0:
+    the kernel reads and writes the host rows directly over the host link;
+    ``chunk_rows`` >= 1: the library's chunked copy-in / kernel / copy-out
+    pipeline through a device workspace.  Returns ``out``.  Ordered on
+    ``stream`` (default: the current stream of ``device``) without
+    synchronising."""
     import torch
     assert not x_host.is_cuda and x_host.dtype in (torch.float32, torch.bfloat16)
     assert x_host.dim() == 2 and x_host.is_contiguous()
@@ -221,15 +224,15 @@ def fr_softmax_host(x_host, out=None, chunk_rows: int | None = None, workspace=N
         out = torch.empty_like(x_host).pin_memory()
     assert out.shape == x_host.shape and out.dtype == x_host.dtype and out.is_contiguous()
     dt = DTYPES["f32"] if x_host.dtype == torch.float32 else DTYPES["bf16"]
-    if chunk_rows is None:  # about 16 MiB of input per chunk
-        chunk_rows = max(1, min(rows, (16 << 20) // (cols * x_host.element_size())))
-    n = lib().fr_softmax_host_workspace(cols, dt, min(chunk_rows, rows))
-    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
-    if workspace is None:
+    if chunk_rows is None:
+        chunk_rows = 0
+    if chunk_rows > 0 and workspace is None:
+        n = lib().fr_softmax_host_workspace(cols, dt, min(chunk_rows, rows))
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
         workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+    nws = 0 if workspace is None else workspace.numel()
     _check(lib().fr_softmax_host(_ptr(x_host), _ptr(out), rows, cols, dt, chunk_rows,
-                                 _ptr(workspace), workspace.numel(), _stream(stream)),
-           "fr_softmax_host")
+                                 _ptr(workspace), nws, _stream(stream)), "fr_softmax_host")
     return out
 
 

@@ -285,20 +285,23 @@ fr_status fr_softmax(const void *x, void *y, int64_t rows, int64_t cols, int64_t
 }
 
 size_t fr_softmax_host_workspace(int64_t cols, fr_dtype dtype, int64_t chunk_rows) {
-  if (cols < 1 || chunk_rows < 1 || (dtype != FR_F32 && dtype != FR_BF16)) return 0;
+  if (cols < 1 || chunk_rows < 1 || (dtype != FR_F32 && dtype != FR_BF16)) return 0;  // 0: direct
   const int64_t es = dtype == FR_F32 ? 4 : 2;
   return fr::host_pipeline_workspace(cols, es, es, chunk_rows);
 }
 
 namespace {
-bool page_locked(const void *p) {
+// The address at which the current device reaches page-locked host memory p
+// (p itself under unified addressing), or nullptr when p is not page-locked.
+void *host_device_ptr(const void *p) {
   cudaPointerAttributes a{};
   if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
     cudaGetLastError();
-    return false;
+    return nullptr;
   }
-  return a.type == cudaMemoryTypeHost;
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
 }
+bool page_locked(const void *p) { return host_device_ptr(p) != nullptr; }
 }  // namespace
 
 fr_status fr_softmax_host(const void *x_host, void *y_host, int64_t rows, int64_t cols,
@@ -306,12 +309,15 @@ fr_status fr_softmax_host(const void *x_host, void *y_host, int64_t rows, int64_
                           size_t workspace_bytes, fr_stream_t stream) {
   if (dtype != FR_F32 && dtype != FR_BF16) return FR_ERR_UNSUPPORTED_DTYPE;
   const int64_t es = dtype == FR_F32 ? 4 : 2;
-  if (!x_host || !y_host || chunk_rows < 1) return FR_ERR_INVALID_ARG;
+  if (!x_host || !y_host || chunk_rows < 0) return FR_ERR_INVALID_ARG;
   if (!shape_ok(rows, cols, cols, es)) return FR_ERR_INVALID_ARG;
   if (!aligned(x_host, es) || !aligned(y_host, es)) return FR_ERR_MISALIGNED;
   fr::DevInfo info;
   if (fr_status st = device_ok(&info)) return st;
   if (!page_locked(x_host) || !page_locked(y_host)) return FR_ERR_INVALID_ARG;
+  if (chunk_rows == 0)  // direct: the kernel reads and writes host memory over the host link
+    return fr_softmax(host_device_ptr(x_host), host_device_ptr(y_host), rows, cols, cols, cols,
+                      dtype, FR_FORM_AUTO, stream);
   if (chunk_rows > rows) chunk_rows = rows;
   if (!workspace || workspace_bytes < fr::host_pipeline_workspace(cols, es, es, chunk_rows))
     return FR_ERR_WORKSPACE_TOO_SMALL;

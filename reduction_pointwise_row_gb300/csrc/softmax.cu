@@ -339,7 +339,7 @@ __device__ __forceinline__ MD block_md(MD st, MD *smem) {
   return r;
 }
 
-template <bool VEC, int T, int U>
+template <bool VEC, int T, int U, bool PF>
 __global__ void __launch_bounds__(T)
 softmax_block_looped(const float *__restrict__ x, float *__restrict__ y, int64_t rows,
                      int64_t cols, int64_t ldx, int64_t ldy) {
@@ -352,15 +352,30 @@ softmax_block_looped(const float *__restrict__ x, float *__restrict__ y, int64_t
     const RowSplit sp = VEC ? row_split(px, cols, 4) : RowSplit{0, 0, static_cast<int>(0)};
     MD st{-INFINITY, 0.0f};
     if constexpr (VEC) {
+      // PF: chunk base + T*U is loaded while chunk base is reduced (two
+      // register buffers), so a thread always has a chunk of loads in flight.
+      // Loads keep the row in L2 for pass 2.
       const float *vx = px + sp.head;
+      V8 nx[U];
+      if constexpr (PF) {
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (tid + T * u < sp.nvec) nx[u] = ld_keep_v8(vx + (tid + T * u) * 8);
+      }
       for (int64_t base = 0; base < sp.nvec; base += T * U) {
         V8 v[U];
+        const int64_t lb = PF ? base + T * U : base;  // the chunk loaded now
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          if constexpr (PF) v[u] = nx[u];
+          const int64_t vi = lb + tid + T * u;
+          if (vi < sp.nvec) (PF ? nx[u] : v[u]) = ld_keep_v8(vx + vi * 8);
+        }
         float cm = -INFINITY;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int64_t vi = base + tid + T * u;
           if (vi < sp.nvec) {
-            v[u] = ld_keep_v8(vx + vi * 8);  // pass 2 re-reads it from L2
 #pragma unroll
             for (int j = 0; j < 8; ++j) cm = max_nan(cm, fbits(v[u].w[j]));
           }
@@ -403,12 +418,20 @@ softmax_block_looped(const float *__restrict__ x, float *__restrict__ y, int64_t
     if constexpr (VEC) {
       const float *vx = px + sp.head;
       float *vy = py + sp.head;
+      V8 nx[U];
+      if constexpr (PF) {
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (tid + T * u < sp.nvec) nx[u] = ld_stream_v8(vx + (tid + T * u) * 8);
+      }
       for (int64_t base = 0; base < sp.nvec; base += T * U) {
         V8 v[U];
+        const int64_t lb = PF ? base + T * U : base;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-          const int64_t vi = base + tid + T * u;
-          if (vi < sp.nvec) v[u] = ld_stream_v8(vx + vi * 8);
+          if constexpr (PF) v[u] = nx[u];
+          const int64_t vi = lb + tid + T * u;
+          if (vi < sp.nvec) (PF ? nx[u] : v[u]) = ld_stream_v8(vx + vi * 8);
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -614,6 +637,18 @@ cudaError_t launch_softmax_async(const float *x, float *y, int64_t rows, int64_t
 namespace {
 bool cluster_shape(int64_t cols, int *T, int *C) {
   const int64_t nvec = cols / 8;  // at least the body's vectors
+  // FR_SOFTMAX_CLUSTER=<threads>x<ctas> pins a shape that holds the row.
+  if (const char *e = getenv("FR_SOFTMAX_CLUSTER"); e != nullptr) {
+    const int t = atoi(e);
+    const char *xp = strchr(e, 'x');
+    const int c = xp != nullptr ? atoi(xp + 1) : 0;
+    if ((t == 256 || t == 512 || t == 1024) && (c == 2 || c == 4 || c == 8) && c <= kSmClusterMax &&
+        nvec <= static_cast<int64_t>(c) * t * 4) {
+      *T = t;
+      *C = c;
+      return true;
+    }
+  }
   for (int t = 256; t <= 1024; t <<= 1)
     for (int c = 2; c <= kSmClusterMax; c <<= 1)
       if (nvec <= static_cast<int64_t>(c) * t * 4) {
@@ -649,10 +684,10 @@ cudaError_t launch_softmax_split(const float *x, float *y, int64_t rows, int64_t
 }
 
 namespace {
-template <int T, int U>
+template <int T, int U, bool PF>
 cudaError_t launch_looped_t(const float *x, float *y, int64_t rows, int64_t cols, int64_t ldx,
                             int64_t ldy, bool vec, int sm_count, int per_sm_cap, cudaStream_t s) {
-  auto kern = vec ? softmax_block_looped<true, T, U> : softmax_block_looped<false, T, U>;
+  auto kern = vec ? softmax_block_looped<true, T, U, PF> : softmax_block_looped<false, T, U, PF>;
   int per_sm = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, T, 0);
   if (e != cudaSuccess) return e;
@@ -669,15 +704,18 @@ cudaError_t launch_softmax_looped(const float *x, float *y, int64_t rows, int64_
                                   int64_t ldx, int64_t ldy, bool vec, int sm_count,
                                   cudaStream_t s) {
   // Many rows: 256-thread CTAs, as many per SM as fit (more rows in flight);
-  // few rows: 512 threads, two per SM.  Measured on GB300: fp32 [8190, 4097]
-  // 48.8 us with 256 threads against 80.3 with 512 and 53.3 with 128;
-  // [511, 65537] 55.1 us with 512 against 63.9 with 256.  FR_SOFTMAX_LOOP=
-  // 128|256|512 pins the CTA size.
+  // few rows: 512 threads, two per SM, each thread loading its next chunk
+  // while it reduces the current one.  Measured on GB300: fp32 [8190, 4097]
+  // 48.8 us with 256 threads against 80.3 with 512 and 53.3 with 128 (56.7
+  // with 256 and the next chunk in flight: 64 registers instead of 48 leave
+  // room for four CTAs per SM instead of five); [511, 65537] 53.8 us with 512
+  // and the next chunk in flight, 55.1 without, 63.9 with 256.
+  // FR_SOFTMAX_LOOP=128|256|512 pins the CTA size.
   const char *e = getenv("FR_SOFTMAX_LOOP");
   const int t = e != nullptr ? atoi(e) : rows >= 4 * static_cast<int64_t>(sm_count) ? 256 : 512;
-  if (t == 128) return launch_looped_t<128, 4>(x, y, rows, cols, ldx, ldy, vec, sm_count, 16, s);
-  if (t == 256) return launch_looped_t<256, 2>(x, y, rows, cols, ldx, ldy, vec, sm_count, 16, s);
-  return launch_looped_t<512, 2>(x, y, rows, cols, ldx, ldy, vec, sm_count, 2, s);
+  if (t == 128) return launch_looped_t<128, 4, false>(x, y, rows, cols, ldx, ldy, vec, sm_count, 16, s);
+  if (t == 256) return launch_looped_t<256, 2, false>(x, y, rows, cols, ldx, ldy, vec, sm_count, 16, s);
+  return launch_looped_t<512, 2, true>(x, y, rows, cols, ldx, ldy, vec, sm_count, 2, s);
 }
 
 }  // namespace fr
