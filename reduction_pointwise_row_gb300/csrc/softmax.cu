@@ -635,6 +635,9 @@ cudaError_t launch_softmax_async(const float *x, float *y, int64_t rows, int64_t
 // smallest T in {256, 512, 1024} whose C-fold (C <= 8) holds the row's body;
 // 0 when no cluster holds it.
 namespace {
+// The smallest CTA size, then the smallest cluster, whose registers hold the
+// row (4 vectors of 8 per thread).  Measured on GB300, fp32 [511, 65537]:
+// 8 CTAs of 256 threads 45.1 us, 4 of 512 48.2, 2 of 1024 56.5.
 bool cluster_shape(int64_t cols, int *T, int *C) {
   const int64_t nvec = cols / 8;  // at least the body's vectors
   // FR_SOFTMAX_CLUSTER=<threads>x<ctas> pins a shape that holds the row.
