@@ -248,12 +248,33 @@ fr_status fr_layernorm(const void *x, const float *gamma, const float *beta, voi
  *   dtype        FR_BF16
  *   workspace    fr_workspace_size(FR_OP_XENT, ...) bytes when loss_mean is
  *                requested (per-CTA partial sums and a ticket; the library
- *                zeroes the ticket on the stream before each launch)
+ *                zeroes the ticket on the stream before each launch).  After
+ *                the call it holds the mean's parts at FR_XENT_PARTS_OFFSET.
  */
 fr_status fr_xent(const void *logits, const int64_t *target, float *loss, float *loss_mean,
                   float *target_logit, int64_t *argmax, int64_t rows, int64_t cols,
                   int64_t ld, int64_t ignore_index, fr_dtype dtype, fr_form form,
                   void *workspace, size_t workspace_bytes, fr_stream_t stream);
+
+/*
+ * The mean over a batch whose rows are sharded across ranks (one process per
+ * GPU, each calling fr_xent on its own rows with loss_mean requested).  Each
+ * call leaves two fp64 values in its workspace at byte FR_XENT_PARTS_OFFSET:
+ * the sum of the losses it averaged and the number of rows it averaged (those
+ * whose target is not ignore_index).  The ranks add their pairs element-wise
+ * (an all-reduce with sum, e.g. NCCL over the 16 bytes in place), then each
+ * calls fr_xent_mean_from_parts, which writes sum / count rounded to fp32
+ * (NaN when no row of the batch counts) -- the mean fr_xent gives on the
+ * whole batch, up to the order of the fp64 additions.  This is the path's one
+ * exchange step; every other step of every op is independent per row.
+ *
+ *   workspace    the workspace of the rank's fr_xent call, parts summed over
+ *                the ranks; read only
+ *   loss_mean    fp32 [1] device output
+ * One single-thread kernel on `stream`.
+ */
+#define FR_XENT_PARTS_OFFSET 16
+fr_status fr_xent_mean_from_parts(const void *workspace, float *loss_mean, fr_stream_t stream);
 
 /* ---- launch configurations ----------------------------------------------
  *

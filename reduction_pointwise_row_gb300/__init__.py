@@ -60,6 +60,7 @@ SIGNATURES = {
                             _int, _vp]),
     "fr_xent": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _int, _vp,
                        _sz, _vp]),
+    "fr_xent_mean_from_parts": (_int, [_vp, _vp, _vp]),
     "fr_check_device_error": (_int, [_vp, ctypes.POINTER(ctypes.c_int32)]),
     "fr_coordinate_descent": (_int, [ctypes.c_int32, _vp, _vp, _vp, ctypes.c_double, _vp, _vp,
                                      _vp, _vp]),
@@ -256,13 +257,54 @@ def fr_layernorm(x, gamma, beta, eps: float = 1e-5, form: str = "auto", out=None
     return out, mean, rstd
 
 
+XENT_PARTS_OFFSET = 16  # FR_XENT_PARTS_OFFSET
+
+
+def xent_mean_parts(workspace):
+    """The two fp64 values an fr_xent call with the mean leaves in its
+    workspace -- the sum of the losses it averaged and the number of rows it
+    averaged -- as a view that an all-reduce can sum in place."""
+    return workspace[XENT_PARTS_OFFSET:XENT_PARTS_OFFSET + 16].view(_torch().float64)
+
+
+def allreduce_mean_parts(parts, group=None):
+    """Sum mean parts element-wise over the ranks of ``group``
+    (torch.distributed, in place): the path's one exchange step."""
+    import torch.distributed as dist
+    dist.all_reduce(parts, op=dist.ReduceOp.SUM, group=group)
+    return parts
+
+
+def fr_xent_mean_from_parts(workspace, mean=None, stream=None):
+    """mean = sum / count from the (summed) parts in an fr_xent workspace."""
+    import torch
+    if mean is None:
+        mean = torch.empty(1, dtype=torch.float32, device=workspace.device)
+    _check(lib().fr_xent_mean_from_parts(_ptr(workspace), _ptr(mean), _stream(stream)),
+           "fr_xent_mean_from_parts")
+    return mean
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _nullcontext():
+    import contextlib
+    return contextlib.nullcontext()
+
+
 def fr_xent(logits, target, ignore_index: int = -100, want_loss: bool = True,
             want_mean: bool = True, want_target_logit: bool = False, want_argmax: bool = False,
-            form: str = "auto", workspace=None, stream=None):
+            form: str = "auto", workspace=None, stream=None, group=None):
     """Cross entropy of bf16 logits rows against int64 targets.
 
     Returns a dict with the requested outputs: ``loss`` [rows], ``mean`` [1],
-    ``target_logit`` [rows], ``argmax`` [rows] (int64).
+    ``target_logit`` [rows], ``argmax`` [rows] (int64).  With ``group`` (a
+    torch.distributed group whose ranks each pass their own rows of one
+    batch), ``mean`` is the mean over the whole batch: the ranks' mean parts
+    are all-reduced between this rank's kernel and the finishing kernel.
     """
     import torch
     assert logits.is_cuda and logits.dtype == torch.bfloat16 and logits.dim() == 2
@@ -281,6 +323,10 @@ def fr_xent(logits, target, ignore_index: int = -100, want_loss: bool = True,
     _check(lib().fr_xent(_ptr(logits), _ptr(target), _ptr(loss), _ptr(mean), _ptr(tl), _ptr(am),
                          rows, cols, _ld(logits), ignore_index, DTYPES["bf16"], FORMS[form],
                          _ptr(ws), nws, _stream(stream)), "fr_xent")
+    if group is not None and want_mean:
+        with torch.cuda.stream(stream) if stream is not None else _nullcontext():
+            allreduce_mean_parts(xent_mean_parts(ws), group)
+            fr_xent_mean_from_parts(ws, mean, stream)
     for k, v in (("loss", loss), ("mean", mean), ("target_logit", tl), ("argmax", am)):
         if v is not None:
             res[k] = v

@@ -410,6 +410,17 @@ fr_status fr_xent(const void *logits, const int64_t *target, float *loss, float 
                   FR_FORM_LOOPED);
 }
 
+fr_status fr_xent_mean_from_parts(const void *workspace, float *loss_mean, fr_stream_t stream) {
+  if (!workspace || !loss_mean) return FR_ERR_INVALID_ARG;
+  if (!aligned(workspace, 16) || !aligned(loss_mean, 4)) return FR_ERR_MISALIGNED;
+  fr::DevInfo info;
+  if (fr_status st = device_ok(&info)) return st;
+  return fr::launch_xent_mean_from_parts(workspace, loss_mean,
+                                         reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FR_OK
+             : FR_ERR_CUDA;
+}
+
 namespace {
 
 fr::XentConfig from_c(const fr_xent_config &c) {

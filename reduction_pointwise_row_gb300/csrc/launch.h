@@ -162,6 +162,7 @@ cudaError_t launch_xent_config(const XentConfig &cfg, const uint16_t *logits,
                                int max_smem_optin, cudaStream_t s);
 
 size_t xent_workspace(int64_t rows, int sm_count);
+cudaError_t launch_xent_mean_from_parts(const void *workspace, float *loss_mean, cudaStream_t s);
 cudaError_t launch_xent(const uint16_t *logits, const int64_t *target, float *loss,
                         float *loss_mean, float *target_logit, int64_t *argmax, int64_t rows,
                         int64_t cols, int64_t ld, int64_t ignore_index, void *workspace,

@@ -64,8 +64,16 @@ __device__ __forceinline__ MD fold_chunk(MD st, float cm) {
   return st;
 }
 
+// Workspace layout: the ticket (bytes 0..3), the batch's mean parts at
+// FR_XENT_PARTS_OFFSET (fp64 sum of the averaged losses, fp64 count of the
+// rows averaged), then one fp64 partial sum and one count per CTA.
+constexpr size_t kPartsOffset = FR_XENT_PARTS_OFFSET;
+constexpr size_t kCtaOffset = kPartsOffset + 16;
+static_assert(kPartsOffset % 8 == 0 && kPartsOffset >= 4, "parts after the ticket, fp64 aligned");
+
 struct Workspace {
   unsigned int *ticket;  // zeroed on the stream before each launch
+  double *parts;         // [2]: sum of the averaged losses, rows averaged
   double *sums;          // [grid]
   long long *counts;     // [grid]
 };
@@ -74,8 +82,9 @@ __device__ __forceinline__ Workspace carve(void *ws, int grid) {
   char *p = static_cast<char *>(ws);
   Workspace w;
   w.ticket = reinterpret_cast<unsigned int *>(p);
-  w.sums = reinterpret_cast<double *>(p + 16);
-  w.counts = reinterpret_cast<long long *>(p + 16 + 8 * static_cast<size_t>(grid));
+  w.parts = reinterpret_cast<double *>(p + kPartsOffset);
+  w.sums = reinterpret_cast<double *>(p + kCtaOffset);
+  w.counts = reinterpret_cast<long long *>(p + kCtaOffset + 8 * static_cast<size_t>(grid));
   return w;
 }
 
@@ -127,6 +136,8 @@ __device__ __forceinline__ void finish_mean(void *ws, float *loss_mean, double c
       S += red_s[i];
       n += red_c[i];
     }
+    w.parts[0] = S;
+    w.parts[1] = static_cast<double>(n);
     *loss_mean = static_cast<float>(S / static_cast<double>(n));
     *w.ticket = 0u;
   }
@@ -805,11 +816,12 @@ int xent_grid(int64_t rows, int sm_count, bool argmax) {
 }  // namespace
 
 size_t xent_workspace(int64_t rows, int sm_count) {
-  // A ticket, then one fp64 sum and one count per CTA of the largest grid.
+  // A ticket, the mean's parts, then one fp64 sum and one count per CTA of
+  // the largest grid.
   int64_t g = static_cast<int64_t>(sm_count) * kMaxCtasPerSm;
   if (g > rows) g = rows;
   if (g < 1) g = 1;
-  return 16 + 16 * static_cast<size_t>(g);
+  return kCtaOffset + 16 * static_cast<size_t>(g);
 }
 
 // The staged kernel, pinned with FR_XENT_VARIANT=staged, when its two row
@@ -1127,6 +1139,21 @@ cudaError_t launch_xent(const uint16_t *logits, const int64_t *target, float *lo
                   &rows, &cols, &ld, &ignore_index};
   return cudaLaunchKernel(argmax != nullptr ? v.kern_arg : v.kern, dim3(grid), dim3(v.threads),
                           args, 0, s);
+}
+
+// The mean from parts that ranks holding shards of one batch have summed
+// (an all-reduce of the two fp64 values each call leaves in its workspace).
+__global__ void xent_mean_from_parts_kernel(const double *__restrict__ parts,
+                                            float *__restrict__ loss_mean) {
+  pdl_enter();
+  *loss_mean = static_cast<float>(parts[0] / parts[1]);
+}
+
+cudaError_t launch_xent_mean_from_parts(const void *workspace, float *loss_mean,
+                                        cudaStream_t s) {
+  const double *parts = reinterpret_cast<const double *>(
+      static_cast<const unsigned char *>(workspace) + kPartsOffset);
+  return launch_k(xent_mean_from_parts_kernel, dim3(1), dim3(1), 0, s, 0, parts, loss_mean);
 }
 
 cudaError_t device_error_word(int **out) {

@@ -1,9 +1,10 @@
 """The N > 1 path on the CPU (gloo, two ranks): each rank holds its shard of
 the rows, the shards together are exactly the global workload, results
-gathered from the ranks equal the oracle on the whole batch, and the bench's
+gathered from the ranks equal the oracle on the whole batch, the cross
+entropy's batch mean comes from the ranks' mean parts summed by the
+binding's all-reduce (the path's one exchange step), and the bench's
 max-over-ranks timing reduction gives every rank the slowest rank's time.
-Rows are independent, so no rank exchanges data on the path itself; the only
-collectives are the bench's barrier and timing reduction."""
+Every other step is independent per row."""
 import os
 import socket
 import sys
@@ -28,6 +29,7 @@ def _rank_main(rank: int, world: int, port: int, out_dir: str):
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     import bench
     import oracle
+    import reduction_pointwise_row_gb300 as fr
     from synth import workloads
 
     dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
@@ -43,6 +45,15 @@ def _rank_main(rank: int, world: int, port: int, out_dir: str):
                 local = o.softmax(w.arrays["x"])
             elif cfg == 4:
                 local = o.xent(w.arrays["logits"], w.arrays["target"], -100)["loss"]
+                # the exchange step: this rank's mean parts, laid out as an
+                # fr_xent workspace holds them, summed over the ranks in place
+                counted = w.arrays["target"] != -100
+                ws = torch.zeros(fr.XENT_PARTS_OFFSET + 16 + 64, dtype=torch.uint8)
+                parts = fr.xent_mean_parts(ws)
+                parts[0] = float(np.sum(local[counted].astype(np.float64)))
+                parts[1] = float(np.count_nonzero(counted))
+                fr.allreduce_mean_parts(parts)
+                results["mean"] = np.array([parts[0].item() / parts[1].item()])
             else:
                 local = o.layernorm(w.arrays["x"], w.arrays["gamma"], w.arrays["beta"],
                                     float(np.float32(1e-5)))[0]
@@ -75,6 +86,8 @@ def test_two_gloo_ranks_shard_rows_and_reduce_timing(tmp_path):
     whole = workloads.make(4, rows=60, cols=5000)
     ref = o.xent(whole.arrays["logits"], whole.arrays["target"], -100)
     assert (got["4"] == ref["loss"]).all()
+    # the batch mean from the ranks' summed parts is the oracle's mean over the batch
+    assert abs(float(got["mean"][0]) - float(ref["mean"])) <= 1e-6 * abs(float(ref["mean"]))
     assert int((whole.arrays["target"] == -100).sum()) == 3  # 5 % of the global batch
     whole = workloads.make(2, rows=24, cols=512)
     assert (got["2"] == o.layernorm(whole.arrays["x"], whole.arrays["gamma"],
