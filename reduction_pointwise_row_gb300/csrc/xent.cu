@@ -10,12 +10,15 @@
 // error word (no trap).
 //
 // Rows need not be aligned (a row of 50257 bf16 is 100514 bytes): each row is
-// split into a head of scalars up to the first 32-byte boundary, a body of
-// 32-byte vectors and a tail of scalars; the masked lanes of the body never
-// exist, so no -inf fill is needed except for the empty chunk.
+// split into a head of scalars up to the first 16-byte boundary, an interior
+// of 16-byte vectors streamed through a per-thread cp.async ring, and a tail
+// of scalars; vectors past the interior's end are filled with -inf (adding
+// nothing to l).
 //
-// The grid is persistent (a fixed number of CTAs per SM, rows strided over
-// CTAs).  The mean over counted rows is deterministic: each CTA adds its rows'
+// The launch configuration (threads, vectors per ring item, ring stages,
+// CTAs per SM) is a point of a box searched by measurement ("Stax (4)",
+// section 9.6); the default is the fastest point on GB300.  The grid is
+// persistent (CTAs per SM x SMs, rows strided over CTAs).  The mean over counted rows is deterministic: each CTA adds its rows'
 // losses in row order into an fp64 partial, writes it to the workspace, and
 // the last CTA to finish (an atomic ticket; nobody waits) adds the partials in
 // a fixed order.
@@ -34,8 +37,6 @@ __device__ int g_fr_device_error;
 
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kCtasPerSm = 2;
 constexpr int kMaxCtasPerSm = 16;  // largest persistent grid: 16 CTAs per SM (workspace bound)
 
 struct ArgBest {
@@ -143,203 +144,6 @@ __device__ __forceinline__ void finish_mean(void *ws, float *loss_mean, double c
   }
 }
 
-// U: 32-byte vectors (16 bf16 each) per thread per chunk.  DB: load the next
-// chunk into a second register buffer while the current one is reduced.
-// T: threads per CTA (one row per CTA at a time).
-template <bool ARGMAX, int U, bool DB, int T = kThreads>
-__global__ void __launch_bounds__(T, (ARGMAX || (DB && U > 1)) ? 1 : 1024 / T)
-xent_rows(const uint16_t *__restrict__ logits, const int64_t *__restrict__ target,
-          float *__restrict__ loss, float *__restrict__ target_logit, int64_t *__restrict__ argmax,
-          float *__restrict__ loss_mean, void *__restrict__ ws, int64_t rows, int64_t cols,
-          int64_t ld, int64_t ignore_index) {
-  // Per-warp partials, double-buffered by row parity so one barrier per row
-  // suffices (the next row writes the other half).
-  constexpr int kThreads = T;
-  __shared__ MD red_md[2][kThreads / 32];
-  __shared__ ArgBest red_arg[2][kThreads / 32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  double cta_sum = 0.0;
-  long long cta_cnt = 0;
-  // Thread 0 fetches each row's target one row ahead, and gathers x[t] at the
-  // start of the row, so neither load is waited for at the row's end.
-  int64_t t_next = (tid == 0 && blockIdx.x < rows) ? target[blockIdx.x] : 0;
-  int parity = 0;
-
-  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, parity ^= 1) {
-    const uint16_t *px = logits + row * ld;
-    int64_t t = 0;
-    uint16_t xt_bits = 0;
-    if (tid == 0) {
-      t = t_next;
-      if (t >= 0 && t < cols) xt_bits = px[t];
-      if (row + gridDim.x < rows) t_next = target[row + gridDim.x];
-    }
-    const RowSplit sp = row_split(px, cols, 2);
-    const uint16_t *vx = px + sp.head;
-    MD st{-INFINITY, 0.0f};
-    ArgBest best{-INFINITY, INT64_MAX};
-    // With DB the next chunk's loads are in flight while the current chunk is
-    // reduced (register double buffering).
-    const int nvec = static_cast<int>(sp.nvec);  // rows shorter than 2^31 (host check)
-    constexpr int kU = U;
-    V8 cur[kU], nxt[kU];
-    if constexpr (DB) {
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int vi = tid + kThreads * u;
-        if (vi < nvec) cur[u] = ld_stream_v8(vx + static_cast<size_t>(vi) * 16);
-      }
-    }
-    for (int base = 0; base < nvec; base += kThreads * kU) {
-      const int nbase = base + kThreads * kU;
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        if constexpr (DB) {
-          const int vi = nbase + tid + kThreads * u;
-          if (vi < nvec) nxt[u] = ld_stream_v8(vx + static_cast<size_t>(vi) * 16);
-        } else {
-          const int vi = base + tid + kThreads * u;
-          if (vi < nvec) cur[u] = ld_stream_v8(vx + static_cast<size_t>(vi) * 16);
-        }
-      }
-      // chunk max on packed bf16 pairs (exact: a max only selects)
-      uint32_t m2 = 0xFF80FF80u;  // (-inf, -inf)
-#pragma unroll
-      for (int u = 0; u < kU; ++u)
-        if (base + tid + kThreads * u < nvec) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) m2 = max_nan_bf16x2(m2, cur[u].w[j]);
-        }
-      const float cm = max_nan(bf16_lo(m2), bf16_hi(m2));
-      if constexpr (ARGMAX) {
-        // Only the first chunk and a chunk that beats the thread's best need a
-        // scan for the first position of their max (elements are visited in
-        // index order, so a later equal value never wins).
-        if (best.i == INT64_MAX || (cm > best.v) || (cm != cm && best.v == best.v)) {
-          bool found = false;
-#pragma unroll
-          for (int u = 0; u < kU; ++u) {
-            const int vi = base + tid + kThreads * u;
-            if (vi < nvec) {
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const float e = (j & 1) ? bf16_hi(cur[u].w[j >> 1]) : bf16_lo(cur[u].w[j >> 1]);
-                const bool hit = (cm != cm) ? (e != e) : (e == cm);
-                if (!found && hit) {
-                  found = true;
-                  best = ArgBest{cm, sp.head + static_cast<int64_t>(vi) * 16 + j};
-                }
-              }
-            }
-          }
-        }
-      }
-      st = fold_chunk(st, cm);
-      if (st.m != -INFINITY) {
-        // exp(x - m) = 2^(x*log2e - m*log2e): one paired FMA and two SFU ops
-        // per two elements, summed with a paired add.
-        const float nmb = -st.m * kLog2e;
-        const uint64_t l2e2 = pack_f32x2(kLog2e, kLog2e), nmb2 = pack_f32x2(nmb, nmb);
-        uint64_t acc2 = 0;
-#pragma unroll
-        for (int u = 0; u < kU; ++u)
-          if (base + tid + kThreads * u < nvec) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const uint32_t w = cur[u].w[j];
-              const uint64_t t2 = fma_f32x2(pack_f32x2(bf16_lo(w), bf16_hi(w)), l2e2, nmb2);
-              acc2 = add_f32x2(acc2, pack_f32x2(ex2(f32x2_lo(t2)), ex2(f32x2_hi(t2))));
-            }
-          }
-        st.d += f32x2_lo(acc2) + f32x2_hi(acc2);
-      }
-      if constexpr (DB) {
-#pragma unroll
-        for (int u = 0; u < kU; ++u) cur[u] = nxt[u];
-      }
-    }
-    // head and tail scalars (at most 15 + 15), one per thread
-    int64_t si = -1;
-    if (tid < sp.head) si = tid;
-    else if (tid < sp.head + sp.tail) si = sp.head + sp.nvec * 16 + (tid - sp.head);
-    if (si >= 0) {
-      const float e = bf16_to_f32(ld_stream_u16(px + si));
-      st = md_merge(st, MD{e, 1.0f});
-      if constexpr (ARGMAX) best = arg_better(best, ArgBest{e, si});
-    }
-
-    // CTA combine
-    st = warp_md(st);
-    if constexpr (ARGMAX) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        ArgBest other{__shfl_xor_sync(0xffffffffu, best.v, o),
-                      static_cast<int64_t>(__shfl_xor_sync(0xffffffffu,
-                                                           static_cast<long long>(best.i), o))};
-        best = arg_better(best, other);
-      }
-    }
-    if (lane == 0) {
-      red_md[parity][warp] = st;
-      if constexpr (ARGMAX) red_arg[parity][warp] = best;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      MD r = lane < kThreads / 32 ? red_md[parity][lane] : MD{-INFINITY, 0.0f};
-      r = warp_md(r);
-      ArgBest b{-INFINITY, INT64_MAX};
-      if constexpr (ARGMAX) {
-        if (lane < kThreads / 32) b = red_arg[parity][lane];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          ArgBest other{__shfl_xor_sync(0xffffffffu, b.v, o),
-                        static_cast<int64_t>(__shfl_xor_sync(0xffffffffu,
-                                                             static_cast<long long>(b.i), o))};
-          b = arg_better(b, other);
-        }
-      }
-      if (lane == 0) {  // thread 0: holds t and x[t]
-        const float lse = r.m + logf(r.d);
-        float l, xt;
-        if (t == ignore_index) {
-          l = 0.0f;
-          xt = 0.0f;
-        } else if (t < 0 || t >= cols) {
-          l = __int_as_float(0x7fc00000);
-          xt = l;
-          atomicCAS(&g_fr_device_error, 0, FR_DEVERR_BAD_TARGET);
-        } else {
-          xt = bf16_to_f32(xt_bits);
-          l = lse - xt;
-        }
-        if (loss) loss[row] = l;
-        if (target_logit) target_logit[row] = xt;
-        if constexpr (ARGMAX) argmax[row] = b.i;
-        if (t != ignore_index) {
-          cta_sum += static_cast<double>(l);
-          ++cta_cnt;
-        }
-      }
-    }
-    // No trailing barrier: the next row uses the other half of red_*, and the
-    // barrier of that row orders this row's reads before the half is reused.
-  }
-
-  if (loss_mean != nullptr) finish_mean<T>(ws, loss_mean, cta_sum, cta_cnt);
-}
-
-// ---- staged variant: whole rows through shared memory by bulk copies --------
-// One persistent CTA per SM with two row buffers: row k + 1's bulk copies are
-// in flight while row k is reduced from shared memory, and row k + 2's are
-// issued as soon as every thread has read row k.  A row's 16-byte aligned
-// interior is copied in kStParts parts (each with its own mbarrier, so work
-// starts when the first part lands); its head and tail (fewer than 8 elements
-// each) are plain loads.  Copies of 25 KB and more stream at HBM speed on
-// GB300, where a CTA's bulk copies complete one after another.
-constexpr int kStThreads = 1024;
-constexpr int kStParts = 4;
-constexpr long long kStWaitBudget = 1LL << 31;  // SM clocks (about one second)
-
 struct RowGeom {
   const uint16_t *row;  // row start
   uint64_t a0;          // first 16-byte boundary at or after the row start
@@ -367,197 +171,6 @@ __device__ __forceinline__ RowGeom row_geom(const uint16_t *logits, int64_t row,
   g.head = static_cast<int>((a0 - s0) / 2);
   g.tail = static_cast<int>((s1 - a1) / 2);
   return g;
-}
-
-__device__ __forceinline__ uint32_t part_begin(uint32_t ibytes, int p) {
-  // parts of equal size rounded up to 32 bytes; the last takes the remainder
-  const uint32_t per = ((ibytes / kStParts) + 31u) & ~31u;
-  const uint32_t b = per * static_cast<uint32_t>(p);
-  return b < ibytes ? b : ibytes;
-}
-
-template <bool ARGMAX>
-__global__ void __launch_bounds__(kStThreads, 1)
-xent_staged(const uint16_t *__restrict__ logits, const int64_t *__restrict__ target,
-            float *__restrict__ loss, float *__restrict__ target_logit,
-            int64_t *__restrict__ argmax, float *__restrict__ loss_mean, void *__restrict__ ws,
-            int64_t rows, int64_t cols, int64_t ld, int64_t ignore_index, uint32_t buf_bytes) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem);  // [2][kStParts]
-  unsigned char *bufs = smem + 128;
-  __shared__ MD red_md[2][kStThreads / 32];
-  __shared__ ArgBest red_arg[2][kStThreads / 32];
-  __shared__ int timed_out;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t G = gridDim.x;
-  const int64_t nk = blockIdx.x < rows ? (rows - blockIdx.x + G - 1) / G : 0;
-  const uint64_t policy = l2_evict_first_policy();
-
-  auto issue = [&](int64_t k) {  // thread 0: row k of this CTA into buffer k & 1
-    if (k >= nk) return;
-    const RowGeom g = row_geom(logits, blockIdx.x + k * G, ld, cols);
-    const int b = static_cast<int>(k & 1);
-    for (int p = 0; p < kStParts; ++p) {
-      const uint32_t lo = part_begin(g.ibytes, p), hi = part_begin(g.ibytes, p + 1);
-      const uint32_t n = (p == kStParts - 1 ? g.ibytes : hi) - lo;
-      mbar_arrive_expect_tx(&full[b * kStParts + p], n);
-      if (n > 0)
-        bulk_copy_g2s(bufs + static_cast<size_t>(b) * buf_bytes + lo,
-                      reinterpret_cast<const unsigned char *>(g.a0) + lo, n,
-                      &full[b * kStParts + p], policy);
-    }
-  };
-
-  if (tid == 0) {
-    timed_out = 0;
-    for (int i = 0; i < 2 * kStParts; ++i) mbar_init(&full[i], 1);
-    mbar_init_fence();
-    issue(0);
-    issue(1);
-  }
-  __syncthreads();
-
-  double cta_sum = 0.0;
-  long long cta_cnt = 0;
-  int64_t t_next = (tid == 0 && nk > 0) ? target[blockIdx.x] : 0;
-  for (int64_t k = 0; k < nk; ++k) {
-    const int64_t row = blockIdx.x + k * G;
-    const int b = static_cast<int>(k & 1);
-    const uint32_t parity = static_cast<uint32_t>((k >> 1) & 1);
-    const RowGeom g = row_geom(logits, row, ld, cols);
-    int64_t t = 0;
-    uint16_t xt_bits = 0;
-    if (tid == 0) {
-      t = t_next;
-      if (t >= 0 && t < cols) xt_bits = g.row[t];
-      if (k + 1 < nk) t_next = target[row + G];
-    }
-    MD st{-INFINITY, 0.0f};
-    ArgBest best{-INFINITY, INT64_MAX};
-    const unsigned char *buf = bufs + static_cast<size_t>(b) * buf_bytes;
-    for (int p = 0; p < kStParts; ++p) {
-      if (!timed_out && !mbar_wait_bounded(&full[b * kStParts + p], parity, kStWaitBudget)) {
-        timed_out = 1;
-        atomicCAS(&g_fr_device_error, 0, FR_DEVERR_TIMEOUT);
-      }
-      const uint32_t lo = part_begin(g.ibytes, p);
-      const uint32_t hi = p == kStParts - 1 ? g.ibytes : part_begin(g.ibytes, p + 1);
-      // 32-byte pieces (16 bf16) of this part, thread-strided; a 16-byte
-      // remainder at the end of the interior is padded with -inf
-      for (uint32_t off = lo + 32u * tid; off < hi; off += 32u * kStThreads) {
-        const bool two = off + 16u < hi;
-        const uint4 a = lds_u4(buf + off);
-        const uint4 c = two ? lds_u4(buf + off + 16u) : make_uint4(0xFF80FF80u, 0xFF80FF80u,
-                                                                  0xFF80FF80u, 0xFF80FF80u);
-        const uint32_t wv[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
-        uint32_t m2 = max_nan_bf16x2(max_nan_bf16x2(a.x, a.y), max_nan_bf16x2(a.z, a.w));
-        m2 = max_nan_bf16x2(m2, max_nan_bf16x2(max_nan_bf16x2(c.x, c.y), max_nan_bf16x2(c.z, c.w)));
-        const float cm = max_nan(bf16_lo(m2), bf16_hi(m2));
-        if constexpr (ARGMAX) {
-          if (best.i == INT64_MAX || cm > best.v || (cm != cm && best.v == best.v)) {
-            bool found = false;
-            const int nval = two ? 16 : 8;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float e = (j & 1) ? bf16_hi(wv[j >> 1]) : bf16_lo(wv[j >> 1]);
-              const bool hit = (cm != cm) ? (e != e) : (e == cm);
-              if (!found && hit && j < nval) {
-                found = true;
-                best = ArgBest{cm, g.head + static_cast<int64_t>(off / 2) + j};
-              }
-            }
-          }
-        }
-        st = fold_chunk(st, cm);
-        if (st.m != -INFINITY) {
-          const float nmb = -st.m * kLog2e;
-          const uint64_t l2e2 = pack_f32x2(kLog2e, kLog2e), nmb2 = pack_f32x2(nmb, nmb);
-          uint64_t acc2 = 0;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint64_t t2 = fma_f32x2(pack_f32x2(bf16_lo(wv[j]), bf16_hi(wv[j])), l2e2, nmb2);
-            acc2 = add_f32x2(acc2, pack_f32x2(ex2(f32x2_lo(t2)), ex2(f32x2_hi(t2))));
-          }
-          st.d += f32x2_lo(acc2) + f32x2_hi(acc2);
-        }
-      }
-    }
-    // head and tail scalars from global memory
-    int64_t si = -1;
-    if (tid < g.head) si = tid;
-    else if (tid < g.head + g.tail) si = g.head + g.ibytes / 2 + (tid - g.head);
-    if (si >= 0) {
-      const float e = bf16_to_f32(ld_stream_u16(g.row + si));
-      st = md_merge(st, MD{e, 1.0f});
-      if constexpr (ARGMAX) best = arg_better(best, ArgBest{e, si});
-    }
-    // CTA combine; the barrier also frees buffer b for row k + 2
-    st = warp_md(st);
-    if constexpr (ARGMAX) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        ArgBest other{__shfl_xor_sync(0xffffffffu, best.v, o),
-                      static_cast<int64_t>(__shfl_xor_sync(0xffffffffu,
-                                                           static_cast<long long>(best.i), o))};
-        best = arg_better(best, other);
-      }
-    }
-    if (lane == 0) {
-      red_md[b][warp] = st;
-      if constexpr (ARGMAX) red_arg[b][warp] = best;
-    }
-    __syncthreads();
-    if (tid == 0 && !timed_out) {
-      fence_proxy_async_smem();
-      issue(k + 2);
-    }
-    if (warp == 0) {
-      MD r = red_md[b][lane];
-      r = warp_md(r);
-      ArgBest bb{-INFINITY, INT64_MAX};
-      if constexpr (ARGMAX) {
-        bb = red_arg[b][lane];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          ArgBest other{__shfl_xor_sync(0xffffffffu, bb.v, o),
-                        static_cast<int64_t>(__shfl_xor_sync(0xffffffffu,
-                                                             static_cast<long long>(bb.i), o))};
-          bb = arg_better(bb, other);
-        }
-      }
-      if (lane == 0) {  // thread 0 holds t and x[t]
-        const float lse = r.m + logf(r.d);
-        float l, xt;
-        if (t == ignore_index) {
-          l = 0.0f;
-          xt = 0.0f;
-        } else if (t < 0 || t >= cols) {
-          l = __int_as_float(0x7fc00000);
-          xt = l;
-          atomicCAS(&g_fr_device_error, 0, FR_DEVERR_BAD_TARGET);
-        } else {
-          xt = bf16_to_f32(xt_bits);
-          l = lse - xt;
-        }
-        if (loss) loss[row] = l;
-        if (target_logit) target_logit[row] = xt;
-        if constexpr (ARGMAX) argmax[row] = bb.i;
-        if (t != ignore_index) {
-          cta_sum += static_cast<double>(l);
-          ++cta_cnt;
-        }
-      }
-    }
-    // red_*[b] is next written two rows later, after the barrier of row k + 1.
-  }
-  if (timed_out && tid == 0)  // last bounded wait on copies that may be in flight
-    for (int i = 0; i < 2 * kStParts; ++i) mbar_wait_bounded(&full[i], 0, kStWaitBudget);
-
-  if (loss_mean != nullptr) finish_mean<kStThreads>(ws, loss_mean, cta_sum, cta_cnt);
-}
-
-uint32_t staged_buf_bytes(int64_t cols) {
-  return static_cast<uint32_t>((2 * cols + 16 + 127) / 128 * 128);
 }
 
 // ---- asynchronous-copy ring variant ---------------------------------------------
@@ -755,64 +368,6 @@ xent_async(const uint16_t *__restrict__ logits, const int64_t *__restrict__ targ
   if (loss_mean != nullptr) finish_mean<T>(ws, loss_mean, cta_sum, cta_cnt);
 }
 
-// Launch-configuration candidates (Stax (4), section 9.6, Algorithm 9.1):
-// a small set of compiled variants, the fastest chosen by measurement on
-// GB300; FR_XENT_VARIANT=<index> forces one (for re-measuring the choice).
-struct XentVariant {
-  const void *kern;      // the non-argmax kernel
-  const void *kern_arg;  // the argmax kernel
-  int threads;
-};
-
-template <int U, bool DB, int T>
-XentVariant make_variant() {
-  return XentVariant{reinterpret_cast<const void *>(&xent_rows<false, U, DB, T>),
-                     reinterpret_cast<const void *>(&xent_rows<true, U, DB, T>), T};
-}
-
-constexpr int kNumVariants = 6;
-constexpr int kDefaultVariant = 0;
-
-XentVariant *variants() {
-  static XentVariant v[kNumVariants] = {
-      make_variant<2, false, 512>(), make_variant<1, true, 512>(), make_variant<4, false, 512>(),
-      make_variant<2, true, 512>(),  make_variant<2, false, 256>(), make_variant<2, false, 128>()};
-  return v;
-}
-
-int chosen_variant() {
-  static int chosen = -1;
-  if (chosen < 0) {
-    chosen = kDefaultVariant;
-    if (const char *e = getenv("FR_XENT_VARIANT")) {
-      const int k = atoi(e);
-      if (k >= 0 && k < kNumVariants) chosen = k;
-    }
-  }
-  return chosen;
-}
-
-// CTAs per SM the chosen kernel keeps resident (registers decide it), so the
-// persistent grid fills every SM whatever the compiler's register count.
-int xent_ctas_per_sm(bool argmax) {
-  XentVariant &v = variants()[chosen_variant()];
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, argmax ? v.kern_arg : v.kern, v.threads,
-                                                    0) != cudaSuccess) {
-    cudaGetLastError();
-    return kCtasPerSm;
-  }
-  return n < 1 ? 1 : n;
-}
-
-// Persistent grid of one kernel: every CTA it can keep resident on every SM.
-int xent_grid(int64_t rows, int sm_count, bool argmax) {
-  int64_t g = static_cast<int64_t>(sm_count) * std::min(xent_ctas_per_sm(argmax), 16);
-  if (g > rows) g = rows;
-  if (g < 1) g = 1;
-  return static_cast<int>(g);
-}
-
 }  // namespace
 
 size_t xent_workspace(int64_t rows, int sm_count) {
@@ -822,104 +377,6 @@ size_t xent_workspace(int64_t rows, int sm_count) {
   if (g > rows) g = rows;
   if (g < 1) g = 1;
   return kCtaOffset + 16 * static_cast<size_t>(g);
-}
-
-// The staged kernel, pinned with FR_XENT_VARIANT=staged, when its two row
-// buffers fit one CTA's shared memory.  Measured on GB300 (8192 x 50257) it
-// is slower than register streaming (230 us against 170 us), so it is not the
-// default.
-bool xent_use_staged(int64_t cols, int max_smem_optin) {
-  const char *e = getenv("FR_XENT_VARIANT");
-  if (e == nullptr || strcmp(e, "staged") != 0) return false;
-  return 128 + 2 * static_cast<size_t>(staged_buf_bytes(cols)) + 4096 <=
-         static_cast<size_t>(max_smem_optin);
-}
-
-cudaError_t launch_xent_staged(const uint16_t *logits, const int64_t *target, float *loss,
-                               float *loss_mean, float *target_logit, int64_t *argmax,
-                               int64_t rows, int64_t cols, int64_t ld, int64_t ignore_index,
-                               void *workspace, int sm_count, cudaStream_t s) {
-  const uint32_t bb = staged_buf_bytes(cols);
-  const size_t smem = 128 + 2 * static_cast<size_t>(bb);
-  const void *kern = argmax != nullptr ? reinterpret_cast<const void *>(&xent_staged<true>)
-                                       : reinterpret_cast<const void *>(&xent_staged<false>);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  int64_t grid = sm_count;  // one CTA per SM (the two buffers fill its shared memory)
-  if (grid > rows) grid = rows;
-  if (loss_mean != nullptr) {
-    e = cudaMemsetAsync(workspace, 0, 16, s);
-    if (e != cudaSuccess) return e;
-  }
-  uint32_t bbv = bb;
-  void *args[] = {&logits, &target, &loss, &target_logit, &argmax, &loss_mean, &workspace,
-                  &rows, &cols, &ld, &ignore_index, &bbv};
-  return cudaLaunchKernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kStThreads), args, smem, s);
-}
-
-struct AsyncVariant {
-  const void *kern, *kern_arg;
-  int threads;
-  size_t smem;
-  int max_per_sm;  // CTAs per SM to launch at most (measured best)
-};
-
-template <int T, int U, int NS>
-AsyncVariant make_async(int max_per_sm) {
-  return AsyncVariant{reinterpret_cast<const void *>(&xent_async<false, T, U, NS>),
-                      reinterpret_cast<const void *>(&xent_async<true, T, U, NS>), T,
-                      static_cast<size_t>(NS) * U * T * 16, max_per_sm};
-}
-
-constexpr int kNumAsync = 7;
-
-// The default launch configuration: measured on GB300 (8192 x 50257 bf16),
-// async2 (256 threads, 4 x 16 bytes per item, 4 stages, 2 CTAs per SM) takes
-// 156 us; async3 159, async5 165, async6 164, async0/1 204, async4 194; the
-// register-streaming variants 169 (0, 4), 183 (1), 192 (2), 195 (5), 224 (3);
-// whole-row bulk-copy staging 230.
-constexpr int kDefaultAsync = 2;
-
-// FR_XENT_VARIANT=async0..async6 selects an asynchronous-copy variant, a bare
-// index a register-streaming one, "staged" the bulk-copy one; unset = default.
-int async_variant() {
-  const char *e = getenv("FR_XENT_VARIANT");
-  if (e == nullptr || e[0] == 0) return kDefaultAsync;
-  if (strncmp(e, "async", 5) != 0) return -1;
-  const int k = atoi(e + 5);
-  return k >= 0 && k < kNumAsync ? k : -1;
-}
-
-cudaError_t launch_xent_async(int which, const uint16_t *logits, const int64_t *target,
-                              float *loss, float *loss_mean, float *target_logit, int64_t *argmax,
-                              int64_t rows, int64_t cols, int64_t ld, int64_t ignore_index,
-                              void *workspace, int sm_count, cudaStream_t s) {
-  static AsyncVariant v[kNumAsync] = {
-      make_async<512, 4, 4>(16), make_async<512, 2, 4>(16), make_async<256, 4, 4>(2),
-      make_async<256, 4, 6>(16), make_async<128, 4, 4>(16), make_async<256, 2, 8>(16),
-      make_async<256, 8, 3>(2)};
-  const AsyncVariant &a = v[which];
-  const void *kern = argmax != nullptr ? a.kern_arg : a.kern;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(a.smem));
-  if (e != cudaSuccess) return e;
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, a.threads, a.smem);
-  if (e != cudaSuccess) return e;
-  if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  if (per_sm > a.max_per_sm) per_sm = a.max_per_sm;
-  if (per_sm > kMaxCtasPerSm) per_sm = kMaxCtasPerSm;
-  int64_t grid = static_cast<int64_t>(sm_count) * per_sm;
-  if (grid > rows) grid = rows;
-  if (loss_mean != nullptr) {
-    e = cudaMemsetAsync(workspace, 0, 16, s);
-    if (e != cudaSuccess) return e;
-  }
-  void *args[] = {&logits, &target, &loss, &target_logit, &argmax, &loss_mean, &workspace,
-                  &rows, &cols, &ld, &ignore_index};
-  return cudaLaunchKernel(kern, dim3(static_cast<unsigned>(grid)), dim3(a.threads), args, a.smem,
-                          s);
 }
 
 namespace {
@@ -1108,37 +565,18 @@ cudaError_t launch_xent(const uint16_t *logits, const int64_t *target, float *lo
                         float *loss_mean, float *target_logit, int64_t *argmax, int64_t rows,
                         int64_t cols, int64_t ld, int64_t ignore_index, void *workspace,
                         int sm_count, int max_smem_optin, cudaStream_t s) {
-  const char *pin = getenv("FR_XENT_VARIANT");
-  if ((pin == nullptr || pin[0] == 0) && argmax != nullptr)
+  if (argmax != nullptr)
     return launch_xent_argmax_default(logits, target, loss, loss_mean, target_logit, argmax, rows,
                                       cols, ld, ignore_index, workspace, sm_count, s);
-  if ((pin == nullptr || pin[0] == 0) && argmax == nullptr) {
-    // the configuration recorded for this shape (fr_xent_tune / _set_config),
-    // else the default point of the box
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    XentConfig cfg = xent_default_config();
-    xent_recorded_config(dev, rows, cols, ld, &cfg);
-    return launch_xent_config(cfg, logits, target, loss, loss_mean, target_logit, rows, cols, ld,
-                              ignore_index, workspace, sm_count, max_smem_optin, s);
-  }
-  if (const int av = async_variant(); av >= 0)
-    return launch_xent_async(av, logits, target, loss, loss_mean, target_logit, argmax, rows,
-                             cols, ld, ignore_index, workspace, sm_count, s);
-  if (xent_use_staged(cols, max_smem_optin))
-    return launch_xent_staged(logits, target, loss, loss_mean, target_logit, argmax, rows, cols,
-                              ld, ignore_index, workspace, sm_count, s);
-  const int grid = xent_grid(rows, sm_count, argmax != nullptr);
-  if (loss_mean != nullptr) {
-    cudaError_t e = cudaMemsetAsync(workspace, 0, 16, s);
-    if (e != cudaSuccess) return e;
-  }
-  const XentVariant &v = variants()[chosen_variant()];
-  void *args[] = {&logits, &target, &loss, &target_logit, &argmax, &loss_mean, &workspace,
-                  &rows, &cols, &ld, &ignore_index};
-  return cudaLaunchKernel(argmax != nullptr ? v.kern_arg : v.kern, dim3(grid), dim3(v.threads),
-                          args, 0, s);
+  // the configuration recorded for this shape (fr_xent_tune / _set_config),
+  // else the default point of the box
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  XentConfig cfg = xent_default_config();
+  xent_recorded_config(dev, rows, cols, ld, &cfg);
+  return launch_xent_config(cfg, logits, target, loss, loss_mean, target_logit, rows, cols, ld,
+                            ignore_index, workspace, sm_count, max_smem_optin, s);
 }
 
 // The mean from parts that ranks holding shards of one batch have summed

@@ -323,21 +323,27 @@ def test_layernorm_constant_rows(o):
 
 # ---------------------------------------------------------------- cross entropy
 
-# register streaming (default), whole rows staged by bulk copies, cp.async ring
-XENT_KERNELS = ["0", "staged", "async0", "async1", "async2", "async3", "async4", "async5", "async6"]
+# the default point of the configuration box (None) and runnable points of
+# other shapes: CTA sizes 128 .. 1024, 1 .. 8 vectors per ring item, 2 .. 8
+# stages, 1 .. 4 CTAs per SM (the argmax kernel always runs at the default
+# point; every runnable point is also checked in test_tune_gpu.py)
+XENT_KERNELS = [None, (256, 4, 4, 2), (512, 2, 8, 1), (1024, 1, 2, 1), (128, 1, 2, 4),
+                (256, 8, 2, 2)]
 
 
-def run_xent(bits, target, ignore=-100, offset=0, pad=0, kernel="staged", argmax=True):
-    """kernel pins the implementation: "staged" or a register variant index."""
-    import os
+def run_xent(bits, target, ignore=-100, offset=0, pad=0, kernel=None, argmax=True):
+    """kernel: None (the default configuration) or a configuration recorded for
+    this shape for the call."""
     rows, cols = bits.shape
     px = place(bits, offset, cols + pad)
     t = torch.from_numpy(target).cuda()
-    os.environ["FR_XENT_VARIANT"] = kernel
+    if kernel is not None:
+        fr.fr_xent_set_config(rows, cols, kernel, ld=cols + pad)
     try:
         r = fr.fr_xent(px.t, t, ignore, want_target_logit=True, want_argmax=argmax)
     finally:
-        os.environ.pop("FR_XENT_VARIANT", None)
+        if kernel is not None:
+            fr.fr_xent_set_config(rows, cols, None, ld=cols + pad)
     torch.cuda.synchronize()
     return {k: v.cpu().numpy() for k, v in r.items()}
 
@@ -358,7 +364,7 @@ def test_xent(o, rows, cols, layout):
     w = workloads.make(4, rows=rows, cols=cols, seed=4000 + rows * 7 + cols)
     ref = o.xent(w.arrays["logits"], w.arrays["target"], -100)
     for kernel in XENT_KERNELS:
-        for argmax in (True, False):
+        for argmax in ((True, False) if kernel is None else (False,)):
             got = run_xent(w.arrays["logits"], w.arrays["target"], -100, *layout, kernel=kernel,
                            argmax=argmax)
             check_xent(got, ref, f"{kernel} argmax={argmax} {rows}x{cols} {layout}")
@@ -378,12 +384,13 @@ def test_xent_ties_nan_and_ignore(o):
     ref = o.xent(bits, t, -100)
     for kernel in XENT_KERNELS:
         for offset in (0, 1):
-            got = run_xent(bits, t, -100, offset=offset, kernel=kernel)
+            got = run_xent(bits, t, -100, offset=offset, kernel=kernel, argmax=kernel is None)
             check_xent(got, ref, f"ties/nan {kernel} offset {offset}")
-            assert got["argmax"][5] == 17 and got["argmax"][6] == 3
+            if kernel is None:
+                assert got["argmax"][5] == 17 and got["argmax"][6] == 3
         # every row ignored: mean is 0/0
         allign = np.full(rows, -100, np.int64)
-        got = run_xent(bits, allign, kernel=kernel)
+        got = run_xent(bits, allign, kernel=kernel, argmax=kernel is None)
         assert np.isnan(got["mean"][0]) and (got["loss"] == 0).all()
     assert fr.fr_check_device_error() == 0
 
@@ -395,7 +402,7 @@ def test_xent_bad_target_sets_device_error(o):
     t[6] = -5           # negative, not ignore_index
     ref = o.xent(w.arrays["logits"], t, -100)
     for kernel in XENT_KERNELS:
-        got = run_xent(w.arrays["logits"], t, kernel=kernel)
+        got = run_xent(w.arrays["logits"], t, kernel=kernel, argmax=kernel is None)
         check_xent(got, ref, f"bad target {kernel}")
         assert np.isnan(got["loss"][[4, 6]]).all()
         assert fr.fr_check_device_error() == 1
