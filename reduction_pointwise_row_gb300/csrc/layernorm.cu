@@ -819,25 +819,30 @@ const FullShape kFullShapes[] = {{"r1a2", full_slots(1, 2), FR_LNF(1, 2)},
 #undef FR_LNF
 
 // The equal-count kernel's shape for a row length: cols = C * T * 32 with
-// C in 1, 2, 4, 8 and T a power of two in 64 .. 256 (the largest that fits),
-// else T = 512.  Measured on GB300 (256 MiB of bf16 rows), at most 256
-// threads per CTA against at most 512: 16384 columns 88.8 against 93.0 us,
-// 32768 86.2 against 89.0, 65536 92.3 against 97.1; the same elsewhere.
-// FR_LAYERNORM_CTA=64|128|256|512 caps T instead.
+// C in 1, 2, 4, 8 and T a power of two in 64 .. 512.  Measured on GB300
+// (256 MiB of bf16 rows, launches back to back): 8192 columns 84.2 us with
+// one CTA of 256 threads, 86.8 with 2 of 128; 16384 84.1 with 2 of 256,
+// 86.1 with 4 of 128, 88.3 with 1 of 512; 32768 86.3 with 4 of 256, 88.8
+// with 2 of 512, 96.0 with 8 of 128; 65536 93.1 with 4 of 512, 95.7-99.4
+// with 8 of 256.  FR_LAYERNORM_CTA=64|128|256|512 caps T.
 bool full_shape(int64_t cols, int *T, int *C) {
   const char *e = getenv("FR_LAYERNORM_CTA");
   const int v = e != nullptr ? atoi(e) : 256;
   const int tmax = v == 64 || v == 128 || v == 512 ? v : 256;
-  for (int pass = 0; pass < 2; ++pass)
-    for (int c = 1; c <= kFullMaxCluster; c <<= 1)
-      for (int t = pass == 0 ? tmax : 512; t >= 64; t >>= 1) {
-        if (pass == 1 && t <= tmax) break;
-        if (cols == static_cast<int64_t>(c) * t * kClCols) {
-          *T = t;
-          *C = c;
-          return true;
+  // Clusters of up to 4 CTAs first (8 cost 5-10 %: [2048, 65536] 96.9 us
+  // with 8 CTAs of 256 threads, 93.0 with 4 of 512), then CTAs of at most
+  // tmax threads, then larger ones.
+  for (int cmax = 4; cmax <= kFullMaxCluster; cmax <<= 1)
+    for (int pass = 0; pass < 2; ++pass)
+      for (int c = 1; c <= cmax; c <<= 1)
+        for (int t = pass == 0 ? tmax : 512; t >= 64; t >>= 1) {
+          if (pass == 1 && t <= tmax) break;
+          if (cols == static_cast<int64_t>(c) * t * kClCols) {
+            *T = t;
+            *C = c;
+            return true;
+          }
         }
-      }
   return false;
 }
 
