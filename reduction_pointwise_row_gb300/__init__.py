@@ -111,21 +111,29 @@ def _check(status: int, where: str):
         raise FRError(status, where)
 
 
+_current_raw_stream = None  # device index -> cudaStream_t of its current stream
+_current_device = None
+
+
 def _stream(stream=None, device_index=None):
-    """The raw cudaStream_t to launch on: `stream`, else the current stream of
-    the current (or given) device."""
-    import torch
+    """The raw cudaStream_t (an int) to launch on: `stream`, else the current
+    stream of the current (or given) device.  The lookups are resolved once:
+    a call costs two C calls, no Stream object (launch-bound shapes feel it)."""
+    global _current_raw_stream, _current_device
     if stream is not None:
-        return ctypes.c_void_p(stream.cuda_stream)
-    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
-    if raw is not None:  # one call instead of building a Stream object
-        idx = torch.cuda.current_device() if device_index is None else device_index
-        return ctypes.c_void_p(raw(idx))
-    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        return stream.cuda_stream
+    if _current_raw_stream is None:
+        import torch
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        _current_raw_stream = raw if raw is not None else (
+            lambda i: torch.cuda.current_stream(i).cuda_stream)
+        _current_device = getattr(torch._C, "_cuda_getDevice", torch.cuda.current_device)
+    return _current_raw_stream(_current_device() if device_index is None else device_index)
 
 
 def _ptr(t):
-    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+    """A tensor's device address as an int (ctypes passes it as void *), or None."""
+    return t.data_ptr() if t is not None else None
 
 
 def _ld(t) -> int:
