@@ -61,10 +61,11 @@ class Oracle:
         lib.oracle_online_attn_row.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp, vp, vp, vp]
         lib.oracle_layernorm.argtypes = [vp, i64, i64, i64, vp, vp, f64, vp, vp, vp]
         lib.oracle_xent.argtypes = [vp, i64, i64, i64, vp, i64, vp, vp, vp, vp, vp, vp, vp]
+        lib.oracle_xent_f32.argtypes = [vp, i64, i64, i64, vp, i64, vp, vp, vp, vp, vp, vp, vp]
         for name in ("oracle_relu_add_sum", "oracle_row_sumsq", "oracle_row_l2norm",
                      "oracle_softmax",
                      "oracle_md_merge", "oracle_md_fold", "oracle_online_attn_row",
-                     "oracle_layernorm", "oracle_xent"):
+                     "oracle_layernorm", "oracle_xent", "oracle_xent_f32"):
             getattr(lib, name).restype = None
         self.lib = lib
         self.planted = lib.oracle_planted()
@@ -144,8 +145,10 @@ class Oracle:
 
     # ---- cross entropy -----------------------------------------------------
     def xent(self, logit_bits: np.ndarray, target: np.ndarray, ignore_index: int = -100):
-        """logit_bits: uint16 bf16 patterns [rows, cols]; target int64 [rows]."""
-        assert logit_bits.dtype == np.uint16 and logit_bits.strides[1] == 2
+        """logit_bits: uint16 bf16 patterns or float32 values [rows, cols];
+        target int64 [rows]."""
+        f32 = logit_bits.dtype == np.float32
+        assert (f32 or logit_bits.dtype == np.uint16) and logit_bits.strides[1] == logit_bits.itemsize
         rows, cols = logit_bits.shape
         t = np.ascontiguousarray(target, dtype=np.int64)
         assert t.shape == (rows,)
@@ -153,7 +156,8 @@ class Oracle:
         am = np.empty(rows, dtype=np.int64)
         mean = ctypes.c_double()
         cnt, bad = ctypes.c_int64(), ctypes.c_int64()
-        self.lib.oracle_xent(logit_bits.ctypes.data, rows, cols, logit_bits.strides[0] // 2,
+        fn = self.lib.oracle_xent_f32 if f32 else self.lib.oracle_xent
+        fn(logit_bits.ctypes.data, rows, cols, logit_bits.strides[0] // logit_bits.itemsize,
                              t.ctypes.data, ignore_index, loss.ctypes.data, lse.ctypes.data,
                              tl.ctypes.data, am.ctypes.data, ctypes.byref(mean),
                              ctypes.byref(cnt), ctypes.byref(bad))

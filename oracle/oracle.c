@@ -270,19 +270,24 @@ void oracle_layernorm(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld,
  * first NaN wins (the pages do not define argmax; lowest index breaks ties).
  * A NaN in the row makes m, LSE and the loss NaN.
  * ---------------------------------------------------------------------- */
-void oracle_xent(const uint16_t *logits, int64_t rows, int64_t cols, int64_t ld,
-                 const int64_t *target, int64_t ignore_index, double *loss, double *lse_out,
-                 double *target_logit, int64_t *argmax, double *mean, int64_t *n_counted,
-                 int64_t *n_bad) {
+/* Logit k of row i, from bf16 bit patterns (f32 == 0) or fp32 values. */
+static double logit_value(const void *logits, int f32, int64_t ld, int64_t i, int64_t k) {
+  if (f32) return (double)((const float *)logits)[i * ld + k];
+  return bf16_value(((const uint16_t *)logits)[i * ld + k]);
+}
+
+static void xent_rows(const void *logits, int f32, int64_t rows, int64_t cols, int64_t ld,
+                      const int64_t *target, int64_t ignore_index, double *loss, double *lse_out,
+                      double *target_logit, int64_t *argmax, double *mean, int64_t *n_counted,
+                      int64_t *n_bad) {
   double sum = 0.0;
   int64_t cnt = 0, bad = 0;
   for (int64_t i = 0; i < rows; ++i) {
-    const uint16_t *row = logits + i * ld;
     double m = -INFINITY;
     int64_t am = 0;
     int has_nan = 0;
     for (int64_t k = 0; k < cols; ++k) {
-      double v = bf16_value(row[k]);
+      double v = logit_value(logits, f32, ld, i, k);
       if (isnan(v)) {
         if (!has_nan) am = k;
         has_nan = 1;
@@ -296,7 +301,7 @@ void oracle_xent(const uint16_t *logits, int64_t rows, int64_t cols, int64_t ld,
     }
     if (has_nan) m = NAN;
     double l = 0.0;
-    for (int64_t k = 0; k < cols; ++k) l += exp(bf16_value(row[k]) - m);
+    for (int64_t k = 0; k < cols; ++k) l += exp(logit_value(logits, f32, ld, i, k) - m);
 #if ORACLE_PLANT == 8
     double lse = log(l); /* planted: max dropped from the LSE */
 #else
@@ -318,7 +323,7 @@ void oracle_xent(const uint16_t *logits, int64_t rows, int64_t cols, int64_t ld,
       ++cnt;
       sum += NAN;
     } else {
-      double xt = bf16_value(row[t]);
+      double xt = logit_value(logits, f32, ld, i, t);
       loss[i] = lse - xt;
       if (target_logit) target_logit[i] = xt;
       ++cnt;
@@ -328,4 +333,22 @@ void oracle_xent(const uint16_t *logits, int64_t rows, int64_t cols, int64_t ld,
   if (mean) *mean = sum / (double)cnt; /* 0/0 = NaN when every row is ignored */
   if (n_counted) *n_counted = cnt;
   if (n_bad) *n_bad = bad;
+}
+
+/* bf16 logits (bit patterns) */
+void oracle_xent(const uint16_t *logits, int64_t rows, int64_t cols, int64_t ld,
+                 const int64_t *target, int64_t ignore_index, double *loss, double *lse_out,
+                 double *target_logit, int64_t *argmax, double *mean, int64_t *n_counted,
+                 int64_t *n_bad) {
+  xent_rows(logits, 0, rows, cols, ld, target, ignore_index, loss, lse_out, target_logit, argmax,
+            mean, n_counted, n_bad);
+}
+
+/* fp32 logits: the same definition on fp32 values */
+void oracle_xent_f32(const float *logits, int64_t rows, int64_t cols, int64_t ld,
+                     const int64_t *target, int64_t ignore_index, double *loss, double *lse_out,
+                     double *target_logit, int64_t *argmax, double *mean, int64_t *n_counted,
+                     int64_t *n_bad) {
+  xent_rows(logits, 1, rows, cols, ld, target, ignore_index, loss, lse_out, target_logit, argmax,
+            mean, n_counted, n_bad);
 }

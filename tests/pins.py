@@ -430,4 +430,42 @@ def pin_xent_shift_invariance(o):
     _close(a["loss"], b["loss"], rtol=1e-12)
 
 
+def pin_xent_f32_vs_torch(o):
+    """fp32 logits (not bf16-representable): torch cross_entropy in fp64 on the
+    same values, reduction none and mean, and its logsumexp."""
+    import torch
+    rng = _rng(21)
+    rows, V = 48, 777
+    x = (3 * rng.standard_normal((rows, V))).astype(np.float32)
+    t = rng.integers(0, V, rows)
+    t[[0, 5]] = -100
+    r = o.xent(x, t, -100)
+    tx, tt = torch.from_numpy(x.astype(np.float64)), torch.from_numpy(t)
+    none = torch.nn.functional.cross_entropy(tx, tt, ignore_index=-100, reduction="none")
+    mean = torch.nn.functional.cross_entropy(tx, tt, ignore_index=-100, reduction="mean")
+    _close(r["loss"], none.numpy(), rtol=1e-12, atol=1e-13)
+    _close(r["mean"], float(mean), rtol=1e-12)
+    _close(r["lse"], torch.logsumexp(tx, dim=1).numpy(), rtol=1e-13)
+    _close(r["target_logit"][t >= 0], x[np.arange(rows), t][t >= 0].astype(np.float64), rtol=0)
+
+
+def pin_xent_f32_keeps_every_bit(o):
+    """fp32 logits are read as fp32: values one fp32 step apart (equal in bf16)
+    keep their order for argmax and their difference in the loss; bf16 values
+    given as fp32 give the bf16 results exactly."""
+    one_up = np.nextafter(np.float32(1.0), np.float32(2.0))
+    x = np.array([[1.0, one_up, 0.5]], np.float32)
+    r = o.xent(x, np.array([0]))
+    assert r["argmax"][0] == 1
+    e = [math.exp(float(v)) for v in x[0]]
+    _close(r["loss"][0], math.log(math.fsum(e)) - 1.0, rtol=1e-14)
+    bits = _bf16_bits((_rng(22).integers(-64, 65, size=(4, 333)) / 16))
+    as_f32 = (bits.astype(np.uint32) << 16).view(np.float32)
+    t = np.array([1, 2, -100, 332])
+    a, b = o.xent(bits, t), o.xent(as_f32, t)
+    for k in ("loss", "lse", "target_logit", "argmax"):
+        assert (np.asarray(a[k]) == np.asarray(b[k])).all(), k
+    assert a["mean"] == b["mean"]
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
