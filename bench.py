@@ -52,7 +52,7 @@ def parse():
     p.add_argument("--only", choices=["relu_add_sum", "softmax", "layernorm", "split", "xent",
                                       "sumsq", "l2norm", "softmax_4097", "softmax_4097_looped",
                                       "softmax_65537", "softmax_65537_looped",
-                                      "looped", "softmax_bf16", "xent_box"],
+                                      "looped", "softmax_bf16", "xent_f32", "xent_box"],
                    help="time one workload alone (for profiler captures) and exit")
     p.add_argument("--form", default="auto", choices=["auto", "persistent", "looped", "split"],
                    help="with --only: force a reduction form")
@@ -461,6 +461,16 @@ def setup_workload(name, fr, workloads, dev, form="auto"):
             calls.append(lambda lg=lg, wsx=wsx: fr.fr_xent(lg, tg, -100, workspace=wsx,
                                                            group=group))
         return calls, "xent", rows, cols, 1 if group is None else 2
+    if name == "xent_f32":  # the cross-entropy shape with fp32 logits
+        rows, cols = 8192, 50257
+        w = workloads.make_xent_f32(rows, cols)
+        tg = torch.from_numpy(w.arrays["target"]).to(dev)
+        for _ in range(nsets("xent_f32", rows, cols)):
+            lg = to_device(w.arrays["logits"], dev)
+            wsx = torch.empty(fr.fr_workspace_size("xent", rows, cols, "f32"),
+                              dtype=torch.uint8, device=dev)
+            calls.append(lambda lg=lg, wsx=wsx: fr.fr_xent(lg, tg, -100, workspace=wsx))
+        return calls, "xent_f32", rows, cols, 1
     raise ValueError(name)
 
 
@@ -469,7 +479,8 @@ EXTRA = {"relu_add_sum": "relu_add_sum_64x128", "layernorm": "layernorm_4096x327
          "sumsq": "sumsq_split_64x16384", "l2norm": "l2norm_looped_16384x16384",
          "softmax_4097": "softmax_8190x4097", "softmax_4097_looped": "softmax_looped_8190x4097",
          "softmax_65537": "softmax_511x65537", "softmax_65537_looped": "softmax_looped_511x65537",
-         "looped": "relu_add_sum_looped_16384x8192", "softmax_bf16": "softmax_bf16_65536x1024"}
+         "looped": "relu_add_sum_looped_16384x8192", "softmax_bf16": "softmax_bf16_65536x1024",
+         "xent_f32": "xent_f32_8192x50257"}
 
 
 def extra_configs(fr, traffic, workloads, timed, dev, peak, args, world, names=None,

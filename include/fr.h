@@ -236,8 +236,8 @@ fr_status fr_layernorm(const void *x, const float *gamma, const float *beta, voi
  * PyTorch's cross_entropy(reduction='mean').  A target outside [0, cols) other
  * than ignore_index gives that row NaN and sets FR_DEVERR_BAD_TARGET.
  *
- *   logits       bf16 [rows, ld] device input; any ld >= cols (rows need not
- *                be 16-byte aligned: heads and tails are peeled)
+ *   logits       bf16 (or fp32) [rows, ld] device input; any ld >= cols (rows
+ *                need not be 16-byte aligned: heads and tails are peeled)
  *   target       int64 [rows] device input
  *   loss         fp32 [rows] device output (may be NULL)
  *   loss_mean    fp32 [1] device output (may be NULL)
@@ -245,7 +245,10 @@ fr_status fr_layernorm(const void *x, const float *gamma, const float *beta, voi
  *                NaN for bad targets); may be NULL
  *   argmax       int64 [rows] device output, first index of the row maximum,
  *                NaN counting as the maximum; may be NULL
- *   dtype        FR_BF16
+ *   dtype        FR_BF16 (logits as bf16 bit patterns, widened exactly) or
+ *                FR_F32; fp32 logits always run at the default launch
+ *                configuration (fr_xent_tune and recorded configurations
+ *                are for bf16 logits)
  *   workspace    fr_workspace_size(FR_OP_XENT, ...) bytes when loss_mean is
  *                requested (per-CTA partial sums and a ticket; the library
  *                zeroes the ticket on the stream before each launch).  After

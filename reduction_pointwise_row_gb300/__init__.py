@@ -306,7 +306,7 @@ def _nullcontext():
 def fr_xent(logits, target, ignore_index: int = -100, want_loss: bool = True,
             want_mean: bool = True, want_target_logit: bool = False, want_argmax: bool = False,
             form: str = "auto", workspace=None, stream=None, group=None):
-    """Cross entropy of bf16 logits rows against int64 targets.
+    """Cross entropy of bf16 or fp32 logits rows against int64 targets.
 
     Returns a dict with the requested outputs: ``loss`` [rows], ``mean`` [1],
     ``target_logit`` [rows], ``argmax`` [rows] (int64).  With ``group`` (a
@@ -315,7 +315,8 @@ def fr_xent(logits, target, ignore_index: int = -100, want_loss: bool = True,
     are all-reduced between this rank's kernel and the finishing kernel.
     """
     import torch
-    assert logits.is_cuda and logits.dtype == torch.bfloat16 and logits.dim() == 2
+    assert logits.is_cuda and logits.dtype in (torch.bfloat16, torch.float32) and logits.dim() == 2
+    dt = "bf16" if logits.dtype == torch.bfloat16 else "f32"
     assert target.dtype == torch.int64 and target.is_cuda
     rows, cols = logits.shape
     assert target.numel() == rows
@@ -327,9 +328,9 @@ def fr_xent(logits, target, ignore_index: int = -100, want_loss: bool = True,
     am = torch.empty(rows, dtype=torch.int64, device=dev) if want_argmax else None
     ws, nws = (None, 0)
     if want_mean:
-        ws, nws = _workspace("xent", rows, cols, "bf16", form, dev, workspace)
+        ws, nws = _workspace("xent", rows, cols, dt, form, dev, workspace)
     _check(lib().fr_xent(_ptr(logits), _ptr(target), _ptr(loss), _ptr(mean), _ptr(tl), _ptr(am),
-                         rows, cols, _ld(logits), ignore_index, DTYPES["bf16"], FORMS[form],
+                         rows, cols, _ld(logits), ignore_index, DTYPES[dt], FORMS[form],
                          _ptr(ws), nws, _stream(stream)), "fr_xent")
     if group is not None and want_mean:
         with torch.cuda.stream(stream) if stream is not None else _nullcontext():

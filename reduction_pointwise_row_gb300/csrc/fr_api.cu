@@ -387,10 +387,11 @@ fr_status fr_xent(const void *logits, const int64_t *target, float *loss, float 
                   float *target_logit, int64_t *argmax, int64_t rows, int64_t cols, int64_t ld,
                   int64_t ignore_index, fr_dtype dtype, fr_form form, void *workspace,
                   size_t workspace_bytes, fr_stream_t stream) {
-  if (dtype != FR_BF16) return FR_ERR_UNSUPPORTED_DTYPE;
+  if (dtype != FR_BF16 && dtype != FR_F32) return FR_ERR_UNSUPPORTED_DTYPE;
+  const int64_t es = dtype == FR_F32 ? 4 : 2;
   if (!logits || !target) return FR_ERR_INVALID_ARG;
-  if (!shape_ok(rows, cols, ld, 2)) return FR_ERR_INVALID_ARG;
-  if (!aligned(logits, 2) || !aligned(target, 8) || (loss && !aligned(loss, 4)) ||
+  if (!shape_ok(rows, cols, ld, es)) return FR_ERR_INVALID_ARG;
+  if (!aligned(logits, es) || !aligned(target, 8) || (loss && !aligned(loss, 4)) ||
       (loss_mean && !aligned(loss_mean, 4)) || (target_logit && !aligned(target_logit, 4)) ||
       (argmax && !aligned(argmax, 8)))
     return FR_ERR_MISALIGNED;
@@ -404,9 +405,9 @@ fr_status fr_xent(const void *logits, const int64_t *target, float *loss, float 
     if (!aligned(workspace, 16)) return FR_ERR_MISALIGNED;
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return launched(fr::launch_xent(static_cast<const uint16_t *>(logits), target, loss, loss_mean,
-                                  target_logit, argmax, rows, cols, ld, ignore_index, workspace,
-                                  info.sm_count, info.max_smem_optin, s),
+  return launched(fr::launch_xent(logits, dtype == FR_F32, target, loss, loss_mean, target_logit,
+                                  argmax, rows, cols, ld, ignore_index, workspace, info.sm_count,
+                                  info.max_smem_optin, s),
                   FR_FORM_LOOPED);
 }
 

@@ -155,7 +155,7 @@ bool xent_recorded_config(int device, int64_t rows, int64_t cols, int64_t ld, Xe
 void xent_record_config(int device, int64_t rows, int64_t cols, int64_t ld,
                         const XentConfig *cfg);
 // The non-argmax kernel with configuration cfg.
-cudaError_t launch_xent_config(const XentConfig &cfg, const uint16_t *logits,
+cudaError_t launch_xent_config(const XentConfig &cfg, const void *logits,
                                const int64_t *target, float *loss, float *loss_mean,
                                float *target_logit, int64_t rows, int64_t cols, int64_t ld,
                                int64_t ignore_index, void *workspace, int sm_count,
@@ -163,7 +163,8 @@ cudaError_t launch_xent_config(const XentConfig &cfg, const uint16_t *logits,
 
 size_t xent_workspace(int64_t rows, int sm_count);
 cudaError_t launch_xent_mean_from_parts(const void *workspace, float *loss_mean, cudaStream_t s);
-cudaError_t launch_xent(const uint16_t *logits, const int64_t *target, float *loss,
+// f32: logits are fp32 (else bf16 bit patterns)
+cudaError_t launch_xent(const void *logits, bool f32, const int64_t *target, float *loss,
                         float *loss_mean, float *target_logit, int64_t *argmax, int64_t rows,
                         int64_t cols, int64_t ld, int64_t ignore_index, void *workspace,
                         int sm_count, int max_smem_optin, cudaStream_t s);

@@ -145,19 +145,21 @@ __device__ __forceinline__ void finish_mean(void *ws, float *loss_mean, double c
 }
 
 struct RowGeom {
-  const uint16_t *row;  // row start
-  uint64_t a0;          // first 16-byte boundary at or after the row start
-  uint32_t ibytes;      // interior bytes (multiple of 16)
-  int head;             // elements before a0
-  int tail;             // elements after the interior
+  const unsigned char *row;  // row start
+  uint64_t a0;               // first 16-byte boundary at or after the row start
+  uint32_t ibytes;           // interior bytes (multiple of 16)
+  int head;                  // elements before a0
+  int tail;                  // elements after the interior
 };
 
-__device__ __forceinline__ RowGeom row_geom(const uint16_t *logits, int64_t row, int64_t ld,
+// ES: bytes per logit (2 for bf16, 4 for fp32)
+template <int ES>
+__device__ __forceinline__ RowGeom row_geom(const void *logits, int64_t row, int64_t ld,
                                             int64_t cols) {
   RowGeom g;
-  g.row = logits + row * ld;
+  g.row = static_cast<const unsigned char *>(logits) + row * ld * ES;
   const uint64_t s0 = reinterpret_cast<uint64_t>(g.row);
-  const uint64_t s1 = s0 + 2 * static_cast<uint64_t>(cols);
+  const uint64_t s1 = s0 + ES * static_cast<uint64_t>(cols);
   const uint64_t a0 = (s0 + 15) & ~uint64_t(15), a1 = s1 & ~uint64_t(15);
   if (a1 <= a0) {  // a row too short to hold an aligned 16 bytes: all head
     g.a0 = s0;
@@ -168,9 +170,21 @@ __device__ __forceinline__ RowGeom row_geom(const uint16_t *logits, int64_t row,
   }
   g.a0 = a0;
   g.ibytes = static_cast<uint32_t>(a1 - a0);
-  g.head = static_cast<int>((a0 - s0) / 2);
-  g.tail = static_cast<int>((s1 - a1) / 2);
+  g.head = static_cast<int>((a0 - s0) / ES);
+  g.tail = static_cast<int>((s1 - a1) / ES);
   return g;
+}
+
+// Logit i of a row as fp32 (bf16 widened exactly), plain or streaming load.
+template <bool F32>
+__device__ __forceinline__ float logit_at(const unsigned char *row, int64_t i) {
+  if constexpr (F32) return reinterpret_cast<const float *>(row)[i];
+  else return bf16_to_f32(reinterpret_cast<const uint16_t *>(row)[i]);
+}
+template <bool F32>
+__device__ __forceinline__ float logit_stream(const unsigned char *row, int64_t i) {
+  if constexpr (F32) return ld_stream_f32(reinterpret_cast<const float *>(row) + i);
+  else return bf16_to_f32(ld_stream_u16(reinterpret_cast<const uint16_t *>(row) + i));
 }
 
 // ---- asynchronous-copy ring variant ---------------------------------------------
@@ -180,13 +194,15 @@ __device__ __forceinline__ RowGeom row_geom(const uint16_t *logits, int64_t row,
 // stages filled with cp.async (no registers held, one commit group per item),
 // continuing across row boundaries, so NS - 1 items per thread are always in
 // flight -- also while the CTA combines a finished row.
-template <bool ARGMAX, int T, int U, int NS>
+template <bool ARGMAX, int T, int U, int NS, bool F32 = false>
 __global__ void __launch_bounds__(T, 1)
-xent_async(const uint16_t *__restrict__ logits, const int64_t *__restrict__ target,
+xent_async(const void *__restrict__ logits, const int64_t *__restrict__ target,
            float *__restrict__ loss, float *__restrict__ target_logit,
            int64_t *__restrict__ argmax, float *__restrict__ loss_mean, void *__restrict__ ws,
            int64_t rows, int64_t cols, int64_t ld, int64_t ignore_index) {
   pdl_enter();
+  constexpr int ES = F32 ? 4 : 2;  // bytes per logit
+  constexpr int EPV = 16 / ES;     // logits per 16-byte vector
   extern __shared__ __align__(128) unsigned char smem[];  // [NS][U][T] x 16 bytes
   __shared__ MD red_md[2][T / 32];
   __shared__ ArgBest red_arg[2][T / 32];
@@ -204,7 +220,7 @@ xent_async(const uint16_t *__restrict__ logits, const int64_t *__restrict__ targ
   RowGeom pg{};
   auto load_row = [&]() {
     for (; pk < nk; ++pk) {
-      pg = row_geom(logits, blockIdx.x + pk * G, ld, cols);
+      pg = row_geom<ES>(logits, blockIdx.x + pk * G, ld, cols);
       pn = static_cast<int>((pg.ibytes / 16 + T * U - 1) / (T * U));
       if (pn > 0) return;
     }
@@ -239,12 +255,12 @@ xent_async(const uint16_t *__restrict__ logits, const int64_t *__restrict__ targ
   int parity = 0;
   for (int64_t k = 0; k < nk; ++k, parity ^= 1) {
     const int64_t row = blockIdx.x + k * G;
-    const RowGeom g = row_geom(logits, row, ld, cols);
+    const RowGeom g = row_geom<ES>(logits, row, ld, cols);
     int64_t t = 0;
-    uint16_t xt_bits = 0;
+    float xt_v = 0.0f;
     if (tid == 0) {
       t = t_next;
-      if (t >= 0 && t < cols) xt_bits = g.row[t];
+      if (t >= 0 && t < cols) xt_v = logit_at<F32>(g.row, t);
       if (k + 1 < nk) t_next = target[row + G];
     }
     const int nv = static_cast<int>(g.ibytes / 16);
@@ -254,21 +270,33 @@ xent_async(const uint16_t *__restrict__ logits, const int64_t *__restrict__ targ
     for (int c = 0; c < nitems; ++c) {
       produce();                 // keep NS - 1 items in flight
       cp_async_wait<NS - 1>();   // this thread's copies of item (k, c) landed
+      // a vector past the interior holds -inf (adds nothing)
+      constexpr uint32_t kNegInf = F32 ? 0xFF800000u : 0xFF80FF80u;
       uint32_t wv[U][4];
-      uint32_t m2 = 0xFF80FF80u;
+      uint32_t m2 = kNegInf;  // bf16: running max of bf16 pairs
+      float mf = -INFINITY;   // fp32: running max
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int v = c * T * U + u * T + tid;
         if (v < nv) {
           const uint4 q = lds_u4(slot(cs, u));
           wv[u][0] = q.x; wv[u][1] = q.y; wv[u][2] = q.z; wv[u][3] = q.w;
-          m2 = max_nan_bf16x2(m2, max_nan_bf16x2(max_nan_bf16x2(q.x, q.y), max_nan_bf16x2(q.z, q.w)));
+          if constexpr (F32)
+            mf = max_nan(max_nan(mf, max_nan(__uint_as_float(q.x), __uint_as_float(q.y))),
+                         max_nan(__uint_as_float(q.z), __uint_as_float(q.w)));
+          else
+            m2 = max_nan_bf16x2(m2, max_nan_bf16x2(max_nan_bf16x2(q.x, q.y), max_nan_bf16x2(q.z, q.w)));
         } else {
-          wv[u][0] = wv[u][1] = wv[u][2] = wv[u][3] = 0xFF80FF80u;  // -inf: adds nothing
+          wv[u][0] = wv[u][1] = wv[u][2] = wv[u][3] = kNegInf;
         }
       }
       cs = cs + 1 == NS ? 0 : cs + 1;
-      const float cm = max_nan(bf16_lo(m2), bf16_hi(m2));
+      const float cm = F32 ? mf : max_nan(bf16_lo(m2), bf16_hi(m2));
+      // logit j (0 .. EPV - 1) of vector u
+      auto elem = [&](int u, int j) {
+        if constexpr (F32) return __uint_as_float(wv[u][j]);
+        else return (j & 1) ? bf16_hi(wv[u][j >> 1]) : bf16_lo(wv[u][j >> 1]);
+      };
       if constexpr (ARGMAX) {
         if (best.i == INT64_MAX || cm > best.v || (cm != cm && best.v == best.v)) {
           bool found = false;
@@ -276,12 +304,12 @@ xent_async(const uint16_t *__restrict__ logits, const int64_t *__restrict__ targ
           for (int u = 0; u < U; ++u) {
             const int v = c * T * U + u * T + tid;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float e = (j & 1) ? bf16_hi(wv[u][j >> 1]) : bf16_lo(wv[u][j >> 1]);
+            for (int j = 0; j < EPV; ++j) {
+              const float e = elem(u, j);
               const bool hit = (cm != cm) ? (e != e) : (e == cm);
               if (!found && hit && v < nv) {
                 found = true;
-                best = ArgBest{cm, g.head + 8 * static_cast<int64_t>(v) + j};
+                best = ArgBest{cm, g.head + EPV * static_cast<int64_t>(v) + j};
               }
             }
           }
@@ -295,9 +323,8 @@ xent_async(const uint16_t *__restrict__ logits, const int64_t *__restrict__ targ
 #pragma unroll
         for (int u = 0; u < U; ++u)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint64_t t2 =
-                fma_f32x2(pack_f32x2(bf16_lo(wv[u][j]), bf16_hi(wv[u][j])), l2e2, nmb2);
+          for (int j = 0; j < EPV / 2; ++j) {  // a pair of logits per step
+            const uint64_t t2 = fma_f32x2(pack_f32x2(elem(u, 2 * j), elem(u, 2 * j + 1)), l2e2, nmb2);
             acc2 = add_f32x2(acc2, pack_f32x2(ex2(f32x2_lo(t2)), ex2(f32x2_hi(t2))));
           }
         st.d += f32x2_lo(acc2) + f32x2_hi(acc2);
@@ -305,9 +332,9 @@ xent_async(const uint16_t *__restrict__ logits, const int64_t *__restrict__ targ
     }
     int64_t si = -1;
     if (tid < g.head) si = tid;
-    else if (tid < g.head + g.tail) si = g.head + g.ibytes / 2 + (tid - g.head);
+    else if (tid < g.head + g.tail) si = g.head + g.ibytes / ES + (tid - g.head);
     if (si >= 0) {
-      const float e = bf16_to_f32(ld_stream_u16(g.row + si));
+      const float e = logit_stream<F32>(g.row, si);
       st = md_merge(st, MD{e, 1.0f});
       if constexpr (ARGMAX) best = arg_better(best, ArgBest{e, si});
     }
@@ -351,7 +378,7 @@ xent_async(const uint16_t *__restrict__ logits, const int64_t *__restrict__ targ
           xt = l;
           atomicCAS(&g_fr_device_error, 0, FR_DEVERR_BAD_TARGET);
         } else {
-          xt = bf16_to_f32(xt_bits);
+          xt = xt_v;
           l = lse - xt;
         }
         if (loss) loss[row] = l;
@@ -475,7 +502,7 @@ cudaError_t capped_smem(size_t need, int per_sm, size_t *out) {
   return cudaSuccess;
 }
 
-cudaError_t launch_xent_config(const XentConfig &cfg, const uint16_t *logits,
+cudaError_t launch_xent_config(const XentConfig &cfg, const void *logits,
                                const int64_t *target, float *loss, float *loss_mean,
                                float *target_logit, int64_t rows, int64_t cols, int64_t ld,
                                int64_t ignore_index, void *workspace, int sm_count,
@@ -524,18 +551,20 @@ void xent_record_config(int device, int64_t rows, int64_t cols, int64_t ld,
   if (cfg) g_recorded.push_back(Recorded{device, rows, cols, ld, *cfg});
 }
 
-// The argmax kernel at the default point of the box (up to its CTAs per SM
-// when the larger argmax kernel keeps fewer resident).
-cudaError_t launch_xent_argmax_default(const uint16_t *logits, const int64_t *target, float *loss,
-                                       float *loss_mean, float *target_logit, int64_t *argmax,
-                                       int64_t rows, int64_t cols, int64_t ld,
-                                       int64_t ignore_index, void *workspace, int sm_count,
-                                       cudaStream_t s) {
+// The kernel at the default point of the box, for the launches the box's
+// table does not cover: with argmax (bf16 or fp32 logits) and fp32 logits
+// without it.  Up to the default's CTAs per SM (fewer when the larger
+// argmax kernel keeps fewer resident).
+template <bool ARGMAX, bool F32>
+cudaError_t launch_xent_default(const void *logits, const int64_t *target, float *loss,
+                                float *loss_mean, float *target_logit, int64_t *argmax,
+                                int64_t rows, int64_t cols, int64_t ld, int64_t ignore_index,
+                                void *workspace, int sm_count, cudaStream_t s) {
   constexpr int T = 128, U = 8, NS = 2;
   const XentConfig d = xent_default_config();
   static_assert(T == 128 && U == 8 && NS == 2, "keep in step with xent_default_config()");
   if (d.threads != T || d.vectors != U || d.stages != NS) return cudaErrorInvalidValue;
-  const void *kern = reinterpret_cast<const void *>(&xent_async<true, T, U, NS>);
+  const void *kern = reinterpret_cast<const void *>(&xent_async<ARGMAX, T, U, NS, F32>);
   const size_t smem = static_cast<size_t>(NS) * U * T * 16;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
@@ -561,13 +590,21 @@ cudaError_t launch_xent_argmax_default(const uint16_t *logits, const int64_t *ta
   return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(T), args, smem_cap, s);
 }
 
-cudaError_t launch_xent(const uint16_t *logits, const int64_t *target, float *loss,
+cudaError_t launch_xent(const void *logits, bool f32, const int64_t *target, float *loss,
                         float *loss_mean, float *target_logit, int64_t *argmax, int64_t rows,
                         int64_t cols, int64_t ld, int64_t ignore_index, void *workspace,
                         int sm_count, int max_smem_optin, cudaStream_t s) {
+  if (f32)  // fp32 logits: the default point of the box
+    return argmax != nullptr
+               ? launch_xent_default<true, true>(logits, target, loss, loss_mean, target_logit,
+                                                 argmax, rows, cols, ld, ignore_index, workspace,
+                                                 sm_count, s)
+               : launch_xent_default<false, true>(logits, target, loss, loss_mean, target_logit,
+                                                  argmax, rows, cols, ld, ignore_index, workspace,
+                                                  sm_count, s);
   if (argmax != nullptr)
-    return launch_xent_argmax_default(logits, target, loss, loss_mean, target_logit, argmax, rows,
-                                      cols, ld, ignore_index, workspace, sm_count, s);
+    return launch_xent_default<true, false>(logits, target, loss, loss_mean, target_logit, argmax,
+                                            rows, cols, ld, ignore_index, workspace, sm_count, s);
   // the configuration recorded for this shape (fr_xent_tune / _set_config),
   // else the default point of the box
   int dev = 0;

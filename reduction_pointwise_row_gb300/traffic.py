@@ -38,4 +38,6 @@ def algorithmic_bytes(op: str, rows: int, cols: int, **kw) -> int:
         return 2 * rows * cols * 2 + 2 * cols * 4 + 2 * rows * 4
     if op == "xent":                  # logits bf16, targets int64, loss fp32 [rows], mean fp32
         return rows * cols * 2 + rows * 8 + rows * 4 + 4
+    if op == "xent_f32":              # the same with fp32 logits
+        return rows * cols * 4 + rows * 8 + rows * 4 + 4
     raise ValueError(op)

@@ -125,3 +125,15 @@ def make_softmax_bf16(rows: int, cols: int, seed: int | None = None) -> Workload
     w = Workload(name=f"softmax bf16 [{rows},{cols}]", op="softmax", rows=rows, cols=cols)
     w.arrays["x"] = normal_bf16((rows, cols), s, 0, 0.0, 4.0)
     return w
+
+
+def make_xent_f32(rows: int, cols: int, seed: int | None = None) -> Workload:
+    """The cross-entropy workload's recipe with fp32 logits: 3 * N(0, 1) in
+    fp32 (not rounded to bf16), targets uniform with 5 % ignored."""
+    s = SEED_BASE + 7 if seed is None else seed
+    w = Workload(name=f"cross entropy fp32 logits [{rows},{cols}]", op="xent", rows=rows,
+                 cols=cols)
+    w.arrays["logits"] = normal_f32((rows, cols), s, 0, 0.0, 3.0)
+    w.arrays["target"] = targets(rows, cols, int(round(0.05 * rows)), IGNORE_INDEX, s, 1)
+    w.params["ignore_index"] = IGNORE_INDEX
+    return w

@@ -125,7 +125,10 @@ def test_argument_validation_needs_no_device():
     assert lib.fr_layernorm(odd, good, good, good, None, None, 4, 8, 8, 8, 1e-5, 1, 0, None) == 4
     # xent
     assert lib.fr_xent(good, None, None, None, None, None, 4, 8, 8, -100, 1, 0, None, 0, None) == 1
-    assert lib.fr_xent(good, good, None, None, None, None, 4, 8, 8, -100, 0, 0, None, 0, None) == 2
+    assert lib.fr_xent(good, good, None, None, None, None, 4, 8, 8, -100, 2, 0, None, 0, None) == 2
+    # fp32 logits must be 4-byte aligned (bf16 ones 2-byte)
+    assert lib.fr_xent(P(0x10002), good, None, None, None, None, 4, 8, 8, -100, 0, 0, None, 0,
+                       None) == 4
     assert lib.fr_xent(good, P(0x10004), None, None, None, None, 4, 8, 8, -100, 1, 0, None, 0,
                        None) == 4
     assert lib.fr_xent(good, good, None, None, None, None, 4, 8, 8, -100, 1, 3, None, 0, None) == 3

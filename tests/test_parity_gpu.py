@@ -371,6 +371,40 @@ def test_xent(o, rows, cols, layout):
     assert fr.fr_check_device_error() == 0
 
 
+@pytest.mark.parametrize("cols", [1, 2, 3, 5, 7, 13, 33, 128, 129, 1000, 4097, 50257])
+@pytest.mark.parametrize("rows", [1, 7, 65])
+@pytest.mark.parametrize("layout", [(0, 0), (1, 0), (3, 5)], ids=["base0", "base1", "base3_pad5"])
+def test_xent_f32_logits(o, rows, cols, layout):
+    """fp32 logits: every output against the oracle on the same fp32 values."""
+    w = workloads.make_xent_f32(rows, cols, seed=4500 + rows * 7 + cols)
+    ref = o.xent(w.arrays["logits"], w.arrays["target"], -100)
+    for argmax in (True, False):
+        got = run_xent(w.arrays["logits"], w.arrays["target"], -100, *layout, argmax=argmax)
+        check_xent(got, ref, f"f32 argmax={argmax} {rows}x{cols} {layout}")
+    assert fr.fr_check_device_error() == 0
+
+
+def test_xent_f32_ties_nan_and_bad_targets(o):
+    rng = np.random.default_rng(6)
+    rows, cols = 40, 3001
+    x = rng.integers(-3, 4, (rows, cols)).astype(np.float32)  # many ties
+    one_up = np.nextafter(np.float32(3.0), np.float32(4.0))
+    x[4, 2000] = one_up             # one fp32 step above the ties: the maximum
+    x[5, 17] = np.nan
+    x[6, [3, 2999]] = np.nan        # two NaNs: first wins
+    x[7, :] = -np.inf
+    t = rng.integers(0, cols, rows)
+    t[[1, 2, 3]] = -100
+    t[9] = cols                     # out of range
+    ref = o.xent(x, t, -100)
+    for offset in (0, 1):
+        got = run_xent(x, t, -100, offset=offset)
+        check_xent(got, ref, f"f32 ties/nan offset {offset}")
+        assert got["argmax"][4] == 2000 and got["argmax"][5] == 17 and got["argmax"][6] == 3
+        assert np.isnan(got["loss"][9])
+        assert fr.fr_check_device_error() == 1
+
+
 def test_xent_ties_nan_and_ignore(o):
     rng = np.random.default_rng(5)
     rows, cols = 40, 3001
