@@ -52,7 +52,8 @@ def parse():
     p.add_argument("--only", choices=["relu_add_sum", "softmax", "layernorm", "split", "xent",
                                       "sumsq", "l2norm", "softmax_4097", "softmax_4097_looped",
                                       "softmax_65537", "softmax_65537_looped",
-                                      "looped", "softmax_bf16", "xent_f32", "xent_box"],
+                                      "looped", "looped_bf16", "softmax_bf16", "xent_f32",
+                                      "xent_box"],
                    help="time one workload alone (for profiler captures) and exit")
     p.add_argument("--form", default="auto", choices=["auto", "persistent", "looped", "split"],
                    help="with --only: force a reduction form")
@@ -403,6 +404,15 @@ def setup_workload(name, fr, workloads, dev, form="auto"):
         out = torch.empty(w.rows, device=dev)
         calls.append(lambda: fr.fr_reduce_relu_add_sum(a, b, 2.0, out=out, form=form))
         return calls, "relu_add_sum", w.rows, w.cols, 1
+    if name == "looped_bf16":
+        # the same in bf16: 16384 x 16384 (1 GiB of a and b), rounded from
+        # Example 1.1's U(-1, 1) inputs
+        w = make_shard(workloads, 0, rows=16384, cols=16384)
+        a = torch.from_numpy(w.arrays["a"]).to(dev).to(torch.bfloat16)
+        b = torch.from_numpy(w.arrays["b"]).to(dev).to(torch.bfloat16)
+        out = torch.empty(w.rows, device=dev)
+        calls.append(lambda: fr.fr_reduce_relu_add_sum(a, b, 2.0, out=out, form=form))
+        return calls, "relu_add_sum_bf16", w.rows, w.cols, 1
     if name == "layernorm":
         w = make_shard(workloads, 2)
         g, bt = to_device(w.arrays["gamma"], dev), to_device(w.arrays["beta"], dev)
@@ -480,7 +490,7 @@ EXTRA = {"relu_add_sum": "relu_add_sum_64x128", "layernorm": "layernorm_4096x327
          "softmax_4097": "softmax_8190x4097", "softmax_4097_looped": "softmax_looped_8190x4097",
          "softmax_65537": "softmax_511x65537", "softmax_65537_looped": "softmax_looped_511x65537",
          "looped": "relu_add_sum_looped_16384x8192", "softmax_bf16": "softmax_bf16_65536x1024",
-         "xent_f32": "xent_f32_8192x50257"}
+         "xent_f32": "xent_f32_8192x50257", "looped_bf16": "relu_add_sum_bf16_looped_16384x16384"}
 
 
 def extra_configs(fr, traffic, workloads, timed, dev, peak, args, world, names=None,

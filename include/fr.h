@@ -113,9 +113,11 @@ size_t fr_workspace_size(fr_op op, int64_t rows, int64_t cols, fr_dtype dtype, f
  * workspace, stage 2 sums them in a fixed order; results are bitwise
  * run-to-run deterministic for a given shape).
  *
- *   a, b       fp32 [rows, lda] / [rows, ldb] device inputs (read only)
+ *   a, b       [rows, lda] / [rows, ldb] device inputs of `dtype` (read only)
  *   out        fp32 [rows] device output
- *   dtype      FR_F32 (the only dtype offered)
+ *   dtype      FR_F32, or FR_BF16 (bit patterns, widened exactly to fp32
+ *              before the sum; the persistent form then holds rows of up
+ *              to 2048 columns instead of 1024)
  *   workspace  device scratch of fr_workspace_size(FR_OP_RELU_ADD_SUM, ...)
  *              bytes (only the split form uses it; may be NULL otherwise)
  */

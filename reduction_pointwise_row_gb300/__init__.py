@@ -171,16 +171,19 @@ def _workspace(op, rows, cols, dtype, form, device, given=None):
 
 def fr_reduce_relu_add_sum(a, b, scale: float = 2.0, form: str = "auto", out=None,
                            workspace=None, stream=None):
-    """out[x] = sum_r scale * relu(a[x, r] + b[x, r]) (fp32 in, fp32 out)."""
+    """out[x] = sum_r scale * relu(a[x, r] + b[x, r]) (fp32 or bf16 in, fp32 out;
+    bf16 inputs are widened exactly to fp32 before the sum)."""
     import torch
-    assert a.is_cuda and b.is_cuda and a.dtype == torch.float32 and b.dtype == torch.float32
+    assert a.is_cuda and b.is_cuda and a.dtype == b.dtype
+    assert a.dtype in (torch.float32, torch.bfloat16)
     assert a.shape == b.shape and a.dim() == 2
+    dt = "f32" if a.dtype == torch.float32 else "bf16"
     rows, cols = a.shape
     if out is None:
         out = torch.empty(rows, dtype=torch.float32, device=a.device)
-    ws, nws = _workspace("relu_add_sum", rows, cols, "f32", form, a.device, workspace)
+    ws, nws = _workspace("relu_add_sum", rows, cols, dt, form, a.device, workspace)
     _check(lib().fr_reduce_relu_add_sum(_ptr(a), _ptr(b), _ptr(out), rows, cols, _ld(a), _ld(b),
-                                        DTYPES["f32"], scale, FORMS[form], _ptr(ws), nws,
+                                        DTYPES[dt], scale, FORMS[form], _ptr(ws), nws,
                                         _stream(stream)), "fr_reduce_relu_add_sum")
     return out
 

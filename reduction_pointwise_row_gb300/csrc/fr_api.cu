@@ -90,8 +90,8 @@ fr_status launched(cudaError_t e, fr_form form) {
 // fit one warp's registers take the persistent form; few long rows that
 // cannot fill the SMs one warp per row take the split form.
 
-fr_form pick_ras(int64_t rows, int64_t cols, int sm_count) {
-  if (cols <= fr::ras_persistent_max_cols()) return FR_FORM_PERSISTENT;
+fr_form pick_ras(int64_t rows, int64_t cols, int sm_count, bool bf16 = false) {
+  if (cols <= fr::ras_persistent_max_cols(bf16)) return FR_FORM_PERSISTENT;
   if (rows < static_cast<int64_t>(sm_count) * 32 && cols >= 16384) return FR_FORM_SPLIT;
   return FR_FORM_LOOPED;
 }
@@ -143,13 +143,13 @@ const char *fr_status_string(fr_status s) {
 fr_form fr_last_form(void) { return g_last_form; }
 
 size_t fr_workspace_size(fr_op op, int64_t rows, int64_t cols, fr_dtype dtype, fr_form form) {
-  (void)dtype;
   if (rows < 1 || cols < 1) return 0;
   fr::DevInfo info;
   if (fr::current_device_info(&info) != cudaSuccess) return 0;
   switch (op) {
     case FR_OP_RELU_ADD_SUM: {
-      const fr_form f = form == FR_FORM_AUTO ? pick_ras(rows, cols, info.sm_count) : form;
+      const fr_form f =
+          form == FR_FORM_AUTO ? pick_ras(rows, cols, info.sm_count, dtype == FR_BF16) : form;
       return f == FR_FORM_SPLIT ? fr::ras_split_workspace(rows, cols, info.sm_count) : 0;
     }
     case FR_OP_SUMSQ: {
@@ -165,30 +165,33 @@ fr_status fr_reduce_relu_add_sum(const void *a, const void *b, float *out, int64
                                  int64_t cols, int64_t lda, int64_t ldb, fr_dtype dtype,
                                  float scale, fr_form form, void *workspace,
                                  size_t workspace_bytes, fr_stream_t stream) {
-  if (dtype != FR_F32) return FR_ERR_UNSUPPORTED_DTYPE;
+  if (dtype != FR_F32 && dtype != FR_BF16) return FR_ERR_UNSUPPORTED_DTYPE;
+  const bool bf16 = dtype == FR_BF16;
+  const int64_t es = bf16 ? 2 : 4;
   if (!a || !b || !out) return FR_ERR_INVALID_ARG;
-  if (!shape_ok(rows, cols, lda, 4) || !shape_ok(rows, cols, ldb, 4)) return FR_ERR_INVALID_ARG;
-  if (!aligned(a, 4) || !aligned(b, 4) || !aligned(out, 4)) return FR_ERR_MISALIGNED;
+  if (!shape_ok(rows, cols, lda, es) || !shape_ok(rows, cols, ldb, es)) return FR_ERR_INVALID_ARG;
+  if (!aligned(a, es) || !aligned(b, es) || !aligned(out, 4)) return FR_ERR_MISALIGNED;
   fr::DevInfo info;
   if (fr_status st = device_ok(&info)) return st;
-  const fr_form f = form == FR_FORM_AUTO ? pick_ras(rows, cols, info.sm_count) : form;
-  const bool vec = same_phase(a, lda, b, ldb, 4);
-  const float *fa = static_cast<const float *>(a);
-  const float *fb = static_cast<const float *>(b);
+  const fr_form f = form == FR_FORM_AUTO ? pick_ras(rows, cols, info.sm_count, bf16) : form;
+  const bool vec = same_phase(a, lda, b, ldb, es);
+  const void *fa = a, *fb = b;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   switch (f) {
     case FR_FORM_PERSISTENT:
-      if (cols > fr::ras_persistent_max_cols()) return FR_ERR_UNSUPPORTED_FORM;
-      return launched(fr::launch_ras_persistent(fa, fb, out, rows, cols, lda, ldb, scale, vec, s), f);
+      if (cols > fr::ras_persistent_max_cols(bf16)) return FR_ERR_UNSUPPORTED_FORM;
+      return launched(fr::launch_ras_persistent(fa, fb, out, rows, cols, lda, ldb, scale, bf16,
+                                                vec, s), f);
     case FR_FORM_LOOPED:
-      return launched(fr::launch_ras_looped(fa, fb, out, rows, cols, lda, ldb, scale, vec, s), f);
+      return launched(fr::launch_ras_looped(fa, fb, out, rows, cols, lda, ldb, scale, bf16, vec,
+                                            s), f);
     case FR_FORM_SPLIT: {
       if (rows > 65535) return FR_ERR_UNSUPPORTED_FORM;
       const size_t need = fr::ras_split_workspace(rows, cols, info.sm_count);
       if (!workspace || workspace_bytes < need) return FR_ERR_WORKSPACE_TOO_SMALL;
       if (!aligned(workspace, 16)) return FR_ERR_MISALIGNED;
       const int segs = fr::ras_split_segments(rows, cols, info.sm_count);
-      return launched(fr::launch_ras_split(fa, fb, out, rows, cols, lda, ldb, scale, vec,
+      return launched(fr::launch_ras_split(fa, fb, out, rows, cols, lda, ldb, scale, bf16, vec,
                                            static_cast<double *>(workspace), segs, s), f);
     }
     default: return FR_ERR_UNSUPPORTED_FORM;

@@ -21,20 +21,21 @@ cudaError_t current_device_info(DevInfo *out);
 // ---- Example 1.1: out[x] = sum_r scale * relu(a + b) ------------------------
 
 // Largest row (elements) the persistent form holds in one pass.
-int64_t ras_persistent_max_cols();
+int64_t ras_persistent_max_cols(bool bf16 = false);
 // Segments per row of the split form for this shape (fixed per device model).
 int ras_split_segments(int64_t rows, int64_t cols, int sm_count);
 size_t ras_split_workspace(int64_t rows, int64_t cols, int sm_count);
 
-cudaError_t launch_ras_persistent(const float *a, const float *b, float *out, int64_t rows,
-                                  int64_t cols, int64_t lda, int64_t ldb, float scale,
+// a, b: fp32, or bf16 bit patterns when bf16 (widened exactly before the sum)
+cudaError_t launch_ras_persistent(const void *a, const void *b, float *out, int64_t rows,
+                                  int64_t cols, int64_t lda, int64_t ldb, float scale, bool bf16,
                                   bool vec, cudaStream_t s);
-cudaError_t launch_ras_looped(const float *a, const float *b, float *out, int64_t rows,
-                              int64_t cols, int64_t lda, int64_t ldb, float scale, bool vec,
-                              cudaStream_t s);
-cudaError_t launch_ras_split(const float *a, const float *b, float *out, int64_t rows,
-                             int64_t cols, int64_t lda, int64_t ldb, float scale, bool vec,
-                             double *partials, int segments, cudaStream_t s);
+cudaError_t launch_ras_looped(const void *a, const void *b, float *out, int64_t rows,
+                              int64_t cols, int64_t lda, int64_t ldb, float scale, bool bf16,
+                              bool vec, cudaStream_t s);
+cudaError_t launch_ras_split(const void *a, const void *b, float *out, int64_t rows,
+                             int64_t cols, int64_t lda, int64_t ldb, float scale, bool bf16,
+                             bool vec, double *partials, int segments, cudaStream_t s);
 
 // ---- Example 6.2 and its L2-norm epilogue: out[x] = (sqrt) sum_r x^2 ------
 // Same forms, segment rule and workspace as above.

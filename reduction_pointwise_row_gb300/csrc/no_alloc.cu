@@ -79,9 +79,7 @@ extern "C" fr_status fr_reduce_relu_add_sum_split_static(const void *a, const vo
   const int64_t d = static_cast<int64_t>(reinterpret_cast<uintptr_t>(a)) -
                     static_cast<int64_t>(reinterpret_cast<uintptr_t>(b));
   const bool vec = (d % 32 == 0) && (((lda - ldb) * 4) % 32 == 0);
-  cudaError_t e = fr::launch_ras_split(static_cast<const float *>(a),
-                                       static_cast<const float *>(b), out, rows, cols, lda, ldb,
-                                       scale, vec, scratch, segments,
-                                       reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = fr::launch_ras_split(a, b, out, rows, cols, lda, ldb, scale, false, vec,
+                                       scratch, segments, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FR_OK : FR_ERR_CUDA;
 }

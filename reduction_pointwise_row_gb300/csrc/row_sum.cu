@@ -49,21 +49,42 @@ struct Square {
   __device__ __forceinline__ float operator()(float x, float) const { return x * x; }
 };
 
-template <class Op>
-__device__ __forceinline__ float term_at(const Op &op, const float *pa, const float *pb,
-                                         int64_t i) {
-  if constexpr (Op::kTwoInputs) return op(ld_stream_f32(pa + i), ld_stream_f32(pb + i));
-  else return op(ld_stream_f32(pa + i), 0.0f);
+// Input element types: fp32, or bf16 widened exactly to fp32 before the
+// prologue (Listing 9.1 loads then computes in fp32).
+struct F32In {
+  using T = float;
+  static constexpr int kES = 4;
+  static constexpr int kN = 8;  // elements per 32-byte vector
+  __device__ __forceinline__ static float at(const T *p, int64_t i) { return ld_stream_f32(p + i); }
+  // value j (0 .. kN - 1) of a 32-byte vector
+  __device__ __forceinline__ static float lane(const V8 &v, int j) { return __uint_as_float(v.w[j]); }
+};
+struct Bf16In {
+  using T = uint16_t;
+  static constexpr int kES = 2;
+  static constexpr int kN = 16;
+  __device__ __forceinline__ static float at(const T *p, int64_t i) { return bf16_to_f32(ld_stream_u16(p + i)); }
+  __device__ __forceinline__ static float lane(const V8 &v, int j) {
+    return (j & 1) ? bf16_hi(v.w[j >> 1]) : bf16_lo(v.w[j >> 1]);
+  }
+};
+
+template <class Op, class In>
+__device__ __forceinline__ float term_at(const Op &op, const typename In::T *pa,
+                                         const typename In::T *pb, int64_t i) {
+  if constexpr (Op::kTwoInputs) return op(In::at(pa, i), In::at(pb, i));
+  else return op(In::at(pa, i), 0.0f);
 }
 
 // N 32-byte vectors of each input in flight per thread (one-input prologues
 // hold no second array).
-template <class Op, int N>
+template <class Op, class In, int N>
 struct VecBuf {
   V8 a[N];
   V8 b[Op::kTwoInputs ? N : 1];
 
-  __device__ __forceinline__ void load(int k, const float *pa, const float *pb, int64_t off) {
+  __device__ __forceinline__ void load(int k, const typename In::T *pa,
+                                       const typename In::T *pb, int64_t off) {
     a[k] = ld_stream_v8(pa + off);
     if constexpr (Op::kTwoInputs) b[k] = ld_stream_v8(pb + off);
   }
@@ -72,10 +93,10 @@ struct VecBuf {
     float t = 0.0f;
     if constexpr (Op::kTwoInputs) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) t += op(__uint_as_float(a[k].w[j]), __uint_as_float(b[k].w[j]));
+      for (int j = 0; j < In::kN; ++j) t += op(In::lane(a[k], j), In::lane(b[k], j));
     } else {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) t += op(__uint_as_float(a[k].w[j]), 0.0f);
+      for (int j = 0; j < In::kN; ++j) t += op(In::lane(a[k], j), 0.0f);
     }
     return t;
   }
@@ -90,41 +111,43 @@ __device__ __forceinline__ float finish(double acc) {
 // Warp-per-row form.  VEC: the input rows share their offset modulo 32 bytes,
 // so one head/body/tail split serves both; otherwise every element is a
 // scalar (still coalesced: lane-strided).  b is unused by one-input prologues.
-template <class Op, bool VEC, bool LOOP, bool SQRT>
+template <class Op, class In, bool VEC, bool LOOP, bool SQRT>
 __global__ void __launch_bounds__(kRowThreads)
-rowsum_warp(const float *__restrict__ a, const float *__restrict__ b, float *__restrict__ out,
-            int64_t rows, int64_t cols, int64_t lda, int64_t ldb, Op op) {
+rowsum_warp(const typename In::T *__restrict__ a, const typename In::T *__restrict__ b,
+            float *__restrict__ out, int64_t rows, int64_t cols, int64_t lda, int64_t ldb, Op op) {
   pdl_enter();
+  using E = typename In::T;
+  constexpr int EPV = In::kN;
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (kRowThreads / 32) + (threadIdx.x >> 5);
   if (row >= rows) return;
-  const float *pa = a + row * lda;
-  const float *pb = Op::kTwoInputs ? b + row * ldb : nullptr;
+  const E *pa = a + row * lda;
+  const E *pb = Op::kTwoInputs ? b + row * ldb : nullptr;
   double acc = 0.0;
   if constexpr (VEC) {
-    const RowSplit sp = row_split(pa, cols, 4);
-    float s = 0.0f;  // head and tail: at most 7 + 7 scalars, one per lane
+    const RowSplit sp = row_split(pa, cols, In::kES);
+    float s = 0.0f;  // head and tail: fewer than 16 scalars each, one per lane
     if (lane < sp.head) {
-      s = term_at(op, pa, pb, lane);
+      s = term_at<Op, In>(op, pa, pb, lane);
     } else if (lane < sp.head + sp.tail) {
-      s = term_at(op, pa, pb, sp.head + sp.nvec * 8 + (lane - sp.head));
+      s = term_at<Op, In>(op, pa, pb, sp.head + sp.nvec * EPV + (lane - sp.head));
     }
     acc = s;
-    const float *va = pa + sp.head;
-    const float *vb = Op::kTwoInputs ? pb + sp.head : nullptr;
-    for (int64_t base = 0; base < sp.nvec; base += 32 * kPersistNV) {
-      VecBuf<Op, kPersistNV> buf;
+    const E *va = pa + sp.head;
+    const E *vb = Op::kTwoInputs ? pb + sp.head : nullptr;
+    // persistent: the row's vectors fit one pass (base 0 only)
+    for (int64_t base = 0; base < (LOOP ? sp.nvec : 1); base += 32 * kPersistNV) {
+      VecBuf<Op, In, kPersistNV> buf;
 #pragma unroll
       for (int k = 0; k < kPersistNV; ++k) {
         const int64_t vi = base + lane + 32 * k;
-        if (vi < sp.nvec) buf.load(k, va, vb, vi * 8);
+        if (vi < sp.nvec) buf.load(k, va, vb, vi * EPV);
       }
       float t = 0.0f;
 #pragma unroll
       for (int k = 0; k < kPersistNV; ++k)
         if (base + lane + 32 * k < sp.nvec) t += buf.terms(k, op);
       acc += static_cast<double>(t);
-      if constexpr (!LOOP) break;
     }
   } else {
     for (int64_t base = 0; base < cols; base += 32 * 8) {
@@ -132,11 +155,11 @@ rowsum_warp(const float *__restrict__ a, const float *__restrict__ b, float *__r
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const int64_t i = base + lane + 32 * k;
-        if (i < cols) t += term_at(op, pa, pb, i);
+        if (i < cols) t += term_at<Op, In>(op, pa, pb, i);
       }
       acc += static_cast<double>(t);
       if constexpr (!LOOP) {
-        if (base + 32 * 8 >= 1024) break;
+        if (base + 32 * 8 >= 32 * EPV * kPersistNV) break;  // the persistent form's row cap
       }
     }
   }
@@ -146,30 +169,33 @@ rowsum_warp(const float *__restrict__ a, const float *__restrict__ b, float *__r
 
 // Split form, stage 1: CTA (seg, row) sums its segment of the row's body
 // vectors (segment 0 also takes the head scalars, the last segment the tail).
-template <class Op, bool VEC>
+template <class Op, class In, bool VEC>
 __global__ void __launch_bounds__(kSplitThreads)
-rowsum_split_stage1(const float *__restrict__ a, const float *__restrict__ b, int64_t cols,
-                    int64_t lda, int64_t ldb, Op op, double *__restrict__ partials, int S) {
+rowsum_split_stage1(const typename In::T *__restrict__ a, const typename In::T *__restrict__ b,
+                    int64_t cols, int64_t lda, int64_t ldb, Op op, double *__restrict__ partials,
+                    int S) {
   pdl_enter();
+  using E = typename In::T;
+  constexpr int EPV = In::kN;
   const int seg = blockIdx.x;
   const int64_t row = blockIdx.y;
   const int tid = threadIdx.x;
-  const float *pa = a + row * lda;
-  const float *pb = Op::kTwoInputs ? b + row * ldb : nullptr;
-  const RowSplit sp = VEC ? row_split(pa, cols, 4) : RowSplit{0, cols, 0};
+  const E *pa = a + row * lda;
+  const E *pb = Op::kTwoInputs ? b + row * ldb : nullptr;
+  const RowSplit sp = VEC ? row_split(pa, cols, In::kES) : RowSplit{0, cols, 0};
   const int64_t per = (sp.nvec + S - 1) / S;
   const int64_t lo = seg * per;
   const int64_t hi = lo + per < sp.nvec ? lo + per : sp.nvec;
   double acc = 0.0;
   if constexpr (VEC) {
-    const float *va = pa + sp.head;
-    const float *vb = Op::kTwoInputs ? pb + sp.head : nullptr;
+    const E *va = pa + sp.head;
+    const E *vb = Op::kTwoInputs ? pb + sp.head : nullptr;
     for (int64_t base = lo; base < hi; base += kSplitThreads * kSplitU) {
-      VecBuf<Op, kSplitU> buf;
+      VecBuf<Op, In, kSplitU> buf;
 #pragma unroll
       for (int u = 0; u < kSplitU; ++u) {
         const int64_t vi = base + tid + kSplitThreads * u;
-        if (vi < hi) buf.load(u, va, vb, vi * 8);
+        if (vi < hi) buf.load(u, va, vb, vi * EPV);
       }
       float t = 0.0f;
 #pragma unroll
@@ -177,16 +203,16 @@ rowsum_split_stage1(const float *__restrict__ a, const float *__restrict__ b, in
         if (base + tid + kSplitThreads * u < hi) t += buf.terms(u, op);
       acc += static_cast<double>(t);
     }
-    if (seg == 0 && tid < sp.head) acc += static_cast<double>(term_at(op, pa, pb, tid));
+    if (seg == 0 && tid < sp.head) acc += static_cast<double>(term_at<Op, In>(op, pa, pb, tid));
     if (seg == S - 1 && tid < sp.tail)
-      acc += static_cast<double>(term_at(op, pa, pb, sp.head + sp.nvec * 8 + tid));
+      acc += static_cast<double>(term_at<Op, In>(op, pa, pb, sp.head + sp.nvec * EPV + tid));
   } else {
     for (int64_t base = lo; base < hi; base += kSplitThreads * 8) {
       float t = 0.0f;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int64_t i = base + tid + kSplitThreads * u;
-        if (i < hi) t += term_at(op, pa, pb, i);
+        if (i < hi) t += term_at<Op, In>(op, pa, pb, i);
       }
       acc += static_cast<double>(t);
     }
@@ -222,31 +248,35 @@ unsigned warp_row_grid(int64_t rows) {
   return static_cast<unsigned>((rows + kRowThreads / 32 - 1) / (kRowThreads / 32));
 }
 
-template <class Op, bool LOOP, bool SQRT>
-cudaError_t launch_warp(const float *a, const float *b, float *out, int64_t rows, int64_t cols,
+template <class Op, class In, bool LOOP, bool SQRT>
+cudaError_t launch_warp(const void *a, const void *b, float *out, int64_t rows, int64_t cols,
                         int64_t lda, int64_t ldb, Op op, bool vec, cudaStream_t s) {
+  using E = typename In::T;
+  const E *ea = static_cast<const E *>(a), *eb = static_cast<const E *>(b);
   const dim3 grid(warp_row_grid(rows)), block(kRowThreads);
   if (vec)
-    return launch_k(rowsum_warp<Op, true, LOOP, SQRT>, grid, block, 0, s, 0, a, b, out, rows, cols,
-                    lda, ldb, op);
-  return launch_k(rowsum_warp<Op, false, LOOP, SQRT>, grid, block, 0, s, 0, a, b, out, rows, cols,
-                  lda, ldb, op);
+    return launch_k(rowsum_warp<Op, In, true, LOOP, SQRT>, grid, block, 0, s, 0, ea, eb, out, rows,
+                    cols, lda, ldb, op);
+  return launch_k(rowsum_warp<Op, In, false, LOOP, SQRT>, grid, block, 0, s, 0, ea, eb, out, rows,
+                  cols, lda, ldb, op);
 }
 
-template <class Op, bool SQRT>
-cudaError_t launch_split(const float *a, const float *b, float *out, int64_t rows, int64_t cols,
+template <class Op, class In, bool SQRT>
+cudaError_t launch_split(const void *a, const void *b, float *out, int64_t rows, int64_t cols,
                          int64_t lda, int64_t ldb, Op op, bool vec, double *partials,
                          int segments, cudaStream_t s) {
   // Ordinary launches: with the programmatic overlap the split form measured
   // slower on GB300 (fp32 [8, 33554432]: 323 us against 309 us), its one-wave
   // stage 1 sharing the SMs with the next call's early-placed CTAs.
+  using E = typename In::T;
+  const E *ea = static_cast<const E *>(a), *eb = static_cast<const E *>(b);
   const dim3 grid(static_cast<unsigned>(segments), static_cast<unsigned>(rows));
   if (vec)
-    rowsum_split_stage1<Op, true><<<grid, kSplitThreads, 0, s>>>(a, b, cols, lda, ldb, op,
-                                                                partials, segments);
+    rowsum_split_stage1<Op, In, true><<<grid, kSplitThreads, 0, s>>>(ea, eb, cols, lda, ldb, op,
+                                                                    partials, segments);
   else
-    rowsum_split_stage1<Op, false><<<grid, kSplitThreads, 0, s>>>(a, b, cols, lda, ldb, op,
-                                                                 partials, segments);
+    rowsum_split_stage1<Op, In, false><<<grid, kSplitThreads, 0, s>>>(ea, eb, cols, lda, ldb, op,
+                                                                     partials, segments);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   rowsum_split_stage2<SQRT><<<warp_row_grid(rows), kRowThreads, 0, s>>>(partials, out, rows,
@@ -256,11 +286,13 @@ cudaError_t launch_split(const float *a, const float *b, float *out, int64_t row
 
 }  // namespace
 
-int64_t ras_persistent_max_cols() { return 32 * 8 * kPersistNV; }
+int64_t ras_persistent_max_cols(bool bf16) {
+  return 32 * static_cast<int64_t>(kPersistNV) * (bf16 ? Bf16In::kN : F32In::kN);
+}
 
 int ras_split_segments(int64_t rows, int64_t cols, int sm_count) {
   // Enough CTAs for four per SM (one wave at the kernel's occupancy), but no
-  // segment shorter than 512 vectors (16 KiB of each input).
+  // segment shorter than 512 vectors (16 KiB of each fp32 input).
   int64_t want = (4LL * sm_count + rows - 1) / rows;
   int64_t units = cols / 8;
   int64_t cap = units / 512;
@@ -274,52 +306,58 @@ size_t ras_split_workspace(int64_t rows, int64_t cols, int sm_count) {
   return static_cast<size_t>(rows) * ras_split_segments(rows, cols, sm_count) * sizeof(double);
 }
 
-cudaError_t launch_ras_persistent(const float *a, const float *b, float *out, int64_t rows,
-                                  int64_t cols, int64_t lda, int64_t ldb, float scale,
+cudaError_t launch_ras_persistent(const void *a, const void *b, float *out, int64_t rows,
+                                  int64_t cols, int64_t lda, int64_t ldb, float scale, bool bf16,
                                   bool vec, cudaStream_t s) {
-  return launch_warp<ReluAdd, false, false>(a, b, out, rows, cols, lda, ldb, ReluAdd{scale},
-                                            vec, s);
+  return bf16 ? launch_warp<ReluAdd, Bf16In, false, false>(a, b, out, rows, cols, lda, ldb,
+                                                           ReluAdd{scale}, vec, s)
+              : launch_warp<ReluAdd, F32In, false, false>(a, b, out, rows, cols, lda, ldb,
+                                                          ReluAdd{scale}, vec, s);
 }
 
-cudaError_t launch_ras_looped(const float *a, const float *b, float *out, int64_t rows,
-                              int64_t cols, int64_t lda, int64_t ldb, float scale, bool vec,
-                              cudaStream_t s) {
-  return launch_warp<ReluAdd, true, false>(a, b, out, rows, cols, lda, ldb, ReluAdd{scale},
-                                           vec, s);
+cudaError_t launch_ras_looped(const void *a, const void *b, float *out, int64_t rows,
+                              int64_t cols, int64_t lda, int64_t ldb, float scale, bool bf16,
+                              bool vec, cudaStream_t s) {
+  return bf16 ? launch_warp<ReluAdd, Bf16In, true, false>(a, b, out, rows, cols, lda, ldb,
+                                                          ReluAdd{scale}, vec, s)
+              : launch_warp<ReluAdd, F32In, true, false>(a, b, out, rows, cols, lda, ldb,
+                                                         ReluAdd{scale}, vec, s);
 }
 
-cudaError_t launch_ras_split(const float *a, const float *b, float *out, int64_t rows,
-                             int64_t cols, int64_t lda, int64_t ldb, float scale, bool vec,
-                             double *partials, int segments, cudaStream_t s) {
-  return launch_split<ReluAdd, false>(a, b, out, rows, cols, lda, ldb, ReluAdd{scale}, vec,
-                                      partials, segments, s);
+cudaError_t launch_ras_split(const void *a, const void *b, float *out, int64_t rows,
+                             int64_t cols, int64_t lda, int64_t ldb, float scale, bool bf16,
+                             bool vec, double *partials, int segments, cudaStream_t s) {
+  return bf16 ? launch_split<ReluAdd, Bf16In, false>(a, b, out, rows, cols, lda, ldb,
+                                                     ReluAdd{scale}, vec, partials, segments, s)
+              : launch_split<ReluAdd, F32In, false>(a, b, out, rows, cols, lda, ldb,
+                                                    ReluAdd{scale}, vec, partials, segments, s);
 }
 
 // One-input rows need no common phase with a second input: every row takes
 // the vector path with its own head/body/tail split.
 cudaError_t launch_sumsq_persistent(const float *x, float *out, int64_t rows, int64_t cols,
                                     int64_t ldx, bool sqrt_out, cudaStream_t s) {
-  return sqrt_out ? launch_warp<Square, false, true>(x, nullptr, out, rows, cols, ldx, 0,
-                                                     Square{}, true, s)
-                  : launch_warp<Square, false, false>(x, nullptr, out, rows, cols, ldx, 0,
-                                                      Square{}, true, s);
+  return sqrt_out ? launch_warp<Square, F32In, false, true>(x, nullptr, out, rows, cols, ldx, 0,
+                                                            Square{}, true, s)
+                  : launch_warp<Square, F32In, false, false>(x, nullptr, out, rows, cols, ldx, 0,
+                                                             Square{}, true, s);
 }
 
 cudaError_t launch_sumsq_looped(const float *x, float *out, int64_t rows, int64_t cols,
                                 int64_t ldx, bool sqrt_out, cudaStream_t s) {
-  return sqrt_out ? launch_warp<Square, true, true>(x, nullptr, out, rows, cols, ldx, 0,
-                                                    Square{}, true, s)
-                  : launch_warp<Square, true, false>(x, nullptr, out, rows, cols, ldx, 0,
-                                                     Square{}, true, s);
+  return sqrt_out ? launch_warp<Square, F32In, true, true>(x, nullptr, out, rows, cols, ldx, 0,
+                                                           Square{}, true, s)
+                  : launch_warp<Square, F32In, true, false>(x, nullptr, out, rows, cols, ldx, 0,
+                                                            Square{}, true, s);
 }
 
 cudaError_t launch_sumsq_split(const float *x, float *out, int64_t rows, int64_t cols,
                                int64_t ldx, bool sqrt_out, double *partials, int segments,
                                cudaStream_t s) {
-  return sqrt_out ? launch_split<Square, true>(x, nullptr, out, rows, cols, ldx, 0, Square{},
-                                               true, partials, segments, s)
-                  : launch_split<Square, false>(x, nullptr, out, rows, cols, ldx, 0, Square{},
-                                                true, partials, segments, s);
+  return sqrt_out ? launch_split<Square, F32In, true>(x, nullptr, out, rows, cols, ldx, 0,
+                                                      Square{}, true, partials, segments, s)
+                  : launch_split<Square, F32In, false>(x, nullptr, out, rows, cols, ldx, 0,
+                                                       Square{}, true, partials, segments, s);
 }
 
 }  // namespace fr

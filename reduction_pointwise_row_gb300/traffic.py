@@ -28,6 +28,8 @@ def fused_softmax_elements(rows: int, cols: int) -> tuple[int, int]:
 def algorithmic_bytes(op: str, rows: int, cols: int, **kw) -> int:
     if op == "relu_add_sum":          # a, b fp32 in; out fp32 [rows]
         return 2 * rows * cols * 4 + rows * 4
+    if op == "relu_add_sum_bf16":     # a, b bf16 in; out fp32 [rows]
+        return 2 * rows * cols * 2 + rows * 4
     if op == "sumsq":                 # x fp32 in; out fp32 [rows]
         return rows * cols * 4 + rows * 4
     if op == "softmax":               # x fp32 in; y fp32 out

@@ -101,7 +101,9 @@ def test_argument_validation_needs_no_device():
     assert lib.fr_reduce_relu_add_sum(None, good, good, 4, 8, 8, 8, 0, 2.0, 0, None, 0, None) == 1
     assert lib.fr_reduce_relu_add_sum(good, good, good, 0, 8, 8, 8, 0, 2.0, 0, None, 0, None) == 1
     assert lib.fr_reduce_relu_add_sum(good, good, good, 4, 8, 7, 8, 0, 2.0, 0, None, 0, None) == 1
-    assert lib.fr_reduce_relu_add_sum(good, good, good, 4, 8, 8, 8, 1, 2.0, 0, None, 0, None) == 2
+    assert lib.fr_reduce_relu_add_sum(good, good, good, 4, 8, 8, 8, 2, 2.0, 0, None, 0, None) == 2
+    # bf16 inputs must be 2-byte aligned
+    assert lib.fr_reduce_relu_add_sum(odd, good, good, 4, 8, 8, 8, 1, 2.0, 0, None, 0, None) == 4
     assert lib.fr_reduce_relu_add_sum(odd, good, good, 4, 8, 8, 8, 0, 2.0, 0, None, 0, None) == 4
     big = 1 << 40
     assert lib.fr_reduce_relu_add_sum(good, good, good, big, big, big, big, 0, 2.0, 0, None, 0,

@@ -109,6 +109,39 @@ def test_relu_add_sum_scale_and_infinities(o):
             assert_close(run_ras(a, b, form, scale=scale), ref, "f32", f"{form} scale {scale}")
 
 
+def _widen(bits):
+    return synth.bf16_bits_to_f32(bits)
+
+
+@pytest.mark.parametrize("cols", [1, 3, 7, 13, 31, 33, 129, 1000, 1024, 2047, 2048, 2049, 4097])
+@pytest.mark.parametrize("rows", [1, 7, 65])
+@pytest.mark.parametrize("layout", LAYOUTS, ids=["aligned", "offset_same_phase", "offset_scalar"])
+def test_relu_add_sum_bf16_forms(o, rows, cols, layout):
+    """bf16 inputs: the oracle on the exactly widened values (the sum a + b in
+    fp32, as for fp32 inputs); persistent up to 2048 columns."""
+    seed = 1500 + rows * 7 + cols
+    a = synth.normal_bf16((rows, cols), seed, 0, 0.0, 1.0)
+    b = synth.normal_bf16((rows, cols), seed, 1, 0.0, 1.0)
+    ref = o.relu_add_sum(_widen(a), _widen(b), 2.0)
+    forms = (["persistent"] if cols <= 2048 else []) + ["looped", "split", "auto"]
+    for form in forms:
+        got = run_ras(a, b, form, layout)
+        assert_close(got, ref, "f32", f"bf16 {form} {rows}x{cols} {layout}")
+
+
+@pytest.mark.parametrize("cols", [128, 2048, 4097, 65535])
+def test_relu_add_sum_bf16_dyadic_is_bit_exact(o, cols):
+    """k/64 values are bf16 numbers: every partial sum is exact, as for fp32."""
+    rng = np.random.default_rng(cols + 1)
+    af = (rng.integers(-64, 65, (9, cols)) / 64).astype(np.float32)
+    bf = (rng.integers(-64, 65, (9, cols)) / 64).astype(np.float32)
+    a, b = (af.view(np.uint32) >> 16).astype(np.uint16), (bf.view(np.uint32) >> 16).astype(np.uint16)
+    assert (_widen(a) == af).all()
+    ref = o.relu_add_sum(af, bf, 2.0).astype(np.float32)
+    for form in (["persistent"] if cols <= 2048 else []) + ["looped", "split"]:
+        assert_bits_equal(run_ras(a, b, form), ref, f"bf16 {form} {cols}")
+
+
 # ---------------------------------------------------------------- softmax
 
 def run_softmax(x, form, layout=(0, 0, 0), kernel=None):
