@@ -90,8 +90,8 @@ __device__ __forceinline__ Welford welford16(const V8 &v) {
 // cols % 16 == 0 (checked by the host); NV vectors of 16 per thread.
 constexpr int kPersistMaxThreads = 512;
 
-template <int NV>
-__global__ void __launch_bounds__(kPersistMaxThreads, 2)
+template <int NV>  // four vectors a thread need more than the 64 registers two CTAs leave
+__global__ void __launch_bounds__(kPersistMaxThreads, NV >= 4 ? 1 : 2)
 layernorm_persistent(const uint16_t *__restrict__ x, const float *__restrict__ gamma,
                      const float *__restrict__ beta, uint16_t *__restrict__ y,
                      float *__restrict__ mean_out, float *__restrict__ rstd_out, int64_t cols,
