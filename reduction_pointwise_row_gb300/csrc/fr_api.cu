@@ -246,7 +246,7 @@ fr_status fr_softmax(const void *x, void *y, int64_t rows, int64_t cols, int64_t
   const bool vec = same_phase(x, ldx, y, ldy, esize);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (dtype == FR_BF16) {
-    const int64_t max_p = fr::softmax_bf16_persistent_max_cols();
+    const int64_t max_p = fr::softmax_bf16_persistent_max_cols(vec);
     const fr_form f = form == FR_FORM_AUTO ? (cols <= max_p ? FR_FORM_PERSISTENT : FR_FORM_LOOPED)
                                            : form;
     const uint16_t *bx = static_cast<const uint16_t *>(x);

@@ -68,7 +68,7 @@ cudaError_t launch_softmax_split(const float *x, float *y, int64_t rows, int64_t
                                  int64_t ldx, int64_t ldy, cudaStream_t s);
 
 // bf16 rows (x and y bf16, fp32 arithmetic): persistent up to 2048 columns.
-int64_t softmax_bf16_persistent_max_cols();
+int64_t softmax_bf16_persistent_max_cols(bool vec);
 cudaError_t launch_softmax_bf16_persistent(const uint16_t *x, uint16_t *y, int64_t rows,
                                            int64_t cols, int64_t ldx, int64_t ldy, bool vec,
                                            cudaStream_t s);

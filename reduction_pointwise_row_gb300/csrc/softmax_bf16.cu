@@ -99,6 +99,77 @@ softmax_bf16_warp_vec(const uint16_t *__restrict__ x, uint16_t *__restrict__ y, 
   if (si >= 0) st_stream_u16(py + si, to_bf16(se * inv));
 }
 
+// Persistent form for longer rows in phase: one CTA of T threads per row,
+// NV vectors of 16 elements per thread (cols <= 16 * T * NV), the
+// exponentials in registers as in the warp form; the max and the sum are CTA
+// reductions (per-warp values through shared memory).
+template <int T, int NV>
+__global__ void __launch_bounds__(T)
+softmax_bf16_cta_vec(const uint16_t *__restrict__ x, uint16_t *__restrict__ y, int64_t cols,
+                     int64_t ldx, int64_t ldy) {
+  pdl_enter();
+  constexpr int W = T / 32;
+  __shared__ float red[2][W];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t row = blockIdx.x;
+  const uint16_t *px = x + row * ldx;
+  uint16_t *py = y + row * ldy;
+  const RowSplit sp = row_split(px, cols, 2);
+  int64_t si = -1;  // head and tail scalars (at most 15 + 15), one per thread
+  if (tid < sp.head) si = tid;
+  else if (tid < sp.head + sp.tail) si = sp.head + sp.nvec * kPer + (tid - sp.head);
+  const uint16_t *vx = px + sp.head;
+  V8 v[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int64_t vi = tid + static_cast<int64_t>(T) * k;
+    if (vi < sp.nvec) v[k] = ld_stream_v8(vx + vi * kPer);
+  }
+  const float sv = si >= 0 ? bf16_to_f32(ld_stream_u16(px + si)) : -INFINITY;
+
+  float m = sv;
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+    if (tid + T * k < sp.nvec) m = max_nan(m, vec_max(v[k]));
+  m = warp_max_nan(m);
+  if (lane == 0) red[0][warp] = m;
+  __syncthreads();
+  m = warp_max_nan(lane < W ? red[0][lane] : -INFINITY);
+  const float mb = m * kLog2e;
+
+  const float se = si >= 0 ? ex2(fmaf(sv, kLog2e, -mb)) : 0.0f;
+  float e[NV][kPer];
+  float d = se;
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+    if (tid + T * k < sp.nvec) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        e[k][2 * j] = ex2(fmaf(bf16_lo(v[k].w[j]), kLog2e, -mb));
+        e[k][2 * j + 1] = ex2(fmaf(bf16_hi(v[k].w[j]), kLog2e, -mb));
+        d += e[k][2 * j] + e[k][2 * j + 1];
+      }
+    }
+  d = warp_sum(d);
+  if (lane == 0) red[1][warp] = d;
+  __syncthreads();
+  d = warp_sum(lane < W ? red[1][lane] : 0.0f);
+  const float inv = __frcp_rn(d);
+
+  uint16_t *vy = py + sp.head;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int64_t vi = tid + static_cast<int64_t>(T) * k;
+    if (vi < sp.nvec) {
+      V8 o;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) o.w[j] = pack_bf16x2(e[k][2 * j] * inv, e[k][2 * j + 1] * inv);
+      st_stream_v8(vy + vi * kPer, o);
+    }
+  }
+  if (si >= 0) st_stream_u16(py + si, to_bf16(se * inv));
+}
+
 // Persistent form, lane-strided scalars (x and y rows out of phase): NS
 // elements per lane, cols <= 32 * NS.
 template <int NS>
@@ -264,12 +335,32 @@ unsigned warp_row_grid(int64_t rows) {
 
 }  // namespace
 
-int64_t softmax_bf16_persistent_max_cols() { return 2048; }
+// Rows up to 2048 take one warp; longer rows in phase take one CTA of up to
+// 1024 threads x 2 vectors (32768 elements).
+int64_t softmax_bf16_persistent_max_cols(bool vec) { return vec ? 32768 : 2048; }
+
+namespace {
+template <int T, int NV>
+cudaError_t launch_bf16_cta(const uint16_t *x, uint16_t *y, int64_t rows, int64_t cols,
+                            int64_t ldx, int64_t ldy, cudaStream_t s) {
+  return launch_k(softmax_bf16_cta_vec<T, NV>, dim3(static_cast<unsigned>(rows)), dim3(T), 0, s,
+                  0, x, y, cols, ldx, ldy);
+}
+}  // namespace
 
 cudaError_t launch_softmax_bf16_persistent(const uint16_t *x, uint16_t *y, int64_t rows,
                                            int64_t cols, int64_t ldx, int64_t ldy, bool vec,
                                            cudaStream_t s) {
   const unsigned grid = warp_row_grid(rows);
+  if (vec && cols > 2048) {
+    if (rows > 0x7fffffff) return cudaErrorInvalidValue;
+    const int64_t nvec = cols / kPer;  // at least the body's vectors
+    if (nvec <= 128 * 2) return launch_bf16_cta<128, 2>(x, y, rows, cols, ldx, ldy, s);
+    if (nvec <= 256 * 2) return launch_bf16_cta<256, 2>(x, y, rows, cols, ldx, ldy, s);
+    if (nvec <= 512 * 2) return launch_bf16_cta<512, 2>(x, y, rows, cols, ldx, ldy, s);
+    if (nvec <= 1024 * 2) return launch_bf16_cta<1024, 2>(x, y, rows, cols, ldx, ldy, s);
+    return cudaErrorInvalidValue;
+  }
   if (vec) {
     const int64_t nv = (cols + 32 * kPer - 1) / (32 * kPer);
     switch (nv) {

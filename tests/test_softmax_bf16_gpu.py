@@ -15,7 +15,7 @@ from synth import workloads
 pytestmark = pytest.mark.gpu
 
 COLS = [1, 2, 15, 16, 17, 31, 129, 511, 512, 513, 1000, 1024, 1536, 2047, 2048, 2049, 4097,
-        65537]
+        8192, 16385, 32768, 32769, 65537]
 # (offset of x, offset of y, extra row padding), in elements
 LAYOUTS = [(0, 0, 0), (3, 3, 7), (0, 5, 0)]
 
@@ -29,8 +29,12 @@ def widen(bits):
     return (bits.astype(np.uint32) << 16).view(np.float32)
 
 
-def forms(cols):
-    return (["persistent"] if cols <= 2048 else []) + ["looped", "auto"]
+def forms(cols, layout=(0, 0, 0)):
+    """persistent: one warp per row up to 2048 columns, one CTA per row up to
+    32768 when x and y rows share their 32-byte phase"""
+    in_phase = (layout[0] - layout[1]) * 2 % 32 == 0
+    persistent = cols <= 2048 or (cols <= 32768 and in_phase)
+    return (["persistent"] if persistent else []) + ["looped", "auto"]
 
 
 def run(bits, form, layout=(0, 0, 0)):
@@ -50,11 +54,11 @@ def run(bits, form, layout=(0, 0, 0)):
 def test_softmax_bf16_forms(o, rows, cols, layout):
     bits = workloads.make_softmax_bf16(rows, cols, seed=6000 + rows * 11 + cols).arrays["x"]
     ref = o.softmax(widen(bits))
-    for form in forms(cols):
+    for form in forms(cols, layout):
         assert_bf16_within_steps(run(bits, form, layout), ref, 1, f"{form} {rows}x{cols} {layout}")
 
 
-@pytest.mark.parametrize("cols", [7, 1000, 2048, 4097])
+@pytest.mark.parametrize("cols", [7, 1000, 2048, 4097, 20000])
 def test_softmax_bf16_special_values(o, cols):
     bits = workloads.make_softmax_bf16(6, cols, seed=61).arrays["x"].copy()
     bits[1, cols // 2] = 0x7FC0               # NaN row
