@@ -15,6 +15,8 @@
 // The max runs on packed bf16 pairs (max.NaN.bf16x2 is exact on bf16 values);
 // NaN anywhere in the row makes the row NaN; masked lanes are -inf for the max
 // and 0 for the sum.
+#include <cstdlib>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -22,7 +24,6 @@ namespace fr {
 namespace {
 
 constexpr int kWarpRowThreads = 256;
-constexpr int kLoopThreads = 512;
 constexpr int kLoopU = 2;
 constexpr int kPer = 16;                    // bf16 per 32-byte vector
 constexpr uint32_t kNegInfBf16x2 = 0xFF80FF80u;
@@ -220,8 +221,9 @@ __device__ __forceinline__ MD fold_chunk(MD st, float cm) {
 }
 
 // CTA-wide merge of the per-thread pairs; every thread gets the row's (m, d).
+template <int T>
 __device__ __forceinline__ MD block_md(MD st, MD *smem) {
-  constexpr int NW = kLoopThreads / 32;
+  constexpr int NW = T / 32;
   st = warp_md(st);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) smem[warp] = st;
@@ -232,11 +234,12 @@ __device__ __forceinline__ MD block_md(MD st, MD *smem) {
   return r;
 }
 
-template <bool VEC>
-__global__ void __launch_bounds__(kLoopThreads)
+template <bool VEC, int T>
+__global__ void __launch_bounds__(T)
 softmax_bf16_block_looped(const uint16_t *__restrict__ x, uint16_t *__restrict__ y, int64_t rows,
                           int64_t cols, int64_t ldx, int64_t ldy) {
-  __shared__ MD red[kLoopThreads / 32];
+  pdl_enter();
+  __shared__ MD red[T / 32];
   const int tid = threadIdx.x;
   for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
     const uint16_t *px = x + row * ldx;
@@ -245,12 +248,12 @@ softmax_bf16_block_looped(const uint16_t *__restrict__ x, uint16_t *__restrict__
     MD st{-INFINITY, 0.0f};
     if constexpr (VEC) {
       const uint16_t *vx = px + sp.head;
-      for (int64_t base = 0; base < sp.nvec; base += kLoopThreads * kLoopU) {
+      for (int64_t base = 0; base < sp.nvec; base += T * kLoopU) {
         V8 v[kLoopU];
         float cm = -INFINITY;
 #pragma unroll
         for (int u = 0; u < kLoopU; ++u) {
-          const int64_t vi = base + tid + kLoopThreads * u;
+          const int64_t vi = base + tid + T * u;
           if (vi < sp.nvec) {
             v[u] = ld_keep_v8(vx + vi * kPer);  // pass 2 re-reads it from L2
             cm = max_nan(cm, vec_max(v[u]));
@@ -261,7 +264,7 @@ softmax_bf16_block_looped(const uint16_t *__restrict__ x, uint16_t *__restrict__
         const float mb = st.m * kLog2e;
 #pragma unroll
         for (int u = 0; u < kLoopU; ++u)
-          if (base + tid + kLoopThreads * u < sp.nvec) {
+          if (base + tid + T * u < sp.nvec) {
 #pragma unroll
             for (int j = 0; j < 8; ++j)
               st.d += ex2(fmaf(bf16_lo(v[u].w[j]), kLog2e, -mb)) +
@@ -273,12 +276,12 @@ softmax_bf16_block_looped(const uint16_t *__restrict__ x, uint16_t *__restrict__
       else if (tid < sp.head + sp.tail) si = sp.head + sp.nvec * kPer + (tid - sp.head);
       if (si >= 0) st = md_merge(st, MD{bf16_to_f32(ld_stream_u16(px + si)), 1.0f});
     } else {
-      for (int64_t base = 0; base < cols; base += kLoopThreads * 8) {
+      for (int64_t base = 0; base < cols; base += T * 8) {
         float v[8];
         float cm = -INFINITY;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const int64_t i = base + tid + kLoopThreads * u;
+          const int64_t i = base + tid + T * u;
           v[u] = i < cols ? bf16_to_f32(ld_stream_u16(px + i)) : -INFINITY;
           cm = max_nan(cm, v[u]);
         }
@@ -287,25 +290,25 @@ softmax_bf16_block_looped(const uint16_t *__restrict__ x, uint16_t *__restrict__
         const float mb = st.m * kLog2e;
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-          if (base + tid + kLoopThreads * u < cols) st.d += ex2(fmaf(v[u], kLog2e, -mb));
+          if (base + tid + T * u < cols) st.d += ex2(fmaf(v[u], kLog2e, -mb));
       }
     }
-    const MD r = block_md(st, red);
+    const MD r = block_md<T>(st, red);
     const float mb = r.m * kLog2e;
     const float inv = __frcp_rn(r.d);
     if constexpr (VEC) {
       const uint16_t *vx = px + sp.head;
       uint16_t *vy = py + sp.head;
-      for (int64_t base = 0; base < sp.nvec; base += kLoopThreads * kLoopU) {
+      for (int64_t base = 0; base < sp.nvec; base += T * kLoopU) {
         V8 v[kLoopU];
 #pragma unroll
         for (int u = 0; u < kLoopU; ++u) {
-          const int64_t vi = base + tid + kLoopThreads * u;
+          const int64_t vi = base + tid + T * u;
           if (vi < sp.nvec) v[u] = ld_stream_v8(vx + vi * kPer);
         }
 #pragma unroll
         for (int u = 0; u < kLoopU; ++u) {
-          const int64_t vi = base + tid + kLoopThreads * u;
+          const int64_t vi = base + tid + T * u;
           if (vi < sp.nvec) {
 #pragma unroll
             for (int j = 0; j < 8; ++j)
@@ -322,7 +325,7 @@ softmax_bf16_block_looped(const uint16_t *__restrict__ x, uint16_t *__restrict__
         st_stream_u16(py + si,
                       to_bf16(ex2(fmaf(bf16_to_f32(ld_stream_u16(px + si)), kLog2e, -mb)) * inv));
     } else {
-      for (int64_t i = tid; i < cols; i += kLoopThreads)
+      for (int64_t i = tid; i < cols; i += T)
         st_stream_u16(py + i,
                       to_bf16(ex2(fmaf(bf16_to_f32(ld_stream_u16(px + i)), kLog2e, -mb)) * inv));
     }
@@ -380,18 +383,39 @@ cudaError_t launch_softmax_bf16_persistent(const uint16_t *x, uint16_t *y, int64
   return cudaGetLastError();
 }
 
+namespace {
+template <int T>
+cudaError_t launch_bf16_looped_t(const uint16_t *x, uint16_t *y, int64_t rows, int64_t cols,
+                                 int64_t ldx, int64_t ldy, bool vec, int sm_count, int per_sm_cap,
+                                 cudaStream_t s) {
+  auto kern = vec ? softmax_bf16_block_looped<true, T> : softmax_bf16_block_looped<false, T>;
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, T, 0);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  if (per_sm > per_sm_cap) per_sm = per_sm_cap;
+  int64_t grid = static_cast<int64_t>(sm_count) * per_sm;  // persistent: rows strided over CTAs
+  if (grid > rows) grid = rows;
+  return launch_k(kern, dim3(static_cast<unsigned>(grid)), dim3(T), 0, s, 0, x, y, rows, cols, ldx,
+                  ldy);
+}
+}  // namespace
+
 cudaError_t launch_softmax_bf16_looped(const uint16_t *x, uint16_t *y, int64_t rows,
                                        int64_t cols, int64_t ldx, int64_t ldy, bool vec,
                                        int sm_count, cudaStream_t s) {
-  int64_t grid = static_cast<int64_t>(sm_count) * 2;
-  if (grid > rows) grid = rows;
-  if (vec)
-    softmax_bf16_block_looped<true><<<static_cast<unsigned>(grid), kLoopThreads, 0, s>>>(
-        x, y, rows, cols, ldx, ldy);
-  else
-    softmax_bf16_block_looped<false><<<static_cast<unsigned>(grid), kLoopThreads, 0, s>>>(
-        x, y, rows, cols, ldx, ldy);
-  return cudaGetLastError();
+  // As for fp32: many rows take small CTAs, as many per SM as fit (the
+  // smallest that covers a row's vectors in one chunk); few rows 512-thread
+  // CTAs, two per SM.  Measured on GB300, bf16 [16380, 4097]: 54.2 us with
+  // 128 threads, 84.5 with 256, 148.5 with 512.  FR_SOFTMAX_LOOP=128|256|512
+  // pins the CTA size.
+  const char *e = getenv("FR_SOFTMAX_LOOP");
+  int t = 512;
+  if (e != nullptr) t = atoi(e);
+  else if (rows >= 4 * static_cast<int64_t>(sm_count)) t = cols / kPer <= 128 * kLoopU ? 128 : 256;
+  if (t == 128) return launch_bf16_looped_t<128>(x, y, rows, cols, ldx, ldy, vec, sm_count, 16, s);
+  if (t == 256) return launch_bf16_looped_t<256>(x, y, rows, cols, ldx, ldy, vec, sm_count, 16, s);
+  return launch_bf16_looped_t<512>(x, y, rows, cols, ldx, ldy, vec, sm_count, 2, s);
 }
 
 }  // namespace fr

@@ -134,3 +134,32 @@ def test_argument_validation_needs_no_device():
     assert lib.fr_xent(good, P(0x10004), None, None, None, None, 4, 8, 8, -100, 1, 0, None, 0,
                        None) == 4
     assert lib.fr_xent(good, good, None, None, None, None, 4, 8, 8, -100, 1, 3, None, 0, None) == 3
+
+
+def test_every_overlapped_kernel_waits_for_its_predecessor():
+    """Launches with the programmatic-overlap attribute (launch_k, launch_pdl)
+    may start a kernel while the one before it still runs; such a kernel must
+    begin with pdl_enter() (griddepcontrol.wait) before touching memory.  Every
+    kernel does, except those launched only without the attribute, listed here."""
+    import glob
+    import re
+    plain_only = {"layernorm_persistent", "layernorm_looped_scalar", "layernorm_ring",
+                  "layernorm_cluster", "softmax_warp_scalar", "softmax_warp_async",
+                  "softmax_bf16_warp_scalar"}
+    seen = set()
+    for f in glob.glob(os.path.join(ROOT, "reduction_pointwise_row_gb300", "csrc", "*.cu")):
+        s = open(f).read()
+        for m in re.finditer(r"__global__", s):
+            brace = s.index("{", m.end())
+            head = re.sub(r"__launch_bounds__\([^)]*\)", "", s[m.end():brace])
+            name = re.findall(r"\b([A-Za-z_]\w*)\s*\(", head)[0]
+            seen.add(name)
+            body = s[brace + 1:brace + 600]
+            statements = [t.strip() for t in body.split(";")]
+            waits = any(t.startswith("pdl_enter()") for t in statements[:2])
+            if name in plain_only:
+                # launched only with <<<>>>, cudaLaunchKernel or without the attribute
+                assert not re.search(r"launch_(k|pdl)\(\s*(&)?" + name + r"\b", s), name
+            else:
+                assert waits, f"{name} ({os.path.basename(f)}) does not begin with pdl_enter()"
+    assert plain_only <= seen

@@ -89,3 +89,16 @@ def test_softmax_bf16_in_place_and_full_headline_shape(o):
     rows = np.random.default_rng(3).choice(32768, 64, replace=False)
     rows.sort()
     assert_bf16_within_steps(got[rows], o.softmax(widen(full[rows])), 1, "sampled rows")
+
+
+@pytest.mark.parametrize("cta", ["128", "256", "512"])
+def test_softmax_bf16_looped_every_cta_size(o, cta, monkeypatch):
+    """The looped form at each CTA size its rule can pick (FR_SOFTMAX_LOOP pins
+    it), rows in and out of phase, short and long."""
+    monkeypatch.setenv("FR_SOFTMAX_LOOP", cta)
+    for rows, cols, layout in ((700, 4097, (0, 0, 0)), (9, 65537, (3, 3, 7)), (40, 3000, (0, 5, 0)),
+                               (5, 17, (0, 0, 0))):
+        bits = workloads.make_softmax_bf16(rows, cols, seed=6500 + cols).arrays["x"]
+        ref = o.softmax(widen(bits))
+        assert_bf16_within_steps(run(bits, "looped", layout), ref, 1,
+                                 f"looped T={cta} {rows}x{cols} {layout}")
