@@ -6,7 +6,8 @@
 // persistent  one warp per row, the row's exponentials held in registers (up
 //             to 2048 elements per warp, 32-byte vectors of 16 bf16 per lane),
 //             the max and the sum in two passes over registers: one read and
-//             one write of each element.
+//             one write of each element; rows of 2049 .. 32768 in phase take
+//             one CTA per row the same way, with CTA reductions.
 // looped      one CTA per row (grid-stride over rows) for longer rows: per-
 //             thread online pairs (m, d) folded chunk by chunk with the merge
 //             of section 9.5, combined across the CTA in any order
