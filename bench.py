@@ -54,7 +54,7 @@ def parse():
                                       "softmax_65537", "softmax_65537_looped",
                                       "looped", "looped_bf16", "softmax_bf16", "xent_f32",
                                       "softmax_bf16_4097", "softmax_bf16_4097_looped",
-                                      "xent_box"],
+                                      "softmax_bf16_65537", "xent_box"],
                    help="time one workload alone (for profiler captures) and exit")
     p.add_argument("--form", default="auto", choices=["auto", "persistent", "looped", "split"],
                    help="with --only: force a reduction form")
@@ -398,6 +398,15 @@ def setup_workload(name, fr, workloads, dev, form="auto"):
             y = torch.empty_like(x)
             calls.append(lambda x=x, y=y: fr.fr_softmax(x, out=y, form=form))
         return calls, "softmax_bf16", w.rows, w.cols, 1
+    if name == "softmax_bf16_65537":
+        # bf16 rows of 65537 (the fp32 sweep's bytes: 1022 rows): AUTO takes
+        # a cluster of CTAs per row
+        w = workloads.make_softmax_bf16(1022, 65537, seed=20261202 + 6 + 1000 * SHARD[0])
+        for _ in range(nsets("softmax_bf16", w.rows, w.cols)):
+            x = to_device(w.arrays["x"], dev)
+            y = torch.empty_like(x)
+            calls.append(lambda x=x, y=y: fr.fr_softmax(x, out=y, form=form))
+        return calls, "softmax_bf16", w.rows, w.cols, 1
     if name in ("softmax_bf16_4097", "softmax_bf16_4097_looped"):
         # bf16 rows of 4097 (the fp32 sweep's bytes: 16380 rows): one CTA per
         # row (AUTO) or the looped online form
@@ -503,7 +512,8 @@ EXTRA = {"relu_add_sum": "relu_add_sum_64x128", "layernorm": "layernorm_4096x327
          "looped": "relu_add_sum_looped_16384x8192", "softmax_bf16": "softmax_bf16_65536x1024",
          "xent_f32": "xent_f32_8192x50257", "looped_bf16": "relu_add_sum_bf16_looped_16384x16384",
          "softmax_bf16_4097": "softmax_bf16_16380x4097",
-         "softmax_bf16_4097_looped": "softmax_bf16_looped_16380x4097"}
+         "softmax_bf16_4097_looped": "softmax_bf16_looped_16380x4097",
+         "softmax_bf16_65537": "softmax_bf16_1022x65537"}
 
 
 def extra_configs(fr, traffic, workloads, timed, dev, peak, args, world, names=None,

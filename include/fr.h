@@ -170,7 +170,8 @@ fr_status fr_reduce_sumsq(const void *x, float *out, int64_t rows, int64_t cols,
  *   dtype      FR_F32 or FR_BF16; persistent up to 1024 (fp32) or 2048 (bf16)
  *              columns with one warp per row, up to 32768 with one CTA per
  *              row when x and y rows share their 32-byte phase; longer rows
- *              take the split (fp32) or looped form
+ *              (or few rows) in phase take the split form (a cluster of CTAs
+ *              per row, up to 262144 columns), the rest the looped form
  */
 fr_status fr_softmax(const void *x, void *y, int64_t rows, int64_t cols, int64_t ldx,
                      int64_t ldy, fr_dtype dtype, fr_form form, fr_stream_t stream);

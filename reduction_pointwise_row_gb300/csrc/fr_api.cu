@@ -247,8 +247,19 @@ fr_status fr_softmax(const void *x, void *y, int64_t rows, int64_t cols, int64_t
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (dtype == FR_BF16) {
     const int64_t max_p = fr::softmax_bf16_persistent_max_cols(vec);
-    const fr_form f = form == FR_FORM_AUTO ? (cols <= max_p ? FR_FORM_PERSISTENT : FR_FORM_LOOPED)
-                                           : form;
+    // the fp32 rule with the bf16 limits: a warp per row up to 2048 columns,
+    // a CTA per row while the rows fill the SMs, a cluster per row for few
+    // or longer rows in phase, else looped
+    fr_form f = form;
+    if (form == FR_FORM_AUTO) {
+      if (cols <= 2048 ||
+          (cols <= max_p && rows >= 4 * static_cast<int64_t>(info.sm_count)))
+        f = FR_FORM_PERSISTENT;
+      else if (vec && cols <= fr::softmax_bf16_split_max_cols())
+        f = FR_FORM_SPLIT;
+      else
+        f = FR_FORM_LOOPED;
+    }
     const uint16_t *bx = static_cast<const uint16_t *>(x);
     uint16_t *by = static_cast<uint16_t *>(y);
     switch (f) {
@@ -258,6 +269,11 @@ fr_status fr_softmax(const void *x, void *y, int64_t rows, int64_t cols, int64_t
       case FR_FORM_LOOPED:
         return launched(fr::launch_softmax_bf16_looped(bx, by, rows, cols, ldx, ldy, vec,
                                                        info.sm_count, s), f);
+      case FR_FORM_SPLIT:
+        if (!vec || cols <= 2048 || cols > fr::softmax_bf16_split_max_cols() ||
+            rows > 0x7fffffff / 8)
+          return FR_ERR_UNSUPPORTED_FORM;
+        return launched(fr::launch_softmax_bf16_split(bx, by, rows, cols, ldx, ldy, s), f);
       default: return FR_ERR_UNSUPPORTED_FORM;
     }
   }

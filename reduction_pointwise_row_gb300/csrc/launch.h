@@ -69,6 +69,11 @@ cudaError_t launch_softmax_split(const float *x, float *y, int64_t rows, int64_t
 
 // bf16 rows (x and y bf16, fp32 arithmetic): persistent up to 2048 columns.
 int64_t softmax_bf16_persistent_max_cols(bool vec);
+// Split form of the bf16 softmax: a thread-block cluster per row (rows in
+// phase, 2049 .. softmax_bf16_split_max_cols() columns).
+int64_t softmax_bf16_split_max_cols();
+cudaError_t launch_softmax_bf16_split(const uint16_t *x, uint16_t *y, int64_t rows, int64_t cols,
+                                      int64_t ldx, int64_t ldy, cudaStream_t s);
 cudaError_t launch_softmax_bf16_persistent(const uint16_t *x, uint16_t *y, int64_t rows,
                                            int64_t cols, int64_t ldx, int64_t ldy, bool vec,
                                            cudaStream_t s);

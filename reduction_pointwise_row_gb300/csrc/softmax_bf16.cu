@@ -17,6 +17,7 @@
 // NaN anywhere in the row makes the row NaN; masked lanes are -inf for the max
 // and 0 for the sum.
 #include <cstdlib>
+#include <cstring>
 
 #include "common.cuh"
 #include "launch.h"
@@ -170,6 +171,120 @@ softmax_bf16_cta_vec(const uint16_t *__restrict__ x, uint16_t *__restrict__ y, i
     }
   }
   if (si >= 0) st_stream_u16(py + si, to_bf16(se * inv));
+}
+
+// Split form for long rows in phase: a thread-block cluster of C CTAs per
+// row, CTA rank q holding its slice of the row's 16-element vectors and their
+// exponentials in registers (rank 0 also the head scalars, rank C - 1 the
+// tail).  Each CTA reduces its slice to (m_q, d_q), pushes the pair into every
+// CTA of the cluster with st.async (counted on the receiver's mbarrier), and
+// once all C pairs are in, merges them in rank order with the merge of
+// section 9.5 -- the same (M, D) in every CTA -- and writes its values scaled
+// by 2^((m_q - M) log2 e) / D.  One read and one write per element.  The wait
+// is bounded; on expiry the kernel records FR_DEVERR_TIMEOUT and goes on.
+constexpr int kBfClusterMax = 8;
+constexpr long long kBfWaitBudget = 1LL << 31;  // SM clocks (about one second)
+
+// RE: recompute the exponentials in the writing pass instead of holding
+// them (registers for twice the vectors per thread; two ex2 per element).
+template <int T, int NV, bool RE>
+__global__ void __launch_bounds__(T)
+softmax_bf16_cluster(const uint16_t *__restrict__ x, uint16_t *__restrict__ y, int64_t cols,
+                     int64_t ldx, int64_t ldy, int *__restrict__ err) {
+  pdl_enter();
+  constexpr int W = T / 32;
+  __shared__ float red[2][W];
+  __shared__ __align__(16) float4 pairs[kBfClusterMax];
+  __shared__ __align__(8) uint64_t xbar;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t C = cluster_nctarank(), q = cluster_ctarank();
+  if (tid == 0) {
+    mbar_init(&xbar, 1);
+    mbar_init_fence();
+    mbar_arrive_expect_tx(&xbar, 16u * C);
+  }
+  __syncthreads();
+  cluster_arrive_relaxed();  // this CTA's mbarrier is ready for the peers' pairs
+  const int64_t row = cluster_id_x();
+  const uint16_t *px = x + row * ldx;
+  uint16_t *py = y + row * ldy;
+  const RowSplit sp = row_split(px, cols, 2);
+  const int64_t per = (sp.nvec + C - 1) / C;
+  const int64_t lo = per * q;
+  const int64_t hi = lo + per < sp.nvec ? lo + per : sp.nvec;
+  int64_t si = -1;  // head scalars: rank 0, threads 0..14; tail: rank C - 1, threads 32..46
+  if (q == 0 && tid < sp.head) si = tid;
+  else if (q == C - 1 && tid >= 32 && tid - 32 < sp.tail) si = sp.head + sp.nvec * kPer + (tid - 32);
+  const uint16_t *vx = px + sp.head;
+  V8 v[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int64_t vi = lo + tid + static_cast<int64_t>(T) * k;
+    if (vi < hi) v[k] = ld_stream_v8(vx + vi * kPer);
+  }
+  const float sv = si >= 0 ? bf16_to_f32(ld_stream_u16(px + si)) : -INFINITY;
+
+  float m = sv;
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+    if (lo + tid + T * k < hi) m = max_nan(m, vec_max(v[k]));
+  m = warp_max_nan(m);
+  if (lane == 0) red[0][warp] = m;
+  __syncthreads();
+  m = warp_max_nan(lane < W ? red[0][lane] : -INFINITY);
+  // a slice of nothing but -inf contributes d = 0 (and scales to 0 below)
+  const float mb = m == -INFINITY ? 0.0f : m * kLog2e;
+
+  const float se = si >= 0 ? ex2(fmaf(sv, kLog2e, -mb)) : 0.0f;
+  float e[RE ? 1 : NV][kPer];
+  float d = se;
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+    if (lo + tid + T * k < hi) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float e0 = ex2(fmaf(bf16_lo(v[k].w[j]), kLog2e, -mb));
+        const float e1 = ex2(fmaf(bf16_hi(v[k].w[j]), kLog2e, -mb));
+        if constexpr (!RE) {
+          e[k][2 * j] = e0;
+          e[k][2 * j + 1] = e1;
+        }
+        d += e0 + e1;
+      }
+    }
+  d = warp_sum(d);
+  if (lane == 0) red[1][warp] = d;
+  __syncthreads();
+  d = warp_sum(lane < W ? red[1][lane] : 0.0f);
+  cluster_wait();  // every peer's mbarrier is initialised
+  if (tid < static_cast<int>(C))
+    st_async_f4(&pairs[q], &xbar, static_cast<uint32_t>(tid), make_float4(m, d, 0.0f, 0.0f));
+  if (!mbar_wait_bounded(&xbar, 0, kBfWaitBudget) && tid == 0) atomicCAS(err, 0, FR_DEVERR_TIMEOUT);
+  float M = -INFINITY;
+  for (uint32_t r = 0; r < C; ++r) M = max_nan(M, pairs[r].x);
+  float D = 0.0f;
+  if (M != -INFINITY)
+    for (uint32_t r = 0; r < C; ++r) D += pairs[r].y * ex2((pairs[r].x - M) * kLog2e);
+  const float scale = (M == -INFINITY ? 1.0f : ex2((m - M) * kLog2e)) * __frcp_rn(D);
+
+  uint16_t *vy = py + sp.head;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int64_t vi = lo + tid + static_cast<int64_t>(T) * k;
+    if (vi < hi) {
+      V8 o;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if constexpr (RE)
+          o.w[j] = pack_bf16x2(ex2(fmaf(bf16_lo(v[k].w[j]), kLog2e, -mb)) * scale,
+                               ex2(fmaf(bf16_hi(v[k].w[j]), kLog2e, -mb)) * scale);
+        else
+          o.w[j] = pack_bf16x2(e[k][2 * j] * scale, e[k][2 * j + 1] * scale);
+      }
+      st_stream_v8(vy + vi * kPer, o);
+    }
+  }
+  if (si >= 0) st_stream_u16(py + si, to_bf16(se * scale));
 }
 
 // Persistent form, lane-strided scalars (x and y rows out of phase): NS
@@ -351,6 +466,57 @@ cudaError_t launch_bf16_cta(const uint16_t *x, uint16_t *y, int64_t rows, int64_
                   0, x, y, cols, ldx, ldy);
 }
 }  // namespace
+
+namespace {
+// The smallest CTA size, then the smallest cluster, whose registers hold the
+// row (nv vectors of 16 per thread).
+bool bf16_cluster_shape(int64_t cols, int nv, int *T, int *C) {
+  const int64_t nvec = cols / kPer;  // at least the body's vectors
+  for (int t = 256; t <= 1024; t <<= 1)
+    for (int c = 2; c <= kBfClusterMax; c <<= 1)
+      if (nvec <= static_cast<int64_t>(c) * t * nv) {
+        *T = t;
+        *C = c;
+        return true;
+      }
+  return false;
+}
+
+template <int T, int NV, bool RE>
+cudaError_t launch_bf16_cluster(const uint16_t *x, uint16_t *y, int64_t rows, int64_t cols,
+                                int64_t ldx, int64_t ldy, int C, cudaStream_t s) {
+  int *err = nullptr;
+  cudaError_t e = device_error_word(&err);
+  if (e != cudaSuccess) return e;
+  return launch_k(softmax_bf16_cluster<T, NV, RE>, dim3(static_cast<unsigned>(rows * C)), dim3(T),
+                  0, s, static_cast<unsigned>(C), x, y, cols, ldx, ldy, err);
+}
+}  // namespace
+
+int64_t softmax_bf16_split_max_cols() {
+  return static_cast<int64_t>(kBfClusterMax) * 1024 * 2 * kPer;
+}
+
+cudaError_t launch_softmax_bf16_split(const uint16_t *x, uint16_t *y, int64_t rows, int64_t cols,
+                                      int64_t ldx, int64_t ldy, cudaStream_t s) {
+  // Exponentials recomputed in the writing pass (4 vectors a thread, twice
+  // the bytes in flight) unless the row needs 1024-thread CTAs; measured on
+  // GB300, bf16 [1022, 65537]: 45.6 us recomputed, 60.1 held (2 vectors a
+  // thread), 55.4 looped.  FR_SOFTMAX_BF16_SPLIT=hold pins the held form.
+  const char *pin = getenv("FR_SOFTMAX_BF16_SPLIT");
+  const bool re = pin == nullptr || strcmp(pin, "hold") != 0;
+  int T = 0, C = 0;
+  if (re && bf16_cluster_shape(cols, 4, &T, &C) && T <= 512 && rows * C <= 0x7fffffff) {
+    if (T == 256) return launch_bf16_cluster<256, 4, true>(x, y, rows, cols, ldx, ldy, C, s);
+    return launch_bf16_cluster<512, 4, true>(x, y, rows, cols, ldx, ldy, C, s);
+  }
+  if (!bf16_cluster_shape(cols, 2, &T, &C) || rows * C > 0x7fffffff) return cudaErrorInvalidValue;
+  switch (T) {
+    case 256: return launch_bf16_cluster<256, 2, false>(x, y, rows, cols, ldx, ldy, C, s);
+    case 512: return launch_bf16_cluster<512, 2, false>(x, y, rows, cols, ldx, ldy, C, s);
+    default: return launch_bf16_cluster<1024, 2, false>(x, y, rows, cols, ldx, ldy, C, s);
+  }
+}
 
 cudaError_t launch_softmax_bf16_persistent(const uint16_t *x, uint16_t *y, int64_t rows,
                                            int64_t cols, int64_t ldx, int64_t ldy, bool vec,

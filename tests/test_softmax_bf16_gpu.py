@@ -15,7 +15,7 @@ from synth import workloads
 pytestmark = pytest.mark.gpu
 
 COLS = [1, 2, 15, 16, 17, 31, 129, 511, 512, 513, 1000, 1024, 1536, 2047, 2048, 2049, 4097,
-        8192, 16385, 32768, 32769, 65537]
+        8192, 16385, 32768, 32769, 65537, 131073, 262144]
 # (offset of x, offset of y, extra row padding), in elements
 LAYOUTS = [(0, 0, 0), (3, 3, 7), (0, 5, 0)]
 
@@ -34,7 +34,8 @@ def forms(cols, layout=(0, 0, 0)):
     32768 when x and y rows share their 32-byte phase"""
     in_phase = (layout[0] - layout[1]) * 2 % 32 == 0
     persistent = cols <= 2048 or (cols <= 32768 and in_phase)
-    return (["persistent"] if persistent else []) + ["looped", "auto"]
+    split = in_phase and 2048 < cols <= 262144  # a cluster of CTAs per row
+    return (["persistent"] if persistent else []) + (["split"] if split else []) + ["looped", "auto"]
 
 
 def run(bits, form, layout=(0, 0, 0)):
