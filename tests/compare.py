@@ -1,6 +1,8 @@
 """Element-wise comparison of GPU results with the oracle.
 
-Rules (the reading of the tolerances is stated in the design doc):
+Rules (fp32 outputs within 1e-5 relative, bf16 within 1e-2, with a floor
+per output kind where the fp32 error scales with something other than the
+value itself, as noted beside each entry of TOL):
   * NaN must sit exactly where the oracle has NaN; +-inf must match exactly;
   * otherwise |g - o| <= rtol * max(|o|, floor) element by element;
   * integer results (indices, gathered bf16 values) are compared bit for bit.
