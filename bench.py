@@ -551,25 +551,26 @@ def extra_configs(fr, traffic, workloads, timed, dev, peak, args, world, names=N
 
 
 def xent_box(fr, workloads, dev, timed, args, peak):
-    """Every runnable point of the cross-entropy kernel's configuration box
-    (threads x vectors x stages x CTAs per SM), timed like the bench's other
-    lines: the measurements behind the default configuration."""
+    """Every runnable point of the cross-entropy kernels' configuration space
+    (the ring kernel's box threads x vectors x stages x CTAs per SM, and the
+    warp-per-row points), timed like the bench's other lines: the
+    measurements behind the default configuration."""
     from reduction_pointwise_row_gb300 import traffic
     calls, op, rows, cols, _ = setup_workload("xent", fr, workloads, dev)
     nb = traffic.algorithmic_bytes(op, rows, cols)
     steps = max(3, min(args.steps, 30))
     out = []
-    for t in (128, 256, 512, 1024):
-        for u in (1, 2, 4, 8):
-            for s in (2, 4, 8):
-                for g in (1, 2, 4, 8, 16):
-                    try:
-                        fr.fr_xent_set_config(rows, cols, (t, u, s, g))
-                    except fr.FRError:
-                        continue
-                    sec, _, _ = timed(calls, steps, args.warmup, 1)
-                    out.append({"config": [t, u, s, g], "us": round(sec * 1e6, 2),
-                                "frac": round(nb / sec / 1e9 / peak, 4)})
+    points = [(t, u, s, g) for t in (128, 256, 512, 1024) for u in (1, 2, 4, 8)
+              for s in (2, 4, 8) for g in (1, 2, 4, 8, 16)]
+    points += [(32, u, 1, g) for u in (4, 8) for g in (1, 2, 4, 8, 16)]  # warp per row
+    for cfg in points:
+        try:
+            fr.fr_xent_set_config(rows, cols, cfg)
+        except fr.FRError:
+            continue
+        sec, _, _ = timed(calls, steps, args.warmup, 1)
+        out.append({"config": list(cfg), "us": round(sec * 1e6, 2),
+                    "frac": round(nb / sec / 1e9 / peak, 4)})
     fr.fr_xent_set_config(rows, cols, None)
     out.sort(key=lambda r: r["us"])
     return {"only": "xent_box", "rows": rows, "cols": cols, "runnable": len(out),

@@ -322,12 +322,19 @@ fr_status fr_coordinate_descent(int32_t p, const int32_t *lo, const int32_t *hi,
                                 double eps, fr_cost_fn cost, void *ctx, int32_t *acceptances,
                                 int32_t *evaluations);
 
-/* A launch configuration of the cross-entropy kernel (fr_xent without
- * argmax): each field a power of two. */
+/* A launch configuration of the cross-entropy kernels (fr_xent without
+ * argmax): each field a power of two.  Two families:
+ *   the ring kernel (a CTA per row, each thread streaming its 16-byte pieces
+ *   through a cp.async ring): threads 128 .. 1024, vectors 1 .. 8 (16-byte
+ *   copies per thread per ring item), stages 2 .. 8, ctas_per_sm 1 .. 16;
+ *   the warp-per-row kernel (a warp streams a row with 32-byte register
+ *   loads, 256-thread CTAs): threads 32, vectors 4 or 8 (32-byte vectors a
+ *   lane holds), stages 1, ctas_per_sm 1 .. 16 (a cap).
+ * The default is the warp-per-row point (32, 8, 1, 2). */
 typedef struct {
-  int32_t threads;     /* threads per CTA, 128 .. 1024 */
-  int32_t vectors;     /* 16-byte copies per thread per ring item, 1 .. 8 */
-  int32_t stages;      /* items in each thread's copy ring, 2 .. 8 */
+  int32_t threads;     /* threads per CTA (32: a warp per row) */
+  int32_t vectors;     /* copies or vectors per thread, see above */
+  int32_t stages;      /* items in each thread's copy ring (1: no ring) */
   int32_t ctas_per_sm; /* CTAs per SM of the persistent grid, 1 .. 16 */
 } fr_xent_config;
 
@@ -351,9 +358,11 @@ fr_status fr_xent_set_config(int64_t rows, int64_t cols, int64_t ld, const fr_xe
  * Chooses and records the configuration for this shape by measurement on the
  * caller's data (Algorithm 9.1 then Algorithm 9.2).  If a configuration is
  * already recorded for the shape it is returned unmeasured (Algorithm 9.1,
- * line 1).  Otherwise a candidate set of six configurations is timed (those
- * that cannot run cost +inf), and coordinate descent with threshold `eps`
- * walks the box threads x vectors x stages x ctas_per_sm from the fastest.
+ * line 1).  Otherwise a candidate set of eight configurations (two warp-per-
+ * row points, six ring points) is timed (those that cannot run cost +inf),
+ * coordinate descent with threshold `eps` walks the ring's box threads x
+ * vectors x stages x ctas_per_sm from the fastest ring point, and the faster
+ * of its result and the best candidate is recorded.
  * Each configuration is timed over `reps` launches after one warm-up launch
  * (CUDA events on `stream`, the median).  The launches write `loss` (which
  * may be NULL); the call synchronises `stream` and must not be captured into

@@ -567,35 +567,49 @@ fr_status fr_xent_tune(const void *logits, const int64_t *target, float *loss, i
     ++evals;
     return time_xent_config(c, lg, target, loss, rows, cols, ld, ignore_index, reps, info, s);
   };
-  // Algorithm 9.1: the fastest of a small candidate set (the hand-picked
-  // shapes the kernel was developed with, and the default).
-  const fr::XentConfig cands[] = {fr::xent_default_config(), {256, 4, 4, 2}, {512, 4, 4, 1},
-                                  {128, 4, 4, 4},            {256, 2, 8, 2}, {256, 8, 2, 2}};
-  double t_best = std::numeric_limits<double>::infinity();
+  // Algorithm 9.1: the fastest of a small candidate set -- the default (the
+  // warp-per-row kernel), its 4-vector point, and the ring points the kernel
+  // was developed with.
+  const fr::XentConfig cands[] = {fr::xent_default_config(), {32, 4, 1, 4},   {128, 8, 2, 4},
+                                  {256, 4, 4, 2},            {512, 4, 4, 1},  {128, 4, 4, 4},
+                                  {256, 2, 8, 2},            {256, 8, 2, 2}};
+  double t_best = std::numeric_limits<double>::infinity(), t_ring = t_best;
+  fr::XentConfig ring{};
   for (const fr::XentConfig &c : cands) {
     const double t = cost(c);
     if (t < t_best) {
       t_best = t;
       best = c;
     }
+    if (c.threads >= 128 && t < t_ring) {
+      t_ring = t;
+      ring = c;
+    }
   }
   if (!std::isfinite(t_best)) return FR_ERR_CUDA;  // nothing could run
-  // Algorithm 9.2 from there over the box of log2 parameters.
-  const int lo[4] = {7, 0, 1, 0}, hi[4] = {10, 3, 3, 4};
-  int c[4] = {ilog2(best.threads), ilog2(best.vectors), ilog2(best.stages),
-              ilog2(best.ctas_per_sm)};
-  const fr::CdResult r = fr::coordinate_descent(4, lo, hi, c, eps, [&](const int *q) {
-    const fr::XentConfig x{1 << q[0], 1 << q[1], 1 << q[2], 1 << q[3]};
-    if (x.threads == best.threads && x.vectors == best.vectors && x.stages == best.stages &&
-        x.ctas_per_sm == best.ctas_per_sm)
-      return t_best;  // already timed
-    return cost(x);
-  });
-  best = fr::XentConfig{1 << c[0], 1 << c[1], 1 << c[2], 1 << c[3]};
+  double t_final = t_best;
+  if (std::isfinite(t_ring)) {
+    // Algorithm 9.2 from the fastest ring point over the ring's box of log2
+    // parameters (the warp-per-row points lie outside it)
+    const int lo[4] = {7, 0, 1, 0}, hi[4] = {10, 3, 3, 4};
+    int c[4] = {ilog2(ring.threads), ilog2(ring.vectors), ilog2(ring.stages),
+                ilog2(ring.ctas_per_sm)};
+    const fr::CdResult r = fr::coordinate_descent(4, lo, hi, c, eps, [&](const int *q) {
+      const fr::XentConfig x{1 << q[0], 1 << q[1], 1 << q[2], 1 << q[3]};
+      if (x.threads == ring.threads && x.vectors == ring.vectors && x.stages == ring.stages &&
+          x.ctas_per_sm == ring.ctas_per_sm)
+        return t_ring;  // already timed
+      return cost(x);
+    });
+    if (r.t < t_best) {
+      best = fr::XentConfig{1 << c[0], 1 << c[1], 1 << c[2], 1 << c[3]};
+      t_final = r.t;
+    }
+  }
   fr::xent_record_config(info.device, rows, cols, ld, &best);
   if (out) *out = to_c(best);
   if (evaluations) *evaluations = evals;
-  if (best_ms) *best_ms = static_cast<float>(r.t);
+  if (best_ms) *best_ms = static_cast<float>(t_final);
   return cudaGetLastError() == cudaSuccess ? FR_OK : FR_ERR_CUDA;
 }
 

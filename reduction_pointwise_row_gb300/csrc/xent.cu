@@ -395,6 +395,162 @@ xent_async(const void *__restrict__ logits, const int64_t *__restrict__ target,
   if (loss_mean != nullptr) finish_mean<T>(ws, loss_mean, cta_sum, cta_cnt);
 }
 
+// ---- warp-per-row variant ------------------------------------------------------
+// Each warp streams whole rows with 32-byte register loads (NV vectors of
+// EPV logits per lane in flight, evict-first), folding every chunk into the
+// lane's online pair (m, l); the lane pairs merge by shuffles (Proposition
+// 9.1), so a row needs no CTA barrier.  The grid is persistent (warp w takes
+// rows w, w + W, ...); each warp adds its rows' losses in row order, the CTA
+// adds its warps' sums in warp order, and the last CTA adds the CTAs' sums
+// in a fixed order (finish_mean).
+constexpr int kWarpCta = 256;
+
+template <bool ARGMAX, bool F32, int NV>
+__global__ void __launch_bounds__(kWarpCta, ARGMAX || NV > 4 ? 2 : 4)
+xent_warp(const void *__restrict__ logits, const int64_t *__restrict__ target,
+          float *__restrict__ loss, float *__restrict__ target_logit, int64_t *__restrict__ argmax,
+          float *__restrict__ loss_mean, void *__restrict__ ws, int64_t rows, int64_t cols,
+          int64_t ld, int64_t ignore_index) {
+  pdl_enter();
+  constexpr int ES = F32 ? 4 : 2;  // bytes per logit
+  constexpr int EPV = 32 / ES;     // logits per 32-byte vector
+  constexpr int W = kWarpCta / 32;
+  __shared__ double warp_s[W];
+  __shared__ long long warp_c[W];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * W + warp;
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * W;
+  const unsigned char *base = static_cast<const unsigned char *>(logits);
+  double w_sum = 0.0;
+  long long w_cnt = 0;
+  for (int64_t row = gw; row < rows; row += nw) {
+    const unsigned char *pr = base + row * ld * ES;
+    const RowSplit sp = row_split(pr, cols, ES);
+    const unsigned char *pv = pr + static_cast<int64_t>(sp.head) * ES;
+    MD st{-INFINITY, 0.0f};
+    ArgBest best{-INFINITY, INT64_MAX};
+    for (int64_t b0 = 0; b0 < sp.nvec; b0 += 32 * NV) {
+      V8 v[NV];
+#pragma unroll
+      for (int k = 0; k < NV; ++k) {
+        const int64_t vi = b0 + lane + 32 * k;
+        if (vi < sp.nvec) v[k] = ld_stream_v8(pv + vi * 32);
+        else
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[k].w[j] = F32 ? 0xFF800000u : 0xFF80FF80u;  // -inf
+      }
+      // logit j (0 .. EPV - 1) of vector k
+      auto elem = [&](int k, int j) {
+        if constexpr (F32) return __uint_as_float(v[k].w[j]);
+        else return (j & 1) ? bf16_hi(v[k].w[j >> 1]) : bf16_lo(v[k].w[j >> 1]);
+      };
+      float cm;
+      if constexpr (F32) {
+        cm = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) cm = max_nan(cm, __uint_as_float(v[k].w[j]));
+      } else {
+        uint32_t m2 = 0xFF80FF80u;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) m2 = max_nan_bf16x2(m2, v[k].w[j]);
+        cm = max_nan(bf16_lo(m2), bf16_hi(m2));
+      }
+      if constexpr (ARGMAX) {
+        if (best.i == INT64_MAX || cm > best.v || (cm != cm && best.v == best.v)) {
+          bool found = false;
+#pragma unroll
+          for (int k = 0; k < NV; ++k) {
+            const int64_t vi = b0 + lane + 32 * k;
+#pragma unroll
+            for (int j = 0; j < EPV; ++j) {
+              const float e = elem(k, j);
+              const bool hit = (cm != cm) ? (e != e) : (e == cm);
+              if (!found && hit && vi < sp.nvec) {
+                found = true;
+                best = ArgBest{cm, sp.head + EPV * vi + j};
+              }
+            }
+          }
+        }
+      }
+      st = fold_chunk(st, cm);
+      if (st.m != -INFINITY) {
+        const float nmb = -st.m * kLog2e;
+        const uint64_t l2e2 = pack_f32x2(kLog2e, kLog2e), nmb2 = pack_f32x2(nmb, nmb);
+        uint64_t acc2 = 0;
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+#pragma unroll
+          for (int j = 0; j < EPV / 2; ++j) {
+            const uint64_t t2 = fma_f32x2(pack_f32x2(elem(k, 2 * j), elem(k, 2 * j + 1)), l2e2, nmb2);
+            acc2 = add_f32x2(acc2, pack_f32x2(ex2(f32x2_lo(t2)), ex2(f32x2_hi(t2))));
+          }
+        st.d += f32x2_lo(acc2) + f32x2_hi(acc2);
+      }
+    }
+    // head and tail scalars, one per lane (fewer than EPV each)
+    int64_t si = -1;
+    if (lane < sp.head) si = lane;
+    else if (lane < sp.head + sp.tail) si = sp.head + sp.nvec * EPV + (lane - sp.head);
+    if (si >= 0) {
+      const float e = logit_stream<F32>(pr, si);
+      st = md_merge(st, MD{e, 1.0f});
+      if constexpr (ARGMAX) best = arg_better(best, ArgBest{e, si});
+    }
+    st = warp_md(st);
+    if constexpr (ARGMAX) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        ArgBest other{__shfl_xor_sync(0xffffffffu, best.v, o),
+                      static_cast<int64_t>(__shfl_xor_sync(0xffffffffu,
+                                                           static_cast<long long>(best.i), o))};
+        best = arg_better(best, other);
+      }
+    }
+    if (lane == 0) {
+      const int64_t t = target[row];
+      const float lse = st.m + logf(st.d);
+      float l, xt;
+      if (t == ignore_index) {
+        l = 0.0f;
+        xt = 0.0f;
+      } else if (t < 0 || t >= cols) {
+        l = __int_as_float(0x7fc00000);
+        xt = l;
+        atomicCAS(&g_fr_device_error, 0, FR_DEVERR_BAD_TARGET);
+      } else {
+        xt = logit_at<F32>(pr, t);
+        l = lse - xt;
+      }
+      if (loss) loss[row] = l;
+      if (target_logit) target_logit[row] = xt;
+      if constexpr (ARGMAX) argmax[row] = best.i;
+      if (t != ignore_index) {
+        w_sum += static_cast<double>(l);
+        ++w_cnt;
+      }
+    }
+  }
+  if (loss_mean == nullptr) return;
+  if (lane == 0) {
+    warp_s[warp] = w_sum;
+    warp_c[warp] = w_cnt;
+  }
+  __syncthreads();
+  double cta_sum = 0.0;
+  long long cta_cnt = 0;
+  if (threadIdx.x == 0)
+    for (int i = 0; i < W; ++i) {  // the CTA's warps in order
+      cta_sum += warp_s[i];
+      cta_cnt += warp_c[i];
+    }
+  finish_mean<kWarpCta>(ws, loss_mean, cta_sum, cta_cnt);
+}
+
 }  // namespace
 
 size_t xent_workspace(int64_t rows, int sm_count) {
@@ -444,14 +600,49 @@ std::vector<Recorded> g_recorded;
 
 }  // namespace
 
-// The fastest of the 67 runnable points of the box, measured on GB300 for
-// bf16 [8192, 50257] with the mean (back to back, rotating inputs):
-// (128, 8, 2, 4) 135.7 us, (128, 2, 8, 4) 137.1, (128, 2, 4, 4) 139.1,
-// (128, 4, 4, 4) 139.5, (256, 4, 4, 2) 143.0 ... (128, 1, 2, 1) 938.6.
-XentConfig xent_default_config() { return XentConfig{128, 8, 2, 4}; }
+cudaError_t capped_smem(size_t need, int per_sm, size_t *out);
+cudaError_t launch_warp_kernel(const void *kern, int per_sm_cap, const void *logits,
+                               const int64_t *target, float *loss, float *loss_mean,
+                               float *target_logit, int64_t *argmax, int64_t rows, int64_t cols,
+                               int64_t ld, int64_t ignore_index, void *workspace, int sm_count,
+                               cudaStream_t s);
+template <bool ARGMAX, bool F32>
+const void *warp_kernel(int nv);
+
+// The default point: the warp-per-row kernel with 8 vectors a lane, two CTAs
+// per SM.  Measured on GB300 for bf16 [8192, 50257] with the mean (back to
+// back, rotating inputs; every runnable point of both families): (32, 8, 1, 2)
+// 126.5 us, (32, 4, 1, 4) 127.5, the ring's fastest point (128, 8, 2, 4)
+// 129.7, (128, 4, 4, 4) 131.7, (128, 2, 8, 4) 136.9 ... (32, 4, 1, 1) 189.2,
+// (128, 1, 2, 1) 938.6.
+XentConfig xent_default_config() { return XentConfig{32, 8, 1, 2}; }
+
+namespace {
+// The warp-per-row family: threads 32 (a warp per row), vectors 4 or 8,
+// stages 1 (no ring), ctas_per_sm the cap on 256-thread CTAs per SM.
+cudaError_t warp_config_check(const XentConfig &cfg) {
+  auto pow2_in = [](int v, int lo, int hi) { return v >= lo && v <= hi && (v & (v - 1)) == 0; };
+  if ((cfg.vectors != 4 && cfg.vectors != 8) || cfg.stages != 1 ||
+      !pow2_in(cfg.ctas_per_sm, 1, kMaxCtasPerSm))
+    return cudaErrorInvalidValue;
+  const void *kern = warp_kernel<false, false>(cfg.vectors);
+  cudaFuncAttributes fa{};
+  cudaError_t err = cudaFuncGetAttributes(&fa, kern);
+  if (err != cudaSuccess) return err;
+  if (fa.localSizeBytes > 0) return cudaErrorInvalidConfiguration;  // spills: t = inf
+  if ((err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 0)) !=
+      cudaSuccess)
+    return err;
+  int per_sm = 0;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarpCta, 0);
+  if (err != cudaSuccess) return err;
+  return per_sm >= cfg.ctas_per_sm ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+}  // namespace
 
 cudaError_t xent_config_check(const XentConfig &cfg, int max_smem_optin) {
   auto pow2_in = [](int v, int lo, int hi) { return v >= lo && v <= hi && (v & (v - 1)) == 0; };
+  if (cfg.threads == 32) return warp_config_check(cfg);
   if (!pow2_in(cfg.threads, 128, 1024) || !pow2_in(cfg.vectors, 1, 8) ||
       !pow2_in(cfg.stages, 2, 8) || !pow2_in(cfg.ctas_per_sm, 1, kMaxCtasPerSm))
     return cudaErrorInvalidValue;
@@ -509,6 +700,10 @@ cudaError_t launch_xent_config(const XentConfig &cfg, const void *logits,
                                int max_smem_optin, cudaStream_t s) {
   cudaError_t e = xent_config_check(cfg, max_smem_optin);
   if (e != cudaSuccess) return e;
+  if (cfg.threads == 32)
+    return launch_warp_kernel(warp_kernel<false, false>(cfg.vectors), cfg.ctas_per_sm, logits,
+                              target, loss, loss_mean, target_logit, nullptr, rows, cols, ld,
+                              ignore_index, workspace, sm_count, s);
   const AsyncEntry *a = async_entry(cfg);
   size_t smem = 0;
   e = capped_smem(static_cast<size_t>(a->NS) * a->U * a->T * 16, cfg.ctas_per_sm, &smem);
@@ -551,66 +746,79 @@ void xent_record_config(int device, int64_t rows, int64_t cols, int64_t ld,
   if (cfg) g_recorded.push_back(Recorded{device, rows, cols, ld, *cfg});
 }
 
-// The kernel at the default point of the box, for the launches the box's
-// table does not cover: with argmax (bf16 or fp32 logits) and fp32 logits
-// without it.  Up to the default's CTAs per SM (fewer when the larger
-// argmax kernel keeps fewer resident).
-template <bool ARGMAX, bool F32>
-cudaError_t launch_xent_default(const void *logits, const int64_t *target, float *loss,
-                                float *loss_mean, float *target_logit, int64_t *argmax,
-                                int64_t rows, int64_t cols, int64_t ld, int64_t ignore_index,
-                                void *workspace, int sm_count, cudaStream_t s) {
-  constexpr int T = 128, U = 8, NS = 2;
-  const XentConfig d = xent_default_config();
-  static_assert(T == 128 && U == 8 && NS == 2, "keep in step with xent_default_config()");
-  if (d.threads != T || d.vectors != U || d.stages != NS) return cudaErrorInvalidValue;
-  const void *kern = reinterpret_cast<const void *>(&xent_async<ARGMAX, T, U, NS, F32>);
-  const size_t smem = static_cast<size_t>(NS) * U * T * 16;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
+// The warp-per-row kernel: a persistent grid of at most per_sm_cap 256-thread
+// CTAs per SM (and what stays resident), shrunk so that every warp takes the
+// same number of rows (8192 rows on 152 SMs x 4 CTAs: 2 rows a warp on 512
+// CTAs, 1.5 % faster than 1 or 2 rows on 608), its dynamic shared memory
+// padded so that no more than that many CTAs share an SM.
+cudaError_t launch_warp_kernel(const void *kern, int per_sm_cap, const void *logits,
+                               const int64_t *target, float *loss, float *loss_mean,
+                               float *target_logit, int64_t *argmax, int64_t rows, int64_t cols,
+                               int64_t ld, int64_t ignore_index, void *workspace, int sm_count,
+                               cudaStream_t s) {
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, T, smem);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 0);
   if (e != cudaSuccess) return e;
-  if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  if (per_sm > d.ctas_per_sm) per_sm = d.ctas_per_sm;
-  size_t smem_cap = 0;
-  if ((e = capped_smem(smem, per_sm, &smem_cap)) != cudaSuccess) return e;
-  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(smem_cap))) != cudaSuccess)
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarpCta, 0)) !=
+      cudaSuccess)
     return e;
-  int64_t grid = static_cast<int64_t>(sm_count) * per_sm;
-  if (grid > rows) grid = rows;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  const int resident = per_sm;
+  if (per_sm > per_sm_cap) per_sm = per_sm_cap;
+  if (per_sm > kMaxCtasPerSm) per_sm = kMaxCtasPerSm;
+  constexpr int64_t W = kWarpCta / 32;
+  const int64_t warps = static_cast<int64_t>(sm_count) * per_sm * W;
+  const int64_t per_warp = (rows + warps - 1) / warps;  // rows a warp takes
+  const int64_t grid = (rows + per_warp * W - 1) / (per_warp * W);
+  // pad only when the cap is below what the registers allow (the padding's
+  // shared-memory carveout cost 3 % when it was not needed)
+  size_t smem = 0;
+  if (per_sm < resident && (e = capped_smem(0, per_sm, &smem)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(smem))) != cudaSuccess)
+    return e;
   if (loss_mean != nullptr) {
     e = cudaMemsetAsync(workspace, 0, 16, s);
     if (e != cudaSuccess) return e;
   }
   void *args[] = {&logits, &target, &loss, &target_logit, &argmax, &loss_mean, &workspace,
                   &rows, &cols, &ld, &ignore_index};
-  return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(T), args, smem_cap, s);
+  return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kWarpCta), args, smem, s);
+}
+
+template <bool ARGMAX, bool F32>
+const void *warp_kernel(int nv) {
+  if constexpr (ARGMAX) {
+    (void)nv;
+    return reinterpret_cast<const void *>(&xent_warp<true, F32, 4>);
+  } else {
+    return nv == 8 ? reinterpret_cast<const void *>(&xent_warp<false, F32, 8>)
+                   : reinterpret_cast<const void *>(&xent_warp<false, F32, 4>);
+  }
 }
 
 cudaError_t launch_xent(const void *logits, bool f32, const int64_t *target, float *loss,
                         float *loss_mean, float *target_logit, int64_t *argmax, int64_t rows,
                         int64_t cols, int64_t ld, int64_t ignore_index, void *workspace,
                         int sm_count, int max_smem_optin, cudaStream_t s) {
-  if (f32)  // fp32 logits: the default point of the box
-    return argmax != nullptr
-               ? launch_xent_default<true, true>(logits, target, loss, loss_mean, target_logit,
-                                                 argmax, rows, cols, ld, ignore_index, workspace,
-                                                 sm_count, s)
-               : launch_xent_default<false, true>(logits, target, loss, loss_mean, target_logit,
-                                                  argmax, rows, cols, ld, ignore_index, workspace,
-                                                  sm_count, s);
+  const XentConfig d = xent_default_config();
+  // fp32 logits: the warp-per-row kernel at the default point; argmax: the
+  // same kernel with 4 vectors a lane (the argmax state leaves no registers
+  // for 8), two CTAs per SM
   if (argmax != nullptr)
-    return launch_xent_default<true, false>(logits, target, loss, loss_mean, target_logit, argmax,
-                                            rows, cols, ld, ignore_index, workspace, sm_count, s);
+    return launch_warp_kernel(f32 ? warp_kernel<true, true>(4) : warp_kernel<true, false>(4), 2,
+                              logits, target, loss, loss_mean, target_logit, argmax, rows, cols,
+                              ld, ignore_index, workspace, sm_count, s);
+  if (f32)
+    return launch_warp_kernel(warp_kernel<false, true>(d.vectors), d.ctas_per_sm, logits, target,
+                              loss, loss_mean, target_logit, argmax, rows, cols, ld, ignore_index,
+                              workspace, sm_count, s);
   // the configuration recorded for this shape (fr_xent_tune / _set_config),
-  // else the default point of the box
+  // else the default point
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  XentConfig cfg = xent_default_config();
+  XentConfig cfg = d;
   xent_recorded_config(dev, rows, cols, ld, &cfg);
   return launch_xent_config(cfg, logits, target, loss, loss_mean, target_logit, rows, cols, ld,
                             ignore_index, workspace, sm_count, max_smem_optin, s);

@@ -356,12 +356,13 @@ def test_layernorm_constant_rows(o):
 
 # ---------------------------------------------------------------- cross entropy
 
-# the default point of the configuration box (None) and runnable points of
-# other shapes: CTA sizes 128 .. 1024, 1 .. 8 vectors per ring item, 2 .. 8
-# stages, 1 .. 4 CTAs per SM (the argmax kernel always runs at the default
-# point; every runnable point is also checked in test_tune_gpu.py)
-XENT_KERNELS = [None, (256, 4, 4, 2), (512, 2, 8, 1), (1024, 1, 2, 1), (128, 1, 2, 4),
-                (256, 8, 2, 2)]
+# the default point (None: the warp-per-row kernel), its 4-vector point, and
+# runnable points of the ring kernel's box: CTA sizes 128 .. 1024, 1 .. 8
+# vectors per ring item, 2 .. 8 stages, 1 .. 4 CTAs per SM (the argmax
+# kernel always runs at the default point; every runnable point is also
+# checked in test_tune_gpu.py)
+XENT_KERNELS = [None, (32, 4, 1, 4), (128, 8, 2, 4), (256, 4, 4, 2), (512, 2, 8, 1),
+                (1024, 1, 2, 1), (128, 1, 2, 4), (256, 8, 2, 2)]
 
 
 def run_xent(bits, target, ignore=-100, offset=0, pad=0, kernel=None, argmax=True):

@@ -1,6 +1,7 @@
 """GPU side of the launch-configuration search ("Stax (4): GPU Codegen and
 Dynamic Shapes", section 9.6): every compiled point of the cross-entropy
-kernel's configuration box gives the oracle's results, configurations that
+kernels' configuration space (the ring kernel's box and the warp-per-row
+points) gives the oracle's results, configurations that
 cannot run are refused, and the tuner (Algorithm 9.1 then 9.2) records a
 configuration that fr_xent then uses."""
 import numpy as np
@@ -16,6 +17,7 @@ from synth import workloads
 pytestmark = pytest.mark.gpu
 
 BOX = [(t, u, s) for t in (128, 256, 512, 1024) for u in (1, 2, 4, 8) for s in (2, 4, 8)]
+WARP = [(32, 4, 1), (32, 8, 1)]  # the warp-per-row family
 
 
 @pytest.fixture(scope="module")
@@ -31,7 +33,7 @@ def test_every_runnable_configuration_matches_the_oracle(o):
     t = torch.from_numpy(w.arrays["target"]).cuda()
     ran = 0
     try:
-        for (th, u, s) in BOX:
+        for (th, u, s) in BOX + WARP:
             for g in (1, 2, 4):
                 try:
                     fr.fr_xent_set_config(rows, cols, (th, u, s, g))
@@ -48,18 +50,20 @@ def test_every_runnable_configuration_matches_the_oracle(o):
                 ran += 1
     finally:
         fr.fr_xent_set_config(rows, cols, None)
-    assert ran >= 60
-    assert fr.fr_xent_get_config(rows, cols) == (128, 8, 2, 4)  # the default again
+    assert ran >= 63
+    assert fr.fr_xent_get_config(rows, cols) == (32, 8, 1, 2)  # the default again
     assert fr.fr_check_device_error() == 0
 
 
 def test_configurations_outside_the_box_or_unrunnable_are_refused():
-    for bad in [(100, 4, 4, 1), (256, 3, 4, 1), (256, 4, 1, 1), (256, 4, 4, 32), (2048, 4, 4, 1)]:
+    for bad in [(100, 4, 4, 1), (256, 3, 4, 1), (256, 4, 1, 1), (256, 4, 4, 32), (2048, 4, 4, 1),
+                (32, 4, 2, 1), (32, 2, 1, 1), (32, 4, 1, 32), (64, 4, 1, 1)]:
         with pytest.raises(fr.FRError, match="INVALID_ARG"):
             fr.fr_xent_set_config(64, 1000, bad)
     for cannot in [(1024, 8, 2, 1),    # not compiled: spills at 1024 threads x 8 vectors
                    (1024, 4, 8, 1),    # 512 KiB of ring
-                   (512, 4, 4, 16)]:   # 16 CTAs of 128 KiB cannot be resident
+                   (512, 4, 4, 16),    # 16 CTAs of 128 KiB cannot be resident
+                   (32, 8, 1, 4)]:     # 8 vectors a lane: two CTAs per SM at most
         with pytest.raises(fr.FRError, match="UNSUPPORTED_FORM"):
             fr.fr_xent_set_config(64, 1000, cannot)
 
@@ -73,8 +77,8 @@ def test_tune_records_a_configuration_that_fr_xent_uses(o):
     try:
         res = fr.fr_xent_tune(lg, t, -100, eps=0.02, reps=3)
         th, u, s, g = res["config"]
-        assert (th, u, s) in BOX and g in (1, 2, 4, 8, 16)
-        assert res["evaluations"] >= 6 and res["ms"] > 0
+        assert (th, u, s) in BOX + WARP and g in (1, 2, 4, 8, 16)
+        assert res["evaluations"] >= 8 and res["ms"] > 0
         assert fr.fr_xent_get_config(rows, cols) == res["config"]
         again = fr.fr_xent_tune(lg, t, -100)  # Algorithm 9.1, line 1: the record, unmeasured
         assert again["config"] == res["config"] and again["evaluations"] == 0
