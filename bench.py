@@ -484,8 +484,7 @@ def setup_workload(name, fr, workloads, dev, form="auto"):
         tg = torch.from_numpy(w.arrays["target"]).to(dev)
         for _ in range(nsets("xent", rows, cols)):
             lg = to_device(w.arrays["logits"], dev)
-            wsx = torch.empty(fr.fr_workspace_size("xent", rows, cols, "bf16"),
-                              dtype=torch.uint8, device=dev)
+            wsx = fr.fr_xent_workspace(rows, cols, "bf16", dev)
             # ranks > 1: the batch mean over every rank's rows (all-reduce of
             # the mean parts, then the finishing kernel)
             calls.append(lambda lg=lg, wsx=wsx: fr.fr_xent(lg, tg, -100, workspace=wsx,
@@ -497,8 +496,7 @@ def setup_workload(name, fr, workloads, dev, form="auto"):
         tg = torch.from_numpy(w.arrays["target"]).to(dev)
         for _ in range(nsets("xent_f32", rows, cols)):
             lg = to_device(w.arrays["logits"], dev)
-            wsx = torch.empty(fr.fr_workspace_size("xent", rows, cols, "f32"),
-                              dtype=torch.uint8, device=dev)
+            wsx = fr.fr_xent_workspace(rows, cols, "f32", dev)
             calls.append(lambda lg=lg, wsx=wsx: fr.fr_xent(lg, tg, -100, workspace=wsx))
         return calls, "xent_f32", rows, cols, 1
     raise ValueError(name)

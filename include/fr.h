@@ -83,6 +83,8 @@ typedef enum {
 #define FR_DEVERR_BAD_TARGET 1 /* a target outside [0, cols) and != ignore_index */
 #define FR_DEVERR_TIMEOUT 2    /* an asynchronous copy did not complete within its
                                   time budget; the kernel gave up and returned */
+#define FR_DEVERR_BAD_WORKSPACE 3 /* fr_xent's workspace was not prepared by
+                                    fr_xent_workspace_init (the mean is not written) */
 
 /* Library version (major*10000 + minor*100 + patch). */
 int fr_version(void);
@@ -255,14 +257,27 @@ fr_status fr_layernorm(const void *x, const float *gamma, const float *beta, voi
  *                configuration (fr_xent_tune and recorded configurations
  *                are for bf16 logits)
  *   workspace    fr_workspace_size(FR_OP_XENT, ...) bytes when loss_mean is
- *                requested (per-CTA partial sums and a ticket; the library
- *                zeroes the ticket on the stream before each launch).  After
+ *                requested (a ticket, the mean's parts and per-CTA partial
+ *                sums), prepared once by fr_xent_workspace_init; every call
+ *                leaves it prepared for the next (the last CTA resets the
+ *                ticket), so no call spends a launch on a reset.  A workspace
+ *                that was not prepared makes the call record
+ *                FR_DEVERR_BAD_WORKSPACE and leave loss_mean unwritten.  After
  *                the call it holds the mean's parts at FR_XENT_PARTS_OFFSET.
+ *                One call at a time may use a workspace.
  */
 fr_status fr_xent(const void *logits, const int64_t *target, float *loss, float *loss_mean,
                   float *target_logit, int64_t *argmax, int64_t rows, int64_t cols,
                   int64_t ld, int64_t ignore_index, fr_dtype dtype, fr_form form,
                   void *workspace, size_t workspace_bytes, fr_stream_t stream);
+
+/*
+ * Prepares an fr_xent workspace (writes its ticket; one single-thread kernel on
+ * `stream`).  Needed once after the workspace is allocated; fr_xent keeps it
+ * prepared.  FR_ERR_INVALID_ARG for NULL, FR_ERR_WORKSPACE_TOO_SMALL under 16
+ * bytes, FR_ERR_MISALIGNED unless 16-byte aligned.
+ */
+fr_status fr_xent_workspace_init(void *workspace, size_t workspace_bytes, fr_stream_t stream);
 
 /*
  * The mean over a batch whose rows are sharded across ranks (one process per

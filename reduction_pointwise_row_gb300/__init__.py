@@ -25,7 +25,8 @@ from . import buildlib as _build
 __all__ = [
     "FR_OK", "FRError", "lib", "fr_version", "fr_workspace_size", "fr_last_form",
     "fr_reduce_relu_add_sum", "fr_reduce_sumsq", "fr_softmax", "fr_softmax_host", "fr_layernorm",
-    "fr_xent",
+    "fr_xent", "fr_xent_workspace", "fr_xent_mean_from_parts", "xent_mean_parts",
+    "allreduce_mean_parts", "XENT_PARTS_OFFSET",
     "fr_reduce_relu_add_sum_split_static", "fr_check_device_error", "FORMS", "OPS",
     "EPILOGUES", "fr_coordinate_descent", "fr_xent_get_config", "fr_xent_set_config",
     "fr_xent_tune",
@@ -61,6 +62,7 @@ SIGNATURES = {
     "fr_xent": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _int, _vp,
                        _sz, _vp]),
     "fr_xent_mean_from_parts": (_int, [_vp, _vp, _vp]),
+    "fr_xent_workspace_init": (_int, [_vp, _sz, _vp]),
     "fr_check_device_error": (_int, [_vp, ctypes.POINTER(ctypes.c_int32)]),
     "fr_coordinate_descent": (_int, [ctypes.c_int32, _vp, _vp, _vp, ctypes.c_double, _vp, _vp,
                                      _vp, _vp]),
@@ -271,6 +273,35 @@ def fr_layernorm(x, gamma, beta, eps: float = 1e-5, form: str = "auto", out=None
 XENT_PARTS_OFFSET = 16  # FR_XENT_PARTS_OFFSET
 
 
+def fr_xent_workspace(rows: int, cols: int, dtype: str = "bf16", device=None, stream=None):
+    """A prepared cross-entropy workspace for this shape (fr_workspace_size
+    bytes, prepared by fr_xent_workspace_init on ``stream``).  Every fr_xent
+    call leaves it prepared; one call at a time may use it."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    n = fr_workspace_size("xent", rows, cols, dtype)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+    _check(lib().fr_xent_workspace_init(_ptr(ws), ws.numel(), _stream(stream, dev.index)),
+           "fr_xent_workspace_init")
+    return ws
+
+
+_XENT_WS = {}  # (device, stream, bytes) -> a prepared workspace the binding reuses
+
+
+def _xent_workspace_for(rows, cols, dtype, device, stream):
+    """The binding's own prepared workspace for calls on this device and
+    stream (calls on one stream are ordered, so they can share it)."""
+    sid = _stream(stream, device.index)
+    n = fr_workspace_size("xent", rows, cols, dtype)
+    key = (device.index, sid)
+    ws = _XENT_WS.get(key)
+    if ws is None or ws.numel() < n:
+        ws = fr_xent_workspace(rows, cols, dtype, device, stream)
+        _XENT_WS[key] = ws
+    return ws
+
+
 def xent_mean_parts(workspace):
     """The two fp64 values an fr_xent call with the mean leaves in its
     workspace -- the sum of the losses it averaged and the number of rows it
@@ -312,7 +343,10 @@ def fr_xent(logits, target, ignore_index: int = -100, want_loss: bool = True,
     """Cross entropy of bf16 or fp32 logits rows against int64 targets.
 
     Returns a dict with the requested outputs: ``loss`` [rows], ``mean`` [1],
-    ``target_logit`` [rows], ``argmax`` [rows] (int64).  With ``group`` (a
+    ``target_logit`` [rows], ``argmax`` [rows] (int64).  ``workspace``, when
+    given, must come from fr_xent_workspace (prepared once; each call keeps
+    it prepared); by default the binding keeps one per device and stream.
+    With ``group`` (a
     torch.distributed group whose ranks each pass their own rows of one
     batch), ``mean`` is the mean over the whole batch: the ranks' mean parts
     are all-reduced between this rank's kernel and the finishing kernel.
@@ -331,7 +365,9 @@ def fr_xent(logits, target, ignore_index: int = -100, want_loss: bool = True,
     am = torch.empty(rows, dtype=torch.int64, device=dev) if want_argmax else None
     ws, nws = (None, 0)
     if want_mean:
-        ws, nws = _workspace("xent", rows, cols, dt, form, dev, workspace)
+        ws = workspace if workspace is not None else _xent_workspace_for(rows, cols, dt, dev,
+                                                                         stream)
+        nws = ws.numel() * ws.element_size()
     _check(lib().fr_xent(_ptr(logits), _ptr(target), _ptr(loss), _ptr(mean), _ptr(tl), _ptr(am),
                          rows, cols, _ld(logits), ignore_index, DTYPES[dt], FORMS[form],
                          _ptr(ws), nws, _stream(stream)), "fr_xent")

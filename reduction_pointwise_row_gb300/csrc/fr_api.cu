@@ -430,6 +430,18 @@ fr_status fr_xent(const void *logits, const int64_t *target, float *loss, float 
                   FR_FORM_LOOPED);
 }
 
+fr_status fr_xent_workspace_init(void *workspace, size_t workspace_bytes, fr_stream_t stream) {
+  if (!workspace) return FR_ERR_INVALID_ARG;
+  if (workspace_bytes < 16) return FR_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned(workspace, 16)) return FR_ERR_MISALIGNED;
+  fr::DevInfo info;
+  if (fr_status st = device_ok(&info)) return st;
+  return fr::launch_xent_workspace_init(workspace, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? FR_OK
+             : FR_ERR_CUDA;
+}
+
 fr_status fr_xent_mean_from_parts(const void *workspace, float *loss_mean, fr_stream_t stream) {
   if (!workspace || !loss_mean) return FR_ERR_INVALID_ARG;
   if (!aligned(workspace, 16) || !aligned(loss_mean, 4)) return FR_ERR_MISALIGNED;

@@ -169,6 +169,7 @@ cudaError_t launch_xent_config(const XentConfig &cfg, const void *logits,
 
 size_t xent_workspace(int64_t rows, int sm_count);
 cudaError_t launch_xent_mean_from_parts(const void *workspace, float *loss_mean, cudaStream_t s);
+cudaError_t launch_xent_workspace_init(void *workspace, cudaStream_t s);
 // f32: logits are fp32 (else bf16 bit patterns)
 cudaError_t launch_xent(const void *logits, bool f32, const int64_t *target, float *loss,
                         float *loss_mean, float *target_logit, int64_t *argmax, int64_t rows,

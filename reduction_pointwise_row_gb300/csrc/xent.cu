@@ -65,24 +65,32 @@ __device__ __forceinline__ MD fold_chunk(MD st, float cm) {
   return st;
 }
 
-// Workspace layout: the ticket (bytes 0..3), the batch's mean parts at
+// Workspace layout: the ticket (bytes 0..7), the batch's mean parts at
 // FR_XENT_PARTS_OFFSET (fp64 sum of the averaged losses, fp64 count of the
 // rows averaged), then one fp64 partial sum and one count per CTA.
+//
+// The ticket holds a tag (high 32 bits) and the CTAs arrived so far (low 32
+// bits).  fr_xent_workspace_init writes the tag with no arrivals; the last
+// CTA of every launch writes it back, so a prepared workspace stays prepared
+// and no launch needs a reset of its own.  A CTA that finds another tag (a
+// workspace never prepared) records FR_DEVERR_BAD_WORKSPACE and the mean is
+// not written.
 constexpr size_t kPartsOffset = FR_XENT_PARTS_OFFSET;
 constexpr size_t kCtaOffset = kPartsOffset + 16;
-static_assert(kPartsOffset % 8 == 0 && kPartsOffset >= 4, "parts after the ticket, fp64 aligned");
+static_assert(kPartsOffset % 8 == 0 && kPartsOffset >= 8, "parts after the ticket, fp64 aligned");
+constexpr unsigned long long kTicketTag = 0x4652584EULL << 32;  // "FRXN", no arrivals
 
 struct Workspace {
-  unsigned int *ticket;  // zeroed on the stream before each launch
-  double *parts;         // [2]: sum of the averaged losses, rows averaged
-  double *sums;          // [grid]
-  long long *counts;     // [grid]
+  unsigned long long *ticket;  // tag | arrivals
+  double *parts;               // [2]: sum of the averaged losses, rows averaged
+  double *sums;                // [grid]
+  long long *counts;           // [grid]
 };
 
 __device__ __forceinline__ Workspace carve(void *ws, int grid) {
   char *p = static_cast<char *>(ws);
   Workspace w;
-  w.ticket = reinterpret_cast<unsigned int *>(p);
+  w.ticket = reinterpret_cast<unsigned long long *>(p);
   w.parts = reinterpret_cast<double *>(p + kPartsOffset);
   w.sums = reinterpret_cast<double *>(p + kCtaOffset);
   w.counts = reinterpret_cast<long long *>(p + kCtaOffset + 8 * static_cast<size_t>(grid));
@@ -92,7 +100,7 @@ __device__ __forceinline__ Workspace carve(void *ws, int grid) {
 // The mean over counted rows, in a fixed order: every CTA stores its fp64
 // partial and count; the last CTA to arrive (an atomic ticket, nobody waits)
 // adds them up -- thread i the partials i, i + T, ... in order, then a fixed
-// tree over the CTA -- writes the mean and re-zeroes the ticket.  Called by
+// tree over the CTA -- writes the mean and resets the ticket to its tag.  Called by
 // every thread of the CTA at the end of the kernel; cta_sum and cta_cnt are
 // thread 0's.  (A single thread adding the partials one after another took
 // 18 us for 304 CTAs on GB300, whose fp64 adds are slow.)
@@ -109,7 +117,13 @@ __device__ __forceinline__ void finish_mean(void *ws, float *loss_mean, double c
     w.sums[blockIdx.x] = cta_sum;
     w.counts[blockIdx.x] = cta_cnt;
     __threadfence();
-    last = atomicAdd(w.ticket, 1u) == gridDim.x - 1;
+    const unsigned long long old = atomicAdd(w.ticket, 1ull);
+    if ((old & ~0xFFFFFFFFull) != kTicketTag) {  // not a prepared workspace
+      atomicCAS(&g_fr_device_error, 0, FR_DEVERR_BAD_WORKSPACE);
+      last = 0;
+    } else {
+      last = (old & 0xFFFFFFFFull) == gridDim.x - 1;
+    }
   }
   __syncthreads();
   if (!last) return;
@@ -140,7 +154,7 @@ __device__ __forceinline__ void finish_mean(void *ws, float *loss_mean, double c
     w.parts[0] = S;
     w.parts[1] = static_cast<double>(n);
     *loss_mean = static_cast<float>(S / static_cast<double>(n));
-    *w.ticket = 0u;
+    *w.ticket = kTicketTag;
   }
 }
 
@@ -713,10 +727,6 @@ cudaError_t launch_xent_config(const XentConfig &cfg, const void *logits,
     return e;
   int64_t grid = static_cast<int64_t>(sm_count) * cfg.ctas_per_sm;
   if (grid > rows) grid = rows;
-  if (loss_mean != nullptr) {
-    e = cudaMemsetAsync(workspace, 0, 16, s);
-    if (e != cudaSuccess) return e;
-  }
   int64_t *no_argmax = nullptr;
   void *args[] = {&logits, &target, &loss, &target_logit, &no_argmax, &loss_mean, &workspace,
                   &rows, &cols, &ld, &ignore_index};
@@ -777,10 +787,6 @@ cudaError_t launch_warp_kernel(const void *kern, int per_sm_cap, const void *log
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(smem))) != cudaSuccess)
     return e;
-  if (loss_mean != nullptr) {
-    e = cudaMemsetAsync(workspace, 0, 16, s);
-    if (e != cudaSuccess) return e;
-  }
   void *args[] = {&logits, &target, &loss, &target_logit, &argmax, &loss_mean, &workspace,
                   &rows, &cols, &ld, &ignore_index};
   return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kWarpCta), args, smem, s);
@@ -822,6 +828,16 @@ cudaError_t launch_xent(const void *logits, bool f32, const int64_t *target, flo
   xent_recorded_config(dev, rows, cols, ld, &cfg);
   return launch_xent_config(cfg, logits, target, loss, loss_mean, target_logit, rows, cols, ld,
                             ignore_index, workspace, sm_count, max_smem_optin, s);
+}
+
+__global__ void xent_workspace_init_kernel(unsigned long long *ticket) {
+  pdl_enter();
+  *ticket = kTicketTag;
+}
+
+cudaError_t launch_xent_workspace_init(void *workspace, cudaStream_t s) {
+  return launch_k(xent_workspace_init_kernel, dim3(1), dim3(1), 0, s, 0,
+                  static_cast<unsigned long long *>(workspace));
 }
 
 // The mean from parts that ranks holding shards of one batch have summed

@@ -65,12 +65,14 @@ int main(int argc, char **argv) {
     return fail("cudaMalloc", (int)e);
   cudaStream_t s;
   if ((e = cudaStreamCreate(&s))) return fail("cudaStreamCreate", (int)e);
+  fr_status st = fr_xent_workspace_init(dws, ws, (fr_stream_t)s);  /* once per workspace */
+  if (st != FR_OK) return fail(fr_status_string(st), (int)st);
   if ((e = cudaMemcpyAsync(dx, x, n * 4, cudaMemcpyHostToDevice, s)) ||
       (e = cudaMemcpyAsync(dlg, lg, n * 2, cudaMemcpyHostToDevice, s)) ||
       (e = cudaMemcpyAsync(dtg, tg, (size_t)rows * 8, cudaMemcpyHostToDevice, s)))
     return fail("copy in", (int)e);
 
-  fr_status st = fr_softmax(dx, dy, rows, cols, cols, cols, FR_F32, FR_FORM_AUTO, (fr_stream_t)s);
+  st = fr_softmax(dx, dy, rows, cols, cols, cols, FR_F32, FR_FORM_AUTO, (fr_stream_t)s);
   if (st != FR_OK) return fail(fr_status_string(st), (int)st);
   st = fr_xent(dlg, (const int64_t *)dtg, (float *)dloss, (float *)dmean, NULL, NULL, rows, cols,
                cols, -100, FR_BF16, FR_FORM_AUTO, dws, ws, (fr_stream_t)s);

@@ -51,8 +51,7 @@ def test_graph_replays_every_op_on_new_data():
     lr = torch.empty(64, device=dev)
     lg = torch.empty(33, 50257, dtype=torch.bfloat16, device=dev)
     tg = torch.empty(33, dtype=torch.int64, device=dev)
-    xws = torch.empty(fr.fr_workspace_size("xent", 33, 50257, "bf16"), dtype=torch.uint8,
-                      device=dev)
+    xws = fr.fr_xent_workspace(33, 50257, "bf16")
     out = {}
 
     def step():

@@ -163,3 +163,13 @@ def test_every_overlapped_kernel_waits_for_its_predecessor():
             else:
                 assert waits, f"{name} ({os.path.basename(f)}) does not begin with pdl_enter()"
     assert plain_only <= seen
+
+
+def test_xent_workspace_init_validates_before_any_device_call():
+    import ctypes
+    import reduction_pointwise_row_gb300 as fr
+    lib = fr.lib()
+    P = ctypes.c_void_p
+    assert lib.fr_xent_workspace_init(None, 64, None) == 1          # NULL
+    assert lib.fr_xent_workspace_init(P(0x10000), 8, None) == 5     # smaller than the ticket
+    assert lib.fr_xent_workspace_init(P(0x10008), 64, None) == 4    # not 16-byte aligned

@@ -26,8 +26,7 @@ def shard_call(logits_bits, target, argmax):
     lg = bf16_tensor(logits_bits)
     t = torch.from_numpy(target).cuda()
     rows, cols = logits_bits.shape
-    ws = torch.zeros(fr.fr_workspace_size("xent", rows, cols, "bf16"), dtype=torch.uint8,
-                     device="cuda")
+    ws = fr.fr_xent_workspace(rows, cols, "bf16")
     r = fr.fr_xent(lg, t, want_argmax=argmax, workspace=ws)
     return r, ws
 
@@ -68,3 +67,31 @@ def test_mean_from_parts_no_counted_row_is_nan():
     assert torch.isnan(fr.fr_xent_mean_from_parts(ws)).all()
     with pytest.raises(fr.FRError, match="MISALIGNED"):
         fr.fr_xent_mean_from_parts(ws[4:])
+
+
+def test_unprepared_workspace_is_reported_and_preparing_fixes_it(o):
+    """A workspace fr_xent_workspace_init never prepared (here all ones) makes
+    the call record FR_DEVERR_BAD_WORKSPACE and leave the mean unwritten (the
+    per-row losses are still right); once prepared, every later call works
+    without another preparation."""
+    w = workloads.make(4, rows=50, cols=3001, seed=4343)
+    lg, t = bf16_tensor(w.arrays["logits"]), torch.from_numpy(w.arrays["target"]).cuda()
+    ref = o.xent(w.arrays["logits"], w.arrays["target"], -100)
+    n = fr.fr_workspace_size("xent", 50, 3001, "bf16")
+    ws = torch.full((n,), 255, dtype=torch.uint8, device="cuda")
+    mean = torch.full((1,), 7.0, device="cuda")
+    lib = fr.lib()
+    loss = torch.empty(50, device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    assert lib.fr_xent(lg.data_ptr(), t.data_ptr(), loss.data_ptr(), mean.data_ptr(), None, None,
+                       50, 3001, 3001, -100, fr.DTYPES["bf16"], 0, ws.data_ptr(), n, st) == 0
+    torch.cuda.synchronize()
+    assert fr.fr_check_device_error() == 3  # FR_DEVERR_BAD_WORKSPACE
+    assert mean.item() == 7.0
+    assert_close(loss.cpu().numpy(), ref["loss"], "loss", "losses with a bad workspace")
+    assert lib.fr_xent_workspace_init(ws.data_ptr(), n, st) == 0
+    for _ in range(3):
+        r = fr.fr_xent(lg, t, workspace=ws)
+        torch.cuda.synchronize()
+        assert fr.fr_check_device_error() == 0
+        assert_close(r["mean"].cpu().numpy()[0], ref["mean"], "loss", "mean once prepared")
