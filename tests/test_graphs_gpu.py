@@ -1,9 +1,9 @@
 """CUDA Graph capture of the library's calls ("Stax (4): GPU Codegen and Dynamic
 Shapes", section 9.9: a fixed sequence of launches recorded once and replayed
 with one submission, valid while the shapes and the buffer addresses stay the
-same).  The calls enqueue kernels (and, for the cross-entropy mean, a memset)
-on the caller's stream without allocating or synchronising, so they can be
-captured; replays on new data written into the captured buffers must match
+same).  The calls enqueue kernels on the caller's stream without allocating
+or synchronising (the cross-entropy workspace is prepared once, before the
+capture), so they can be captured; replays on new data written into the captured buffers must match
 the oracle."""
 import numpy as np
 import pytest
