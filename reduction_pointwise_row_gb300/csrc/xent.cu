@@ -207,7 +207,10 @@ __device__ __forceinline__ float logit_stream(const unsigned char *row, int64_t 
 // aligned interior).  Items go through a per-thread ring of NS shared-memory
 // stages filled with cp.async (no registers held, one commit group per item),
 // continuing across row boundaries, so NS - 1 items per thread are always in
-// flight -- also while the CTA combines a finished row.
+// flight -- also while the CTA combines a finished row.  The template covers
+// argmax and fp32 logits; the library instantiates it over its configuration
+// box for bf16 logits without argmax (the warp-per-row kernel serves the
+// other cases).
 template <bool ARGMAX, int T, int U, int NS, bool F32 = false>
 __global__ void __launch_bounds__(T, 1)
 xent_async(const void *__restrict__ logits, const int64_t *__restrict__ target,
