@@ -173,3 +173,18 @@ def test_xent_workspace_init_validates_before_any_device_call():
     assert lib.fr_xent_workspace_init(None, 64, None) == 1          # NULL
     assert lib.fr_xent_workspace_init(P(0x10000), 8, None) == 5     # smaller than the ticket
     assert lib.fr_xent_workspace_init(P(0x10008), 64, None) == 4    # not 16-byte aligned
+
+
+def test_traffic_model_counts_each_dtype_by_its_width():
+    """Each op's algorithmic bytes: inputs read once and outputs written once,
+    at the width of their dtype (bf16 rows move half the bytes of fp32 rows;
+    the per-row vectors are the same)."""
+    from reduction_pointwise_row_gb300 import traffic as t
+    R, C = 300, 1000
+    assert t.algorithmic_bytes("relu_add_sum", R, C) == 2 * R * C * 4 + 4 * R
+    assert t.algorithmic_bytes("relu_add_sum_bf16", R, C) == 2 * R * C * 2 + 4 * R
+    assert t.algorithmic_bytes("softmax", R, C) == 2 * t.algorithmic_bytes("softmax_bf16", R, C)
+    assert (t.algorithmic_bytes("xent_f32", R, C) - t.algorithmic_bytes("xent", R, C)
+            == R * C * 2)
+    assert t.algorithmic_bytes("sumsq", R, C) == R * C * 4 + 4 * R
+    assert t.algorithmic_bytes("layernorm", R, C) == 4 * R * C + 8 * C + 8 * R
