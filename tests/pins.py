@@ -33,7 +33,10 @@ def _close(a, b, rtol, atol=0.0):
     a, b = np.asarray(a, dtype=np.float64), np.asarray(b, dtype=np.float64)
     assert a.shape == b.shape, (a.shape, b.shape)
     ok = np.isclose(a, b, rtol=rtol, atol=atol, equal_nan=True)
-    assert ok.all(), f"max |diff| {np.nanmax(np.abs(a - b))} at {np.argwhere(~ok)[:5].tolist()}"
+    if not ok.all():
+        bad = np.argwhere(~ok)[:5].tolist()
+        raise AssertionError(f"{int((~ok).sum())} mismatches, first at {bad}: "
+                             f"{a[~ok][:5].tolist()} vs {b[~ok][:5].tolist()}")
 
 
 def _bf16_bits(vals):
