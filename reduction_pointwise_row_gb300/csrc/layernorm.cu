@@ -86,6 +86,9 @@ __device__ __forceinline__ Welford welford16(const V8 &v) {
   return Welford{16.0f, mean, q};
 }
 
+// Bound of every mbarrier wait, in SM clocks (about one second).
+constexpr long long kWaitBudget = 1LL << 31;
+
 // Persistent form.  Requires 32-byte aligned x/y rows, gamma, beta and
 // cols % 16 == 0 (checked by the host); NV vectors of 16 per thread.
 constexpr int kPersistMaxThreads = 512;
@@ -287,7 +290,7 @@ layernorm_ring(const uint16_t *__restrict__ x, const float *__restrict__ gamma,
         const int64_t kk = k0 + r;
         if (kk < nk && !timed_out &&
             !mbar_wait_bounded(&full[kk % kRingBufs], static_cast<uint32_t>((kk / kRingBufs) & 1),
-                               1LL << 31)) {
+                               kWaitBudget)) {
           timed_out = 1;
           atomicCAS(err, 0, FR_DEVERR_TIMEOUT);
         }
@@ -360,11 +363,9 @@ layernorm_ring(const uint16_t *__restrict__ x, const float *__restrict__ gamma,
   if constexpr (BULK) {
     __syncthreads();
     if (tid == 0 && timed_out)  // last bounded wait on copies that may be in flight
-      for (int b = 0; b < kRingBufs; ++b) mbar_wait_bounded(&full[b], 0, 1LL << 31);
+      for (int b = 0; b < kRingBufs; ++b) mbar_wait_bounded(&full[b], 0, kWaitBudget);
   }
 }
-
-constexpr long long kWaitBudget = 1LL << 31;  // SM clocks (about one second) per wait
 
 // ---- cluster form: gamma/beta resident in registers -----------------------------
 // A cluster of C CTAs (C = 1 or 2) splits every row into C column slices of
@@ -470,7 +471,7 @@ layernorm_cluster(const uint16_t *__restrict__ x, const float *__restrict__ gamm
       const int64_t kp = k - 1;
       const int sl = static_cast<int>(kp % kClSlots);
       if (!timed_out &&
-          !mbar_wait_bounded(&pbar[sl], static_cast<uint32_t>((kp / kClSlots) & 1), 1LL << 31)) {
+          !mbar_wait_bounded(&pbar[sl], static_cast<uint32_t>((kp / kClSlots) & 1), kWaitBudget)) {
         timed_out = 1;
         atomicCAS(err, 0, FR_DEVERR_TIMEOUT);
       }
@@ -632,7 +633,7 @@ layernorm_cluster_full(const uint16_t *__restrict__ x, const float *__restrict__
   auto wait_row = [&](int64_t k) {
     if (!timed_out &&
         !mbar_wait_bounded(&landed[k % kSlotsR], static_cast<uint32_t>((k / kSlotsR) & 1),
-                           1LL << 31)) {
+                           kWaitBudget)) {
       timed_out = 1;
       atomicCAS(err, 0, FR_DEVERR_TIMEOUT);
     }
@@ -716,7 +717,7 @@ layernorm_cluster_full(const uint16_t *__restrict__ x, const float *__restrict__
       const int64_t sp = s - 1;
       const int sl = static_cast<int>(sp % kClSlots);
       if (!timed_out &&
-          !mbar_wait_bounded(&pbar[sl], static_cast<uint32_t>((sp / kClSlots) & 1), 1LL << 31)) {
+          !mbar_wait_bounded(&pbar[sl], static_cast<uint32_t>((sp / kClSlots) & 1), kWaitBudget)) {
         timed_out = 1;
         atomicCAS(err, 0, FR_DEVERR_TIMEOUT);
       }
@@ -773,7 +774,7 @@ layernorm_cluster_full(const uint16_t *__restrict__ x, const float *__restrict__
   }
   if (timed_out && tid == 0)  // last bounded wait on copies that may be in flight
     for (int64_t k = nr > kSlotsR ? nr - kSlotsR : 0; k < nr; ++k)
-      mbar_wait_bounded(&landed[k % kSlotsR], static_cast<uint32_t>((k / kSlotsR) & 1), 1LL << 31);
+      mbar_wait_bounded(&landed[k % kSlotsR], static_cast<uint32_t>((k / kSlotsR) & 1), kWaitBudget);
   // No CTA may leave while a peer can still write into its shared memory.
   cluster_arrive();
   cluster_wait();
