@@ -13,7 +13,7 @@ import oracle
 import reduction_pointwise_row_gb300 as fr
 import synth
 from compare import assert_bits_equal, assert_close
-from gpu_util import bf16_to_f32_host, bf16_tensor, empty_like_placed, place
+from gpu_util import bf16_to_f32_host, empty_like_placed, place
 from synth import workloads
 
 pytestmark = pytest.mark.gpu
