@@ -133,6 +133,17 @@ def _stream(stream=None, device_index=None):
     return _current_raw_stream(_current_device() if device_index is None else device_index)
 
 
+def _on_current_device(*ts):
+    """The library launches on the current CUDA device: refuse tensors that
+    live on another one (their addresses mean nothing there)."""
+    _stream()  # resolves the device lookup
+    cur = _current_device()
+    for t in ts:
+        if t is not None and t.get_device() != cur:
+            raise ValueError(f"tensor on cuda:{t.get_device()}, current device is cuda:{cur}: "
+                             "call inside torch.cuda.device(...)")
+
+
 def _ptr(t):
     """A tensor's device address as an int (ctypes passes it as void *), or None."""
     return t.data_ptr() if t is not None else None
@@ -183,6 +194,7 @@ def fr_reduce_relu_add_sum(a, b, scale: float = 2.0, form: str = "auto", out=Non
     rows, cols = a.shape
     if out is None:
         out = torch.empty(rows, dtype=torch.float32, device=a.device)
+    _on_current_device(a, b, out)
     ws, nws = _workspace("relu_add_sum", rows, cols, dt, form, a.device, workspace)
     _check(lib().fr_reduce_relu_add_sum(_ptr(a), _ptr(b), _ptr(out), rows, cols, _ld(a), _ld(b),
                                         DTYPES[dt], scale, FORMS[form], _ptr(ws), nws,
@@ -199,6 +211,7 @@ def fr_reduce_sumsq(x, epilogue: str = "sum", form: str = "auto", out=None, work
     rows, cols = x.shape
     if out is None:
         out = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _on_current_device(x, out)
     ws, nws = _workspace("sumsq", rows, cols, "f32", form, x.device, workspace)
     _check(lib().fr_reduce_sumsq(_ptr(x), _ptr(out), rows, cols, _ld(x), DTYPES["f32"],
                                  EPILOGUES[epilogue], FORMS[form], _ptr(ws), nws,
@@ -216,6 +229,7 @@ def fr_softmax(x, form: str = "auto", out=None, stream=None):
         out = torch.empty_like(x)
     assert out.dtype == x.dtype and out.shape == x.shape
     dt = DTYPES["f32"] if x.dtype == torch.float32 else DTYPES["bf16"]
+    _on_current_device(x, out)
     _check(lib().fr_softmax(_ptr(x), _ptr(out), rows, cols, _ld(x), _ld(out), dt,
                             FORMS[form], _stream(stream)), "fr_softmax")
     return out
@@ -264,6 +278,7 @@ def fr_layernorm(x, gamma, beta, eps: float = 1e-5, form: str = "auto", out=None
         mean = torch.empty(rows, dtype=torch.float32, device=x.device)
     if rstd is None:
         rstd = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _on_current_device(x, gamma, beta, out, mean, rstd)
     _check(lib().fr_layernorm(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(out), _ptr(mean), _ptr(rstd),
                               rows, cols, _ld(x), _ld(out), eps, DTYPES["bf16"], FORMS[form],
                               _stream(stream)), "fr_layernorm")
@@ -363,6 +378,7 @@ def fr_xent(logits, target, ignore_index: int = -100, want_loss: bool = True,
     mean = torch.empty(1, dtype=torch.float32, device=dev) if want_mean else None
     tl = torch.empty(rows, dtype=torch.float32, device=dev) if want_target_logit else None
     am = torch.empty(rows, dtype=torch.int64, device=dev) if want_argmax else None
+    _on_current_device(logits, target)
     ws, nws = (None, 0)
     if want_mean:
         ws = workspace if workspace is not None else _xent_workspace_for(rows, cols, dt, dev,
@@ -392,6 +408,7 @@ def fr_reduce_relu_add_sum_split_static(a, b, scale: float = 2.0, out=None, stre
     rows, cols = a.shape
     if out is None:
         out = torch.empty(rows, dtype=torch.float32, device=a.device)
+    _on_current_device(a, b, out)
     _check(lib().fr_reduce_relu_add_sum_split_static(_ptr(a), _ptr(b), _ptr(out), rows, cols,
                                                      _ld(a), _ld(b), DTYPES["f32"], scale,
                                                      _stream(stream)),

@@ -96,5 +96,36 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB
 
 
+def build_variant(name: str, defines: list[str], recompile=("layernorm.cu",)) -> str:
+    """A test-only variant of the library: the sources named in `recompile`
+    compiled again with `defines` (e.g. ``["-DFR_TEST_WAIT_BUDGET=1"]``) and
+    linked with the main build's other objects into ``_lib/<name>/libfr.so``.
+    Nothing in the product loads it."""
+    build()
+    nvcc = _nvcc()
+    out_dir = os.path.join(OUT_DIR, name)
+    os.makedirs(out_dir, exist_ok=True)
+    common = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, *ARCH]
+    objs = []
+    for src in _sources():
+        base = os.path.basename(src)
+        if base in recompile:
+            obj = os.path.join(out_dir, base + ".o")
+            r = subprocess.run([nvcc, *common, *defines, "-c", src, "-o", obj],
+                               capture_output=True, text=True)
+            if r.returncode != 0:
+                raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}{r.stderr}")
+        else:
+            obj = os.path.join(OUT_DIR, "obj", base + ".o")
+        objs.append(obj)
+    lib = os.path.join(out_dir, "libfr.so")
+    libdir = _cuda_lib_dir(nvcc)
+    r = subprocess.run([nvcc, "-shared", *ARCH, "-cudart", "shared", "-o", lib, *objs, "-L",
+                        libdir, f"-Xlinker=-rpath={libdir}"], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}{r.stderr}")
+    return lib
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

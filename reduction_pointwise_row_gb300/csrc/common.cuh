@@ -255,6 +255,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of phase `parity` (returns at once).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for phase `parity` of the barrier for at most `budget` SM clocks.
 // Returns false on timeout (the caller records an error and stops waiting).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,

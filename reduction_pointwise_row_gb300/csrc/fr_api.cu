@@ -53,8 +53,14 @@ cudaError_t current_device_info(DevInfo *out) {
 }  // namespace fr
 
 namespace {
-
 thread_local fr_form g_last_form = FR_FORM_AUTO;
+}  // namespace
+
+namespace fr {
+void set_last_form(int form) { g_last_form = static_cast<fr_form>(form); }
+}  // namespace fr
+
+namespace {
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -284,8 +290,10 @@ fr_status fr_softmax(const void *x, void *y, int64_t rows, int64_t cols, int64_t
     case FR_FORM_PERSISTENT: {
       if (cols > fr::softmax_persistent_max_cols(vec)) return FR_ERR_UNSUPPORTED_FORM;
       // FR_SOFTMAX_KERNEL=async|plain pins the persistent kernel.  Default:
-      // plain (measured on GB300, fp32 [32768, 1024]: 45.2 us; the per-warp
-      // cp.async ring runs half the warps per SM and takes 49.0 us).
+      // plain (measured on GB300, fp32 [32768, 1024] back to back: 40.2-41.2
+      // us as programmatic dependents, 43.0 us without; the per-warp cp.async
+      // ring runs half the warps per SM and took 49.0 us against 45.2 for
+      // plain when both were ordinary launches).
       const char *pin = getenv("FR_SOFTMAX_KERNEL");
       const bool use_async = pin != nullptr && strcmp(pin, "async") == 0;
       const bool aligned16 = aligned(x, 16) && aligned(y, 16) && ldx % 4 == 0 && ldy % 4 == 0;

@@ -17,6 +17,9 @@ struct DevInfo {
   int max_smem_optin;  // bytes of shared memory one CTA may opt in to
 };
 cudaError_t current_device_info(DevInfo *out);
+// Records the form of a call that enqueued its kernels (what fr_last_form
+// returns on this host thread).
+void set_last_form(int form);
 
 // ---- Example 1.1: out[x] = sum_r scale * relu(a + b) ------------------------
 

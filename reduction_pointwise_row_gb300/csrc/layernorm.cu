@@ -11,11 +11,24 @@
 // (1979):  n = na + nb,  delta = mb - ma,  mean = ma + delta * nb / n,
 // M2 = M2a + M2b + delta^2 * na * nb / n.  All in fp32.
 //
-// persistent  one CTA per row, the row held in registers as packed bf16
-//             (x read once from HBM, y written once).
-// looped      one CTA per row, grid-stride over rows: pass 1 streams the row
-//             in chunks merging Welford triples, pass 2 streams it again
-//             (from L2) to write y.  Any alignment (scalar lane-strided).
+// Kernels, in the order the looped form prefers them:
+// layernorm_cluster_full  rows of C*T*32 columns (C in 1, 2, 4, 8 CTAs of T in
+//             64 .. 512 threads): a persistent grid of thread-block clusters,
+//             each CTA owning a fixed column slice of every row (its gamma and
+//             beta held in registers), each row slice staged in shared memory
+//             by one bulk copy, the C slices' (mean, M2) pairs exchanged
+//             through distributed shared memory and merged with equal counts;
+//             the default for 2048 .. 131072 columns.
+// layernorm_cluster  the same with 512 threads and C = 1 or 2 for other
+//             lengths that are multiples of 32 * C (per-thread cp.async ring).
+// layernorm_ring  one persistent CTA per SM, rows staged whole in a ring of
+//             shared-memory buffers (per-thread cp.async or one bulk copy per
+//             row), R rows normalised per gamma/beta pass.
+// layernorm_looped_scalar  any alignment and length: lane-strided scalars,
+//             pass 1 merges Welford triples over chunks, pass 2 re-reads the
+//             row (from L2) to write y.
+// layernorm_persistent  the persistent form: one CTA per row, the row held in
+//             registers as packed bf16 (x read once, y written once).
 #include <cstdlib>
 #include <cstring>
 
@@ -86,8 +99,27 @@ __device__ __forceinline__ Welford welford16(const V8 &v) {
   return Welford{16.0f, mean, q};
 }
 
-// Bound of every mbarrier wait, in SM clocks (about one second).
+// Bound of every mbarrier wait, in SM clocks (about one second).  A wait that
+// runs out records FR_DEVERR_TIMEOUT; its kernel then issues no further copy,
+// skips its remaining waits on data (its outputs are garbage) and, before it
+// exits, waits -- again bounded -- for the copies it issued before the timeout.
 constexpr long long kWaitBudget = 1LL << 31;
+// The first wait of layernorm_ring's bulk staging.  A test build
+// (-DFR_TEST_WAIT_BUDGET=<clocks>) shortens its budget so that it runs out
+// while its copy is still in flight, to exercise the path above; every other
+// wait, the final drain included, keeps the full budget.
+// The shortened wait polls without blocking (mbarrier.try_wait may suspend
+// the thread for a while before it gives up; test_wait answers at once).
+__device__ __forceinline__ bool first_wait(uint64_t *bar, uint32_t parity) {
+#ifdef FR_TEST_WAIT_BUDGET
+  const long long t0 = clock64();
+  while (!mbar_test_wait(bar, parity))
+    if (clock64() - t0 > FR_TEST_WAIT_BUDGET) return false;
+  return true;
+#else
+  return mbar_wait_bounded(bar, parity, kWaitBudget);
+#endif
+}
 
 // Persistent form.  Requires 32-byte aligned x/y rows, gamma, beta and
 // cols % 16 == 0 (checked by the host); NV vectors of 16 per thread.
@@ -243,6 +275,7 @@ layernorm_ring(const uint16_t *__restrict__ x, const float *__restrict__ gamma,
   // rows of this CTA: blockIdx.x + k * G for k < nk
   const int64_t nk = blockIdx.x < rows ? (rows - blockIdx.x + G - 1) / G : 0;
   const uint64_t policy = l2_evict_first_policy();
+  int64_t last_issued = -1;  // thread 0: the last row whose bulk copy it issued
 
   auto stage_bulk = [&](int64_t k) {  // thread 0: row k into buffer k % kRingBufs
     if (k < nk) {
@@ -250,6 +283,7 @@ layernorm_ring(const uint16_t *__restrict__ x, const float *__restrict__ gamma,
       mbar_arrive_expect_tx(&full[b], static_cast<uint32_t>(buf_bytes));
       bulk_copy_g2s(smem + static_cast<size_t>(b) * buf_bytes, x + (blockIdx.x + k * G) * ldx,
                     static_cast<uint32_t>(buf_bytes), &full[b], policy);
+      last_issued = k;
     }
   };
   auto stage = [&](int64_t k) {  // this thread's pieces of row k into buffer k % kRingBufs
@@ -288,9 +322,10 @@ layernorm_ring(const uint16_t *__restrict__ x, const float *__restrict__ gamma,
     for (int r = 0; r < R; ++r) {
       if constexpr (BULK) {
         const int64_t kk = k0 + r;
+        const uint32_t par = static_cast<uint32_t>((kk / kRingBufs) & 1);
         if (kk < nk && !timed_out &&
-            !mbar_wait_bounded(&full[kk % kRingBufs], static_cast<uint32_t>((kk / kRingBufs) & 1),
-                               kWaitBudget)) {
+            !(kk == 0 ? first_wait(&full[0], par)
+                      : mbar_wait_bounded(&full[kk % kRingBufs], par, kWaitBudget))) {
           timed_out = 1;
           atomicCAS(err, 0, FR_DEVERR_TIMEOUT);
         }
@@ -361,14 +396,23 @@ layernorm_ring(const uint16_t *__restrict__ x, const float *__restrict__ gamma,
   }
   cp_async_wait<0>();  // no copy may still target this CTA's shared memory
   if constexpr (BULK) {
+    // After a timeout thread 0 issued no further copy.  A buffer is refilled
+    // only once every thread's wait on its previous row succeeded, so at most
+    // its latest copy can be in flight, and the latest copies of the
+    // kRingBufs buffers are those of the last kRingBufs rows issued: wait for
+    // each (a completed phase returns at once).
     __syncthreads();
-    if (tid == 0 && timed_out)  // last bounded wait on copies that may be in flight
-      for (int b = 0; b < kRingBufs; ++b) mbar_wait_bounded(&full[b], 0, kWaitBudget);
+    if (tid == 0 && timed_out)
+      for (int64_t k = last_issued - kRingBufs + 1 < 0 ? 0 : last_issued - kRingBufs + 1;
+           k <= last_issued; ++k)
+        mbar_wait_bounded(&full[k % kRingBufs], static_cast<uint32_t>((k / kRingBufs) & 1),
+                          kWaitBudget);
   }
 }
 
 // ---- cluster form: gamma/beta resident in registers -----------------------------
-// A cluster of C CTAs (C = 1 or 2) splits every row into C column slices of
+// (The general cluster kernel; the equal-count kernel below takes clusters of
+// up to 8 CTAs.)  A cluster of C CTAs (C = 1 or 2) splits every row into C column slices of
 // S = cols / C <= 16384; thread t of CTA rank q owns the 32 columns
 // q*S + 32t .. + 31 for the whole kernel, so its 32 gamma and 32 beta values
 // live in registers and per row only x comes in and y goes out -- no per-row
@@ -622,12 +666,14 @@ layernorm_cluster_full(const uint16_t *__restrict__ x, const float *__restrict__
     c1.w[4] = d.x; c1.w[5] = d.y; c1.w[6] = d.z; c1.w[7] = d.w;
   };
   const uint64_t policy = l2_evict_first_policy();
+  int64_t last_issued = -1;  // thread 0: the last row whose slice it requested
   auto issue = [&](int64_t k) {  // thread 0: this CTA's slice of row k, one bulk copy
-    if (k < nr) {
+    if (k < nr && !timed_out) {
       uint64_t *b = &landed[k % kSlotsR];
       mbar_arrive_expect_tx(b, slice);
       bulk_copy_g2s(slot_of(k), x + row_of(k) * ldx + static_cast<int64_t>(q) * S, slice, b,
                     policy);
+      last_issued = k;
     }
   };
   auto wait_row = [&](int64_t k) {
@@ -727,7 +773,7 @@ layernorm_cluster_full(const uint16_t *__restrict__ x, const float *__restrict__
 #pragma unroll
       for (int rk = 0; rk < kFullMaxCluster; ++rk)
         u[rk] = rk < static_cast<int>(C) ? slot[sl][rk] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      if (tid == 0 && sp + kClSlots < ns) mbar_arrive_expect_tx(&pbar[sl], part_bytes);
+      if (tid == 0 && sp + kClSlots < ns && !timed_out) mbar_arrive_expect_tx(&pbar[sl], part_bytes);
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         const int64_t k = sp * R + r;
@@ -772,8 +818,13 @@ layernorm_cluster_full(const uint16_t *__restrict__ x, const float *__restrict__
       }
     }
   }
-  if (timed_out && tid == 0)  // last bounded wait on copies that may be in flight
-    for (int64_t k = nr > kSlotsR ? nr - kSlotsR : 0; k < nr; ++k)
+  // After a timeout no slot was refilled; a slot is refilled only after every
+  // thread's wait on its previous row succeeded, so at most its latest copy
+  // is in flight, and the last kSlotsR rows issued hold the latest copy of
+  // every slot: wait for those (a completed phase returns at once).
+  if (timed_out && tid == 0)
+    for (int64_t k = last_issued - kSlotsR + 1 < 0 ? 0 : last_issued - kSlotsR + 1;
+         k <= last_issued; ++k)
       mbar_wait_bounded(&landed[k % kSlotsR], static_cast<uint32_t>((k / kSlotsR) & 1), kWaitBudget);
   // No CTA may leave while a peer can still write into its shared memory.
   cluster_arrive();

@@ -81,5 +81,7 @@ extern "C" fr_status fr_reduce_relu_add_sum_split_static(const void *a, const vo
   const bool vec = (d % 32 == 0) && (((lda - ldb) * 4) % 32 == 0);
   cudaError_t e = fr::launch_ras_split(a, b, out, rows, cols, lda, ldb, scale, false, vec,
                                        scratch, segments, reinterpret_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? FR_OK : FR_ERR_CUDA;
+  if (e != cudaSuccess) return FR_ERR_CUDA;
+  fr::set_last_form(FR_FORM_SPLIT);
+  return FR_OK;
 }

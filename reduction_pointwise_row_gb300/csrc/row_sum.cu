@@ -334,11 +334,15 @@ cudaError_t launch_ras_split(const void *a, const void *b, float *out, int64_t r
 }
 
 // One-input rows need no common phase with a second input: every row takes
-// the vector path with its own head/body/tail split.
+// the vector path with its own head/body/tail split.  The L2 norm's persistent
+// form runs the looped instance: a row within the persistent limit is exactly
+// one pass of its loop, with the same loads in flight, while the separate
+// persistent instance kept three registers on the stack around the fp64
+// square root (12 bytes of spill per thread under -Xptxas -v).
 cudaError_t launch_sumsq_persistent(const float *x, float *out, int64_t rows, int64_t cols,
                                     int64_t ldx, bool sqrt_out, cudaStream_t s) {
-  return sqrt_out ? launch_warp<Square, F32In, false, true>(x, nullptr, out, rows, cols, ldx, 0,
-                                                            Square{}, true, s)
+  return sqrt_out ? launch_warp<Square, F32In, true, true>(x, nullptr, out, rows, cols, ldx, 0,
+                                                           Square{}, true, s)
                   : launch_warp<Square, F32In, false, false>(x, nullptr, out, rows, cols, ldx, 0,
                                                              Square{}, true, s);
 }
