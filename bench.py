@@ -54,10 +54,12 @@ def parse():
                                       "softmax_65537", "softmax_65537_looped",
                                       "looped", "looped_bf16", "softmax_bf16", "xent_f32",
                                       "softmax_bf16_4097", "softmax_bf16_4097_looped",
-                                      "softmax_bf16_65537", "xent_box"],
+                                      "softmax_bf16_65537", "xent_box", "form_sweep"],
                    help="time one workload alone (for profiler captures) and exit")
     p.add_argument("--form", default="auto", choices=["auto", "persistent", "looped", "split"],
                    help="with --only: force a reduction form")
+    p.add_argument("--sweep-ops", default="relu_add_sum,softmax,softmax_bf16,layernorm",
+                   help="with --only form_sweep: the ops to sweep")
     return p.parse_args()
 
 
@@ -199,24 +201,33 @@ def run_ours(args):
     def max_ranks(x: float) -> float:
         return max_over_ranks(x, world, dev)
 
-    def timed(calls, steps, warmup, launches_per_call):
+    def timed(calls, steps, warmup, launches_per_call, blocks=BLOCKS):
         """Device time (s) per step: `steps` calls back to back, cycling over the
         rotating input sets, between two CUDA events on the launching stream
-        (a barrier and a synchronize on both sides); the slowest rank's."""
+        (a barrier and a synchronize on both sides); the slowest rank's.  The
+        first block of `steps` calls gives the time; `blocks` - 1 more blocks
+        of the same calls give the spread.  Returns (time per step of the
+        first block, launches in all blocks, times per step of every block)."""
         for i in range(warmup):
             calls[i % len(calls)]()
-        barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        w0 = time.time()
-        e0.record(stream)
-        for i in range(steps):
-            calls[i % len(calls)]()
-        e1.record(stream)
-        barrier()
-        if clocks:
-            clocks.window(w0, time.time())
-        return max_ranks(e0.elapsed_time(e1) / 1e3 / steps), launches_per_call * steps, None
+        per_block = []
+        for _ in range(blocks):
+            barrier()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            w0 = time.time()
+            e0.record(stream)
+            for i in range(steps):
+                calls[i % len(calls)]()
+            e1.record(stream)
+            barrier()
+            if clocks:
+                clocks.window(w0, time.time())
+            per_block.append(max_ranks(e0.elapsed_time(e1) / 1e3 / steps))
+        return per_block[0], launches_per_call * steps * blocks, per_block
 
+    if args.only == "form_sweep":
+        form_sweep(fr, dev, timed, args, peak, rank)
+        return
     if args.only == "xent_box":
         if rank == 0:
             print(json.dumps(xent_box(fr, workloads, dev, timed, args, peak)), flush=True)
@@ -235,7 +246,7 @@ def run_ours(args):
     calls[0]()
     form = fr.fr_last_form()
     nbytes = traffic.algorithmic_bytes("softmax", rows, cols)
-    t_launch, launches, ms = timed(calls, args.steps, args.warmup, 1)
+    t_launch, launches, blocks_h = timed(calls, args.steps, args.warmup, 1)
     value = world * nbytes / t_launch / 1e9
     nsets = len(calls)
     del calls
@@ -247,7 +258,7 @@ def run_ours(args):
     srcs = [torch.empty(rows, cols, device=dev) for _ in range(nsets)]
     dsts = [torch.empty(rows, cols, device=dev) for _ in range(nsets)]
     copies = [lambda a=a, b=b: b.copy_(a) for a, b in zip(srcs, dsts)]
-    t_copy, _, _ = timed(copies, args.steps, args.warmup, 0)
+    t_copy, _, _ = timed(copies, args.steps, args.warmup, 0, blocks=1)
     del srcs, dsts, copies
 
     # ---- e2e: the library's host-buffer entry point (fr_softmax_host) on the
@@ -289,6 +300,13 @@ def run_ours(args):
         per_config = extra_configs(fr, traffic, workloads, timed, dev, peak, args, world)
         launches += sum(v.pop("_launches") for v in per_config.values())
 
+    head_key = "softmax_32768x1024" if world == 1 else f"softmax_{rows}x{cols}"
+    head_entry = {"op": "softmax", "rows": rows, "cols": cols, "form": form,
+                  "us": round(t_launch * 1e6, 3), "gbs": round(nbytes / t_launch / 1e9, 2),
+                  "frac": round(nbytes / t_launch / 1e9 / peak, 4),
+                  "rows_per_s": round(world * rows / t_launch, 1), **spread_us(blocks_h),
+                  "rotating_sets": nsets}
+    per_config = {head_key: head_entry, **per_config}
     clk = clocks.stop()
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -315,7 +333,12 @@ def run_ours(args):
     }
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline(w)
-        print(json.dumps(line), flush=True)
+        if not args.no_extra:
+            line["cpu_baseline"]["per_config"] = cpu_baselines(w)
+        # last, so that a reader keeping only the end of the line has every
+        # configuration: the five workloads in one compact block
+        line["configs"] = compact_configs(per_config, line["cpu_baseline"])
+        print(json.dumps(line, separators=(",", ":")), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -521,13 +544,13 @@ def extra_configs(fr, traffic, workloads, timed, dev, peak, args, world, names=N
     for name in (names or EXTRA):
         calls, op, rows, cols, lpc = setup_workload(name, fr, workloads, dev, form)
         calls[0]()
-        t, n, _ = timed(calls, steps, args.warmup, lpc)
+        t, n, per_block = timed(calls, steps, args.warmup, lpc)
         nb = traffic.algorithmic_bytes(op, rows, cols)
         res[EXTRA.get(name, name)] = {
             "op": op, "rows": rows, "cols": cols, "form": fr.fr_last_form(),
             "us": round(t * 1e6, 3), "gbs": round(nb / t / 1e9, 2),
             "frac": round(nb / t / 1e9 / peak, 4), "rows_per_s": round(world * rows / t, 1),
-            "_launches": n, "rotating_sets": len(calls)}
+            **spread_us(per_block), "_launches": n, "rotating_sets": len(calls)}
         if name in ("relu_add_sum", "sumsq"):
             res[EXTRA[name]].update(graph_replay(calls[0], steps, args.warmup))
             res[EXTRA[name]]["_launches"] += GRAPH_CALLS * steps * lpc
@@ -542,7 +565,7 @@ def extra_configs(fr, traffic, workloads, timed, dev, peak, args, world, names=N
             srcs = [torch.empty(rows * cols, dtype=torch.bfloat16, device=dev) for _ in range(2)]
             dsts = [torch.empty_like(srcs[0]) for _ in range(2)]
             cps = [lambda a=a, b=b: b.copy_(a) for a, b in zip(srcs, dsts)]
-            tc, _, _ = timed(cps, steps, args.warmup, 0)
+            tc, _, _ = timed(cps, steps, args.warmup, 0, blocks=1)
             res[EXTRA.get(name, name)]["same_bytes_device_copy_gbs"] = round(nb / tc / 1e9, 2)
             del srcs, dsts, cps
     return res
@@ -566,13 +589,139 @@ def xent_box(fr, workloads, dev, timed, args, peak):
             fr.fr_xent_set_config(rows, cols, cfg)
         except fr.FRError:
             continue
-        sec, _, _ = timed(calls, steps, args.warmup, 1)
+        sec, _, _ = timed(calls, steps, args.warmup, 1, blocks=1)
         out.append({"config": list(cfg), "us": round(sec * 1e6, 2),
                     "frac": round(nb / sec / 1e9 / peak, 4)})
     fr.fr_xent_set_config(rows, cols, None)
     out.sort(key=lambda r: r["us"])
     return {"only": "xent_box", "rows": rows, "cols": cols, "runnable": len(out),
             "default_config": list(fr.fr_xent_get_config(rows, cols)), "points": out}
+
+
+# Shapes of the form sweep (rows x cols per op; every form that can run is
+# timed).  Around the selection rules: warp-per-row rows (<= 1024 fp32), the
+# split form's few-long-rows corner, one CTA or one cluster per row.
+SWEEP_RAS_ROWS = (8, 32, 128, 512, 1024, 2048, 4096, 8192)
+SWEEP_RAS_COLS = (1024, 4096, 16384, 65536, 262144, 1048576, 4194304)
+SWEEP_SM_ROWS = (16, 64, 152, 304, 608, 1216, 2432, 4864, 16384)
+SWEEP_SM_COLS = (1025, 2048, 4097, 8192, 16384, 32768, 65537, 131072, 262144)
+SWEEP_LN_COLS = (768, 1024, 2048, 4096, 5120, 8192, 12288, 16384, 32768, 65536)
+SWEEP_BYTES_MAX = 1 << 30  # largest input footprint of one call
+
+
+def form_sweep(fr, dev, timed, args, peak, rank):
+    """Every reduction form (and LayerNorm kernel) that can run, timed on a
+    grid of shapes the way the bench times its workloads: back-to-back calls
+    over rotating views of buffers that together exceed the L2 (1 GiB),
+    inputs filled on the device (uniform(-1, 1); the times do not depend on
+    the values).  Prints one JSON line per shape: the time per call of each
+    form (median of three K-step blocks), the fastest, and AUTO's pick."""
+    import torch
+    from reduction_pointwise_row_gb300 import traffic
+    steps = max(5, min(args.steps, 20))
+    name = torch.cuda.get_device_name(dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+
+    ops = set(args.sweep_ops.split(","))
+
+    def rotating(rows, cols, dtype, bytes_per_set, fill=True):
+        """Views of one buffer, set k at element offset k*rows*cols (so two
+        such lists of one shape pair up in the same 32-byte phase)."""
+        n = max(2, -(-ROTATE_BYTES // max(bytes_per_set, 1)))
+        buf = torch.empty(n * rows, cols, dtype=dtype, device=dev)
+        if fill:
+            buf.uniform_(-1.0, 1.0)
+        return [buf[k * rows:(k + 1) * rows] for k in range(n)]
+
+    def measure(make_calls, forms, op, rows, cols):
+        res = {}
+        for f in forms:
+            calls = make_calls(f)
+            try:
+                calls[0]()
+            except fr.FRError:
+                continue
+            if f == "auto":
+                res["auto_form"] = fr.fr_last_form()
+                continue
+            _, _, per = timed(calls, steps, 3, 1, blocks=3)
+            res[f] = round(sorted(per)[1] * 1e6, 3)
+        times = {k: v for k, v in res.items() if k != "auto_form"}
+        best = min(times, key=times.get) if times else None
+        nb = traffic.algorithmic_bytes(op, rows, cols)
+        line = {"op": op, "rows": rows, "cols": cols, "device": name, "sms": sms, "us": times,
+                "fastest": best, "auto": res.get("auto_form"),
+                "best_frac": round(nb / (times[best] * 1e-6) / 1e9 / peak, 4) if best else None}
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+
+    forms3 = ["auto", "persistent", "looped", "split"]
+    # Example 1.1, fp32
+    for rows in SWEEP_RAS_ROWS:
+        for cols in SWEEP_RAS_COLS:
+            if "relu_add_sum" not in ops or rows * cols * 8 > SWEEP_BYTES_MAX:
+                continue
+            As = rotating(rows, cols, torch.float32, rows * cols * 8)
+            Bs = rotating(rows, cols, torch.float32, rows * cols * 8)
+            out = torch.empty(rows, device=dev)
+            ws = torch.empty(max(16, fr.fr_workspace_size("relu_add_sum", rows, cols, "f32",
+                                                          "split")), dtype=torch.uint8, device=dev)
+
+            def mk(f, As=As, Bs=Bs, out=out, ws=ws):
+                return [lambda a=a, b=b: fr.fr_reduce_relu_add_sum(a, b, 2.0, out=out, form=f,
+                                                                  workspace=ws)
+                        for a, b in zip(As, Bs)]
+            measure(mk, forms3, "relu_add_sum", rows, cols)
+            del As, Bs
+    # softmax, fp32 and bf16
+    for dtype, op in ((torch.float32, "softmax"), (torch.bfloat16, "softmax_bf16")):
+        es = 4 if dtype == torch.float32 else 2
+        for rows in SWEEP_SM_ROWS:
+            for cols in SWEEP_SM_COLS:
+                if (op not in ops or rows * cols * es * 2 > SWEEP_BYTES_MAX or
+                        rows * cols * es < (1 << 20)):
+                    continue
+                Xs = rotating(rows, cols, dtype, 2 * rows * cols * es)
+                Ys = rotating(rows, cols, dtype, 2 * rows * cols * es, fill=False)
+
+                def mk(f, Xs=Xs, Ys=Ys):
+                    return [lambda x=x, y=y: fr.fr_softmax(x, out=y, form=f) for x, y in zip(Xs, Ys)]
+                measure(mk, forms3, op, rows, cols)
+                del Xs, Ys
+    # LayerNorm: its kernels (the looped form's cluster, ring and scalar
+    # kernels, and the persistent form), 256 MiB of x per call
+    for cols in SWEEP_LN_COLS if "layernorm" in ops else ():
+        rows = (1 << 27) // cols
+        Xs = rotating(rows, cols, torch.bfloat16, 4 * rows * cols)
+        Ys = rotating(rows, cols, torch.bfloat16, 4 * rows * cols, fill=False)
+        g = torch.ones(cols, device=dev)
+        bt = torch.zeros(cols, device=dev)
+        mean = torch.empty(rows, device=dev)
+        rstd = torch.empty(rows, device=dev)
+        res, auto_kernel = {}, None
+        for kname, f in (("auto", "auto"), ("cluster", "looped"), ("ring", "looped"),
+                         ("scalar", "looped"), ("persistent", "persistent")):
+            os.environ["FR_LAYERNORM_KERNEL"] = "" if kname in ("auto", "persistent") else kname
+            calls = [lambda x=x, y=y, f=f: fr.fr_layernorm(x, g, bt, 1e-5, form=f, out=y, mean=mean,
+                                                          rstd=rstd) for x, y in zip(Xs, Ys)]
+            try:
+                calls[0]()
+            except fr.FRError:
+                continue
+            if kname == "auto":
+                auto_kernel = fr.fr_last_form()
+                continue
+            _, _, per = timed(calls, steps, 3, 1, blocks=3)
+            res[kname] = round(sorted(per)[1] * 1e6, 3)
+        os.environ.pop("FR_LAYERNORM_KERNEL", None)
+        best = min(res, key=res.get)
+        nb = traffic.algorithmic_bytes("layernorm", rows, cols)
+        if rank == 0:
+            print(json.dumps({"op": "layernorm", "rows": rows, "cols": cols, "device": name,
+                              "sms": sms, "us": res, "fastest": best, "auto": auto_kernel,
+                              "best_frac": round(nb / (res[best] * 1e-6) / 1e9 / peak, 4)}),
+                  flush=True)
+        del Xs, Ys
 
 
 def tune_xent(fr, workloads, dev, calls, timed, steps, args, nb, peak):
@@ -587,7 +736,7 @@ def tune_xent(fr, workloads, dev, calls, timed, steps, args, nb, peak):
     default = fr.fr_xent_get_config(w.rows, w.cols)
     r = fr.fr_xent_tune(lg, tg, -100, eps=0.02, reps=5)
     del lg
-    t, n, _ = timed(calls, steps, args.warmup, 1)
+    t, n, _ = timed(calls, steps, args.warmup, 1, blocks=1)
     fr.fr_xent_set_config(w.rows, w.cols, None)
     return {"default_config": list(default), "tuned_config": list(r["config"]),
             "tune_evaluations": r["evaluations"], "tuned_us": round(t * 1e6, 3),
@@ -596,6 +745,15 @@ def tune_xent(fr, workloads, dev, calls, timed, steps, args, nb, peak):
 
 
 CPU_BASELINE_SECONDS = 1.0  # wall time of repeated oracle passes per CPU measurement
+BLOCKS = 7  # K-step blocks per workload: the first gives the time, all give the spread
+
+
+def spread_us(per_block):
+    """p10 / median / p90 of the per-step times of the K-step blocks (us)."""
+    import numpy as np
+    q = np.percentile(np.asarray(per_block) * 1e6, [10, 50, 90])
+    return {"p10_us": round(float(q[0]), 3), "p50_us": round(float(q[1]), 3),
+            "p90_us": round(float(q[2]), 3), "blocks": len(per_block)}
 GRAPH_CALLS = 64  # calls recorded in one CUDA graph for the launch-bound case
 
 
@@ -665,6 +823,107 @@ def cpu_baseline(w):
             "sample": f"{rows} of {w.rows} rows x {w.cols} per pass (fp64 C oracle, rows split "
                       f"over {cores} threads, {nn} passes in {round(nn * dtn, 2)} s; single-threaded "
                       f"alongside, {n1} passes)"}
+
+
+# The five workloads' entries in per_config (configuration index -> key).
+CONFIG_KEYS = {0: "relu_add_sum_64x128", 1: "softmax_32768x1024", 2: "layernorm_4096x32768",
+               3: "relu_add_sum_split_8x33554432", 4: "xent_8192x50257"}
+CONFIG_NAMES = {0: "relu_add_sum f32 64x128 (Example 1.1)", 1: "softmax f32 32768x1024",
+                2: "layernorm bf16 4096x32768", 3: "relu_add_sum split f32 8x33554432",
+                4: "xent bf16 8192x50257"}
+
+
+def compact_configs(per_config, cpu):
+    """configs 0-4 in a few keys each: us per step (first K-step block), GB/s,
+    fraction of the measured peak, rows/s, the p10/p90 over the blocks, the
+    form, and the oracle's GB/s on the host cores."""
+    out = {}
+    cpu_pc = cpu.get("per_config", {})
+    for i, key in CONFIG_KEYS.items():
+        e = per_config.get(key)
+        if e is None:
+            continue
+        c = {"w": CONFIG_NAMES[i], "form": e["form"], "us": e["us"], "gbs": e["gbs"],
+             "frac": e["frac"], "rows_s": e["rows_per_s"], "p10_us": e["p10_us"],
+             "p90_us": e["p90_us"]}
+        if "graph_us_per_call" in e:
+            c["graph_us"] = e["graph_us_per_call"]
+        if str(i) in cpu_pc:
+            c["cpu_gbs"] = cpu_pc[str(i)]["gbs"]
+        out[str(i)] = c
+    return out
+
+
+def _mean_pass(fn):
+    """Mean wall time of fn over CPU_BASELINE_SECONDS (after one untimed call)."""
+    fn()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= CPU_BASELINE_SECONDS:
+            return el / n, n
+
+
+def cpu_baselines(w_softmax):
+    """The oracle as it stands on every configuration's workload (or a stated
+    sample of it), rows -- or, for the split workload's eight rows, column
+    blocks -- spread over the host cores by threads calling the C oracle.
+    Returns {config index: {gbs, rows_per_s, seconds, cores, sample}}."""
+    import concurrent.futures as cf
+    import numpy as np
+    import oracle
+    from reduction_pointwise_row_gb300 import traffic
+    from synth import workloads
+    o = oracle.get()
+    cores = os.cpu_count() or 1
+    res = {}
+
+    def blocks_of(arr, n):
+        return [arr[i * len(arr) // n:(i + 1) * len(arr) // n] for i in range(n)]
+
+    def record(cfg, nbytes, rows_equiv, fn, threads, sample):
+        dt, n = _mean_pass(fn)
+        res[str(cfg)] = {"gbs": round(nbytes / dt / 1e9, 4), "rows_per_s": round(rows_equiv / dt, 1),
+                         "seconds": round(dt, 5), "passes": n, "cores": threads, "sample": sample}
+
+    with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        # 0: Example 1.1, the whole [64, 128] on one thread (too small to split)
+        w = workloads.make(0)
+        a, b = w.arrays["a"], w.arrays["b"]
+        record(0, traffic.algorithmic_bytes("relu_add_sum", 64, 128), 64,
+               lambda: o.relu_add_sum(a, b, 2.0), 1, "all 64 rows x 128")
+        # 1: the headline softmax, every row
+        x = w_softmax.arrays["x"]
+        xb = blocks_of(x, cores)
+        record(1, traffic.algorithmic_bytes("softmax", *x.shape), x.shape[0],
+               lambda: list(ex.map(o.softmax, xb)), cores, f"all {x.shape[0]} rows x {x.shape[1]}")
+        # 2: LayerNorm, every row
+        w = workloads.make(2)
+        xs, g, bt = w.arrays["x"], w.arrays["gamma"], w.arrays["beta"]
+        xsb = blocks_of(xs, cores)
+        record(2, traffic.algorithmic_bytes("layernorm", w.rows, w.cols), w.rows,
+               lambda: list(ex.map(lambda blk: o.layernorm(blk, g, bt, 1e-5), xsb)), cores,
+               f"all {w.rows} rows x {w.cols}")
+        # 3: the split workload's 8 rows, the first 2^22 columns of each, in
+        # `cores` column blocks (each block a contiguous copy)
+        cols3 = 1 << 22
+        w = workloads.make(3, cols=cols3)
+        ab = [(np.ascontiguousarray(w.arrays["a"][:, i * cols3 // cores:(i + 1) * cols3 // cores]),
+               np.ascontiguousarray(w.arrays["b"][:, i * cols3 // cores:(i + 1) * cols3 // cores]))
+              for i in range(cores)]
+        record(3, traffic.algorithmic_bytes("relu_add_sum", 8, cols3), 8 * cols3 / 33554432,
+               lambda: list(ex.map(lambda p: o.relu_add_sum(p[0], p[1], 2.0), ab)), cores,
+               f"8 rows x the first {cols3} of 33554432 columns, in {cores} column blocks")
+        # 4: cross entropy on the first 2048 of 8192 rows
+        w = workloads.make(4, rows=2048)
+        lg, tg = w.arrays["logits"], w.arrays["target"]
+        parts = list(zip(blocks_of(lg, cores), blocks_of(tg, cores)))
+        record(4, traffic.algorithmic_bytes("xent", w.rows, w.cols), w.rows,
+               lambda: list(ex.map(lambda p: o.xent(p[0], p[1], -100), parts)), cores,
+               f"the first {w.rows} of 8192 rows x {w.cols}")
+    return res
 
 
 def run_reference(args):

@@ -96,6 +96,18 @@ const char *fr_status_string(fr_status status);
 fr_form fr_last_form(void);
 
 /*
+ * The form FR_FORM_AUTO picks for `op` on rows x cols of `dtype` on a device
+ * with `sm_count` SMs, for rows whose inputs and outputs share their offset
+ * modulo 32 bytes (contiguous tensors of one shape do; other layouts may take
+ * the looped form instead).  LayerNorm assumes sm_103's 227 KiB of opt-in
+ * shared memory.  A host-side query: no device is touched.  FR_FORM_AUTO (0)
+ * for arguments no call accepts.  The rules are measured crossovers of the
+ * forms on GB300 (Stax (4), section 9.6, Algorithm 9.1: the fastest measured
+ * candidate per shape, recorded).
+ */
+fr_form fr_auto_form(fr_op op, fr_dtype dtype, int64_t rows, int64_t cols, int32_t sm_count);
+
+/*
  * Bytes of device workspace that `op` needs for this shape and form
  * (0 when none).  FR_FORM_AUTO reports the need of the form AUTO will pick.
  * The workspace must be 16-byte aligned; its contents on entry are ignored.

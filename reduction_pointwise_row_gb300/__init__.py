@@ -23,7 +23,7 @@ import os
 from . import buildlib as _build
 
 __all__ = [
-    "FR_OK", "FRError", "lib", "fr_version", "fr_workspace_size", "fr_last_form",
+    "FR_OK", "FRError", "lib", "fr_version", "fr_workspace_size", "fr_last_form", "fr_auto_form",
     "fr_reduce_relu_add_sum", "fr_reduce_sumsq", "fr_softmax", "fr_softmax_host", "fr_layernorm",
     "fr_xent", "fr_xent_workspace", "fr_xent_mean_from_parts", "xent_mean_parts",
     "allreduce_mean_parts", "XENT_PARTS_OFFSET",
@@ -51,6 +51,7 @@ SIGNATURES = {
     "fr_status_string": (ctypes.c_char_p, [_int]),
     "fr_last_form": (_int, []),
     "fr_workspace_size": (_sz, [_int, _i64, _i64, _int, _int]),
+    "fr_auto_form": (_int, [_int, _int, _i64, _i64, ctypes.c_int32]),
     "fr_reduce_relu_add_sum": (_int, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _f32, _int,
                                       _vp, _sz, _vp]),
     "fr_reduce_sumsq": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp, _sz, _vp]),
@@ -160,6 +161,12 @@ def fr_version() -> int:
 
 def fr_last_form() -> str:
     return FORM_NAMES[lib().fr_last_form()]
+
+
+def fr_auto_form(op: str, rows: int, cols: int, dtype: str = "f32", sm_count: int = 152) -> str:
+    """The form AUTO picks for this shape on a device with ``sm_count`` SMs
+    (host-side; no device needed)."""
+    return FORM_NAMES[lib().fr_auto_form(OPS[op], DTYPES[dtype], rows, cols, sm_count)]
 
 
 def fr_workspace_size(op: str, rows: int, cols: int, dtype: str = "f32", form: str = "auto") -> int:

@@ -96,6 +96,9 @@ fr_status launched(cudaError_t e, fr_form form) {
 // fit one warp's registers take the persistent form; few long rows that
 // cannot fill the SMs one warp per row take the split form.
 
+// Shared memory one CTA may opt in to on sm_103 (227 KiB).
+constexpr int kSm103SmemOptin = 232448;
+
 fr_form pick_ras(int64_t rows, int64_t cols, int sm_count, bool bf16 = false) {
   if (cols <= fr::ras_persistent_max_cols(bf16)) return FR_FORM_PERSISTENT;
   if (rows < static_cast<int64_t>(sm_count) * 32 && cols >= 16384) return FR_FORM_SPLIT;
@@ -111,6 +114,18 @@ fr_form pick_softmax(int64_t rows, int64_t cols, bool vec, int sm_count) {
       rows >= 4 * static_cast<int64_t>(sm_count))
     return FR_FORM_PERSISTENT;
   if (vec && cols <= fr::softmax_split_max_cols()) return FR_FORM_SPLIT;
+  return FR_FORM_LOOPED;
+}
+
+// bf16 rows: the fp32 rule with the bf16 limits -- a warp per row up to 2048
+// columns, a CTA per row while the rows fill the SMs, a cluster per row for
+// few or longer rows in phase, else looped.
+fr_form pick_softmax_bf16(int64_t rows, int64_t cols, bool vec, int sm_count) {
+  if (cols <= 2048 ||
+      (cols <= fr::softmax_bf16_persistent_max_cols(vec) &&
+       rows >= 4 * static_cast<int64_t>(sm_count)))
+    return FR_FORM_PERSISTENT;
+  if (vec && cols <= fr::softmax_bf16_split_max_cols()) return FR_FORM_SPLIT;
   return FR_FORM_LOOPED;
 }
 
@@ -147,6 +162,23 @@ const char *fr_status_string(fr_status s) {
 }
 
 fr_form fr_last_form(void) { return g_last_form; }
+
+fr_form fr_auto_form(fr_op op, fr_dtype dtype, int64_t rows, int64_t cols, int32_t sm_count) {
+  if (rows < 1 || cols < 1 || sm_count < 1) return FR_FORM_AUTO;
+  if (dtype != FR_F32 && dtype != FR_BF16) return FR_FORM_AUTO;
+  switch (op) {
+    case FR_OP_RELU_ADD_SUM: return pick_ras(rows, cols, sm_count, dtype == FR_BF16);
+    case FR_OP_SUMSQ: return dtype == FR_F32 ? pick_ras(rows, cols, sm_count) : FR_FORM_AUTO;
+    case FR_OP_SOFTMAX:
+      return dtype == FR_F32 ? pick_softmax(rows, cols, true, sm_count)
+                             : pick_softmax_bf16(rows, cols, true, sm_count);
+    case FR_OP_LAYERNORM:
+      return dtype == FR_BF16 ? pick_layernorm(rows, cols, cols % 16 == 0, true, kSm103SmemOptin)
+                              : FR_FORM_AUTO;
+    case FR_OP_XENT: return FR_FORM_LOOPED;
+  }
+  return FR_FORM_AUTO;
+}
 
 size_t fr_workspace_size(fr_op op, int64_t rows, int64_t cols, fr_dtype dtype, fr_form form) {
   if (rows < 1 || cols < 1) return 0;
@@ -253,19 +285,8 @@ fr_status fr_softmax(const void *x, void *y, int64_t rows, int64_t cols, int64_t
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (dtype == FR_BF16) {
     const int64_t max_p = fr::softmax_bf16_persistent_max_cols(vec);
-    // the fp32 rule with the bf16 limits: a warp per row up to 2048 columns,
-    // a CTA per row while the rows fill the SMs, a cluster per row for few
-    // or longer rows in phase, else looped
-    fr_form f = form;
-    if (form == FR_FORM_AUTO) {
-      if (cols <= 2048 ||
-          (cols <= max_p && rows >= 4 * static_cast<int64_t>(info.sm_count)))
-        f = FR_FORM_PERSISTENT;
-      else if (vec && cols <= fr::softmax_bf16_split_max_cols())
-        f = FR_FORM_SPLIT;
-      else
-        f = FR_FORM_LOOPED;
-    }
+    const fr_form f =
+        form == FR_FORM_AUTO ? pick_softmax_bf16(rows, cols, vec, info.sm_count) : form;
     const uint16_t *bx = static_cast<const uint16_t *>(x);
     uint16_t *by = static_cast<uint16_t *>(y);
     switch (f) {
