@@ -609,6 +609,32 @@ __device__ __forceinline__ void stats16(const V8 &v, float &mean, float &m2) {
   m2 = f32x2_lo(q) + f32x2_hi(q);
 }
 
+// (mean, M2) of the 32 bf16 values of two 32-byte vectors in one pass, by
+// sums shifted by one of the values, c: S1 = sum (x - c), S2 = sum (x - c)^2,
+// mean = c + S1 / 32, M2 = S2 - S1^2 / 32 (the shifted-data form of Chan,
+// Golub and LeVeque, 1983).  Since c is one of the 32 values, M2 >= (c -
+// mean)^2, so the cancellation in S2 - S1^2 / 32 loses at most a factor 33 of
+// relative precision (about 2e-6 in fp32), and x - c is exact for bf16
+// values.  Paired fp32 arithmetic, two columns an instruction.
+__device__ __forceinline__ void stats32(const V8 &a, const V8 &b, float &mean, float &m2) {
+  const float c = bf16_lo(a.w[0]);
+  const uint64_t nc = pack_f32x2(-c, -c);
+  uint64_t s0 = 0, s1 = 0, q0 = 0, q1 = 0;
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    const uint64_t da = add_f32x2(unpack_pair(a.w[h]), nc);
+    const uint64_t db = add_f32x2(unpack_pair(b.w[h]), nc);
+    s0 = add_f32x2(s0, da);
+    s1 = add_f32x2(s1, db);
+    q0 = fma_f32x2(da, da, q0);
+    q1 = fma_f32x2(db, db, q1);
+  }
+  const uint64_t sv = add_f32x2(s0, s1), qv = add_f32x2(q0, q1);
+  const float S1 = f32x2_lo(sv) + f32x2_hi(sv), S2 = f32x2_lo(qv) + f32x2_hi(qv);
+  mean = fmaf(S1, 1.0f / 32.0f, c);
+  m2 = fmaxf(fmaf(-S1, S1 * (1.0f / 32.0f), S2), 0.0f);
+}
+
 // T threads per CTA (a power of two, 64 .. 512), a cluster of C CTAs
 // (1, 2, 4 or 8) per row: cols = C * T * 32.  R rows per step, A rows ahead.
 // Launch bounds: the CTAs of up to 512 threads that one SM holds at 128
@@ -649,16 +675,6 @@ layernorm_cluster_full(const uint16_t *__restrict__ x, const float *__restrict__
 
   auto row_of = [&](int64_t k) { return cid + k * ncl; };
   auto slot_of = [&](int64_t k) { return smem + static_cast<size_t>(k % kSlotsR) * slice; };
-  uint64_t g2[kClCols / 2], b2[kClCols / 2];  // gamma/beta pairs of this thread's columns
-#pragma unroll
-  for (int h = 0; h < kClCols / 4; ++h) {  // chunk h / 2, columns 4 (h % 2) .. + 3
-    const int64_t col = cbase + kChunkStride * (h >> 1) + 4 * (h & 1);
-    const float4 gv = ld_keep_f4(gamma + col), bv = ld_keep_f4(beta + col);
-    g2[2 * h] = pack_f32x2(gv.x, gv.y);
-    g2[2 * h + 1] = pack_f32x2(gv.z, gv.w);
-    b2[2 * h] = pack_f32x2(bv.x, bv.y);
-    b2[2 * h + 1] = pack_f32x2(bv.z, bv.w);
-  }
   // this thread's 32 values of a staged row: chunks 0, 1 in one V8, 2, 3 in another
   auto read_row = [&](int64_t k, V8 &c0, V8 &c1) {
     const unsigned char *p = slot_of(k) + static_cast<size_t>(tid) * 16;
@@ -689,13 +705,26 @@ layernorm_cluster_full(const uint16_t *__restrict__ x, const float *__restrict__
     }
   };
 
+  // The first rows are requested before anything else: the gamma/beta loads
+  // and the cluster barrier below overlap their flight (loading gamma/beta
+  // first held the first copies back, about 1 us of a 4 us start).
   if (tid == 0) {
     timed_out = 0;
     for (int i = 0; i < kSlotsR; ++i) mbar_init(&landed[i], 1);
     for (int i = 0; i < kClSlots; ++i) mbar_init(&pbar[i], 1);
     mbar_init_fence();
-    for (int64_t st = 0; st < kClSlots && st < ns; ++st) mbar_arrive_expect_tx(&pbar[st], part_bytes);
     for (int i = 0; i < kAhead; ++i) issue(i);
+    for (int64_t st = 0; st < kClSlots && st < ns; ++st) mbar_arrive_expect_tx(&pbar[st], part_bytes);
+  }
+  uint64_t g2[kClCols / 2], b2[kClCols / 2];  // gamma/beta pairs of this thread's columns
+#pragma unroll
+  for (int h = 0; h < kClCols / 4; ++h) {  // chunk h / 2, columns 4 (h % 2) .. + 3
+    const int64_t col = cbase + kChunkStride * (h >> 1) + 4 * (h & 1);
+    const float4 gv = ld_keep_f4(gamma + col), bv = ld_keep_f4(beta + col);
+    g2[2 * h] = pack_f32x2(gv.x, gv.y);
+    g2[2 * h + 1] = pack_f32x2(gv.z, gv.w);
+    b2[2 * h] = pack_f32x2(bv.x, bv.y);
+    b2[2 * h + 1] = pack_f32x2(bv.z, bv.w);
   }
   __syncthreads();
   cluster_arrive();  // every CTA's barriers are armed before anyone sends
@@ -713,16 +742,13 @@ layernorm_cluster_full(const uint16_t *__restrict__ x, const float *__restrict__
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         const int64_t k = s * R + r;
-        float mb = 0.0f, m2b = 0.0f;
         mean[r] = m2[r] = 0.0f;
         if (k < nr) {
           wait_row(k);
           V8 c0, c1;
           read_row(k, c0, c1);
-          stats16(c0, mean[r], m2[r]);
-          stats16(c1, mb, m2b);
+          stats32(c0, c1, mean[r], m2[r]);
         }
-        merge_equal(mean[r], m2[r], mb, m2b, 8.0f);  // 16 + 16
       }
       float half_n = 16.0f;  // half of each side's count
 #pragma unroll
