@@ -583,30 +583,9 @@ __device__ __forceinline__ void merge_equal(float &mean, float &m2, float mean_b
   m2 = fmaf(delta * delta, half_n, m2 + m2_b);
 }
 
-// (mean, M2) of the 16 bf16 values of one 32-byte vector, two passes over
-// registers in paired fp32 (the values are unpacked again for the second
-// pass rather than held: registers are the cluster kernel's limit).
+// Two bf16 values of a word as a pair of fp32 (low half first).
 __device__ __forceinline__ uint64_t unpack_pair(uint32_t w) {
   return pack_f32x2(bf16_lo(w), bf16_hi(w));
-}
-__device__ __forceinline__ void stats16(const V8 &v, float &mean, float &m2) {
-  const uint64_t s =
-      add_f32x2(add_f32x2(add_f32x2(unpack_pair(v.w[0]), unpack_pair(v.w[1])),
-                          add_f32x2(unpack_pair(v.w[2]), unpack_pair(v.w[3]))),
-                add_f32x2(add_f32x2(unpack_pair(v.w[4]), unpack_pair(v.w[5])),
-                          add_f32x2(unpack_pair(v.w[6]), unpack_pair(v.w[7]))));
-  mean = (f32x2_lo(s) + f32x2_hi(s)) * (1.0f / 16.0f);
-  const uint64_t nm = pack_f32x2(-mean, -mean);
-  uint64_t q0 = 0, q1 = 0;
-#pragma unroll
-  for (int h = 0; h < 8; h += 2) {
-    const uint64_t d0 = add_f32x2(unpack_pair(v.w[h]), nm);
-    const uint64_t d1 = add_f32x2(unpack_pair(v.w[h + 1]), nm);
-    q0 = fma_f32x2(d0, d0, q0);
-    q1 = fma_f32x2(d1, d1, q1);
-  }
-  const uint64_t q = add_f32x2(q0, q1);
-  m2 = f32x2_lo(q) + f32x2_hi(q);
 }
 
 // (mean, M2) of the 32 bf16 values of two 32-byte vectors in one pass, by
