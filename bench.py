@@ -60,6 +60,8 @@ def parse():
                    help="with --only: force a reduction form")
     p.add_argument("--sweep-ops", default="relu_add_sum,softmax,softmax_bf16,layernorm",
                    help="with --only form_sweep: the ops to sweep")
+    p.add_argument("--sweep-md", metavar="JSONL",
+                   help="print the form table (markdown) of a form_sweep output and exit")
     return p.parse_args()
 
 
@@ -605,7 +607,8 @@ SWEEP_RAS_ROWS = (8, 32, 128, 512, 1024, 2048, 4096, 8192)
 SWEEP_RAS_COLS = (1024, 4096, 16384, 65536, 262144, 1048576, 4194304)
 SWEEP_SM_ROWS = (16, 64, 152, 304, 608, 1216, 2432, 4864, 16384)
 SWEEP_SM_COLS = (1025, 2048, 4097, 8192, 16384, 32768, 65537, 131072, 262144)
-SWEEP_LN_COLS = (768, 1024, 2048, 4096, 5120, 8192, 12288, 16384, 32768, 65536)
+SWEEP_LN_COLS = (768, 1024, 1536, 2048, 2560, 3072, 4096, 5120, 6144, 8192, 12288, 16384, 32768,
+                 65536)
 SWEEP_BYTES_MAX = 1 << 30  # largest input footprint of one call
 
 
@@ -634,28 +637,28 @@ def form_sweep(fr, dev, timed, args, peak, rank):
         return [buf[k * rows:(k + 1) * rows] for k in range(n)]
 
     def measure(make_calls, forms, op, rows, cols):
-        res = {}
+        res, auto_form, auto_us = {}, None, None
         for f in forms:
             calls = make_calls(f)
             try:
                 calls[0]()
             except fr.FRError:
                 continue
-            if f == "auto":
-                res["auto_form"] = fr.fr_last_form()
-                continue
             _, _, per = timed(calls, steps, 3, 1, blocks=3)
-            res[f] = round(sorted(per)[1] * 1e6, 3)
-        times = {k: v for k, v in res.items() if k != "auto_form"}
-        best = min(times, key=times.get) if times else None
+            t = round(sorted(per)[1] * 1e6, 3)
+            if f == "auto":
+                auto_form, auto_us = fr.fr_last_form(), t
+            else:
+                res[f] = t
+        best = min(res, key=res.get) if res else None
         nb = traffic.algorithmic_bytes(op, rows, cols)
-        line = {"op": op, "rows": rows, "cols": cols, "device": name, "sms": sms, "us": times,
-                "fastest": best, "auto": res.get("auto_form"),
-                "best_frac": round(nb / (times[best] * 1e-6) / 1e9 / peak, 4) if best else None}
+        line = {"op": op, "rows": rows, "cols": cols, "device": name, "sms": sms, "us": res,
+                "fastest": best, "auto": auto_form, "auto_us": auto_us,
+                "best_frac": round(nb / (res[best] * 1e-6) / 1e9 / peak, 4) if best else None}
         if rank == 0:
             print(json.dumps(line), flush=True)
 
-    forms3 = ["auto", "persistent", "looped", "split"]
+    forms3 = ["persistent", "looped", "split", "auto"]  # AUTO last: every form warmed alike
     # Example 1.1, fp32
     for rows in SWEEP_RAS_ROWS:
         for cols in SWEEP_RAS_COLS:
@@ -698,27 +701,29 @@ def form_sweep(fr, dev, timed, args, peak, rank):
         bt = torch.zeros(cols, device=dev)
         mean = torch.empty(rows, device=dev)
         rstd = torch.empty(rows, device=dev)
-        res, auto_kernel = {}, None
-        for kname, f in (("auto", "auto"), ("cluster", "looped"), ("ring", "looped"),
-                         ("scalar", "looped"), ("persistent", "persistent")):
-            os.environ["FR_LAYERNORM_KERNEL"] = "" if kname in ("auto", "persistent") else kname
+        res, auto_form, auto_us = {}, None, None
+        for kname, f in (("cluster", "looped"), ("ring", "looped"), ("scalar", "looped"),
+                         ("rows", "persistent"), ("cta", "persistent"), ("auto", "auto")):
+            os.environ["FR_LAYERNORM_KERNEL"] = "" if kname == "auto" else kname
             calls = [lambda x=x, y=y, f=f: fr.fr_layernorm(x, g, bt, 1e-5, form=f, out=y, mean=mean,
                                                           rstd=rstd) for x, y in zip(Xs, Ys)]
             try:
                 calls[0]()
             except fr.FRError:
                 continue
-            if kname == "auto":
-                auto_kernel = fr.fr_last_form()
-                continue
             _, _, per = timed(calls, steps, 3, 1, blocks=3)
-            res[kname] = round(sorted(per)[1] * 1e6, 3)
+            t = round(sorted(per)[1] * 1e6, 3)
+            if kname == "auto":
+                auto_form, auto_us = fr.fr_last_form(), t
+            else:
+                res[kname] = t
         os.environ.pop("FR_LAYERNORM_KERNEL", None)
         best = min(res, key=res.get)
         nb = traffic.algorithmic_bytes("layernorm", rows, cols)
         if rank == 0:
             print(json.dumps({"op": "layernorm", "rows": rows, "cols": cols, "device": name,
-                              "sms": sms, "us": res, "fastest": best, "auto": auto_kernel,
+                              "sms": sms, "us": res, "fastest": best, "auto": auto_form,
+                              "auto_us": auto_us,
                               "best_frac": round(nb / (res[best] * 1e-6) / 1e9 / peak, 4)}),
                   flush=True)
         del Xs, Ys
@@ -968,8 +973,33 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+SWEEP_DTYPE = {"relu_add_sum": "f32", "softmax": "f32", "softmax_bf16": "bf16", "layernorm": "bf16"}
+
+
+def sweep_markdown(path: str) -> str:
+    """The form table: one line per shape with every form's (for LayerNorm,
+    every kernel's) time, the fastest, the form AUTO took and its time."""
+    lines = [json.loads(ln) for ln in open(path) if ln.startswith("{")]
+    dev = {(d["device"], d["sms"]) for d in lines}
+    out = ["| op | dtype | rows | cols | us per call by form (kernel) | fastest | AUTO form | "
+           "AUTO us | AUTO / fastest | fastest, % of peak |",
+           "|---|---|---|---|---|---|---|---|---|---|"]
+    for d in lines:
+        op = d["op"]
+        times = "; ".join(f"{k} {v:.2f}" for k, v in d["us"].items())
+        best = d["us"][d["fastest"]]
+        out.append(f"| {op.replace('_bf16', '')} | {SWEEP_DTYPE[op]} | {d['rows']} | {d['cols']} | "
+                   f"{times} | {d['fastest']} | {d['auto']} | {d['auto_us']:.2f} | "
+                   f"{d['auto_us'] / best:.3f} | {100 * d['best_frac']:.1f} |")
+    head = [f"device: {', '.join(f'{n} ({m} SMs)' for n, m in sorted(dev))}", ""]
+    return "\n".join(head + out)
+
+
 def main():
     args = parse()
+    if args.sweep_md:
+        print(sweep_markdown(args.sweep_md))
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -169,6 +169,13 @@ def fr_auto_form(op: str, rows: int, cols: int, dtype: str = "f32", sm_count: in
     return FORM_NAMES[lib().fr_auto_form(OPS[op], DTYPES[dtype], rows, cols, sm_count)]
 
 
+def sm_count(device=None) -> int:
+    """SMs of the current (or given) CUDA device."""
+    import torch
+    return torch.cuda.get_device_properties(
+        torch.cuda.current_device() if device is None else device).multi_processor_count
+
+
 def fr_workspace_size(op: str, rows: int, cols: int, dtype: str = "f32", form: str = "auto") -> int:
     return lib().fr_workspace_size(OPS[op], rows, cols, DTYPES[dtype], FORMS[form])
 

@@ -39,6 +39,16 @@ __device__ __forceinline__ V8 ld_stream_v8(const void *p) {
   return v;
 }
 
+// 16-byte read-once load: no L1 allocation, and `policy` (an L2 policy from
+// createpolicy, e.g. l2_evict_first_policy()) as the L2 hint.
+__device__ __forceinline__ uint4 ld_stream_u4(const void *p, uint64_t policy) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p), "l"(policy));
+  return v;
+}
+
 // 32-byte load of data that many CTAs re-read (kept in L2 normally).
 __device__ __forceinline__ V8 ld_keep_v8(const void *p) {
   V8 v;

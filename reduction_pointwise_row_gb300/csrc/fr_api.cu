@@ -92,49 +92,78 @@ fr_status launched(cudaError_t e, fr_form form) {
 }
 
 // ---- form selection ---------------------------------------------------------
-// Rules measured on GB300 (see the form table in the design notes): rows that
-// fit one warp's registers take the persistent form; few long rows that
-// cannot fill the SMs one warp per row take the split form.
+// Algorithm 9.1 of "Stax (4): GPU Codegen and Dynamic Shapes", section 9.6:
+// every form that can run was timed on GB300 (152 SMs) over a grid of shapes
+// (bench.py --only form_sweep; the table with every time is
+// profiles/form_table_gb300.md), and each rule below puts its threshold at a
+// measured crossover.  Thresholds on rows scale with the SM count.
 
 // Shared memory one CTA may opt in to on sm_103 (227 KiB).
 constexpr int kSm103SmemOptin = 232448;
 
+// Example 1.1 and the sum of squares.  A row within one warp's registers:
+// persistent.  Otherwise one warp per row streams the row (looped); that warp
+// takes one dependent round trip per 32-byte vector a lane, so few long rows
+// leave the GPU waiting on latency, and the split form (every SM on every
+// row, plus a second small launch) wins.  Crossovers per input row of
+// row_bytes: 64 KiB rows split up to 128 rows and loop from 512 (at 512 x
+// 16384 fp32: looped 21.1 us, split 22.9; at 128: split 12.6, looped 18.3);
+// 256 KiB rows split up to 1024 rows and tie at 2048 (1024 x 65536: split
+// 84.3, looped 89.5; 2048: looped 153.3, split 154.9).
 fr_form pick_ras(int64_t rows, int64_t cols, int sm_count, bool bf16 = false) {
   if (cols <= fr::ras_persistent_max_cols(bf16)) return FR_FORM_PERSISTENT;
-  if (rows < static_cast<int64_t>(sm_count) * 32 && cols >= 16384) return FR_FORM_SPLIT;
+  const int64_t row_bytes = cols * (bf16 ? 2 : 4);
+  const int64_t sms = sm_count;
+  if ((rows < 2 * sms && row_bytes >= (64 << 10)) || (rows < 12 * sms && row_bytes >= (256 << 10)))
+    return FR_FORM_SPLIT;
   return FR_FORM_LOOPED;
 }
 
+// fp32 softmax, rows in phase.  Up to 1024 columns a warp per row; up to 8192
+// a CTA per row at every row count (at fewer than 4 x SMs rows every form
+// takes the launch time, 6.2-7 us; at 2432 x 8192: CTA per row 25.4 us,
+// cluster 32.8); from 16384 a cluster of CTAs per row (16384: within 2 % of a
+// CTA per row; 32768: 94.6 us against 105.9 at 2432 rows); at 262144 columns
+// the looped form once the rows fill the SMs (152 rows: looped 78.2 us, split
+// 79.8; 64 rows: split 39.4, looped 60.6).  Rows out of phase: looped past
+// 1024 columns.
 fr_form pick_softmax(int64_t rows, int64_t cols, bool vec, int sm_count) {
-  // A row within a warp: persistent.  Longer in-phase rows: persistent with a
-  // CTA per row while there are enough rows to fill the SMs, else split over a
-  // cluster of CTAs; rows out of phase or too long for a cluster: looped.
   if (cols <= 1024) return FR_FORM_PERSISTENT;
-  if (vec && cols <= fr::softmax_persistent_max_cols(vec) &&
-      rows >= 4 * static_cast<int64_t>(sm_count))
-    return FR_FORM_PERSISTENT;
-  if (vec && cols <= fr::softmax_split_max_cols()) return FR_FORM_SPLIT;
+  if (!vec) return FR_FORM_LOOPED;
+  if (cols <= 8192) return FR_FORM_PERSISTENT;
+  if (cols <= 131072 || (cols <= fr::softmax_split_max_cols() && rows < sm_count))
+    return FR_FORM_SPLIT;
   return FR_FORM_LOOPED;
 }
 
-// bf16 rows: the fp32 rule with the bf16 limits -- a warp per row up to 2048
-// columns, a CTA per row while the rows fill the SMs, a cluster per row for
-// few or longer rows in phase, else looped.
+// bf16 softmax, rows in phase.  Up to 2048 columns a warp per row, up to 8192
+// a CTA per row; at 16384 the looped form once there are 4 x SMs rows (608:
+// looped 9.4 us, CTA per row 10.5; 4864: 52.0 against 60.3), a CTA per row
+// below; at 32768 a CTA per row while the rows are no more than the SMs (152:
+// 6.7 us against 7.7 for a cluster per row), else, up to 262144 columns, a
+// cluster per row (2432 x 32768: 50.2 us, looped 55.3, CTA per row 73.9).
 fr_form pick_softmax_bf16(int64_t rows, int64_t cols, bool vec, int sm_count) {
-  if (cols <= 2048 ||
-      (cols <= fr::softmax_bf16_persistent_max_cols(vec) &&
-       rows >= 4 * static_cast<int64_t>(sm_count)))
-    return FR_FORM_PERSISTENT;
-  if (vec && cols <= fr::softmax_bf16_split_max_cols()) return FR_FORM_SPLIT;
+  if (cols <= 2048) return FR_FORM_PERSISTENT;
+  if (!vec) return FR_FORM_LOOPED;
+  if (cols <= 8192) return FR_FORM_PERSISTENT;
+  if (cols <= 16384) return rows >= 4 * static_cast<int64_t>(sm_count) ? FR_FORM_LOOPED
+                                                                       : FR_FORM_PERSISTENT;
+  if (cols <= 32768 && rows <= sm_count) return FR_FORM_PERSISTENT;
+  if (cols <= fr::softmax_bf16_split_max_cols()) return FR_FORM_SPLIT;
   return FR_FORM_LOOPED;
 }
 
-fr_form pick_layernorm(int64_t, int64_t cols, bool vec, bool aligned16, int max_smem_optin) {
-  // Measured on GB300, bf16 [4096, 32768]: looped cluster (gamma/beta in
-  // registers, rows split over a 2-CTA cluster, every thread 32 columns)
-  // 91.4 us, its general form 132 us, looped cp.async ring (two rows per
-  // gamma/beta pass) 137 us, persistent 168 us, looped scalar 265 us.  The
-  // looped form tries cluster, then ring, then scalar.
+// LayerNorm (bf16 rows of 256 MiB, back to back).  Rows of C x T x 32 columns
+// from 2048 up (2048 .. 131072 in powers of two): the looped cluster kernel,
+// gamma/beta in registers (4096: 84.5 us against 92.2 for row groups; 32768:
+// 86.4 against 134.6 for the ring); other rows whose gamma/beta fit in shared
+// memory: the persistent row-group kernel (768: 90.1 us, 1536: 83.7, 5120:
+// 100.8, 12288: 133.7, against 263.8, 198.9, 166.9 and 149.3 for the next
+// best); else the looped general cluster, ring or scalar kernel.
+fr_form pick_layernorm(int64_t, int64_t cols, bool vec, bool aligned16, bool rows16,
+                       int max_smem_optin) {
+  if (cols >= 2048 && fr::layernorm_cluster_full_ok(cols, aligned16)) return FR_FORM_LOOPED;
+  if (fr::layernorm_rows_ok(cols, rows16, max_smem_optin)) return FR_FORM_PERSISTENT;
   if (fr::layernorm_cluster_ok(cols, aligned16) || fr::layernorm_ring_ok(cols, vec, max_smem_optin))
     return FR_FORM_LOOPED;
   return fr::layernorm_persistent_ok(cols, vec) ? FR_FORM_PERSISTENT : FR_FORM_LOOPED;
@@ -173,8 +202,9 @@ fr_form fr_auto_form(fr_op op, fr_dtype dtype, int64_t rows, int64_t cols, int32
       return dtype == FR_F32 ? pick_softmax(rows, cols, true, sm_count)
                              : pick_softmax_bf16(rows, cols, true, sm_count);
     case FR_OP_LAYERNORM:
-      return dtype == FR_BF16 ? pick_layernorm(rows, cols, cols % 16 == 0, true, kSm103SmemOptin)
-                              : FR_FORM_AUTO;
+      return dtype == FR_BF16
+                 ? pick_layernorm(rows, cols, cols % 16 == 0, true, cols % 8 == 0, kSm103SmemOptin)
+                 : FR_FORM_AUTO;
     case FR_OP_XENT: return FR_FORM_LOOPED;
   }
   return FR_FORM_AUTO;
@@ -400,16 +430,29 @@ fr_status fr_layernorm(const void *x, const float *gamma, const float *beta, voi
                    ldx % 16 == 0 && ldy % 16 == 0 && cols % 16 == 0;
   const bool aligned16 = aligned(x, 32) && aligned(y, 32) && aligned(gamma, 16) &&
                          aligned(beta, 16) && ldx % 16 == 0 && ldy % 16 == 0;
-  const fr_form f =
-      form == FR_FORM_AUTO ? pick_layernorm(rows, cols, vec, aligned16, info.max_smem_optin) : form;
+  // row groups: 16-byte aligned rows (every row start: ld % 8 == 0) and gamma/beta
+  const bool rows16 = aligned(x, 16) && aligned(y, 16) && aligned(gamma, 16) &&
+                      aligned(beta, 16) && ldx % 8 == 0 && ldy % 8 == 0;
+  const fr_form f = form == FR_FORM_AUTO
+                       ? pick_layernorm(rows, cols, vec, aligned16, rows16, info.max_smem_optin)
+                       : form;
   const uint16_t *bx = static_cast<const uint16_t *>(x);
   uint16_t *by = static_cast<uint16_t *>(y);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   switch (f) {
-    case FR_FORM_PERSISTENT:
+    case FR_FORM_PERSISTENT: {
+      // A row held on chip in one pass: by a group of warps, gamma/beta in
+      // shared memory (default), or by one CTA with gamma/beta re-read from
+      // L2 (FR_LAYERNORM_KERNEL=cta pins it).
+      const char *pin = getenv("FR_LAYERNORM_KERNEL");
+      const bool cta = pin != nullptr && strcmp(pin, "cta") == 0;
+      if (!cta && fr::layernorm_rows_ok(cols, rows16, info.max_smem_optin))
+        return launched(fr::launch_layernorm_rows(bx, gamma, beta, by, mean, rstd, rows, cols, ldx,
+                                                  ldy, eps, info.sm_count, s), f);
       if (!fr::layernorm_persistent_ok(cols, vec)) return FR_ERR_UNSUPPORTED_FORM;
       return launched(fr::launch_layernorm_persistent(bx, gamma, beta, by, mean, rstd, rows, cols,
                                                       ldx, ldy, eps, s), f);
+    }
     case FR_FORM_LOOPED: {
       // FR_LAYERNORM_KERNEL=cluster|ring|scalar pins one looped kernel (for
       // re-measuring the choice and for tests); unset = the first that fits.

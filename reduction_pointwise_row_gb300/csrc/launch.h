@@ -95,10 +95,21 @@ bool layernorm_persistent_ok(int64_t cols, bool vec);
 // cols % (16 * cluster) == 0 and at most 32768 columns (8 CTAs x 256 threads
 // x 16 columns).
 bool layernorm_cluster_ok(int64_t cols, bool aligned);
+// The equal-count cluster kernel: cols = C x T x 32 (T a power of two in
+// 64 .. 512 threads, C in 1, 2, 4, 8 CTAs), aligned as above.
+bool layernorm_cluster_full_ok(int64_t cols, bool aligned);
 cudaError_t launch_layernorm_cluster(const uint16_t *x, const float *gamma, const float *beta,
                                      uint16_t *y, float *mean, float *rstd, int64_t rows,
                                      int64_t cols, int64_t ldx, int64_t ldy, float eps,
                                      cudaStream_t s);
+// Row groups: gamma/beta in shared memory, each row in the registers of a
+// group of warps (cols % 8 == 0 and at most 16384, 16-byte aligned rows and
+// gamma/beta, 8 * cols bytes of shared memory).
+bool layernorm_rows_ok(int64_t cols, bool aligned16, int max_smem_optin);
+cudaError_t launch_layernorm_rows(const uint16_t *x, const float *gamma, const float *beta,
+                                  uint16_t *y, float *mean, float *rstd, int64_t rows,
+                                  int64_t cols, int64_t ldx, int64_t ldy, float eps, int sm_count,
+                                  cudaStream_t s);
 bool layernorm_ring_ok(int64_t cols, bool vec, int max_smem_optin);
 size_t layernorm_ring_smem(int64_t cols, int nbuf);
 cudaError_t launch_layernorm_ring(const uint16_t *x, const float *gamma, const float *beta,

@@ -121,6 +121,157 @@ __device__ __forceinline__ bool first_wait(uint64_t *bar, uint32_t parity) {
 #endif
 }
 
+// ---- row groups: gamma/beta in shared memory, rows in registers --------------
+// For rows up to 16384 columns (cols % 8 == 0, 16-byte aligned rows and
+// gamma/beta).  A persistent grid of 256-thread CTAs, each holding the whole
+// of gamma and beta in shared memory (loaded once), works on rows with
+// groups of WG warps: 8 / WG rows at a time per CTA.  Thread j of a group owns
+// the 16-byte chunks j + 32 WG c (c < NC) of its row, 8 columns each, so a
+// warp's loads and stores are 512 contiguous bytes.  Statistics: each thread's
+// values two-pass in registers (sum, then squared deviations), triples merged
+// with Chan's formula across the warp by shuffles and across the group's
+// warps through shared memory (one named barrier per row, slots double
+// buffered).  One read of x, one write of y; gamma/beta come from shared
+// memory for every row.
+constexpr int kRgThreads = 256;
+
+template <int WG>
+__device__ __forceinline__ void group_sync(int group) {
+  if constexpr (WG > 1)
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(WG * 32) : "memory");
+}
+
+// Chan merge that returns the other side exactly when one side is empty.
+__device__ __forceinline__ Welford merge_or_keep(Welford a, Welford b) {
+  if (b.n == 0.0f) return a;
+  if (a.n == 0.0f) return b;
+  return chan_merge(a, b);
+}
+
+// PF: the next row's chunks are loaded while the current row is worked on.
+template <int WG, int NC, bool PF>
+__global__ void __launch_bounds__(kRgThreads)
+layernorm_rows(const uint16_t *__restrict__ x, const float *__restrict__ gamma,
+               const float *__restrict__ beta, uint16_t *__restrict__ y,
+               float *__restrict__ mean_out, float *__restrict__ rstd_out, int64_t rows,
+               int64_t cols, int64_t ldx, int64_t ldy, float eps) {
+  pdl_enter();
+  constexpr int kGroups = kRgThreads / 32 / WG;  // rows a CTA works on at once
+  extern __shared__ __align__(16) float gb[];      // gamma [cols], then beta [cols]
+  __shared__ Welford part[2][kRgThreads / 32];     // per-warp triples, by row parity
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int group = warp / WG, gt = (warp % WG) * 32 + lane;
+  const int nch = static_cast<int>(cols >> 3);  // 16-byte chunks of a row
+  for (int i = tid; i < nch * 2; i += kRgThreads) {
+    const float *src = i < nch ? gamma + 8 * i : beta + 8 * (i - nch);
+    float4 *dst = reinterpret_cast<float4 *>(gb + 8 * i);
+    dst[0] = ld_keep_f4(src);
+    dst[1] = ld_keep_f4(src + 4);
+  }
+  __syncthreads();
+  const float *sg = gb, *sb = gb + cols;
+  const uint64_t policy = l2_evict_first_policy();
+  int nv = 0;  // this thread's chunks of a row
+#pragma unroll
+  for (int c = 0; c < NC; ++c) nv += gt + 32 * WG * c < nch;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * kGroups;
+  int64_t row = static_cast<int64_t>(blockIdx.x) * kGroups + group;
+  uint4 nx[PF ? NC : 1];
+  if constexpr (PF) {
+    if (row < rows) {
+#pragma unroll
+      for (int c = 0; c < NC; ++c)
+        if (c < nv) nx[c] = ld_stream_u4(x + row * ldx + 8 * (gt + 32 * WG * c), policy);
+    }
+  }
+  int it = 0;
+  for (; row < rows; row += step, ++it) {
+    uint4 v[NC];
+    if constexpr (PF) {
+#pragma unroll
+      for (int c = 0; c < NC; ++c) v[c] = nx[c];
+      if (row + step < rows) {
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+          if (c < nv) nx[c] = ld_stream_u4(x + (row + step) * ldx + 8 * (gt + 32 * WG * c), policy);
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < NC; ++c)
+        if (c < nv) v[c] = ld_stream_u4(x + row * ldx + 8 * (gt + 32 * WG * c), policy);
+    }
+    // two passes over the thread's values: mean, then squared deviations
+    uint64_t s2 = 0;
+#pragma unroll
+    for (int c = 0; c < NC; ++c)
+      if (c < nv) {
+        s2 = add_f32x2(s2, add_f32x2(pack_f32x2(bf16_lo(v[c].x), bf16_hi(v[c].x)),
+                                     pack_f32x2(bf16_lo(v[c].y), bf16_hi(v[c].y))));
+        s2 = add_f32x2(s2, add_f32x2(pack_f32x2(bf16_lo(v[c].z), bf16_hi(v[c].z)),
+                                     pack_f32x2(bf16_lo(v[c].w), bf16_hi(v[c].w))));
+      }
+    const float n_t = static_cast<float>(8 * nv);
+    const float mean_t = nv > 0 ? (f32x2_lo(s2) + f32x2_hi(s2)) / n_t : 0.0f;
+    const uint64_t nm = pack_f32x2(-mean_t, -mean_t);
+    uint64_t q2 = 0;
+#pragma unroll
+    for (int c = 0; c < NC; ++c)
+      if (c < nv) {
+        const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const uint64_t d = add_f32x2(pack_f32x2(bf16_lo(w[h]), bf16_hi(w[h])), nm);
+          q2 = fma_f32x2(d, d, q2);
+        }
+      }
+    Welford t = warp_welford(Welford{n_t, mean_t, f32x2_lo(q2) + f32x2_hi(q2)});
+    if constexpr (WG > 1) {
+      // the group's WG triples on lanes 0 .. WG - 1, merged by a fixed xor
+      // tree (the same bits in every warp of the group), then broadcast
+      if (lane == 0) part[it & 1][warp] = t;
+      group_sync<WG>(group);
+      t = lane < WG ? part[it & 1][group * WG + lane] : Welford{0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int o = WG / 2; o > 0; o >>= 1)
+        t = merge_or_keep(t, Welford{__shfl_xor_sync(0xffffffffu, t.n, o),
+                                     __shfl_xor_sync(0xffffffffu, t.mean, o),
+                                     __shfl_xor_sync(0xffffffffu, t.m2, o)});
+      t = Welford{__shfl_sync(0xffffffffu, t.n, 0), __shfl_sync(0xffffffffu, t.mean, 0),
+                  __shfl_sync(0xffffffffu, t.m2, 0)};
+    }
+    const float mean = t.mean;
+    const float rstd = rsqrtf(fmaf(t.m2, __frcp_rn(t.n), eps));
+    if (gt == 0) {
+      if (mean_out) mean_out[row] = mean;
+      if (rstd_out) rstd_out[row] = rstd;
+    }
+    uint16_t *yr = y + row * ldy;
+    const uint64_t nmr = pack_f32x2(-mean, -mean), r2 = pack_f32x2(rstd, rstd);
+#pragma unroll
+    for (int c = 0; c < NC; ++c)
+      if (c < nv) {
+        const int j = gt + 32 * WG * c;
+        const float4 g0 = *reinterpret_cast<const float4 *>(sg + 8 * j);
+        const float4 g1 = *reinterpret_cast<const float4 *>(sg + 8 * j + 4);
+        const float4 b0 = *reinterpret_cast<const float4 *>(sb + 8 * j);
+        const float4 b1 = *reinterpret_cast<const float4 *>(sb + 8 * j + 4);
+        const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+        const uint64_t gg[4] = {pack_f32x2(g0.x, g0.y), pack_f32x2(g0.z, g0.w),
+                                pack_f32x2(g1.x, g1.y), pack_f32x2(g1.z, g1.w)};
+        const uint64_t bb[4] = {pack_f32x2(b0.x, b0.y), pack_f32x2(b0.z, b0.w),
+                                pack_f32x2(b1.x, b1.y), pack_f32x2(b1.z, b1.w)};
+        uint32_t o[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const uint64_t d = add_f32x2(pack_f32x2(bf16_lo(w[h]), bf16_hi(w[h])), nmr);
+          const uint64_t yv = fma_f32x2(mul_f32x2(d, r2), gg[h], bb[h]);
+          o[h] = pack_bf16x2(f32x2_lo(yv), f32x2_hi(yv));
+        }
+        st_stream_u4(yr + 8 * j, make_uint4(o[0], o[1], o[2], o[3]));
+      }
+  }
+}
+
 // Persistent form.  Requires 32-byte aligned x/y rows, gamma, beta and
 // cols % 16 == 0 (checked by the host); NV vectors of 16 per thread.
 constexpr int kPersistMaxThreads = 512;
@@ -843,10 +994,14 @@ layernorm_cluster_full(const uint16_t *__restrict__ x, const float *__restrict__
 }  // namespace
 
 // Cluster size: the smallest C in {1, 2} with slices of at most 16384
-// columns (32 columns per thread).
+// columns (32 columns per thread), and only when the slices keep at least
+// half the 512 threads busy (a slice of 8192 columns or more: at 768 columns
+// the kernel took 1649 us, 24 of 512 threads working, against 90 us for row
+// groups; at 5120, 278 against 240 for the ring; at 12288, 149).
 int cluster_size_for(int64_t cols) {
   for (int c = 1; c <= kClMaxCluster; c <<= 1)
-    if (cols % (kClCols * c) == 0 && cols / c <= kClMaxSlice) return c;
+    if (cols % (kClCols * c) == 0 && cols / c <= kClMaxSlice && cols / c >= kClMaxSlice / 2)
+      return c;
   return 0;
 }
 
@@ -912,6 +1067,11 @@ bool full_shape(int64_t cols, int *T, int *C) {
 bool layernorm_cluster_ok(int64_t cols, bool aligned) {
   int t = 0, c = 0;
   return aligned && (cluster_size_for(cols) > 0 || full_shape(cols, &t, &c));
+}
+
+bool layernorm_cluster_full_ok(int64_t cols, bool aligned) {
+  int t = 0, c = 0;
+  return aligned && full_shape(cols, &t, &c);
 }
 
 cudaError_t launch_layernorm_cluster(const uint16_t *x, const float *gamma, const float *beta,
@@ -1018,6 +1178,63 @@ cudaError_t launch_layernorm_ring(const uint16_t *x, const float *gamma, const f
   void *args[] = {&x, &gamma, &beta, &y, &mean, &rstd, &rows, &cols, &ldx, &ldy, &eps, &err};
   return cudaLaunchKernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kRingThreads), args, smem,
                           s);
+}
+
+// Row groups: the fewest warps per row (1, 2, 4 or 8) that hold it in at most
+// NMAX chunks of 8 columns a thread; NC rounded up to 2, 4, 6 or 8.
+// FR_LAYERNORM_ROWS_NC=4|8 sets NMAX (default 8).
+namespace {
+bool rows_shape(int64_t cols, int *WG, int *NC) {
+  const int64_t nch = cols / 8;
+  const char *e = getenv("FR_LAYERNORM_ROWS_NC");
+  const int nmax = e != nullptr && atoi(e) == 4 ? 4 : 8;
+  for (int wg = 1; wg <= 8; wg <<= 1) {
+    const int64_t need = (nch + 32 * wg - 1) / (32 * wg);
+    if (need <= nmax) {
+      *WG = wg;
+      *NC = need <= 2 ? 2 : need <= 4 ? 4 : need <= 6 ? 6 : 8;
+      return true;
+    }
+  }
+  return false;
+}
+}  // namespace
+
+bool layernorm_rows_ok(int64_t cols, bool aligned16, int max_smem_optin) {
+  int wg = 0, nc = 0;
+  return aligned16 && cols % 8 == 0 && rows_shape(cols, &wg, &nc) &&
+         static_cast<int64_t>(cols) * 8 + 1024 <= max_smem_optin;
+}
+
+cudaError_t launch_layernorm_rows(const uint16_t *x, const float *gamma, const float *beta,
+                                  uint16_t *y, float *mean, float *rstd, int64_t rows,
+                                  int64_t cols, int64_t ldx, int64_t ldy, float eps, int sm_count,
+                                  cudaStream_t s) {
+  int WG = 0, NC = 0;
+  if (!rows_shape(cols, &WG, &NC)) return cudaErrorInvalidValue;
+  using K = void (*)(const uint16_t *, const float *, const float *, uint16_t *, float *, float *,
+                     int64_t, int64_t, int64_t, int64_t, float);
+  // chunks of up to 4 a thread: the next row prefetched into registers;
+  // 6 or 8: no prefetch (registers), more rows in flight instead
+#define FR_LNR(W)                                                                        \
+  (NC == 2 ? layernorm_rows<W, 2, true> : NC == 4 ? layernorm_rows<W, 4, true>           \
+   : NC == 6 ? layernorm_rows<W, 6, false> : layernorm_rows<W, 8, false>)
+  K kern = WG == 1 ? FR_LNR(1) : WG == 2 ? FR_LNR(2) : WG == 4 ? FR_LNR(4) : FR_LNR(8);
+#undef FR_LNR
+  const size_t smem = static_cast<size_t>(cols) * 8;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRgThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  const int groups = kRgThreads / 32 / WG;
+  int64_t grid = static_cast<int64_t>(sm_count) * per_sm;
+  const int64_t need = (rows + groups - 1) / groups;
+  if (grid > need) grid = need;
+  return launch_k(kern, dim3(static_cast<unsigned>(grid)), dim3(kRgThreads), smem, s, 0, x, gamma,
+                  beta, y, mean, rstd, rows, cols, ldx, ldy, eps);
 }
 
 bool layernorm_persistent_ok(int64_t cols, bool vec) {

@@ -1,0 +1,59 @@
+"""The form selection against the committed measurements (no GPU).
+
+profiles/form_table_gb300.md holds, for a grid of shapes, the time of every
+reduction form (for LayerNorm, every kernel) measured on GB300 and the form
+AUTO took with its own time (bench.py --only form_sweep).  Algorithm 9.1 of
+"Stax (4): GPU Codegen and Dynamic Shapes", section 9.6, picks the fastest
+measured candidate per shape; here the rules of fr_auto_form must (1) still
+name the form AUTO took in that measurement -- a changed rule needs a new
+measurement -- and (2) have cost no more than the timing noise over the
+fastest candidate: AUTO's time within 6 % + 0.6 us of the fastest (two timings
+of one kernel in one sweep differed by up to 6 %, and launch-bound shapes
+take 6-8 us give or take 0.6).
+"""
+import os
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+TABLE = os.path.join(ROOT, "profiles", "form_table_gb300.md")
+
+
+def table_rows():
+    rows = []
+    sms = None
+    for line in open(TABLE):
+        if line.startswith("device:"):
+            sms = int(line.split("(")[1].split()[0])
+        if not line.startswith("| ") or line.startswith("| op ") or line.startswith("|---"):
+            continue
+        f = [c.strip() for c in line.strip().strip("|").split("|")]
+        times = {k: float(v) for k, v in (t.split() for t in f[4].split(";"))}
+        rows.append(dict(op=f[0], dtype=f[1], rows=int(f[2]), cols=int(f[3]), times=times,
+                         fastest=f[5], auto=f[6], auto_us=float(f[7])))
+    assert sms and rows
+    return sms, rows
+
+
+def test_table_covers_every_op_and_the_forms():
+    _, rows = table_rows()
+    ops = {(r["op"], r["dtype"]) for r in rows}
+    assert ops == {("relu_add_sum", "f32"), ("softmax", "f32"), ("softmax", "bf16"),
+                   ("layernorm", "bf16")}
+    assert len(rows) >= 150
+
+
+def test_rules_name_the_form_auto_took():
+    import reduction_pointwise_row_gb300 as fr
+    sms, rows = table_rows()
+    for r in rows:
+        assert fr.fr_auto_form(r["op"], r["rows"], r["cols"], r["dtype"], sms) == r["auto"], r
+
+
+@pytest.mark.parametrize("tol,abs_us", [(0.06, 0.6)])
+def test_auto_is_within_noise_of_the_fastest(tol, abs_us):
+    _, rows = table_rows()
+    slow = [(r["op"], r["dtype"], r["rows"], r["cols"], r["auto"], r["auto_us"], r["fastest"],
+             r["times"][r["fastest"]]) for r in rows
+            if r["auto_us"] > (1 + tol) * r["times"][r["fastest"]] + abs_us]
+    assert not slow, slow

@@ -206,12 +206,12 @@ def test_softmax_special_values(o, cols):
 @pytest.mark.parametrize("cols", [1025, 8193, 32769, 65537, 131071, 262144])
 def test_softmax_split_long_rows(o, cols):
     """The cluster split form on few long rows, row by row against the oracle,
-    and the form AUTO picks for them (split while a cluster holds the row)."""
+    and AUTO on them picks the form fr_auto_form names."""
     w = workloads.make(1, rows=3, cols=cols, seed=2900 + cols)
     ref = o.softmax(w.arrays["x"])
     assert_close(run_softmax(w.arrays["x"], "split"), ref, "f32", f"split 3x{cols}")
     assert_close(run_softmax(w.arrays["x"], "auto"), ref, "f32", f"auto 3x{cols}")
-    assert fr.fr_last_form() == "split"
+    assert fr.fr_last_form() == fr.fr_auto_form("softmax", 3, cols, "f32", fr.sm_count())
 
 
 def test_softmax_in_place_and_rows_sum_to_one(o):
@@ -265,7 +265,9 @@ def test_layernorm_forms(o, rows, cols, offset):
     eps = float(np.float32(w.params["eps"]))
     ry, rm, rr = o.layernorm(w.arrays["x"], w.arrays["gamma"], w.arrays["beta"], eps)
     vec_ok = offset == 0 and cols % 16 == 0 and cols <= 32768
-    runs = ([("persistent", None)] if vec_ok else []) + \
+    rows_ok = offset == 0 and cols % 8 == 0 and cols <= 16384  # row-group kernel
+    runs = ([("persistent", None)] if vec_ok or rows_ok else []) + \
+        ([("persistent", "cta")] if vec_ok else []) + \
         [("looped", k) for k in ("cluster", "ring", "ring-bulk", "scalar")]
     for form, kernel in runs:
         y, m, r = run_layernorm(w.arrays["x"], w.arrays["gamma"], w.arrays["beta"], eps, form,
@@ -274,11 +276,33 @@ def test_layernorm_forms(o, rows, cols, offset):
         assert_close(y, ry, "bf16", f"{what} y")
         assert_close(m, rm, "mean", f"{what} mean")
         assert_close(r, rr, "f32", f"{what} rstd")
-    if not vec_ok:
+    if not vec_ok and not rows_ok:
         with pytest.raises(fr.FRError) as e:
             run_layernorm(w.arrays["x"], w.arrays["gamma"], w.arrays["beta"], eps, "persistent",
                           offset)
         assert e.value.status == 3
+
+
+@pytest.mark.parametrize("cols", [8, 16, 256, 264, 768, 1000, 1024, 1032, 2048, 3072, 4104, 5120,
+                                  8192, 12288, 16384])
+def test_layernorm_row_groups(o, cols):
+    """The row-group kernel (gamma/beta in shared memory, a row in the
+    registers of 1, 2, 4 or 8 warps): more rows than the persistent grid has
+    groups, ragged chunk counts, a constant row and a large-mean row."""
+    for rows in (1, 7, 301, 2500):
+        w = workloads.make(2, rows=rows, cols=cols, seed=3900 + rows + cols)
+        x = w.arrays["x"].copy()
+        if rows >= 7:
+            x[2, :] = 0x3F80   # 1.0: var 0
+            x[5, :] = 0x4780   # 65536: large mean, var 0
+        eps = float(np.float32(w.params["eps"]))
+        ry, rm, rr = o.layernorm(x, w.arrays["gamma"], w.arrays["beta"], eps)
+        y, m, r = run_layernorm(x, w.arrays["gamma"], w.arrays["beta"], eps, "persistent",
+                                kernel="rows")
+        what = f"rows kernel {rows}x{cols}"
+        assert_close(y, ry, "bf16", f"{what} y")
+        assert_close(m, rm, "mean", f"{what} mean")
+        assert_close(r, rr, "f32", f"{what} rstd")
 
 
 @pytest.mark.parametrize("cta", ["256", "512", "128"])
@@ -525,7 +549,10 @@ def test_auto_form_choices():
     assert fr.fr_last_form() == "persistent"  # one CTA per row, enough rows
     x = torch.zeros(16, 4097, device="cuda")
     fr.fr_softmax(x)
-    assert fr.fr_last_form() == "split"  # too few rows: a cluster per row
+    assert fr.fr_last_form() == "persistent"  # up to 8192 columns at any row count
+    x = torch.zeros(16, 16384, device="cuda")
+    fr.fr_softmax(x)
+    assert fr.fr_last_form() == "split"  # a cluster per row from 16384 columns
     x = torch.zeros(4, 32769, device="cuda")
     fr.fr_softmax(x)
     assert fr.fr_last_form() == "split"
