@@ -62,6 +62,9 @@ def parse():
                    help="with --only form_sweep: the ops to sweep")
     p.add_argument("--sweep-md", metavar="JSONL",
                    help="print the form table (markdown) of a form_sweep output and exit")
+    p.add_argument("--launches-md", metavar="CSV",
+                   help="print the per-kernel summary (markdown) of an ncu launch list "
+                        "(--metrics gpu__time_duration.sum --csv) and exit")
     return p.parse_args()
 
 
@@ -995,8 +998,44 @@ def sweep_markdown(path: str) -> str:
     return "\n".join(head + out)
 
 
+HOST_ROWS_NS = 300_000  # softmax launches longer than this read and write host memory (e2e)
+
+
+def launches_markdown(path: str) -> str:
+    """Launches, total time and share per kernel of an ncu launch list.  The
+    softmax kernel's end-to-end launches (rows in page-locked host memory,
+    fr_softmax_host's direct form, about 900 us each) are listed apart from
+    its device-resident launches (under 300 us)."""
+    import csv
+    import re as _re
+    rows = [r for r in csv.reader(ln for ln in open(path) if ln.startswith('"'))]
+    head, rows = rows[0], rows[1:]
+    ki, ui, vi = head.index("Kernel Name"), head.index("Metric Unit"), head.index("Metric Value")
+    scale = {"ns": 1.0, "nsecond": 1.0, "us": 1e3, "usecond": 1e3, "ms": 1e6, "msecond": 1e6}
+    groups = {}
+    for r in rows:
+        ns = float(r[vi].replace(",", "")) * scale[r[ui]]
+        name = _re.sub(r"^void ", "", r[ki])
+        name = name.replace("fr::<unnamed>::", "")
+        name = _re.sub(r"\(.*$", "", name)
+        if name.startswith("softmax_warp_vec") and ns > HOST_ROWS_NS:
+            name += " (rows in host memory, e2e)"
+        g = groups.setdefault(name, [0, 0.0])
+        g[0] += 1
+        g[1] += ns
+    total = sum(g[1] for g in groups.values())
+    out = [f"{len(rows)} launches, {total / 1e3:.1f} us in all.", "",
+           "| kernel | launches | total us | mean us | share |", "|---|---|---|---|---|"]
+    for name, (n, t) in sorted(groups.items(), key=lambda kv: -kv[1][1]):
+        out.append(f"| `{name}` | {n} | {t / 1e3:.1f} | {t / n / 1e3:.2f} | {100 * t / total:.1f} % |")
+    return "\n".join(out)
+
+
 def main():
     args = parse()
+    if args.launches_md:
+        print(launches_markdown(args.launches_md))
+        return
     if args.sweep_md:
         print(sweep_markdown(args.sweep_md))
         return
