@@ -54,7 +54,8 @@ def parse():
                                       "softmax_65537", "softmax_65537_looped",
                                       "looped", "looped_bf16", "softmax_bf16", "xent_f32",
                                       "softmax_bf16_4097", "softmax_bf16_4097_looped",
-                                      "softmax_bf16_65537", "xent_box", "form_sweep"],
+                                      "softmax_bf16_65537", "xent_box", "form_sweep",
+                                      "layernorm_768", "layernorm_5120", "layernorm_12288"],
                    help="time one workload alone (for profiler captures) and exit")
     p.add_argument("--form", default="auto", choices=["auto", "persistent", "looped", "split"],
                    help="with --only: force a reduction form")
@@ -463,6 +464,21 @@ def setup_workload(name, fr, workloads, dev, form="auto"):
         return calls, "relu_add_sum_bf16", w.rows, w.cols, 1
     if name == "layernorm":
         w = make_shard(workloads, 2)
+        g, bt = to_device(w.arrays["gamma"], dev), to_device(w.arrays["beta"], dev)
+        for _ in range(nsets("layernorm", w.rows, w.cols)):
+            x = to_device(w.arrays["x"], dev)
+            y = torch.empty_like(x)
+            mean = torch.empty(w.rows, device=dev)
+            rstd = torch.empty(w.rows, device=dev)
+            calls.append(lambda x=x, y=y, mean=mean, rstd=rstd:
+                         fr.fr_layernorm(x, g, bt, 1e-5, out=y, mean=mean, rstd=rstd,
+                                         form=form))
+        return calls, "layernorm", w.rows, w.cols, 1
+    if name.startswith("layernorm_"):
+        # LayerNorm at another hidden size, 256 MiB of x (the workload's
+        # distribution, gamma/beta of that length)
+        cols = int(name.split("_")[1])
+        w = make_shard(workloads, 2, rows=(1 << 27) // cols, cols=cols)
         g, bt = to_device(w.arrays["gamma"], dev), to_device(w.arrays["beta"], dev)
         for _ in range(nsets("layernorm", w.rows, w.cols)):
             x = to_device(w.arrays["x"], dev)

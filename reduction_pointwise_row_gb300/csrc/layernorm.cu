@@ -149,7 +149,9 @@ __device__ __forceinline__ Welford merge_or_keep(Welford a, Welford b) {
 }
 
 // PF: the next row's chunks are loaded while the current row is worked on.
-template <int WG, int NC, bool PF>
+// PL: gamma/beta in shared memory as four float4 planes (below); otherwise
+// chunk by chunk, gamma [cols] then beta [cols].
+template <int WG, int NC, bool PF, bool PL>
 __global__ void __launch_bounds__(kRgThreads)
 layernorm_rows(const uint16_t *__restrict__ x, const float *__restrict__ gamma,
                const float *__restrict__ beta, uint16_t *__restrict__ y,
@@ -157,19 +159,26 @@ layernorm_rows(const uint16_t *__restrict__ x, const float *__restrict__ gamma,
                int64_t cols, int64_t ldx, int64_t ldy, float eps) {
   pdl_enter();
   constexpr int kGroups = kRgThreads / 32 / WG;  // rows a CTA works on at once
-  extern __shared__ __align__(16) float gb[];      // gamma [cols], then beta [cols]
+  // gamma and beta of chunk j (its 8 columns) as four float4 planes:
+  // gb[j] = gamma 8j..8j+3, gb[nch + j] = gamma 8j+4..8j+7, then beta the
+  // same at 2 nch and 3 nch, so a warp reading one plane for 32 consecutive
+  // chunks reads 512 contiguous bytes (one 32-byte chunk a lane would take
+  // twice the shared-memory wavefronts)
+  extern __shared__ __align__(16) float4 gb[];
   __shared__ Welford part[2][kRgThreads / 32];     // per-warp triples, by row parity
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int group = warp / WG, gt = (warp % WG) * 32 + lane;
   const int nch = static_cast<int>(cols >> 3);  // 16-byte chunks of a row
-  for (int i = tid; i < nch * 2; i += kRgThreads) {
-    const float *src = i < nch ? gamma + 8 * i : beta + 8 * (i - nch);
-    float4 *dst = reinterpret_cast<float4 *>(gb + 8 * i);
-    dst[0] = ld_keep_f4(src);
-    dst[1] = ld_keep_f4(src + 4);
+  if constexpr (PL) {
+    for (int i = tid; i < nch * 4; i += kRgThreads) {
+      const int plane = i / nch, j = i - plane * nch;
+      gb[i] = ld_keep_f4((plane < 2 ? gamma : beta) + 8 * j + 4 * (plane & 1));
+    }
+  } else {
+    for (int i = tid; i < nch * 4; i += kRgThreads)
+      gb[i] = ld_keep_f4((i < 2 * nch ? gamma : beta - 8 * nch) + 4 * i);
   }
   __syncthreads();
-  const float *sg = gb, *sb = gb + cols;
   const uint64_t policy = l2_evict_first_policy();
   int nv = 0;  // this thread's chunks of a row
 #pragma unroll
@@ -251,10 +260,9 @@ layernorm_rows(const uint16_t *__restrict__ x, const float *__restrict__ gamma,
     for (int c = 0; c < NC; ++c)
       if (c < nv) {
         const int j = gt + 32 * WG * c;
-        const float4 g0 = *reinterpret_cast<const float4 *>(sg + 8 * j);
-        const float4 g1 = *reinterpret_cast<const float4 *>(sg + 8 * j + 4);
-        const float4 b0 = *reinterpret_cast<const float4 *>(sb + 8 * j);
-        const float4 b1 = *reinterpret_cast<const float4 *>(sb + 8 * j + 4);
+        const float4 g0 = PL ? gb[j] : gb[2 * j], g1 = PL ? gb[nch + j] : gb[2 * j + 1],
+                     b0 = PL ? gb[2 * nch + j] : gb[2 * nch + 2 * j],
+                     b1 = PL ? gb[3 * nch + j] : gb[2 * nch + 2 * j + 1];
         const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
         const uint64_t gg[4] = {pack_f32x2(g0.x, g0.y), pack_f32x2(g0.z, g0.w),
                                 pack_f32x2(g1.x, g1.y), pack_f32x2(g1.z, g1.w)};
@@ -1216,10 +1224,37 @@ cudaError_t launch_layernorm_rows(const uint16_t *x, const float *gamma, const f
                      int64_t, int64_t, int64_t, int64_t, float);
   // chunks of up to 4 a thread: the next row prefetched into registers;
   // 6 or 8: no prefetch (registers), more rows in flight instead
-#define FR_LNR(W)                                                                        \
-  (NC == 2 ? layernorm_rows<W, 2, true> : NC == 4 ? layernorm_rows<W, 4, true>           \
-   : NC == 6 ? layernorm_rows<W, 6, false> : layernorm_rows<W, 8, false>)
-  K kern = WG == 1 ? FR_LNR(1) : WG == 2 ? FR_LNR(2) : WG == 4 ? FR_LNR(4) : FR_LNR(8);
+  // (more than one warp a row only when one warp would need more than the
+  // chunks allowed a thread, so never with 2)
+  // gamma/beta layout, measured on GB300 (256 MiB of x, us per call, chunk
+  // by chunk / planes): 768 columns 90.8 / 89.5, 1024 85.5 / 96.4, 1536
+  // 84.2 / 96.0, 2560 92.4 / 85.0, 3072 88.9 / 93.7, 5120 100.9 / 88.6, 6144
+  // 106.3 / 99.6, 12288 134.0 / 127.4.  The planes, though they halve the
+  // shared-memory wavefronts (768: 20.6 M to 12.0 M), were slower where one
+  // or two warps hold a row and every thread holds all NC chunks; the rule
+  // below picks the faster layout at all eight sizes.
+  // FR_LAYERNORM_ROWS_GB=planar|chunk pins one.
+  const int64_t nch = cols / 8;
+  const bool full_chunks = nch % (32 * static_cast<int64_t>(WG)) == 0 &&
+                           nch / (32 * static_cast<int64_t>(WG)) == NC;
+  bool pl = WG >= 4 || !full_chunks;
+  if (const char *gl = getenv("FR_LAYERNORM_ROWS_GB"); gl != nullptr)
+    pl = strcmp(gl, "planar") == 0;
+  // Rows past 8192 columns (8 warps a row, 64 KiB and more of gamma/beta: at
+  // most three CTAs an SM) prefetch the next row with 6 or 8 chunks a thread
+  // too: fewer rows in flight otherwise.
+  const bool pf8 = cols > 8192;
+#define FR_LNR(W, P)                                                                     \
+  (NC == 4 ? layernorm_rows<W, 4, true, P> : NC == 6 ? layernorm_rows<W, 6, false, P>    \
+           : layernorm_rows<W, 8, false, P>)
+#define FR_LNR8(P)                                                                       \
+  (pf8 ? (NC == 6 ? layernorm_rows<8, 6, true, P> : layernorm_rows<8, 8, true, P>)       \
+       : FR_LNR(8, P))
+  K kern = pl ? (WG == 1 ? (NC == 2 ? layernorm_rows<1, 2, true, true> : FR_LNR(1, true))
+                 : WG == 2 ? FR_LNR(2, true) : WG == 4 ? FR_LNR(4, true) : FR_LNR8(true))
+              : (WG == 1 ? (NC == 2 ? layernorm_rows<1, 2, true, false> : FR_LNR(1, false))
+                 : WG == 2 ? FR_LNR(2, false) : WG == 4 ? FR_LNR(4, false) : FR_LNR8(false));
+#undef FR_LNR8
 #undef FR_LNR
   const size_t smem = static_cast<size_t>(cols) * 8;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -285,10 +285,21 @@ def test_layernorm_forms(o, rows, cols, offset):
 
 @pytest.mark.parametrize("cols", [8, 16, 256, 264, 768, 1000, 1024, 1032, 2048, 3072, 4104, 5120,
                                   8192, 12288, 16384])
-def test_layernorm_row_groups(o, cols):
-    """The row-group kernel (gamma/beta in shared memory, a row in the
-    registers of 1, 2, 4 or 8 warps): more rows than the persistent grid has
-    groups, ragged chunk counts, a constant row and a large-mean row."""
+@pytest.mark.parametrize("layout", ["chunk", "planar"])
+def test_layernorm_row_groups(o, cols, layout):
+    """The row-group kernel (gamma/beta in shared memory, chunk by chunk or as
+    four float4 planes; a row in the registers of 1, 2, 4 or 8 warps): more
+    rows than the persistent grid has groups, ragged chunk counts, a constant
+    row and a large-mean row."""
+    import os
+    os.environ["FR_LAYERNORM_ROWS_GB"] = layout
+    try:
+        _row_groups(o, cols)
+    finally:
+        os.environ.pop("FR_LAYERNORM_ROWS_GB", None)
+
+
+def _row_groups(o, cols):
     for rows in (1, 7, 301, 2500):
         w = workloads.make(2, rows=rows, cols=cols, seed=3900 + rows + cols)
         x = w.arrays["x"].copy()
