@@ -59,7 +59,7 @@ def parse():
                    help="time one workload alone (for profiler captures) and exit")
     p.add_argument("--form", default="auto", choices=["auto", "persistent", "looped", "split"],
                    help="with --only: force a reduction form")
-    p.add_argument("--sweep-ops", default="relu_add_sum,softmax,softmax_bf16,layernorm",
+    p.add_argument("--sweep-ops", default="relu_add_sum,softmax,softmax_bf16,softmax_offset,layernorm",
                    help="with --only form_sweep: the ops to sweep")
     p.add_argument("--sweep-md", metavar="JSONL",
                    help="print the form table (markdown) of a form_sweep output and exit")
@@ -626,6 +626,7 @@ SWEEP_RAS_ROWS = (8, 32, 128, 512, 1024, 2048, 4096, 8192)
 SWEEP_RAS_COLS = (1024, 4096, 16384, 65536, 262144, 1048576, 4194304)
 SWEEP_SM_ROWS = (16, 64, 152, 304, 608, 1216, 2432, 4864, 16384)
 SWEEP_SM_COLS = (1025, 2048, 4097, 8192, 16384, 32768, 65537, 131072, 262144)
+SWEEP_OFFSET_COLS = (1025, 2048, 4097, 8192, 16384, 32768, 65537)
 SWEEP_LN_COLS = (768, 1024, 1536, 2048, 2560, 3072, 4096, 5120, 6144, 8192, 12288, 16384, 32768,
                  65536)
 SWEEP_BYTES_MAX = 1 << 30  # largest input footprint of one call
@@ -710,6 +711,23 @@ def form_sweep(fr, dev, timed, args, peak, rank):
                     return [lambda x=x, y=y: fr.fr_softmax(x, out=y, form=f) for x, y in zip(Xs, Ys)]
                 measure(mk, forms3, op, rows, cols)
                 del Xs, Ys
+    # fp32 softmax with x one element past y's phase (every row out of
+    # 32-byte phase: no vector pairing of x and y)
+    for rows in SWEEP_SM_ROWS:
+        for cols in SWEEP_OFFSET_COLS:
+            if ("softmax_offset" not in ops or rows * cols * 8 > SWEEP_BYTES_MAX or
+                    rows * cols * 4 < (1 << 20)):
+                continue
+            nset = max(2, -(-ROTATE_BYTES // (8 * rows * cols)))
+            flat = torch.empty(nset * rows * cols + 8, device=dev).uniform_(-1.0, 1.0)
+            Xs = [flat[1 + k * rows * cols:1 + (k + 1) * rows * cols].view(rows, cols)
+                  for k in range(nset)]
+            Ys = rotating(rows, cols, torch.float32, 8 * rows * cols, fill=False)
+
+            def mk(f, Xs=Xs, Ys=Ys):
+                return [lambda x=x, y=y: fr.fr_softmax(x, out=y, form=f) for x, y in zip(Xs, Ys)]
+            measure(mk, forms3, "softmax_offset", rows, cols)
+            del Xs, Ys, flat
     # LayerNorm: its kernels (the looped form's cluster, ring and scalar
     # kernels, and the persistent form), 256 MiB of x per call
     for cols in SWEEP_LN_COLS if "layernorm" in ops else ():
@@ -992,7 +1010,8 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-SWEEP_DTYPE = {"relu_add_sum": "f32", "softmax": "f32", "softmax_bf16": "bf16", "layernorm": "bf16"}
+SWEEP_DTYPE = {"relu_add_sum": "f32", "softmax": "f32", "softmax_bf16": "bf16",
+               "softmax_offset": "f32", "layernorm": "bf16"}
 
 
 def sweep_markdown(path: str) -> str:
@@ -1007,7 +1026,8 @@ def sweep_markdown(path: str) -> str:
         op = d["op"]
         times = "; ".join(f"{k} {v:.2f}" for k, v in d["us"].items())
         best = d["us"][d["fastest"]]
-        out.append(f"| {op.replace('_bf16', '')} | {SWEEP_DTYPE[op]} | {d['rows']} | {d['cols']} | "
+        name = op.replace('_bf16', '').replace('softmax_offset', 'softmax, x out of phase')
+        out.append(f"| {name} | {SWEEP_DTYPE[op]} | {d['rows']} | {d['cols']} | "
                    f"{times} | {d['fastest']} | {d['auto']} | {d['auto_us']:.2f} | "
                    f"{d['auto_us'] / best:.3f} | {100 * d['best_frac']:.1f} |")
     head = [f"device: {', '.join(f'{n} ({m} SMs)' for n, m in sorted(dev))}", ""]

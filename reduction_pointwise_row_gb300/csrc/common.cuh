@@ -13,6 +13,9 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
 #include <cuda_runtime.h>
 
 #include "../../include/fr.h"
@@ -316,6 +319,12 @@ __device__ __forceinline__ void cp_async_16(void *dst, const void *src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
                : "memory");
 }
+// The same with an L2 policy (createpolicy) as the hint.
+__device__ __forceinline__ void cp_async_16_hint(void *dst, const void *src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)),
+               "l"(src), "l"(policy)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
@@ -509,6 +518,77 @@ inline cudaError_t launch_pdl(const void *kern, dim3 grid, dim3 block, void **ar
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelExC(&cfg, kern, args);
+}
+
+// ---- launch properties, looked up once ---------------------------------------
+// The dynamic shared memory a kernel may use and its occupancy depend only on
+// the kernel, the device and the launch shape, so each is asked of the runtime
+// once and remembered (a launch-bound call otherwise pays for the driver calls
+// on every launch).
+
+// Raises kern's dynamic shared-memory limit on the current device to at least
+// `bytes` (a limit, so a larger earlier setting serves).
+inline cudaError_t set_smem_limit(const void *kern, size_t bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void *>, size_t> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  size_t &have = done[{dev, kern}];
+  if (have >= bytes && (have > 0 || bytes == 0)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(bytes));
+  if (e == cudaSuccess) have = bytes > have ? bytes : have;
+  return e;
+}
+
+// CTAs of `threads` threads and `smem` dynamic bytes that one SM holds.
+inline cudaError_t blocks_per_sm(int *out, const void *kern, int threads, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, const void *, int, size_t>, int> known;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const auto key = std::make_tuple(dev, kern, threads, smem);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = known.find(key);
+    if (it != known.end()) {
+      *out = it->second;
+      return cudaSuccess;
+    }
+  }
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, kern, threads, smem);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  known[key] = *out;
+  return cudaSuccess;
+}
+
+// Clusters of cfg's shape (clusterDim.x CTAs of blockDim.x threads,
+// dynamicSmemBytes each) resident on the device at once.
+inline cudaError_t resident_clusters(int *out, const void *kern, const cudaLaunchConfig_t &cfg,
+                                     unsigned cluster) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, const void *, unsigned, size_t, unsigned>, int> known;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const auto key = std::make_tuple(dev, kern, cfg.blockDim.x, cfg.dynamicSmemBytes, cluster);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = known.find(key);
+    if (it != known.end()) {
+      *out = it->second;
+      return cudaSuccess;
+    }
+  }
+  e = cudaOccupancyMaxActiveClusters(out, kern, &cfg);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  known[key] = *out;
+  return cudaSuccess;
 }
 
 }  // namespace fr

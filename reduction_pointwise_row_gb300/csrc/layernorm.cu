@@ -1110,8 +1110,7 @@ cudaError_t launch_layernorm_cluster(const uint16_t *x, const float *gamma, cons
   LnKern kern = full ? sh->kern[ti] : layernorm_cluster;
   const size_t smem = !full ? cluster_smem(cols, C)
                             : static_cast<size_t>(sh->slots) * static_cast<size_t>(cols / C) * 2;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem));
+  e = set_smem_limit(reinterpret_cast<const void *>(kern), smem);
   if (e != cudaSuccess) return e;
   if (C > 8) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
@@ -1127,7 +1126,7 @@ cudaError_t launch_layernorm_cluster(const uint16_t *x, const float *gamma, cons
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(C));
   int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+  e = resident_clusters(&clusters, reinterpret_cast<const void *>(kern), cfg, cfg.attrs[0].val.clusterDim.x);
   if (e != cudaSuccess) return e;
   if (clusters < 1) return cudaErrorInvalidConfiguration;
   int64_t ncl = clusters;  // persistent: every cluster that can be resident
@@ -1174,11 +1173,10 @@ cudaError_t launch_layernorm_ring(const uint16_t *x, const float *gamma, const f
                      : reinterpret_cast<const void *>(&layernorm_ring<2, false>));
   int *err = nullptr;
   if (cudaError_t ee = device_error_word(&err); ee != cudaSuccess) return ee;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(kern), smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRingThreads, smem);
+  e = blocks_per_sm(&per_sm, reinterpret_cast<const void *>(kern), kRingThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   int64_t grid = static_cast<int64_t>(sm_count) * per_sm;
@@ -1257,11 +1255,10 @@ cudaError_t launch_layernorm_rows(const uint16_t *x, const float *gamma, const f
 #undef FR_LNR8
 #undef FR_LNR
   const size_t smem = static_cast<size_t>(cols) * 8;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(kern), smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRgThreads, smem);
+  e = blocks_per_sm(&per_sm, reinterpret_cast<const void *>(kern), kRgThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   const int groups = kRgThreads / 32 / WG;

@@ -316,6 +316,124 @@ softmax_cluster(const float *__restrict__ x, float *__restrict__ y, int64_t cols
   if (si >= 0) st_stream_f32(py + si, se * scale);
 }
 
+// Persistent form for rows whose x and y do not share their offset within a
+// 32-byte sector (the kernels above pair x's vectors with y's): one CTA per
+// row stages x in shared memory with 16-byte asynchronous copies at x's
+// alignment (element i at srow[i + ox], ox putting x's 16-byte chunks on
+// 16-byte boundaries), takes the max and the exponentials there (written back
+// in place, one ex2 per element), and writes y in 16-byte chunks at y's
+// alignment: each chunk is cut from two aligned float4 of shared memory by a
+// shift the whole CTA shares.  One read of x and one write of y, for rows of
+// up to kStageMaxCols elements.
+constexpr int kStageMaxCols = 32768;
+
+template <int T>
+__global__ void __launch_bounds__(T)
+softmax_cta_stage(const float *__restrict__ x, float *__restrict__ y, int64_t cols, int64_t ldx,
+                  int64_t ldy) {
+  pdl_enter();
+  constexpr int W = T / 32;
+  extern __shared__ __align__(16) float srow[];  // cols + 8 floats
+  __shared__ float red[2][W];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t row = blockIdx.x;
+  const float *px = x + row * ldx;
+  float *py = y + row * ldy;
+  const int n = static_cast<int>(cols);
+  const int hx = min(n, static_cast<int>(((16 - (reinterpret_cast<uintptr_t>(px) & 15)) & 15) >> 2));
+  const int ox = (4 - (hx & 3)) & 3;
+  const int ncx = (n - hx) >> 2;  // x's whole 16-byte chunks
+  const uint64_t policy = l2_evict_first_policy();
+  for (int c = tid; c < ncx; c += T) cp_async_16_hint(srow + ox + hx + 4 * c, px + hx + 4 * c, policy);
+  cp_async_commit();
+  const int tx0 = hx + 4 * ncx;
+  if (tid < hx) srow[ox + tid] = ld_stream_f32(px + tid);
+  if (tid < n - tx0) srow[ox + tx0 + tid] = ld_stream_f32(px + tx0 + tid);
+  cp_async_wait<0>();
+  __syncthreads();
+
+  const float4 *body = reinterpret_cast<const float4 *>(srow + ox + hx);  // x's chunks
+  float m = -INFINITY;
+  for (int c = tid; c < ncx; c += T) {
+    const float4 v = body[c];
+    m = max_nan(max_nan(m, v.x), max_nan(v.y, max_nan(v.z, v.w)));
+  }
+  if (tid < hx) m = max_nan(m, srow[ox + tid]);
+  if (tid < n - tx0) m = max_nan(m, srow[ox + tx0 + tid]);
+  m = warp_max_nan(m);
+  if (lane == 0) red[0][warp] = m;
+  __syncthreads();
+  m = warp_max_nan(lane < W ? red[0][lane] : -INFINITY);
+  const float mb = m * kLog2e;
+
+  float d = 0.0f;
+  float4 *wbody = reinterpret_cast<float4 *>(srow + ox + hx);
+  for (int c = tid; c < ncx; c += T) {
+    float4 v = wbody[c];
+    v.x = ex2(fmaf(v.x, kLog2e, -mb));
+    v.y = ex2(fmaf(v.y, kLog2e, -mb));
+    v.z = ex2(fmaf(v.z, kLog2e, -mb));
+    v.w = ex2(fmaf(v.w, kLog2e, -mb));
+    wbody[c] = v;
+    d += (v.x + v.y) + (v.z + v.w);
+  }
+  if (tid < hx) {
+    const float e = ex2(fmaf(srow[ox + tid], kLog2e, -mb));
+    srow[ox + tid] = e;
+    d += e;
+  }
+  if (tid < n - tx0) {
+    const float e = ex2(fmaf(srow[ox + tx0 + tid], kLog2e, -mb));
+    srow[ox + tx0 + tid] = e;
+    d += e;
+  }
+  d = warp_sum(d);
+  if (lane == 0) red[1][warp] = d;
+  __syncthreads();  // also: every exponential is in shared memory
+  d = warp_sum(lane < W ? red[1][lane] : 0.0f);
+  const float inv = __frcp_rn(d);
+
+  // y: hy scalars up to its 16-byte boundary, then 16-byte chunks; y's chunk
+  // c holds elements hy + 4c .. + 3, at srow[ox + hy + 4c ...], sh floats past
+  // a 16-byte boundary (sh the same for every chunk)
+  const int hy = min(n, static_cast<int>(((16 - (reinterpret_cast<uintptr_t>(py) & 15)) & 15) >> 2));
+  const int ncy = (n - hy) >> 2;
+  const int base = ox + hy, sh = base & 3;
+  const float4 *al = reinterpret_cast<const float4 *>(srow + (base - sh));
+  float *vy = py + hy;
+  auto put = [&](int c, float4 o) {
+    asm volatile("st.global.cs.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(vy + 4 * c), "f"(o.x * inv),
+                 "f"(o.y * inv), "f"(o.z * inv), "f"(o.w * inv)
+                 : "memory");
+  };
+  switch (sh) {  // uniform: one branch for the whole CTA
+    case 0:
+      for (int c = tid; c < ncy; c += T) put(c, al[c]);
+      break;
+    case 1:
+      for (int c = tid; c < ncy; c += T) {
+        const float4 a = al[c], b = al[c + 1];
+        put(c, make_float4(a.y, a.z, a.w, b.x));
+      }
+      break;
+    case 2:
+      for (int c = tid; c < ncy; c += T) {
+        const float4 a = al[c], b = al[c + 1];
+        put(c, make_float4(a.z, a.w, b.x, b.y));
+      }
+      break;
+    default:
+      for (int c = tid; c < ncy; c += T) {
+        const float4 a = al[c], b = al[c + 1];
+        put(c, make_float4(a.w, b.x, b.y, b.z));
+      }
+      break;
+  }
+  const int ty0 = hy + 4 * ncy;
+  if (tid < hy) st_stream_f32(py + tid, srow[ox + tid] * inv);
+  if (tid < n - ty0) st_stream_f32(py + ty0 + tid, srow[ox + ty0 + tid] * inv);
+}
+
 // Fold `n` values (already max-reduced to cm) into the online pair st.
 __device__ __forceinline__ MD fold_chunk(MD st, float cm) {
   const float M = max_nan(st.m, cm);
@@ -550,10 +668,10 @@ unsigned warp_row_grid(int64_t rows) {
 
 }  // namespace
 
-// Rows up to 1024 take one warp; longer rows with a shared 32-byte phase take
-// one CTA of up to 1024 threads x 4 vectors (32768 elements, 128 KiB of
-// registers).
-int64_t softmax_persistent_max_cols(bool vec) { return vec ? 32768 : 1024; }
+// Rows up to 1024 take one warp; longer rows one CTA, holding the row in
+// registers (x and y in phase: up to 1024 threads x 4 vectors, 128 KiB of
+// registers) or in shared memory (out of phase), up to 32768 elements.
+int64_t softmax_persistent_max_cols(bool) { return 32768; }
 
 namespace {
 template <int T, int NV>
@@ -576,6 +694,21 @@ cudaError_t launch_softmax_persistent(const float *x, float *y, int64_t rows, in
     if (nvec <= 512 * 4) return launch_cta<512, 4>(x, y, rows, cols, ldx, ldy, s);
     if (nvec <= 1024 * 4) return launch_cta<1024, 4>(x, y, rows, cols, ldx, ldy, s);
     return cudaErrorInvalidValue;
+  }
+  if (!vec && cols > 1024) {  // out of phase: the row staged in shared memory
+    if (rows > 0x7fffffff || cols > kStageMaxCols) return cudaErrorInvalidValue;
+    // four to twelve 16-byte chunks a thread (measured on GB300, us per call:
+    // 16384 x 1025 with 64 threads 24.3, 128 27.2; x 2048 with 128 41.1, 64
+    // 43.4; x 4097 with 256 84.1, 128 80.5, 512 117.5, and at 1216 rows 10.2
+    // with 256, 12.5 with 128; x 8192 with 256 154.0, 512 164.1)
+    const size_t smem = (static_cast<size_t>(cols) + 8) * 4;
+    const int T = cols <= 1536 ? 64 : cols <= 3072 ? 128 : cols <= 12288 ? 256 : 512;
+    auto kern = T == 64 ? softmax_cta_stage<64> : T == 128 ? softmax_cta_stage<128>
+              : T == 256 ? softmax_cta_stage<256> : softmax_cta_stage<512>;
+    cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(kern), smem);
+    if (e != cudaSuccess) return e;
+    return launch_k(kern, dim3(static_cast<unsigned>(rows)), dim3(T), smem, s, 0, x, y, cols, ldx,
+                    ldy);
   }
   if (vec) {
     const int64_t nv = (cols + 255) / 256;
@@ -616,11 +749,10 @@ cudaError_t launch_softmax_async(const float *x, float *y, int64_t rows, int64_t
   }
   const int vp = vpl <= 1 ? 1 : vpl <= 2 ? 2 : vpl <= 4 ? 4 : 8;
   const size_t smem = static_cast<size_t>(kAsyncThreads / 32) * kAsyncStages * vp * 32 * 16;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(kern), smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kAsyncThreads, smem);
+  e = blocks_per_sm(&per_sm, reinterpret_cast<const void *>(kern), kAsyncThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   int64_t grid = static_cast<int64_t>(sm_count) * per_sm;
@@ -692,7 +824,7 @@ cudaError_t launch_looped_t(const float *x, float *y, int64_t rows, int64_t cols
                             int64_t ldy, bool vec, int sm_count, int per_sm_cap, cudaStream_t s) {
   auto kern = vec ? softmax_block_looped<true, T, U, PF> : softmax_block_looped<false, T, U, PF>;
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, T, 0);
+  cudaError_t e = blocks_per_sm(&per_sm, reinterpret_cast<const void *>(kern), T, 0);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   if (per_sm > per_sm_cap) per_sm = per_sm_cap;

@@ -557,7 +557,7 @@ cudaError_t launch_bf16_looped_t(const uint16_t *x, uint16_t *y, int64_t rows, i
                                  cudaStream_t s) {
   auto kern = vec ? softmax_bf16_block_looped<true, T> : softmax_bf16_block_looped<false, T>;
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, T, 0);
+  cudaError_t e = blocks_per_sm(&per_sm, reinterpret_cast<const void *>(kern), T, 0);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   if (per_sm > per_sm_cap) per_sm = per_sm_cap;

@@ -647,11 +647,11 @@ cudaError_t warp_config_check(const XentConfig &cfg) {
   cudaError_t err = cudaFuncGetAttributes(&fa, kern);
   if (err != cudaSuccess) return err;
   if (fa.localSizeBytes > 0) return cudaErrorInvalidConfiguration;  // spills: t = inf
-  if ((err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 0)) !=
+  if ((err = set_smem_limit(reinterpret_cast<const void *>(kern), 0)) !=
       cudaSuccess)
     return err;
   int per_sm = 0;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarpCta, 0);
+  err = blocks_per_sm(&per_sm, reinterpret_cast<const void *>(kern), kWarpCta, 0);
   if (err != cudaSuccess) return err;
   return per_sm >= cfg.ctas_per_sm ? cudaSuccess : cudaErrorInvalidConfiguration;
 }
@@ -671,11 +671,10 @@ cudaError_t xent_config_check(const XentConfig &cfg, int max_smem_optin) {
   cudaError_t err = cudaFuncGetAttributes(&fa, e->kern);
   if (err != cudaSuccess) return err;
   if (fa.localSizeBytes > 0) return cudaErrorInvalidConfiguration;  // spills: t = inf
-  err = cudaFuncSetAttribute(e->kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
+  err = set_smem_limit(reinterpret_cast<const void *>(e->kern), smem);
   if (err != cudaSuccess) return err;
   int per_sm = 0;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, e->kern, e->T, smem);
+  err = blocks_per_sm(&per_sm, reinterpret_cast<const void *>(e->kern), e->T, smem);
   if (err != cudaSuccess) return err;
   return per_sm >= cfg.ctas_per_sm ? cudaSuccess : cudaErrorInvalidConfiguration;
 }
@@ -725,8 +724,7 @@ cudaError_t launch_xent_config(const XentConfig &cfg, const void *logits,
   size_t smem = 0;
   e = capped_smem(static_cast<size_t>(a->NS) * a->U * a->T * 16, cfg.ctas_per_sm, &smem);
   if (e != cudaSuccess) return e;
-  if ((e = cudaFuncSetAttribute(a->kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(smem))) != cudaSuccess)
+  if ((e = set_smem_limit(reinterpret_cast<const void *>(a->kern), smem)) != cudaSuccess)
     return e;
   int64_t grid = static_cast<int64_t>(sm_count) * cfg.ctas_per_sm;
   if (grid > rows) grid = rows;
@@ -770,9 +768,9 @@ cudaError_t launch_warp_kernel(const void *kern, int per_sm_cap, const void *log
                                int64_t ld, int64_t ignore_index, void *workspace, int sm_count,
                                cudaStream_t s) {
   int per_sm = 0;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 0);
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(kern), 0);
   if (e != cudaSuccess) return e;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarpCta, 0)) !=
+  if ((e = blocks_per_sm(&per_sm, reinterpret_cast<const void *>(kern), kWarpCta, 0)) !=
       cudaSuccess)
     return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
@@ -787,8 +785,7 @@ cudaError_t launch_warp_kernel(const void *kern, int per_sm_cap, const void *log
   // shared-memory carveout cost 3 % when it was not needed)
   size_t smem = 0;
   if (per_sm < resident && (e = capped_smem(0, per_sm, &smem)) != cudaSuccess) return e;
-  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(smem))) != cudaSuccess)
+  if ((e = set_smem_limit(reinterpret_cast<const void *>(kern), smem)) != cudaSuccess)
     return e;
   void *args[] = {&logits, &target, &loss, &target_logit, &argmax, &loss_mean, &workspace,
                   &rows, &cols, &ld, &ignore_index};

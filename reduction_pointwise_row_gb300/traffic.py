@@ -34,6 +34,8 @@ def algorithmic_bytes(op: str, rows: int, cols: int, **kw) -> int:
         return rows * cols * 4 + rows * 4
     if op == "softmax":               # x fp32 in; y fp32 out
         return 2 * rows * cols * 4
+    if op == "softmax_offset":        # fp32 softmax, x and y out of phase: same bytes
+        return 2 * rows * cols * 4
     if op == "softmax_bf16":          # x bf16 in; y bf16 out
         return 2 * rows * cols * 2
     if op == "layernorm":             # x bf16 in, y bf16 out, gamma/beta fp32, mean/rstd fp32

@@ -31,9 +31,10 @@ def o():
 def forms_for(op, cols, in_phase=True):
     if op == "relu_add_sum":
         return (["persistent"] if cols <= 1024 else []) + ["looped", "split"]
-    if op == "softmax":  # in phase, rows past 1024 stay persistent (a CTA per row) or
-        # split over a cluster of CTAs
-        return ((["persistent"] if cols <= 1024 or (cols <= 32768 and in_phase) else []) +
+    if op == "softmax":  # rows past 1024 stay persistent (a CTA per row, the row in
+        # registers in phase, in shared memory out of phase) up to 32768 columns;
+        # in phase they also split over a cluster of CTAs
+        return ((["persistent"] if cols <= 32768 else []) +
                 (["split"] if in_phase and 1024 < cols <= 262144 else []) + ["looped"])
     raise ValueError(op)
 
@@ -164,7 +165,9 @@ def run_softmax(x, form, layout=(0, 0, 0), kernel=None):
 
 @pytest.mark.parametrize("cols", COLS + [2048, 2055, 2056, 8193, 16385, 32768, 32769, 65537])
 @pytest.mark.parametrize("rows", [1, 7, 33])
-@pytest.mark.parametrize("layout", LAYOUTS, ids=["aligned", "offset_same_phase", "offset_scalar"])
+@pytest.mark.parametrize("layout", LAYOUTS + [(1, 0, 3), (2, 7, 1), (3, 1, 0)],
+                         ids=["aligned", "offset_same_phase", "offset_scalar", "out_of_phase_1",
+                              "out_of_phase_2", "out_of_phase_3"])
 def test_softmax_forms(o, rows, cols, layout):
     w = workloads.make(1, rows=rows, cols=cols, seed=2000 + rows * 7 + cols)
     ref = o.softmax(w.arrays["x"])
@@ -528,10 +531,18 @@ def test_error_statuses_on_device():
     buf = torch.zeros(4 * 2001 + 3, device="cuda")  # x and y rows out of 32-byte phase
     xs = buf[:4 * 2001].view(4, 2001)[:, :2000]
     ys = torch.empty(4 * 2000 + 3, device="cuda")[3:].view(4, 2000)
-    for form in ("persistent", "split"):
-        with pytest.raises(fr.FRError) as e:
-            fr.fr_softmax(xs, form=form, out=ys)
-        assert e.value.status == 3
+    with pytest.raises(fr.FRError) as e:  # the cluster form pairs x's vectors with y's
+        fr.fr_softmax(xs, form="split", out=ys)
+    assert e.value.status == 3
+    fr.fr_softmax(xs, form="persistent", out=ys)  # staged in shared memory
+    assert fr.fr_last_form() == "persistent"
+    torch.cuda.synchronize()
+    assert torch.allclose(ys, torch.full_like(ys, 1.0 / 2000))
+    with pytest.raises(fr.FRError) as e:  # out of phase and past 32768 columns
+        big = torch.zeros(2 * 40001, device="cuda")
+        fr.fr_softmax(big.view(2, 40001)[:, 1:], form="persistent",
+                      out=torch.empty(2, 40000, device="cuda"))
+    assert e.value.status == 3
     a = torch.zeros(2, 1 << 20, device="cuda")
     ws = torch.empty(8, dtype=torch.uint8, device="cuda")
     with pytest.raises(fr.FRError) as e:
