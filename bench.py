@@ -55,7 +55,8 @@ def parse():
                                       "looped", "looped_bf16", "softmax_bf16", "xent_f32",
                                       "softmax_bf16_4097", "softmax_bf16_4097_looped",
                                       "softmax_bf16_65537", "xent_box", "form_sweep",
-                                      "layernorm_768", "layernorm_5120", "layernorm_12288"],
+                                      "layernorm_768", "layernorm_5120", "layernorm_12288",
+                                      "softmax_4097_offset"],
                    help="time one workload alone (for profiler captures) and exit")
     p.add_argument("--form", default="auto", choices=["auto", "persistent", "looped", "split"],
                    help="with --only: force a reduction form")
@@ -418,6 +419,18 @@ def setup_workload(name, fr, workloads, dev, form="auto"):
             x = to_device(w.arrays["x"], dev)
             y = torch.empty_like(x)
             calls.append(lambda x=x, y=y: fr.fr_softmax(x, out=y, form=f))
+        return calls, "softmax", w.rows, w.cols, 1
+    if name == "softmax_4097_offset":
+        # rows of 4097 with x one element past y's 32-byte phase (8190 rows,
+        # 256 MiB): the persistent form stages each row in shared memory
+        w = make_shard(workloads, 1, rows=(1 << 25) // 4097, cols=4097)
+        n = w.rows * w.cols
+        for _ in range(nsets("softmax", w.rows, w.cols)):
+            flat = torch.empty(n + 8, device=dev)
+            flat[1:n + 1].copy_(torch.from_numpy(w.arrays["x"].reshape(-1)))
+            x = flat[1:n + 1].view(w.rows, w.cols)
+            y = torch.empty(w.rows, w.cols, device=dev)
+            calls.append(lambda x=x, y=y, flat=flat: fr.fr_softmax(x, out=y, form=form))
         return calls, "softmax", w.rows, w.cols, 1
     if name == "softmax_bf16":
         # the bf16 softmax on [65536, 1024] (the fp32 workload's 256 MiB)
