@@ -36,6 +36,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 HEADLINE = 1
+# LayerNorm hidden sizes that --only layernorm_<cols> times alone (256 MiB of x)
+LN_HIDDEN = (768, 1024, 1536, 2048, 2560, 3072, 4096, 8192, 5120, 6144, 7168, 10240, 12288, 14336, 20480, 24576)
 METRIC = "fused row-reduction achieved HBM GB/s and % of GB300 peak; rows/s per config"
 UNIT = "GB/s"
 PROFILE = os.path.join(ROOT, "profiles", "softmax_persistent_32768x1024.md")
@@ -55,8 +57,8 @@ def parse():
                                       "looped", "looped_bf16", "softmax_bf16", "xent_f32",
                                       "softmax_bf16_4097", "softmax_bf16_4097_looped",
                                       "softmax_bf16_65537", "xent_box", "form_sweep",
-                                      "layernorm_768", "layernorm_5120", "layernorm_12288",
-                                      "softmax_4097_offset"],
+                                      "softmax_4097_offset",
+                                      *[f"layernorm_{c}" for c in LN_HIDDEN]],
                    help="time one workload alone (for profiler captures) and exit")
     p.add_argument("--form", default="auto", choices=["auto", "persistent", "looped", "split"],
                    help="with --only: force a reduction form")
@@ -640,8 +642,8 @@ SWEEP_RAS_COLS = (1024, 4096, 16384, 65536, 262144, 1048576, 4194304)
 SWEEP_SM_ROWS = (16, 64, 152, 304, 608, 1216, 2432, 4864, 16384)
 SWEEP_SM_COLS = (1025, 2048, 4097, 8192, 16384, 32768, 65537, 131072, 262144)
 SWEEP_OFFSET_COLS = (1025, 2048, 4097, 8192, 16384, 32768, 65537)
-SWEEP_LN_COLS = (768, 1024, 1536, 2048, 2560, 3072, 4096, 5120, 6144, 8192, 12288, 16384, 32768,
-                 65536)
+SWEEP_LN_COLS = (768, 1024, 1536, 2048, 2560, 3072, 4096, 5120, 6144, 7168, 8192, 10240, 12288,
+                 14336, 16384, 20480, 24576, 32768, 65536)
 SWEEP_BYTES_MAX = 1 << 30  # largest input footprint of one call
 
 

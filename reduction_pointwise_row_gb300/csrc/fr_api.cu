@@ -159,16 +159,18 @@ fr_form pick_softmax_bf16(int64_t rows, int64_t cols, bool vec, int sm_count) {
   return FR_FORM_LOOPED;
 }
 
-// LayerNorm (bf16 rows of 256 MiB, back to back).  Rows of C x T x 32 columns
-// from 2048 up (2048 .. 131072 in powers of two): the looped cluster kernel,
-// gamma/beta in registers (4096: 84.5 us against 92.2 for row groups; 32768:
-// 86.4 against 134.6 for the ring); other rows whose gamma/beta fit in shared
-// memory: the persistent row-group kernel (768: 90.1 us, 1536: 83.7, 5120:
-// 100.8, 12288: 133.7, against 263.8, 198.9, 166.9 and 149.3 for the next
-// best); else the looped general cluster, ring or scalar kernel.
+// LayerNorm (bf16 rows of 256 MiB, back to back).  Rows of C x T x 32
+// columns whose CTAs have 4, 5, 7, 8 or 16 warps: the looped cluster kernel,
+// gamma/beta in registers (4096: 84.7 us, 5120: 84.5, 10240: 84.5, 32768:
+// 86.6); CTAs of 2, 3 or 6 warps (2048, 3072, 6144, 12288 columns: 86.5, 89.2,
+// 88.9, 88.9 us) lose to the persistent row-group kernel (82.7, 88.6, 86.5,
+// 85.2), which also takes the other rows whose gamma/beta fit in shared memory
+// (768: 84.0 us, 1536: 84.1, 2560: 86.8); else the looped general cluster,
+// ring or scalar kernel.
 fr_form pick_layernorm(int64_t, int64_t cols, bool vec, bool aligned16, bool rows16,
                        int max_smem_optin) {
-  if (cols >= 2048 && fr::layernorm_cluster_full_ok(cols, aligned16)) return FR_FORM_LOOPED;
+  const int t = fr::layernorm_cluster_full_threads(cols, aligned16);
+  if (t != 0 && t != 64 && t != 96 && t != 192) return FR_FORM_LOOPED;
   if (fr::layernorm_rows_ok(cols, rows16, max_smem_optin)) return FR_FORM_PERSISTENT;
   if (fr::layernorm_cluster_ok(cols, aligned16) || fr::layernorm_ring_ok(cols, vec, max_smem_optin))
     return FR_FORM_LOOPED;

@@ -96,8 +96,9 @@ bool layernorm_persistent_ok(int64_t cols, bool vec);
 // x 16 columns).
 bool layernorm_cluster_ok(int64_t cols, bool aligned);
 // The equal-count cluster kernel: cols = C x T x 32 (T a power of two in
-// 64 .. 512 threads, C in 1, 2, 4, 8 CTAs), aligned as above.
-bool layernorm_cluster_full_ok(int64_t cols, bool aligned);
+// 64 .. 512 threads, or 96, 160, 192, 224; C in 1, 2, 4, 8 CTAs), aligned as
+// above.  Returns the CTA size T it takes for a row length (0: none).
+int layernorm_cluster_full_threads(int64_t cols, bool aligned);
 cudaError_t launch_layernorm_cluster(const uint16_t *x, const float *gamma, const float *beta,
                                      uint16_t *y, float *mean, float *rstd, int64_t rows,
                                      int64_t cols, int64_t ldx, int64_t ldy, float eps,

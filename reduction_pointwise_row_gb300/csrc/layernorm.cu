@@ -60,6 +60,15 @@ __device__ __forceinline__ Welford chan_merge(Welford a, Welford b) {
   return r;
 }
 
+// Chan's merge of two sides of equal count 2 half_n: weight 1/2, correction
+// delta^2 * half_n (no reciprocal).
+__device__ __forceinline__ void merge_equal(float &mean, float &m2, float mean_b, float m2_b,
+                                            float half_n) {
+  const float delta = mean_b - mean;
+  mean = fmaf(delta, 0.5f, mean);
+  m2 = fmaf(delta * delta, half_n, m2 + m2_b);
+}
+
 __device__ __forceinline__ Welford warp_welford(Welford w) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -131,8 +140,9 @@ __device__ __forceinline__ bool first_wait(uint64_t *bar, uint32_t parity) {
 // values two-pass in registers (sum, then squared deviations), triples merged
 // with Chan's formula across the warp by shuffles and across the group's
 // warps through shared memory (one named barrier per row, slots double
-// buffered).  One read of x, one write of y; gamma/beta come from shared
-// memory for every row.
+// buffered); when every thread holds the same number of chunks, every merge
+// joins equal counts and takes no reciprocal.  One read of x, one write of y;
+// gamma/beta come from shared memory for every row.
 constexpr int kRgThreads = 256;
 
 template <int WG>
@@ -151,12 +161,23 @@ __device__ __forceinline__ Welford merge_or_keep(Welford a, Welford b) {
 // PF: the next row's chunks are loaded while the current row is worked on.
 // PL: gamma/beta in shared memory as four float4 planes (below); otherwise
 // chunk by chunk, gamma [cols] then beta [cols].
-template <int WG, int NC, bool PF, bool PL>
-__global__ void __launch_bounds__(kRgThreads)
+// EQ: every thread of a group holds the same number of chunks (the row's
+// chunks are a multiple of the group's threads), so every merge joins two
+// equal counts (weight 1/2, no reciprocal); otherwise Chan's general merge.
+// Launch bounds: three CTAs an SM (at most 80 registers a thread) where a
+// thread holds at most 8 chunks of rows, counting the prefetched one.
+// Measured on GB300 (256 MiB of x, us per call, bounds of 1 / 3 / 4 CTAs):
+// 768 columns 94.5 / 84.1 / 90.1, 1024 89.1 / 84.3 / 85.6, 2560 100.4 /
+// 87.4 / 92.6, 4096 94.4 / 86.6 / 89.8, 8192 93.1 / 88.3 / 85.5: left to
+// itself the compiler stopped at 64 registers with spills; at four CTAs it
+// spills more.
+template <int WG, int NC, bool PF, bool PL, bool EQ>
+__global__ void __launch_bounds__(kRgThreads, NC * (PF ? 2 : 1) <= 8 ? 3 : 1)
 layernorm_rows(const uint16_t *__restrict__ x, const float *__restrict__ gamma,
                const float *__restrict__ beta, uint16_t *__restrict__ y,
                float *__restrict__ mean_out, float *__restrict__ rstd_out, int64_t rows,
-               int64_t cols, int64_t ldx, int64_t ldy, float eps) {
+               int64_t cols, int64_t ldx, int64_t ldy, float eps, float inv_n,
+               float inv_nt_eq, float half_nt_eq) {
   pdl_enter();
   constexpr int kGroups = kRgThreads / 32 / WG;  // rows a CTA works on at once
   // gamma and beta of chunk j (its 8 columns) as four float4 planes:
@@ -183,6 +204,10 @@ layernorm_rows(const uint16_t *__restrict__ x, const float *__restrict__ gamma,
   int nv = 0;  // this thread's chunks of a row
 #pragma unroll
   for (int c = 0; c < NC; ++c) nv += gt + 32 * WG * c < nch;
+  // 1 / cols, and with equal counts 1 / (values a thread) and half of that
+  // count, come from the host as arguments
+  const float n_t = static_cast<float>(8 * nv);
+  const float inv_nt = EQ ? inv_nt_eq : nv > 0 ? 1.0f / n_t : 0.0f;
   const int64_t step = static_cast<int64_t>(gridDim.x) * kGroups;
   int64_t row = static_cast<int64_t>(blockIdx.x) * kGroups + group;
   uint4 nx[PF ? NC : 1];
@@ -219,8 +244,7 @@ layernorm_rows(const uint16_t *__restrict__ x, const float *__restrict__ gamma,
         s2 = add_f32x2(s2, add_f32x2(pack_f32x2(bf16_lo(v[c].z), bf16_hi(v[c].z)),
                                      pack_f32x2(bf16_lo(v[c].w), bf16_hi(v[c].w))));
       }
-    const float n_t = static_cast<float>(8 * nv);
-    const float mean_t = nv > 0 ? (f32x2_lo(s2) + f32x2_hi(s2)) / n_t : 0.0f;
+    const float mean_t = (f32x2_lo(s2) + f32x2_hi(s2)) * inv_nt;
     const uint64_t nm = pack_f32x2(-mean_t, -mean_t);
     uint64_t q2 = 0;
 #pragma unroll
@@ -233,23 +257,50 @@ layernorm_rows(const uint16_t *__restrict__ x, const float *__restrict__ gamma,
           q2 = fma_f32x2(d, d, q2);
         }
       }
-    Welford t = warp_welford(Welford{n_t, mean_t, f32x2_lo(q2) + f32x2_hi(q2)});
-    if constexpr (WG > 1) {
-      // the group's WG triples on lanes 0 .. WG - 1, merged by a fixed xor
-      // tree (the same bits in every warp of the group), then broadcast
-      if (lane == 0) part[it & 1][warp] = t;
-      group_sync<WG>(group);
-      t = lane < WG ? part[it & 1][group * WG + lane] : Welford{0.0f, 0.0f, 0.0f};
+    float mean, m2;
+    if constexpr (EQ) {
+      mean = mean_t;
+      m2 = f32x2_lo(q2) + f32x2_hi(q2);
+      float hn = half_nt_eq;
 #pragma unroll
-      for (int o = WG / 2; o > 0; o >>= 1)
-        t = merge_or_keep(t, Welford{__shfl_xor_sync(0xffffffffu, t.n, o),
-                                     __shfl_xor_sync(0xffffffffu, t.mean, o),
-                                     __shfl_xor_sync(0xffffffffu, t.m2, o)});
-      t = Welford{__shfl_sync(0xffffffffu, t.n, 0), __shfl_sync(0xffffffffu, t.mean, 0),
-                  __shfl_sync(0xffffffffu, t.m2, 0)};
+      for (int o = 16; o > 0; o >>= 1, hn *= 2.0f)
+        merge_equal(mean, m2, __shfl_xor_sync(0xffffffffu, mean, o),
+                    __shfl_xor_sync(0xffffffffu, m2, o), hn);
+      if constexpr (WG > 1) {
+        // the group's WG pairs (equal counts) on lanes 0 .. WG - 1, merged
+        // by a fixed xor tree
+        if (lane == 0) part[it & 1][warp] = Welford{0.0f, mean, m2};
+        group_sync<WG>(group);
+        const Welford u = part[it & 1][group * WG + (lane & (WG - 1))];
+        mean = u.mean;
+        m2 = u.m2;
+#pragma unroll
+        for (int o = WG / 2; o > 0; o >>= 1, hn *= 2.0f)
+          merge_equal(mean, m2, __shfl_xor_sync(0xffffffffu, mean, o),
+                      __shfl_xor_sync(0xffffffffu, m2, o), hn);
+      }
+      // lane 0's result in every lane (the xor tree's lanes may differ in
+      // the last bit)
+      mean = __shfl_sync(0xffffffffu, mean, 0);
+      m2 = __shfl_sync(0xffffffffu, m2, 0);
+    } else {
+      Welford t = warp_welford(Welford{n_t, mean_t, f32x2_lo(q2) + f32x2_hi(q2)});
+      if constexpr (WG > 1) {
+        // the group's WG triples on lanes 0 .. WG - 1, merged by a fixed xor
+        // tree (the same bits in every warp of the group)
+        if (lane == 0) part[it & 1][warp] = t;
+        group_sync<WG>(group);
+        t = lane < WG ? part[it & 1][group * WG + lane] : Welford{0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int o = WG / 2; o > 0; o >>= 1)
+          t = merge_or_keep(t, Welford{__shfl_xor_sync(0xffffffffu, t.n, o),
+                                       __shfl_xor_sync(0xffffffffu, t.mean, o),
+                                       __shfl_xor_sync(0xffffffffu, t.m2, o)});
+      }
+      mean = __shfl_sync(0xffffffffu, t.mean, 0);
+      m2 = __shfl_sync(0xffffffffu, t.m2, 0);
     }
-    const float mean = t.mean;
-    const float rstd = rsqrtf(fmaf(t.m2, __frcp_rn(t.n), eps));
+    const float rstd = rsqrtf(fmaf(m2, inv_n, eps));
     if (gt == 0) {
       if (mean_out) mean_out[row] = mean;
       if (rstd_out) rstd_out[row] = rstd;
@@ -735,13 +786,6 @@ layernorm_cluster(const uint16_t *__restrict__ x, const float *__restrict__ gamm
 __host__ __device__ constexpr int full_slots(int R, int A) { return 2 * R + A; }
 constexpr int kFullMaxCluster = 8;
 
-__device__ __forceinline__ void merge_equal(float &mean, float &m2, float mean_b, float m2_b,
-                                            float half_n) {
-  const float delta = mean_b - mean;
-  mean = fmaf(delta, 0.5f, mean);
-  m2 = fmaf(delta * delta, half_n, m2 + m2_b);
-}
-
 // Two bf16 values of a word as a pair of fp32 (low half first).
 __device__ __forceinline__ uint64_t unpack_pair(uint32_t w) {
   return pack_f32x2(bf16_lo(w), bf16_hi(w));
@@ -773,8 +817,9 @@ __device__ __forceinline__ void stats32(const V8 &a, const V8 &b, float &mean, f
   m2 = fmaxf(fmaf(-S1, S1 * (1.0f / 32.0f), S2), 0.0f);
 }
 
-// T threads per CTA (a power of two, 64 .. 512), a cluster of C CTAs
-// (1, 2, 4 or 8) per row: cols = C * T * 32.  R rows per step, A rows ahead.
+// T threads per CTA (a power of two, 64 .. 512, or 96, 160, 192, 224), a
+// cluster of C CTAs (1, 2, 4 or 8) per row: cols = C * T * 32.  R rows per
+// step, A rows ahead.
 // Launch bounds: the CTAs of up to 512 threads that one SM holds at 128
 // registers a thread (two CTAs of 256 threads: 16 warps); a register more and
 // only one CTA of 256 fits, which halves the bytes in flight (measured on
@@ -906,19 +951,40 @@ layernorm_cluster_full(const uint16_t *__restrict__ x, const float *__restrict__
       }
       if (warp == 0) {  // the CTA's W warp pairs (1024 values each) on lanes 0..W-1
         float wm[R], w2[R];
+        if constexpr ((W & (W - 1)) == 0) {  // equal counts at every level of the tree
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const float2 t = red[s & 1][r][lane & (W - 1)];
-          wm[r] = t.x;
-          w2[r] = t.y;
+          for (int r = 0; r < R; ++r) {
+            const float2 t = red[s & 1][r][lane & (W - 1)];
+            wm[r] = t.x;
+            w2[r] = t.y;
+          }
+          float hn = 512.0f;
+#pragma unroll
+          for (int o = W / 2; o > 0; o >>= 1, hn *= 2.0f)
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+              merge_equal(wm[r], w2[r], __shfl_xor_sync(0xffffffffu, wm[r], o),
+                          __shfl_xor_sync(0xffffffffu, w2[r], o), hn);
+        } else {  // W = 3, 5, 6, 7: the warps' pairs folded in warp order, in every lane
+          // (pair k joins the first k: weight 1 / (k + 1), correction
+          // delta^2 * 1024 k / (k + 1), constants of the fold)
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const float2 t = red[s & 1][r][0];
+            wm[r] = t.x;
+            w2[r] = t.y;
+          }
+#pragma unroll
+          for (int k = 1; k < W; ++k)
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              const float2 t = red[s & 1][r][k];
+              const float delta = t.x - wm[r];
+              wm[r] = fmaf(delta, 1.0f / static_cast<float>(k + 1), wm[r]);
+              w2[r] = fmaf(delta * delta, 1024.0f * static_cast<float>(k) / static_cast<float>(k + 1),
+                           w2[r] + t.y);
+            }
         }
-        float hn = 512.0f;
-#pragma unroll
-        for (int o = W / 2; o > 0; o >>= 1, hn *= 2.0f)
-#pragma unroll
-          for (int r = 0; r < R; ++r)
-            merge_equal(wm[r], w2[r], __shfl_xor_sync(0xffffffffu, wm[r], o),
-                        __shfl_xor_sync(0xffffffffu, w2[r], o), hn);
         if (lane < static_cast<int>(C)) {
           const int sl = static_cast<int>(s % kClSlots);
           st_async_f4(&slot[sl][q], &pbar[sl], static_cast<uint32_t>(lane),
@@ -1034,6 +1100,11 @@ struct FullShape {
 #define FR_LNF(R, A)                                                                       \
   {layernorm_cluster_full<64, R, A>, layernorm_cluster_full<128, R, A>,                      \
    layernorm_cluster_full<256, R, A>, layernorm_cluster_full<512, R, A>}
+// CTAs of 3, 5, 6 and 7 warps (rows of 3, 5, 6, 7, 10, 12, 14, 20, 24 or 28
+// times 1024 columns), in the default shape only.
+constexpr int kOddT[] = {96, 160, 192, 224};
+const LnKern kFullOdd[] = {layernorm_cluster_full<96, 1, 2>, layernorm_cluster_full<160, 1, 2>,
+                           layernorm_cluster_full<192, 1, 2>, layernorm_cluster_full<224, 1, 2>};
 const FullShape kFullShapes[] = {{"r1a2", full_slots(1, 2), FR_LNF(1, 2)},
                                  {"r1a1", full_slots(1, 1), FR_LNF(1, 1)},
                                  {"r1a3", full_slots(1, 3), FR_LNF(1, 3)},
@@ -1043,7 +1114,7 @@ const FullShape kFullShapes[] = {{"r1a2", full_slots(1, 2), FR_LNF(1, 2)},
 #undef FR_LNF
 
 // The equal-count kernel's shape for a row length: cols = C * T * 32 with
-// C in 1, 2, 4, 8 and T a power of two in 64 .. 512.  Measured on GB300
+// C in 1, 2, 4, 8 and T a power of two in 64 .. 512 or one of kOddT.  Measured on GB300
 // (256 MiB of bf16 rows, launches back to back): 8192 columns 84.2 us with
 // one CTA of 256 threads, 86.8 with 2 of 128; 16384 84.1 with 2 of 256,
 // 86.1 with 4 of 128, 88.3 with 1 of 512; 32768 86.3 with 4 of 256, 88.8
@@ -1055,12 +1126,13 @@ bool full_shape(int64_t cols, int *T, int *C) {
   const int tmax = v == 64 || v == 128 || v == 512 ? v : 256;
   // Clusters of up to 4 CTAs first (8 cost 5-10 %: [2048, 65536] 96.9 us
   // with 8 CTAs of 256 threads, 93.0 with 4 of 512), then CTAs of at most
-  // tmax threads, then larger ones.
+  // tmax threads (the largest such), then larger ones.
+  constexpr int kTs[] = {512, 256, 224, 192, 160, 128, 96, 64};
   for (int cmax = 4; cmax <= kFullMaxCluster; cmax <<= 1)
     for (int pass = 0; pass < 2; ++pass)
       for (int c = 1; c <= cmax; c <<= 1)
-        for (int t = pass == 0 ? tmax : 512; t >= 64; t >>= 1) {
-          if (pass == 1 && t <= tmax) break;
+        for (int t : kTs) {
+          if ((pass == 0) != (t <= tmax)) continue;
           if (cols == static_cast<int64_t>(c) * t * kClCols) {
             *T = t;
             *C = c;
@@ -1070,6 +1142,20 @@ bool full_shape(int64_t cols, int *T, int *C) {
   return false;
 }
 
+// The equal-count kernel of a shape for T threads.  The odd CTA sizes exist
+// in the default shape (r1a2) only, which a pinned shape falls back to there.
+LnKern full_kernel(const FullShape &sh, int T) {
+  switch (T) {
+    case 64: return sh.kern[0];
+    case 128: return sh.kern[1];
+    case 256: return sh.kern[2];
+    case 512: return sh.kern[3];
+  }
+  for (size_t i = 0; i < sizeof kOddT / sizeof kOddT[0]; ++i)
+    if (kOddT[i] == T) return kFullOdd[i];
+  return nullptr;
+}
+
 }  // namespace
 
 bool layernorm_cluster_ok(int64_t cols, bool aligned) {
@@ -1077,9 +1163,9 @@ bool layernorm_cluster_ok(int64_t cols, bool aligned) {
   return aligned && (cluster_size_for(cols) > 0 || full_shape(cols, &t, &c));
 }
 
-bool layernorm_cluster_full_ok(int64_t cols, bool aligned) {
+int layernorm_cluster_full_threads(int64_t cols, bool aligned) {
   int t = 0, c = 0;
-  return aligned && full_shape(cols, &t, &c);
+  return aligned && full_shape(cols, &t, &c) ? t : 0;
 }
 
 cudaError_t launch_layernorm_cluster(const uint16_t *x, const float *gamma, const float *beta,
@@ -1106,8 +1192,9 @@ cudaError_t launch_layernorm_cluster(const uint16_t *x, const float *gamma, cons
   const FullShape *sh = &kFullShapes[0];
   for (const FullShape &c : kFullShapes)
     if (pinned(c.name)) sh = &c;
-  const int ti = T == 64 ? 0 : T == 128 ? 1 : T == 256 ? 2 : 3;
-  LnKern kern = full ? sh->kern[ti] : layernorm_cluster;
+  LnKern kern = full ? full_kernel(*sh, T) : layernorm_cluster;
+  if (kern == nullptr) return cudaErrorInvalidValue;
+  if (full && (T & (T - 1)) != 0) sh = &kFullShapes[0];
   const size_t smem = !full ? cluster_smem(cols, C)
                             : static_cast<size_t>(sh->slots) * static_cast<size_t>(cols / C) * 2;
   e = set_smem_limit(reinterpret_cast<const void *>(kern), smem);
@@ -1206,6 +1293,32 @@ bool rows_shape(int64_t cols, int *WG, int *NC) {
 }
 }  // namespace
 
+using RowsKern = void (*)(const uint16_t *, const float *, const float *, uint16_t *, float *,
+                         float *, int64_t, int64_t, int64_t, int64_t, float, float, float, float);
+
+// The row-group kernel for WG warps a row and NC chunks a thread: the next
+// row prefetched into registers with 2 or 4 chunks, and with 6 or 8 when pf8
+// (8 warps a row); otherwise more rows in flight instead.
+template <int W, bool P, bool E>
+RowsKern rows_nc(int NC, bool pf8) {
+  if constexpr (W == 1)
+    if (NC == 2) return layernorm_rows<1, 2, true, P, E>;
+  if (NC == 4) return layernorm_rows<W, 4, true, P, E>;
+  if constexpr (W == 8)
+    if (pf8) return NC == 6 ? layernorm_rows<8, 6, true, P, E> : layernorm_rows<8, 8, true, P, E>;
+  return NC == 6 ? layernorm_rows<W, 6, false, P, E> : layernorm_rows<W, 8, false, P, E>;
+}
+
+template <bool P, bool E>
+RowsKern rows_kernel(int WG, int NC, bool pf8) {
+  switch (WG) {
+    case 1: return rows_nc<1, P, E>(NC, pf8);
+    case 2: return rows_nc<2, P, E>(NC, pf8);
+    case 4: return rows_nc<4, P, E>(NC, pf8);
+    default: return rows_nc<8, P, E>(NC, pf8);
+  }
+}
+
 bool layernorm_rows_ok(int64_t cols, bool aligned16, int max_smem_optin) {
   int wg = 0, nc = 0;
   return aligned16 && cols % 8 == 0 && rows_shape(cols, &wg, &nc) &&
@@ -1218,12 +1331,6 @@ cudaError_t launch_layernorm_rows(const uint16_t *x, const float *gamma, const f
                                   cudaStream_t s) {
   int WG = 0, NC = 0;
   if (!rows_shape(cols, &WG, &NC)) return cudaErrorInvalidValue;
-  using K = void (*)(const uint16_t *, const float *, const float *, uint16_t *, float *, float *,
-                     int64_t, int64_t, int64_t, int64_t, float);
-  // chunks of up to 4 a thread: the next row prefetched into registers;
-  // 6 or 8: no prefetch (registers), more rows in flight instead
-  // (more than one warp a row only when one warp would need more than the
-  // chunks allowed a thread, so never with 2)
   // gamma/beta layout, measured on GB300 (256 MiB of x, us per call, chunk
   // by chunk / planes): 768 columns 90.8 / 89.5, 1024 85.5 / 96.4, 1536
   // 84.2 / 96.0, 2560 92.4 / 85.0, 3072 88.9 / 93.7, 5120 100.9 / 88.6, 6144
@@ -1231,7 +1338,8 @@ cudaError_t launch_layernorm_rows(const uint16_t *x, const float *gamma, const f
   // shared-memory wavefronts (768: 20.6 M to 12.0 M), were slower where one
   // or two warps hold a row and every thread holds all NC chunks; the rule
   // below picks the faster layout at all eight sizes.
-  // FR_LAYERNORM_ROWS_GB=planar|chunk pins one.
+  // FR_LAYERNORM_ROWS_GB=planar|chunk pins one where every thread holds the
+  // same number of chunks; rows with unequal counts always take the planes.
   const int64_t nch = cols / 8;
   const bool full_chunks = nch % (32 * static_cast<int64_t>(WG)) == 0 &&
                            nch / (32 * static_cast<int64_t>(WG)) == NC;
@@ -1242,18 +1350,12 @@ cudaError_t launch_layernorm_rows(const uint16_t *x, const float *gamma, const f
   // most three CTAs an SM) prefetch the next row with 6 or 8 chunks a thread
   // too: fewer rows in flight otherwise.
   const bool pf8 = cols > 8192;
-#define FR_LNR(W, P)                                                                     \
-  (NC == 4 ? layernorm_rows<W, 4, true, P> : NC == 6 ? layernorm_rows<W, 6, false, P>    \
-           : layernorm_rows<W, 8, false, P>)
-#define FR_LNR8(P)                                                                       \
-  (pf8 ? (NC == 6 ? layernorm_rows<8, 6, true, P> : layernorm_rows<8, 8, true, P>)       \
-       : FR_LNR(8, P))
-  K kern = pl ? (WG == 1 ? (NC == 2 ? layernorm_rows<1, 2, true, true> : FR_LNR(1, true))
-                 : WG == 2 ? FR_LNR(2, true) : WG == 4 ? FR_LNR(4, true) : FR_LNR8(true))
-              : (WG == 1 ? (NC == 2 ? layernorm_rows<1, 2, true, false> : FR_LNR(1, false))
-                 : WG == 2 ? FR_LNR(2, false) : WG == 4 ? FR_LNR(4, false) : FR_LNR8(false));
-#undef FR_LNR8
-#undef FR_LNR
+  const bool eq = nch % (32 * static_cast<int64_t>(WG)) == 0;
+  RowsKern kern = !eq ? rows_kernel<true, false>(WG, NC, pf8)
+               : pl ? rows_kernel<true, true>(WG, NC, pf8) : rows_kernel<false, true>(WG, NC, pf8);
+  const float inv_n = 1.0f / static_cast<float>(cols);
+  const float n_t = eq ? static_cast<float>(8 * (nch / (32 * WG))) : 1.0f;  // values a thread
+  const float inv_nt = 1.0f / n_t, half_nt = 0.5f * n_t;
   const size_t smem = static_cast<size_t>(cols) * 8;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(kern), smem);
   if (e != cudaSuccess) return e;
@@ -1266,7 +1368,7 @@ cudaError_t launch_layernorm_rows(const uint16_t *x, const float *gamma, const f
   const int64_t need = (rows + groups - 1) / groups;
   if (grid > need) grid = need;
   return launch_k(kern, dim3(static_cast<unsigned>(grid)), dim3(kRgThreads), smem, s, 0, x, gamma,
-                  beta, y, mean, rstd, rows, cols, ldx, ldy, eps);
+                  beta, y, mean, rstd, rows, cols, ldx, ldy, eps, inv_n, inv_nt, half_nt);
 }
 
 bool layernorm_persistent_ok(int64_t cols, bool vec) {

@@ -377,6 +377,36 @@ def test_layernorm_equal_count_shapes(o, variant, cols):
     assert fr.fr_check_device_error() == 0
 
 
+@pytest.mark.parametrize("cta", ["256", "128", "512"])
+@pytest.mark.parametrize("cols", [3072, 5120, 6144, 7168, 10240, 12288, 14336, 20480, 24576])
+def test_layernorm_equal_count_odd_warps(o, cols, cta):
+    """The equal-count cluster kernel with CTAs of 3, 5, 6 or 7 warps (the
+    CTA-level merge carries counts through a tree over the next power of two):
+    every row length a multiple of 1024 that such CTAs tile, with the CTA-size
+    cap moving some of them to other (C, T) pairs (12288: 2 x 192 by default,
+    4 x 96 under a cap of 128)."""
+    import os
+    for rows in (1, 5, 77, 301):
+        w = workloads.make(2, rows=rows, cols=cols, seed=3800 + rows + cols)
+        x = w.arrays["x"].copy()
+        if rows >= 5:
+            x[2, :] = 0x3F80  # 1.0: var 0
+            x[4, :] = 0x4780  # 65536: large mean, var 0
+        eps = float(np.float32(w.params["eps"]))
+        ry, rm, rr = o.layernorm(x, w.arrays["gamma"], w.arrays["beta"], eps)
+        os.environ["FR_LAYERNORM_CTA"] = cta
+        try:
+            y, m, r = run_layernorm(x, w.arrays["gamma"], w.arrays["beta"], eps, "looped",
+                                    kernel="cluster")
+        finally:
+            os.environ.pop("FR_LAYERNORM_CTA", None)
+        what = f"cap {cta} {rows}x{cols}"
+        assert_close(y, ry, "bf16", f"{what} y")
+        assert_close(m, rm, "mean", f"{what} mean")
+        assert_close(r, rr, "f32", f"{what} rstd")
+    assert fr.fr_check_device_error() == 0
+
+
 def test_layernorm_constant_rows(o):
     cols = 4096
     x = np.full((4, cols), 0x4060, np.uint16)  # 3.5 in bf16
