@@ -62,7 +62,8 @@ def parse():
                    help="time one workload alone (for profiler captures) and exit")
     p.add_argument("--form", default="auto", choices=["auto", "persistent", "looped", "split"],
                    help="with --only: force a reduction form")
-    p.add_argument("--sweep-ops", default="relu_add_sum,softmax,softmax_bf16,softmax_offset,layernorm",
+    p.add_argument("--sweep-ops", default="relu_add_sum,softmax,softmax_bf16,softmax_offset,"
+                   "softmax_bf16_offset,layernorm",
                    help="with --only form_sweep: the ops to sweep")
     p.add_argument("--sweep-md", metavar="JSONL",
                    help="print the form table (markdown) of a form_sweep output and exit")
@@ -726,23 +727,27 @@ def form_sweep(fr, dev, timed, args, peak, rank):
                     return [lambda x=x, y=y: fr.fr_softmax(x, out=y, form=f) for x, y in zip(Xs, Ys)]
                 measure(mk, forms3, op, rows, cols)
                 del Xs, Ys
-    # fp32 softmax with x one element past y's phase (every row out of
-    # 32-byte phase: no vector pairing of x and y)
-    for rows in SWEEP_SM_ROWS:
-        for cols in SWEEP_OFFSET_COLS:
-            if ("softmax_offset" not in ops or rows * cols * 8 > SWEEP_BYTES_MAX or
-                    rows * cols * 4 < (1 << 20)):
-                continue
-            nset = max(2, -(-ROTATE_BYTES // (8 * rows * cols)))
-            flat = torch.empty(nset * rows * cols + 8, device=dev).uniform_(-1.0, 1.0)
-            Xs = [flat[1 + k * rows * cols:1 + (k + 1) * rows * cols].view(rows, cols)
-                  for k in range(nset)]
-            Ys = rotating(rows, cols, torch.float32, 8 * rows * cols, fill=False)
+    # softmax with x one element past y's phase (every row out of 32-byte
+    # phase: no vector pairing of x and y), fp32 and bf16
+    for dtype, op in ((torch.float32, "softmax_offset"), (torch.bfloat16, "softmax_bf16_offset")):
+        es = 4 if dtype == torch.float32 else 2
+        for rows in SWEEP_SM_ROWS:
+            for cols in SWEEP_OFFSET_COLS:
+                if (op not in ops or rows * cols * es * 2 > SWEEP_BYTES_MAX or
+                        rows * cols * es < (1 << 20)):
+                    continue
+                nset = max(2, -(-ROTATE_BYTES // (2 * es * rows * cols)))
+                flat = torch.empty(nset * rows * cols + 16, device=dev,
+                                   dtype=dtype).uniform_(-1.0, 1.0)
+                Xs = [flat[1 + k * rows * cols:1 + (k + 1) * rows * cols].view(rows, cols)
+                      for k in range(nset)]
+                Ys = rotating(rows, cols, dtype, 2 * es * rows * cols, fill=False)
 
-            def mk(f, Xs=Xs, Ys=Ys):
-                return [lambda x=x, y=y: fr.fr_softmax(x, out=y, form=f) for x, y in zip(Xs, Ys)]
-            measure(mk, forms3, "softmax_offset", rows, cols)
-            del Xs, Ys, flat
+                def mk(f, Xs=Xs, Ys=Ys):
+                    return [lambda x=x, y=y: fr.fr_softmax(x, out=y, form=f)
+                            for x, y in zip(Xs, Ys)]
+                measure(mk, forms3, op, rows, cols)
+                del Xs, Ys, flat
     # LayerNorm: its kernels (the looped form's cluster, ring and scalar
     # kernels, and the persistent form), 256 MiB of x per call
     for cols in SWEEP_LN_COLS if "layernorm" in ops else ():
@@ -1026,7 +1031,7 @@ def run_reference(args):
 
 
 SWEEP_DTYPE = {"relu_add_sum": "f32", "softmax": "f32", "softmax_bf16": "bf16",
-               "softmax_offset": "f32", "layernorm": "bf16"}
+               "softmax_offset": "f32", "softmax_bf16_offset": "bf16", "layernorm": "bf16"}
 
 
 def sweep_markdown(path: str) -> str:

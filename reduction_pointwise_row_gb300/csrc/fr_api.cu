@@ -142,7 +142,10 @@ fr_form pick_softmax(int64_t rows, int64_t cols, bool vec, int sm_count) {
   return FR_FORM_LOOPED;
 }
 
-// bf16 softmax, rows in phase.  Up to 2048 columns a warp per row, up to 8192
+// bf16 softmax.  Rows out of phase: up to 32768 columns a CTA per row, the row
+// staged in shared memory (16384 x 4097: 48.3 us, looped 87.8; 4864 x 32768:
+// 95.1 against 183.5), looped beyond.
+// Rows in phase: up to 2048 columns a warp per row, up to 8192
 // a CTA per row; at 16384 the looped form once there are 4 x SMs rows (608:
 // looped 9.4 us, CTA per row 10.5; 4864: 52.0 against 60.3), a CTA per row
 // below; at 32768 a CTA per row while the rows are no more than the SMs (152:
@@ -150,7 +153,7 @@ fr_form pick_softmax(int64_t rows, int64_t cols, bool vec, int sm_count) {
 // cluster per row (2432 x 32768: 50.2 us, looped 55.3, CTA per row 73.9).
 fr_form pick_softmax_bf16(int64_t rows, int64_t cols, bool vec, int sm_count) {
   if (cols <= 2048) return FR_FORM_PERSISTENT;
-  if (!vec) return FR_FORM_LOOPED;
+  if (!vec) return cols <= 32768 ? FR_FORM_PERSISTENT : FR_FORM_LOOPED;
   if (cols <= 8192) return FR_FORM_PERSISTENT;
   if (cols <= 16384) return rows >= 4 * static_cast<int64_t>(sm_count) ? FR_FORM_LOOPED
                                                                        : FR_FORM_PERSISTENT;
@@ -330,7 +333,8 @@ fr_status fr_softmax(const void *x, void *y, int64_t rows, int64_t cols, int64_t
     switch (f) {
       case FR_FORM_PERSISTENT:
         if (cols > max_p) return FR_ERR_UNSUPPORTED_FORM;
-        return launched(fr::launch_softmax_bf16_persistent(bx, by, rows, cols, ldx, ldy, vec, s), f);
+        return launched(fr::launch_softmax_bf16_persistent(bx, by, rows, cols, ldx, ldy, vec,
+                                                                   info.sm_count, s), f);
       case FR_FORM_LOOPED:
         return launched(fr::launch_softmax_bf16_looped(bx, by, rows, cols, ldx, ldy, vec,
                                                        info.sm_count, s), f);

@@ -70,7 +70,9 @@ int64_t softmax_split_max_cols();
 cudaError_t launch_softmax_split(const float *x, float *y, int64_t rows, int64_t cols,
                                  int64_t ldx, int64_t ldy, cudaStream_t s);
 
-// bf16 rows (x and y bf16, fp32 arithmetic): persistent up to 2048 columns.
+// bf16 rows (x and y bf16, fp32 arithmetic): persistent up to 32768 columns
+// (a warp per row up to 2048; then a CTA per row, in phase the row in
+// registers, out of phase staged in shared memory).
 int64_t softmax_bf16_persistent_max_cols(bool vec);
 // Split form of the bf16 softmax: a thread-block cluster per row (rows in
 // phase, 2049 .. softmax_bf16_split_max_cols() columns).
@@ -79,7 +81,7 @@ cudaError_t launch_softmax_bf16_split(const uint16_t *x, uint16_t *y, int64_t ro
                                       int64_t ldx, int64_t ldy, cudaStream_t s);
 cudaError_t launch_softmax_bf16_persistent(const uint16_t *x, uint16_t *y, int64_t rows,
                                            int64_t cols, int64_t ldx, int64_t ldy, bool vec,
-                                           cudaStream_t s);
+                                           int sm_count, cudaStream_t s);
 cudaError_t launch_softmax_bf16_looped(const uint16_t *x, uint16_t *y, int64_t rows,
                                        int64_t cols, int64_t ldx, int64_t ldy, bool vec,
                                        int sm_count, cudaStream_t s);

@@ -434,6 +434,136 @@ softmax_cta_stage(const float *__restrict__ x, float *__restrict__ y, int64_t co
   if (tid < n - ty0) st_stream_f32(py + ty0 + tid, srow[ox + ty0 + tid] * inv);
 }
 
+// Persistent form for rows out of phase, held in registers: one CTA of T
+// threads (a multiple of 32, blockDim) per row, NV 16-byte chunks of x a
+// thread, loaded at x's alignment (chunk c = tid + T k, the row's first and
+// last chunks element by element).  With x's chunk 0 starting ox elements
+// before the row and y's oy before it (ox >= oy, one chunk before the row
+// added when x's offset is the smaller), y's chunk c holds the last 4 - s
+// values of x's chunk c and the first s of chunk c + 1, s = ox - oy the same
+// for the whole row: a thread gets them from the next lane with s shuffles,
+// and the last lane of a warp from the chunks lane 0 of the next warp left in
+// shared memory before the second barrier.  One read of x and one write of y,
+// nothing staged.
+template <int S, int NV>
+__device__ __forceinline__ void write_shifted(float4 (&v)[NV], const float4 (*first)[NV],
+                                              float *py, float *ya, int n, int oy, int ny,
+                                              float inv, int tid, int T) {
+  const int lane = tid & 31, warp = tid >> 5, nw = T >> 5;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    float4 nb = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if constexpr (S > 0) {
+      nb.x = __shfl_down_sync(0xffffffffu, v[k].x, 1);
+      if constexpr (S > 1) nb.y = __shfl_down_sync(0xffffffffu, v[k].y, 1);
+      if constexpr (S > 2) nb.z = __shfl_down_sync(0xffffffffu, v[k].z, 1);
+      if (lane == 31) {
+        if (warp + 1 < nw) nb = first[warp + 1][k];
+        else if (k + 1 < NV) nb = first[0][k + 1];
+      }
+    }
+    const float4 a = v[k];
+    float4 o = S == 0 ? a
+             : S == 1 ? make_float4(a.y, a.z, a.w, nb.x)
+             : S == 2 ? make_float4(a.z, a.w, nb.x, nb.y)
+                      : make_float4(a.w, nb.x, nb.y, nb.z);
+    o.x *= inv;
+    o.y *= inv;
+    o.z *= inv;
+    o.w *= inv;
+    const int c = tid + T * k;
+    if (c < ny) {
+      const int e0 = 4 * c - oy;
+      if (e0 >= 0 && e0 + 4 <= n) {
+        st_stream_u4(ya + 4 * c, make_uint4(__float_as_uint(o.x), __float_as_uint(o.y),
+                                            __float_as_uint(o.z), __float_as_uint(o.w)));
+      } else {
+        const float ov[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (e0 + j >= 0 && e0 + j < n) st_stream_f32(py + e0 + j, ov[j]);
+      }
+    }
+  }
+}
+
+constexpr int kShiftMaxThreads = 512;
+constexpr int kShiftChunks = 8;
+
+template <int NV>
+__global__ void __launch_bounds__(kShiftMaxThreads)
+softmax_cta_shift(const float *__restrict__ x, float *__restrict__ y, int64_t cols, int64_t ldx,
+                  int64_t ldy) {
+  pdl_enter();
+  constexpr int kMaxW = kShiftMaxThreads / 32;
+  __shared__ float red[2][kMaxW];
+  __shared__ float4 first[kMaxW][NV];  // lane 0's chunks (exponentials) per warp
+  const int T = blockDim.x, nw = T >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t row = blockIdx.x;
+  const float *px = x + row * ldx;
+  float *py = y + row * ldy;
+  const int n = static_cast<int>(cols);
+  const int ox0 = static_cast<int>((reinterpret_cast<uintptr_t>(px) & 15) >> 2);
+  const int oy = static_cast<int>((reinterpret_cast<uintptr_t>(py) & 15) >> 2);
+  const int ox = ox0 < oy ? ox0 + 4 : ox0;
+  const int nx = (n + ox + 3) >> 2, ny = (n + oy + 3) >> 2;
+  const float *xa = px - ox;  // x's chunk c at xa + 4c, 16-byte aligned
+  float *ya = py - oy;
+  const uint64_t policy = l2_evict_first_policy();
+  float4 v[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int c = tid + T * k;
+    const int e0 = 4 * c - ox;
+    v[k] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    if (c < nx) {
+      if (e0 >= 0 && e0 + 4 <= n) {
+        const uint4 u = ld_stream_u4(xa + 4 * c, policy);
+        v[k] = make_float4(fbits(u.x), fbits(u.y), fbits(u.z), fbits(u.w));
+      } else {
+        float t[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          t[j] = e0 + j >= 0 && e0 + j < n ? ld_stream_f32(px + e0 + j) : -INFINITY;
+        v[k] = make_float4(t[0], t[1], t[2], t[3]);
+      }
+    }
+  }
+  float m = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+    m = max_nan(m, max_nan(max_nan(v[k].x, v[k].y), max_nan(v[k].z, v[k].w)));
+  m = warp_max_nan(m);
+  if (lane == 0) red[0][warp] = m;
+  __syncthreads();
+  m = warp_max_nan(lane < nw ? red[0][lane] : -INFINITY);
+  const float mb = m * kLog2e;
+  float d = 0.0f;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {  // masked slots: ex2(-inf) = 0
+    v[k].x = ex2(fmaf(v[k].x, kLog2e, -mb));
+    v[k].y = ex2(fmaf(v[k].y, kLog2e, -mb));
+    v[k].z = ex2(fmaf(v[k].z, kLog2e, -mb));
+    v[k].w = ex2(fmaf(v[k].w, kLog2e, -mb));
+    d += (v[k].x + v[k].y) + (v[k].z + v[k].w);
+  }
+  if (lane == 0)
+#pragma unroll
+    for (int k = 0; k < NV; ++k) first[warp][k] = v[k];
+  d = warp_sum(d);
+  if (lane == 0) red[1][warp] = d;
+  __syncthreads();  // also: every warp's first chunks are in shared memory
+  d = warp_sum(lane < nw ? red[1][lane] : 0.0f);
+  const float inv = __frcp_rn(d);
+  switch (ox - oy) {  // uniform: one branch for the whole CTA
+    case 0: write_shifted<0, NV>(v, first, py, ya, n, oy, ny, inv, tid, T); break;
+    case 1: write_shifted<1, NV>(v, first, py, ya, n, oy, ny, inv, tid, T); break;
+    case 2: write_shifted<2, NV>(v, first, py, ya, n, oy, ny, inv, tid, T); break;
+    default: write_shifted<3, NV>(v, first, py, ya, n, oy, ny, inv, tid, T); break;
+  }
+}
+
 // Fold `n` values (already max-reduced to cm) into the online pair st.
 __device__ __forceinline__ MD fold_chunk(MD st, float cm) {
   const float M = max_nan(st.m, cm);
@@ -695,8 +825,26 @@ cudaError_t launch_softmax_persistent(const float *x, float *y, int64_t rows, in
     if (nvec <= 1024 * 4) return launch_cta<1024, 4>(x, y, rows, cols, ldx, ldy, s);
     return cudaErrorInvalidValue;
   }
-  if (!vec && cols > 1024) {  // out of phase: the row staged in shared memory
+  if (!vec && cols > 1024) {  // out of phase
     if (rows > 0x7fffffff || cols > kStageMaxCols) return cudaErrorInvalidValue;
+    // Rows of up to 4608 columns: the row in registers, shifted by shuffles
+    // (8 chunks a thread, the fewest warps that hold the row at any offset);
+    // longer rows staged in shared memory.  Measured on GB300 (fp32, x one
+    // element past y's phase, us per call, registers / staged): 16384 x 1536
+    // 31.6 / 33.4, x 3072 59.4 / 60.0, x 4097 78.7 / 83.9, x 5120 96.7 /
+    // 96.9, x 8192 157.7 / 153.6; 4864 x 16384 109.1 / 94.7.
+    // FR_SOFTMAX_OOP=shift|stage pins one (shift: up to 16374 columns).
+    const char *oop = getenv("FR_SOFTMAX_OOP");
+    const bool pin_shift = oop != nullptr && strcmp(oop, "shift") == 0;
+    const bool pin_stage = oop != nullptr && strcmp(oop, "stage") == 0;
+    const int64_t nx = (cols + 7 + 3) / 4;  // chunks at the largest offset
+    if (!pin_stage && (cols <= 4608 || pin_shift) && nx <= kShiftMaxThreads * kShiftChunks) {
+      int64_t t = (nx + 32 * kShiftChunks - 1) / (32 * kShiftChunks) * 32;
+      if (t < 64) t = 64;
+      return launch_k(softmax_cta_shift<kShiftChunks>, dim3(static_cast<unsigned>(rows)),
+                      dim3(static_cast<unsigned>(t)), 0, s, 0, x, y, cols, ldx, ldy);
+    }
+    // else the row staged in shared memory
     // four to twelve 16-byte chunks a thread (measured on GB300, us per call:
     // 16384 x 1025 with 64 threads 24.3, 128 27.2; x 2048 with 128 41.1, 64
     // 43.4; x 4097 with 256 84.1, 128 80.5, 512 117.5, and at 1216 rows 10.2

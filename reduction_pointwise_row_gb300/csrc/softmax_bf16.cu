@@ -7,7 +7,8 @@
 //             to 2048 elements per warp, 32-byte vectors of 16 bf16 per lane),
 //             the max and the sum in two passes over registers: one read and
 //             one write of each element; rows of 2049 .. 32768 in phase take
-//             one CTA per row the same way, with CTA reductions.
+//             one CTA per row the same way, with CTA reductions; rows out of
+//             phase one CTA per row with the row staged in shared memory.
 // looped      one CTA per row (grid-stride over rows) for longer rows: per-
 //             thread online pairs (m, d) folded chunk by chunk with the merge
 //             of section 9.5, combined across the CTA in any order
@@ -171,6 +172,133 @@ softmax_bf16_cta_vec(const uint16_t *__restrict__ x, uint16_t *__restrict__ y, i
     }
   }
   if (si >= 0) st_stream_u16(py + si, to_bf16(se * inv));
+}
+
+// The 8 halves from half S of the 16 halves a[0..3], b[0..3].
+template <int S>
+__device__ __forceinline__ uint4 cut_halves(const uint32_t (&a)[4], const uint32_t (&b)[4]) {
+  uint32_t c[8] = {a[0], a[1], a[2], a[3], b[0], b[1], b[2], b[3]};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    o[i] = (S & 1) ? __byte_perm(c[i + S / 2], c[i + S / 2 + 1], 0x5432) : c[i + S / 2];
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// y's value of a word of two raw x elements, packed to bf16
+__device__ __forceinline__ uint32_t softmax_word(uint32_t w, float mb, float inv) {
+  return pack_bf16x2(ex2(fmaf(bf16_lo(w), kLog2e, -mb)) * inv,
+                     ex2(fmaf(bf16_hi(w), kLog2e, -mb)) * inv);
+}
+
+// The persistent form's other kernel for rows out of phase: one CTA of T
+// threads per row stages x (raw bf16) in shared memory with 16-byte
+// asynchronous copies at x's alignment (element i at srow[i + ox], ox putting
+// x's 16-byte chunks on 16-byte boundaries); the max comes from packed pairs,
+// the sum from one exponential per element, and y's 16-byte chunks are cut
+// from two aligned chunks of shared memory by a shift the whole CTA shares,
+// their exponentials taken again there (two per element in all: 2 bytes of
+// shared memory a column instead of 4 of registers, so more rows in flight
+// per SM).  One read of x and one write of y, up to kBfStageMaxCols columns.
+constexpr int kBfStageMaxCols = 32768;
+
+template <int S>
+__device__ __forceinline__ void bf16_stage_put(const uint4 *al, uint16_t *vy, int ncy, float mb,
+                                               float inv, int tid, int T) {
+  for (int c = tid; c < ncy; c += T) {
+    const uint4 ra = al[c];
+    uint4 r = ra;
+    if constexpr (S > 0) {
+      const uint4 rb = al[c + 1];
+      const uint32_t a[4] = {ra.x, ra.y, ra.z, ra.w}, b[4] = {rb.x, rb.y, rb.z, rb.w};
+      r = cut_halves<S>(a, b);
+    }
+    st_stream_u4(vy + 8 * c, make_uint4(softmax_word(r.x, mb, inv), softmax_word(r.y, mb, inv),
+                                        softmax_word(r.z, mb, inv), softmax_word(r.w, mb, inv)));
+  }
+}
+
+template <int T>
+__global__ void __launch_bounds__(T)
+softmax_bf16_cta_stage(const uint16_t *__restrict__ x, uint16_t *__restrict__ y, int64_t cols,
+                       int64_t ldx, int64_t ldy) {
+  pdl_enter();
+  constexpr int W = T / 32;
+  extern __shared__ __align__(16) uint16_t srow16[];  // cols + 16 elements
+  __shared__ float red[2][W];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t row = blockIdx.x;
+  const uint16_t *px = x + row * ldx;
+  uint16_t *py = y + row * ldy;
+  const int n = static_cast<int>(cols);
+  const int hx = min(n, static_cast<int>(((16 - (reinterpret_cast<uintptr_t>(px) & 15)) & 15) >> 1));
+  const int ox = (8 - (hx & 7)) & 7;
+  const int ncx = (n - hx) >> 3;  // x's whole 16-byte chunks
+  const uint64_t policy = l2_evict_first_policy();
+  for (int c = tid; c < ncx; c += T)
+    cp_async_16_hint(srow16 + ox + hx + 8 * c, px + hx + 8 * c, policy);
+  cp_async_commit();
+  const int tx0 = hx + 8 * ncx;
+  if (tid < hx) srow16[ox + tid] = ld_stream_u16(px + tid);
+  if (tid < n - tx0) srow16[ox + tx0 + tid] = ld_stream_u16(px + tx0 + tid);
+  cp_async_wait<0>();
+  __syncthreads();
+
+  const uint4 *body = reinterpret_cast<const uint4 *>(srow16 + ox + hx);  // x's chunks
+  uint32_t mw = kNegInfBf16x2;
+  for (int c = tid; c < ncx; c += T) {
+    const uint4 v = body[c];
+    mw = max_nan_bf16x2(max_nan_bf16x2(mw, max_nan_bf16x2(v.x, v.y)), max_nan_bf16x2(v.z, v.w));
+  }
+  float m = max_nan(bf16_lo(mw), bf16_hi(mw));
+  if (tid < hx) m = max_nan(m, bf16_to_f32(srow16[ox + tid]));
+  if (tid < n - tx0) m = max_nan(m, bf16_to_f32(srow16[ox + tx0 + tid]));
+  m = warp_max_nan(m);
+  if (lane == 0) red[0][warp] = m;
+  __syncthreads();
+  m = warp_max_nan(lane < W ? red[0][lane] : -INFINITY);
+  const float mb = m * kLog2e;
+
+  float d = 0.0f;
+  for (int c = tid; c < ncx; c += T) {
+    const uint4 v = body[c];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      d += ex2(fmaf(bf16_lo(w[j]), kLog2e, -mb)) + ex2(fmaf(bf16_hi(w[j]), kLog2e, -mb));
+  }
+  if (tid < hx) d += ex2(fmaf(bf16_to_f32(srow16[ox + tid]), kLog2e, -mb));
+  if (tid < n - tx0) d += ex2(fmaf(bf16_to_f32(srow16[ox + tx0 + tid]), kLog2e, -mb));
+  d = warp_sum(d);
+  if (lane == 0) red[1][warp] = d;
+  __syncthreads();
+  d = warp_sum(lane < W ? red[1][lane] : 0.0f);
+  const float inv = __frcp_rn(d);
+
+  // y: hy scalars up to its 16-byte boundary, then 16-byte chunks; y's chunk
+  // c holds elements hy + 8c .. + 7, at srow16[ox + hy + 8c ...], sh elements
+  // past a 16-byte boundary (the same for every chunk)
+  const int hy = min(n, static_cast<int>(((16 - (reinterpret_cast<uintptr_t>(py) & 15)) & 15) >> 1));
+  const int ncy = (n - hy) >> 3;
+  const int base = ox + hy, sh = base & 7;
+  const uint4 *al = reinterpret_cast<const uint4 *>(srow16 + (base - sh));
+  uint16_t *vy = py + hy;
+  switch (sh) {  // uniform: one branch for the whole CTA
+    case 0: bf16_stage_put<0>(al, vy, ncy, mb, inv, tid, T); break;
+    case 1: bf16_stage_put<1>(al, vy, ncy, mb, inv, tid, T); break;
+    case 2: bf16_stage_put<2>(al, vy, ncy, mb, inv, tid, T); break;
+    case 3: bf16_stage_put<3>(al, vy, ncy, mb, inv, tid, T); break;
+    case 4: bf16_stage_put<4>(al, vy, ncy, mb, inv, tid, T); break;
+    case 5: bf16_stage_put<5>(al, vy, ncy, mb, inv, tid, T); break;
+    case 6: bf16_stage_put<6>(al, vy, ncy, mb, inv, tid, T); break;
+    default: bf16_stage_put<7>(al, vy, ncy, mb, inv, tid, T); break;
+  }
+  const int ty0 = hy + 8 * ncy;
+  auto scalar_y = [&](int i) {
+    st_stream_u16(py + i, to_bf16(ex2(fmaf(bf16_to_f32(srow16[ox + i]), kLog2e, -mb)) * inv));
+  };
+  if (tid < hy) scalar_y(tid);
+  if (tid < n - ty0) scalar_y(ty0 + tid);
 }
 
 // Split form for long rows in phase: a thread-block cluster of C CTAs per
@@ -456,7 +584,7 @@ unsigned warp_row_grid(int64_t rows) {
 
 // Rows up to 2048 take one warp; longer rows in phase take one CTA of up to
 // 1024 threads x 2 vectors (32768 elements).
-int64_t softmax_bf16_persistent_max_cols(bool vec) { return vec ? 32768 : 2048; }
+int64_t softmax_bf16_persistent_max_cols(bool) { return 32768; }
 
 namespace {
 template <int T, int NV>
@@ -520,7 +648,7 @@ cudaError_t launch_softmax_bf16_split(const uint16_t *x, uint16_t *y, int64_t ro
 
 cudaError_t launch_softmax_bf16_persistent(const uint16_t *x, uint16_t *y, int64_t rows,
                                            int64_t cols, int64_t ldx, int64_t ldy, bool vec,
-                                           cudaStream_t s) {
+                                           int sm_count, cudaStream_t s) {
   const unsigned grid = warp_row_grid(rows);
   if (vec && cols > 2048) {
     if (rows > 0x7fffffff) return cudaErrorInvalidValue;
@@ -530,6 +658,26 @@ cudaError_t launch_softmax_bf16_persistent(const uint16_t *x, uint16_t *y, int64
     if (nvec <= 512 * 2) return launch_bf16_cta<512, 2>(x, y, rows, cols, ldx, ldy, s);
     if (nvec <= 1024 * 2) return launch_bf16_cta<1024, 2>(x, y, rows, cols, ldx, ldy, s);
     return cudaErrorInvalidValue;
+  }
+  // Out of phase: rows of 2049 .. 32768 columns staged in shared memory, and
+  // of 1025 .. 2048 too from 32 x SMs rows, a warp per row below (measured
+  // on GB300, us per call, warp / staged: 4864 x 1025 12.7 / 8.2, 16384 x
+  // 1536 35.3 / 22.1, 32768 x 2048 68.8 / 54.6; 1216 x 1025 7.3 / 8.2).
+  // FR_SOFTMAX_OOP=stage|warp pins the choice for 1025 .. 2048 columns.
+  const char *oop = getenv("FR_SOFTMAX_OOP");
+  const bool stage_short = oop != nullptr ? strcmp(oop, "stage") == 0
+                                          : rows >= 32 * static_cast<int64_t>(sm_count);
+  if (!vec && (cols > 2048 || (stage_short && cols > 1024))) {  // staged
+    if (rows > 0x7fffffff || cols > kBfStageMaxCols) return cudaErrorInvalidValue;
+    // four to eight 16-byte chunks a thread
+    const size_t smem = (static_cast<size_t>(cols) + 16) * 2;
+    const int T = cols <= 4096 ? 64 : cols <= 8192 ? 128 : cols <= 16384 ? 256 : 512;
+    auto kern = T == 64 ? softmax_bf16_cta_stage<64> : T == 128 ? softmax_bf16_cta_stage<128>
+              : T == 256 ? softmax_bf16_cta_stage<256> : softmax_bf16_cta_stage<512>;
+    cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(kern), smem);
+    if (e != cudaSuccess) return e;
+    return launch_k(kern, dim3(static_cast<unsigned>(rows)), dim3(T), smem, s, 0, x, y, cols, ldx,
+                    ldy);
   }
   if (vec) {
     const int64_t nv = (cols + 32 * kPer - 1) / (32 * kPer);

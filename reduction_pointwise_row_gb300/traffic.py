@@ -38,6 +38,8 @@ def algorithmic_bytes(op: str, rows: int, cols: int, **kw) -> int:
         return 2 * rows * cols * 4
     if op == "softmax_bf16":          # x bf16 in; y bf16 out
         return 2 * rows * cols * 2
+    if op == "softmax_bf16_offset":   # bf16 softmax, x and y out of phase: same bytes
+        return 2 * rows * cols * 2
     if op == "layernorm":             # x bf16 in, y bf16 out, gamma/beta fp32, mean/rstd fp32
         return 2 * rows * cols * 2 + 2 * cols * 4 + 2 * rows * 4
     if op == "xent":                  # logits bf16, targets int64, loss fp32 [rows], mean fp32

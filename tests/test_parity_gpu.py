@@ -163,11 +163,14 @@ def run_softmax(x, form, layout=(0, 0, 0), kernel=None):
     return py.t.cpu().numpy()
 
 
-@pytest.mark.parametrize("cols", COLS + [2048, 2055, 2056, 8193, 16385, 32768, 32769, 65537])
+# out of phase the persistent form holds rows of up to 4608 columns in
+# registers and stages longer ones (up to 32768) in shared memory
+@pytest.mark.parametrize("cols", COLS + [2048, 2055, 2056, 4608, 4609, 8193, 16385, 32768, 32769,
+                                         65537])
 @pytest.mark.parametrize("rows", [1, 7, 33])
-@pytest.mark.parametrize("layout", LAYOUTS + [(1, 0, 3), (2, 7, 1), (3, 1, 0)],
+@pytest.mark.parametrize("layout", LAYOUTS + [(1, 0, 3), (2, 7, 1), (3, 1, 0), (4, 0, 1)],
                          ids=["aligned", "offset_same_phase", "offset_scalar", "out_of_phase_1",
-                              "out_of_phase_2", "out_of_phase_3"])
+                              "out_of_phase_2", "out_of_phase_3", "out_of_phase_16B"])
 def test_softmax_forms(o, rows, cols, layout):
     w = workloads.make(1, rows=rows, cols=cols, seed=2000 + rows * 7 + cols)
     ref = o.softmax(w.arrays["x"])
@@ -176,6 +179,24 @@ def test_softmax_forms(o, rows, cols, layout):
         for kernel in (("async", "plain") if form == "persistent" else (None,)):
             assert_close(run_softmax(w.arrays["x"], form, layout, kernel), ref, "f32",
                          f"{form}/{kernel} {rows}x{cols} {layout}")
+
+
+@pytest.mark.parametrize("kernel,cols", [("stage", 1025), ("stage", 2055), ("stage", 4097),
+                                         ("shift", 8192), ("shift", 12289), ("shift", 16374)])
+@pytest.mark.parametrize("layout", [(1, 0, 3), (2, 7, 1), (4, 0, 1)])
+def test_softmax_out_of_phase_pinned(o, kernel, cols, layout):
+    """The out-of-phase kernels where AUTO does not take them, pinned by
+    FR_SOFTMAX_OOP: x staged in shared memory for short rows, the row in
+    registers with 8 chunks a thread up to 16 warps (16374 columns at any
+    offset) for long ones."""
+    import os
+    w = workloads.make(1, rows=7, cols=cols, seed=2700 + cols)
+    os.environ["FR_SOFTMAX_OOP"] = kernel
+    try:
+        got = run_softmax(w.arrays["x"], "persistent", layout)
+    finally:
+        os.environ.pop("FR_SOFTMAX_OOP", None)
+    assert_close(got, o.softmax(w.arrays["x"]), "f32", f"{kernel} 7x{cols} {layout}")
 
 
 @pytest.mark.parametrize("cols", [c for c in COLS if c <= 1024])
@@ -204,6 +225,11 @@ def test_softmax_special_values(o, cols):
         got = run_softmax(x, form)
         assert_close(got, ref, "f32", f"{form} special {cols}")
         assert np.isnan(got[[1, 3, 4]]).all() and np.isfinite(got[[0, 2, 5]]).all()
+    for layout in ((1, 0, 3), (2, 7, 1)):  # out of phase (rows staggered by the padding)
+        for form in forms_for("softmax", cols, in_phase=False):
+            got = run_softmax(x, form, layout)
+            assert_close(got, ref, "f32", f"{form} special {cols} {layout}")
+            assert np.isnan(got[[1, 3, 4]]).all() and np.isfinite(got[[0, 2, 5]]).all()
 
 
 @pytest.mark.parametrize("cols", [1025, 8193, 32769, 65537, 131071, 262144])
@@ -564,7 +590,7 @@ def test_error_statuses_on_device():
     with pytest.raises(fr.FRError) as e:  # the cluster form pairs x's vectors with y's
         fr.fr_softmax(xs, form="split", out=ys)
     assert e.value.status == 3
-    fr.fr_softmax(xs, form="persistent", out=ys)  # staged in shared memory
+    fr.fr_softmax(xs, form="persistent", out=ys)  # the row in registers, shifted
     assert fr.fr_last_form() == "persistent"
     torch.cuda.synchronize()
     assert torch.allclose(ys, torch.full_like(ys, 1.0 / 2000))

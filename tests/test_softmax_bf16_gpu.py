@@ -31,9 +31,10 @@ def widen(bits):
 
 def forms(cols, layout=(0, 0, 0)):
     """persistent: one warp per row up to 2048 columns, one CTA per row up to
-    32768 when x and y rows share their 32-byte phase"""
+    32768 (the row in registers in phase, staged in shared memory out of
+    phase)"""
     in_phase = (layout[0] - layout[1]) * 2 % 32 == 0
-    persistent = cols <= 2048 or (cols <= 32768 and in_phase)
+    persistent = cols <= 32768
     split = in_phase and 2048 < cols <= 262144  # a cluster of CTAs per row
     return (["persistent"] if persistent else []) + (["split"] if split else []) + ["looped", "auto"]
 
@@ -59,6 +60,34 @@ def test_softmax_bf16_forms(o, rows, cols, layout):
         assert_bf16_within_steps(run(bits, form, layout), ref, 1, f"{form} {rows}x{cols} {layout}")
 
 
+# x past y by 1 .. 8 elements (shift 0 at 16 bytes: in 16-byte, not 32-byte
+# phase), rows staggered by the padding
+OOP_LAYOUTS = [(1, 0, 3), (2, 0, 1), (0, 5, 0), (4, 0, 2), (5, 0, 0), (6, 0, 1), (7, 0, 5),
+               (8, 0, 0)]
+
+
+@pytest.mark.parametrize("cols", [2049, 2055, 4096, 4097, 8192, 16369, 16385, 32768, 32769])
+@pytest.mark.parametrize("rows", [1, 9, 40])
+@pytest.mark.parametrize("layout", OOP_LAYOUTS)
+def test_softmax_bf16_out_of_phase(o, rows, cols, layout):
+    bits = workloads.make_softmax_bf16(rows, cols, seed=6500 + rows * 11 + cols).arrays["x"]
+    ref = o.softmax(widen(bits))
+    for form in forms(cols, layout):
+        assert_bf16_within_steps(run(bits, form, layout), ref, 1, f"{form} {rows}x{cols} {layout}")
+
+
+@pytest.mark.parametrize("kernel", ["stage", "warp"])
+@pytest.mark.parametrize("cols", [1025, 1536, 2047, 2048])
+@pytest.mark.parametrize("layout", [(1, 0, 3), (0, 5, 0), (8, 0, 0)])
+def test_softmax_bf16_out_of_phase_short_rows(o, kernel, cols, layout, monkeypatch):
+    """Rows of 1025 .. 2048 columns out of phase: staged in shared memory (the
+    default from 32 x SMs rows) or a warp per row, pinned by FR_SOFTMAX_OOP."""
+    monkeypatch.setenv("FR_SOFTMAX_OOP", kernel)
+    bits = workloads.make_softmax_bf16(40, cols, seed=6700 + cols).arrays["x"]
+    ref = o.softmax(widen(bits))
+    assert_bf16_within_steps(run(bits, "persistent", layout), ref, 1, f"{kernel} 40x{cols} {layout}")
+
+
 @pytest.mark.parametrize("cols", [7, 1000, 2048, 4097, 20000])
 def test_softmax_bf16_special_values(o, cols):
     bits = workloads.make_softmax_bf16(6, cols, seed=61).arrays["x"].copy()
@@ -67,9 +96,10 @@ def test_softmax_bf16_special_values(o, cols):
     bits[3, :] = 0xFF80                       # all -inf: 0/0
     bits[4, cols - 1] = 0x7F80                # +inf: inf - inf
     ref = o.softmax(widen(bits))
-    for form in forms(cols):
-        got = run(bits, form)
-        assert_bf16_within_steps(got, ref, 1, f"{form} special {cols}")
+    for layout in ((0, 0, 0), (1, 0, 3), (0, 5, 0)):
+        for form in forms(cols, layout):
+            got = run(bits, form, layout)
+            assert_bf16_within_steps(got, ref, 1, f"{form} special {cols} {layout}")
 
 
 def test_softmax_bf16_in_place_and_full_headline_shape(o):
