@@ -183,9 +183,12 @@ fr_status fr_reduce_sumsq(const void *x, float *out, int64_t rows, int64_t cols,
  *              buffer when ldx == ldy
  *   dtype      FR_F32 or FR_BF16; persistent up to 1024 (fp32) or 2048 (bf16)
  *              columns with one warp per row, up to 32768 with one CTA per
- *              row when x and y rows share their 32-byte phase; longer rows
- *              (or few rows) in phase take the split form (a cluster of CTAs
- *              per row, up to 262144 columns), the rest the looped form
+ *              row (the row in registers; for x and y rows at different
+ *              offsets within a 32-byte sector, fp32 rows of up to 4608
+ *              columns in registers with y's chunks shifted, longer ones
+ *              and bf16 rows staged in shared memory); longer rows (or few
+ *              rows) in phase take the split form (a cluster of CTAs per row,
+ *              up to 262144 columns), the rest the looped form
  */
 fr_status fr_softmax(const void *x, void *y, int64_t rows, int64_t cols, int64_t ldx,
                      int64_t ldy, fr_dtype dtype, fr_form form, fr_stream_t stream);
@@ -231,7 +234,11 @@ fr_status fr_softmax_host(const void *x_host, void *y_host, int64_t rows, int64_
  * streams each row through a shared-memory ring filled by bulk asynchronous
  * copies (the multi-stage staging of "Stax (4)", section 9.8, and the tensor
  * descriptors of "CMU 15-779 Lecture 8", section 5) and normalises from the
- * staged copy; the persistent form keeps the row in registers.
+ * staged copy; the persistent form keeps the row in registers.  FR_FORM_AUTO
+ * takes the looped form where cols = C x T x 32 with CTAs of T = 128, 160,
+ * 224, 256 or 512 threads (a cluster of C CTAs a row, 32 columns a thread),
+ * else the persistent form up to 16384 columns (cols % 8 == 0, 16-byte
+ * aligned rows), else the looped form.
  *
  *   x          bf16 [rows, ldx] device input (uint16 bit patterns)
  *   gamma,beta fp32 [cols] device inputs
