@@ -126,16 +126,15 @@ fr_form pick_ras(int64_t rows, int64_t cols, int sm_count, bool bf16 = false) {
 // CTA per row; 32768: 94.6 us against 105.9 at 2432 rows); at 262144 columns
 // the looped form once the rows fill the SMs (152 rows: looped 78.2 us, split
 // 79.8; 64 rows: split 39.4, looped 60.6).  Rows out of phase (x and y at
-// different offsets within a 32-byte sector): a CTA per row with the row
-// staged in shared memory up to 32768 columns, looped beyond.
+// different offsets within a 32-byte sector): a CTA per row up to 32768
+// columns (the row in registers up to 4608, staged in shared memory beyond),
+// looped beyond that.  Below 4 x SMs rows of 8192-16384 columns the two
+// forms are within launch noise of each other (five sweeps, means: 304 x
+// 16384 CTA per row 12.2 us, looped 11.3; 152 x 16384 8.8 against 9.5; 608 x
+// 16384 16.7 against 20.3).
 fr_form pick_softmax(int64_t rows, int64_t cols, bool vec, int sm_count) {
   if (cols <= 1024) return FR_FORM_PERSISTENT;
-  if (!vec)  // out of phase: the staged CTA per row, but at 8192-16384 columns only
-             // once the rows fill 4 x SMs (304 x 16384: looped 10.6 us, staged 12.2)
-    return cols <= fr::softmax_persistent_max_cols(false) &&
-                   (cols <= 6144 || cols > 16384 || rows >= 4 * static_cast<int64_t>(sm_count))
-               ? FR_FORM_PERSISTENT
-               : FR_FORM_LOOPED;
+  if (!vec) return cols <= fr::softmax_persistent_max_cols(false) ? FR_FORM_PERSISTENT : FR_FORM_LOOPED;
   if (cols <= 8192) return FR_FORM_PERSISTENT;
   if (cols <= 131072 || (cols <= fr::softmax_split_max_cols() && rows < sm_count))
     return FR_FORM_SPLIT;

@@ -664,22 +664,33 @@ softmax_block_looped(const float *__restrict__ x, float *__restrict__ y, int64_t
     const float mb = r.m * kLog2e;
     const float inv = __frcp_rn(r.d);
     if constexpr (VEC) {
+      // Pass 2 walks the chunks last to first: pass 1 read them first to
+      // last, so the chunks L2 still holds when a row is longer than its
+      // share of L2 are the ones read again first (measured on GB300: 1216 x
+      // 65537 140.2 us against 147.1 first to last, 2432 x 32768 128.1
+      // against 134.7).
       const float *vx = px + sp.head;
       float *vy = py + sp.head;
+      const int64_t nck = (sp.nvec + T * U - 1) / (T * U);
       V8 nx[U];
       if constexpr (PF) {
+        if (nck > 0) {
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-          if (tid + T * u < sp.nvec) nx[u] = ld_stream_v8(vx + (tid + T * u) * 8);
+          for (int u = 0; u < U; ++u) {
+            const int64_t vi = (nck - 1) * T * U + tid + T * u;
+            if (vi < sp.nvec) nx[u] = ld_stream_v8(vx + vi * 8);
+          }
+        }
       }
-      for (int64_t base = 0; base < sp.nvec; base += T * U) {
+      for (int64_t ck = nck - 1; ck >= 0; --ck) {
+        const int64_t base = ck * T * U;
         V8 v[U];
-        const int64_t lb = PF ? base + T * U : base;
+        const int64_t lb = PF ? base - T * U : base;  // the chunk loaded now
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           if constexpr (PF) v[u] = nx[u];
           const int64_t vi = lb + tid + T * u;
-          if (vi < sp.nvec) (PF ? nx[u] : v[u]) = ld_stream_v8(vx + vi * 8);
+          if (lb >= 0 && vi < sp.nvec) (PF ? nx[u] : v[u]) = ld_stream_v8(vx + vi * 8);
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -696,7 +707,8 @@ softmax_block_looped(const float *__restrict__ x, float *__restrict__ y, int64_t
       if (tid < sp.head) si = tid;
       else if (tid < sp.head + sp.tail) si = sp.head + sp.nvec * 8 + (tid - sp.head);
       if (si >= 0) st_stream_f32(py + si, ex2(fmaf(ld_stream_f32(px + si), kLog2e, -mb)) * inv);
-    } else {
+    } else {  // first to last (last to first measured slower here: 1216 x 65537
+              // out of phase 200.1 us against 180.6)
       for (int64_t i = tid; i < cols; i += T)
         st_stream_f32(py + i, ex2(fmaf(ld_stream_f32(px + i), kLog2e, -mb)) * inv);
     }

@@ -541,9 +541,14 @@ softmax_bf16_block_looped(const uint16_t *__restrict__ x, uint16_t *__restrict__
     const float mb = r.m * kLog2e;
     const float inv = __frcp_rn(r.d);
     if constexpr (VEC) {
+      // Pass 2 walks the chunks last to first: pass 1 read them first to
+      // last, so the chunks L2 still holds when a row is longer than its
+      // share of L2 are the ones read again first (measured on GB300: 1216 x
+      // 131072 134.8 us against 141.9 first to last).
       const uint16_t *vx = px + sp.head;
       uint16_t *vy = py + sp.head;
-      for (int64_t base = 0; base < sp.nvec; base += T * kLoopU) {
+      for (int64_t base = (sp.nvec - 1) / (T * kLoopU) * (T * kLoopU); base >= 0;
+           base -= T * kLoopU) {
         V8 v[kLoopU];
 #pragma unroll
         for (int u = 0; u < kLoopU; ++u) {
@@ -568,10 +573,23 @@ softmax_bf16_block_looped(const uint16_t *__restrict__ x, uint16_t *__restrict__
       if (si >= 0)
         st_stream_u16(py + si,
                       to_bf16(ex2(fmaf(bf16_to_f32(ld_stream_u16(px + si)), kLog2e, -mb)) * inv));
-    } else {
-      for (int64_t i = tid; i < cols; i += T)
-        st_stream_u16(py + i,
-                      to_bf16(ex2(fmaf(bf16_to_f32(ld_stream_u16(px + i)), kLog2e, -mb)) * inv));
+    } else {  // chunks of 8 a thread, last to first as above (out of phase,
+              // measured on GB300: 152 x 65537 29.2 us against 33.5 first to
+              // last, 608 x 65537 68.8 against 75.3)
+      for (int64_t base = (cols - 1) / (T * 8) * (T * 8); base >= 0; base -= T * 8) {
+        uint16_t v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int64_t i = base + tid + T * u;
+          v[u] = i < cols ? ld_stream_u16(px + i) : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int64_t i = base + tid + T * u;
+          if (i < cols)
+            st_stream_u16(py + i, to_bf16(ex2(fmaf(bf16_to_f32(v[u]), kLog2e, -mb)) * inv));
+        }
+      }
     }
   }
 }

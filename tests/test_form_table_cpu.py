@@ -48,15 +48,12 @@ def test_table_covers_every_op_and_the_forms():
 
 def test_rules_name_the_form_auto_took():
     """fr_auto_form answers for rows in phase; rows out of phase take the
-    persistent form up to 32768 columns (fp32: at 6145 .. 16384 columns only
-    from 4 x SMs rows), looped beyond."""
+    persistent form up to 32768 columns, looped beyond."""
     import reduction_pointwise_row_gb300 as fr
     sms, rows = table_rows()
     for r in rows:
         if r["op"] == OUT_OF_PHASE:
-            staged = (r["dtype"] == "bf16" or r["cols"] <= 6144 or r["cols"] > 16384 or
-                      r["rows"] >= 4 * sms)
-            want = "persistent" if r["cols"] <= 32768 and staged else "looped"
+            want = "persistent" if r["cols"] <= 32768 else "looped"
         else:
             want = fr.fr_auto_form(r["op"], r["rows"], r["cols"], r["dtype"], sms)
         assert want == r["auto"], r
