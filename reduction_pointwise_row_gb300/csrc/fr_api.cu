@@ -145,17 +145,20 @@ fr_form pick_softmax(int64_t rows, int64_t cols, bool vec, int sm_count) {
 // staged in shared memory (16384 x 4097: 48.3 us, looped 87.8; 4864 x 32768:
 // 95.1 against 183.5), looped beyond.
 // Rows in phase: up to 2048 columns a warp per row, up to 8192
-// a CTA per row; at 16384 the looped form once there are 4 x SMs rows (608:
-// looped 9.4 us, CTA per row 10.5; 4864: 52.0 against 60.3), a CTA per row
-// below; at 32768 a CTA per row while the rows are no more than the SMs (152:
+// a CTA per row; at 16384 the looped form from 4 x SMs rows (608: looped 9.4
+// us, CTA per row 10.5), a CTA per row below, and a CTA per row again from 8
+// x SMs rows, where the persistent form stages the row in shared memory
+// (1216: 15.2 us, looped 15.8; 16384: 153.2 against 165.6); at 32768 a CTA per row while the rows are no more than the SMs (152:
 // 6.7 us against 7.7 for a cluster per row), else, up to 262144 columns, a
 // cluster per row (2432 x 32768: 50.2 us, looped 55.3, CTA per row 73.9).
 fr_form pick_softmax_bf16(int64_t rows, int64_t cols, bool vec, int sm_count) {
   if (cols <= 2048) return FR_FORM_PERSISTENT;
   if (!vec) return cols <= 32768 ? FR_FORM_PERSISTENT : FR_FORM_LOOPED;
   if (cols <= 8192) return FR_FORM_PERSISTENT;
-  if (cols <= 16384) return rows >= 4 * static_cast<int64_t>(sm_count) ? FR_FORM_LOOPED
-                                                                       : FR_FORM_PERSISTENT;
+  if (cols <= 16384) {  // from 8 x SMs rows the persistent form stages rows in shared memory
+    const int64_t sms = sm_count;
+    return rows >= 8 * sms || rows < 4 * sms ? FR_FORM_PERSISTENT : FR_FORM_LOOPED;
+  }
   if (cols <= 32768 && rows <= sm_count) return FR_FORM_PERSISTENT;
   if (cols <= fr::softmax_bf16_split_max_cols()) return FR_FORM_SPLIT;
   return FR_FORM_LOOPED;

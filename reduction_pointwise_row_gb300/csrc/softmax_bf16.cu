@@ -668,7 +668,19 @@ cudaError_t launch_softmax_bf16_persistent(const uint16_t *x, uint16_t *y, int64
                                            int64_t cols, int64_t ldx, int64_t ldy, bool vec,
                                            int sm_count, cudaStream_t s) {
   const unsigned grid = warp_row_grid(rows);
-  if (vec && cols > 2048) {
+  // In phase, rows of 8193 .. 16384 columns from 8 x SMs rows take the
+  // staged kernel below too: 32 KiB of shared memory a row fits seven rows an
+  // SM, where the register kernel's 512-thread CTAs fit two (measured on
+  // GB300, us per call, registers / staged / looped: 16384 x 16384 153.2 /
+  // 153.2 / 165.6 -- above 24 x SMs rows the same kernel --, 2432 x 16384
+  // 32.2 / 26.0 / 27.9, 1216 x 16384 18.4 / 15.2 / 15.8, 1216 x 12288 15.8 /
+  // 12.6 / 13.3).  FR_SOFTMAX_BF16_CTA=regs|stage pins the kernel.
+  const char *cta_pin = getenv("FR_SOFTMAX_BF16_CTA");
+  const bool stage_long =
+      vec && cols > 8192 && cols <= 16384 &&
+      (cta_pin != nullptr ? strcmp(cta_pin, "stage") == 0
+                          : rows >= 8 * static_cast<int64_t>(sm_count));
+  if (vec && cols > 2048 && !stage_long) {
     if (rows > 0x7fffffff) return cudaErrorInvalidValue;
     const int64_t nvec = cols / kPer;  // at least the body's vectors
     if (nvec <= 128 * 2) return launch_bf16_cta<128, 2>(x, y, rows, cols, ldx, ldy, s);
@@ -685,7 +697,7 @@ cudaError_t launch_softmax_bf16_persistent(const uint16_t *x, uint16_t *y, int64
   const char *oop = getenv("FR_SOFTMAX_OOP");
   const bool stage_short = oop != nullptr ? strcmp(oop, "stage") == 0
                                           : rows >= 32 * static_cast<int64_t>(sm_count);
-  if (!vec && (cols > 2048 || (stage_short && cols > 1024))) {  // staged
+  if ((!vec && (cols > 2048 || (stage_short && cols > 1024))) || stage_long) {  // staged
     if (rows > 0x7fffffff || cols > kBfStageMaxCols) return cudaErrorInvalidValue;
     // four to eight 16-byte chunks a thread
     const size_t smem = (static_cast<size_t>(cols) + 16) * 2;

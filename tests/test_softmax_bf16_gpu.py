@@ -88,6 +88,28 @@ def test_softmax_bf16_out_of_phase_short_rows(o, kernel, cols, layout, monkeypat
     assert_bf16_within_steps(run(bits, "persistent", layout), ref, 1, f"{kernel} 40x{cols} {layout}")
 
 
+@pytest.mark.parametrize("cols", [8193, 12000, 16384])
+@pytest.mark.parametrize("layout", [(0, 0, 0), (3, 3, 7)])
+def test_softmax_bf16_long_rows_staged_in_phase(o, cols, layout, monkeypatch):
+    """Rows in phase of 8193 .. 16384 columns through the staged kernel
+    (AUTO's persistent kernel there from 8 x SMs rows; pinned here)."""
+    monkeypatch.setenv("FR_SOFTMAX_BF16_CTA", "stage")
+    bits = workloads.make_softmax_bf16(9, cols, seed=6800 + cols).arrays["x"]
+    ref = o.softmax(widen(bits))
+    assert_bf16_within_steps(run(bits, "persistent", layout), ref, 1, f"stage 9x{cols} {layout}")
+
+
+def test_softmax_bf16_many_long_rows_auto(o):
+    """8 x 152 rows of 16384 columns in phase: AUTO's persistent form stages
+    them; the first and last 32 rows against the oracle."""
+    rows, cols = 8 * 152, 16384
+    bits = workloads.make_softmax_bf16(rows, cols, seed=6900).arrays["x"]
+    got = run(bits, "auto")
+    assert fr.fr_last_form() == fr.fr_auto_form("softmax", rows, cols, "bf16", fr.sm_count())
+    for sl in (slice(0, 32), slice(rows - 32, rows)):
+        assert_bf16_within_steps(got[sl], o.softmax(widen(bits[sl])), 1, f"auto {rows}x{cols}")
+
+
 @pytest.mark.parametrize("cols", [7, 1000, 2048, 4097, 20000])
 def test_softmax_bf16_special_values(o, cols):
     bits = workloads.make_softmax_bf16(6, cols, seed=61).arrays["x"].copy()
