@@ -265,9 +265,13 @@ template <class Op, class In, bool SQRT>
 cudaError_t launch_split(const void *a, const void *b, float *out, int64_t rows, int64_t cols,
                          int64_t lda, int64_t ldb, Op op, bool vec, double *partials,
                          int segments, cudaStream_t s) {
-  // Ordinary launches: with the programmatic overlap the split form measured
-  // slower on GB300 (fp32 [8, 33554432]: 323 us against 309 us), its one-wave
-  // stage 1 sharing the SMs with the next call's early-placed CTAs.
+  // Stage 1 an ordinary launch: as a programmatic dependent of the call
+  // before, the split form measured slower on GB300 (fp32 [8, 33554432]: 323
+  // us against 309 us), its one-wave stage 1 sharing the SMs with the next
+  // call's early-placed CTAs.  Stage 2 a programmatic dependent of stage 1:
+  // placed as stage 1's CTAs exit, it saves 1.5-2 us a call (8 x 1048576:
+  // 19.1 us against 21.0; 32 x 1048576: 46.5 against 48.3; 8 x 33554432:
+  // 307.6 against 309.5).
   using E = typename In::T;
   const E *ea = static_cast<const E *>(a), *eb = static_cast<const E *>(b);
   const dim3 grid(static_cast<unsigned>(segments), static_cast<unsigned>(rows));
@@ -279,9 +283,8 @@ cudaError_t launch_split(const void *a, const void *b, float *out, int64_t rows,
                                                                      partials, segments);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  rowsum_split_stage2<SQRT><<<warp_row_grid(rows), kRowThreads, 0, s>>>(partials, out, rows,
-                                                                        segments);
-  return cudaGetLastError();
+  return launch_k(rowsum_split_stage2<SQRT>, dim3(warp_row_grid(rows)), dim3(kRowThreads), 0, s, 0,
+                  static_cast<const double *>(partials), out, rows, segments);
 }
 
 }  // namespace
