@@ -4,7 +4,13 @@
 //
 // persistent  one warp per row, the row held in registers (up to 1024 fp32 per
 //             warp), the max and the sum taken in two passes over registers:
-//             one read and one write of each element (the 2N lower bound).
+//             one read and one write of each element (the 2N lower bound);
+//             longer rows one CTA per row the same way.  Rows whose x and y
+//             sit at different offsets within a 32-byte sector: a CTA per row
+//             with the row in registers and y's chunks shifted by shuffles
+//             (up to 4608 columns) or the row staged in shared memory.
+// split       a thread-block cluster per row, each CTA a slice in registers,
+//             the slices' (m, d) exchanged through distributed shared memory.
 // looped      one CTA per row (grid-stride over rows) for rows longer than a
 //             warp can hold.  Pass 1 keeps a per-thread online pair (m, d) and
 //             folds each chunk in with the merge of section 9.5 (a chunk's max
