@@ -154,9 +154,11 @@ def kernel_source_hash():
     helpers it inlines: other kernels of the same file may change without
     invalidating its counters."""
     text = open(KERNEL_SRC).read()
-    start = text.index("template <int NV>\n__global__ void __launch_bounds__(kWarpRowThreads)\n"
-                       "softmax_warp_vec(")
-    end = text.index("\n}\n", start) + 3
+    name = text.find("\nsoftmax_warp_vec(")
+    if name < 0:
+        return None
+    start = text.rfind("\ntemplate <", 0, name) + 1
+    end = text.index("\n}\n", name) + 3
     h = hashlib.sha256(text[start:end].encode())
     with open(os.path.join(ROOT, "reduction_pointwise_row_gb300", "csrc", "common.cuh"), "rb") as f:
         h.update(f.read())
@@ -281,8 +283,9 @@ def run_ours(args):
     # ---- e2e: the library's host-buffer entry point (fr_softmax_host) on the
     # same rows in page-locked host memory, every byte crossing the host link
     # inside the timed region.  Direct form: the kernel reads x and writes y
-    # in host memory over NVLink-C2C (900 us per step on GB300, against 950
-    # for the staged form with 4096-row chunks, the best of 512 .. 32768).
+    # in host memory over NVLink-C2C (790 us per step on GB300 from a grid of a
+    # quarter of the SMs' CTAs, against 950 for the staged form with 4096-row
+    # chunks, the best of 512 .. 32768).
     y_host = torch.empty_like(x_host).pin_memory()
     e2e_steps = max(3, min(args.steps, 20))
     E2E_CHUNK = 0  # direct
@@ -1079,7 +1082,7 @@ HOST_ROWS_NS = 300_000  # softmax launches longer than this read and write host 
 def launches_markdown(path: str) -> str:
     """Launches, total time and share per kernel of an ncu launch list.  The
     softmax kernel's end-to-end launches (rows in page-locked host memory,
-    fr_softmax_host's direct form, about 900 us each) are listed apart from
+    fr_softmax_host's direct form, about 790 us each) are listed apart from
     its device-resident launches (under 300 us)."""
     import csv
     import re as _re

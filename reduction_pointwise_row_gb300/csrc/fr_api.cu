@@ -407,9 +407,18 @@ fr_status fr_softmax_host(const void *x_host, void *y_host, int64_t rows, int64_
   fr::DevInfo info;
   if (fr_status st = device_ok(&info)) return st;
   if (!page_locked(x_host) || !page_locked(y_host)) return FR_ERR_INVALID_ARG;
-  if (chunk_rows == 0)  // direct: the kernel reads and writes host memory over the host link
-    return fr_softmax(host_device_ptr(x_host), host_device_ptr(y_host), rows, cols, cols, cols,
-                      dtype, FR_FORM_AUTO, stream);
+  if (chunk_rows == 0) {  // direct: the kernel reads and writes host memory over the host link
+    const void *dx = host_device_ptr(x_host);
+    void *dy = host_device_ptr(y_host);
+    if (dtype == FR_F32 && cols <= 1024 && same_phase(dx, cols, dy, cols, 4) &&
+        rows <= 0x7fffffffLL * 8)
+      return launched(fr::launch_softmax_host_rows(static_cast<const float *>(dx),
+                                                   static_cast<float *>(dy), rows, cols,
+                                                   info.sm_count,
+                                                   reinterpret_cast<cudaStream_t>(stream)),
+                      FR_FORM_PERSISTENT);
+    return fr_softmax(dx, dy, rows, cols, cols, cols, dtype, FR_FORM_AUTO, stream);
+  }
   if (chunk_rows > rows) chunk_rows = rows;
   if (!workspace || workspace_bytes < fr::host_pipeline_workspace(cols, es, es, chunk_rows))
     return FR_ERR_WORKSPACE_TOO_SMALL;

@@ -53,6 +53,10 @@ cudaError_t launch_sumsq_split(const float *x, float *out, int64_t rows, int64_t
 // ---- softmax ---------------------------------------------------------------
 
 int64_t softmax_persistent_max_cols(bool vec);
+// fp32 rows of at most 1024 columns in host memory, x and y in phase, ld =
+// cols: the persistent form over a small grid (a quarter of the SMs' CTAs).
+cudaError_t launch_softmax_host_rows(const float *x, float *y, int64_t rows, int64_t cols,
+                                     int sm_count, cudaStream_t s);
 cudaError_t launch_softmax_persistent(const float *x, float *y, int64_t rows, int64_t cols,
                                       int64_t ldx, int64_t ldy, bool vec, cudaStream_t s);
 // Persistent warp-per-row form with a per-warp cp.async ring (16-byte aligned

@@ -37,68 +37,79 @@ __device__ __forceinline__ float fbits(uint32_t w) { return __uint_as_float(w); 
 
 // Persistent form, 32-byte vectors: NV vectors per lane (cols <= 256*NV).
 // x and y rows share their offset modulo 32 bytes (checked by the host).
-template <int NV>
+// HOST: rows in host memory, read and written over the host link by a grid
+// of a few CTAs an SM whose warps take rows row, row + W, row + 2W, ... (W
+// the grid's warps), which bounds the requests in flight on the link; a warp
+// for every row at once oversubscribes it.
+template <int NV, bool HOST = false>
 __global__ void __launch_bounds__(kWarpRowThreads)
 softmax_warp_vec(const float *__restrict__ x, float *__restrict__ y, int64_t rows, int64_t cols,
                  int64_t ldx, int64_t ldy) {
   pdl_enter();
   const int lane = threadIdx.x & 31;
-  const int64_t row =
+  const int64_t first =
       static_cast<int64_t>(blockIdx.x) * (kWarpRowThreads / 32) + (threadIdx.x >> 5);
-  if (row >= rows) return;
-  const float *px = x + row * ldx;
-  float *py = y + row * ldy;
-  const RowSplit sp = row_split(px, cols, 4);
-  // head and tail scalars (at most 7 + 7): one per lane
-  int64_t si = -1;
-  if (lane < sp.head) si = lane;
-  else if (lane < sp.head + sp.tail) si = sp.head + sp.nvec * 8 + (lane - sp.head);
-  const float *vx = px + sp.head;
-  V8 v[NV];
+  auto one_row = [&](int64_t row) {
+    const float *px = x + row * ldx;
+    float *py = y + row * ldy;
+    const RowSplit sp = row_split(px, cols, 4);
+    // head and tail scalars (at most 7 + 7): one per lane
+    int64_t si = -1;
+    if (lane < sp.head) si = lane;
+    else if (lane < sp.head + sp.tail) si = sp.head + sp.nvec * 8 + (lane - sp.head);
+    const float *vx = px + sp.head;
+    V8 v[NV];
 #pragma unroll
-  for (int k = 0; k < NV; ++k) {
-    const int64_t vi = lane + 32 * k;
-    if (vi < sp.nvec) v[k] = ld_stream_v8(vx + vi * 8);
-  }
-  float sv = -INFINITY;
-  if (si >= 0) sv = ld_stream_f32(px + si);
-
-  float m = sv;
-#pragma unroll
-  for (int k = 0; k < NV; ++k)
-    if (lane + 32 * k < sp.nvec) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) m = max_nan(m, fbits(v[k].w[j]));
+    for (int k = 0; k < NV; ++k) {
+      const int64_t vi = lane + 32 * k;
+      if (vi < sp.nvec) v[k] = ld_stream_v8(vx + vi * 8);
     }
-  m = warp_max_nan(m);
-  const float mb = m * kLog2e;
+    float sv = -INFINITY;
+    if (si >= 0) sv = ld_stream_f32(px + si);
 
-  float se = si >= 0 ? ex2(fmaf(sv, kLog2e, -mb)) : 0.0f;
-  float d = se;
+    float m = sv;
 #pragma unroll
-  for (int k = 0; k < NV; ++k)
-    if (lane + 32 * k < sp.nvec) {
+    for (int k = 0; k < NV; ++k)
+      if (lane + 32 * k < sp.nvec) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float e = ex2(fmaf(fbits(v[k].w[j]), kLog2e, -mb));
-        v[k].w[j] = __float_as_uint(e);
-        d += e;
+        for (int j = 0; j < 8; ++j) m = max_nan(m, fbits(v[k].w[j]));
+      }
+    m = warp_max_nan(m);
+    const float mb = m * kLog2e;
+
+    float se = si >= 0 ? ex2(fmaf(sv, kLog2e, -mb)) : 0.0f;
+    float d = se;
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+      if (lane + 32 * k < sp.nvec) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float e = ex2(fmaf(fbits(v[k].w[j]), kLog2e, -mb));
+          v[k].w[j] = __float_as_uint(e);
+          d += e;
+        }
+      }
+    d = warp_sum(d);
+    const float inv = __frcp_rn(d);
+
+    float *vy = py + sp.head;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int64_t vi = lane + 32 * k;
+      if (vi < sp.nvec) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[k].w[j] = __float_as_uint(fbits(v[k].w[j]) * inv);
+        st_stream_v8(vy + vi * 8, v[k]);
       }
     }
-  d = warp_sum(d);
-  const float inv = __frcp_rn(d);
-
-  float *vy = py + sp.head;
-#pragma unroll
-  for (int k = 0; k < NV; ++k) {
-    const int64_t vi = lane + 32 * k;
-    if (vi < sp.nvec) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[k].w[j] = __float_as_uint(fbits(v[k].w[j]) * inv);
-      st_stream_v8(vy + vi * 8, v[k]);
-    }
+    if (si >= 0) st_stream_f32(py + si, se * inv);
+  };
+  if constexpr (HOST) {
+    const int64_t step = static_cast<int64_t>(gridDim.x) * (kWarpRowThreads / 32);
+    for (int64_t row = first; row < rows; row += step) one_row(row);
+  } else {
+    if (first < rows) one_row(first);
   }
-  if (si >= 0) st_stream_f32(py + si, se * inv);
 }
 
 // Persistent form, scalar lane-strided elements (rows without a shared 32-byte
@@ -893,6 +904,33 @@ cudaError_t launch_softmax_persistent(const float *x, float *y, int64_t rows, in
     else return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
+}
+
+// Rows in host memory (fp32, at most 1024 columns, x and y in phase): the
+// warp-per-row kernel over a small grid whose warps take rows in turn, so
+// that the host link sees a bounded number of requests in flight.  Measured
+// on GB300 (fp32 [32768, 1024] in page-locked memory, x in and y out over
+// NVLink-C2C, GB/s both ways): 19 CTAs of 8 warps 337.2, 38 340.4, 76 338.4,
+// 152 334.3, 304 325.3, 608 298.1, a warp for every row (4096 CTAs) 304.2 --
+// about 1.2 MB of loads in flight is what the link serves best.
+// FR_HOST_GRID=<CTAs> pins the grid (default a quarter of the SMs).
+cudaError_t launch_softmax_host_rows(const float *x, float *y, int64_t rows, int64_t cols,
+                                     int sm_count, cudaStream_t s) {
+  const int64_t nv = (cols + 255) / 256;
+  if (nv < 1 || nv > 4) return cudaErrorInvalidValue;
+  int64_t grid = sm_count / 4 > 0 ? sm_count / 4 : 1;
+  if (const char *e = getenv("FR_HOST_GRID")) {
+    const int v = atoi(e);
+    if (v >= 1 && v <= 65535) grid = v;
+  }
+  const int64_t need = (rows + kWarpRowThreads / 32 - 1) / (kWarpRowThreads / 32);
+  if (grid > need) grid = need;
+  void (*kern)(const float *, float *, int64_t, int64_t, int64_t, int64_t) =
+      nv == 1 ? softmax_warp_vec<1, true> : nv == 2 ? softmax_warp_vec<2, true>
+                                          : nv == 3 ? softmax_warp_vec<3, true>
+                                                    : softmax_warp_vec<4, true>;
+  return launch_k(kern, dim3(static_cast<unsigned>(grid)), dim3(kWarpRowThreads), 0, s, 0, x, y,
+                  rows, cols, cols, cols);
 }
 
 bool softmax_async_ok(int64_t cols, bool aligned16) { return aligned16 && cols <= 1024; }
