@@ -417,6 +417,13 @@ fr_status fr_softmax_host(const void *x_host, void *y_host, int64_t rows, int64_
                                                    info.sm_count,
                                                    reinterpret_cast<cudaStream_t>(stream)),
                       FR_FORM_PERSISTENT);
+    if (dtype == FR_BF16 && cols <= 2048 && same_phase(dx, cols, dy, cols, 2) &&
+        rows <= 0x7fffffffLL * 8)
+      return launched(fr::launch_softmax_bf16_host_rows(static_cast<const uint16_t *>(dx),
+                                                        static_cast<uint16_t *>(dy), rows, cols,
+                                                        info.sm_count,
+                                                        reinterpret_cast<cudaStream_t>(stream)),
+                      FR_FORM_PERSISTENT);
     return fr_softmax(dx, dy, rows, cols, cols, cols, dtype, FR_FORM_AUTO, stream);
   }
   if (chunk_rows > rows) chunk_rows = rows;

@@ -78,6 +78,10 @@ cudaError_t launch_softmax_split(const float *x, float *y, int64_t rows, int64_t
 // (a warp per row up to 2048; then a CTA per row, in phase the row in
 // registers, out of phase staged in shared memory).
 int64_t softmax_bf16_persistent_max_cols(bool vec);
+// bf16 rows of at most 2048 columns in host memory, x and y in phase, ld =
+// cols: the persistent form over a small grid (a quarter of the SMs' CTAs).
+cudaError_t launch_softmax_bf16_host_rows(const uint16_t *x, uint16_t *y, int64_t rows,
+                                          int64_t cols, int sm_count, cudaStream_t s);
 // Split form of the bf16 softmax: a thread-block cluster per row (rows in
 // phase, 2049 .. softmax_bf16_split_max_cols() columns).
 int64_t softmax_bf16_split_max_cols();

@@ -41,66 +41,77 @@ __device__ __forceinline__ float vec_max(const V8 &v) {
 // Persistent form, 32-byte vectors: NV vectors of 16 elements per lane
 // (cols <= 512 * NV).  x and y rows share their offset modulo 32 bytes.  The
 // 16 * NV exponentials stay in registers (89 at NV = 4, no spill).
-template <int NV>
+// HOST: rows in host memory over the host link, from a small grid whose
+// warps take rows row, row + W, ... (W the grid's warps): a bounded number of
+// requests in flight (the fp32 kernel's launch_softmax_host_rows has the
+// measurements).
+template <int NV, bool HOST = false>
 __global__ void __launch_bounds__(kWarpRowThreads, 1)
 softmax_bf16_warp_vec(const uint16_t *__restrict__ x, uint16_t *__restrict__ y, int64_t rows,
                       int64_t cols, int64_t ldx, int64_t ldy) {
   pdl_enter();
   const int lane = threadIdx.x & 31;
-  const int64_t row =
+  const int64_t first =
       static_cast<int64_t>(blockIdx.x) * (kWarpRowThreads / 32) + (threadIdx.x >> 5);
-  if (row >= rows) return;
-  const uint16_t *px = x + row * ldx;
-  uint16_t *py = y + row * ldy;
-  const RowSplit sp = row_split(px, cols, 2);
-  // head and tail scalars (at most 15 + 15): one per lane
-  int64_t si = -1;
-  if (lane < sp.head) si = lane;
-  else if (lane < sp.head + sp.tail) si = sp.head + sp.nvec * kPer + (lane - sp.head);
-  const uint16_t *vx = px + sp.head;
-  V8 v[NV];
+  auto one_row = [&](int64_t row) {
+    const uint16_t *px = x + row * ldx;
+    uint16_t *py = y + row * ldy;
+    const RowSplit sp = row_split(px, cols, 2);
+    // head and tail scalars (at most 15 + 15): one per lane
+    int64_t si = -1;
+    if (lane < sp.head) si = lane;
+    else if (lane < sp.head + sp.tail) si = sp.head + sp.nvec * kPer + (lane - sp.head);
+    const uint16_t *vx = px + sp.head;
+    V8 v[NV];
 #pragma unroll
-  for (int k = 0; k < NV; ++k) {
-    const int64_t vi = lane + 32 * k;
-    if (vi < sp.nvec) v[k] = ld_stream_v8(vx + vi * kPer);
-  }
-  const float sv = si >= 0 ? bf16_to_f32(ld_stream_u16(px + si)) : -INFINITY;
+    for (int k = 0; k < NV; ++k) {
+      const int64_t vi = lane + 32 * k;
+      if (vi < sp.nvec) v[k] = ld_stream_v8(vx + vi * kPer);
+    }
+    const float sv = si >= 0 ? bf16_to_f32(ld_stream_u16(px + si)) : -INFINITY;
 
-  float m = sv;
+    float m = sv;
 #pragma unroll
-  for (int k = 0; k < NV; ++k)
-    if (lane + 32 * k < sp.nvec) m = max_nan(m, vec_max(v[k]));
-  m = warp_max_nan(m);
-  const float mb = m * kLog2e;
+    for (int k = 0; k < NV; ++k)
+      if (lane + 32 * k < sp.nvec) m = max_nan(m, vec_max(v[k]));
+    m = warp_max_nan(m);
+    const float mb = m * kLog2e;
 
-  const float se = si >= 0 ? ex2(fmaf(sv, kLog2e, -mb)) : 0.0f;
-  float e[NV][kPer];
-  float d = se;
+    const float se = si >= 0 ? ex2(fmaf(sv, kLog2e, -mb)) : 0.0f;
+    float e[NV][kPer];
+    float d = se;
 #pragma unroll
-  for (int k = 0; k < NV; ++k)
-    if (lane + 32 * k < sp.nvec) {
+    for (int k = 0; k < NV; ++k)
+      if (lane + 32 * k < sp.nvec) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        e[k][2 * j] = ex2(fmaf(bf16_lo(v[k].w[j]), kLog2e, -mb));
-        e[k][2 * j + 1] = ex2(fmaf(bf16_hi(v[k].w[j]), kLog2e, -mb));
-        d += e[k][2 * j] + e[k][2 * j + 1];
+        for (int j = 0; j < 8; ++j) {
+          e[k][2 * j] = ex2(fmaf(bf16_lo(v[k].w[j]), kLog2e, -mb));
+          e[k][2 * j + 1] = ex2(fmaf(bf16_hi(v[k].w[j]), kLog2e, -mb));
+          d += e[k][2 * j] + e[k][2 * j + 1];
+        }
+      }
+    d = warp_sum(d);
+    const float inv = __frcp_rn(d);
+
+    uint16_t *vy = py + sp.head;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int64_t vi = lane + 32 * k;
+      if (vi < sp.nvec) {
+        V8 o;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o.w[j] = pack_bf16x2(e[k][2 * j] * inv, e[k][2 * j + 1] * inv);
+        st_stream_v8(vy + vi * kPer, o);
       }
     }
-  d = warp_sum(d);
-  const float inv = __frcp_rn(d);
-
-  uint16_t *vy = py + sp.head;
-#pragma unroll
-  for (int k = 0; k < NV; ++k) {
-    const int64_t vi = lane + 32 * k;
-    if (vi < sp.nvec) {
-      V8 o;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) o.w[j] = pack_bf16x2(e[k][2 * j] * inv, e[k][2 * j + 1] * inv);
-      st_stream_v8(vy + vi * kPer, o);
-    }
+    if (si >= 0) st_stream_u16(py + si, to_bf16(se * inv));
+  };
+  if constexpr (HOST) {
+    const int64_t step = static_cast<int64_t>(gridDim.x) * (kWarpRowThreads / 32);
+    for (int64_t row = first; row < rows; row += step) one_row(row);
+  } else {
+    if (first < rows) one_row(first);
   }
-  if (si >= 0) st_stream_u16(py + si, to_bf16(se * inv));
 }
 
 // Persistent form for longer rows in phase: one CTA of T threads per row,
@@ -599,6 +610,31 @@ unsigned warp_row_grid(int64_t rows) {
 }
 
 }  // namespace
+
+// bf16 rows of at most 2048 columns in host memory, x and y in phase, ld =
+// cols: the warp kernel over a grid of a quarter of the SMs' CTAs
+// (FR_HOST_GRID=<CTAs> pins it).  Measured on GB300 (bf16 [65536, 1024],
+// GB/s both ways): 19 CTAs 258.5, 38 335.5, 76 336.9, 152 337.7, a warp for
+// every row 335.6 -- rows half the bytes of fp32 ones oversubscribe the link
+// less.
+cudaError_t launch_softmax_bf16_host_rows(const uint16_t *x, uint16_t *y, int64_t rows,
+                                          int64_t cols, int sm_count, cudaStream_t s) {
+  const int64_t nv = (cols + 32 * kPer - 1) / (32 * kPer);
+  if (nv < 1 || nv > 4) return cudaErrorInvalidValue;
+  int64_t grid = sm_count / 4 > 0 ? sm_count / 4 : 1;
+  if (const char *e = getenv("FR_HOST_GRID")) {
+    const int v = atoi(e);
+    if (v >= 1 && v <= 65535) grid = v;
+  }
+  const int64_t need = (rows + kWarpRowThreads / 32 - 1) / (kWarpRowThreads / 32);
+  if (grid > need) grid = need;
+  void (*kern)(const uint16_t *, uint16_t *, int64_t, int64_t, int64_t, int64_t) =
+      nv == 1 ? softmax_bf16_warp_vec<1, true> : nv == 2 ? softmax_bf16_warp_vec<2, true>
+                                               : nv == 3 ? softmax_bf16_warp_vec<3, true>
+                                                         : softmax_bf16_warp_vec<4, true>;
+  return launch_k(kern, dim3(static_cast<unsigned>(grid)), dim3(kWarpRowThreads), 0, s, 0, x, y,
+                  rows, cols, cols, cols);
+}
 
 // Rows up to 2048 take one warp; longer rows in phase take one CTA of up to
 // 1024 threads x 2 vectors (32768 elements).

@@ -49,6 +49,34 @@ def test_host_pipeline_bf16_and_in_place(o):
     assert_bf16_within_steps(x2.view(torch.int16).numpy().view(np.uint16), ref, 1, "in place direct")
 
 
+@pytest.mark.parametrize("grid", [None, "1", "3", "1000"])
+@pytest.mark.parametrize("dtype,cols", [("f32", 100), ("f32", 257), ("f32", 600), ("f32", 1024),
+                                        ("bf16", 300), ("bf16", 513), ("bf16", 1500),
+                                        ("bf16", 2048)])
+def test_host_direct_small_grid(o, dtype, cols, grid, monkeypatch):
+    """The direct form's persistent grid (warps taking rows in turn): the
+    default (a quarter of the SMs), one CTA, three, and more CTAs than the
+    rows need; rows not a multiple of the grid's warps."""
+    if grid is not None:
+        monkeypatch.setenv("FR_HOST_GRID", grid)
+    rows = 1237
+    if dtype == "f32":
+        w = workloads.make(1, rows=rows, cols=cols, seed=8100 + cols)
+        x = torch.from_numpy(w.arrays["x"]).pin_memory()
+        y = fr.fr_softmax_host(x, chunk_rows=0)
+        torch.cuda.current_stream().synchronize()
+        assert_close(y.numpy(), o.softmax(w.arrays["x"]), "f32", f"direct {rows}x{cols} grid {grid}")
+    else:
+        bits = workloads.make_softmax_bf16(rows, cols, seed=8200 + cols).arrays["x"]
+        x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+        ref = o.softmax((bits.astype(np.uint32) << 16).view(np.float32))
+        y = fr.fr_softmax_host(x, chunk_rows=0)
+        torch.cuda.current_stream().synchronize()
+        assert_bf16_within_steps(y.view(torch.int16).numpy().view(np.uint16), ref, 1,
+                                 f"direct bf16 {rows}x{cols} grid {grid}")
+    assert fr.fr_last_form() == "persistent"
+
+
 def test_host_pipeline_orders_after_earlier_work_and_full_shape(o):
     """Work queued on the stream before the call (a copy into the pinned input)
     comes first; the softmax workload's shape, sampled rows against the oracle."""
