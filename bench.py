@@ -663,8 +663,8 @@ def xent_box(fr, workloads, dev, timed, args, peak):
 SWEEP_RAS_ROWS = (8, 32, 128, 512, 1024, 2048, 4096, 8192)
 SWEEP_RAS_COLS = (1024, 4096, 16384, 65536, 262144, 1048576, 4194304)
 SWEEP_SM_ROWS = (16, 64, 152, 304, 608, 1216, 2432, 4864, 16384)
-SWEEP_SM_COLS = (1025, 2048, 4097, 8192, 16384, 32768, 65537, 131072, 262144)
-SWEEP_OFFSET_COLS = (1025, 2048, 4097, 8192, 16384, 32768, 65537)
+SWEEP_SM_COLS = (1025, 2048, 4097, 8192, 16384, 32768, 65537, 131072, 262144, 393216)
+SWEEP_OFFSET_COLS = (1025, 2048, 4097, 8192, 16384, 32768, 65537, 131072)
 SWEEP_LN_COLS = (768, 1024, 1536, 2048, 2560, 3072, 4096, 5120, 6144, 7168, 8192, 10240, 12288,
                  14336, 16384, 20480, 24576, 32768, 65536)
 SWEEP_BYTES_MAX = 1 << 30  # largest input footprint of one call

@@ -449,6 +449,18 @@ __device__ __forceinline__ RowSplit row_split(const void *p, int64_t cols, int e
   return s;
 }
 
+// The 16 bytes from 2-byte half S (0 .. 7) of the 32 bytes a[0..3], b[0..3]:
+// a 16-byte chunk at one alignment cut from two chunks at another.
+template <int S>
+__device__ __forceinline__ uint4 cut_halves(const uint32_t (&a)[4], const uint32_t (&b)[4]) {
+  uint32_t c[8] = {a[0], a[1], a[2], a[3], b[0], b[1], b[2], b[3]};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    o[i] = (S & 1) ? __byte_perm(c[i + S / 2], c[i + S / 2 + 1], 0x5432) : c[i + S / 2];
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // ---- programmatic dependent launch ------------------------------------------
 // A kernel launched with launch_k may be placed on the SMs while the kernel
 // before it on the stream is finishing (its CTAs take the slots that kernel's

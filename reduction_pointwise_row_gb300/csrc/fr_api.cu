@@ -85,6 +85,15 @@ fr_status device_ok(fr::DevInfo *info) {
   return FR_OK;
 }
 
+// The split form of the softmax: a cluster per row with the slices in
+// registers where x and y rows are in phase and the row fits, else the
+// cluster that stages its slices in shared memory (FR_SOFTMAX_SPLIT=stage
+// pins the latter for every row).
+bool split_staged_pinned() {
+  const char *e = getenv("FR_SOFTMAX_SPLIT");
+  return e != nullptr && strcmp(e, "stage") == 0;
+}
+
 fr_status launched(cudaError_t e, fr_form form) {
   if (e != cudaSuccess) return FR_ERR_CUDA;
   g_last_form = form;
@@ -128,22 +137,32 @@ fr_form pick_ras(int64_t rows, int64_t cols, int sm_count, bool bf16 = false) {
 // 79.8; 64 rows: split 39.4, looped 60.6).  Rows out of phase (x and y at
 // different offsets within a 32-byte sector): a CTA per row up to 32768
 // columns (the row in registers up to 4608, staged in shared memory beyond),
-// looped beyond that.  Below 4 x SMs rows of 8192-16384 columns the two
+// then a cluster per row with its slices staged in shared memory (608 x
+// 65537: 72.7 us, looped 96.2; 608 x 131072: 148.7 against 191.4), looped past its reach.  Rows in phase past 262144
+// columns: the staged cluster below SMs rows (64 x 393216: 61.3 us, looped
+// 90.8; at 152 rows 130.3 against 114.2).  Below 4 x SMs rows of 8192-16384 columns the two
 // forms are within launch noise of each other (five sweeps, means: 304 x
 // 16384 CTA per row 12.2 us, looped 11.3; 152 x 16384 8.8 against 9.5; 608 x
 // 16384 16.7 against 20.3).
 fr_form pick_softmax(int64_t rows, int64_t cols, bool vec, int sm_count) {
   if (cols <= 1024) return FR_FORM_PERSISTENT;
-  if (!vec) return cols <= fr::softmax_persistent_max_cols(false) ? FR_FORM_PERSISTENT : FR_FORM_LOOPED;
+  if (!vec)
+    return cols <= fr::softmax_persistent_max_cols(false) ? FR_FORM_PERSISTENT
+           : cols <= fr::softmax_stage_split_max_cols(4)  ? FR_FORM_SPLIT
+                                                          : FR_FORM_LOOPED;
   if (cols <= 8192) return FR_FORM_PERSISTENT;
-  if (cols <= 131072 || (cols <= fr::softmax_split_max_cols() && rows < sm_count))
+  if (cols <= 131072 || (cols <= fr::softmax_stage_split_max_cols(4) && rows < sm_count))
     return FR_FORM_SPLIT;
   return FR_FORM_LOOPED;
 }
 
 // bf16 softmax.  Rows out of phase: up to 32768 columns a CTA per row, the row
 // staged in shared memory (16384 x 4097: 48.3 us, looped 87.8; 4864 x 32768:
-// 95.1 against 183.5), looped beyond.
+// 95.1 against 183.5), then a cluster per row with staged slices (608 x
+// 65537: 35.7 us, looped 67.7; 2432 x 65537: 119.2 against 206.9), looped
+// past its reach.  Rows in phase past 262144 columns: the staged cluster
+// below SMs rows (64 x 393216: 29.6 us, looped 50.9; at 152 rows 70.2
+// against 60.2).
 // Rows in phase: up to 2048 columns a warp per row, up to 8192
 // a CTA per row; at 16384 the looped form from 4 x SMs rows (608: looped 9.4
 // us, CTA per row 10.5), a CTA per row below, and a CTA per row again from 8
@@ -153,7 +172,10 @@ fr_form pick_softmax(int64_t rows, int64_t cols, bool vec, int sm_count) {
 // cluster per row (2432 x 32768: 50.2 us, looped 55.3, CTA per row 73.9).
 fr_form pick_softmax_bf16(int64_t rows, int64_t cols, bool vec, int sm_count) {
   if (cols <= 2048) return FR_FORM_PERSISTENT;
-  if (!vec) return cols <= 32768 ? FR_FORM_PERSISTENT : FR_FORM_LOOPED;
+  if (!vec)
+    return cols <= 32768                                 ? FR_FORM_PERSISTENT
+           : cols <= fr::softmax_stage_split_max_cols(2) ? FR_FORM_SPLIT
+                                                         : FR_FORM_LOOPED;
   if (cols <= 8192) return FR_FORM_PERSISTENT;
   if (cols <= 16384) {  // from 8 x SMs rows the persistent form stages rows in shared memory
     const int64_t sms = sm_count;
@@ -161,7 +183,8 @@ fr_form pick_softmax_bf16(int64_t rows, int64_t cols, bool vec, int sm_count) {
   }
   if (cols <= 32768 && rows <= sm_count) return FR_FORM_PERSISTENT;
   if (cols <= fr::softmax_bf16_split_max_cols()) return FR_FORM_SPLIT;
-  return FR_FORM_LOOPED;
+  return rows < sm_count && cols <= fr::softmax_stage_split_max_cols(2) ? FR_FORM_SPLIT
+                                                                         : FR_FORM_LOOPED;
 }
 
 // LayerNorm (bf16 rows of 256 MiB, back to back).  Rows of C x T x 32
@@ -341,10 +364,11 @@ fr_status fr_softmax(const void *x, void *y, int64_t rows, int64_t cols, int64_t
         return launched(fr::launch_softmax_bf16_looped(bx, by, rows, cols, ldx, ldy, vec,
                                                        info.sm_count, s), f);
       case FR_FORM_SPLIT:
-        if (!vec || cols <= 2048 || cols > fr::softmax_bf16_split_max_cols() ||
-            rows > 0x7fffffff / 8)
-          return FR_ERR_UNSUPPORTED_FORM;
-        return launched(fr::launch_softmax_bf16_split(bx, by, rows, cols, ldx, ldy, s), f);
+        if (cols <= 2048 || rows > 0x7fffffff / 8) return FR_ERR_UNSUPPORTED_FORM;
+        if (vec && cols <= fr::softmax_bf16_split_max_cols() && !split_staged_pinned())
+          return launched(fr::launch_softmax_bf16_split(bx, by, rows, cols, ldx, ldy, s), f);
+        if (cols > fr::softmax_stage_split_max_cols(2)) return FR_ERR_UNSUPPORTED_FORM;
+        return launched(fr::launch_softmax_split_staged(bx, by, rows, cols, ldx, ldy, 2, s), f);
       default: return FR_ERR_UNSUPPORTED_FORM;
     }
   }
@@ -369,9 +393,11 @@ fr_status fr_softmax(const void *x, void *y, int64_t rows, int64_t cols, int64_t
     case FR_FORM_LOOPED:
       return launched(fr::launch_softmax_looped(fx, fy, rows, cols, ldx, ldy, vec, info.sm_count, s), f);
     case FR_FORM_SPLIT:
-      if (!vec || cols <= 1024 || cols > fr::softmax_split_max_cols() || rows > 0x7fffffff / 8)
-        return FR_ERR_UNSUPPORTED_FORM;
-      return launched(fr::launch_softmax_split(fx, fy, rows, cols, ldx, ldy, s), f);
+      if (cols <= 1024 || rows > 0x7fffffff / 8) return FR_ERR_UNSUPPORTED_FORM;
+      if (vec && cols <= fr::softmax_split_max_cols() && !split_staged_pinned())
+        return launched(fr::launch_softmax_split(fx, fy, rows, cols, ldx, ldy, s), f);
+      if (cols > fr::softmax_stage_split_max_cols(4)) return FR_ERR_UNSUPPORTED_FORM;
+      return launched(fr::launch_softmax_split_staged(fx, fy, rows, cols, ldx, ldy, 4, s), f);
     default: return FR_ERR_UNSUPPORTED_FORM;
   }
 }

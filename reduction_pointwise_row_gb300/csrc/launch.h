@@ -53,6 +53,12 @@ cudaError_t launch_sumsq_split(const float *x, float *out, int64_t rows, int64_t
 // ---- softmax ---------------------------------------------------------------
 
 int64_t softmax_persistent_max_cols(bool vec);
+// Split form, the row staged in shared memory: a cluster of 2-8 CTAs per row
+// (any offsets of x and y; es = 4 for fp32, 2 for bf16 rows), up to
+// softmax_stage_split_max_cols(es) columns.
+int64_t softmax_stage_split_max_cols(int es);
+cudaError_t launch_softmax_split_staged(const void *x, void *y, int64_t rows, int64_t cols,
+                                        int64_t ldx, int64_t ldy, int es, cudaStream_t s);
 // fp32 rows of at most 1024 columns in host memory, x and y in phase, ld =
 // cols: the persistent form over a small grid (a quarter of the SMs' CTAs).
 cudaError_t launch_softmax_host_rows(const float *x, float *y, int64_t rows, int64_t cols,

@@ -185,17 +185,6 @@ softmax_bf16_cta_vec(const uint16_t *__restrict__ x, uint16_t *__restrict__ y, i
   if (si >= 0) st_stream_u16(py + si, to_bf16(se * inv));
 }
 
-// The 8 halves from half S of the 16 halves a[0..3], b[0..3].
-template <int S>
-__device__ __forceinline__ uint4 cut_halves(const uint32_t (&a)[4], const uint32_t (&b)[4]) {
-  uint32_t c[8] = {a[0], a[1], a[2], a[3], b[0], b[1], b[2], b[3]};
-  uint32_t o[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    o[i] = (S & 1) ? __byte_perm(c[i + S / 2], c[i + S / 2 + 1], 0x5432) : c[i + S / 2];
-  return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
 // y's value of a word of two raw x elements, packed to bf16
 __device__ __forceinline__ uint32_t softmax_word(uint32_t w, float mb, float inv) {
   return pack_bf16x2(ex2(fmaf(bf16_lo(w), kLog2e, -mb)) * inv,

@@ -1,0 +1,279 @@
+// Row softmax, split form with the row staged in shared memory ("Stax (4):
+// GPU Codegen and Dynamic Shapes", sections 9.4 and 9.5; "CMU 15-779
+// Lecture 8", section 3):
+//     m = max_r x,   y = exp(x - m) / sum_r exp(x - m),
+// for rows that neither a CTA nor a cluster holds in registers: rows whose x
+// and y sit at different offsets within a 16-byte chunk, and rows longer than
+// the register cluster's reach.  A thread-block cluster of C CTAs takes a
+// row; CTA q owns a run of y's 16-byte chunks and stages the x elements of
+// those chunks in its shared memory by 16-byte asynchronous copies at x's
+// alignment (the run's ragged ends element by element).  Each CTA reduces its
+// run to the pair (m_q, d_q) -- the max, then the sum of exponentials, both
+// over shared memory -- and pushes it into every CTA of the cluster with
+// st.async (counted on the receiver's mbarrier); once all C pairs are in, a
+// CTA merges them in rank order with the merge of section 9.5 (the same
+// (M, D) in every CTA) and writes its run of y: each 16-byte chunk cut from
+// two aligned chunks of shared memory by a shift the CTA shares, its
+// exponentials taken again (two ex2 per element in all, none kept).  One read
+// of x and one write of y.  The wait is bounded; on expiry the kernel records
+// FR_DEVERR_TIMEOUT and goes on.  fp32 and bf16 rows (fp32 arithmetic).
+#include <cstdlib>
+#include <cstring>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace fr {
+namespace {
+
+constexpr int kScMaxCluster = 8;
+constexpr long long kScWaitBudget = 1LL << 31;  // SM clocks (about one second)
+constexpr uint32_t kNegInfBf16x2 = 0xFF80FF80u;
+
+// Element type traits: a 16-byte chunk's max, its sum of 2^(x log2 e - mb),
+// and y's chunk for it; one element as fp32 and back.
+template <typename E>
+struct Chunk;
+
+template <>
+struct Chunk<float> {
+  static constexpr int kV = 4;
+  static __device__ __forceinline__ float max(uint4 r) {
+    return max_nan(max_nan(__uint_as_float(r.x), __uint_as_float(r.y)),
+                   max_nan(__uint_as_float(r.z), __uint_as_float(r.w)));
+  }
+  static __device__ __forceinline__ float sum(uint4 r, float mb) {
+    return (ex2(fmaf(__uint_as_float(r.x), kLog2e, -mb)) +
+            ex2(fmaf(__uint_as_float(r.y), kLog2e, -mb))) +
+           (ex2(fmaf(__uint_as_float(r.z), kLog2e, -mb)) +
+            ex2(fmaf(__uint_as_float(r.w), kLog2e, -mb)));
+  }
+  static __device__ __forceinline__ uint32_t out1(uint32_t w, float mb, float inv) {
+    return __float_as_uint(ex2(fmaf(__uint_as_float(w), kLog2e, -mb)) * inv);
+  }
+  static __device__ __forceinline__ uint4 out(uint4 r, float mb, float inv) {
+    return make_uint4(out1(r.x, mb, inv), out1(r.y, mb, inv), out1(r.z, mb, inv),
+                      out1(r.w, mb, inv));
+  }
+  static __device__ __forceinline__ float get(float v) { return v; }
+  static __device__ __forceinline__ float put(float v) { return v; }
+  static __device__ __forceinline__ float load1(const float *p) { return ld_stream_f32(p); }
+  static __device__ __forceinline__ void store1(float *p, float v) { st_stream_f32(p, v); }
+};
+
+template <>
+struct Chunk<uint16_t> {
+  static constexpr int kV = 8;
+  static __device__ __forceinline__ float max(uint4 r) {
+    const uint32_t m = max_nan_bf16x2(max_nan_bf16x2(r.x, r.y), max_nan_bf16x2(r.z, r.w));
+    return max_nan(bf16_lo(m), bf16_hi(m));
+  }
+  static __device__ __forceinline__ float sum2(uint32_t w, float mb) {
+    return ex2(fmaf(bf16_lo(w), kLog2e, -mb)) + ex2(fmaf(bf16_hi(w), kLog2e, -mb));
+  }
+  static __device__ __forceinline__ float sum(uint4 r, float mb) {
+    return (sum2(r.x, mb) + sum2(r.y, mb)) + (sum2(r.z, mb) + sum2(r.w, mb));
+  }
+  static __device__ __forceinline__ uint32_t out2(uint32_t w, float mb, float inv) {
+    return pack_bf16x2(ex2(fmaf(bf16_lo(w), kLog2e, -mb)) * inv,
+                       ex2(fmaf(bf16_hi(w), kLog2e, -mb)) * inv);
+  }
+  static __device__ __forceinline__ uint4 out(uint4 r, float mb, float inv) {
+    return make_uint4(out2(r.x, mb, inv), out2(r.y, mb, inv), out2(r.z, mb, inv),
+                      out2(r.w, mb, inv));
+  }
+  static __device__ __forceinline__ float get(uint16_t v) { return bf16_to_f32(v); }
+  static __device__ __forceinline__ uint16_t put(float v) { return to_bf16(v); }
+  static __device__ __forceinline__ uint16_t load1(const uint16_t *p) { return ld_stream_u16(p); }
+  static __device__ __forceinline__ void store1(uint16_t *p, uint16_t v) { st_stream_u16(p, v); }
+};
+
+// y's full chunks [cf, cl) of this CTA's run, chunk c at element V c - oy,
+// staged at srow[V c - oy - e_lo + ox]: sh (in 2-byte halves) past a 16-byte
+// boundary for every chunk.
+template <typename E, int SH>
+__device__ __forceinline__ void put_run(const E *srow, E *py, int cf, int cl, int oy, int e_lo,
+                                        int ox, float mb, float inv, int tid, int T) {
+  using K = Chunk<E>;
+  constexpr int V = K::kV, SE = SH * 2 / static_cast<int>(sizeof(E));  // shift in elements
+  for (int c = cf + tid; c < cl; c += T) {
+    const int p = V * c - oy - e_lo + ox - SE;  // 16-byte aligned
+    const uint4 *al = reinterpret_cast<const uint4 *>(srow + p);
+    uint4 r = al[0];
+    if constexpr (SH > 0) {
+      const uint4 ra = al[0], rb = al[1];
+      const uint32_t a[4] = {ra.x, ra.y, ra.z, ra.w}, b[4] = {rb.x, rb.y, rb.z, rb.w};
+      r = cut_halves<SH>(a, b);
+    }
+    st_stream_u4(py + (V * c - oy), K::out(r, mb, inv));
+  }
+}
+
+template <typename E, int T>
+__global__ void __launch_bounds__(T)
+softmax_cluster_stage(const E *__restrict__ x, E *__restrict__ y, int64_t cols, int64_t ldx,
+                      int64_t ldy, int *__restrict__ err) {
+  pdl_enter();
+  using K = Chunk<E>;
+  constexpr int V = K::kV, ES = static_cast<int>(sizeof(E)), W = T / 32;
+  extern __shared__ __align__(16) unsigned char sraw[];
+  E *srow = reinterpret_cast<E *>(sraw);
+  __shared__ float red[2][W];
+  __shared__ __align__(16) float4 pairs[kScMaxCluster];
+  __shared__ __align__(8) uint64_t xbar;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t C = cluster_nctarank(), q = cluster_ctarank();
+  if (tid == 0) {
+    mbar_init(&xbar, 1);
+    mbar_init_fence();
+    mbar_arrive_expect_tx(&xbar, 16u * C);
+  }
+  __syncthreads();
+  cluster_arrive_relaxed();  // this CTA's mbarrier is ready for the peers' pairs
+  const int64_t row = cluster_id_x();
+  const E *px = x + row * ldx;
+  E *py = y + row * ldy;
+  const int n = static_cast<int>(cols);
+  // y's chunks: chunk c holds elements V c - oy .. V c - oy + V - 1 (those in
+  // the row); CTA q owns chunks [c0, c1) and so elements [e_lo, e_hi)
+  const int oy = static_cast<int>((reinterpret_cast<uintptr_t>(py) & 15) / ES);
+  const int ny = (n + oy + V - 1) / V;
+  const int kc = (ny + static_cast<int>(C) - 1) / static_cast<int>(C);
+  const int c0 = min(ny, static_cast<int>(q) * kc), c1 = min(ny, c0 + kc);
+  const int e_lo = c0 < c1 ? max(0, V * c0 - oy) : 0;
+  const int e_hi = c0 < c1 ? min(n, V * c1 - oy) : 0;
+  const int nl = e_hi - e_lo;
+  // stage x[e_lo, e_hi): hx elements up to x's 16-byte boundary, whole
+  // chunks, the rest; element e at srow[e - e_lo + ox], x's chunks 16-byte
+  // aligned in shared memory
+  const E *pl = px + e_lo;
+  const int hx = min(nl, static_cast<int>(((16 - (reinterpret_cast<uintptr_t>(pl) & 15)) & 15) / ES));
+  const int ox = (V - hx % V) % V;
+  const int ncx = (nl - hx) / V;
+  const uint64_t policy = l2_evict_first_policy();
+  for (int c = tid; c < ncx; c += T) cp_async_16_hint(srow + ox + hx + V * c, pl + hx + V * c, policy);
+  cp_async_commit();
+  const int tx0 = hx + V * ncx;
+  if (tid < hx) srow[ox + tid] = K::load1(pl + tid);
+  if (tid < nl - tx0) srow[ox + tx0 + tid] = K::load1(pl + tx0 + tid);
+  cp_async_wait<0>();
+  __syncthreads();
+
+  const uint4 *body = reinterpret_cast<const uint4 *>(srow + ox + hx);
+  float m = -INFINITY;
+  for (int c = tid; c < ncx; c += T) m = max_nan(m, K::max(body[c]));
+  if (tid < hx) m = max_nan(m, K::get(srow[ox + tid]));
+  if (tid < nl - tx0) m = max_nan(m, K::get(srow[ox + tx0 + tid]));
+  m = warp_max_nan(m);
+  if (lane == 0) red[0][warp] = m;
+  __syncthreads();
+  m = warp_max_nan(lane < W ? red[0][lane] : -INFINITY);
+  // a run of nothing but -inf (or of nothing) contributes d = 0
+  const float mq = m == -INFINITY ? 0.0f : m * kLog2e;
+  float d = 0.0f;
+  for (int c = tid; c < ncx; c += T) d += K::sum(body[c], mq);
+  if (tid < hx) d += ex2(fmaf(K::get(srow[ox + tid]), kLog2e, -mq));
+  if (tid < nl - tx0) d += ex2(fmaf(K::get(srow[ox + tx0 + tid]), kLog2e, -mq));
+  d = warp_sum(d);
+  if (lane == 0) red[1][warp] = d;
+  __syncthreads();
+  d = warp_sum(lane < W ? red[1][lane] : 0.0f);
+  cluster_wait();  // every peer's mbarrier is initialised
+  if (tid < static_cast<int>(C))
+    st_async_f4(&pairs[q], &xbar, static_cast<uint32_t>(tid), make_float4(m, d, 0.0f, 0.0f));
+  if (!mbar_wait_bounded(&xbar, 0, kScWaitBudget) && tid == 0) atomicCAS(err, 0, FR_DEVERR_TIMEOUT);
+  // the C pairs merged in rank order: the same (M, D) in every CTA
+  float M = -INFINITY;
+  for (uint32_t r = 0; r < C; ++r) M = max_nan(M, pairs[r].x);
+  float D = 0.0f;
+  if (M != -INFINITY)
+    for (uint32_t r = 0; r < C; ++r) D += pairs[r].y * ex2((pairs[r].x - M) * kLog2e);
+  const float mb = M * kLog2e, inv = __frcp_rn(D);
+
+  // y: the run's full 16-byte chunks, then its ragged ends element by element
+  const int cf = c0 + ((c0 == 0 && oy > 0) ? 1 : 0);
+  const int cl = (c1 > c0 && V * c1 - oy > n) ? c1 - 1 : c1;
+  int fl = e_hi, fh = e_hi;  // the full chunks' elements
+  if (cl > cf) {
+    fl = V * cf - oy;
+    fh = V * cl - oy;
+    const int sh = ((V * cf - oy - e_lo + ox) % V) * ES / 2;  // in 2-byte halves
+    switch (sh) {  // uniform: one branch for the whole CTA
+      case 0: put_run<E, 0>(srow, py, cf, cl, oy, e_lo, ox, mb, inv, tid, T); break;
+      case 1: put_run<E, 1>(srow, py, cf, cl, oy, e_lo, ox, mb, inv, tid, T); break;
+      case 2: put_run<E, 2>(srow, py, cf, cl, oy, e_lo, ox, mb, inv, tid, T); break;
+      case 3: put_run<E, 3>(srow, py, cf, cl, oy, e_lo, ox, mb, inv, tid, T); break;
+      case 4: put_run<E, 4>(srow, py, cf, cl, oy, e_lo, ox, mb, inv, tid, T); break;
+      case 5: put_run<E, 5>(srow, py, cf, cl, oy, e_lo, ox, mb, inv, tid, T); break;
+      case 6: put_run<E, 6>(srow, py, cf, cl, oy, e_lo, ox, mb, inv, tid, T); break;
+      default: put_run<E, 7>(srow, py, cf, cl, oy, e_lo, ox, mb, inv, tid, T); break;
+    }
+  }
+  const int nfront = min(fl, e_hi) - e_lo, nback = e_hi - max(fh, e_lo);
+  auto scalar_y = [&](int e) {
+    K::store1(py + e, K::put(ex2(fmaf(K::get(srow[e - e_lo + ox]), kLog2e, -mb)) * inv));
+  };
+  if (tid < nfront) scalar_y(e_lo + tid);
+  else if (tid >= 32 && tid - 32 < nback && fh < e_hi) scalar_y(max(fh, e_lo) + tid - 32);
+}
+
+template <typename E, int T>
+cudaError_t launch_stage_t(const E *x, E *y, int64_t rows, int64_t cols, int64_t ldx,
+                           int64_t ldy, int C, size_t smem, cudaStream_t s) {
+  int *err = nullptr;
+  cudaError_t e = device_error_word(&err);
+  if (e != cudaSuccess) return e;
+  e = set_smem_limit(reinterpret_cast<const void *>(softmax_cluster_stage<E, T>), smem);
+  if (e != cudaSuccess) return e;
+  return launch_k(softmax_cluster_stage<E, T>, dim3(static_cast<unsigned>(rows * C)), dim3(T),
+                  smem, s, static_cast<unsigned>(C), x, y, cols, ldx, ldy, err);
+}
+
+// The cluster for a row: the fewest CTAs (2, 4 or 8) whose runs take at most
+// 96 KiB of shared memory each (two CTAs an SM), else 8 CTAs of up to 200 KiB
+// (one an SM); 512 threads for runs past 64 KiB, 256 below.
+bool stage_shape(int64_t cols, int es, int *C, size_t *smem, int *T) {
+  const int v = 16 / es;
+  for (int pass = 0; pass < 2; ++pass)
+    for (int c = 2; c <= kScMaxCluster; c <<= 1) {
+      const int64_t ny = (cols + v - 1) / v + 1;  // chunks at the largest offset
+      const int64_t kc = (ny + c - 1) / c;
+      const size_t bytes = static_cast<size_t>((kc + 3) * v) * es;  // run + shift + padding
+      if (bytes <= (pass == 0 ? (96u << 10) : (200u << 10))) {
+        *C = c;
+        *smem = (bytes + 15) / 16 * 16;
+        *T = bytes > (64u << 10) ? 512 : 256;
+        return true;
+      }
+    }
+  return false;
+}
+
+}  // namespace
+
+int64_t softmax_stage_split_max_cols(int es) {
+  // the longest row stage_shape takes (200 KiB runs over 8 CTAs, less the
+  // chunks of shift and padding)
+  const int v = 16 / es;
+  return (static_cast<int64_t>((200u << 10) / es / v) - 3) * kScMaxCluster * v - 2 * v;
+}
+
+cudaError_t launch_softmax_split_staged(const void *x, void *y, int64_t rows, int64_t cols,
+                                        int64_t ldx, int64_t ldy, int es, cudaStream_t s) {
+  int C = 0, T = 0;
+  size_t smem = 0;
+  if (!stage_shape(cols, es, &C, &smem, &T) || rows * C > 0x7fffffff || cols > 0x7fffffff)
+    return cudaErrorInvalidValue;
+  if (es == 4) {
+    const float *fx = static_cast<const float *>(x);
+    float *fy = static_cast<float *>(y);
+    return T == 512 ? launch_stage_t<float, 512>(fx, fy, rows, cols, ldx, ldy, C, smem, s)
+                    : launch_stage_t<float, 256>(fx, fy, rows, cols, ldx, ldy, C, smem, s);
+  }
+  const uint16_t *bx = static_cast<const uint16_t *>(x);
+  uint16_t *by = static_cast<uint16_t *>(y);
+  return T == 512 ? launch_stage_t<uint16_t, 512>(bx, by, rows, cols, ldx, ldy, C, smem, s)
+                  : launch_stage_t<uint16_t, 256>(bx, by, rows, cols, ldx, ldy, C, smem, s);
+}
+
+}  // namespace fr

@@ -23,6 +23,9 @@ COLS = [1, 2, 3, 7, 13, 31, 33, 127, 128, 129, 781, 1000, 1023, 1024, 1025, 4097
 LAYOUTS = [(0, 0, 0), (1, 1, 5), (0, 3, 0)]
 
 
+STAGE_SPLIT_MAX_F32 = 409496  # the staged split's longest fp32 row
+
+
 @pytest.fixture(scope="module")
 def o():
     return oracle.get()
@@ -31,11 +34,12 @@ def o():
 def forms_for(op, cols, in_phase=True):
     if op == "relu_add_sum":
         return (["persistent"] if cols <= 1024 else []) + ["looped", "split"]
-    if op == "softmax":  # rows past 1024 stay persistent (a CTA per row, the row in
-        # registers in phase, in shared memory out of phase) up to 32768 columns;
-        # in phase they also split over a cluster of CTAs
+    if op == "softmax":  # rows past 1024 stay persistent (a CTA per row) up to 32768
+        # columns; they also split over a cluster of CTAs (the slices in
+        # registers in phase up to 262144 columns, else staged in shared
+        # memory, up to 409496)
         return ((["persistent"] if cols <= 32768 else []) +
-                (["split"] if in_phase and 1024 < cols <= 262144 else []) + ["looped"])
+                (["split"] if 1024 < cols <= STAGE_SPLIT_MAX_F32 else []) + ["looped"])
     raise ValueError(op)
 
 
@@ -230,6 +234,37 @@ def test_softmax_special_values(o, cols):
             got = run_softmax(x, form, layout)
             assert_close(got, ref, "f32", f"{form} special {cols} {layout}")
             assert np.isnan(got[[1, 3, 4]]).all() and np.isfinite(got[[0, 2, 5]]).all()
+
+
+@pytest.mark.parametrize("cols", [1025, 8193, 40000, 65537, 262145, 409496])
+@pytest.mark.parametrize("layout", [(0, 0, 0), (1, 0, 3), (2, 7, 1), (4, 0, 1)])
+@pytest.mark.parametrize("pin", [None, "stage"])
+def test_softmax_split_staged(o, cols, layout, pin, monkeypatch):
+    """The split form with the slices staged in shared memory: rows out of
+    phase, rows past the register cluster's reach (262144), and with
+    FR_SOFTMAX_SPLIT=stage rows in phase too; 2-8 CTAs a cluster by length."""
+    if pin:
+        monkeypatch.setenv("FR_SOFTMAX_SPLIT", pin)
+    rows = 3 if cols > 100000 else 7
+    w = workloads.make(1, rows=rows, cols=cols, seed=2950 + cols)
+    ref = o.softmax(w.arrays["x"])
+    assert_close(run_softmax(w.arrays["x"], "split", layout), ref, "f32",
+                 f"staged split {rows}x{cols} {layout} {pin}")
+    assert fr.fr_check_device_error() == 0
+
+
+@pytest.mark.parametrize("cols", [1025, 40000, 65537])
+def test_softmax_split_staged_special_values(o, cols):
+    x = workloads.make(1, rows=6, cols=cols, seed=71).arrays["x"].copy()
+    x[1, cols // 2] = np.nan                 # NaN row
+    x[2, : cols // 2] = -np.inf              # partly -inf (whole slices of it)
+    x[3, :] = -np.inf                        # all -inf: 0/0
+    x[4, cols - 1] = np.inf                  # +inf: inf - inf
+    ref = o.softmax(x)
+    for layout in ((0, 0, 0), (1, 0, 3)):
+        got = run_softmax(x, "split", layout)
+        assert_close(got, ref, "f32", f"staged split special {cols} {layout}")
+        assert np.isnan(got[[1, 3, 4]]).all() and np.isfinite(got[[0, 2, 5]]).all()
 
 
 @pytest.mark.parametrize("cols", [1025, 8193, 32769, 65537, 131071, 262144])
@@ -581,15 +616,16 @@ def test_error_statuses_on_device():
     with pytest.raises(fr.FRError) as e:  # short enough for one warp: no split
         fr.fr_softmax(torch.zeros(4, 1000, device="cuda"), form="split")
     assert e.value.status == 3
-    with pytest.raises(fr.FRError) as e:  # longer than a cluster holds
-        fr.fr_softmax(torch.zeros(2, 262145, device="cuda"), form="split")
+    with pytest.raises(fr.FRError) as e:  # longer than a cluster holds, even staged
+        fr.fr_softmax(torch.zeros(2, STAGE_SPLIT_MAX_F32 + 1, device="cuda"), form="split")
     assert e.value.status == 3
     buf = torch.zeros(4 * 2001 + 3, device="cuda")  # x and y rows out of 32-byte phase
     xs = buf[:4 * 2001].view(4, 2001)[:, :2000]
     ys = torch.empty(4 * 2000 + 3, device="cuda")[3:].view(4, 2000)
-    with pytest.raises(fr.FRError) as e:  # the cluster form pairs x's vectors with y's
-        fr.fr_softmax(xs, form="split", out=ys)
-    assert e.value.status == 3
+    fr.fr_softmax(xs, form="split", out=ys)  # a cluster per row, staged
+    assert fr.fr_last_form() == "split"
+    torch.cuda.synchronize()
+    assert torch.allclose(ys, torch.full_like(ys, 1.0 / 2000))
     fr.fr_softmax(xs, form="persistent", out=ys)  # the row in registers, shifted
     assert fr.fr_last_form() == "persistent"
     torch.cuda.synchronize()
@@ -635,5 +671,8 @@ def test_auto_form_choices():
     fr.fr_softmax(x)
     assert fr.fr_last_form() == "split"
     x = torch.zeros(2, 300000, device="cuda")
+    fr.fr_softmax(x)
+    assert fr.fr_last_form() == "split"  # past the registers' reach: a cluster, staged
+    x = torch.zeros(2, STAGE_SPLIT_MAX_F32 + 1, device="cuda")
     fr.fr_softmax(x)
     assert fr.fr_last_form() == "looped"  # longer than a cluster holds

@@ -35,7 +35,7 @@ def forms(cols, layout=(0, 0, 0)):
     phase)"""
     in_phase = (layout[0] - layout[1]) * 2 % 32 == 0
     persistent = cols <= 32768
-    split = in_phase and 2048 < cols <= 262144  # a cluster of CTAs per row
+    split = 2048 < cols <= 818992  # a cluster of CTAs per row (staged out of phase)
     return (["persistent"] if persistent else []) + (["split"] if split else []) + ["looped", "auto"]
 
 
@@ -108,6 +108,18 @@ def test_softmax_bf16_many_long_rows_auto(o):
     assert fr.fr_last_form() == fr.fr_auto_form("softmax", rows, cols, "bf16", fr.sm_count())
     for sl in (slice(0, 32), slice(rows - 32, rows)):
         assert_bf16_within_steps(got[sl], o.softmax(widen(bits[sl])), 1, f"auto {rows}x{cols}")
+
+
+@pytest.mark.parametrize("cols", [2049, 65537, 300001, 818992])
+@pytest.mark.parametrize("layout", [(0, 0, 0), (1, 0, 3), (0, 5, 0), (8, 0, 0)])
+def test_softmax_bf16_split_staged(o, cols, layout, monkeypatch):
+    """The split form with bf16 slices staged in shared memory (pinned in
+    phase; out of phase and past 262144 columns it is the split form)."""
+    monkeypatch.setenv("FR_SOFTMAX_SPLIT", "stage")
+    rows = 2 if cols > 100000 else 7
+    bits = workloads.make_softmax_bf16(rows, cols, seed=7000 + cols).arrays["x"]
+    ref = o.softmax(widen(bits))
+    assert_bf16_within_steps(run(bits, "split", layout), ref, 1, f"staged {rows}x{cols} {layout}")
 
 
 @pytest.mark.parametrize("cols", [7, 1000, 2048, 4097, 20000])
