@@ -58,6 +58,7 @@ def parse():
                                       "softmax_bf16_4097", "softmax_bf16_4097_looped",
                                       "softmax_bf16_65537", "xent_box", "form_sweep",
                                       "softmax_4097_offset", "softmax_bf16_8192_offset",
+                                      "softmax_65537_offset",
                                       *[f"layernorm_{c}" for c in LN_HIDDEN]],
                    help="time one workload alone (for profiler captures) and exit")
     p.add_argument("--form", default="auto", choices=["auto", "persistent", "looped", "split"],
@@ -432,6 +433,18 @@ def setup_workload(name, fr, workloads, dev, form="auto"):
             x = to_device(w.arrays["x"], dev)
             y = torch.empty_like(x)
             calls.append(lambda x=x, y=y: fr.fr_softmax(x, out=y, form=f))
+        return calls, "softmax", w.rows, w.cols, 1
+    if name == "softmax_65537_offset":
+        # rows of 65537 with x one element past y's phase (511 rows, 128 MiB
+        # of x): the split form stages each CTA's run in shared memory
+        w = make_shard(workloads, 1, rows=(1 << 25) // 65537, cols=65537)
+        n = w.rows * w.cols
+        for _ in range(nsets("softmax", w.rows, w.cols)):
+            flat = torch.empty(n + 8, device=dev)
+            flat[1:n + 1].copy_(torch.from_numpy(w.arrays["x"].reshape(-1)))
+            x = flat[1:n + 1].view(w.rows, w.cols)
+            y = torch.empty(w.rows, w.cols, device=dev)
+            calls.append(lambda x=x, y=y, flat=flat: fr.fr_softmax(x, out=y, form=form))
         return calls, "softmax", w.rows, w.cols, 1
     if name == "softmax_4097_offset":
         # rows of 4097 with x one element past y's 32-byte phase (8190 rows,

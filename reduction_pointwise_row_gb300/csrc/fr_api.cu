@@ -138,7 +138,7 @@ fr_form pick_ras(int64_t rows, int64_t cols, int sm_count, bool bf16 = false) {
 // different offsets within a 32-byte sector): a CTA per row up to 32768
 // columns (the row in registers up to 4608, staged in shared memory beyond),
 // then a cluster per row with its slices staged in shared memory (608 x
-// 65537: 72.7 us, looped 96.2; 608 x 131072: 148.7 against 191.4), looped past its reach.  Rows in phase past 262144
+// 65537: 62.6 us, looped 96.2; 608 x 131072: 148.0 against 191.4), looped past its reach.  Rows in phase past 262144
 // columns: the staged cluster below SMs rows (64 x 393216: 61.3 us, looped
 // 90.8; at 152 rows 130.3 against 114.2).  Below 4 x SMs rows of 8192-16384 columns the two
 // forms are within launch noise of each other (five sweeps, means: 304 x
@@ -146,10 +146,12 @@ fr_form pick_ras(int64_t rows, int64_t cols, int sm_count, bool bf16 = false) {
 // 16384 16.7 against 20.3).
 fr_form pick_softmax(int64_t rows, int64_t cols, bool vec, int sm_count) {
   if (cols <= 1024) return FR_FORM_PERSISTENT;
-  if (!vec)
-    return cols <= fr::softmax_persistent_max_cols(false) ? FR_FORM_PERSISTENT
-           : cols <= fr::softmax_stage_split_max_cols(4)  ? FR_FORM_SPLIT
-                                                          : FR_FORM_LOOPED;
+  if (!vec) {  // (with under SMs / 4 rows of 16385 .. 32768 columns the cluster
+              // spreads a row over more SMs: 16 x 32768 6.3-7.1 us, a CTA per row 7.6)
+    if (cols <= fr::softmax_persistent_max_cols(false))
+      return cols > 16384 && rows * 4 < sm_count ? FR_FORM_SPLIT : FR_FORM_PERSISTENT;
+    return cols <= fr::softmax_stage_split_max_cols(4) ? FR_FORM_SPLIT : FR_FORM_LOOPED;
+  }
   if (cols <= 8192) return FR_FORM_PERSISTENT;
   if (cols <= 131072 || (cols <= fr::softmax_stage_split_max_cols(4) && rows < sm_count))
     return FR_FORM_SPLIT;
@@ -159,10 +161,10 @@ fr_form pick_softmax(int64_t rows, int64_t cols, bool vec, int sm_count) {
 // bf16 softmax.  Rows out of phase: up to 32768 columns a CTA per row, the row
 // staged in shared memory (16384 x 4097: 48.3 us, looped 87.8; 4864 x 32768:
 // 95.1 against 183.5), then a cluster per row with staged slices (608 x
-// 65537: 35.7 us, looped 67.7; 2432 x 65537: 119.2 against 206.9), looped
+// 65537: 32.9 us, looped 67.7; 2432 x 65537: 108.3 against 206.9), looped
 // past its reach.  Rows in phase past 262144 columns: the staged cluster
-// below SMs rows (64 x 393216: 29.6 us, looped 50.9; at 152 rows 70.2
-// against 60.2).
+// (393216: 64 rows 27.1 us, looped 50.9; 608 rows 183.3 against 222.9), past
+// 393216 columns (runs over 100 KiB, one CTA an SM) only below SMs rows.
 // Rows in phase: up to 2048 columns a warp per row, up to 8192
 // a CTA per row; at 16384 the looped form from 4 x SMs rows (608: looped 9.4
 // us, CTA per row 10.5), a CTA per row below, and a CTA per row again from 8
@@ -183,8 +185,11 @@ fr_form pick_softmax_bf16(int64_t rows, int64_t cols, bool vec, int sm_count) {
   }
   if (cols <= 32768 && rows <= sm_count) return FR_FORM_PERSISTENT;
   if (cols <= fr::softmax_bf16_split_max_cols()) return FR_FORM_SPLIT;
-  return rows < sm_count && cols <= fr::softmax_stage_split_max_cols(2) ? FR_FORM_SPLIT
-                                                                         : FR_FORM_LOOPED;
+  // past the registers' reach the staged cluster: up to 393216 columns (runs
+  // under 100 KiB, two CTAs an SM) at any row count, longer rows below SMs rows
+  return (cols <= 393216 || rows < sm_count) && cols <= fr::softmax_stage_split_max_cols(2)
+             ? FR_FORM_SPLIT
+             : FR_FORM_LOOPED;
 }
 
 // LayerNorm (bf16 rows of 256 MiB, back to back).  Rows of C x T x 32

@@ -230,22 +230,30 @@ cudaError_t launch_stage_t(const E *x, E *y, int64_t rows, int64_t cols, int64_t
 }
 
 // The cluster for a row: the fewest CTAs (2, 4 or 8) whose runs take at most
-// 96 KiB of shared memory each (two CTAs an SM), else 8 CTAs of up to 200 KiB
-// (one an SM); 512 threads for runs past 64 KiB, 256 below.
+// 48 KiB of shared memory each, else 8 CTAs with runs of up to 200 KiB; 512
+// threads for runs past 64 KiB, 256 below.  Measured on GB300 (us per call,
+// runs of at most 96 / 48 / 32 KiB): fp32 out of phase 608 x 32769 38.8 /
+// 33.6 / 42.1, 608 x 65537 73.1 / 62.6 / 83.2, 2432 x 32769 132.0 / 114.1 /
+// 152.1; bf16 2432 x 65537 119.5 / 108.3 / 136.4 -- runs of about 32 KiB,
+// four to seven CTAs an SM.  FR_STAGE_RUN_KB=<KiB> sets the bound.
 bool stage_shape(int64_t cols, int es, int *C, size_t *smem, int *T) {
   const int v = 16 / es;
-  for (int pass = 0; pass < 2; ++pass)
-    for (int c = 2; c <= kScMaxCluster; c <<= 1) {
-      const int64_t ny = (cols + v - 1) / v + 1;  // chunks at the largest offset
-      const int64_t kc = (ny + c - 1) / c;
-      const size_t bytes = static_cast<size_t>((kc + 3) * v) * es;  // run + shift + padding
-      if (bytes <= (pass == 0 ? (96u << 10) : (200u << 10))) {
-        *C = c;
-        *smem = (bytes + 15) / 16 * 16;
-        *T = bytes > (64u << 10) ? 512 : 256;
-        return true;
-      }
+  size_t target = 48u << 10;
+  if (const char *e = getenv("FR_STAGE_RUN_KB")) {
+    const int kb = atoi(e);
+    if (kb >= 4 && kb <= 200) target = static_cast<size_t>(kb) << 10;
+  }
+  const int64_t ny = (cols + v - 1) / v + 1;  // y's chunks at the largest offset
+  for (int c = 2; c <= kScMaxCluster; c <<= 1) {
+    const int64_t kc = (ny + c - 1) / c;
+    const size_t bytes = static_cast<size_t>((kc + 3) * v) * es;  // run + shift + padding
+    if (bytes <= target || (c == kScMaxCluster && bytes <= (200u << 10))) {
+      *C = c;
+      *smem = (bytes + 15) / 16 * 16;
+      *T = bytes > (64u << 10) ? 512 : 256;
+      return true;
     }
+  }
   return false;
 }
 
