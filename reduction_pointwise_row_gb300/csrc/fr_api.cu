@@ -146,10 +146,14 @@ fr_form pick_ras(int64_t rows, int64_t cols, int sm_count, bool bf16 = false) {
 // 16384 16.7 against 20.3).
 fr_form pick_softmax(int64_t rows, int64_t cols, bool vec, int sm_count) {
   if (cols <= 1024) return FR_FORM_PERSISTENT;
-  if (!vec) {  // (with under SMs / 4 rows of 16385 .. 32768 columns the cluster
-              // spreads a row over more SMs: 16 x 32768 6.3-7.1 us, a CTA per row 7.6)
+  if (!vec) {  // rows of 16385 .. 32768 columns: a staged cluster per row under SMs / 4
+              // rows (16 x 32768: 6.5 us, a CTA per row 7.6) and from 4 x SMs rows (its
+              // 32 KiB runs against the CTA's 128 KiB, one an SM: 2432 x 32768 121.4
+              // against 126.1), a CTA per row between (304 x 32768: 20.2 against 21.1)
+    const int64_t sms = sm_count;
     if (cols <= fr::softmax_persistent_max_cols(false))
-      return cols > 16384 && rows * 4 < sm_count ? FR_FORM_SPLIT : FR_FORM_PERSISTENT;
+      return cols > 16384 && (rows * 4 < sms || rows >= 4 * sms) ? FR_FORM_SPLIT
+                                                                 : FR_FORM_PERSISTENT;
     return cols <= fr::softmax_stage_split_max_cols(4) ? FR_FORM_SPLIT : FR_FORM_LOOPED;
   }
   if (cols <= 8192) return FR_FORM_PERSISTENT;

@@ -49,14 +49,16 @@ def test_table_covers_every_op_and_the_forms():
 def test_rules_name_the_form_auto_took():
     """fr_auto_form answers for rows in phase; rows out of phase take the
     persistent form up to 32768 columns (fp32 rows past 16384 columns, fewer
-    than SMs / 4 of them: the split form), then the split form (a cluster
-    per row, staged) up to 409496 fp32 / 818992 bf16 columns, looped beyond."""
+    than SMs / 4 or at least 4 x SMs of them: the split form), then the split
+    form (a cluster per row, staged) up to 409496 fp32 / 818992 bf16 columns,
+    looped beyond."""
     import reduction_pointwise_row_gb300 as fr
     sms, rows = table_rows()
     for r in rows:
         if r["op"] == OUT_OF_PHASE:
             reach = 409496 if r["dtype"] == "f32" else 818992
-            few = r["dtype"] == "f32" and r["cols"] > 16384 and r["rows"] * 4 < sms
+            few = (r["dtype"] == "f32" and r["cols"] > 16384 and
+                   (r["rows"] * 4 < sms or r["rows"] >= 4 * sms))
             want = ("split" if few and r["cols"] <= 32768 else
                     "persistent" if r["cols"] <= 32768 else
                     "split" if r["cols"] <= reach else "looped")
