@@ -606,7 +606,11 @@ EXTRA = {"relu_add_sum": "relu_add_sum_64x128", "layernorm": "layernorm_4096x327
          "xent_f32": "xent_f32_8192x50257", "looped_bf16": "relu_add_sum_bf16_looped_16384x16384",
          "softmax_bf16_4097": "softmax_bf16_16380x4097",
          "softmax_bf16_4097_looped": "softmax_bf16_looped_16380x4097",
-         "softmax_bf16_65537": "softmax_bf16_1022x65537"}
+         "softmax_bf16_65537": "softmax_bf16_1022x65537",
+         "softmax_4097_offset": "softmax_offset_8190x4097",
+         "softmax_65537_offset": "softmax_offset_511x65537",
+         "softmax_bf16_8192_offset": "softmax_bf16_offset_8192x8192",
+         "layernorm_768": "layernorm_174762x768", "layernorm_6144": "layernorm_21845x6144"}
 
 
 def extra_configs(fr, traffic, workloads, timed, dev, peak, args, world, names=None,
