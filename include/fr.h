@@ -200,10 +200,10 @@ fr_status fr_softmax(const void *x, void *y, int64_t rows, int64_t cols, int64_t
  *   direct (chunk_rows = 0): the softmax kernel itself reads x_host and writes
  *     y_host where they are, over the host link (NVLink-C2C on GB300, which
  *     keeps the GPU coherent with host memory); no staging, no workspace.
- *     fp32 rows of up to 1024 columns take a small grid (a quarter of the
- *     SMs' CTAs, warps taking rows in turn): the link serves a bounded number
- *     of requests in flight best (340 GB/s both ways against 304 with a warp
- *     for every row at once).
+ *     fp32 rows of up to 1024 columns and bf16 rows of up to 2048 take a
+ *     small grid (a quarter of the SMs' CTAs, warps taking rows in turn): the
+ *     link serves a bounded number of requests in flight best (fp32: 340 GB/s
+ *     both ways against 304 with a warp for every row at once).
  *   staged (chunk_rows >= 1): the rows go to the device in chunks of
  *     `chunk_rows`, through three device staging slots each way (the caller's
  *     workspace), and come back the same way, with a chunk's copy in, the
