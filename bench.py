@@ -58,7 +58,7 @@ def parse():
                                       "softmax_bf16_4097", "softmax_bf16_4097_looped",
                                       "softmax_bf16_65537", "xent_box", "form_sweep",
                                       "softmax_4097_offset", "softmax_bf16_8192_offset",
-                                      "softmax_65537_offset",
+                                      "softmax_65537_offset", "softmax_8192_offset",
                                       *[f"layernorm_{c}" for c in LN_HIDDEN]],
                    help="time one workload alone (for profiler captures) and exit")
     p.add_argument("--form", default="auto", choices=["auto", "persistent", "looped", "split"],
@@ -434,6 +434,18 @@ def setup_workload(name, fr, workloads, dev, form="auto"):
             y = torch.empty_like(x)
             calls.append(lambda x=x, y=y: fr.fr_softmax(x, out=y, form=f))
         return calls, "softmax", w.rows, w.cols, 1
+    if name == "softmax_8192_offset":
+        # rows of 8192 with x one element past y's phase (4096 rows, 128 MiB
+        # of x): the persistent form stages each row in shared memory
+        w = make_shard(workloads, 1, rows=(1 << 25) // 8192, cols=8192)
+        n = w.rows * w.cols
+        for _ in range(nsets("softmax", w.rows, w.cols)):
+            flat = torch.empty(n + 8, device=dev)
+            flat[1:n + 1].copy_(torch.from_numpy(w.arrays["x"].reshape(-1)))
+            x = flat[1:n + 1].view(w.rows, w.cols)
+            y = torch.empty(w.rows, w.cols, device=dev)
+            calls.append(lambda x=x, y=y, flat=flat: fr.fr_softmax(x, out=y, form=form))
+        return calls, "softmax", w.rows, w.cols, 1
     if name == "softmax_65537_offset":
         # rows of 65537 with x one element past y's phase (511 rows, 128 MiB
         # of x): the split form stages each CTA's run in shared memory
@@ -608,6 +620,7 @@ EXTRA = {"relu_add_sum": "relu_add_sum_64x128", "layernorm": "layernorm_4096x327
          "softmax_bf16_4097_looped": "softmax_bf16_looped_16380x4097",
          "softmax_bf16_65537": "softmax_bf16_1022x65537",
          "softmax_4097_offset": "softmax_offset_8190x4097",
+         "softmax_8192_offset": "softmax_offset_4096x8192",
          "softmax_65537_offset": "softmax_offset_511x65537",
          "softmax_bf16_8192_offset": "softmax_bf16_offset_8192x8192",
          "layernorm_768": "layernorm_174762x768", "layernorm_6144": "layernorm_21845x6144"}
