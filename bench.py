@@ -59,6 +59,7 @@ def parse():
                                       "softmax_bf16_65537", "xent_box", "form_sweep",
                                       "softmax_4097_offset", "softmax_bf16_8192_offset",
                                       "softmax_65537_offset", "softmax_8192_offset",
+                                      "softmax_262144", "softmax_bf16_262144",
                                       *[f"layernorm_{c}" for c in LN_HIDDEN]],
                    help="time one workload alone (for profiler captures) and exit")
     p.add_argument("--form", default="auto", choices=["auto", "persistent", "looped", "split"],
@@ -434,6 +435,19 @@ def setup_workload(name, fr, workloads, dev, form="auto"):
             y = torch.empty_like(x)
             calls.append(lambda x=x, y=y: fr.fr_softmax(x, out=y, form=f))
         return calls, "softmax", w.rows, w.cols, 1
+    if name in ("softmax_262144", "softmax_bf16_262144"):
+        # rows of 262144 in phase (fp32 304 rows, bf16 608: 304 MiB of x):
+        # the split form, a cluster per row whose CTAs stream their runs twice
+        bf16 = "bf16" in name
+        rows = 608 if bf16 else 304
+        op = "softmax_bf16" if bf16 else "softmax"
+        w = (workloads.make_softmax_bf16(rows, 262144, seed=20261202 + 7 + 1000 * SHARD[0])
+             if bf16 else make_shard(workloads, 1, rows=rows, cols=262144))
+        for _ in range(nsets(op, w.rows, w.cols)):
+            x = to_device(w.arrays["x"], dev)
+            y = torch.empty_like(x)
+            calls.append(lambda x=x, y=y: fr.fr_softmax(x, out=y, form=form))
+        return calls, op, w.rows, w.cols, 1
     if name == "softmax_8192_offset":
         # rows of 8192 with x one element past y's phase (4096 rows, 128 MiB
         # of x): the persistent form stages each row in shared memory
@@ -619,6 +633,7 @@ EXTRA = {"relu_add_sum": "relu_add_sum_64x128", "layernorm": "layernorm_4096x327
          "softmax_bf16_4097": "softmax_bf16_16380x4097",
          "softmax_bf16_4097_looped": "softmax_bf16_looped_16380x4097",
          "softmax_bf16_65537": "softmax_bf16_1022x65537",
+         "softmax_262144": "softmax_304x262144", "softmax_bf16_262144": "softmax_bf16_608x262144",
          "softmax_4097_offset": "softmax_offset_8190x4097",
          "softmax_8192_offset": "softmax_offset_4096x8192",
          "softmax_65537_offset": "softmax_offset_511x65537",
@@ -693,7 +708,7 @@ def xent_box(fr, workloads, dev, timed, args, peak):
 SWEEP_RAS_ROWS = (8, 32, 128, 512, 1024, 2048, 4096, 8192)
 SWEEP_RAS_COLS = (1024, 4096, 16384, 65536, 262144, 1048576, 4194304)
 SWEEP_SM_ROWS = (16, 64, 152, 304, 608, 1216, 2432, 4864, 16384)
-SWEEP_SM_COLS = (1025, 2048, 4097, 8192, 16384, 32768, 65537, 131072, 262144, 393216)
+SWEEP_SM_COLS = (1025, 2048, 4097, 8192, 16384, 32768, 65537, 131072, 262144, 393216, 1048576)
 SWEEP_OFFSET_COLS = (1025, 2048, 4097, 8192, 16384, 32768, 65537, 131072)
 SWEEP_LN_COLS = (768, 1024, 1536, 2048, 2560, 3072, 4096, 5120, 6144, 7168, 8192, 10240, 12288,
                  14336, 16384, 20480, 24576, 32768, 65536)

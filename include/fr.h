@@ -187,10 +187,12 @@ fr_status fr_reduce_sumsq(const void *x, float *out, int64_t rows, int64_t cols,
  *              offsets within a 32-byte sector, fp32 rows of up to 4608
  *              columns in registers with y's chunks shifted, longer ones
  *              and bf16 rows staged in shared memory); longer rows (or few
- *              rows) take the split form (a cluster of CTAs per row: the
- *              slices in registers for rows in phase up to 262144 columns,
- *              else staged in shared memory, up to 409496 fp32 or 818992 bf16
- *              columns), the rest the looped form
+ *              rows) take the split form (a cluster of CTAs per row).  Rows
+ *              in phase: the slices in registers up to 384 KiB rows, past
+ *              that (any length) each CTA streams its run twice, the second
+ *              time from L2.  Rows out of phase: the runs staged in shared
+ *              memory, up to 409496 fp32 or 818992 bf16 columns, the looped
+ *              form beyond
  */
 fr_status fr_softmax(const void *x, void *y, int64_t rows, int64_t cols, int64_t ldx,
                      int64_t ldy, fr_dtype dtype, fr_form form, fr_stream_t stream);

@@ -85,14 +85,28 @@ fr_status device_ok(fr::DevInfo *info) {
   return FR_OK;
 }
 
-// The split form of the softmax: a cluster per row with the slices in
-// registers where x and y rows are in phase and the row fits, else the
-// cluster that stages its slices in shared memory (FR_SOFTMAX_SPLIT=stage
-// pins the latter for every row).
-bool split_staged_pinned() {
+// The split form of the softmax: a cluster of CTAs per row.  Rows in phase
+// (x and y at the same offset within a 32-byte sector): the slices in
+// registers, or for rows longer than split_loops allows the cluster whose
+// CTAs stream their runs twice; rows out of phase: the cluster that stages
+// its runs in shared memory.  FR_SOFTMAX_SPLIT=stage pins the staged cluster
+// for every row, FR_SOFTMAX_SPLIT=loop the streaming one for every row in
+// phase.
+bool split_pinned(const char *v) {
   const char *e = getenv("FR_SOFTMAX_SPLIT");
-  return e != nullptr && strcmp(e, "stage") == 0;
+  return e != nullptr && strcmp(e, v) == 0;
 }
+bool split_staged_pinned() { return split_pinned("stage"); }
+
+// Rows in phase longer than 384 KiB: the streaming cluster.  Measured on
+// GB300 (us per call, back to back; register cluster / streaming cluster):
+// 256 KiB rows -- fp32 65537 columns: 608 rows 53.0 / 56.2, 1216 rows 99.2 /
+// 106.2; bf16 131072: 304 rows 30.5 / 32.4, 1216 rows 102.1 / 112.2; 512 KiB
+// rows -- fp32 131072: 152 rows 32.7 / 31.1, 608 rows 111.8 / 101.9; bf16
+// 262144: 152 rows 35.5 / 32.3, 608 rows 119.9 / 104.2; 1 MiB rows -- fp32
+// 262144: 152 rows 80.8 / 61.4, 304 rows 156.6 / 109.0.  The crossover lies
+// between 256 and 512 KiB; the rule takes the middle.
+bool split_loops(int64_t cols, int es) { return cols * es > (384 << 10); }
 
 fr_status launched(cudaError_t e, fr_form form) {
   if (e != cudaSuccess) return FR_ERR_CUDA;
@@ -132,18 +146,19 @@ fr_form pick_ras(int64_t rows, int64_t cols, int sm_count, bool bf16 = false) {
 // a CTA per row at every row count (at fewer than 4 x SMs rows every form
 // takes the launch time, 6.2-7 us; at 2432 x 8192: CTA per row 25.4 us,
 // cluster 32.8); from 16384 a cluster of CTAs per row (16384: within 2 % of a
-// CTA per row; 32768: 94.6 us against 105.9 at 2432 rows); at 262144 columns
-// the looped form once the rows fill the SMs (152 rows: looped 78.2 us, split
-// 79.8; 64 rows: split 39.4, looped 60.6).  Rows out of phase (x and y at
-// different offsets within a 32-byte sector): a CTA per row up to 32768
-// columns (the row in registers up to 4608, staged in shared memory beyond),
-// then a cluster per row with its slices staged in shared memory (608 x
-// 65537: 62.6 us, looped 96.2; 608 x 131072: 148.0 against 191.4), looped past its reach.  Rows in phase past 262144
-// columns: the staged cluster below SMs rows (64 x 393216: 61.3 us, looped
-// 90.8; at 152 rows 130.3 against 114.2).  Below 4 x SMs rows of 8192-16384 columns the two
-// forms are within launch noise of each other (five sweeps, means: 304 x
-// 16384 CTA per row 12.2 us, looped 11.3; 152 x 16384 8.8 against 9.5; 608 x
-// 16384 16.7 against 20.3).
+// CTA per row; 32768: 94.6 us against 105.9 at 2432 rows), its CTAs streaming
+// their runs twice past 384 KiB rows (see split_loops), which beats the
+// looped form at every row count measured (152 x 262144: 61.4 us, looped
+// 76.0; 304 x 393216: 174.8 against 219.8; 64 x 1048576: 116.2 against
+// 233.3; 16 x 4194304: 143.1 against 672.9).  Below 4 x SMs rows of
+// 8192-16384 columns the two forms are within launch noise of each other
+// (five sweeps, means: 304 x 16384 CTA per row 12.2 us, looped 11.3; 152 x
+// 16384 8.8 against 9.5; 608 x 16384 16.7 against 20.3).  Rows out of phase
+// (x and y at different offsets within a 32-byte sector): a CTA per row up to
+// 32768 columns (the row in registers up to 4608, staged in shared memory
+// beyond), then a cluster per row with its runs staged in shared memory (608
+// x 65537: 62.6 us, looped 96.2; 608 x 131072: 148.0 against 191.4), looped
+// past its reach.
 fr_form pick_softmax(int64_t rows, int64_t cols, bool vec, int sm_count) {
   if (cols <= 1024) return FR_FORM_PERSISTENT;
   if (!vec) {  // rows of 16385 .. 32768 columns: a staged cluster per row under SMs / 4
@@ -156,26 +171,23 @@ fr_form pick_softmax(int64_t rows, int64_t cols, bool vec, int sm_count) {
                                                                  : FR_FORM_PERSISTENT;
     return cols <= fr::softmax_stage_split_max_cols(4) ? FR_FORM_SPLIT : FR_FORM_LOOPED;
   }
-  if (cols <= 8192) return FR_FORM_PERSISTENT;
-  if (cols <= 131072 || (cols <= fr::softmax_stage_split_max_cols(4) && rows < sm_count))
-    return FR_FORM_SPLIT;
-  return FR_FORM_LOOPED;
+  return cols <= 8192 ? FR_FORM_PERSISTENT : FR_FORM_SPLIT;
 }
 
 // bf16 softmax.  Rows out of phase: up to 32768 columns a CTA per row, the row
 // staged in shared memory (16384 x 4097: 48.3 us, looped 87.8; 4864 x 32768:
-// 95.1 against 183.5), then a cluster per row with staged slices (608 x
-// 65537: 32.9 us, looped 67.7; 2432 x 65537: 108.3 against 206.9), looped
-// past its reach.  Rows in phase past 262144 columns: the staged cluster
-// (393216: 64 rows 27.1 us, looped 50.9; 608 rows 183.3 against 222.9), past
-// 393216 columns (runs over 100 KiB, one CTA an SM) only below SMs rows.
-// Rows in phase: up to 2048 columns a warp per row, up to 8192
-// a CTA per row; at 16384 the looped form from 4 x SMs rows (608: looped 9.4
-// us, CTA per row 10.5), a CTA per row below, and a CTA per row again from 8
-// x SMs rows, where the persistent form stages the row in shared memory
-// (1216: 15.2 us, looped 15.8; 16384: 153.2 against 165.6); at 32768 a CTA per row while the rows are no more than the SMs (152:
-// 6.7 us against 7.7 for a cluster per row), else, up to 262144 columns, a
-// cluster per row (2432 x 32768: 50.2 us, looped 55.3, CTA per row 73.9).
+// 95.1 against 183.5), then a cluster per row with staged runs (608 x 65537:
+// 32.9 us, looped 67.7; 2432 x 65537: 108.3 against 206.9), looped past its
+// reach.  Rows in phase: up to 2048 columns a warp per row, up to 8192 a CTA
+// per row; at 16384 the looped form from 4 x SMs rows (608: looped 9.4 us, CTA
+// per row 10.5), a CTA per row below, and a CTA per row again from 8 x SMs
+// rows, where the persistent form stages the row in shared memory (1216: 15.2
+// us, looped 15.8; 16384: 153.2 against 165.6); at 32768 a CTA per row while
+// the rows are no more than the SMs (152: 6.7 us against 7.7 for a cluster per
+// row), else a cluster per row (2432 x 32768: 50.2 us, looped 55.3, CTA per
+// row 73.9), its CTAs streaming their runs twice past 384 KiB rows (see
+// split_loops; 304 x 393216: 90.7 us, looped 108.5; 64 x 1048576: 56.5
+// against 138.5; 16 x 4194304: 80.8 against 424.3).
 fr_form pick_softmax_bf16(int64_t rows, int64_t cols, bool vec, int sm_count) {
   if (cols <= 2048) return FR_FORM_PERSISTENT;
   if (!vec)
@@ -187,13 +199,7 @@ fr_form pick_softmax_bf16(int64_t rows, int64_t cols, bool vec, int sm_count) {
     const int64_t sms = sm_count;
     return rows >= 8 * sms || rows < 4 * sms ? FR_FORM_PERSISTENT : FR_FORM_LOOPED;
   }
-  if (cols <= 32768 && rows <= sm_count) return FR_FORM_PERSISTENT;
-  if (cols <= fr::softmax_bf16_split_max_cols()) return FR_FORM_SPLIT;
-  // past the registers' reach the staged cluster: up to 393216 columns (runs
-  // under 100 KiB, two CTAs an SM) at any row count, longer rows below SMs rows
-  return (cols <= 393216 || rows < sm_count) && cols <= fr::softmax_stage_split_max_cols(2)
-             ? FR_FORM_SPLIT
-             : FR_FORM_LOOPED;
+  return cols <= 32768 && rows <= sm_count ? FR_FORM_PERSISTENT : FR_FORM_SPLIT;
 }
 
 // LayerNorm (bf16 rows of 256 MiB, back to back).  Rows of C x T x 32
@@ -374,7 +380,12 @@ fr_status fr_softmax(const void *x, void *y, int64_t rows, int64_t cols, int64_t
                                                        info.sm_count, s), f);
       case FR_FORM_SPLIT:
         if (cols <= 2048 || rows > 0x7fffffff / 8) return FR_ERR_UNSUPPORTED_FORM;
-        if (vec && cols <= fr::softmax_bf16_split_max_cols() && !split_staged_pinned())
+        if (vec && !split_staged_pinned() &&
+            (split_pinned("loop") || split_loops(cols, 2) ||
+             cols > fr::softmax_bf16_split_max_cols()))
+          return launched(fr::launch_softmax_split_looped(bx, by, rows, cols, ldx, ldy, 2,
+                                                          info.sm_count, s), f);
+        if (vec && !split_staged_pinned())
           return launched(fr::launch_softmax_bf16_split(bx, by, rows, cols, ldx, ldy, s), f);
         if (cols > fr::softmax_stage_split_max_cols(2)) return FR_ERR_UNSUPPORTED_FORM;
         return launched(fr::launch_softmax_split_staged(bx, by, rows, cols, ldx, ldy, 2, s), f);
@@ -403,7 +414,11 @@ fr_status fr_softmax(const void *x, void *y, int64_t rows, int64_t cols, int64_t
       return launched(fr::launch_softmax_looped(fx, fy, rows, cols, ldx, ldy, vec, info.sm_count, s), f);
     case FR_FORM_SPLIT:
       if (cols <= 1024 || rows > 0x7fffffff / 8) return FR_ERR_UNSUPPORTED_FORM;
-      if (vec && cols <= fr::softmax_split_max_cols() && !split_staged_pinned())
+      if (vec && !split_staged_pinned() &&
+          (split_pinned("loop") || split_loops(cols, 4) || cols > fr::softmax_split_max_cols()))
+        return launched(fr::launch_softmax_split_looped(fx, fy, rows, cols, ldx, ldy, 4,
+                                                        info.sm_count, s), f);
+      if (vec && !split_staged_pinned())
         return launched(fr::launch_softmax_split(fx, fy, rows, cols, ldx, ldy, s), f);
       if (cols > fr::softmax_stage_split_max_cols(4)) return FR_ERR_UNSUPPORTED_FORM;
       return launched(fr::launch_softmax_split_staged(fx, fy, rows, cols, ldx, ldy, 4, s), f);

@@ -16,6 +16,16 @@
 // shares, its exponentials taken again (none kept).  One read of x and one
 // write of y.  The wait is bounded; on expiry the kernel records
 // FR_DEVERR_TIMEOUT and goes on.  fp32 and bf16 rows (fp32 arithmetic).
+//
+// Rows in phase (x and y at the same offset within a 32-byte sector) longer
+// than a cluster's shared memory holds, or with so many rows that the staged
+// runs leave one CTA an SM, take softmax_cluster_loop instead: the same
+// cluster and exchange, but each CTA streams its run of x twice -- once
+// folding the chunks into (m_q, d_q) with the merge of section 9.5, once after
+// the exchange to write y -- the looped form of section 9.4 (2) within a
+// cluster.  A run is 1/C of the row, so the second read follows the first
+// within a few microseconds and finds x in L2; the CTAs an SM are set so that
+// the runs read once and not yet again fit in about a third of L2.
 #include <cstdlib>
 #include <cstring>
 
@@ -312,6 +322,197 @@ cudaError_t launch_softmax_split_staged(const void *x, void *y, int64_t rows, in
   uint16_t *by = static_cast<uint16_t *>(y);
   return T == 512 ? launch_stage_t<uint16_t, 512>(bx, by, rows, cols, ldx, ldy, C, smem, s)
                   : launch_stage_t<uint16_t, 256>(bx, by, rows, cols, ldx, ldy, C, smem, s);
+}
+
+
+namespace {
+
+// 16-byte load kept in L2 (the second pass reads it again); no L1 allocation.
+__device__ __forceinline__ uint4 ld_again_u4(const void *p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
+constexpr int kLoopU = 8;  // 16-byte chunks a thread has in flight per pass
+
+// One cluster of C CTAs per row, x and y rows in phase; CTA q takes the whole
+// 16-byte chunks [c0, c1) of the row (the chunks of y and of x coincide),
+// CTA 0 the ragged head, CTA C - 1 the ragged tail.
+template <typename E, int T>
+__global__ void __launch_bounds__(T, 1024 / T)
+softmax_cluster_loop(const E *__restrict__ x, E *__restrict__ y, int cols, int64_t ldx,
+                     int64_t ldy, int *__restrict__ err) {
+  pdl_enter();
+  using K = Chunk<E>;
+  constexpr int V = K::kV, ES = static_cast<int>(sizeof(E)), W = T / 32, U = kLoopU;
+  __shared__ float red[2][W];
+  __shared__ __align__(16) float4 pairs[kScMaxCluster];
+  __shared__ __align__(8) uint64_t xbar;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t C = cluster_nctarank(), q = cluster_ctarank();
+  if (tid == 0) {
+    mbar_init(&xbar, 1);
+    mbar_init_fence();
+    mbar_arrive_expect_tx(&xbar, 16u * C);
+  }
+  __syncthreads();
+  cluster_arrive_relaxed();  // this CTA's mbarrier is ready for the peers' pairs
+  const int64_t row = cluster_id_x();
+  const E *px = x + row * ldx;
+  E *py = y + row * ldy;
+  const int n = cols;
+  // h elements before the first whole chunk, nf whole chunks, then the tail
+  const int h = min(n, static_cast<int>(((16 - (reinterpret_cast<uintptr_t>(px) & 15)) & 15) / ES));
+  const int nf = (n - h) / V, t0 = h + V * nf, tail = n - t0;
+  const int kc = (nf + static_cast<int>(C) - 1) / static_cast<int>(C);
+  const int c0 = min(nf, static_cast<int>(q) * kc), c1 = min(nf, c0 + kc);
+  const uint4 *xv = reinterpret_cast<const uint4 *>(px + h);
+  uint4 *yv = reinterpret_cast<uint4 *>(py + h);
+  const bool head_here = q == 0 && tid < h;
+  const bool tail_here = q == C - 1 && tid >= 32 && tid - 32 < tail;
+  const int se = head_here ? tid : t0 + tid - 32;  // this thread's ragged element
+
+  // pass 1: (m, d) of the run, U chunks at a time: their max, one rescale of
+  // d to it, then their exponentials against it
+  MD st{-INFINITY, 0.0f};
+  for (int base = c0 + tid; base < c1; base += T * U) {
+    uint4 r[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (base + T * u < c1) r[u] = ld_again_u4(xv + base + T * u);
+    float gm = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (base + T * u < c1) gm = max_nan(gm, K::max(r[u]));
+    const float M = max_nan(st.m, gm);
+    if (M == -INFINITY) continue;  // nothing but -inf so far: adds 0
+    if (M != st.m) st.d *= ex2((st.m - M) * kLog2e);  // 0 while st.m is -inf
+    st.m = M;
+    const float mb = M * kLog2e;
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (base + T * u < c1) st.d += K::sum(r[u], mb);
+  }
+  if (head_here || tail_here) st = md_merge(st, MD{K::get(K::load1(px + se)), 1.0f});
+  st = warp_md(st);
+  if (lane == 0) {
+    red[0][warp] = st.m;
+    red[1][warp] = st.d;
+  }
+  __syncthreads();
+  const MD cta = warp_md(lane < W ? MD{red[0][lane], red[1][lane]} : MD{-INFINITY, 0.0f});
+
+  cluster_wait();  // every peer's mbarrier is initialised
+  if (tid < static_cast<int>(C))
+    st_async_f4(&pairs[q], &xbar, static_cast<uint32_t>(tid), make_float4(cta.m, cta.d, 0.0f, 0.0f));
+  if (!mbar_wait_bounded(&xbar, 0, kScWaitBudget) && tid == 0) atomicCAS(err, 0, FR_DEVERR_TIMEOUT);
+  // the C pairs merged in rank order: the same (M, D) in every CTA
+  float M = -INFINITY;
+  for (uint32_t r = 0; r < C; ++r) M = max_nan(M, pairs[r].x);
+  float D = 0.0f;
+  if (M != -INFINITY)
+    for (uint32_t r = 0; r < C; ++r) D += pairs[r].y * ex2((pairs[r].x - M) * kLog2e);
+  const float mb = M * kLog2e, inv = __frcp_rn(D);
+
+  // pass 2: the run again, its blocks of T U chunks in reverse order (the
+  // ones read last in pass 1 first: what of a run too long for L2 is still
+  // there), each chunk's last read (first out of L2), y written out
+  const uint64_t policy = l2_evict_first_policy();
+  for (int it = (c1 - c0 + T * U - 1) / (T * U) - 1; it >= 0; --it) {
+    const int base = c0 + it * T * U + tid;
+    uint4 r[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (base + T * u < c1) r[u] = ld_stream_u4(xv + base + T * u, policy);
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (base + T * u < c1) st_stream_u4(yv + base + T * u, K::out(r[u], mb, inv));
+  }
+  if (head_here || tail_here)
+    K::store1(py + se, K::put(ex2(fmaf(K::get(K::load1(px + se)), kLog2e, -mb)) * inv));
+}
+
+template <typename E, int T>
+cudaError_t launch_loop_t(const E *x, E *y, int64_t rows, int64_t cols, int64_t ldx,
+                          int64_t ldy, int C, int per_sm, cudaStream_t s) {
+  int *err = nullptr;
+  cudaError_t e = device_error_word(&err);
+  if (e != cudaSuccess) return e;
+  const void *kern = reinterpret_cast<const void *>(softmax_cluster_loop<E, T>);
+  // CTAs an SM: what the registers allow, held to per_sm by padding the
+  // dynamic shared memory ((per_sm + 1) padded CTAs do not fit an SM)
+  if ((e = set_smem_limit(kern, 0)) != cudaSuccess) return e;
+  int resident = 0;
+  if ((e = blocks_per_sm(&resident, kern, T, 0)) != cudaSuccess) return e;
+  size_t smem = 0;
+  if (resident > per_sm) {
+    int dev = 0, per_sm_smem = 0, reserved = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&per_sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                                    dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) !=
+            cudaSuccess)
+      return e;
+    smem = static_cast<size_t>((per_sm_smem / (per_sm + 1) - reserved + 1023) / 1024 * 1024);
+    if ((e = set_smem_limit(kern, smem)) != cudaSuccess) return e;
+  }
+  return launch_k(softmax_cluster_loop<E, T>, dim3(static_cast<unsigned>(rows * C)), dim3(T),
+                  smem, s, static_cast<unsigned>(C), x, y, static_cast<int>(cols), ldx, ldy, err);
+}
+
+// The loop cluster's shape: C = 8 CTAs a row; four CTAs of 256 threads an SM
+// while the runs read once and not yet again -- every resident CTA's run --
+// fit in 64 MB (half of L2), else two of 512.  Measured on GB300 (us per call,
+// back to back; CTAs an SM 1 / 2 / 4): fp32 152 x 262144 84.7 / 60.6 / 70.5,
+// 304 x 393216 234.4 / 174.8 / 207.3, 16 x 4194304 172.3 / 143.1 / 197.7;
+// bf16 304 x 262144 120.6 / 66.0 / 56.5, 152 x 393216 76.3 / 51.7 / 48.3,
+// 64 x 1048576 71.3 / 57.0 / 64.7; clusters of 4 were slower than of 8 but
+// at bf16 64 x 393216 (22.8 against 25.6 at two CTAs an SM, 22.5 at four).
+// FR_LOOP_C=4|8, FR_LOOP_K=1|2|4 and FR_LOOP_L2_MB=<MB> pin them.
+void loop_shape(int64_t cols, int es, int sm_count, int *C, int *per_sm) {
+  *C = kScMaxCluster;
+  if (const char *e = getenv("FR_LOOP_C"); e != nullptr && atoi(e) == 4) *C = 4;
+  int64_t budget = 64ll << 20;
+  if (const char *e = getenv("FR_LOOP_L2_MB")) {
+    const int mb = atoi(e);
+    if (mb >= 1 && mb <= 1024) budget = static_cast<int64_t>(mb) << 20;
+  }
+  const int64_t run = cols * es / *C;
+  *per_sm = static_cast<int64_t>(sm_count) * 4 * run <= budget ? 4 : 2;
+  if (const char *e = getenv("FR_LOOP_K")) {
+    const int k = atoi(e);
+    if (k == 1 || k == 2 || k == 4) *per_sm = k;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_softmax_split_looped(const void *x, void *y, int64_t rows, int64_t cols,
+                                        int64_t ldx, int64_t ldy, int es, int sm_count,
+                                        cudaStream_t s) {
+  if (rows < 1 || cols < 1 || cols > 0x7fffffff || rows * kScMaxCluster > 0x7fffffff)
+    return cudaErrorInvalidValue;
+  int C = 0, per_sm = 0;
+  loop_shape(cols, es, sm_count, &C, &per_sm);
+  if (es == 4) {
+    const float *fx = static_cast<const float *>(x);
+    float *fy = static_cast<float *>(y);
+    switch (per_sm) {
+      case 4: return launch_loop_t<float, 256>(fx, fy, rows, cols, ldx, ldy, C, 4, s);
+      case 2: return launch_loop_t<float, 512>(fx, fy, rows, cols, ldx, ldy, C, 2, s);
+      default: return launch_loop_t<float, 1024>(fx, fy, rows, cols, ldx, ldy, C, 1, s);
+    }
+  }
+  const uint16_t *bx = static_cast<const uint16_t *>(x);
+  uint16_t *by = static_cast<uint16_t *>(y);
+  switch (per_sm) {
+    case 4: return launch_loop_t<uint16_t, 256>(bx, by, rows, cols, ldx, ldy, C, 4, s);
+    case 2: return launch_loop_t<uint16_t, 512>(bx, by, rows, cols, ldx, ldy, C, 2, s);
+    default: return launch_loop_t<uint16_t, 1024>(bx, by, rows, cols, ldx, ldy, C, 1, s);
+  }
 }
 
 }  // namespace fr

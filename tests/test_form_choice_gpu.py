@@ -36,7 +36,8 @@ def rotating(rows, cols, dtype, per_set_bytes):
 
 
 CASES = [("relu_add_sum", 8, 1 << 22), ("relu_add_sum", 4096, 16384), ("softmax", 2432, 32768),
-         ("softmax_bf16", 4864, 16384), ("layernorm", 174762, 768), ("layernorm", 4096, 32768)]
+         ("softmax", 304, 262144), ("softmax_bf16", 4864, 16384), ("layernorm", 174762, 768),
+         ("layernorm", 4096, 32768)]
 
 
 @pytest.mark.parametrize("op,rows,cols", CASES)

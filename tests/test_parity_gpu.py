@@ -35,11 +35,12 @@ def forms_for(op, cols, in_phase=True):
     if op == "relu_add_sum":
         return (["persistent"] if cols <= 1024 else []) + ["looped", "split"]
     if op == "softmax":  # rows past 1024 stay persistent (a CTA per row) up to 32768
-        # columns; they also split over a cluster of CTAs (the slices in
-        # registers in phase up to 262144 columns, else staged in shared
-        # memory, up to 409496)
-        return ((["persistent"] if cols <= 32768 else []) +
-                (["split"] if 1024 < cols <= STAGE_SPLIT_MAX_F32 else []) + ["looped"])
+        # columns; they also split over a cluster of CTAs (in phase: the
+        # slices in registers up to 262144 columns, streamed twice beyond;
+        # out of phase: staged in shared memory, up to 409496)
+        split = cols > 1024 and (in_phase or cols <= STAGE_SPLIT_MAX_F32)
+        return ((["persistent"] if cols <= 32768 else []) + (["split"] if split else []) +
+                ["looped"])
     raise ValueError(op)
 
 
@@ -265,6 +266,71 @@ def test_softmax_split_staged_special_values(o, cols):
         got = run_softmax(x, "split", layout)
         assert_close(got, ref, "f32", f"staged split special {cols} {layout}")
         assert np.isnan(got[[1, 3, 4]]).all() and np.isfinite(got[[0, 2, 5]]).all()
+
+
+@pytest.mark.parametrize("cols", [1025, 8193, 40000, 65537, 131073, 262145, 409497, 1000003])
+@pytest.mark.parametrize("layout", [(0, 0, 0), (1, 1, 5), (3, 3, 0)])
+def test_softmax_split_loop(o, cols, layout, monkeypatch):
+    """The split form's streaming cluster (FR_SOFTMAX_SPLIT=loop pins it for
+    every row in phase): each CTA of the row's cluster folds its run into
+    (m, d), the pairs are exchanged, and the run is read again to write y;
+    rows staggered so that every CTA 0 and CTA C-1 has a ragged head or tail."""
+    monkeypatch.setenv("FR_SOFTMAX_SPLIT", "loop")
+    rows = 3 if cols > 100000 else 7
+    w = workloads.make(1, rows=rows, cols=cols, seed=3050 + cols)
+    ref = o.softmax(w.arrays["x"])
+    assert_close(run_softmax(w.arrays["x"], "split", layout), ref, "f32",
+                 f"loop split {rows}x{cols} {layout}")
+    assert fr.fr_check_device_error() == 0
+
+
+@pytest.mark.parametrize("shape", [{"FR_LOOP_K": "1"}, {"FR_LOOP_K": "2"},
+                                   {"FR_LOOP_K": "4", "FR_LOOP_C": "4"}],
+                         ids=["k1", "k2", "k4c4"])
+@pytest.mark.parametrize("cols", [8193, 262145])
+def test_softmax_split_loop_shapes(o, cols, shape, monkeypatch):
+    """Every CTA size (1024, 512 or 256 threads: one, two or four CTAs an SM)
+    and both cluster sizes of the streaming cluster."""
+    monkeypatch.setenv("FR_SOFTMAX_SPLIT", "loop")
+    for k, v in shape.items():
+        monkeypatch.setenv(k, v)
+    w = workloads.make(1, rows=5, cols=cols, seed=3150 + cols)
+    ref = o.softmax(w.arrays["x"])
+    assert_close(run_softmax(w.arrays["x"], "split", (1, 1, 5)), ref, "f32",
+                 f"loop split 5x{cols} {shape}")
+
+
+@pytest.mark.parametrize("cols", [1025, 40000, 65537, 409497])
+def test_softmax_split_loop_special_values(o, cols, monkeypatch):
+    monkeypatch.setenv("FR_SOFTMAX_SPLIT", "loop")
+    x = workloads.make(1, rows=6, cols=cols, seed=73).arrays["x"].copy()
+    x[1, cols // 2] = np.nan                 # NaN row
+    x[2, : cols // 2] = -np.inf              # partly -inf (whole runs of it)
+    x[3, :] = -np.inf                        # all -inf: 0/0
+    x[4, cols - 1] = np.inf                  # +inf: inf - inf
+    ref = o.softmax(x)
+    for layout in ((0, 0, 0), (1, 1, 5)):
+        got = run_softmax(x, "split", layout)
+        assert_close(got, ref, "f32", f"loop split special {cols} {layout}")
+        assert np.isnan(got[[1, 3, 4]]).all() and np.isfinite(got[[0, 2, 5]]).all()
+
+
+def test_softmax_split_loop_in_place_and_unpinned(o, monkeypatch):
+    """In place through the streaming cluster, and rows in phase past the
+    staged cluster's reach take it unpinned."""
+    monkeypatch.setenv("FR_SOFTMAX_SPLIT", "loop")
+    w = workloads.make(1, rows=5, cols=70001, seed=3300)
+    ref = o.softmax(w.arrays["x"])
+    t = torch.from_numpy(w.arrays["x"]).cuda()
+    fr.fr_softmax(t, form="split", out=t)
+    got = t.cpu().numpy()
+    assert_close(got, ref, "f32", "loop split in place")
+    assert np.abs(got.astype(np.float64).sum(1) - 1).max() < 1e-5
+    monkeypatch.delenv("FR_SOFTMAX_SPLIT")
+    w = workloads.make(1, rows=2, cols=STAGE_SPLIT_MAX_F32 + 1, seed=3301)
+    assert_close(run_softmax(w.arrays["x"], "split"), o.softmax(w.arrays["x"]), "f32",
+                 "split past the staged reach")
+    assert fr.fr_last_form() == "split"
 
 
 @pytest.mark.parametrize("cols", [1025, 8193, 32769, 65537, 131071, 262144])
@@ -616,8 +682,10 @@ def test_error_statuses_on_device():
     with pytest.raises(fr.FRError) as e:  # short enough for one warp: no split
         fr.fr_softmax(torch.zeros(4, 1000, device="cuda"), form="split")
     assert e.value.status == 3
-    with pytest.raises(fr.FRError) as e:  # longer than a cluster holds, even staged
-        fr.fr_softmax(torch.zeros(2, STAGE_SPLIT_MAX_F32 + 1, device="cuda"), form="split")
+    with pytest.raises(fr.FRError) as e:  # out of phase and longer than a staged cluster holds
+        n = STAGE_SPLIT_MAX_F32 + 1
+        fr.fr_softmax(torch.zeros(2 * n + 1, device="cuda")[1:].view(2, n), form="split",
+                      out=torch.empty(2, n, device="cuda"))
     assert e.value.status == 3
     buf = torch.zeros(4 * 2001 + 3, device="cuda")  # x and y rows out of 32-byte phase
     xs = buf[:4 * 2001].view(4, 2001)[:, :2000]
@@ -675,4 +743,8 @@ def test_auto_form_choices():
     assert fr.fr_last_form() == "split"  # past the registers' reach: a cluster, staged
     x = torch.zeros(2, STAGE_SPLIT_MAX_F32 + 1, device="cuda")
     fr.fr_softmax(x)
-    assert fr.fr_last_form() == "looped"  # longer than a cluster holds
+    assert fr.fr_last_form() == "split"  # a cluster streaming its runs twice, at any length
+    n = STAGE_SPLIT_MAX_F32 + 1
+    fr.fr_softmax(torch.zeros(2 * n + 1, device="cuda")[1:].view(2, n),
+                  out=torch.empty(2, n, device="cuda"))
+    assert fr.fr_last_form() == "looped"  # out of phase and longer than a staged cluster holds

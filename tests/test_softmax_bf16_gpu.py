@@ -35,7 +35,9 @@ def forms(cols, layout=(0, 0, 0)):
     phase)"""
     in_phase = (layout[0] - layout[1]) * 2 % 32 == 0
     persistent = cols <= 32768
-    split = 2048 < cols <= 818992  # a cluster of CTAs per row (staged out of phase)
+    # a cluster of CTAs per row (in phase at any length; out of phase staged,
+    # up to 818992 columns)
+    split = cols > 2048 and (in_phase or cols <= 818992)
     return (["persistent"] if persistent else []) + (["split"] if split else []) + ["looped", "auto"]
 
 
@@ -120,6 +122,33 @@ def test_softmax_bf16_split_staged(o, cols, layout, monkeypatch):
     bits = workloads.make_softmax_bf16(rows, cols, seed=7000 + cols).arrays["x"]
     ref = o.softmax(widen(bits))
     assert_bf16_within_steps(run(bits, "split", layout), ref, 1, f"staged {rows}x{cols} {layout}")
+
+
+@pytest.mark.parametrize("cols", [2049, 65537, 300001, 818993, 1000003])
+@pytest.mark.parametrize("layout", [(0, 0, 0), (3, 3, 7), (16, 16, 0)])
+def test_softmax_bf16_split_loop(o, cols, layout, monkeypatch):
+    """The split form's streaming cluster on bf16 rows in phase (pinned below
+    the staged cluster's reach, unpinned past it)."""
+    if cols <= 818992:
+        monkeypatch.setenv("FR_SOFTMAX_SPLIT", "loop")
+    rows = 2 if cols > 100000 else 7
+    bits = workloads.make_softmax_bf16(rows, cols, seed=7100 + cols).arrays["x"]
+    ref = o.softmax(widen(bits))
+    assert_bf16_within_steps(run(bits, "split", layout), ref, 1, f"loop {rows}x{cols} {layout}")
+    assert fr.fr_check_device_error() == 0
+
+
+@pytest.mark.parametrize("cols", [4097, 300001])
+def test_softmax_bf16_split_loop_special_values(o, cols, monkeypatch):
+    monkeypatch.setenv("FR_SOFTMAX_SPLIT", "loop")
+    bits = workloads.make_softmax_bf16(6, cols, seed=62).arrays["x"].copy()
+    bits[1, cols // 2] = 0x7FC0               # NaN row
+    bits[2, : cols // 2] = 0xFF80             # partly -inf
+    bits[3, :] = 0xFF80                       # all -inf: 0/0
+    bits[4, cols - 1] = 0x7F80                # +inf: inf - inf
+    ref = o.softmax(widen(bits))
+    for layout in ((0, 0, 0), (3, 3, 7)):
+        assert_bf16_within_steps(run(bits, "split", layout), ref, 1, f"loop special {cols} {layout}")
 
 
 @pytest.mark.parametrize("cols", [7, 1000, 2048, 4097, 20000])
