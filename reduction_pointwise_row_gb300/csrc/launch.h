@@ -60,8 +60,8 @@ int64_t softmax_stage_split_max_cols(int es);
 cudaError_t launch_softmax_split_staged(const void *x, void *y, int64_t rows, int64_t cols,
                                         int64_t ldx, int64_t ldy, int es, cudaStream_t s);
 // Split form for rows in phase (x and y at the same offset within a 32-byte
-// sector), any length up to 2^31 - 1 columns: a cluster of 4 or 8 CTAs per
-// row, each streaming its run of the row twice (the second read from L2).
+// sector), any length up to 2^31 - 1 columns: a cluster of 4, 8 or 16 CTAs
+// per row, each streaming its run of the row twice (the second read from L2).
 cudaError_t launch_softmax_split_looped(const void *x, void *y, int64_t rows, int64_t cols,
                                         int64_t ldx, int64_t ldy, int es, int sm_count,
                                         cudaStream_t s);

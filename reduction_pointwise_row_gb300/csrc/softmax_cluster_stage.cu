@@ -28,6 +28,9 @@
 // the runs read once and not yet again fit in about a third of L2.
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
+#include <set>
+#include <utility>
 
 #include "common.cuh"
 #include "launch.h"
@@ -337,6 +340,7 @@ __device__ __forceinline__ uint4 ld_again_u4(const void *p) {
 }
 
 constexpr int kLoopU = 8;  // 16-byte chunks a thread has in flight per pass
+constexpr int kLoopMaxCluster = 16;  // beyond the portable 8: opted in per kernel
 
 // One cluster of C CTAs per row, x and y rows in phase; CTA q takes the whole
 // 16-byte chunks [c0, c1) of the row (the chunks of y and of x coincide),
@@ -349,7 +353,7 @@ softmax_cluster_loop(const E *__restrict__ x, E *__restrict__ y, int cols, int64
   using K = Chunk<E>;
   constexpr int V = K::kV, ES = static_cast<int>(sizeof(E)), W = T / 32, U = kLoopU;
   __shared__ float red[2][W];
-  __shared__ __align__(16) float4 pairs[kScMaxCluster];
+  __shared__ __align__(16) float4 pairs[kLoopMaxCluster];
   __shared__ __align__(8) uint64_t xbar;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t C = cluster_nctarank(), q = cluster_ctarank();
@@ -442,9 +446,38 @@ cudaError_t launch_loop_t(const E *x, E *y, int64_t rows, int64_t cols, int64_t 
   cudaError_t e = device_error_word(&err);
   if (e != cudaSuccess) return e;
   const void *kern = reinterpret_cast<const void *>(softmax_cluster_loop<E, T>);
+  if (C > 8) {  // clusters past the portable size are opted in to once per device
+    static std::mutex mu;
+    static std::set<std::pair<int, const void *>> done;
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!done.count({dev, kern})) {
+      if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) !=
+          cudaSuccess)
+        return e;
+      done.insert({dev, kern});
+    }
+  }
   // CTAs an SM: what the registers allow, held to per_sm by padding the
   // dynamic shared memory ((per_sm + 1) padded CTAs do not fit an SM)
   if ((e = set_smem_limit(kern, 0)) != cudaSuccess) return e;
+  if (C > 8) {  // a device (or partition) that holds no cluster of C: 8
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(C);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(C));
+    cfg.blockDim = dim3(T);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if ((e = resident_clusters(&clusters, kern, cfg, static_cast<unsigned>(C))) != cudaSuccess)
+      return e;
+    if (clusters < 1) C = 8;
+  }
   int resident = 0;
   if ((e = blocks_per_sm(&resident, kern, T, 0)) != cudaSuccess) return e;
   size_t smem = 0;
@@ -463,18 +496,30 @@ cudaError_t launch_loop_t(const E *x, E *y, int64_t rows, int64_t cols, int64_t 
                   smem, s, static_cast<unsigned>(C), x, y, static_cast<int>(cols), ldx, ldy, err);
 }
 
-// The loop cluster's shape: C = 8 CTAs a row; four CTAs of 256 threads an SM
-// while the runs read once and not yet again -- every resident CTA's run --
-// fit in 64 MB (half of L2), else two of 512.  Measured on GB300 (us per call,
-// back to back; CTAs an SM 1 / 2 / 4): fp32 152 x 262144 84.7 / 60.6 / 70.5,
-// 304 x 393216 234.4 / 174.8 / 207.3, 16 x 4194304 172.3 / 143.1 / 197.7;
-// bf16 304 x 262144 120.6 / 66.0 / 56.5, 152 x 393216 76.3 / 51.7 / 48.3,
-// 64 x 1048576 71.3 / 57.0 / 64.7; clusters of 4 were slower than of 8 but
-// at bf16 64 x 393216 (22.8 against 25.6 at two CTAs an SM, 22.5 at four).
-// FR_LOOP_C=4|8, FR_LOOP_K=1|2|4 and FR_LOOP_L2_MB=<MB> pin them.
-void loop_shape(int64_t cols, int es, int sm_count, int *C, int *per_sm) {
+// The loop cluster's shape: C = 8 CTAs a row, 16 for fp32 rows of 1 to 4 MiB;
+// four CTAs of 256 threads an SM while the runs read once and not yet again
+// -- every resident CTA's run -- fit in 64 MB (half of L2), else two of 512.
+// Measured on GB300 (us per call, back to back).  CTAs an SM 1 / 2 / 4 with C
+// = 8: fp32 152 x 262144 84.7 / 60.6 / 70.5, 304 x 393216 234.4 / 174.8 /
+// 207.3, 16 x 4194304 172.3 / 143.1 / 197.7; bf16 304 x 262144 120.6 / 66.0 /
+// 56.5, 152 x 393216 76.3 / 51.7 / 48.3, 64 x 1048576 71.3 / 57.0 / 64.7.
+// Clusters of 16 (shorter runs: each cluster lives half as long, so the last
+// rows leave the GPU idle for less time), against 8 at the rule's CTAs an SM:
+// fp32 304 x 262144 106.8 / 109.5, 152 x 393216 86.5 / 90.7, 64 x 1048576
+// 107.6 / 116.5, but 16 x 4194304 150.2 / 143.6 and 608 x 131072 116.1 /
+// 102.0; bf16 slower at every length but 4194304 (608 x 262144 122.1 / 104.3,
+// 64 x 1048576 61.3 / 56.6, 16 x 4194304 74.2 / 80.6).  Clusters of 4 were
+// slower than of 8 but at bf16 64 x 393216 (22.8 against 25.6 at two CTAs an
+// SM, 22.5 at four).
+// FR_LOOP_C=4|8|16, FR_LOOP_K=1|2|4 and FR_LOOP_L2_MB=<MB> pin them.
+void loop_shape(int64_t rows, int64_t cols, int es, int sm_count, int *C, int *per_sm) {
   *C = kScMaxCluster;
-  if (const char *e = getenv("FR_LOOP_C"); e != nullptr && atoi(e) == 4) *C = 4;
+  if (es == 4 && cols * es >= (1 << 20) && cols * es <= (4 << 20) && rows * 16 <= 0x7fffffff)
+    *C = 16;
+  if (const char *e = getenv("FR_LOOP_C")) {
+    const int c = atoi(e);
+    if (c == 4 || (c == 16 && rows * 16 <= 0x7fffffff)) *C = c;
+  }
   int64_t budget = 64ll << 20;
   if (const char *e = getenv("FR_LOOP_L2_MB")) {
     const int mb = atoi(e);
@@ -496,7 +541,7 @@ cudaError_t launch_softmax_split_looped(const void *x, void *y, int64_t rows, in
   if (rows < 1 || cols < 1 || cols > 0x7fffffff || rows * kScMaxCluster > 0x7fffffff)
     return cudaErrorInvalidValue;
   int C = 0, per_sm = 0;
-  loop_shape(cols, es, sm_count, &C, &per_sm);
+  loop_shape(rows, cols, es, sm_count, &C, &per_sm);
   if (es == 4) {
     const float *fx = static_cast<const float *>(x);
     float *fy = static_cast<float *>(y);

@@ -285,12 +285,15 @@ def test_softmax_split_loop(o, cols, layout, monkeypatch):
 
 
 @pytest.mark.parametrize("shape", [{"FR_LOOP_K": "1"}, {"FR_LOOP_K": "2"},
-                                   {"FR_LOOP_K": "4", "FR_LOOP_C": "4"}],
-                         ids=["k1", "k2", "k4c4"])
+                                   {"FR_LOOP_K": "4", "FR_LOOP_C": "4"},
+                                   {"FR_LOOP_K": "2", "FR_LOOP_C": "16"},
+                                   {"FR_LOOP_K": "4", "FR_LOOP_C": "16"}],
+                         ids=["k1", "k2", "k4c4", "k2c16", "k4c16"])
 @pytest.mark.parametrize("cols", [8193, 262145])
 def test_softmax_split_loop_shapes(o, cols, shape, monkeypatch):
     """Every CTA size (1024, 512 or 256 threads: one, two or four CTAs an SM)
-    and both cluster sizes of the streaming cluster."""
+    and every cluster size (4, 8, and 16 CTAs past the portable limit) of the
+    streaming cluster."""
     monkeypatch.setenv("FR_SOFTMAX_SPLIT", "loop")
     for k, v in shape.items():
         monkeypatch.setenv(k, v)
