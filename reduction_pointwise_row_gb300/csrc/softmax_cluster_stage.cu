@@ -2,9 +2,9 @@
 // GPU Codegen and Dynamic Shapes", sections 9.4 and 9.5; "CMU 15-779
 // Lecture 8", section 3):
 //     m = max_r x,   y = exp(x - m) / sum_r exp(x - m),
-// for rows that neither a CTA nor a cluster holds in registers: rows whose x
-// and y sit at different offsets within a 16-byte chunk, and rows longer than
-// the register cluster's reach.  A thread-block cluster of C CTAs takes a
+// for rows that neither a CTA nor a cluster holds in registers and whose x
+// and y sit at different offsets within a 32-byte sector (and for any row
+// with FR_SOFTMAX_SPLIT=stage).  A thread-block cluster of C CTAs takes a
 // row; CTA q owns a run of y's 16-byte chunks and stages the x elements of
 // those chunks in its shared memory by 16-byte asynchronous copies at x's
 // alignment (the run's ragged ends element by element).  Each CTA reduces its
@@ -18,14 +18,15 @@
 // FR_DEVERR_TIMEOUT and goes on.  fp32 and bf16 rows (fp32 arithmetic).
 //
 // Rows in phase (x and y at the same offset within a 32-byte sector) longer
-// than a cluster's shared memory holds, or with so many rows that the staged
-// runs leave one CTA an SM, take softmax_cluster_loop instead: the same
+// than 384 KiB, at any length, take softmax_cluster_loop: the same kind of
 // cluster and exchange, but each CTA streams its run of x twice -- once
 // folding the chunks into (m_q, d_q) with the merge of section 9.5, once after
 // the exchange to write y -- the looped form of section 9.4 (2) within a
-// cluster.  A run is 1/C of the row, so the second read follows the first
-// within a few microseconds and finds x in L2; the CTAs an SM are set so that
-// the runs read once and not yet again fit in about a third of L2.
+// cluster.  A run is 1/C of the row (C = 8, or 16 for fp32 rows of 1-4 MiB),
+// so the second read follows the first within a few microseconds and finds x
+// in L2; the CTAs an SM are set so that the runs read once and not yet again
+// fit in half of L2, and the second pass goes through the run backwards, so
+// that a run too long for L2 still finds its last-read part there.
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
