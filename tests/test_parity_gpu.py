@@ -318,6 +318,19 @@ def test_softmax_split_loop_special_values(o, cols, monkeypatch):
         assert np.isnan(got[[1, 3, 4]]).all() and np.isfinite(got[[0, 2, 5]]).all()
 
 
+@pytest.mark.parametrize("rows,cols", [(200, 262145), (40, 1048577)])
+def test_softmax_split_loop_many_rows(o, rows, cols):
+    """AUTO on many long rows in phase: many waves of clusters (16 CTAs a row
+    at these lengths); the first, middle and last rows against the oracle."""
+    w = workloads.make(1, rows=rows, cols=cols, seed=3400 + rows)
+    got = run_softmax(w.arrays["x"], "auto")
+    assert fr.fr_last_form() == "split"
+    for r in (0, 1, rows // 2, rows - 2, rows - 1):
+        assert_close(got[r:r + 1], o.softmax(w.arrays["x"][r:r + 1]), "f32",
+                     f"loop split row {r} of {rows}x{cols}")
+    assert fr.fr_check_device_error() == 0
+
+
 def test_softmax_split_loop_in_place_and_unpinned(o, monkeypatch):
     """In place through the streaming cluster, and rows in phase past the
     staged cluster's reach take it unpinned."""

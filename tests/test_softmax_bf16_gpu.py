@@ -138,6 +138,18 @@ def test_softmax_bf16_split_loop(o, cols, layout, monkeypatch):
     assert fr.fr_check_device_error() == 0
 
 
+def test_softmax_bf16_split_loop_many_rows(o):
+    """AUTO on 320 bf16 rows of 300001 in phase (many waves of clusters);
+    the first, middle and last rows against the oracle."""
+    rows, cols = 320, 300001
+    bits = workloads.make_softmax_bf16(rows, cols, seed=7300).arrays["x"]
+    got = run(bits, "auto")
+    assert fr.fr_last_form() == "split"
+    for r in (0, 1, rows // 2, rows - 2, rows - 1):
+        assert_bf16_within_steps(got[r:r + 1], o.softmax(widen(bits[r:r + 1])), 1,
+                                 f"loop row {r} of {rows}x{cols}")
+
+
 @pytest.mark.parametrize("cols", [4097, 300001])
 def test_softmax_bf16_split_loop_special_values(o, cols, monkeypatch):
     monkeypatch.setenv("FR_SOFTMAX_SPLIT", "loop")
