@@ -462,8 +462,6 @@ cudaError_t launch_loop_t(const E *x, E *y, int64_t rows, int64_t cols, int64_t 
       done.insert({dev, kern});
     }
   }
-  // CTAs an SM: what the registers allow, held to per_sm by padding the
-  // dynamic shared memory ((per_sm + 1) padded CTAs do not fit an SM)
   if ((e = set_smem_limit(kern, 0)) != cudaSuccess) return e;
   if (C > 8) {  // a device (or partition) that holds no cluster of C: 8
     cudaLaunchConfig_t cfg = {};
@@ -481,6 +479,8 @@ cudaError_t launch_loop_t(const E *x, E *y, int64_t rows, int64_t cols, int64_t 
       return e;
     if (clusters < 1) C = 8;
   }
+  // CTAs an SM: what the registers allow, held to per_sm by padding the
+  // dynamic shared memory ((per_sm + 1) padded CTAs do not fit an SM)
   int resident = 0;
   if ((e = blocks_per_sm(&resident, kern, T, 0)) != cudaSuccess) return e;
   size_t smem = 0;
